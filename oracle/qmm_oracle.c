@@ -135,8 +135,16 @@ static float rdf32(const uint8_t* p) { float f; memcpy(&f, p, 4); return f; }
 static void wrf32(uint8_t* p, float f) { memcpy(p, &f, 4); }
 static int16_t rdi16(const uint8_t* p) { return (int16_t)rd16(p); }
 
-/* round to nearest integer, ties to even (the default IEEE rounding mode) */
-static int rne(float v) { return (int)nearbyintf(v); }
+/* round to nearest integer, ties to even (the default IEEE rounding mode); a value
+ * beyond the int range saturates and NaN gives 0, so the conversion is defined for
+ * every input (only degenerate scales can produce such quotients) */
+static int rne(float v) {
+    float r = nearbyintf(v);
+    if (r != r) return 0;
+    if (r >= 2147483648.0f) return 2147483647;
+    if (r <= -2147483648.0f) return -2147483647 - 1;
+    return (int)r;
+}
 static int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
 /* ------------------------------------------------------------------------- */

@@ -31,7 +31,7 @@ MUTANTS = [
     ("q4_K high scale bits", "sc[s] = (b[s + 4] & 15) | ((b[s - 4] >> 6) << 4);", "sc[s] = (b[s + 4] & 15) | ((b[s - 4] >> 6) << 3);"),
     ("q8_K bsums skip a code", "for (int i = 0; i < 16; i++) {\n                float v = xb[g * 16 + i] * id;\n                int q = clampi(rne(v), -128, 127);\n                ob[4 + g * 16 + i] = (uint8_t)(int8_t)q;\n                sum += q;",
      "for (int i = 0; i < 16; i++) {\n                float v = xb[g * 16 + i] * id;\n                int q = clampi(rne(v), -128, 127);\n                ob[4 + g * 16 + i] = (uint8_t)(int8_t)q;\n                if (i) sum += q;"),
-    ("q8_0 rounds half away from zero", "static int rne(float v) { return (int)nearbyintf(v); }", "static int rne(float v) { return (int)roundf(v); }"),
+    ("q8_0 rounds half away from zero", "float r = nearbyintf(v);", "float r = roundf(v);"),
 ]
 
 PINS = [name for name in dir(pins) if name.startswith("test_")]
