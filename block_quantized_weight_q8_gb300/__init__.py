@@ -1,0 +1,209 @@
+"""Python binding of libqmm (the C ABI declared in include/qmm.h).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls, converts tensors to device pointers and the current torch
+stream to a cudaStream_t, and raises QmmError on a non-OK status.  All
+arithmetic runs in the CUDA kernels of libqmm.so; there is no other path.
+Tensors may be torch CUDA tensors or raw integer device addresses.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .buildlib import LIB, build  # noqa: F401
+
+QMM_Q4_0, QMM_Q8_0, QMM_Q4_K, QMM_Q6_K, QMM_Q2_K, QMM_Q8_K = range(6)
+TYPES = {"q4_0": QMM_Q4_0, "q8_0": QMM_Q8_0, "q4_K": QMM_Q4_K, "q6_K": QMM_Q6_K, "q2_K": QMM_Q2_K,
+         "q8_K": QMM_Q8_K}
+WEIGHT_TYPES = ("q4_0", "q8_0", "q4_K", "q6_K", "q2_K")
+
+STATUS = {0: "QMM_OK", 1: "QMM_E_NULL", 2: "QMM_E_SHAPE", 3: "QMM_E_TYPE", 4: "QMM_E_ALIGN",
+          5: "QMM_E_SCRATCH", 6: "QMM_E_CUDA", 7: "QMM_E_TIMEOUT"}
+
+# every entry point the header declares, with its argument kinds
+# p: pointer, i: int64, s: size_t, t: int (type code), c: int, q: stream
+SIGNATURES = {
+    "qmm_block_bytes": ("t", ctypes.c_size_t),
+    "qmm_block_values": ("t", ctypes.c_int),
+    "qmm_row_bytes": ("ti", ctypes.c_size_t),
+    "qmm_act_type": ("t", ctypes.c_int),
+    "qmm_status_str": ("c", ctypes.c_char_p),
+    "qmm_quantize_q8_0": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q8_K": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q4_0": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q4_K": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q6_K": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q2_K": ("ppiiq", ctypes.c_int),
+    "qmm_matvec_q4_0": ("pppiiq", ctypes.c_int),
+    "qmm_matvec_q8_0": ("pppiiq", ctypes.c_int),
+    "qmm_matvec_q4_K": ("pppiiq", ctypes.c_int),
+    "qmm_matvec_q6_K": ("pppiiq", ctypes.c_int),
+    "qmm_matvec_q2_K": ("pppiiq", ctypes.c_int),
+    "qmm_linear_q4_0": ("pppspiiiq", ctypes.c_int),
+    "qmm_linear_q8_0": ("pppspiiiq", ctypes.c_int),
+    "qmm_linear_q4_K": ("pppspiiiq", ctypes.c_int),
+    "qmm_linear_q6_K": ("pppspiiiq", ctypes.c_int),
+    "qmm_linear_q2_K": ("pppspiiiq", ctypes.c_int),
+    "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
+    "qmm_blocksums": ("tpppiiiq", ctypes.c_int),
+    "qmm_device_status": ("c", ctypes.c_int),
+}
+_CT = {"p": ctypes.c_void_p, "i": ctypes.c_int64, "s": ctypes.c_size_t, "t": ctypes.c_int, "c": ctypes.c_int,
+       "q": ctypes.c_void_p}
+
+_lib = None
+
+
+class QmmError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s (%s)" % (fn, STATUS.get(status, status), _status_str(status)))
+
+
+def load(path: str = LIB):
+    """Load libqmm.so (built in-tree by build()); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError("libqmm.so is not built (%s): run block_quantized_weight_q8_gb300.build()" % path)
+    L = ctypes.CDLL(path)
+    for name, (kinds, res) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.argtypes = [_CT[k] for k in kinds]
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _status_str(status: int) -> str:
+    try:
+        return load().qmm_status_str(int(status)).decode()
+    except Exception:
+        return "?"
+
+
+def ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def stream_handle(stream=None) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _call(name, *args):
+    r = getattr(load(), name)(*args)
+    if r != 0:
+        raise QmmError(name, r)
+
+
+def _type(t) -> int:
+    return TYPES[t] if isinstance(t, str) else int(t)
+
+
+# ---- formats
+def qmm_block_bytes(t) -> int:
+    return int(load().qmm_block_bytes(_type(t)))
+
+
+def qmm_block_values(t) -> int:
+    return int(load().qmm_block_values(_type(t)))
+
+
+def qmm_row_bytes(t, K: int) -> int:
+    return int(load().qmm_row_bytes(_type(t), int(K)))
+
+
+def qmm_act_type(wtype) -> int:
+    return int(load().qmm_act_type(_type(wtype)))
+
+
+# ---- quantizers
+def qmm_quantize_q8_0(x, xq, M, K, stream=None):
+    _call("qmm_quantize_q8_0", ptr(x), ptr(xq), int(M), int(K), stream_handle(stream))
+
+
+def qmm_quantize_q8_K(x, xq, M, K, stream=None):
+    _call("qmm_quantize_q8_K", ptr(x), ptr(xq), int(M), int(K), stream_handle(stream))
+
+
+def qmm_quantize_q4_0(w, wq, N, K, stream=None):
+    _call("qmm_quantize_q4_0", ptr(w), ptr(wq), int(N), int(K), stream_handle(stream))
+
+
+def qmm_quantize_q4_K(w, wq, N, K, stream=None):
+    _call("qmm_quantize_q4_K", ptr(w), ptr(wq), int(N), int(K), stream_handle(stream))
+
+
+def qmm_quantize_q6_K(w, wq, N, K, stream=None):
+    _call("qmm_quantize_q6_K", ptr(w), ptr(wq), int(N), int(K), stream_handle(stream))
+
+
+def qmm_quantize_q2_K(w, wq, N, K, stream=None):
+    _call("qmm_quantize_q2_K", ptr(w), ptr(wq), int(N), int(K), stream_handle(stream))
+
+
+def quantize(t, x, out, rows, K, stream=None):
+    """qmm_quantize_<t> by type name (q8_0 also quantizes Q8_0 weights)."""
+    _call("qmm_quantize_" + t, ptr(x), ptr(out), int(rows), int(K), stream_handle(stream))
+
+
+# ---- matvec / linear / matmul
+def _mv(name):
+    def f(W, xq, y, N, K, stream=None):
+        _call(name, ptr(W), ptr(xq), ptr(y), int(N), int(K), stream_handle(stream))
+    f.__name__ = name
+    return f
+
+
+qmm_matvec_q4_0 = _mv("qmm_matvec_q4_0")
+qmm_matvec_q8_0 = _mv("qmm_matvec_q8_0")
+qmm_matvec_q4_K = _mv("qmm_matvec_q4_K")
+qmm_matvec_q6_K = _mv("qmm_matvec_q6_K")
+qmm_matvec_q2_K = _mv("qmm_matvec_q2_K")
+
+
+def matvec(wtype, W, xq, y, N, K, stream=None):
+    _call("qmm_matvec_" + wtype, ptr(W), ptr(xq), ptr(y), int(N), int(K), stream_handle(stream))
+
+
+def _lin(name):
+    def f(W, x, scratch, scratch_bytes, y, M, N, K, stream=None):
+        _call(name, ptr(W), ptr(x), ptr(scratch), int(scratch_bytes), ptr(y), int(M), int(N), int(K),
+              stream_handle(stream))
+    f.__name__ = name
+    return f
+
+
+qmm_linear_q4_0 = _lin("qmm_linear_q4_0")
+qmm_linear_q8_0 = _lin("qmm_linear_q8_0")
+qmm_linear_q4_K = _lin("qmm_linear_q4_K")
+qmm_linear_q6_K = _lin("qmm_linear_q6_K")
+qmm_linear_q2_K = _lin("qmm_linear_q2_K")
+
+
+def linear(wtype, W, x, scratch, scratch_bytes, y, M, N, K, stream=None):
+    _call("qmm_linear_" + wtype, ptr(W), ptr(x), ptr(scratch), int(scratch_bytes), ptr(y), int(M), int(N), int(K),
+          stream_handle(stream))
+
+
+def qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=None):
+    _call("qmm_matmul_q4_0", ptr(W), ptr(xq), ptr(Y), int(M), int(N), int(K), stream_handle(stream))
+
+
+def qmm_blocksums(wtype, W, xq, s, M, N, K, stream=None):
+    _call("qmm_blocksums", _type(wtype), ptr(W), ptr(xq), ptr(s), int(M), int(N), int(K), stream_handle(stream))
+
+
+def qmm_device_status(clear: bool = False) -> int:
+    return int(load().qmm_device_status(1 if clear else 0))

@@ -1,0 +1,95 @@
+// api.cu -- format queries, status strings, the quantize+matmul entry points
+// with the activation pairing fixed by the weight type, and the device status
+// word read-back.
+#include "qmm_device.cuh"
+#include "qmm_host.h"
+
+namespace qmm {
+qmm_status quantize_act_launch(int act, const float* x, void* xq, int64_t M, int64_t K, cudaStream_t stream, bool pdl);
+qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
+                           bool pdl);
+qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t stream, bool pdl);
+
+// [minfer] "10 . CPU matmul: quantized weights x Q8_0 activations" s3.2
+// (cpu_quant_matmul_f32): the weight type alone decides the activation format;
+// quantize once into the caller's scratch, then multiply.
+static qmm_status linear(int wt, const void* W, const float* x, void* scratch, size_t scratch_bytes, float* y,
+                         int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    if (!W || !x || !scratch || !y) return QMM_E_NULL;
+    qmm_status st = check_shape(wt, M, N, K);
+    if (st != QMM_OK) return st;
+    if (!aligned16(W) || !aligned16(x) || !aligned16(scratch) || !aligned16(y)) return QMM_E_ALIGN;
+    const int act = act_type_of(wt);
+    const size_t xrb = row_bytes_of(act, K);
+    if (scratch_bytes < (size_t)M * xrb) return QMM_E_SCRATCH;
+    if (wt == QMM_Q4_0 && M > 1) {
+        st = quantize_act_launch(act, x, scratch, M, K, stream, true);
+        if (st != QMM_OK) return st;
+        return matmul_q4_0_launch(W, scratch, y, M, N, K, stream, true);
+    }
+    st = quantize_act_launch(act, x, scratch, M, K, stream, M == 1);
+    if (st != QMM_OK) return st;
+    for (int64_t t = 0; t < M; t++) {
+        st = matvec_dispatch(wt, W, (const uint8_t*)scratch + t * xrb, y + t * N, N, K, stream, M == 1);
+        if (st != QMM_OK) return st;
+    }
+    return QMM_OK;
+}
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+unsigned qmm_internal_matvec_error(int clear);
+unsigned qmm_internal_matmul_error(int clear);
+
+size_t qmm_block_bytes(int type) { return block_bytes_of(type); }
+int qmm_block_values(int type) { return block_values_of(type); }
+size_t qmm_row_bytes(int type, int64_t K) { return row_bytes_of(type, K); }
+int qmm_act_type(int wtype) { return act_type_of(wtype); }
+
+const char* qmm_status_str(qmm_status s) {
+    switch (s) {
+    case QMM_OK: return "ok";
+    case QMM_E_NULL: return "a required pointer is NULL";
+    case QMM_E_SHAPE: return "M, N or K out of range, or K not a multiple of the block size";
+    case QMM_E_TYPE: return "unknown block type";
+    case QMM_E_ALIGN: return "a base pointer is not 16-byte aligned";
+    case QMM_E_SCRATCH: return "the scratch buffer is too small";
+    case QMM_E_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case QMM_E_TIMEOUT: return "a bounded device wait ran out";
+    default: return "unknown status";
+    }
+}
+
+qmm_status qmm_linear_q4_0(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q4_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_linear_q8_0(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q8_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_linear_q4_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q4_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_linear_q6_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q6_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_linear_q2_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q2_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+
+qmm_status qmm_device_status(int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return QMM_E_CUDA;
+    const unsigned e = qmm_internal_matvec_error(clear) | qmm_internal_matmul_error(clear);
+    if (cudaGetLastError() != cudaSuccess) return QMM_E_CUDA;
+    return e ? QMM_E_TIMEOUT : QMM_OK;
+}
+
+}  // extern "C"

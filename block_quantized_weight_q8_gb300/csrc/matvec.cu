@@ -1,0 +1,397 @@
+// matvec.cu -- the decode matvec (one token): y[o] = row o of the block-quantized
+// W against one Q8_0 / Q8_K activation row, for Q4_0, Q8_0, Q4_K, Q6_K and Q2_K.
+//
+// Design (GB300): the kernel is HBM-bound, so it is built around keeping the
+// weight stream in flight.  Each CTA owns a contiguous range of rows (an even
+// split of N over the grid).  One thread streams that range into a ring of
+// shared-memory stages with 1-D bulk copies (cp.async.bulk, completing on an
+// mbarrier) tagged evict-first in L2; the copies cover the 16-byte aligned
+// superset of each stage's rows, so no block layout (18, 34, 84, 210 B) needs
+// to be aligned.  Meanwhile the CTA unpacks the activation row once into
+// shared memory (contiguous int8 codes plus f32 scales and int32 group sums).
+// Each row of a stage is then owned by `lpr` lanes of one warp, which decode
+// whole blocks from shared memory, take the exact integer block dot with
+// __dp4a, fold it into fp32 once per block, and reduce with warp shuffles in a
+// fixed order -- so every y[o] is written by one lane, identically on every
+// run ([minfer] s3.3: row ownership, no split reduction).
+//
+// Formulas: [minfer] "10 . CPU matmul: quantized weights x Q8_0 activations"
+// s3.2 (the scalar kernels, the K-quant dot walked); [ggml] "ggml Q4_0 vec_dot
+// Walkthrough" s1.2 and s2.
+#include <stdio.h>
+
+#include "qmm_device.cuh"
+#include "qmm_host.h"
+
+namespace qmm {
+
+static __device__ unsigned int g_matvec_error = 0;
+
+constexpr int kThreads = 256;
+constexpr int kMaxStages = 8;
+
+struct MatvecPlan {
+    int lpr;            // lanes per row (power of two, 1..32)
+    int rows_per_stage; // 8 warps x (32 / lpr)
+    int nstages;
+    uint32_t stage_cap; // bytes per stage buffer (with slack for unaligned reads)
+    uint32_t act_bytes; // shared bytes before the first stage buffer
+    uint32_t smem;      // total dynamic shared memory
+    int grid;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// shared layout: [mbarriers: 128 B][codes: K B][scales: 4*nd B][sums: 4*nsum B] | stages...
+__host__ __device__ inline uint32_t act_region_bytes(int act, int K) {
+    const int nd = act == QMM_Q8_0 ? K / 32 : K / 256;
+    const int nsum = act == QMM_Q8_0 ? K / 32 : K / 16;
+    return align_up(128u + (uint32_t)K + 4u * nd + 4u * nsum, 128u);
+}
+
+template <int WT>
+__device__ __forceinline__ float unit_contrib(const SmemBytes& w, uint32_t o, const ActView& a, int u) {
+    if constexpr (WT == QMM_Q4_0 || WT == QMM_Q8_0) {
+        uint32_t db;
+        const int isum = (WT == QMM_Q4_0) ? q4_0_isum(w, o, a, u, &db) : q8_0_isum(w, o, a, u, &db);
+        return (float)isum * h2f(db) * a.d[u];
+    } else if constexpr (WT == QMM_Q6_K) {
+        int v, m;
+        uint32_t db;
+        q6_K_isums(w, o, a, u, &v, &m, &db);
+        const float d = h2f(db) * a.d[u];
+        return d * (float)(v - 32 * m);
+    } else {
+        int v, m;
+        uint32_t db, dmb;
+        if constexpr (WT == QMM_Q4_K) q4_K_isums(w, o, a, u, &v, &m, &db, &dmb);
+        else q2_K_isums(w, o, a, u, &v, &m, &db, &dmb);
+        const float d = h2f(db) * a.d[u];
+        const float dmin = h2f(dmb) * a.d[u];
+        // the page's order: subtract the min term, then add the value term
+        return -(dmin * (float)m) + d * (float)v;
+    }
+}
+
+template <int WT>
+__global__ void __launch_bounds__(kThreads) matvec_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq,
+                                                          float* __restrict__ y, int N, int K, int lpr, int nstages,
+                                                          uint32_t stage_cap, uint32_t act_bytes, int pdl) {
+    using F = Fmt<WT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* aq = smem + 128;
+    const int nd = F::ACT == QMM_Q8_0 ? K / 32 : K / 256;
+    float* ad = reinterpret_cast<float*>(aq + K);
+    int* as = reinterpret_cast<int*>(ad + nd);
+    uint8_t* stages = smem + act_bytes;
+
+    const int tid = threadIdx.x;
+    const int units = K / F::BV;
+    const uint64_t rb = (uint64_t)units * F::BB;
+    const int rows_per_warp = 32 / lpr;
+    const int R = (kThreads / 32) * rows_per_warp;
+    const int r_begin = (int)(((int64_t)N * blockIdx.x) / gridDim.x);
+    const int r_end = (int)(((int64_t)N * (blockIdx.x + 1)) / gridDim.x);
+    const int nst = (r_end - r_begin + R - 1) / R;
+    const uint64_t total = (uint64_t)N * rb;
+    const uint64_t total_al = total & ~15ull;
+
+    if (tid == 0) {
+        for (int i = 0; i < nstages; i++) mbar_init(smem_u32(&bars[i]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int s) {
+        const int r0 = r_begin + s * R;
+        const int r1 = min(r0 + R, r_end);
+        const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
+        uint64_t a1 = ((uint64_t)r1 * rb + 15ull) & ~15ull;
+        if (a1 > total_al) a1 = total_al;
+        const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
+        const int buf = s % nstages;
+        const uint32_t bar = smem_u32(&bars[buf]);
+        mbar_arrive_expect_tx(bar, bytes);
+        if (bytes) bulk_g2s(smem_u32(stages + (size_t)buf * stage_cap), W + a0, bytes, bar, pol);
+    };
+    if (tid == 0) {
+        const int first = nst < nstages ? nst : nstages;
+        for (int s = 0; s < first; s++) issue(s);
+    }
+
+    // the activation row comes from the previous kernel in the stream
+    if (pdl) pdl_wait();
+    if constexpr (F::ACT == QMM_Q8_0) unpack_q8_0_row(xq, K, aq, ad, as);
+    else unpack_q8_K_row(xq, K, aq, ad, as);
+    __syncthreads();
+
+    const ActView act{smem_u32(aq), ad, as};
+    const int warp = tid >> 5, lane = tid & 31;
+    const int rsub = lane / lpr, li = lane % lpr;
+
+    for (int s = 0; s < nst; s++) {
+        const int buf = s % nstages;
+        const uint32_t parity = (uint32_t)(s / nstages) & 1u;
+        const bool ok = mbar_wait_bounded(smem_u32(&bars[buf]), parity, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicOr(&g_matvec_error, kErrTimeout);
+            return;
+        }
+        const int r0 = r_begin + s * R;
+        const int r1 = min(r0 + R, r_end);
+        const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
+        uint8_t* sbuf = stages + (size_t)buf * stage_cap;
+        const uint64_t g1 = (uint64_t)r1 * rb;
+        if (g1 > total_al) {  // the last < 16 bytes of W: not reachable by a 16-byte bulk copy
+            const uint64_t t0 = total_al > a0 ? total_al : a0;
+            for (uint64_t i = t0 + tid; i < g1; i += kThreads) sbuf[i - a0] = W[i];
+            __syncthreads();
+        }
+        const SmemBytes wv{smem_u32(sbuf)};
+        const int row = r0 + warp * rows_per_warp + rsub;
+        float acc = 0.0f;
+        if (row < r1) {
+            const uint32_t ro = (uint32_t)((uint64_t)row * rb - a0);
+            for (int u = li; u < units; u += lpr) acc += unit_contrib<WT>(wv, ro + (uint32_t)(u * F::BB), act, u);
+        }
+        for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (row < r1 && li == 0) y[row] = acc;
+        __syncthreads();
+        if (tid == 0 && s + nstages < nst) issue(s + nstages);
+    }
+}
+
+// ------------------------------------------------------------------ blocksums (verification)
+// One CTA per (token, group of rows): copies the rows' bytes into shared memory
+// with plain loads and runs the same decoders, writing the integers.
+template <int WT>
+__global__ void __launch_bounds__(kThreads) blocksums_kernel(const uint8_t* __restrict__ W,
+                                                             const uint8_t* __restrict__ xq, int32_t* __restrict__ out,
+                                                             int N, int K, int rows_per_cta, uint32_t act_bytes) {
+    using F = Fmt<WT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* aq = smem + 128;
+    const int nd = F::ACT == QMM_Q8_0 ? K / 32 : K / 256;
+    float* ad = reinterpret_cast<float*>(aq + K);
+    int* as = reinterpret_cast<int*>(ad + nd);
+    uint8_t* wbuf = smem + act_bytes;
+
+    const int t = blockIdx.y;
+    const int units = K / F::BV;
+    const uint64_t rb = (uint64_t)units * F::BB;
+    const uint64_t xrb = F::ACT == QMM_Q8_0 ? (uint64_t)(K / 32) * Q8_0_BB : (uint64_t)(K / 256) * Q8_K_BB;
+    const uint8_t* xrow = xq + (uint64_t)t * xrb;
+    if constexpr (F::ACT == QMM_Q8_0) unpack_q8_0_row(xrow, K, aq, ad, as);
+    else unpack_q8_K_row(xrow, K, aq, ad, as);
+
+    const int r0 = blockIdx.x * rows_per_cta;
+    const int r1 = min(r0 + rows_per_cta, N);
+    const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
+    const uint64_t g1 = (uint64_t)r1 * rb;
+    for (uint64_t i = a0 + threadIdx.x; i < g1; i += blockDim.x) wbuf[i - a0] = W[i];
+    __syncthreads();
+
+    const ActView act{smem_u32(aq), ad, as};
+    const SmemBytes wv{smem_u32(wbuf)};
+    const int per = F::ACT == QMM_Q8_0 ? units : 2 * units;
+    for (int i = threadIdx.x; i < (r1 - r0) * units; i += blockDim.x) {
+        const int row = r0 + i / units, u = i % units;
+        const uint32_t o = (uint32_t)((uint64_t)row * rb - a0) + (uint32_t)(u * F::BB);
+        int32_t* dst = out + ((uint64_t)t * N + row) * per;
+        uint32_t db, dmb;
+        int v = 0, m = 0;
+        if constexpr (WT == QMM_Q4_0) v = q4_0_isum(wv, o, act, u, &db);
+        else if constexpr (WT == QMM_Q8_0) v = q8_0_isum(wv, o, act, u, &db);
+        else if constexpr (WT == QMM_Q4_K) q4_K_isums(wv, o, act, u, &v, &m, &db, &dmb);
+        else if constexpr (WT == QMM_Q2_K) q2_K_isums(wv, o, act, u, &v, &m, &db, &dmb);
+        else q6_K_isums(wv, o, act, u, &v, &m, &db);
+        if constexpr (F::ACT == QMM_Q8_0) {
+            dst[u] = v;
+        } else {
+            dst[2 * u] = v;
+            dst[2 * u + 1] = m;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+qmm_status current_device(DeviceInfo* info) {
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMM_E_CUDA;
+    if (cache[dev].device != dev) {
+        DeviceInfo d;
+        d.device = dev;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return QMM_E_CUDA;
+        if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return QMM_E_CUDA;
+        cache[dev] = d;
+    }
+    *info = cache[dev];
+    return QMM_OK;
+}
+
+// Picks lanes-per-row, rows per stage, stage count and grid for (format, N, K).
+template <int WT>
+static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, MatvecPlan* p) {
+    using F = Fmt<WT>;
+    const int units = (int)(K / F::BV);
+    int lpr = 1;
+    while (lpr < 32 && lpr < units) lpr <<= 1;
+    p->lpr = lpr;
+    p->rows_per_stage = (kThreads / 32) * (32 / lpr);
+    const uint64_t rb = (uint64_t)units * F::BB;
+    const uint64_t cap = align_up((uint32_t)(p->rows_per_stage * rb + 48), 128u);
+    p->act_bytes = act_region_bytes(F::ACT, (int)K);
+    const uint64_t budget = (uint64_t)dev.max_smem_optin - p->act_bytes;
+    if (cap > budget) return QMM_E_SHAPE;
+    p->stage_cap = (uint32_t)cap;
+    // as many stages as fit, up to kMaxStages, keeping about 160 KB of weights in flight
+    int ns = (int)(budget / cap);
+    if (ns > kMaxStages) ns = kMaxStages;
+    const int want = (int)((160u * 1024u + cap - 1) / cap);
+    if (ns > want) ns = want < 2 ? 2 : want;
+    if (ns < 1) return QMM_E_SHAPE;
+    p->nstages = ns;
+    p->smem = p->act_bytes + (uint32_t)ns * p->stage_cap;
+    const int64_t stages_total = (N + p->rows_per_stage - 1) / p->rows_per_stage;
+    int64_t grid = dev.sms;
+    if (grid > stages_total) grid = stages_total;
+    if (grid < 1) grid = 1;
+    p->grid = (int)grid;
+    return QMM_OK;
+}
+
+template <int WT>
+static qmm_status launch_matvec(const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
+                                bool pdl) {
+    DeviceInfo dev;
+    qmm_status st = current_device(&dev);
+    if (st != QMM_OK) return st;
+    MatvecPlan p;
+    st = plan_matvec<WT>(N, K, dev, &p);
+    if (st != QMM_OK) return st;
+    static bool attr_set[64] = {false};
+    if (!attr_set[dev.device]) {
+        if (cudaFuncSetAttribute(matvec_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin) !=
+            cudaSuccess)
+            return QMM_E_CUDA;
+        attr_set[dev.device] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT>, (const uint8_t*)W, (const uint8_t*)xq, y, (int)N,
+                                             (int)K, p.lpr, p.nstages, p.stage_cap, p.act_bytes, pdl ? 1 : 0);
+    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
+
+// Public calls require 16-byte aligned bases; internal per-token calls pass rows
+// of a larger buffer, which the kernel accepts at their natural alignment (W
+// 16 bytes for the bulk copies, an activation row 2 bytes, y 4 bytes).
+static qmm_status matvec_checked(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K,
+                                 cudaStream_t stream, bool pdl, bool public_call = true) {
+    if (!W || !xq || !y) return QMM_E_NULL;
+    qmm_status st = check_shape(wt, 1, N, K);
+    if (st != QMM_OK) return st;
+    if (public_call && (!aligned16(W) || !aligned16(xq) || !aligned16(y))) return QMM_E_ALIGN;
+    if (!aligned16(W) || ((uintptr_t)xq & 1u) || ((uintptr_t)y & 3u)) return QMM_E_ALIGN;
+    switch (wt) {
+    case QMM_Q4_0: return launch_matvec<QMM_Q4_0>(W, xq, y, N, K, stream, pdl);
+    case QMM_Q8_0: return launch_matvec<QMM_Q8_0>(W, xq, y, N, K, stream, pdl);
+    case QMM_Q4_K: return launch_matvec<QMM_Q4_K>(W, xq, y, N, K, stream, pdl);
+    case QMM_Q6_K: return launch_matvec<QMM_Q6_K>(W, xq, y, N, K, stream, pdl);
+    case QMM_Q2_K: return launch_matvec<QMM_Q2_K>(W, xq, y, N, K, stream, pdl);
+    default: return QMM_E_TYPE;
+    }
+}
+
+qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
+                           bool pdl) {
+    return matvec_checked(wt, W, xq, y, N, K, stream, pdl, false);
+}
+
+template <int WT>
+static qmm_status launch_blocksums(const void* W, const void* xq, int32_t* s, int64_t M, int64_t N, int64_t K,
+                                   cudaStream_t stream) {
+    using F = Fmt<WT>;
+    DeviceInfo dev;
+    qmm_status st = current_device(&dev);
+    if (st != QMM_OK) return st;
+    const uint64_t rb = (uint64_t)(K / F::BV) * F::BB;
+    const uint32_t act = act_region_bytes(F::ACT, (int)K);
+    int rows = (int)(16384 / rb);
+    if (rows < 1) rows = 1;
+    if (rows > 64) rows = 64;
+    const uint64_t smem = act + align_up((uint32_t)(rows * rb + 48), 128u);
+    if (smem > (uint64_t)dev.max_smem_optin) return QMM_E_SHAPE;
+    if (cudaFuncSetAttribute(blocksums_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin) !=
+        cudaSuccess)
+        return QMM_E_CUDA;
+    const dim3 grid((unsigned)((N + rows - 1) / rows), (unsigned)M);
+    if (M > 65535) return QMM_E_SHAPE;
+    blocksums_kernel<WT><<<grid, kThreads, (size_t)smem, stream>>>((const uint8_t*)W, (const uint8_t*)xq, s, (int)N,
+                                                                   (int)K, rows, act);
+    return launch_status();
+}
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+qmm_status qmm_matvec_q4_0(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q4_0, W, xq, y, N, K, (cudaStream_t)stream, false);
+}
+qmm_status qmm_matvec_q8_0(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q8_0, W, xq, y, N, K, (cudaStream_t)stream, false);
+}
+qmm_status qmm_matvec_q4_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q4_K, W, xq, y, N, K, (cudaStream_t)stream, false);
+}
+qmm_status qmm_matvec_q6_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q6_K, W, xq, y, N, K, (cudaStream_t)stream, false);
+}
+qmm_status qmm_matvec_q2_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q2_K, W, xq, y, N, K, (cudaStream_t)stream, false);
+}
+
+qmm_status qmm_blocksums(int wtype, const void* W, const void* xq, int32_t* s, int64_t M, int64_t N, int64_t K,
+                         qmm_stream_t stream) {
+    if (act_type_of(wtype) < 0) return QMM_E_TYPE;
+    if (!W || !xq || !s) return QMM_E_NULL;
+    qmm_status st = check_shape(wtype, M, N, K);
+    if (st != QMM_OK) return st;
+    if (!aligned16(W) || !aligned16(xq) || !aligned16(s)) return QMM_E_ALIGN;
+    cudaStream_t cs = (cudaStream_t)stream;
+    switch (wtype) {
+    case QMM_Q4_0: return launch_blocksums<QMM_Q4_0>(W, xq, s, M, N, K, cs);
+    case QMM_Q8_0: return launch_blocksums<QMM_Q8_0>(W, xq, s, M, N, K, cs);
+    case QMM_Q4_K: return launch_blocksums<QMM_Q4_K>(W, xq, s, M, N, K, cs);
+    case QMM_Q6_K: return launch_blocksums<QMM_Q6_K>(W, xq, s, M, N, K, cs);
+    case QMM_Q2_K: return launch_blocksums<QMM_Q2_K>(W, xq, s, M, N, K, cs);
+    default: return QMM_E_TYPE;
+    }
+}
+
+unsigned qmm_internal_matvec_error(int clear) {
+    unsigned v = 0;
+    cudaMemcpyFromSymbol(&v, g_matvec_error, sizeof(v));
+    if (clear) {
+        const unsigned z = 0;
+        cudaMemcpyToSymbol(g_matvec_error, &z, sizeof(z));
+    }
+    return v;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// qmm_host.h -- host-side helpers shared by the libqmm translation units:
+// argument validation, device properties, and launch utilities.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qmm.h"
+
+namespace qmm {
+
+constexpr int64_t kMaxK = 65536;
+constexpr int64_t kMaxDim = 2147483647LL;
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+inline int block_values_of(int t) {
+    switch (t) {
+    case QMM_Q4_0: case QMM_Q8_0: return 32;
+    case QMM_Q4_K: case QMM_Q6_K: case QMM_Q2_K: case QMM_Q8_K: return 256;
+    default: return 0;
+    }
+}
+inline size_t block_bytes_of(int t) {
+    switch (t) {
+    case QMM_Q4_0: return 18;
+    case QMM_Q8_0: return 34;
+    case QMM_Q4_K: return 144;
+    case QMM_Q6_K: return 210;
+    case QMM_Q2_K: return 84;
+    case QMM_Q8_K: return 292;
+    default: return 0;
+    }
+}
+inline int act_type_of(int wt) {
+    switch (wt) {
+    case QMM_Q4_0: case QMM_Q8_0: return QMM_Q8_0;
+    case QMM_Q4_K: case QMM_Q6_K: case QMM_Q2_K: return QMM_Q8_K;
+    default: return -1;
+    }
+}
+inline size_t row_bytes_of(int t, int64_t K) {
+    const int bv = block_values_of(t);
+    if (bv == 0 || K <= 0 || K % bv) return 0;
+    return (size_t)(K / bv) * block_bytes_of(t);
+}
+
+// Shape check shared by the calls: M, N, K in range, K a multiple of the
+// block of type t, K within the shared-memory activation limit.
+inline qmm_status check_shape(int t, int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxK) return QMM_E_SHAPE;
+    const int bv = block_values_of(t);
+    if (bv == 0) return QMM_E_TYPE;
+    if (K % bv) return QMM_E_SHAPE;
+    return QMM_OK;
+}
+
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    int max_smem_optin = 0;
+};
+
+// Properties of the current device (cached per device id).
+qmm_status current_device(DeviceInfo* info);
+
+inline qmm_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
+
+}  // namespace qmm

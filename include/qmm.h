@@ -1,0 +1,194 @@
+/*
+ * qmm.h -- C ABI of libqmm: block-quantized weight x Q8 activation matmul on
+ * GB300 (sm_103a).
+ *
+ * y = W . x where W stays in its block-quantized form (Q4_0, Q8_0, Q4_K, Q6_K,
+ * Q2_K) and is never dequantized as a whole, x is quantized on the fly to Q8_0
+ * or Q8_K, and every block is an exact integer dot product whose per-block
+ * scales (and K-quant mins) are folded into an fp32 accumulator once per block.
+ *
+ * Pages the operations follow (cited by title and section):
+ *   [minfer] "10 . CPU matmul: quantized weights x Q8_0 activations"
+ *   [ggml]   "ggml Q4_0 vec_dot Walkthrough"
+ *   [krafla] "Architecture"
+ *   [kvad]   "kvad -- the same ideas, at scale"
+ *
+ * Conventions shared by every call
+ *   Layout.   All buffers are little-endian, packed, with no padding.  W is
+ *             row-major: N rows of qmm_row_bytes(type, K) bytes.  Activation
+ *             blocks are [M][K / block_values] blocks, and outputs are fp32
+ *             [M][N], token-major ([minfer] s2.3 and s3.4: out is [nt][od]).
+ *   Pointers. Device pointers, owned by the caller, valid for the whole
+ *             asynchronous call.  Nothing is allocated on any call.
+ *   Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *             default stream).  Calls are asynchronous on it; none synchronizes.
+ *   Errors.   Every call returns a qmm_status.  Arguments are checked on the
+ *             host before anything is launched; a failed check launches
+ *             nothing.  A launch failure returns QMM_E_CUDA.  No call aborts,
+ *             and no kernel traps: a device-side wait that runs out of time
+ *             records QMM_E_TIMEOUT, read back with qmm_device_status().
+ *   Alignment. Every base pointer must be 16-byte aligned (W, xq, x, y).
+ *   Limits.   M, N, K >= 1; K a multiple of 32 (Q4_0, Q8_0) or 256 (K-quants,
+ *             [minfer] s3.4: "id % 256 == 0 for K-quants"); K <= 65536;
+ *             N <= 2^31 - 1; M <= 2^31 - 1.
+ *   Results.  Each output element is computed by exactly one thread in a fixed
+ *             order, so results are identical from run to run ([minfer] s3.3).
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_E_NULL = 1,     /* a required pointer is NULL */
+    QMM_E_SHAPE = 2,    /* M, N or K out of range, or K not a multiple of the block */
+    QMM_E_TYPE = 3,     /* unknown type code */
+    QMM_E_ALIGN = 4,    /* a base pointer is not 16-byte aligned */
+    QMM_E_SCRATCH = 5,  /* a caller scratch buffer is too small */
+    QMM_E_CUDA = 6,     /* a CUDA runtime call or kernel launch failed */
+    QMM_E_TIMEOUT = 7   /* a bounded device wait ran out (see qmm_device_status) */
+} qmm_status;
+
+/* Block types.  Byte sizes per block: Q4_0 18 B / 32 values, Q8_0 34 B / 32,
+ * Q4_K 144 B / 256, Q6_K 210 B / 256, Q2_K 84 B / 256, Q8_K 292 B / 256
+ * ([minfer] s2.3 block.rs; [ggml] s1.1 and s1.2).
+ *   Q4_0: f16 d @0, qs[16] @2; byte j holds element j (low nibble) and j+16
+ *         (high nibble); value d*(q-8)                              [ggml] s2
+ *   Q8_0: f16 d @0, int8 qs[32] @2; value d*q                       [ggml] s1.1
+ *   Q4_K: f16 d @0, f16 dmin @2, 12 B of 6-bit scales/mins @4, qs[128] @16;
+ *         value d*sc_s*q - dmin*m_s per 32-value sub-block s      [minfer] s3.2
+ *   Q6_K: ql[128] @0, qh[64] @128, int8 scales[16] @192, f16 d @208;
+ *         value d*sc_g*(q-32) per 16-value group       (GGUF layout, a reading)
+ *   Q2_K: scales[16] @0 (sc low, m high nibble), qs[64] @16, f16 d @80,
+ *         f16 dmin @82; value d*sc_g*q - dmin*m_g                   [ggml] s1.2
+ *   Q8_K: f32 d @0, int8 qs[256] @4, int16 bsums[16] @260 (activations only) */
+typedef enum { QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_Q4_K = 2, QMM_Q6_K = 3, QMM_Q2_K = 4, QMM_Q8_K = 5 } qmm_type;
+
+typedef void* qmm_stream_t; /* a cudaStream_t */
+
+/* ---- formats ------------------------------------------------------------ */
+QMM_API size_t qmm_block_bytes(int type);                 /* 0 for an unknown type */
+QMM_API int qmm_block_values(int type);                   /* 32 or 256; 0 for an unknown type */
+QMM_API size_t qmm_row_bytes(int type, int64_t K);        /* 0 if K is not a positive multiple */
+QMM_API int qmm_act_type(int wtype);                      /* QMM_Q8_0 or QMM_Q8_K: the pairing rule
+                                                     of [minfer] s2.4; -1 for a bad type */
+QMM_API const char* qmm_status_str(qmm_status s);         /* static string, never NULL */
+
+/* ---- activation quantizers (hot path) ----------------------------------- */
+/* [minfer] s3.2 "The activation quantizers" (quantize_row_q8_0): per 32 values
+ * amax = max|x|, d = amax/127 stored as f16 (round to nearest even), inverse
+ * 127/amax (0 for an all-zero block), codes = x * inverse rounded to nearest even
+ * and saturated to int8.  x: f32 [M][K]; xq: [M][K/32] Q8_0 blocks (34 B each).
+ * Every float operation is IEEE-rounded as written, so the codes and d are
+ * bit-identical to a scalar implementation of the same steps.  Also quantizes
+ * Q8_0 weights (same block, same rule). */
+QMM_API qmm_status qmm_quantize_q8_0(const float* x, void* xq, int64_t M, int64_t K, qmm_stream_t stream);
+
+/* [minfer] s3.2 (quantize_row_q8_k_buf): per 256 values amax, d = amax/127 kept
+ * as f32, the same rounding with inverse 127/amax (a reading: the page's sketch
+ * writes 1/d), codes saturated to [-128, 127], and bsums[g] the exact sum of the
+ * 16 saturated codes of group g.  x: f32 [M][K]; xq: [M][K/256] Q8_K blocks. */
+QMM_API qmm_status qmm_quantize_q8_K(const float* x, void* xq, int64_t M, int64_t K, qmm_stream_t stream);
+
+/* ---- weight quantizers (input preparation, not on the timed path) ------- */
+/* Each turns f32 weights [N][K] into N rows of blocks, with every float step
+ * IEEE-rounded as written.
+ *   Q4_0 ([ggml] s1.1; [kvad] "The scale that wasted a code"): m = the value of
+ *     largest magnitude (first on a tie), d = m / -8 stored as f16, codes
+ *     min(15, trunc(x / d + 8.5)) (x times the f32 inverse 1/d) -- m decodes as
+ *     code -8, the opposite extreme clips to 7/8.
+ *   Q4_K (reading): per sub-block min_s = max(0, -min x), scale_s =
+ *     (max x + min_s)/15; d = max scale_s / 63, dmin = max min_s / 63 (f16);
+ *     6-bit sc_s = rne(scale_s/d), m_s = rne(min_s/dmin); codes
+ *     rne((x + f16(dmin)*m_s) / (f16(d)*sc_s)) in 0..15.
+ *   Q2_K (reading): the same over 16 groups of 16 with /3, /15, 4-bit sc/m,
+ *     codes 0..3.
+ *   Q6_K (reading): per group the signed extreme m_g, s_g = m_g / -32;
+ *     d = max|s_g| / 127 (f16), int8 sc_g = rne(s_g/d), codes
+ *     rne(x / (f16(d)*sc_g)) in -32..31, stored +32.
+ * Q8_0 weights use qmm_quantize_q8_0. */
+QMM_API qmm_status qmm_quantize_q4_0(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_quantize_q4_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_quantize_q6_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_quantize_q2_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
+
+/* ---- decode matvec, one token (hot path) -------------------------------- */
+/* y[o] = sum over blocks b of the row's block dot, folded in fp32:
+ *   Q4_0, Q8_0 (x in Q8_0): y += (float)isum_b * d_w * d_x, isum_b the exact
+ *     int32 code dot of block b ([minfer] s3.2 scalar kernel; [ggml] s2).
+ *   Q4_K, Q2_K (x in Q8_K): per super-block, with d = d_w*d_x and
+ *     dmin = dmin_w*d_x: y -= dmin*min_term; y += d*value_term, where
+ *     value_term = sum of sc * (code dot) over the sub-blocks/groups and
+ *     min_term = sum of m * (activation group sums from bsums)
+ *     ([minfer] s3.2, the K-quant dot walked; [ggml] s1.2).
+ *   Q6_K (x in Q8_K): y += (d_w*d_x) * sum_g sc_g * sum (q-32)*a (reading).
+ * W: N rows; xq: one activation row; y: f32 [N].  The fp32 fold per thread and
+ * the reduction across threads follow a fixed order, which differs from a
+ * left-to-right scalar sum; results agree with one within 1e-5 of the row's
+ * L2 norm ([krafla] Numerics: block sums exact, float order per machine). */
+QMM_API qmm_status qmm_matvec_q4_0(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_matvec_q8_0(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_matvec_q4_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_matvec_q6_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_matvec_q2_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+
+/* ---- quantize + matvec with the pairing fixed (hot path) ---------------- */
+/* [minfer] s3.2 (cpu_quant_matmul_f32): the activation format is chosen by the
+ * weight type in one place, so no caller can pair the wrong formats.  Quantizes
+ * x (f32 [M][K]) into the caller's scratch (at least M * qmm_row_bytes(
+ * qmm_act_type(wtype), K) bytes, 16-byte aligned), then computes y (f32 [M][N]).
+ * With M = 1 the matvec starts streaming W while x is being quantized. */
+QMM_API qmm_status qmm_linear_q4_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_q8_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_q4_K(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_q6_K(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_q2_K(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+
+/* ---- prefill matmul, M tokens (hot path) -------------------------------- */
+/* Y[t][o] = sum_b d_w[o,b] * d_x[t,b] * isum[t,o,b] for M tokens at once: the
+ * weights are read once per tile of tokens and reused across them ([krafla]
+ * "Batched prompt prefill"; [kvad] "Batched prefill, and i8mm").  The integer
+ * block sums run on the tensor cores with integer-valued operands (exact), and
+ * each 32-wide block's sum is rescaled into fp32 by d_w*d_x.
+ * W: N rows of Q4_0; xq: [M][K/32] Q8_0 blocks; Y: f32 [M][N]. */
+QMM_API qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream);
+
+/* ---- verification hooks (not on the hot path) --------------------------- */
+/* The exact int32 block sums the kernels fold, for bit-exact checking:
+ * s[t][o][b] for every token t, row o and block b; Q4_0/Q8_0 give one int32 per
+ * 32-value block (sum of code products), the K-quants two per super-block:
+ * (value term, min term) -- Q4_K: (sum_s sc_s*dot_s, sum_s m_s*(bsum_2s +
+ * bsum_2s+1)); Q2_K: (sum_g sc_g*dot_g, sum_g m_g*bsum_g); Q6_K: (sum_g sc_g *
+ * dot_g with the stored codes 0..63, sum_g sc_g*bsum_g), whose integer is
+ * value - 32*min.  s: int32 [M][N][per-row count], computed by the same device
+ * decode routines the matvec uses. */
+QMM_API qmm_status qmm_blocksums(int wtype, const void* W, const void* xq, int32_t* s, int64_t M, int64_t N, int64_t K,
+                         qmm_stream_t stream);
+
+/* Reads (and with clear != 0 resets) the device error word that bounded waits
+ * set when they run out.  Synchronizes the device.  QMM_OK when no wait ran out. */
+QMM_API qmm_status qmm_device_status(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

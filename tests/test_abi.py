@@ -1,0 +1,129 @@
+"""The C-ABI boundary on the CPU: the library builds, loads, exports every entry point
+include/qmm.h declares, and rejects bad arguments on the host before any CUDA call (these
+checks run without a GPU).  No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+import block_quantized_weight_q8_gb300 as qmm
+
+HEADER = os.path.join(ROOT, "include", "qmm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qmm.build()
+    return qmm.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"QMM_API\s+[\w\s\*]+?\b(qmm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("qmm_quantize_q8_0", "qmm_quantize_q8_K", "qmm_matvec_q4_0", "qmm_matvec_q8_0",
+                 "qmm_matvec_q4_K", "qmm_matvec_q6_K", "qmm_matvec_q2_K", "qmm_matmul_q4_0",
+                 "qmm_linear_q4_0", "qmm_blocksums", "qmm_status_str", "qmm_row_bytes"):
+        assert want in names
+    assert set(names) == set(qmm.SIGNATURES), set(names) ^ set(qmm.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", qmm.LIB], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(qmm_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert getattr(lib, n) is not None
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "qmm.h"\nint main(void){return (int)qmm_block_bytes(QMM_Q4_0) - 18;}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER), str(src)],
+                   check=True)
+
+
+def test_formats(lib):
+    sizes = {"q4_0": (18, 32), "q8_0": (34, 32), "q4_K": (144, 256), "q6_K": (210, 256), "q2_K": (84, 256),
+             "q8_K": (292, 256)}
+    for t, (bb, bv) in sizes.items():
+        assert qmm.qmm_block_bytes(t) == bb and qmm.qmm_block_values(t) == bv
+    assert qmm.qmm_row_bytes("q4_0", 896) == 504
+    assert qmm.qmm_row_bytes("q8_0", 4096) == 4352
+    assert qmm.qmm_row_bytes("q4_K", 4096) == 16 * 144
+    assert qmm.qmm_row_bytes("q4_K", 4000) == 0
+    assert qmm.qmm_block_bytes(99) == 0
+    assert qmm.qmm_act_type("q4_0") == qmm.QMM_Q8_0 and qmm.qmm_act_type("q6_K") == qmm.QMM_Q8_K
+    assert qmm.qmm_act_type(99) == -1
+    for s in range(8):
+        assert lib.qmm_status_str(s)
+    assert lib.qmm_status_str(1234) == b"unknown status"
+
+
+# Host-side validation: every one of these returns before any CUDA call.
+A = 1 << 20          # a fake, 16-byte aligned address that is never dereferenced
+U = A + 4            # a fake misaligned address
+
+
+@pytest.mark.parametrize("name", ["qmm_matvec_q4_0", "qmm_matvec_q8_0", "qmm_matvec_q4_K", "qmm_matvec_q6_K",
+                                  "qmm_matvec_q2_K"])
+def test_matvec_rejects_bad_arguments(lib, name):
+    f = getattr(lib, name)
+    K = 256
+    assert f(None, A, A, 8, K, None) == 1          # NULL
+    assert f(A, None, A, 8, K, None) == 1
+    assert f(A, A, None, 8, K, None) == 1
+    assert f(A, A, A, 0, K, None) == 2             # N < 1
+    assert f(A, A, A, 8, 0, None) == 2             # K < 1
+    assert f(A, A, A, 8, K + 16, None) == 2        # K not a multiple of the block
+    assert f(A, A, A, 8, 65536 + 256, None) == 2   # K above the limit
+    assert f(A, A, A, 1 << 31, K, None) == 2       # N above the limit
+    assert f(U, A, A, 8, K, None) == 4             # misaligned
+    assert f(A, U, A, 8, K, None) == 4
+    assert f(A, A, U, 8, K, None) == 4
+
+
+def test_quantizers_reject_bad_arguments(lib):
+    for name, bv in (("qmm_quantize_q8_0", 32), ("qmm_quantize_q8_K", 256), ("qmm_quantize_q4_0", 32),
+                     ("qmm_quantize_q4_K", 256), ("qmm_quantize_q6_K", 256), ("qmm_quantize_q2_K", 256)):
+        f = getattr(lib, name)
+        assert f(None, A, 1, bv, None) == 1
+        assert f(A, None, 1, bv, None) == 1
+        assert f(A, A, 0, bv, None) == 2
+        assert f(A, A, 1, bv + 16, None) == 2
+        assert f(U, A, 1, bv, None) == 4
+
+
+def test_linear_rejects_bad_arguments(lib):
+    f = lib.qmm_linear_q4_K
+    need = 3 * qmm.qmm_row_bytes("q8_K", 512)
+    assert f(A, A, A, need - 1, A, 3, 64, 512, None) == 5      # scratch too small
+    assert f(A, A, None, need, A, 3, 64, 512, None) == 1
+    assert f(A, A, A, need, A, 3, 64, 500, None) == 2
+    assert f(A, A, U, need, A, 3, 64, 512, None) == 4
+    g = lib.qmm_linear_q4_0
+    assert g(A, A, A, 34 * 8 - 1, A, 1, 64, 256, None) == 5
+
+
+def test_matmul_and_blocksums_reject_bad_arguments(lib):
+    assert lib.qmm_matmul_q4_0(A, A, A, 0, 64, 256, None) == 2
+    assert lib.qmm_matmul_q4_0(A, A, None, 4, 64, 256, None) == 1
+    assert lib.qmm_matmul_q4_0(A, U, A, 4, 64, 256, None) == 4
+    assert lib.qmm_matmul_q4_0(A, A, A, 4, 64, 48, None) == 2
+    assert lib.qmm_blocksums(7, A, A, A, 1, 1, 256, None) == 3
+    assert lib.qmm_blocksums(qmm.QMM_Q8_K, A, A, A, 1, 1, 256, None) == 3   # not a weight type
+    assert lib.qmm_blocksums(qmm.QMM_Q4_K, A, A, A, 1, 1, 128, None) == 2
+
+
+def test_binding_raises(lib):
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.qmm_matvec_q4_0(0, A, A, 8, 256, stream=0)
+    assert e.value.status == 1 and "NULL" in str(e.value)
