@@ -27,26 +27,26 @@ namespace qmm {
 
 static __device__ unsigned int g_matvec_error = 0;
 
-constexpr int kThreads = 256;
-constexpr int kMaxStages = 8;
+constexpr int kThreads = 256;  // blocksums kernel
 
 struct MatvecPlan {
-    int lpr;            // lanes per row (power of two, 1..32)
-    int rows_per_stage; // 8 warps x (32 / lpr)
-    int nstages;
-    uint32_t stage_cap; // bytes per stage buffer (with slack for unaligned reads)
-    uint32_t act_bytes; // shared bytes before the first stage buffer
-    uint32_t smem;      // total dynamic shared memory
+    int nwc;              // consumer warps (16 or 8); one more warp produces
+    int lpr;              // lanes per row (power of two, 1..32)
+    int stage_rows;       // rows per stage (whole passes of 32 / lpr rows)
+    int nstages;          // stage buffers in the ring
+    uint32_t stage_bytes; // bytes per stage buffer (with slack for unaligned reads)
+    uint32_t act_bytes;   // shared bytes before the first stage (barriers, activation)
+    uint32_t smem;        // total dynamic shared memory
     int grid;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-// shared layout: [mbarriers: 128 B][codes: K B][scales: 4*nd B][sums: 4*nsum B] | stages...
+// activation region: [codes: K B][scales: 4*nd B][sums: 4*nsum B], 128-byte padded
 __host__ __device__ inline uint32_t act_region_bytes(int act, int K) {
     const int nd = act == QMM_Q8_0 ? K / 32 : K / 256;
     const int nsum = act == QMM_Q8_0 ? K / 32 : K / 16;
-    return align_up(128u + (uint32_t)K + 4u * nd + 4u * nsum, 128u);
+    return align_up((uint32_t)K + 4u * nd + 4u * nsum, 128u);
 }
 
 template <int WT>
@@ -73,93 +73,141 @@ __device__ __forceinline__ float unit_contrib(const SmemBytes& w, uint32_t o, co
     }
 }
 
-template <int WT>
-__global__ void __launch_bounds__(kThreads) matvec_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq,
-                                                          float* __restrict__ y, int N, int K, int lpr, int nstages,
-                                                          uint32_t stage_cap, uint32_t act_bytes, int pdl) {
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// The decode matvec: a warp-specialized stream.  Each CTA owns an even share of
+// the rows, cut into stages of `stage_rows` rows.  One producer warp streams the
+// stages into a ring of `nstages` shared-memory buffers with 1-D bulk copies
+// (cp.async.bulk completing on the stage's "full" mbarrier, evict-first in L2);
+// the copies cover the 16-byte aligned superset of each stage's rows, so no
+// block layout needs to be aligned.  NWC consumer warps take the rows of each
+// stage in passes of 32 / lpr rows (`lpr` lanes per row), decode whole blocks
+// from shared memory, take the exact integer block dots with __dp4a, fold each
+// into fp32 once per block and reduce with shuffles in a fixed order; each
+// consumer warp then arrives on the stage's "empty" mbarrier, and the producer
+// refills the buffer once all have.  No CTA-wide barrier sits in the loop, and
+// every y[o] is written by one lane, identically on every run ([minfer] s3.3:
+// row ownership, no split reduction).
+//
+// With pdl set the kernel is one link of a programmatic-dependent-launch chain:
+// it lets its successor launch at once, streams its own weights (which nothing
+// writes) right away, and waits for its predecessor's grid before it reads the
+// activation or writes y.
+template <int WT, int NWC>
+__global__ void __launch_bounds__((NWC + 1) * 32, 1) matvec_kernel(const uint8_t* __restrict__ W,
+                                                                const uint8_t* __restrict__ xq, float* __restrict__ y,
+                                                                int N, int K, int lpr, int stage_rows, int nstages,
+                                                                uint32_t stage_bytes, uint32_t act_bytes, int pdl) {
     using F = Fmt<WT>;
+    if (pdl) pdl_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    uint8_t* aq = smem + 128;
+    // [0, 16*nstages): full and empty mbarriers | activation | stage buffers
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + nstages;
+    const uint32_t bar_bytes = align_up(16u * nstages, 128u);
+    uint8_t* aq = smem + bar_bytes;
     const int nd = F::ACT == QMM_Q8_0 ? K / 32 : K / 256;
     float* ad = reinterpret_cast<float*>(aq + K);
     int* as = reinterpret_cast<int*>(ad + nd);
     uint8_t* stages = smem + act_bytes;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int units = K / F::BV;
     const uint64_t rb = (uint64_t)units * F::BB;
-    const int rows_per_warp = 32 / lpr;
-    const int R = (kThreads / 32) * rows_per_warp;
     const int r_begin = (int)(((int64_t)N * blockIdx.x) / gridDim.x);
     const int r_end = (int)(((int64_t)N * (blockIdx.x + 1)) / gridDim.x);
-    const int nst = (r_end - r_begin + R - 1) / R;
+    const int nst = (r_end - r_begin + stage_rows - 1) / stage_rows;
     const uint64_t total = (uint64_t)N * rb;
     const uint64_t total_al = total & ~15ull;
 
     if (tid == 0) {
-        for (int i = 0; i < nstages; i++) mbar_init(smem_u32(&bars[i]), 1);
+        for (int i = 0; i < nstages; i++) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), NWC);
+        }
         fence_mbar_init();
     }
     __syncthreads();
 
-    const uint64_t pol = policy_evict_first();
-    auto issue = [&](int s) {
-        const int r0 = r_begin + s * R;
-        const int r1 = min(r0 + R, r_end);
-        const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
-        uint64_t a1 = ((uint64_t)r1 * rb + 15ull) & ~15ull;
-        if (a1 > total_al) a1 = total_al;
-        const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
-        const int buf = s % nstages;
-        const uint32_t bar = smem_u32(&bars[buf]);
-        mbar_arrive_expect_tx(bar, bytes);
-        if (bytes) bulk_g2s(smem_u32(stages + (size_t)buf * stage_cap), W + a0, bytes, bar, pol);
-    };
-    if (tid == 0) {
-        const int first = nst < nstages ? nst : nstages;
-        for (int s = 0; s < first; s++) issue(s);
+    if (warp == NWC) {  // ------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            for (int s = 0; s < nst; s++) {
+                const int buf = s % nstages;
+                if (s >= nstages &&
+                    !mbar_wait_bounded(smem_u32(&empty[buf]), (uint32_t)((s / nstages) - 1) & 1u, kWaitLimitNs)) {
+                    atomicOr(&g_matvec_error, kErrTimeout);
+                    break;
+                }
+                const int r0 = r_begin + s * stage_rows;
+                const int r1 = min(r0 + stage_rows, r_end);
+                const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
+                uint64_t a1 = ((uint64_t)r1 * rb + 15ull) & ~15ull;
+                if (a1 > total_al) a1 = total_al;
+                const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
+                const uint32_t bar = smem_u32(&full[buf]);
+                mbar_arrive_expect_tx(bar, bytes);
+                if (bytes) bulk_g2s(smem_u32(stages + (size_t)buf * stage_bytes), W + a0, bytes, bar, pol);
+            }
+        }
+        return;
     }
 
-    // the activation row comes from the previous kernel in the stream
-    if (pdl) pdl_wait();
-    if constexpr (F::ACT == QMM_Q8_0) unpack_q8_0_row(xq, K, aq, ad, as);
-    else unpack_q8_K_row(xq, K, aq, ad, as);
-    __syncthreads();
-
-    const ActView act{smem_u32(aq), ad, as};
-    const int warp = tid >> 5, lane = tid & 31;
+    // ---------------------------------------------------------------- consumers
+    if (pdl) pdl_wait();  // the activation row comes from the previous kernel
+    {
+        // unpack with the consumer warps only (the producer has left)
+        const int nthr = NWC * 32;
+        if constexpr (F::ACT == QMM_Q8_0) {
+            for (int b = tid; b < nd; b += nthr) unpack_q8_0_block(xq, K, b, aq, ad, as);
+        } else {
+            for (int i = tid; i < nd * 73; i += nthr) unpack_q8_K_word(xq, nd, i, aq, ad, as);
+        }
+        consumer_sync(nthr);
+    }
+    const ActView act{aq, ad, as, nd};
+    const int rows_per_pass = 32 / lpr;
     const int rsub = lane / lpr, li = lane % lpr;
-
     for (int s = 0; s < nst; s++) {
         const int buf = s % nstages;
-        const uint32_t parity = (uint32_t)(s / nstages) & 1u;
-        const bool ok = mbar_wait_bounded(smem_u32(&bars[buf]), parity, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicOr(&g_matvec_error, kErrTimeout);
+        const bool ok = mbar_wait_bounded(smem_u32(&full[buf]), (uint32_t)(s / nstages) & 1u, kWaitLimitNs);
+        if (__any_sync(0xffffffffu, !ok)) {
+            if (lane == 0) atomicOr(&g_matvec_error, kErrTimeout);
             return;
         }
-        const int r0 = r_begin + s * R;
-        const int r1 = min(r0 + R, r_end);
+        const int r0 = r_begin + s * stage_rows;
+        const int r1 = min(r0 + stage_rows, r_end);
         const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
-        uint8_t* sbuf = stages + (size_t)buf * stage_cap;
-        const uint64_t g1 = (uint64_t)r1 * rb;
-        if (g1 > total_al) {  // the last < 16 bytes of W: not reachable by a 16-byte bulk copy
-            const uint64_t t0 = total_al > a0 ? total_al : a0;
-            for (uint64_t i = t0 + tid; i < g1; i += kThreads) sbuf[i - a0] = W[i];
-            __syncthreads();
+        uint8_t* sbuf = stages + (size_t)buf * stage_bytes;
+        const SmemBytes wv{sbuf};
+        // passes of this stage go to warps round-robin, rotated by stage, so that
+        // with fewer passes than warps successive stages land on different warps
+        const int npass = (r1 - r0 + rows_per_pass - 1) / rows_per_pass;
+        const int rot = (int)(((int64_t)s * stage_rows / rows_per_pass) % NWC);
+        for (int p = (warp - rot + NWC) % NWC; p < npass; p += NWC) {
+            const int row = r0 + p * rows_per_pass + rsub;
+            if (row == N - 1 && (uint64_t)N * rb > total_al) {
+                // the last < 16 bytes of W lie in the last row: not reachable by a
+                // 16-byte bulk copy, so this warp fetches them itself
+                for (uint64_t i = total_al + li; i < total; i += lpr) sbuf[i - a0] = W[i];
+            }
+            __syncwarp();
+            float acc = 0.0f;
+            if (row < r1) {
+                const uint32_t ro = (uint32_t)((uint64_t)row * rb - a0);
+#pragma unroll 4
+                for (int u = li; u < units; u += lpr) acc += unit_contrib<WT>(wv, ro + (uint32_t)(u * F::BB), act, u);
+            }
+            for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (row < r1 && li == 0) y[row] = acc;
         }
-        const SmemBytes wv{smem_u32(sbuf)};
-        const int row = r0 + warp * rows_per_warp + rsub;
-        float acc = 0.0f;
-        if (row < r1) {
-            const uint32_t ro = (uint32_t)((uint64_t)row * rb - a0);
-            for (int u = li; u < units; u += lpr) acc += unit_contrib<WT>(wv, ro + (uint32_t)(u * F::BB), act, u);
-        }
-        for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (row < r1 && li == 0) y[row] = acc;
-        __syncthreads();
-        if (tid == 0 && s + nstages < nst) issue(s + nstages);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[buf]));
     }
 }
 
@@ -193,8 +241,8 @@ __global__ void __launch_bounds__(kThreads) blocksums_kernel(const uint8_t* __re
     for (uint64_t i = a0 + threadIdx.x; i < g1; i += blockDim.x) wbuf[i - a0] = W[i];
     __syncthreads();
 
-    const ActView act{smem_u32(aq), ad, as};
-    const SmemBytes wv{smem_u32(wbuf)};
+    const ActView act{aq, ad, as, nd};
+    const SmemBytes wv{wbuf};
     const int per = F::ACT == QMM_Q8_0 ? units : 2 * units;
     for (int i = threadIdx.x; i < (r1 - r0) * units; i += blockDim.x) {
         const int row = r0 + i / units, u = i % units;
@@ -233,7 +281,10 @@ qmm_status current_device(DeviceInfo* info) {
     return QMM_OK;
 }
 
-// Picks lanes-per-row, rows per stage, stage count and grid for (format, N, K).
+// Picks the launch shape for (format, N, K): lanes per row cover the row's
+// blocks (a pass = 32 / lpr rows); a stage is whole passes and about 32 KB (at
+// least one pass); 2-4 stages in flight; 16 consumer warps unless a pass is so
+// large that a stage must be smaller, then 8 or 4.
 template <int WT>
 static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, MatvecPlan* p) {
     using F = Fmt<WT>;
@@ -241,27 +292,59 @@ static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, Matve
     int lpr = 1;
     while (lpr < 32 && lpr < units) lpr <<= 1;
     p->lpr = lpr;
-    p->rows_per_stage = (kThreads / 32) * (32 / lpr);
     const uint64_t rb = (uint64_t)units * F::BB;
-    const uint64_t cap = align_up((uint32_t)(p->rows_per_stage * rb + 48), 128u);
-    p->act_bytes = act_region_bytes(F::ACT, (int)K);
-    const uint64_t budget = (uint64_t)dev.max_smem_optin - p->act_bytes;
-    if (cap > budget) return QMM_E_SHAPE;
-    p->stage_cap = (uint32_t)cap;
-    // as many stages as fit, up to kMaxStages, keeping about 160 KB of weights in flight
-    int ns = (int)(budget / cap);
-    if (ns > kMaxStages) ns = kMaxStages;
-    const int want = (int)((160u * 1024u + cap - 1) / cap);
-    if (ns > want) ns = want < 2 ? 2 : want;
+    const int rpp = 32 / lpr;
+    const uint64_t pass_bytes = (uint64_t)rpp * rb;
+    int npass = (int)((32u * 1024u) / pass_bytes);
+    if (npass < 1) npass = 1;
+    p->stage_rows = npass * rpp;
+    const uint64_t sb = align_up((uint32_t)(npass * pass_bytes + 48), 128u);
+    if (sb > 0x7FFFFFFFull) return QMM_E_SHAPE;
+    p->stage_bytes = (uint32_t)sb;
+    const uint32_t act = act_region_bytes(F::ACT, (int)K);
+    const uint64_t total = (uint64_t)dev.max_smem_optin;
+    int ns = 0;
+    for (int cand = 4; cand >= 1; cand--) {
+        const uint64_t need = align_up(16u * cand, 128u) + act + (uint64_t)cand * p->stage_bytes;
+        if (need <= total) { ns = cand; break; }
+    }
     if (ns < 1) return QMM_E_SHAPE;
-    p->nstages = ns;
-    p->smem = p->act_bytes + (uint32_t)ns * p->stage_cap;
-    const int64_t stages_total = (N + p->rows_per_stage - 1) / p->rows_per_stage;
+    p->nstages = ns < 3 ? ns : 3;
+    p->nwc = pass_bytes > 16384 ? 8 : 16;
+    p->act_bytes = align_up(16u * p->nstages, 128u) + act;
+    p->smem = p->act_bytes + (uint32_t)p->nstages * p->stage_bytes;
     int64_t grid = dev.sms;
+    const int64_t stages_total = (N + p->stage_rows - 1) / p->stage_rows;
     if (grid > stages_total) grid = stages_total;
     if (grid < 1) grid = 1;
     p->grid = (int)grid;
     return QMM_OK;
+}
+
+template <int WT, int NWC>
+static qmm_status launch_matvec_nt(const void* W, const void* xq, float* y, int64_t N, int64_t K,
+                                   const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
+    static bool attr_set[64] = {false};
+    if (!attr_set[dev.device]) {
+        if (cudaFuncSetAttribute(matvec_kernel<WT, NWC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 dev.max_smem_optin) != cudaSuccess)
+            return QMM_E_CUDA;
+        attr_set[dev.device] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((NWC + 1) * 32);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, NWC>, (const uint8_t*)W, (const uint8_t*)xq, y,
+                                             (int)N, (int)K, p.lpr, p.stage_rows, p.nstages, p.stage_bytes,
+                                             p.act_bytes, pdl ? 1 : 0);
+    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
 template <int WT>
@@ -273,26 +356,8 @@ static qmm_status launch_matvec(const void* W, const void* xq, float* y, int64_t
     MatvecPlan p;
     st = plan_matvec<WT>(N, K, dev, &p);
     if (st != QMM_OK) return st;
-    static bool attr_set[64] = {false};
-    if (!attr_set[dev.device]) {
-        if (cudaFuncSetAttribute(matvec_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin) !=
-            cudaSuccess)
-            return QMM_E_CUDA;
-        attr_set[dev.device] = true;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT>, (const uint8_t*)W, (const uint8_t*)xq, y, (int)N,
-                                             (int)K, p.lpr, p.nstages, p.stage_cap, p.act_bytes, pdl ? 1 : 0);
-    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+    if (p.nwc == 16) return launch_matvec_nt<WT, 16>(W, xq, y, N, K, p, dev, stream, pdl);
+    return launch_matvec_nt<WT, 8>(W, xq, y, N, K, p, dev, stream, pdl);
 }
 
 // Public calls require 16-byte aligned bases; internal per-token calls pass rows
@@ -328,7 +393,7 @@ static qmm_status launch_blocksums(const void* W, const void* xq, int32_t* s, in
     qmm_status st = current_device(&dev);
     if (st != QMM_OK) return st;
     const uint64_t rb = (uint64_t)(K / F::BV) * F::BB;
-    const uint32_t act = act_region_bytes(F::ACT, (int)K);
+    const uint32_t act = 128u + act_region_bytes(F::ACT, (int)K);
     int rows = (int)(16384 / rb);
     if (rows < 1) rows = 1;
     if (rows > 64) rows = 64;

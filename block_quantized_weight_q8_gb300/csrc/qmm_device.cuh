@@ -114,46 +114,51 @@ constexpr unsigned kErrTimeout = 1u;
 // ---------------------------------------------------------------- unaligned byte reader
 // A view of bytes in shared memory at a 2-byte-aligned offset.  word(i) returns
 // the 4 bytes at off + 4i (little-endian), assembled from aligned 32-bit loads.
+// Plain C++ loads, so the compiler orders them after the barriers that publish
+// the data and is free to batch them.
 struct SmemBytes {
-    uint32_t base;  // shared-memory address of byte 0 of the view
-    __device__ __forceinline__ uint32_t u16(uint32_t off) const { return lds16(base + off); }
-    __device__ __forceinline__ uint32_t u8(uint32_t off) const {
-        uint32_t w = lds32((base + off) & ~3u);
-        return (w >> (8 * ((base + off) & 3u))) & 0xFFu;
+    const uint8_t* base;  // shared-memory pointer to byte 0 of the view (16-byte aligned)
+    __device__ __forceinline__ uint32_t w32(uint32_t off) const {  // off % 4 == 0
+        return *reinterpret_cast<const uint32_t*>(base + off);
     }
-    // n consecutive words starting at byte `off` (off even), into out[0..n)
+    __device__ __forceinline__ uint32_t u16(uint32_t off) const {  // off % 2 == 0
+        return *reinterpret_cast<const unsigned short*>(base + off);
+    }
+    // NW consecutive little-endian words starting at byte `off` (off even)
     template <int NW>
     __device__ __forceinline__ void words(uint32_t off, uint32_t* out) const {
-        const uint32_t a = base + off;
-        const uint32_t a0 = a & ~3u;
-        const uint32_t sh = (a & 3u) * 8u;
-        uint32_t prev = lds32(a0);
+        const uint32_t a0 = off & ~3u;
+        const uint32_t sh = (off & 3u) * 8u;
+        uint32_t raw[NW + 1];
 #pragma unroll
-        for (int i = 0; i < NW; i++) {
-            uint32_t next = lds32(a0 + 4u * (i + 1));
-            out[i] = __funnelshift_r(prev, next, sh);
-            prev = next;
-        }
+        for (int i = 0; i <= NW; i++) raw[i] = w32(a0 + 4u * i);
+#pragma unroll
+        for (int i = 0; i < NW; i++) out[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
     }
     // the same when `off` is known to be 4-byte aligned
     template <int NW>
     __device__ __forceinline__ void words_aligned(uint32_t off, uint32_t* out) const {
 #pragma unroll
-        for (int i = 0; i < NW; i++) out[i] = lds32(base + off + 4u * i);
+        for (int i = 0; i < NW; i++) out[i] = w32(off + 4u * i);
     }
 };
 
-// The activation row, unpacked once per CTA into shared memory:
-//   q[K]      int8 codes, 16-byte aligned, contiguous
-//   d[nb]     f32 block scales (Q8_0: from f16; Q8_K: as stored)
-//   s[...]    Q8_0: int32 sum of each block's 32 codes (used for the Q4_0 -8);
-//             Q8_K: int32 bsums, 16 per super-block.
+// The activation row, unpacked once per CTA into shared memory, chunk-major:
+//   q         int8 codes as 16-byte chunks, chunk c of block u at (c*n + u)*16
+//             (n = blocks per row), so lanes working on consecutive blocks read
+//             consecutive 16-byte words -- no bank conflicts
+//   d[n]      f32 block scales (Q8_0: from f16; Q8_K: as stored)
+//   s         Q8_0: int32 sum of each block's 32 codes, s[u] (for the Q4_0 -8);
+//             Q8_K: int32 bsums, group g of block u at s[g*n + u].
 struct ActView {
-    uint32_t q;  // shared address of the int8 codes
+    const uint8_t* q;
     const float* d;
     const int* s;
-    __device__ __forceinline__ uint32_t qword(uint32_t elem) const { return lds32(q + elem); }
-    __device__ __forceinline__ uint4 qvec(uint32_t elem) const { return lds128(q + elem); }
+    int n;
+    __device__ __forceinline__ uint4 chunk(int u, int c) const {
+        return *reinterpret_cast<const uint4*>(q + ((size_t)c * n + u) * 16);
+    }
+    __device__ __forceinline__ int bsum(int u, int g) const { return s[g * n + u]; }
 };
 
 // ---------------------------------------------------------------- block decoders
@@ -171,15 +176,15 @@ __device__ __forceinline__ int q4_0_isum(const SmemBytes& w, uint32_t o, const A
     *d_bits = w.u16(o);
     uint32_t qs[4];
     w.words<4>(o + 2, qs);
-    const uint4 lo = a.qvec(32u * b), hi = a.qvec(32u * b + 16u);
+    const uint4 lo = a.chunk(b, 0), hi = a.chunk(b, 1);
     const uint32_t al[4] = {lo.x, lo.y, lo.z, lo.w}, ah[4] = {hi.x, hi.y, hi.z, hi.w};
-    int s = 0;
+    int s0 = 0, s1 = 0;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        s = dp4a(qs[i] & 0x0F0F0F0Fu, al[i], s);
-        s = dp4a((qs[i] >> 4) & 0x0F0F0F0Fu, ah[i], s);
+        s0 = dp4a(qs[i] & 0x0F0F0F0Fu, al[i], s0);
+        s1 = dp4a((qs[i] >> 4) & 0x0F0F0F0Fu, ah[i], s1);
     }
-    return s - 8 * a.s[b];
+    return s0 + s1 - 8 * a.s[b];
 }
 
 // Q8_0 x Q8_0: isum = sum_j w_j * a_j ([minfer] s3.2, the Q8_0 kernel).
@@ -188,41 +193,40 @@ __device__ __forceinline__ int q8_0_isum(const SmemBytes& w, uint32_t o, const A
     *d_bits = w.u16(o);
     uint32_t qs[8];
     w.words<8>(o + 2, qs);
-    const uint4 lo = a.qvec(32u * b), hi = a.qvec(32u * b + 16u);
-    int s = 0;
-    s = dp4a(qs[0], lo.x, s); s = dp4a(qs[1], lo.y, s); s = dp4a(qs[2], lo.z, s); s = dp4a(qs[3], lo.w, s);
-    s = dp4a(qs[4], hi.x, s); s = dp4a(qs[5], hi.y, s); s = dp4a(qs[6], hi.z, s); s = dp4a(qs[7], hi.w, s);
-    return s;
+    const uint4 lo = a.chunk(b, 0), hi = a.chunk(b, 1);
+    int s0 = 0, s1 = 0;
+    s0 = dp4a(qs[0], lo.x, s0); s1 = dp4a(qs[1], lo.y, s1); s0 = dp4a(qs[2], lo.z, s0); s1 = dp4a(qs[3], lo.w, s1);
+    s0 = dp4a(qs[4], hi.x, s0); s1 = dp4a(qs[5], hi.y, s1); s0 = dp4a(qs[6], hi.z, s0); s1 = dp4a(qs[7], hi.w, s1);
+    return s0 + s1;
 }
 
 // Q4_K x Q8_K ([minfer] s3.2, the K-quant dot walked): for chunk j of 32 nibble
 // bytes, low nibbles pair with activations 64j + l, high with 64j + 32 + l;
 // value = sum_j s_lo*sc[2j] + s_hi*sc[2j+1]; min = sum_s m_s*(bsum_2s + bsum_2s+1).
-// The super-block starts 4-byte aligned (144-byte blocks, 16-byte aligned rows).
+// 144-byte super-blocks in 16-byte aligned rows: read with 16-byte loads.
 __device__ __forceinline__ void q4_K_isums(const SmemBytes& w, uint32_t o, const ActView& a, int u, int* value,
                                            int* minterm, uint32_t* d_bits, uint32_t* dmin_bits) {
-    uint32_t h[4];
-    w.words_aligned<4>(o, h);
-    *d_bits = h[0] & 0xFFFFu;
-    *dmin_bits = h[0] >> 16;
-    // 6-bit scales and mins (GGUF packing, a reading): bytes b0..b11 = h[1..3]
-    const uint32_t sc_lo = h[1] & 0x3F3F3F3Fu;                                   // sc 0..3
-    const uint32_t mn_lo = h[2] & 0x3F3F3F3Fu;                                   // m 0..3
-    const uint32_t sc_hi = (h[3] & 0x0F0F0F0Fu) | ((h[1] >> 2) & 0x30303030u);   // sc 4..7
-    const uint32_t mn_hi = ((h[3] >> 4) & 0x0F0F0F0Fu) | ((h[2] >> 2) & 0x30303030u);  // m 4..7
-    const int* bs = a.s + 16 * u;
+    const uint4 h = *reinterpret_cast<const uint4*>(w.base + o);
+    *d_bits = h.x & 0xFFFFu;
+    *dmin_bits = h.x >> 16;
+    // 6-bit scales and mins (GGUF packing, a reading): bytes b0..b11 = h.y, h.z, h.w
+    const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;                                   // sc 0..3
+    const uint32_t mn_lo = h.z & 0x3F3F3F3Fu;                                   // m 0..3
+    const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);   // sc 4..7
+    const uint32_t mn_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);  // m 4..7
     int m = 0;
 #pragma unroll
-    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_lo, s) * (bs[2 * s] + bs[2 * s + 1]);
+    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_lo, s) * (a.bsum(u, 2 * s) + a.bsum(u, 2 * s + 1));
 #pragma unroll
-    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_hi, s) * (bs[8 + 2 * s] + bs[8 + 2 * s + 1]);
+    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_hi, s) * (a.bsum(u, 8 + 2 * s) + a.bsum(u, 9 + 2 * s));
     int v = 0;
 #pragma unroll
     for (int j = 0; j < 4; j++) {
-        uint32_t q[8];
-        w.words_aligned<8>(o + 16 + 32 * j, q);
-        const uint32_t e = 256u * u + 64u * j;
-        const uint4 l0 = a.qvec(e), l1 = a.qvec(e + 16), h0 = a.qvec(e + 32), h1 = a.qvec(e + 48);
+        const uint4 q0 = *reinterpret_cast<const uint4*>(w.base + o + 16 + 32 * j);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(w.base + o + 32 + 32 * j);
+        const uint32_t q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint4 l0 = a.chunk(u, 4 * j), l1 = a.chunk(u, 4 * j + 1);
+        const uint4 h0 = a.chunk(u, 4 * j + 2), h1 = a.chunk(u, 4 * j + 3);
         const uint32_t al[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
         const uint32_t ah[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
         int s_lo = 0, s_hi = 0;
@@ -245,21 +249,19 @@ __device__ __forceinline__ void q2_K_isums(const SmemBytes& w, uint32_t o, const
                                            int* minterm, uint32_t* d_bits, uint32_t* dmin_bits) {
     uint32_t scw[4];
     w.words_aligned<4>(o, scw);
-    const uint32_t dd = lds32(w.base + o + 80);
+    const uint32_t dd = w.w32(o + 80);
     *d_bits = dd & 0xFFFFu;
     *dmin_bits = dd >> 16;
-    const int* bs = a.s + 16 * u;
     int m = 0, v = 0;
 #pragma unroll
-    for (int g = 0; g < 16; g++) m += (int)(byte_of(scw[g >> 2], g & 3) >> 4) * bs[g];
+    for (int g = 0; g < 16; g++) m += (int)(byte_of(scw[g >> 2], g & 3) >> 4) * a.bsum(u, g);
 #pragma unroll
     for (int h = 0; h < 2; h++) {
         uint32_t q[8];
         w.words_aligned<8>(o + 16 + 32 * h, q);
 #pragma unroll
         for (int s = 0; s < 4; s++) {
-            const uint32_t e = 256u * u + 128u * h + 32u * s;
-            const uint4 a0 = a.qvec(e), a1 = a.qvec(e + 16);
+            const uint4 a0 = a.chunk(u, 8 * h + 2 * s), a1 = a.chunk(u, 8 * h + 2 * s + 1);
             const uint32_t sh = 2u * s;
             int g0 = 0, g1 = 0;
             g0 = dp4a((q[0] >> sh) & 0x03030303u, a0.x, g0);
@@ -287,39 +289,34 @@ __device__ __forceinline__ void q6_K_isums(const SmemBytes& w, uint32_t o, const
     uint32_t scw[4];
     w.words<4>(o + 192, scw);
     *d_bits = w.u16(o + 208);
-    const int* bs = a.s + 16 * u;
     int m = 0, v = 0;
 #pragma unroll
-    for (int g = 0; g < 16; g++) m += (int)(int8_t)byte_of(scw[g >> 2], g & 3) * bs[g];
+    for (int g = 0; g < 16; g++) m += (int)(int8_t)byte_of(scw[g >> 2], g & 3) * a.bsum(u, g);
 #pragma unroll
     for (int n = 0; n < 2; n++) {
         uint32_t A[8], B[8], H[8];
         w.words<8>(o + 64 * n, A);
         w.words<8>(o + 64 * n + 32, B);
         w.words<8>(o + 128 + 32 * n, H);
-        int acc[4][2];
-#pragma unroll
-        for (int k = 0; k < 4; k++) acc[k][0] = acc[k][1] = 0;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const uint32_t q0 = (A[i] & 0x0F0F0F0Fu) | ((H[i] << 4) & 0x30303030u);
-            const uint32_t q1 = (B[i] & 0x0F0F0F0Fu) | ((H[i] << 2) & 0x30303030u);
-            const uint32_t q2 = ((A[i] >> 4) & 0x0F0F0F0Fu) | (H[i] & 0x30303030u);
-            const uint32_t q3 = ((B[i] >> 4) & 0x0F0F0F0Fu) | ((H[i] >> 2) & 0x30303030u);
-            const uint32_t e = 256u * u + 128u * n + 4u * i;
-            const int half = i >> 2;
-            acc[0][half] = dp4a(q0, a.qword(e), acc[0][half]);
-            acc[1][half] = dp4a(q1, a.qword(e + 32), acc[1][half]);
-            acc[2][half] = dp4a(q2, a.qword(e + 64), acc[2][half]);
-            acc[3][half] = dp4a(q3, a.qword(e + 96), acc[3][half]);
-        }
 #pragma unroll
         for (int k = 0; k < 4; k++) {
+            // elements 128n + 32k + 4i: chunks 8n + 2k (i < 4) and 8n + 2k + 1 (i >= 4)
+            const uint4 c0 = a.chunk(u, 8 * n + 2 * k), c1 = a.chunk(u, 8 * n + 2 * k + 1);
+            const uint32_t av[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            int acc0 = 0, acc1 = 0;
 #pragma unroll
-            for (int hf = 0; hf < 2; hf++) {
-                const int g = 8 * n + 2 * k + hf;
-                v += (int)(int8_t)byte_of(scw[g >> 2], g & 3) * acc[k][hf];
+            for (int i = 0; i < 8; i++) {
+                uint32_t q;
+                if (k == 0) q = (A[i] & 0x0F0F0F0Fu) | ((H[i] << 4) & 0x30303030u);
+                else if (k == 1) q = (B[i] & 0x0F0F0F0Fu) | ((H[i] << 2) & 0x30303030u);
+                else if (k == 2) q = ((A[i] >> 4) & 0x0F0F0F0Fu) | (H[i] & 0x30303030u);
+                else q = ((B[i] >> 4) & 0x0F0F0F0Fu) | ((H[i] >> 2) & 0x30303030u);
+                if (i < 4) acc0 = dp4a(q, av[i], acc0);
+                else acc1 = dp4a(q, av[i], acc1);
             }
+            const int g = 8 * n + 2 * k;
+            v += (int)(int8_t)byte_of(scw[g >> 2], g & 3) * acc0;
+            v += (int)(int8_t)byte_of(scw[(g + 1) >> 2], (g + 1) & 3) * acc1;
         }
     }
     *value = v;
@@ -328,43 +325,53 @@ __device__ __forceinline__ void q6_K_isums(const SmemBytes& w, uint32_t o, const
 
 // ---------------------------------------------------------------- activation unpack
 // Unpacks one activation row (Q8_0 or Q8_K blocks in global memory, row base
-// at least 2-byte aligned) into the shared-memory ActView arrays.  All threads
-// of the CTA take part; the caller synchronizes afterwards.
+// at least 2-byte aligned) into the chunk-major ActView arrays, one item per
+// call so that any set of threads can share the work; the caller synchronizes
+// those threads afterwards.
+__device__ __forceinline__ void unpack_q8_0_block(const uint8_t* __restrict__ row, int K, int b, uint8_t* q, float* d,
+                                                  int* s) {
+    const int nb = K / 32;
+    const unsigned short* p = reinterpret_cast<const unsigned short*>(row + 34 * b);
+    d[b] = h2f(p[0]);
+    uint32_t wv[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        wv[i] = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
+        sum = dp4a(wv[i], 0x01010101u, sum);
+    }
+    *reinterpret_cast<uint4*>(q + (size_t)b * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    *reinterpret_cast<uint4*>(q + ((size_t)nb + b) * 16) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    s[b] = sum;
+}
+
+// item i of ns * 73: word k = i % 73 of super-block u = i / 73 (d, 64 code
+// words, 8 bsum words)
+__device__ __forceinline__ void unpack_q8_K_word(const uint8_t* __restrict__ row, int ns, int i, uint8_t* q, float* d,
+                                                 int* s) {
+    const int u = i / 73, k = i % 73;
+    const uint32_t wv = *reinterpret_cast<const uint32_t*>(row + 292 * u + 4 * k);
+    if (k == 0) {
+        d[u] = __uint_as_float(wv);
+    } else if (k <= 64) {
+        const int c = (k - 1) >> 2, wi = (k - 1) & 3;
+        *reinterpret_cast<uint32_t*>(q + ((size_t)c * ns + u) * 16 + 4 * wi) = wv;
+    } else {
+        const int g = 2 * (k - 65);
+        s[g * ns + u] = (int)(int16_t)(wv & 0xFFFFu);
+        s[(g + 1) * ns + u] = (int)(int16_t)(wv >> 16);
+    }
+}
+
 __device__ __forceinline__ void unpack_q8_0_row(const uint8_t* __restrict__ row, int K, uint8_t* q, float* d,
                                                 int* s) {
-    const int nb = K / 32;
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-        const unsigned short* p = reinterpret_cast<const unsigned short*>(row + 34 * b);
-        d[b] = h2f(p[0]);
-        uint32_t* qo = reinterpret_cast<uint32_t*>(q + 32 * b);
-        int sum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const uint32_t wv = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
-            qo[i] = wv;
-            sum = dp4a(wv, 0x01010101u, sum);
-        }
-        s[b] = sum;
-    }
+    for (int b = threadIdx.x; b < K / 32; b += blockDim.x) unpack_q8_0_block(row, K, b, q, d, s);
 }
 
 __device__ __forceinline__ void unpack_q8_K_row(const uint8_t* __restrict__ row, int K, uint8_t* q, float* d,
                                                 int* s) {
     const int ns = K / 256;
-    // 73 words per block: d, 64 code words, 8 bsum words
-    for (int i = threadIdx.x; i < ns * 73; i += blockDim.x) {
-        const int u = i / 73, k = i % 73;
-        const uint32_t wv = *reinterpret_cast<const uint32_t*>(row + 292 * u + 4 * k);
-        if (k == 0) {
-            d[u] = __uint_as_float(wv);
-        } else if (k <= 64) {
-            *reinterpret_cast<uint32_t*>(q + 256 * u + 4 * (k - 1)) = wv;
-        } else {
-            const int g = 2 * (k - 65);
-            s[16 * u + g] = (int)(int16_t)(wv & 0xFFFFu);
-            s[16 * u + g + 1] = (int)(int16_t)(wv >> 16);
-        }
-    }
+    for (int i = threadIdx.x; i < ns * 73; i += blockDim.x) unpack_q8_K_word(row, ns, i, q, d, s);
 }
 
 }  // namespace qmm

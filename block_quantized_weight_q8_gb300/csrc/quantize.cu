@@ -25,9 +25,15 @@ __device__ __forceinline__ void st_u16(uint8_t* p, uint32_t v) {
 // f16, inverse 127/amax (0 for an all-zero block), codes rne(x * inverse)
 // saturated to int8.  Eight threads per block, four values each; the flat
 // [M][K] input is a flat array of blocks because K is a multiple of 32.
+// With pdl set the kernel is a link of a programmatic-dependent-launch chain:
+// it lets the consumer launch (and start streaming its weights) at once, and
+// waits for the previous grid before it reads x or writes xq.
 __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __restrict__ x, uint8_t* __restrict__ out,
                                                             int64_t nblocks, int pdl) {
-    if (pdl) pdl_launch_dependents();  // the consumer may start streaming its weights
+    if (pdl) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t b = gt >> 3;
     const int part = (int)(gt & 7);
@@ -57,7 +63,10 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __rest
 // 2g+1 hold group g.
 __global__ void __launch_bounds__(256) quantize_q8_K_kernel(const float4* __restrict__ x, uint8_t* __restrict__ out,
                                                             int64_t nblocks, int pdl) {
-    if (pdl) pdl_launch_dependents();
+    if (pdl) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
     const int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (b >= nblocks) return;  // whole warps leave together
@@ -287,19 +296,30 @@ static qmm_status check_quant_args(int t, const float* x, const void* xq, int64_
 
 qmm_status quantize_act_launch(int act, const float* x, void* xq, int64_t M, int64_t K, cudaStream_t stream,
                                bool pdl) {
+    int64_t grid;
+    int64_t nblocks;
     if (act == QMM_Q8_0) {
-        const int64_t nblocks = M * (K / 32);
-        const int64_t threads = nblocks * 8;
-        const int64_t grid = (threads + 255) / 256;
-        if (grid > 0x7FFFFFFFLL) return QMM_E_SHAPE;
-        quantize_q8_0_kernel<<<(unsigned)grid, 256, 0, stream>>>((const float4*)x, (uint8_t*)xq, nblocks, pdl ? 1 : 0);
+        nblocks = M * (K / 32);
+        grid = (nblocks * 8 + 255) / 256;
     } else {
-        const int64_t nblocks = M * (K / 256);
-        const int64_t grid = (nblocks * 32 + 255) / 256;
-        if (grid > 0x7FFFFFFFLL) return QMM_E_SHAPE;
-        quantize_q8_K_kernel<<<(unsigned)grid, 256, 0, stream>>>((const float4*)x, (uint8_t*)xq, nblocks, pdl ? 1 : 0);
+        nblocks = M * (K / 256);
+        grid = (nblocks * 32 + 255) / 256;
     }
-    return launch_status();
+    if (grid > 0x7FFFFFFFLL) return QMM_E_SHAPE;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e =
+        act == QMM_Q8_0
+            ? cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel, (const float4*)x, (uint8_t*)xq, nblocks, pdl ? 1 : 0)
+            : cudaLaunchKernelEx(&cfg, quantize_q8_K_kernel, (const float4*)x, (uint8_t*)xq, nblocks, pdl ? 1 : 0);
+    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
 template <class Kern>
