@@ -1,0 +1,563 @@
+"""Benchmark of the block-quantized weight x Q8 activation matmul on GB300.
+
+One JSON line on rank 0.  The headline workload is the Q8_0 x Q8_0 decode
+matvec of an 8B-class FFN gate (N = 12288 rows, K = 4096, one token): a step
+quantizes the token's activation (Q8_0) and streams the whole weight matrix
+through the matvec, and `value` is weight bytes per second over exactly K timed
+steps.  The same run measures, as extra keys, the other workloads (Q4_0
+4864x896, the Q4_K_M decoder-layer set, Q2_K 12288x4096, the Q4_0 prefill at
+M = 128/512/2048), the dominant kernel against the HBM roofline, the
+end-to-end path from pinned host memory, and the CPU oracle on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qmm|reference]
+
+Under torchrun each rank runs its own copy of the workload on its own GPU (the
+matvec shards along independent output rows, so ranks need no collective);
+`value` is the bytes of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "quant matvec weight-stream GB/s (M=1) & prefill int8 TOPS, % of roofline"
+HEADLINE = "q8_0_matvec_12288x4096"
+L2_BYTES = 129 * 10**6
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+PROFILE_FILE = os.path.join(ROOT, "profiles", "matvec_q8_0_12288x4096.txt")
+MATVEC_SOURCES = ["block_quantized_weight_q8_gb300/csrc/matvec.cu", "block_quantized_weight_q8_gb300/csrc/qmm_device.cuh"]
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env():
+    """(rank, local_rank, world_size) from the torchrun environment; (0, 0, 1) without it."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """The maximum of x over ranks (x itself on one rank)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, seconds_per_rank: float, world: int, device=None):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    t = reduce_max(seconds_per_rank, world, device)
+    return units_per_rank * world / t, t
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 200 ms while the benchmark runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [s for (t, s) in self.samples if any(a - 0.05 <= t <= b + 0.05 for a, b in self.windows)]
+        pool = inside if len(inside) >= 3 else [s for (_, s) in self.samples]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in pool:
+            f = [x.strip() for x in s.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(pool), "in_timed_regions": len(inside) >= 3}
+
+
+# ------------------------------------------------------------------ helpers
+def act_of(wtype):
+    return "q8_0" if wtype in ("q4_0", "q8_0") else "q8_K"
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def matvec_source_hash():
+    h = hashlib.sha256()
+    for p in MATVEC_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    try:
+        text = open(PROFILE_FILE).read()
+    except OSError:
+        return None, "no profile summary"
+    m_hash = re.search(r"kernel source hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram bytes per launch:\s*([0-9]+)", text)
+    if not (m_hash and m_bytes):
+        return None, "profile summary incomplete"
+    if m_hash.group(1) != matvec_source_hash():
+        return None, "kernel changed since the ncu capture"
+    return int(m_bytes.group(1)), "ncu capture"
+
+
+class Timer:
+    """CUDA events on a stream, bracketed by barrier + synchronize."""
+
+    def __init__(self, torch, stream, world, clocks):
+        self.torch, self.stream, self.world, self.clocks = torch, stream, world, clocks
+
+    def run(self, fn, iters: int) -> float:
+        torch = self.torch
+        barrier(self.world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        w0 = time.time()
+        e0.record(self.stream)
+        for i in range(iters):
+            fn(i)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        w1 = time.time()
+        barrier(self.world)
+        if self.clocks is not None:
+            self.clocks.mark(w0, w1)
+        return e0.elapsed_time(e1) / 1000.0  # seconds
+
+
+def make_graph(torch, stream, body, count: int):
+    """Capture `count` calls of body(i) into one CUDA graph on `stream`."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(count):
+            body(i)
+    return g
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank, local_rank, world):
+    import torch
+
+    import block_quantized_weight_q8_gb300 as qmm
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    init_dist(world, "nccl")
+    qmm.build()
+    qmm.load()
+    peaks = load_peaks()
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    stream = torch.cuda.Stream(device=dev)
+    timer = Timer(torch, stream, world, clocks)
+    out = {}
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def quantized_weights(wtype, N, K, seed, stream_id=0, jitter=False):
+        w = to_dev(workloads.weights_f32(N, K, seed, stream=stream_id, row_jitter=jitter))
+        W = torch.empty(N * qmm.qmm_row_bytes(wtype, K), dtype=torch.uint8, device=dev)
+        qmm.quantize(wtype, w, W, N, K, stream=torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        del w
+        return W
+
+    def copies_for(nbytes):
+        return max(2, int(np.ceil(2.5 * L2_BYTES / nbytes)))
+
+    graph_steps = 64
+
+    # ---------------- headline: Q8_0 decode step (quantize + matvec)
+    cfg = workloads.WORKLOADS[HEADLINE]
+    N, K = cfg["N"], cfg["K"]
+    W0 = quantized_weights("q8_0", N, K, cfg["seed"])
+    wbytes = W0.numel()
+    C = copies_for(wbytes)
+    Ws = [W0] + [W0.clone() for _ in range(C - 1)]
+    x = to_dev(workloads.activations_f32(1, K, cfg["seed"]))
+    xrb = qmm.qmm_row_bytes("q8_0", K)
+    xq = torch.empty(xrb, dtype=torch.uint8, device=dev)
+    y = torch.empty(N, dtype=torch.float32, device=dev)
+    sh = stream.cuda_stream
+
+    def step(i):
+        qmm.qmm_linear_q8_0(Ws[i % C], x, xq, xrb, y, 1, N, K, stream=sh)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+        graph = make_graph(torch, stream, step, graph_steps)
+    torch.cuda.synchronize()
+
+    def replay(n_steps):
+        full, rest = divmod(n_steps, graph_steps)
+        for _ in range(full):
+            graph.replay()
+        for i in range(rest):
+            step(i)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // graph_steps)):
+            graph.replay()
+        secs = timer.run(lambda i: replay(args.steps), 1)
+    value, tmax = aggregate(wbytes * args.steps, secs, world, dev)
+    ms_per_step = tmax / args.steps * 1e3
+    launches = 2 * args.steps
+
+    # dominant kernel alone (matvec, chained launches) for the roofline
+    def mv(i):
+        qmm.qmm_matvec_q8_0(Ws[i % C], xq, y, N, K, stream=sh)
+
+    with torch.cuda.stream(stream):
+        mv_graph = make_graph(torch, stream, mv, graph_steps)
+        mv_graph.replay()
+        reps = max(4, (args.steps + graph_steps - 1) // graph_steps)
+        mv_secs = timer.run(lambda i: mv_graph.replay(), reps)
+    mv_launch_s = mv_secs / (reps * graph_steps)
+    algo_bytes = wbytes + xrb + 4 * N
+    achieved = algo_bytes / mv_launch_s / 1e9
+    traffic, traffic_src = profiled_traffic()
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "kernel": "matvec_kernel<Q8_0>", "algorithmic_bytes_per_launch": algo_bytes,
+                "launch_us": round(mv_launch_s * 1e6, 3),
+                "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs: a copy kernel, read+write)" % peaks["source"],
+                "traffic_source": traffic_src}
+
+    # ---------------- end to end: pinned host x -> device, linear, y -> pinned host
+    x_host = torch.from_numpy(workloads.activations_f32(1, K, cfg["seed"] + 7)).pin_memory()
+    y_host = torch.empty(N, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty(K, dtype=torch.float32, device=dev)
+
+    def e2e_step(i):
+        x_dev.copy_(x_host.view(-1), non_blocking=True)
+        qmm.qmm_linear_q8_0(Ws[i % C], x_dev, xq, xrb, y, 1, N, K, stream=sh)
+        y_host.copy_(y, non_blocking=True)
+
+    e2e_steps = min(args.steps, 2000)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+        e2e_secs = timer.run(e2e_step, e2e_steps)
+    e2e_value, _ = aggregate(wbytes * e2e_steps, e2e_secs, world, dev)
+    e2e = {"value": round(e2e_value / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": 4 * K,
+           "d2h_bytes_per_step": 4 * N, "steps": e2e_steps,
+           "note": "eager calls through the public binding, host copies inside the timed region"}
+    del Ws, W0
+
+    # ---------------- other workloads
+    extra = {}
+    if not args.headline_only:
+        extra = other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantized_weights, copies_for)
+
+    clock_info = clocks.summary() if clocks else None
+    if clocks:
+        clocks.stop()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value / 1e9, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic (seeded N(0,0.02) weights quantized on the GPU; N(0,1) activation with 1% x20)",
+            "config": {"workload": HEADLINE, "wtype": "q8_0", "M": 1, "N": N, "K": K, "weight_bytes": wbytes,
+                       "step": "qmm_linear_q8_0: quantize_q8_0(x) + matvec_q8_0, chained launches, CUDA graph",
+                       "l2": "weights rotate over %d resident copies (%.0f MB > 2x the 129 MB L2)" % (
+                           C, C * wbytes / 1e6),
+                       "parallelism": "replicas: each rank streams its own weights" if world > 1 else "1 GPU"},
+            "roofline": roofline,
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "clocks": clock_info,
+            "configs": extra,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+
+
+def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantized_weights, copies_for):
+    res = {}
+    sh = stream.cuda_stream
+    hbm = peaks["hbm_gbs"]
+    steps = max(16, min(args.steps, 512))
+    graph_steps = 16
+
+    def timed_graph(body, n_body):
+        with torch.cuda.stream(stream):
+            for i in range(2):
+                body(i)
+            g = make_graph(torch, stream, body, n_body)
+            g.replay()
+            reps = max(2, steps // n_body)
+            secs = timer.run(lambda i: g.replay(), reps)
+        return secs / (reps * n_body)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # single matvecs
+    for name in ("q4_0_matvec_4864x896", "q2_K_matvec_12288x4096"):
+        cfg = workloads.WORKLOADS[name]
+        wtype, N, K = cfg["wtype"], cfg["N"], cfg["K"]
+        W0 = quantized_weights(wtype, N, K, cfg["seed"])
+        C = copies_for(W0.numel())
+        Ws = [W0] + [W0.clone() for _ in range(C - 1)]
+        act = act_of(wtype)
+        x = to_dev(workloads.activations_f32(1, K, cfg["seed"]))
+        xrb = qmm.qmm_row_bytes(act, K)
+        xq = torch.empty(xrb, dtype=torch.uint8, device=dev)
+        y = torch.empty(N, dtype=torch.float32, device=dev)
+
+        def step(i):
+            qmm.linear(wtype, Ws[i % C], x, xq, xrb, y, 1, N, K, stream=sh)
+
+        def mv(i):
+            qmm.matvec(wtype, Ws[i % C], xq, y, N, K, stream=sh)
+
+        t_step = timed_graph(step, graph_steps)
+        t_mv = timed_graph(mv, graph_steps)
+        wb = W0.numel()
+        res[name] = {"step_us": round(t_step * 1e6, 3), "GB/s": round(wb / t_step / 1e9, 1),
+                     "matvec_us": round(t_mv * 1e6, 3), "matvec_GB/s": round(wb / t_mv / 1e9, 1),
+                     "frac_hbm": round(wb / t_mv / 1e9 / hbm, 4), "weight_bytes": wb, "copies": C}
+        del Ws, W0
+
+    # the decoder-layer set: quantize(x_h) shared by Wq Wk Wv W_gate W_up; Wo and W_down on their own inputs
+    cfg = workloads.WORKLOADS["q4_K_M_layer_4096"]
+    mats = []
+    for i, (label, wtype, N, K) in enumerate(cfg["matrices"]):
+        mats.append((label, wtype, N, K, quantized_weights(wtype, N, K, cfg["seed"], stream_id=i, jitter=True)))
+    layer_bytes = sum(m[4].numel() for m in mats)
+    C = max(2, int(np.ceil(2.5 * 129e6 / layer_bytes)))
+    sets = [mats] + [[(a, b, c, d, W.clone()) for (a, b, c, d, W) in mats] for _ in range(C - 1)]
+    xh = to_dev(workloads.activations_f32(1, 4096, cfg["seed"]))
+    xo = to_dev(workloads.activations_f32(1, 4096, cfg["seed"] + 1))
+    xd = to_dev(workloads.activations_f32(1, 12288, cfg["seed"] + 2))
+    qh = torch.empty(qmm.qmm_row_bytes("q8_K", 4096), dtype=torch.uint8, device=dev)
+    qo = torch.empty_like(qh)
+    qd = torch.empty(qmm.qmm_row_bytes("q8_K", 12288), dtype=torch.uint8, device=dev)
+    outs = {m[0]: torch.empty(m[2], dtype=torch.float32, device=dev) for m in mats}
+
+    def layer(i):
+        s = sets[i % C]
+        qmm.qmm_quantize_q8_K(xh, qh, 1, 4096, stream=sh)
+        for (label, wtype, N, K, W) in s:
+            if label in ("Wq", "Wk", "Wv", "W_gate", "W_up"):
+                qmm.matvec(wtype, W, qh, outs[label], N, K, stream=sh)
+        qmm.qmm_quantize_q8_K(xo, qo, 1, 4096, stream=sh)
+        qmm.matvec("q4_K", s[3][4], qo, outs["Wo"], 4096, 4096, stream=sh)
+        qmm.qmm_quantize_q8_K(xd, qd, 1, 12288, stream=sh)
+        qmm.matvec("q6_K", s[6][4], qd, outs["W_down"], 4096, 12288, stream=sh)
+
+    t_layer = timed_graph(layer, 8)
+    res["q4_K_M_layer_4096"] = {"layer_us": round(t_layer * 1e6, 3), "GB/s": round(layer_bytes / t_layer / 1e9, 1),
+                                "frac_hbm": round(layer_bytes / t_layer / 1e9 / hbm, 4), "weight_bytes": layer_bytes,
+                                "equiv_tok_s_36_layers_matmuls_only": round(1.0 / (36 * t_layer), 1),
+                                "launches_per_layer": 10, "copies": C}
+    del sets, mats
+
+    # prefill
+    cfg = workloads.WORKLOADS["q4_0_prefill_512x12288x4096"]
+    N, K = cfg["N"], cfg["K"]
+    W = quantized_weights("q4_0", N, K, cfg["seed"])
+    pre = {}
+    for M in cfg["M_sweep"]:
+        x = to_dev(workloads.activations_f32(M, K, cfg["seed"] + M))
+        xrb = qmm.qmm_row_bytes("q8_0", K)
+        xq = torch.empty(M * xrb, dtype=torch.uint8, device=dev)
+        Y = torch.empty(M, N, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            qmm.qmm_quantize_q8_0(x, xq, M, K, stream=sh)
+
+        def mm(i):
+            qmm.qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=sh)
+
+        t = timed_graph(mm, 2)
+        ops = 2.0 * M * N * K
+        tops = ops / t / 1e12
+        pre["M=%d" % M] = {"us": round(t * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
+                           "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4),
+                           "frac_hbm_weight_stream": round(W.numel() / t / 1e9 / hbm, 4)}
+    res["q4_0_prefill_12288x4096"] = pre
+    return res
+
+
+# ------------------------------------------------------------------ CPU baseline (the oracle)
+def cpu_sample(nthreads: int, target_s: float):
+    """Time the oracle on the headline workload: quantize the token and run the matvec over as many
+    whole repetitions as fill about target_s seconds.  Returns (GB/s, seconds, reps, rows)."""
+    import oracle
+
+    cfg = workloads.WORKLOADS[HEADLINE]
+    N, K = cfg["N"], cfg["K"]
+    w = workloads.weights_f32(N, K, cfg["seed"])
+    W = oracle.quantize("q8_0", w)
+    x = workloads.activations_f32(1, K, cfg["seed"])
+    t0 = time.perf_counter()
+    xq = oracle.quantize("q8_0", x)
+    oracle.matmul("q8_0", W, xq, 1, N, K, nthreads=nthreads)
+    one = time.perf_counter() - t0
+    reps = max(1, int(target_s / max(one, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        xq = oracle.quantize("q8_0", x)
+        oracle.matmul("q8_0", W, xq, 1, N, K, nthreads=nthreads)
+    secs = time.perf_counter() - t0
+    return W.size * reps / secs / 1e9, secs, reps, N
+
+
+def cpu_baseline(args):
+    nthreads = os.cpu_count() or 1
+    gbs, secs, reps, rows = cpu_sample(nthreads, args.cpu_seconds)
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": "%d full steps of the %s workload (quantize + %d-row matvec), %.1f s, rows split over %d "
+                      "threads" % (reps, HEADLINE, rows, secs, nthreads)}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, timed on the host cores, same metric and workload."""
+    if rank != 0:
+        return
+    import oracle
+
+    nthreads = os.cpu_count() or 1
+    cfg = workloads.WORKLOADS[HEADLINE]
+    N, K = cfg["N"], cfg["K"]
+    W = oracle.quantize("q8_0", workloads.weights_f32(N, K, cfg["seed"]))
+    x = workloads.activations_f32(1, K, cfg["seed"])
+    rb = W.shape[1]
+    # each step: a bounded sample of the workload (the first `rows` rows), sized so the run ends in minutes
+    t0 = time.perf_counter()
+    oracle.matmul("q8_0", W, oracle.quantize("q8_0", x), 1, N, K, nthreads=nthreads)
+    full = time.perf_counter() - t0
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    rows = int(min(N, max(64, N * budget / max(full, 1e-4))))
+    Ws = np.ascontiguousarray(W[:rows])
+    for _ in range(args.warmup):
+        oracle.matmul("q8_0", Ws, oracle.quantize("q8_0", x), 1, rows, K, nthreads=nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmul("q8_0", Ws, oracle.quantize("q8_0", x), 1, rows, K, nthreads=nthreads)
+    secs = time.perf_counter() - t0
+    value = rows * rb * args.steps / secs / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic (seeded)",
+            "config": {"workload": HEADLINE, "wtype": "q8_0", "M": 1, "N": N, "K": K, "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                             "sample": "%d of %d rows per step, rows split over %d threads" % (rows, N, nthreads)},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4096)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["qmm", "reference"], default="qmm")
+    ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, local_rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
