@@ -46,6 +46,7 @@ SIGNATURES = {
     "qmm_linear_q6_K": ("pppspiiiq", ctypes.c_int),
     "qmm_linear_q2_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
+    "qmm_linear_noalloc": ("tpppiiiq", ctypes.c_int),
     "qmm_blocksums": ("tpppiiiq", ctypes.c_int),
     "qmm_device_status": ("c", ctypes.c_int),
 }
@@ -195,6 +196,12 @@ qmm_linear_q2_K = _lin("qmm_linear_q2_K")
 def linear(wtype, W, x, scratch, scratch_bytes, y, M, N, K, stream=None):
     _call("qmm_linear_" + wtype, ptr(W), ptr(x), ptr(scratch), int(scratch_bytes), ptr(y), int(M), int(N), int(K),
           stream_handle(stream))
+
+
+def qmm_linear_noalloc(wtype, W, x, y, M, N, K, stream=None):
+    """qmm_linear_<wtype> without a workspace argument: the library's own 1 MiB device array holds the
+    quantized rows (see include/qmm.h for the limit and the sharing rules)."""
+    _call("qmm_linear_noalloc", _type(wtype), ptr(W), ptr(x), ptr(y), int(M), int(N), int(K), stream_handle(stream))
 
 
 def qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=None):

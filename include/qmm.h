@@ -161,6 +161,28 @@ QMM_API qmm_status qmm_linear_q6_K(const void* W, const float* x, void* xq_scrat
 QMM_API qmm_status qmm_linear_q2_K(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
                            int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
 
+/* ---- quantize + multiply without a caller workspace ---------------------- */
+/* No counterpart on the pages: an addition for callers that cannot give the
+ * library a device buffer (a plugin inside an application that owns all device
+ * memory and passes in only inputs and outputs; a loop that must never call
+ * cudaMalloc, which can block on the device or fail; a fixed memory budget).
+ * Same result as qmm_linear_<wtype> (wtype a QMM_Q* weight type), but the
+ * quantized activation rows go to one 1 MiB array in device memory owned by the
+ * library, which every GPU that loads the library keeps until the process exits.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Limit: M * qmm_row_bytes(qmm_act_type(wtype), K) <= 1 MiB (240 tokens of
+ *     Q8_0 or 224 of Q8_K at K = 4096); larger calls return QMM_E_SCRATCH and
+ *     launch nothing.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - Every call, on every stream, uses the same array: calls that may overlap
+ *     on the GPU race with each other.  Issue them on one stream (or order them).
+ *   - The array keeps the last call's contents; nothing in it needs to start at
+ *     zero, because each call writes every byte it reads.
+ * Errors as for qmm_linear_<wtype>, plus QMM_E_TYPE for a non-weight type. */
+QMM_API qmm_status qmm_linear_noalloc(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t N,
+                                      int64_t K, qmm_stream_t stream);
+
 /* ---- prefill matmul, M tokens (hot path) -------------------------------- */
 /* Y[t][o] = sum_b d_w[o,b] * d_x[t,b] * isum[t,o,b] for M tokens at once: the
  * weights are read once per tile of tokens and reused across them ([krafla]
