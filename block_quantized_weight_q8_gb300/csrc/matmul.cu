@@ -1,4 +1,37 @@
-// matmul.cu -- the prefill matmul Y[M][N] = xq[M] . W^T for Q4_0 weights.
+// matmul.cu -- the prefill matmul Y[M][N] for Q4_0 weights x Q8_0 activations,
+// M tokens at once, on the 5th-generation tensor cores.
+//
+// Y[t][o] = sum_b d_w[o,b] * d_x[t,b] * isum[t,o,b] ([krafla] "Architecture",
+// Batched prompt prefill; [kvad] "Batched prefill, and i8mm"): the weights are
+// read once per tile of 128 tokens instead of once per token.
+//
+// sm_103a has no int8 tensor-core MMA (ptxas rejects tcgen05.mma .kind::i8 for
+// this target), so the integer codes go through .kind::f16 with fp16 operands:
+// every Q4_0 code (-8..7) and Q8_0 code (-128..127) is an exact fp16 value, all
+// products are exact, and each 32-wide block's sum (|sum| <= 32*8*128 < 2^24) is
+// exact in the fp32 accumulator -- the MMA computes the same integer isum the
+// scalar kernel does ([minfer] s3.2: the integer dot is exact; [ggml] s2).
+// Each block's sum is then folded into an fp32 accumulator once, scaled by
+// d_w * d_x, exactly as the pages' kernels fold per block.
+//
+// One CTA per output tile of 128 weight rows x 128 tokens:
+//   warp 0   producer: 2-D TMA loads of the raw weight bytes (128 rows x 8 blocks)
+//            and the raw activation bytes (128 tokens x 8 blocks) into a ring of
+//            raw stages; also owns the tensor-memory allocation
+//   warp 1   MMA issuer: per block, two tcgen05.mma (K = 16 each) into one of four
+//            128-column TMEM accumulators, then tcgen05.commit
+//   warps 2-9 converters (2-5 weight rows, 6-9 tokens): each thread loads its
+//            row of the raw stage into registers with 16-byte loads, then writes
+//            each block as fp16 operands in the UMMA K-major core-matrix layout
+//            (8 rows x 16 bytes per core matrix) plus its f32 scale
+//   warps 10-25 epilogue: tcgen05.ld of each block's exact sums (32 tokens of one
+//            weight row per thread), y += v * (d_w*d_x) in registers in block
+//            order, then the token-major store
+// All waits are bounded; a timeout records QMM_E_TIMEOUT, every warp still
+// reaches the end, and TMEM is freed.
+#include <cuda.h>
+#include <mutex>
+
 #include "qmm_device.cuh"
 #include "qmm_host.h"
 
@@ -9,14 +42,479 @@ static __device__ unsigned int g_matmul_error = 0;
 qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
                            bool pdl);
 
+namespace mm {
+
+constexpr int BM = 128;            // weight rows per tile (MMA M, TMEM lanes)
+constexpr int BN = 128;            // tokens per tile (MMA N, TMEM columns per accumulator)
+constexpr int KB = 8;              // Q blocks per raw stage (256 K values)
+constexpr int RAW_STAGES = 2;
+constexpr int OP_SLOTS = 4;        // converted blocks in flight
+constexpr int SC_SLOTS = 32;       // block scales in flight (outlive the operands)
+constexpr int NACC = 4;            // TMEM accumulators (4 x 128 columns = all 512)
+constexpr int W_RAW = BM * KB * 18;   // 18432
+constexpr int X_RAW = BN * KB * 34;   // 34816
+constexpr int RAW_BYTES = W_RAW + X_RAW;
+constexpr int OP_A = BM * 32 * 2;     // 8192: fp16 weights of one block
+constexpr int OP_B = BN * 32 * 2;     // 8192: fp16 activations of one block
+constexpr int NUM_CONV_WARPS = 8, NUM_EPI_WARPS = 16;  // converters: 4 for weights, 4 for activations
+constexpr int THREADS = (2 + NUM_CONV_WARPS + NUM_EPI_WARPS) * 32;  // 832
+constexpr int TMEM_COLS = NACC * BN;  // 512
+
+// shared memory layout (offsets from the 1024-byte aligned dynamic shared memory base)
+constexpr int OFF_RAW = 0;
+constexpr int OFF_OPA = OFF_RAW + RAW_STAGES * RAW_BYTES;       // 106496
+constexpr int OFF_OPB = OFF_OPA + OP_SLOTS * OP_A;              // 139264
+constexpr int OFF_SCW = OFF_OPB + OP_SLOTS * OP_B;              // 172032
+constexpr int OFF_SCX = OFF_SCW + SC_SLOTS * BM * 4;            // 176128
+constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;            // 180224
+// barriers: raw_full[2] raw_empty[2] op_full[4] op_empty[4] sc_empty[8] acc_full[4] acc_empty[4]
+constexpr int NBARS = 2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + 2 * NACC;
+constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+constexpr int SMEM_BYTES = OFF_TMEM + 16;
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of
+// 8 rows x 16 bytes stored as 128 contiguous bytes; `lbo` is the byte step
+// between core matrices along K, `sbo` along M/N.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+    // base offset 0, relative LBO, swizzle mode 0 (none)
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B f16, both K-major, N, M.
+__host__ __device__ constexpr uint32_t instr_desc_f16(int m, int n) {
+    return (1u << 4)                       // D format: f32
+           | (0u << 7) | (0u << 10)        // A, B format: f16
+           | (0u << 15) | (0u << 16)       // A, B K-major
+           | ((uint32_t)(n >> 3) << 17)    // N >> 3
+           | ((uint32_t)(m >> 4) << 24);   // M >> 4
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes into 32 registers.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%"
+        "20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 16 consecutive TMEM columns of this warp's 32 lanes into 16 registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+
+// fp16 bits of (1024 + byte) for two bytes picked by `sel` from x, next to 0x64.
+__device__ __forceinline__ uint32_t bytes_to_h2(uint32_t x, uint32_t sel) { return __byte_perm(x, 0x64646464u, sel); }
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Byte offset of element k (0..31, K order) of row r in a K-major core-matrix
+// operand of one 32-wide block: core matrix (r/8, k/8) at ((r/8)*4 + k/8)*128.
+__device__ __forceinline__ uint32_t op_off(int r, int kq) {  // kq = k / 8
+    return (uint32_t)(((r >> 3) * 4 + kq) * 128 + (r & 7) * 16);
+}
+
+struct Bars {
+    uint32_t base;
+    __device__ uint32_t raw_full(int i) const { return base + 8u * i; }
+    __device__ uint32_t raw_empty(int i) const { return base + 8u * (RAW_STAGES + i); }
+    __device__ uint32_t op_full(int i) const { return base + 8u * (2 * RAW_STAGES + i); }
+    __device__ uint32_t op_empty(int i) const { return base + 8u * (2 * RAW_STAGES + OP_SLOTS + i); }
+    __device__ uint32_t sc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + i); }
+    __device__ uint32_t acc_full(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + i); }
+    __device__ uint32_t acc_empty(int i) const {
+        return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + NACC + i);
+    }
+};
+
+// wait with a time limit; on failure set the error word and the CTA's abort flag.
+// The fast path (phase already complete) is a single try_wait: the roles here
+// share their schedulers with FP32-heavy warps, so every instruction counts.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
+    atomicOr(&g_matmul_error, kErrTimeout);
+    *abort_flag = 1;
+    return false;
+}
+
+// packed pairs of f32 (2 values per 64-bit register pair)
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
+
+__global__ void __launch_bounds__(THREADS, 1)
+    matmul_q4_0_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                       float* __restrict__ Y, int M, int N, int K, int pdl) {
+    if (pdl) pdl_launch_dependents();
+    // used directly (not re-aligned by integer arithmetic) so that the compiler
+    // keeps every access in the shared state space
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = smem_u32(smem);
+    if (sbase & 127u) {  // the TMA destinations and operand tiles need 128-byte alignment
+        if (threadIdx.x == 0) atomicOr(&g_matmul_error, kErrTimeout);
+        return;
+    }
+    const Bars bars{sbase + OFF_BAR};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_TMEM + 8);
+    const float* scw = reinterpret_cast<const float*>(smem + OFF_SCW);
+    const float* scx = reinterpret_cast<const float*>(smem + OFF_SCX);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o0 = blockIdx.x * BM, t0 = blockIdx.y * BN;
+    const int nb = K / 32;
+    const int nchunks = nb / KB;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RAW_STAGES; i++) {
+            mbar_init(bars.raw_full(i), 1);
+            mbar_init(bars.raw_empty(i), NUM_CONV_WARPS);
+        }
+        for (int i = 0; i < OP_SLOTS; i++) {
+            mbar_init(bars.op_full(i), NUM_CONV_WARPS);
+            mbar_init(bars.op_empty(i), 1);
+        }
+        for (int i = 0; i < SC_SLOTS; i++) mbar_init(bars.sc_empty(i), NUM_EPI_WARPS);
+        for (int i = 0; i < NACC; i++) {
+            mbar_init(bars.acc_full(i), 1);
+            mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {  // allocate the TMEM accumulators (whole warp)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            if (pdl) pdl_wait();  // the activation comes from the previous kernel
+            for (int c = 0; c < nchunks; c++) {
+                const int s = c % RAW_STAGES;
+                if (c >= RAW_STAGES && !wait_or_abort(bars.raw_empty(s), ((c / RAW_STAGES) - 1) & 1, abort_flag))
+                    break;
+                const uint32_t dst = sbase + OFF_RAW + s * RAW_BYTES;
+                mbar_arrive_expect_tx(bars.raw_full(s), RAW_BYTES);
+                tma_load_2d(dst, &wmap, c * (KB * 18 / 2), o0, bars.raw_full(s));
+                tma_load_2d(dst + W_RAW, &xmap, c * (KB * 34 / 2), t0, bars.raw_full(s));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc_f16(BM, BN);
+            // descriptors of slot 0; slot os adds os * OP_A (>> 4) to the address field
+            const uint64_t a0 = smem_desc(sbase + OFF_OPA, 128, 512);
+            const uint64_t b0 = smem_desc(sbase + OFF_OPB, 128, 512);
+            for (int b = 0; b < nb; b++) {
+                const int os = b % OP_SLOTS, ac = b % NACC;
+                if (!wait_or_abort(bars.op_full(os), (b / OP_SLOTS) & 1, abort_flag)) break;
+                if (b >= NACC && !wait_or_abort(bars.acc_empty(ac), ((b / NACC) - 1) & 1, abort_flag)) break;
+                tc_fence_after();
+                const uint64_t ad = a0 + (uint64_t)(os * (OP_A >> 4));
+                const uint64_t bd = b0 + (uint64_t)(os * (OP_B >> 4));
+                const uint32_t d = tmem + (uint32_t)(ac * BN);
+                mma_f16(d, ad, bd, idesc, 0);                    // K 0..15: core matrices 0, 1
+                mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1);  // K 16..31: core matrices 2, 3
+                mma_commit(bars.op_empty(os));
+                mma_commit(bars.acc_full(ac));
+            }
+        }
+    } else if (warp < 2 + NUM_CONV_WARPS) {
+        // ------------------------------------------------------------ converters
+        const bool is_w = warp < 2 + NUM_CONV_WARPS / 2;
+        const int r = (warp - (is_w ? 2 : 2 + NUM_CONV_WARPS / 2)) * 32 + lane;  // weight row or token, 0..127
+        for (int c = 0; c < nchunks; c++) {
+            const int s = c % RAW_STAGES;
+            if (!wait_or_abort(bars.raw_full(s), (c / RAW_STAGES) & 1, abort_flag)) break;
+            if (is_w) {
+                // this weight row's 8 blocks: 144 bytes, 16-byte aligned
+                uint32_t raw[36];
+                const uint4* src = reinterpret_cast<const uint4*>(smem + OFF_RAW + s * RAW_BYTES + r * (KB * 18));
+#pragma unroll
+                for (int i = 0; i < 9; i++) {
+                    const uint4 v = src[i];
+                    raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.raw_empty(s));
+#pragma unroll
+                for (int lb = 0; lb < KB; lb++) {
+                    const int b = c * KB + lb, os = b % OP_SLOTS, ss = b % SC_SLOTS;
+                    if (b >= OP_SLOTS && !wait_or_abort(bars.op_empty(os), ((b / OP_SLOTS) - 1) & 1, abort_flag)) break;
+                    if (b >= SC_SLOTS && !wait_or_abort(bars.sc_empty(ss), ((b / SC_SLOTS) - 1) & 1, abort_flag)) break;
+                    // block lb: f16 d at byte 18*lb, nibbles at 18*lb + 2 (element j low, j+16 high)
+                    const int off = 18 * lb;
+                    const uint32_t dbits = __funnelshift_r(raw[off / 4], raw[off / 4 + 1], 8 * (off % 4)) & 0xFFFFu;
+                    uint32_t lo[4], hi[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int qo = off + 2 + 4 * i;
+                        const uint32_t q = __funnelshift_r(raw[qo / 4], raw[qo / 4 + 1], 8 * (qo % 4));
+                        lo[i] = q & 0x0F0F0F0Fu;
+                        hi[i] = (q >> 4) & 0x0F0F0F0Fu;
+                    }
+                    const uint32_t m8 = 0x64086408u;  // (1032, 1032): 1024 + n - 1032 = n - 8
+                    uint8_t* A = smem + OFF_OPA + os * OP_A;
+#pragma unroll
+                    for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7
+                        const uint32_t w0 = kq < 2 ? lo[2 * kq] : hi[2 * (kq - 2)];
+                        const uint32_t w1 = kq < 2 ? lo[2 * kq + 1] : hi[2 * (kq - 2) + 1];
+                        uint4 v;
+                        v.x = h2_sub(bytes_to_h2(w0, 0x5140), m8);
+                        v.y = h2_sub(bytes_to_h2(w0, 0x7362), m8);
+                        v.z = h2_sub(bytes_to_h2(w1, 0x5140), m8);
+                        v.w = h2_sub(bytes_to_h2(w1, 0x7362), m8);
+                        *reinterpret_cast<uint4*>(A + op_off(r, kq)) = v;
+                    }
+                    reinterpret_cast<float*>(smem + OFF_SCW)[ss * BM + r] = h2f(dbits);
+                    fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.op_full(os));
+                }
+            } else {
+                // this token's 8 blocks: 272 bytes, 16-byte aligned, read as two windows of
+                // 144 bytes (bytes 0..143 hold blocks 0-3, bytes 128..271 hold blocks 4-7)
+                const uint8_t* row = smem + OFF_RAW + s * RAW_BYTES + W_RAW + r * (KB * 34);
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    uint32_t raw[36];
+                    const uint4* src = reinterpret_cast<const uint4*>(row + 128 * h);
+#pragma unroll
+                    for (int i = 0; i < 9; i++) {
+                        const uint4 v = src[i];
+                        raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
+                    }
+                    if (h == 1) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.raw_empty(s));
+                    }
+#pragma unroll
+                    for (int lq = 0; lq < KB / 2; lq++) {
+                        const int lb = 4 * h + lq;
+                        const int b = c * KB + lb, os = b % OP_SLOTS, ss = b % SC_SLOTS;
+                        if (b >= OP_SLOTS && !wait_or_abort(bars.op_empty(os), ((b / OP_SLOTS) - 1) & 1, abort_flag))
+                            break;
+                        if (b >= SC_SLOTS && !wait_or_abort(bars.sc_empty(ss), ((b / SC_SLOTS) - 1) & 1, abort_flag))
+                            break;
+                        // block lb: f16 d at byte 34*lb, 32 int8 codes at 34*lb + 2 (window-relative)
+                        const int off = 34 * lb - 128 * h;
+                        const uint32_t dbits =
+                            __funnelshift_r(raw[off / 4], raw[off / 4 + 1], 8 * (off % 4)) & 0xFFFFu;
+                        const uint32_t m128 = 0x64806480u;  // (1152, 1152): 1024 + (a + 128) - 1152 = a
+                        uint8_t* Bop = smem + OFF_OPB + os * OP_B;
+#pragma unroll
+                        for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7: code words 2kq, 2kq+1
+                            const int q0 = off + 2 + 8 * kq, q1 = q0 + 4;
+                            const uint32_t w0 =
+                                __funnelshift_r(raw[q0 / 4], raw[q0 / 4 + 1], 8 * (q0 % 4)) ^ 0x80808080u;
+                            const uint32_t w1 =
+                                __funnelshift_r(raw[q1 / 4], raw[q1 / 4 + 1], 8 * (q1 % 4)) ^ 0x80808080u;
+                            uint4 v;
+                            v.x = h2_sub(bytes_to_h2(w0, 0x5140), m128);
+                            v.y = h2_sub(bytes_to_h2(w0, 0x7362), m128);
+                            v.z = h2_sub(bytes_to_h2(w1, 0x5140), m128);
+                            v.w = h2_sub(bytes_to_h2(w1, 0x7362), m128);
+                            *reinterpret_cast<uint4*>(Bop + op_off(r, kq)) = v;
+                        }
+                        reinterpret_cast<float*>(smem + OFF_SCX)[ss * BN + r] = h2f(dbits);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.op_full(os));
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - (2 + NUM_CONV_WARPS);  // 0..15
+        const int quad = warp & 3;                    // TMEM lane quadrant this warp may access
+        const int cg = e >> 2;                        // which 32 columns (tokens)
+        const int row = quad * 32 + lane;             // weight row within the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        uint64_t acc[16];  // running sums of tokens 2j, 2j+1 as packed f32 pairs
+#pragma unroll
+        for (int j = 0; j < 16; j++) acc[j] = 0;
+        for (int b = 0; b < nb; b++) {
+            const int ac = b % NACC, ss = b % SC_SLOTS;
+            if (!wait_or_abort(bars.acc_full(ac), (b / NACC) & 1, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t dwb = __float_as_uint(scw[ss * BM + row]);
+            const uint64_t dw2 = f2_pack(dwb, dwb);
+            const uint64_t* dxs = reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                uint32_t v[16];
+                tmem_ld16(lane_base + (uint32_t)(ac * BN + cg * 32 + 16 * h), v);
+                tmem_ld_wait();
+                if (h == 1) {  // the block's sums are in registers: the accumulator may be reused
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.acc_empty(ac));
+                }
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const uint64_t sc = f2_mul(dw2, dxs[8 * h + j]);  // (d_w*d_x[t], d_w*d_x[t+1])
+                    acc[8 * h + j] = f2_fma(f2_pack(v[2 * j], v[2 * j + 1]), sc, acc[8 * h + j]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.sc_empty(ss));
+        }
+        if (pdl) pdl_wait();  // Y may be read or written by the previous kernel
+        const int o = o0 + row;
+        if (!*abort_flag && o < N) {
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                const int t = t0 + cg * 32 + j;
+                const uint32_t bits = (j & 1) ? (uint32_t)(acc[j >> 1] >> 32) : (uint32_t)acc[j >> 1];
+                if (t < M) Y[(size_t)t * N + o] = __uint_as_float(bits);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace mm
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A 2-D map over `rows` rows of `row_bytes` bytes, viewed as 16-bit elements,
+// with boxes of `box_bytes` x 128 rows; rows beyond the end read as zeros.
+static bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {row_bytes / 2, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_bytes / 2, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor-core path needs 16-byte row strides (K a multiple of 256) and
+// enough tokens to fill a tile reasonably; other shapes run one matvec per token.
+static bool tensor_core_shape(int64_t M, int64_t K) { return K % 256 == 0 && M >= 8; }
+
 qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                               cudaStream_t stream, bool pdl) {
-    const size_t xrb = row_bytes_of(QMM_Q8_0, K);
-    for (int64_t t = 0; t < M; t++) {
-        qmm_status st = matvec_dispatch(QMM_Q4_0, W, (const uint8_t*)xq + t * xrb, Y + t * N, N, K, stream, pdl);
-        if (st != QMM_OK) return st;
+    if (!tensor_core_shape(M, K)) {
+        const size_t xrb = row_bytes_of(QMM_Q8_0, K);
+        for (int64_t t = 0; t < M; t++) {
+            qmm_status st = matvec_dispatch(QMM_Q4_0, W, (const uint8_t*)xq + t * xrb, Y + t * N, N, K, stream, pdl);
+            if (st != QMM_OK) return st;
+        }
+        return QMM_OK;
     }
-    return QMM_OK;
+    if ((N + mm::BM - 1) / mm::BM > 0x7FFFFFFF || (M + mm::BN - 1) / mm::BN > 65535) return QMM_E_SHAPE;
+    CUtensorMap wmap, xmap;
+    if (!make_map(&wmap, W, row_bytes_of(QMM_Q4_0, K), (uint64_t)N, mm::KB * 18) ||
+        !make_map(&xmap, xq, row_bytes_of(QMM_Q8_0, K), (uint64_t)M, mm::KB * 34))
+        return QMM_E_CUDA;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMM_E_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(mm::matmul_q4_0_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mm::SMEM_BYTES) != cudaSuccess)
+            return QMM_E_CUDA;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + mm::BN - 1) / mm::BN));
+    cfg.blockDim = dim3(mm::THREADS);
+    cfg.dynamicSmemBytes = mm::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, mm::matmul_q4_0_kernel, wmap, xmap, Y, (int)M, (int)N, (int)K, pdl ? 1 : 0);
+    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
 }  // namespace qmm
