@@ -51,6 +51,7 @@ constexpr int RAW_STAGES = 2;
 constexpr int OP_SLOTS = 4;        // converted blocks in flight
 constexpr int SC_SLOTS = 32;       // block scales in flight (outlive the operands)
 constexpr int NACC = 4;            // TMEM accumulators (4 x 128 columns = all 512)
+static_assert(OP_SLOTS == NACC, "one barrier tracks both an operand slot and its accumulator");
 constexpr int W_RAW = BM * KB * 18;   // 18432
 constexpr int X_RAW = BN * KB * 34;   // 34816
 constexpr int RAW_BYTES = W_RAW + X_RAW;
@@ -67,8 +68,8 @@ constexpr int OFF_OPB = OFF_OPA + OP_SLOTS * OP_A;              // 139264
 constexpr int OFF_SCW = OFF_OPB + OP_SLOTS * OP_B;              // 172032
 constexpr int OFF_SCX = OFF_SCW + SC_SLOTS * BM * 4;            // 176128
 constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;            // 180224
-// barriers: raw_full[2] raw_empty[2] op_full[4] op_empty[4] sc_empty[8] acc_full[4] acc_empty[4]
-constexpr int NBARS = 2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + 2 * NACC;
+// barriers: raw_full[2] raw_empty[2] op_full[4] mma_done[4] sc_empty[32] acc_empty[4]
+constexpr int NBARS = 2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + NACC;
 constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
 constexpr int SMEM_BYTES = OFF_TMEM + 16;
 
@@ -159,12 +160,13 @@ struct Bars {
     __device__ uint32_t raw_full(int i) const { return base + 8u * i; }
     __device__ uint32_t raw_empty(int i) const { return base + 8u * (RAW_STAGES + i); }
     __device__ uint32_t op_full(int i) const { return base + 8u * (2 * RAW_STAGES + i); }
-    __device__ uint32_t op_empty(int i) const { return base + 8u * (2 * RAW_STAGES + OP_SLOTS + i); }
+    // MMA of the block in slot i complete: its operands may be overwritten and its
+    // accumulator read (one tcgen05.commit serves both)
+    __device__ uint32_t mma_done(int i) const { return base + 8u * (2 * RAW_STAGES + OP_SLOTS + i); }
+    __device__ uint32_t op_empty(int i) const { return mma_done(i); }
+    __device__ uint32_t acc_full(int i) const { return mma_done(i); }
     __device__ uint32_t sc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + i); }
-    __device__ uint32_t acc_full(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + i); }
-    __device__ uint32_t acc_empty(int i) const {
-        return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + NACC + i);
-    }
+    __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + i); }
 };
 
 // wait with a time limit; on failure set the error word and the CTA's abort flag.
@@ -222,13 +224,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int i = 0; i < OP_SLOTS; i++) {
             mbar_init(bars.op_full(i), NUM_CONV_WARPS);
-            mbar_init(bars.op_empty(i), 1);
+            mbar_init(bars.mma_done(i), 1);
         }
         for (int i = 0; i < SC_SLOTS; i++) mbar_init(bars.sc_empty(i), NUM_EPI_WARPS);
-        for (int i = 0; i < NACC; i++) {
-            mbar_init(bars.acc_full(i), 1);
-            mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
-        }
+        for (int i = 0; i < NACC; i++) mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -274,8 +273,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d = tmem + (uint32_t)(ac * BN);
                 mma_f16(d, ad, bd, idesc, 0);                    // K 0..15: core matrices 0, 1
                 mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1);  // K 16..31: core matrices 2, 3
-                mma_commit(bars.op_empty(os));
-                mma_commit(bars.acc_full(ac));
+                mma_commit(bars.mma_done(os));
             }
         }
     } else if (warp < 2 + NUM_CONV_WARPS) {

@@ -29,13 +29,16 @@ static __device__ unsigned int g_matvec_error = 0;
 
 constexpr int kThreads = 256;  // blocksums kernel
 
+constexpr int kMaxWarps = 16;  // matvec CTA: up to 16 warps, each with its own ring
+
 struct MatvecPlan {
-    int nwc;              // consumer warps (16 or 8); one more warp produces
+    bool su;              // decode whole super-units (Q8_0 / Q4_0 with K % 256 == 0)
+    int nw;               // warps per CTA
     int lpr;              // lanes per row (power of two, 1..32)
-    int stage_rows;       // rows per stage (whole passes of 32 / lpr rows)
-    int nstages;          // stage buffers in the ring
-    uint32_t stage_bytes; // bytes per stage buffer (with slack for unaligned reads)
-    uint32_t act_bytes;   // shared bytes before the first stage (barriers, activation)
+    int item_rows;        // rows per item (whole passes of 32 / lpr rows)
+    int depth;            // slots in each warp's ring
+    uint32_t slot_bytes;  // bytes per slot (the item's 16-byte aligned superset)
+    uint32_t act_bytes;   // shared bytes before the first slot (barriers, activation)
     uint32_t smem;        // total dynamic shared memory
     int grid;
 };
@@ -73,125 +76,121 @@ __device__ __forceinline__ float unit_contrib(const SmemBytes& w, uint32_t o, co
     }
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+// Issues the bulk copy of item `it` (rows [r0, r1) of W, as their 16-byte
+// aligned superset, the last < 16 bytes of W excepted) into a slot.
+__device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t rb, uint64_t total_al, int r0, int r1,
+                                           uint8_t* slot, uint32_t bar, uint64_t pol) {
+    const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
+    uint64_t a1 = ((uint64_t)r1 * rb + 15ull) & ~15ull;
+    if (a1 > total_al) a1 = total_al;
+    const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
+    mbar_arrive_expect_tx(bar, bytes);
+    if (bytes) bulk_g2s(smem_u32(slot), W + a0, bytes, bar, pol);
 }
 
-// The decode matvec: a warp-specialized stream.  Each CTA owns an even share of
-// the rows, cut into stages of `stage_rows` rows.  One producer warp streams the
-// stages into a ring of `nstages` shared-memory buffers with 1-D bulk copies
-// (cp.async.bulk completing on the stage's "full" mbarrier, evict-first in L2);
-// the copies cover the 16-byte aligned superset of each stage's rows, so no
-// block layout needs to be aligned.  NWC consumer warps take the rows of each
-// stage in passes of 32 / lpr rows (`lpr` lanes per row), decode whole blocks
-// from shared memory, take the exact integer block dots with __dp4a, fold each
-// into fp32 once per block and reduce with shuffles in a fixed order; each
-// consumer warp then arrives on the stage's "empty" mbarrier, and the producer
-// refills the buffer once all have.  No CTA-wide barrier sits in the loop, and
-// every y[o] is written by one lane, identically on every run ([minfer] s3.3:
-// row ownership, no split reduction).
+// The decode matvec.  Each CTA owns an even share of the rows, cut into items
+// of `item_rows` rows (whole passes of 32 / lpr rows).  Warp w of the CTA takes
+// items w, w + nw, w + 2nw, ... and streams them through its own ring of
+// `depth` shared-memory slots with 1-D bulk copies (cp.async.bulk completing
+// on the slot's mbarrier, evict-first in L2).  A warp refills a slot as soon as
+// it has decoded it, so no warp waits for another and no CTA-wide barrier sits
+// in the stream.  Lanes take the units of a row (a block, a super-block or,
+// with SU, a super-unit of 8 blocks) in steps of `lpr`, decode them from shared
+// memory, take the exact integer block dots with dp4a, fold each into fp32 once
+// per block and reduce with shuffles in a fixed order; every y[o] is written by
+// one lane, identically on every run ([minfer] "10 . CPU matmul: quantized
+// weights x Q8_0 activations" s3.3: row ownership, no split reduction).
 //
 // With pdl set the kernel is one link of a programmatic-dependent-launch chain:
-// it lets its successor launch at once, streams its own weights (which nothing
-// writes) right away, and waits for its predecessor's grid before it reads the
-// activation or writes y.
-template <int WT, int NWC>
-__global__ void __launch_bounds__((NWC + 1) * 32, 1) matvec_kernel(const uint8_t* __restrict__ W,
-                                                                const uint8_t* __restrict__ xq, float* __restrict__ y,
-                                                                int N, int K, int lpr, int stage_rows, int nstages,
-                                                                uint32_t stage_bytes, uint32_t act_bytes, int pdl) {
+// it lets its successor launch at once and streams the first item of each warp
+// (the weights, which nothing writes) before it waits for its predecessor's
+// grid; only then does it read the activation, issue the remaining copies and
+// write y.  Few copies are in flight while the activation is read, so its
+// loads are not queued behind the whole weight stream.
+template <int WT, bool SU>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t* __restrict__ W,
+                                                                  const uint8_t* __restrict__ xq, float* __restrict__ y,
+                                                                  int N, int K, int lpr, int item_rows, int depth,
+                                                                  uint32_t slot_bytes, uint32_t act_bytes, int pdl) {
     using F = Fmt<WT>;
     if (pdl) pdl_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem[];
-    // [0, 16*nstages): full and empty mbarriers | activation | stage buffers
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + nstages;
-    const uint32_t bar_bytes = align_up(16u * nstages, 128u);
-    uint8_t* aq = smem + bar_bytes;
-    const int nd = F::ACT == QMM_Q8_0 ? K / 32 : K / 256;
-    float* ad = reinterpret_cast<float*>(aq + K);
-    int* as = reinterpret_cast<int*>(ad + nd);
-    uint8_t* stages = smem + act_bytes;
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nw = blockDim.x >> 5;
+    // [barriers: nw * depth][activation][slots: nw * depth * slot_bytes]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem) + warp * depth;
+    uint8_t* aq = smem + align_up(8u * nw * depth, 128u);
+    const int nd = F::ACT == QMM_Q8_0 ? K / 32 : K / 256;
+    const int nsu = K / 256;
+    const int qbytes = SU ? (WT == QMM_Q4_0 ? 288 * nsu : 272 * nsu) : K;
+    float* ad = reinterpret_cast<float*>(aq + qbytes);
+    int* as = reinterpret_cast<int*>(ad + nd);
+    uint8_t* slots = smem + act_bytes + (size_t)warp * depth * slot_bytes;
+
     const int units = K / F::BV;
     const uint64_t rb = (uint64_t)units * F::BB;
     const int r_begin = (int)(((int64_t)N * blockIdx.x) / gridDim.x);
     const int r_end = (int)(((int64_t)N * (blockIdx.x + 1)) / gridDim.x);
-    const int nst = (r_end - r_begin + stage_rows - 1) / stage_rows;
+    const int nitems = (r_end - r_begin + item_rows - 1) / item_rows;
+    const int my_items = nitems > warp ? (nitems - warp + nw - 1) / nw : 0;
     const uint64_t total = (uint64_t)N * rb;
     const uint64_t total_al = total & ~15ull;
 
-    if (tid == 0) {
-        for (int i = 0; i < nstages; i++) {
-            mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), NWC);
-        }
+    uint64_t pol = 0;
+    if (lane == 0) {
+        for (int i = 0; i < depth; i++) mbar_init(smem_u32(&full[i]), 1);
         fence_mbar_init();
-    }
-    __syncthreads();
-
-    if (warp == NWC) {  // ------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            for (int s = 0; s < nst; s++) {
-                const int buf = s % nstages;
-                if (s >= nstages &&
-                    !mbar_wait_bounded(smem_u32(&empty[buf]), (uint32_t)((s / nstages) - 1) & 1u, kWaitLimitNs)) {
-                    atomicOr(&g_matvec_error, kErrTimeout);
-                    break;
-                }
-                const int r0 = r_begin + s * stage_rows;
-                const int r1 = min(r0 + stage_rows, r_end);
-                const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
-                uint64_t a1 = ((uint64_t)r1 * rb + 15ull) & ~15ull;
-                if (a1 > total_al) a1 = total_al;
-                const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
-                const uint32_t bar = smem_u32(&full[buf]);
-                mbar_arrive_expect_tx(bar, bytes);
-                if (bytes) bulk_g2s(smem_u32(stages + (size_t)buf * stage_bytes), W + a0, bytes, bar, pol);
-            }
+        pol = policy_evict_first();
+        if (my_items > 0) {
+            const int r0 = r_begin + warp * item_rows;
+            issue_item(W, rb, total_al, r0, min(r0 + item_rows, r_end), slots, smem_u32(&full[0]), pol);
         }
-        return;
     }
+    __syncwarp();
 
-    // ---------------------------------------------------------------- consumers
     if (pdl) pdl_wait();  // the activation row comes from the previous kernel
     {
-        // unpack with the consumer warps only (the producer has left)
-        const int nthr = NWC * 32;
-        if constexpr (F::ACT == QMM_Q8_0) {
+        const int nthr = blockDim.x;
+        if constexpr (SU) {
+            if constexpr (WT == QMM_Q8_0) {
+                for (int i = tid; i < nsu * 17; i += nthr) su_prep_q8_0_chunk(xq, nsu, i, aq);
+                for (int b = tid; b < nd; b += nthr) su_prep_block<false>(xq, nsu, b, aq, ad, as);
+            } else {
+                for (int b = tid; b < nd; b += nthr) su_prep_block<true>(xq, nsu, b, aq, ad, as);
+            }
+        } else if constexpr (F::ACT == QMM_Q8_0) {
             for (int b = tid; b < nd; b += nthr) unpack_q8_0_block(xq, K, b, aq, ad, as);
         } else {
             for (int i = tid; i < nd * 73; i += nthr) unpack_q8_K_word(xq, nd, i, aq, ad, as);
         }
-        consumer_sync(nthr);
+        __syncthreads();
     }
+    if (lane == 0) {
+        for (int k = 1; k < depth && k < my_items; k++) {
+            const int r0 = r_begin + (warp + k * nw) * item_rows;
+            issue_item(W, rb, total_al, r0, min(r0 + item_rows, r_end), slots + (size_t)k * slot_bytes,
+                       smem_u32(&full[k]), pol);
+        }
+    }
+
     const ActView act{aq, ad, as, nd};
     const int rows_per_pass = 32 / lpr;
     const int rsub = lane / lpr, li = lane % lpr;
-    for (int s = 0; s < nst; s++) {
-        const int buf = s % nstages;
-        const bool ok = mbar_wait_bounded(smem_u32(&full[buf]), (uint32_t)(s / nstages) & 1u, kWaitLimitNs);
+    for (int k = 0; k < my_items; k++) {
+        const int slot = k % depth;
+        const bool ok = mbar_wait_bounded(smem_u32(&full[slot]), (uint32_t)(k / depth) & 1u, kWaitLimitNs);
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane == 0) atomicOr(&g_matvec_error, kErrTimeout);
             return;
         }
-        const int r0 = r_begin + s * stage_rows;
-        const int r1 = min(r0 + stage_rows, r_end);
+        const int r0 = r_begin + (warp + k * nw) * item_rows;
+        const int r1 = min(r0 + item_rows, r_end);
         const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
-        uint8_t* sbuf = stages + (size_t)buf * stage_bytes;
+        uint8_t* sbuf = slots + (size_t)slot * slot_bytes;
         const SmemBytes wv{sbuf};
-        // passes of this stage go to warps round-robin, rotated by stage, so that
-        // with fewer passes than warps successive stages land on different warps
-        const int npass = (r1 - r0 + rows_per_pass - 1) / rows_per_pass;
-        const int rot = (int)(((int64_t)s * stage_rows / rows_per_pass) % NWC);
-        for (int p = (warp - rot + NWC) % NWC; p < npass; p += NWC) {
-            const int row = r0 + p * rows_per_pass + rsub;
-            if (row == N - 1 && (uint64_t)N * rb > total_al) {
+        for (int rr = r0; rr < r1; rr += rows_per_pass) {
+            const int row = rr + rsub;
+            if (row == N - 1 && total > total_al) {
                 // the last < 16 bytes of W lie in the last row: not reachable by a
                 // 16-byte bulk copy, so this warp fetches them itself
                 for (uint64_t i = total_al + li; i < total; i += lpr) sbuf[i - a0] = W[i];
@@ -200,14 +199,25 @@ __global__ void __launch_bounds__((NWC + 1) * 32, 1) matvec_kernel(const uint8_t
             float acc = 0.0f;
             if (row < r1) {
                 const uint32_t ro = (uint32_t)((uint64_t)row * rb - a0);
+                if constexpr (SU) {
+                    for (int u = li; u < nsu; u += lpr) {
+                        if constexpr (WT == QMM_Q8_0) acc += su_q8_0(sbuf + ro + 272u * u, aq, nsu, u, ad + 8 * u);
+                        else acc += su_q4_0(sbuf + ro + 144u * u, aq, nsu, u, ad + 8 * u, as + 8 * u);
+                    }
+                } else {
 #pragma unroll 4
-                for (int u = li; u < units; u += lpr) acc += unit_contrib<WT>(wv, ro + (uint32_t)(u * F::BB), act, u);
+                    for (int u = li; u < units; u += lpr)
+                        acc += unit_contrib<WT>(wv, ro + (uint32_t)(u * F::BB), act, u);
+                }
             }
             for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (row < r1 && li == 0) y[row] = acc;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[buf]));
+        if (lane == 0 && k + depth < my_items) {
+            const int q0 = r_begin + (warp + (k + depth) * nw) * item_rows;
+            issue_item(W, rb, total_al, q0, min(q0 + item_rows, r_end), sbuf, smem_u32(&full[slot]), pol);
+        }
     }
 }
 
@@ -281,59 +291,72 @@ qmm_status current_device(DeviceInfo* info) {
     return QMM_OK;
 }
 
-// Picks the launch shape for (format, N, K): lanes per row cover the row's
-// blocks (a pass = 32 / lpr rows); a stage is whole passes and about 32 KB (at
-// least one pass); 2-4 stages in flight; 16 consumer warps unless a pass is so
-// large that a stage must be smaller, then 8 or 4.
+// activation bytes in shared memory for a plan (without the barriers)
+__host__ inline uint32_t matvec_act_bytes(int wt, int act, int K, bool su) {
+    if (!su) return act_region_bytes(act, K);
+    const int nsu = K / 256, nd = K / 32;
+    return align_up((uint32_t)((wt == QMM_Q4_0 ? 288 : 272) * nsu + 8 * nd), 128u);
+}
+
+// Picks the launch shape for (format, N, K).  Lanes per row cover the row's
+// units (a pass = 32 / lpr rows); an item is one pass, or several when a pass
+// is under 2 KB.  Each warp keeps two items in flight when 12 or more warps fit
+// that way, else one item with 16 warps (more warps beat a deeper ring there).
+// One CTA per SM.
 template <int WT>
 static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, MatvecPlan* p) {
     using F = Fmt<WT>;
-    const int units = (int)(K / F::BV);
+    p->su = (WT == QMM_Q8_0 || WT == QMM_Q4_0) && K % 256 == 0;
+    const int nunit = p->su ? (int)(K / 256) : (int)(K / F::BV);
     int lpr = 1;
-    while (lpr < 32 && lpr < units) lpr <<= 1;
+    while (lpr < 32 && lpr < nunit) lpr <<= 1;
     p->lpr = lpr;
-    const uint64_t rb = (uint64_t)units * F::BB;
+    const uint64_t rb = (uint64_t)(K / F::BV) * F::BB;
     const int rpp = 32 / lpr;
     const uint64_t pass_bytes = (uint64_t)rpp * rb;
-    int npass = (int)((32u * 1024u) / pass_bytes);
+    int npass = (int)(4096u / pass_bytes);
     if (npass < 1) npass = 1;
-    p->stage_rows = npass * rpp;
-    const uint64_t sb = align_up((uint32_t)(npass * pass_bytes + 48), 128u);
+    p->item_rows = npass * rpp;
+    const uint64_t sb = align_up((uint32_t)(npass * pass_bytes + 32), 128u);
     if (sb > 0x7FFFFFFFull) return QMM_E_SHAPE;
-    p->stage_bytes = (uint32_t)sb;
-    const uint32_t act = act_region_bytes(F::ACT, (int)K);
-    const uint64_t total = (uint64_t)dev.max_smem_optin;
-    int ns = 0;
-    for (int cand = 4; cand >= 1; cand--) {
-        const uint64_t need = align_up(16u * cand, 128u) + act + (uint64_t)cand * p->stage_bytes;
-        if (need <= total) { ns = cand; break; }
+    p->slot_bytes = (uint32_t)sb;
+    const uint32_t act = matvec_act_bytes(WT, F::ACT, (int)K, p->su);
+    const uint32_t bar_max = align_up(8u * kMaxWarps * 2, 128u);
+    if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + sb) return QMM_E_SHAPE;
+    const uint64_t budget = (uint64_t)dev.max_smem_optin - bar_max - act;
+    int nw = (int)(budget / (2 * sb));
+    if (nw >= 12) {
+        p->depth = 2;
+    } else {
+        p->depth = 1;
+        nw = (int)(budget / sb);
     }
-    if (ns < 1) return QMM_E_SHAPE;
-    p->nstages = ns < 3 ? ns : 3;
-    p->nwc = pass_bytes > 16384 ? 8 : 16;
-    p->act_bytes = align_up(16u * p->nstages, 128u) + act;
-    p->smem = p->act_bytes + (uint32_t)p->nstages * p->stage_bytes;
+    if (nw > kMaxWarps) nw = kMaxWarps;
+    if (nw < 1) return QMM_E_SHAPE;
+    p->nw = nw;
+    p->act_bytes = align_up(8u * nw * p->depth, 128u) + act;
+    p->smem = p->act_bytes + (uint32_t)(nw * p->depth) * p->slot_bytes;
     int64_t grid = dev.sms;
-    const int64_t stages_total = (N + p->stage_rows - 1) / p->stage_rows;
-    if (grid > stages_total) grid = stages_total;
+    const int64_t items = (N + p->item_rows - 1) / p->item_rows;
+    if (grid > items) grid = items;
     if (grid < 1) grid = 1;
     p->grid = (int)grid;
     return QMM_OK;
 }
 
-template <int WT, int NWC>
-static qmm_status launch_matvec_nt(const void* W, const void* xq, float* y, int64_t N, int64_t K,
+template <int WT, bool SU>
+static qmm_status launch_matvec_su(const void* W, const void* xq, float* y, int64_t N, int64_t K,
                                    const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
     static bool attr_set[64] = {false};
     if (!attr_set[dev.device]) {
-        if (cudaFuncSetAttribute(matvec_kernel<WT, NWC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(matvec_kernel<WT, SU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dev.max_smem_optin) != cudaSuccess)
             return QMM_E_CUDA;
         attr_set[dev.device] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3((NWC + 1) * 32);
+    cfg.blockDim = dim3((unsigned)(p.nw * 32));
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -341,9 +364,9 @@ static qmm_status launch_matvec_nt(const void* W, const void* xq, float* y, int6
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, NWC>, (const uint8_t*)W, (const uint8_t*)xq, y,
-                                             (int)N, (int)K, p.lpr, p.stage_rows, p.nstages, p.stage_bytes,
-                                             p.act_bytes, pdl ? 1 : 0);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, SU>, (const uint8_t*)W, (const uint8_t*)xq, y,
+                                             (int)N, (int)K, p.lpr, p.item_rows, p.depth, p.slot_bytes, p.act_bytes,
+                                             pdl ? 1 : 0);
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
@@ -356,8 +379,10 @@ static qmm_status launch_matvec(const void* W, const void* xq, float* y, int64_t
     MatvecPlan p;
     st = plan_matvec<WT>(N, K, dev, &p);
     if (st != QMM_OK) return st;
-    if (p.nwc == 16) return launch_matvec_nt<WT, 16>(W, xq, y, N, K, p, dev, stream, pdl);
-    return launch_matvec_nt<WT, 8>(W, xq, y, N, K, p, dev, stream, pdl);
+    if constexpr (WT == QMM_Q8_0 || WT == QMM_Q4_0) {
+        if (p.su) return launch_matvec_su<WT, true>(W, xq, y, N, K, p, dev, stream, pdl);
+    }
+    return launch_matvec_su<WT, false>(W, xq, y, N, K, p, dev, stream, pdl);
 }
 
 // Public calls require 16-byte aligned bases; internal per-token calls pass rows

@@ -53,6 +53,12 @@ __device__ __forceinline__ float h2f(uint32_t bits) {
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a((int)a, (int)b, c);
 }
+// unsigned bytes of a times signed bytes of b, summed into c
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return (w >> (8 * k)) & 0xFFu; }
 
 // ---------------------------------------------------------------- mbarrier + bulk copy
@@ -79,11 +85,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// try_wait that lets the hardware suspend the thread (up to `hint_ns`) until the
+// phase completes, instead of returning at once: waiting warps stop competing
+// for issue slots with the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait: gives up after `limit_ns` of wall time and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;
@@ -372,6 +390,150 @@ __device__ __forceinline__ void unpack_q8_K_row(const uint8_t* __restrict__ row,
                                                 int* s) {
     const int ns = K / 256;
     for (int i = threadIdx.x; i < ns * 73; i += blockDim.x) unpack_q8_K_word(row, ns, i, q, d, s);
+}
+
+// ---------------------------------------------------------------- super-units (Q8_0, Q4_0 weights)
+// Eight consecutive 32-value blocks form a "super-unit": 272 bytes for Q8_0
+// (17 chunks of 16 B), 144 bytes for Q4_0 (9 chunks).  When a row holds whole
+// super-units (K % 256 == 0) every super-unit starts on a 16-byte boundary, so
+// one lane can read its super-unit with aligned 16-byte loads and no byte
+// shuffling.  Each 4-byte word x of a super-unit holds codes of at most one
+// block, namely block (4x + 1) / 34 (Q8_0) or (4x + 1) / 18 (Q4_0): the two
+// f16 scale bytes sit between the codes of neighbouring blocks.  The activation
+// is laid out in the same byte positions with zeros where the weight has its
+// scale, so a word-by-word dp4a over the super-unit yields each block's exact
+// integer code dot, the scale bytes contributing nothing.
+//
+// Activation arrays (chunk-major so that lanes on consecutive super-units read
+// consecutive 16-byte words):
+//   Q8_0: chunk c of super-unit u at (c*nsu + u)*16: the activation row's own
+//         bytes [272u + 16c, +16) with the f16 d fields zeroed.
+//   Q4_0: two planes in the weight's byte layout: byte y = 18b + 2 + j of
+//         super-unit u holds activation code 32(8u+b) + j (plane 0, paired with
+//         the low nibble of weight byte j) or 32(8u+b) + 16 + j (plane 1, the
+//         high nibble) ([ggml] "ggml Q4_0 vec_dot Walkthrough" s2: byte j holds
+//         elements j and j+16); plane p, chunk c at ((9p + c)*nsu + u)*16.
+//   d[b]: f32 activation scale of block b; s[b]: int32 sum of its 32 codes.
+
+// Q8_0 activation item i of nsu*17 (one 16-byte chunk); row at least 2-byte aligned
+__device__ __forceinline__ void su_prep_q8_0_chunk(const uint8_t* __restrict__ row, int nsu, int i, uint8_t* q) {
+    const int u = i / 17, c = i - 17 * u;
+    const uint8_t* src = row + 272 * u + 16 * c;
+    uint32_t w[4];
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+    } else {
+        const unsigned short* p = reinterpret_cast<const unsigned short*>(src);
+#pragma unroll
+        for (int j = 0; j < 4; j++) w[j] = (uint32_t)p[2 * j] | ((uint32_t)p[2 * j + 1] << 16);
+    }
+    // zero the d field of every block b whose first byte 34b falls in this chunk
+#pragma unroll
+    for (int b = 0; b < 8; b++) {
+        const int pos = 34 * b - 16 * c;
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            if (pos >= 4 * j && pos < 4 * j + 4) w[j] &= (pos & 2) ? 0x0000FFFFu : 0xFFFF0000u;
+    }
+    *reinterpret_cast<uint4*>(q + ((size_t)c * nsu + u) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// block b of a Q8_0 activation row: its f32 scale and code sum; for Q4_0 also
+// scatters the codes into the two planes
+template <bool PLANES>
+__device__ __forceinline__ void su_prep_block(const uint8_t* __restrict__ row, int nsu, int b, uint8_t* q, float* d,
+                                              int* s) {
+    const unsigned short* p = reinterpret_cast<const unsigned short*>(row + 34 * b);
+    d[b] = h2f(p[0]);
+    uint32_t w[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        w[i] = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
+        sum = dp4a(w[i], 0x01010101u, sum);
+    }
+    s[b] = sum;
+    if constexpr (PLANES) {
+        const int u = b >> 3, bb = b & 7;
+#pragma unroll
+        for (int pl = 0; pl < 2; pl++) {
+            const int y0 = 18 * bb;  // the weight's d field: zero in both planes
+            *reinterpret_cast<unsigned short*>(q + ((size_t)(9 * pl + y0 / 16) * nsu + u) * 16 + (y0 & 15)) = 0;
+#pragma unroll
+            for (int h = 0; h < 8; h++) {
+                const int y = 18 * bb + 2 + 2 * h;  // even, so the pair never straddles a chunk
+                const int code = 16 * pl + 2 * h;
+                const uint32_t pair = (w[code >> 2] >> (16 * ((code >> 1) & 1))) & 0xFFFFu;
+                *reinterpret_cast<unsigned short*>(q + ((size_t)(9 * pl + y / 16) * nsu + u) * 16 + (y & 15)) =
+                    (unsigned short)pair;
+            }
+        }
+    }
+}
+
+// The f32 fold of one super-unit: for each of its 8 blocks, isum * d_w * d_x
+// added in block order ([minfer] "10 . CPU matmul: quantized weights x Q8_0
+// activations" s3.2, the Q8_0 kernel).  w: the super-unit in shared memory
+// (16-byte aligned); q: the activation array; d: the 8 activation scales.
+__device__ __forceinline__ float su_q8_0(const uint8_t* w, const uint8_t* q, int nsu, int u, const float* d) {
+    int s[8];
+    uint32_t dw[8];
+#pragma unroll
+    for (int b = 0; b < 8; b++) s[b] = 0;
+#pragma unroll
+    for (int c = 0; c < 17; c++) {
+        const uint4 wc = *reinterpret_cast<const uint4*>(w + 16 * c);
+        const uint4 ac = *reinterpret_cast<const uint4*>(q + ((size_t)c * nsu + u) * 16);
+        const uint32_t ww[4] = {wc.x, wc.y, wc.z, wc.w}, aa[4] = {ac.x, ac.y, ac.z, ac.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int x = 4 * c + j;
+            s[(4 * x + 1) / 34] = dp4a(ww[j], aa[j], s[(4 * x + 1) / 34]);
+#pragma unroll
+            for (int b = 0; b < 8; b++)
+                if ((34 * b) / 4 == x) dw[b] = ((34 * b) % 4 == 0) ? (ww[j] & 0xFFFFu) : (ww[j] >> 16);
+        }
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 8; b++) acc += (float)s[b] * h2f(dw[b]) * d[b];
+    return acc;
+}
+
+// Q4_0: isum_b = sum n_lo*a_lo + sum n_hi*a_hi - 8*sum(a) ([ggml] s2).  The
+// high nibbles are taken in place (byte & 0xF0 = 16 n) with an unsigned x
+// signed dp4a; the block's sum is a multiple of 16, divided out exactly.
+__device__ __forceinline__ float su_q4_0(const uint8_t* w, const uint8_t* q, int nsu, int u, const float* d,
+                                         const int* asum) {
+    int s[8], t[8];
+    uint32_t dw[8];
+#pragma unroll
+    for (int b = 0; b < 8; b++) s[b] = 0, t[b] = 0;
+#pragma unroll
+    for (int c = 0; c < 9; c++) {
+        const uint4 wc = *reinterpret_cast<const uint4*>(w + 16 * c);
+        const uint4 lo = *reinterpret_cast<const uint4*>(q + ((size_t)c * nsu + u) * 16);
+        const uint4 hi = *reinterpret_cast<const uint4*>(q + ((size_t)(9 + c) * nsu + u) * 16);
+        const uint32_t ww[4] = {wc.x, wc.y, wc.z, wc.w}, al[4] = {lo.x, lo.y, lo.z, lo.w},
+                       ah[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int x = 4 * c + j, b = (4 * x + 1) / 18;
+            s[b] = dp4a(ww[j] & 0x0F0F0F0Fu, al[j], s[b]);
+            t[b] = dp4a_us(ww[j] & 0xF0F0F0F0u, ah[j], t[b]);
+#pragma unroll
+            for (int bb = 0; bb < 8; bb++)
+                if ((18 * bb) / 4 == x) dw[bb] = ((18 * bb) % 4 == 0) ? (ww[j] & 0xFFFFu) : (ww[j] >> 16);
+        }
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 8; b++) {
+        const int isum = s[b] + (t[b] >> 4) - 8 * asum[b];
+        acc += (float)isum * h2f(dw[b]) * d[b];
+    }
+    return acc;
 }
 
 }  // namespace qmm
