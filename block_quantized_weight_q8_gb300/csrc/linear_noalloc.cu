@@ -20,6 +20,8 @@ namespace qmm {
 qmm_status quantize_act_launch(int act, const float* x, void* xq, int64_t M, int64_t K, cudaStream_t stream, bool pdl);
 qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
                            bool pdl);
+qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq_out, float* y, int64_t N, int64_t K,
+                                 cudaStream_t stream, bool pdl);
 qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                               cudaStream_t stream, bool pdl);
 
@@ -73,10 +75,21 @@ qmm_status qmm_linear_noalloc(int wtype, const void* W, const float* x, float* y
         if (st != QMM_OK) return st;
         return matmul_q4_0_launch(W, scratch, y, M, N, K, cs, true);
     }
-    st = quantize_act_launch(act, x, scratch, M, K, cs, M == 1);
+    // one launch per token that quantizes its row and multiplies; a row too
+    // large for that kernel's shared memory is quantized by its own kernel first
+    st = matvec_fused_dispatch(wtype, W, x, scratch, y, N, K, cs, true);
+    if (st == QMM_OK) {
+        for (int64_t t = 1; t < M; t++) {
+            st = matvec_fused_dispatch(wtype, W, x + t * K, (uint8_t*)scratch + t * xrb, y + t * N, N, K, cs, true);
+            if (st != QMM_OK) return st;
+        }
+        return QMM_OK;
+    }
+    if (st != QMM_E_SHAPE) return st;
+    st = quantize_act_launch(act, x, scratch, M, K, cs, true);
     if (st != QMM_OK) return st;
     for (int64_t t = 0; t < M; t++) {
-        st = matvec_dispatch(wtype, W, (const uint8_t*)scratch + t * xrb, y + t * N, N, K, cs, M == 1);
+        st = matvec_dispatch(wtype, W, (const uint8_t*)scratch + t * xrb, y + t * N, N, K, cs, true);
         if (st != QMM_OK) return st;
     }
     return QMM_OK;

@@ -527,7 +527,7 @@ qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, i
     qmm_status st = check_shape(QMM_Q4_0, M, N, K);
     if (st != QMM_OK) return st;
     if (!aligned16(W) || !aligned16(xq) || !aligned16(Y)) return QMM_E_ALIGN;
-    return matmul_q4_0_launch(W, xq, Y, M, N, K, (cudaStream_t)stream, false);
+    return matmul_q4_0_launch(W, xq, Y, M, N, K, (cudaStream_t)stream, true);
 }
 
 unsigned qmm_internal_matmul_error(int clear) {

@@ -107,11 +107,19 @@ __device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t rb, uint64
 // grid; only then does it read the activation, issue the remaining copies and
 // write y.  Few copies are in flight while the activation is read, so its
 // loads are not queued behind the whole weight stream.
-template <int WT, bool SU>
+//
+// With FUSE the kernel takes the f32 activation row x instead of xq and
+// quantizes it itself (every CTA, into shared memory, with the same per-block
+// arithmetic as the standalone quantizer, so the codes are the same bytes);
+// CTA 0 also stores the quantized row to xq_out when that is not null.  One
+// launch then does the whole quantize + multiply of a decode token.
+template <int WT, bool SU, bool FUSE>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t* __restrict__ W,
-                                                                  const uint8_t* __restrict__ xq, float* __restrict__ y,
-                                                                  int N, int K, int lpr, int item_rows, int depth,
-                                                                  uint32_t slot_bytes, uint32_t act_bytes, int pdl) {
+                                                                  const uint8_t* __restrict__ xq,
+                                                                  const float* __restrict__ x, uint8_t* xq_out,
+                                                                  float* __restrict__ y, int N, int K, int lpr,
+                                                                  int item_rows, int depth, uint32_t slot_bytes,
+                                                                  uint32_t act_bytes, int pdl) {
     using F = Fmt<WT>;
     if (pdl) pdl_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem[];
@@ -125,6 +133,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
     const int qbytes = SU ? (WT == QMM_Q4_0 ? 288 * nsu : 272 * nsu) : K;
     float* ad = reinterpret_cast<float*>(aq + qbytes);
     int* as = reinterpret_cast<int*>(ad + nd);
+    uint8_t* xs = reinterpret_cast<uint8_t*>(as + (SU ? nd : (F::ACT == QMM_Q8_0 ? nd : K / 16)));
+    xs = reinterpret_cast<uint8_t*>(((uintptr_t)xs + 15u) & ~(uintptr_t)15u);  // FUSE: the quantized row
     uint8_t* slots = smem + act_bytes + (size_t)warp * depth * slot_bytes;
 
     const int units = K / F::BV;
@@ -151,6 +161,45 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
     if (pdl) pdl_wait();  // the activation row comes from the previous kernel
     {
         const int nthr = blockDim.x;
+        if constexpr (FUSE) {
+            // x is read in rounds of four 16-byte loads per thread, all issued
+            // before any is used, so a row of up to 4 * 16 * blockDim bytes costs
+            // one memory round trip
+            const float4* x4 = reinterpret_cast<const float4*>(x);
+            if constexpr (F::ACT == QMM_Q8_0) {
+                const int items = (K / 32) * 8;
+                for (int base = warp * 32; base < items; base += 4 * nthr) {
+                    float4 v[4];
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const int gt = base + r * nthr + lane;
+                        v[r] = gt < items ? x4[gt] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const int gt = base + r * nthr + lane;
+                        const bool active = gt < items;
+                        quant_q8_0_part(v[r], active, gt & 7, xs + (active ? (gt >> 3) * 34 : 0));
+                    }
+                }
+            } else {
+                for (int b0 = warp; b0 < nd; b0 += 2 * nw) {
+                    const int b1 = b0 + nw;
+                    const float4 v0 = x4[b0 * 64 + 2 * lane], v1 = x4[b0 * 64 + 2 * lane + 1];
+                    float4 v2 = make_float4(0.f, 0.f, 0.f, 0.f), v3 = v2;
+                    if (b1 < nd) v2 = x4[b1 * 64 + 2 * lane], v3 = x4[b1 * 64 + 2 * lane + 1];
+                    quant_q8_K_lane(v0, v1, lane, xs + b0 * 292);
+                    if (b1 < nd) quant_q8_K_lane(v2, v3, lane, xs + b1 * 292);
+                }
+            }
+            __syncthreads();
+            if (blockIdx.x == 0 && xq_out != nullptr) {
+                const int halves = (F::ACT == QMM_Q8_0 ? (K / 32) * 34 : (K / 256) * 292) / 2;
+                for (int i = tid; i < halves; i += nthr)
+                    reinterpret_cast<unsigned short*>(xq_out)[i] = reinterpret_cast<const unsigned short*>(xs)[i];
+            }
+            xq = xs;
+        }
         if constexpr (SU) {
             if constexpr (WT == QMM_Q8_0) {
                 for (int i = tid; i < nsu * 17; i += nthr) su_prep_q8_0_chunk(xq, nsu, i, aq);
@@ -304,7 +353,7 @@ __host__ inline uint32_t matvec_act_bytes(int wt, int act, int K, bool su) {
 // that way, else one item with 16 warps (more warps beat a deeper ring there).
 // One CTA per SM.
 template <int WT>
-static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, MatvecPlan* p) {
+static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, bool fuse, MatvecPlan* p) {
     using F = Fmt<WT>;
     p->su = (WT == QMM_Q8_0 || WT == QMM_Q4_0) && K % 256 == 0;
     const int nunit = p->su ? (int)(K / 256) : (int)(K / F::BV);
@@ -320,7 +369,8 @@ static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, Matve
     const uint64_t sb = align_up((uint32_t)(npass * pass_bytes + 32), 128u);
     if (sb > 0x7FFFFFFFull) return QMM_E_SHAPE;
     p->slot_bytes = (uint32_t)sb;
-    const uint32_t act = matvec_act_bytes(WT, F::ACT, (int)K, p->su);
+    uint32_t act = matvec_act_bytes(WT, F::ACT, (int)K, p->su);
+    if (fuse) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);  // the quantized row
     const uint32_t bar_max = align_up(8u * kMaxWarps * 2, 128u);
     if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + sb) return QMM_E_SHAPE;
     const uint64_t budget = (uint64_t)dev.max_smem_optin - bar_max - act;
@@ -344,12 +394,13 @@ static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, Matve
     return QMM_OK;
 }
 
-template <int WT, bool SU>
-static qmm_status launch_matvec_su(const void* W, const void* xq, float* y, int64_t N, int64_t K,
-                                   const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
+template <int WT, bool SU, bool FUSE>
+static qmm_status launch_matvec_su(const void* W, const void* xq, const float* x, void* xq_out, float* y, int64_t N,
+                                   int64_t K, const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream,
+                                   bool pdl) {
     static bool attr_set[64] = {false};
     if (!attr_set[dev.device]) {
-        if (cudaFuncSetAttribute(matvec_kernel<WT, SU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(matvec_kernel<WT, SU, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dev.max_smem_optin) != cudaSuccess)
             return QMM_E_CUDA;
         attr_set[dev.device] = true;
@@ -364,50 +415,69 @@ static qmm_status launch_matvec_su(const void* W, const void* xq, float* y, int6
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, SU>, (const uint8_t*)W, (const uint8_t*)xq, y,
-                                             (int)N, (int)K, p.lpr, p.item_rows, p.depth, p.slot_bytes, p.act_bytes,
-                                             pdl ? 1 : 0);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, SU, FUSE>, (const uint8_t*)W,
+                                             (const uint8_t*)xq, x, (uint8_t*)xq_out, y, (int)N, (int)K, p.lpr,
+                                             p.item_rows, p.depth, p.slot_bytes, p.act_bytes, pdl ? 1 : 0);
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
+// x == nullptr: multiply the quantized row xq.  Otherwise quantize x in the
+// kernel (xq then names where CTA 0 stores the quantized row, or is null).
 template <int WT>
-static qmm_status launch_matvec(const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
-                                bool pdl) {
+static qmm_status launch_matvec(const void* W, const void* xq, const float* x, float* y, int64_t N, int64_t K,
+                                cudaStream_t stream, bool pdl) {
     DeviceInfo dev;
     qmm_status st = current_device(&dev);
     if (st != QMM_OK) return st;
     MatvecPlan p;
-    st = plan_matvec<WT>(N, K, dev, &p);
+    const bool fuse = x != nullptr;
+    st = plan_matvec<WT>(N, K, dev, fuse, &p);
     if (st != QMM_OK) return st;
-    if constexpr (WT == QMM_Q8_0 || WT == QMM_Q4_0) {
-        if (p.su) return launch_matvec_su<WT, true>(W, xq, y, N, K, p, dev, stream, pdl);
+    if (fuse) {
+        if constexpr (WT == QMM_Q8_0 || WT == QMM_Q4_0) {
+            if (p.su) return launch_matvec_su<WT, true, true>(W, nullptr, x, (void*)xq, y, N, K, p, dev, stream, pdl);
+        }
+        return launch_matvec_su<WT, false, true>(W, nullptr, x, (void*)xq, y, N, K, p, dev, stream, pdl);
     }
-    return launch_matvec_su<WT, false>(W, xq, y, N, K, p, dev, stream, pdl);
+    if constexpr (WT == QMM_Q8_0 || WT == QMM_Q4_0) {
+        if (p.su) return launch_matvec_su<WT, true, false>(W, xq, nullptr, nullptr, y, N, K, p, dev, stream, pdl);
+    }
+    return launch_matvec_su<WT, false, false>(W, xq, nullptr, nullptr, y, N, K, p, dev, stream, pdl);
 }
 
 // Public calls require 16-byte aligned bases; internal per-token calls pass rows
 // of a larger buffer, which the kernel accepts at their natural alignment (W
-// 16 bytes for the bulk copies, an activation row 2 bytes, y 4 bytes).
-static qmm_status matvec_checked(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K,
-                                 cudaStream_t stream, bool pdl, bool public_call = true) {
-    if (!W || !xq || !y) return QMM_E_NULL;
+// 16 bytes for the bulk copies, an activation row 2 bytes, y 4 bytes; an f32
+// row x to quantize in the kernel 16 bytes).
+static qmm_status matvec_checked(int wt, const void* W, const void* xq, const float* x, float* y, int64_t N,
+                                 int64_t K, cudaStream_t stream, bool pdl, bool public_call) {
+    if (!W || (!xq && !x) || !y) return QMM_E_NULL;
     qmm_status st = check_shape(wt, 1, N, K);
     if (st != QMM_OK) return st;
     if (public_call && (!aligned16(W) || !aligned16(xq) || !aligned16(y))) return QMM_E_ALIGN;
-    if (!aligned16(W) || ((uintptr_t)xq & 1u) || ((uintptr_t)y & 3u)) return QMM_E_ALIGN;
+    if (!aligned16(W) || ((uintptr_t)xq & 1u) || ((uintptr_t)y & 3u) || !aligned16(x)) return QMM_E_ALIGN;
     switch (wt) {
-    case QMM_Q4_0: return launch_matvec<QMM_Q4_0>(W, xq, y, N, K, stream, pdl);
-    case QMM_Q8_0: return launch_matvec<QMM_Q8_0>(W, xq, y, N, K, stream, pdl);
-    case QMM_Q4_K: return launch_matvec<QMM_Q4_K>(W, xq, y, N, K, stream, pdl);
-    case QMM_Q6_K: return launch_matvec<QMM_Q6_K>(W, xq, y, N, K, stream, pdl);
-    case QMM_Q2_K: return launch_matvec<QMM_Q2_K>(W, xq, y, N, K, stream, pdl);
+    case QMM_Q4_0: return launch_matvec<QMM_Q4_0>(W, xq, x, y, N, K, stream, pdl);
+    case QMM_Q8_0: return launch_matvec<QMM_Q8_0>(W, xq, x, y, N, K, stream, pdl);
+    case QMM_Q4_K: return launch_matvec<QMM_Q4_K>(W, xq, x, y, N, K, stream, pdl);
+    case QMM_Q6_K: return launch_matvec<QMM_Q6_K>(W, xq, x, y, N, K, stream, pdl);
+    case QMM_Q2_K: return launch_matvec<QMM_Q2_K>(W, xq, x, y, N, K, stream, pdl);
     default: return QMM_E_TYPE;
     }
 }
 
 qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
                            bool pdl) {
-    return matvec_checked(wt, W, xq, y, N, K, stream, pdl, false);
+    return matvec_checked(wt, W, xq, nullptr, y, N, K, stream, pdl, false);
+}
+
+// Quantize one f32 row x and multiply, in one launch; the quantized row is also
+// stored to xq_out (when not null).  Fails with QMM_E_SHAPE when the row does not
+// fit the kernel's shared memory, so the caller can quantize separately instead.
+qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq_out, float* y, int64_t N, int64_t K,
+                                 cudaStream_t stream, bool pdl) {
+    if (!x) return QMM_E_NULL;
+    return matvec_checked(wt, W, xq_out, x, y, N, K, stream, pdl, false);
 }
 
 template <int WT>
@@ -441,19 +511,19 @@ using namespace qmm;
 extern "C" {
 
 qmm_status qmm_matvec_q4_0(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
-    return matvec_checked(QMM_Q4_0, W, xq, y, N, K, (cudaStream_t)stream, false);
+    return matvec_checked(QMM_Q4_0, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
 }
 qmm_status qmm_matvec_q8_0(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
-    return matvec_checked(QMM_Q8_0, W, xq, y, N, K, (cudaStream_t)stream, false);
+    return matvec_checked(QMM_Q8_0, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
 }
 qmm_status qmm_matvec_q4_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
-    return matvec_checked(QMM_Q4_K, W, xq, y, N, K, (cudaStream_t)stream, false);
+    return matvec_checked(QMM_Q4_K, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
 }
 qmm_status qmm_matvec_q6_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
-    return matvec_checked(QMM_Q6_K, W, xq, y, N, K, (cudaStream_t)stream, false);
+    return matvec_checked(QMM_Q6_K, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
 }
 qmm_status qmm_matvec_q2_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
-    return matvec_checked(QMM_Q2_K, W, xq, y, N, K, (cudaStream_t)stream, false);
+    return matvec_checked(QMM_Q2_K, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
 }
 
 qmm_status qmm_blocksums(int wtype, const void* W, const void* xq, int32_t* s, int64_t M, int64_t N, int64_t K,

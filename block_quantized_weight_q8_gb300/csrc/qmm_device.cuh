@@ -392,6 +392,75 @@ __device__ __forceinline__ void unpack_q8_K_row(const uint8_t* __restrict__ row,
     for (int i = threadIdx.x; i < ns * 73; i += blockDim.x) unpack_q8_K_word(row, ns, i, q, d, s);
 }
 
+// ---------------------------------------------------------------- activation quantizers
+// The per-block arithmetic of the Q8_0 / Q8_K activation quantizers, shared by
+// the standalone quantize kernels and the matvec kernels that quantize their
+// own input, so both write the same bytes.  Every float operation is an
+// explicitly IEEE-rounded intrinsic (no contraction), as the pages' scalar
+// definitions round each step once ([krafla] "Architecture", Numerics).
+__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+__device__ __forceinline__ uint32_t f2h_bits(float f) { return (uint32_t)__half_as_ushort(__float2half_rn(f)); }
+// 16-bit stores for every f16 field (a byte store of the low half of a
+// __float2half_rn result was seen to store 0 with this toolchain)
+__device__ __forceinline__ void st_u16(uint8_t* p, uint32_t v) {
+    *reinterpret_cast<unsigned short*>(p) = (unsigned short)(v & 0xFFFFu);
+}
+
+// Q8_0 ([minfer] "10 . CPU matmul: quantized weights x Q8_0 activations" s3.2):
+// per 32 values amax = max|x|, d = amax/127 stored as f16, inverse 127/amax (0
+// for an all-zero block), codes rne(x * inverse) saturated to int8.  Eight
+// consecutive lanes (part = lane & 7) hold a block, four values each; all 32
+// lanes of the warp call, inactive ones with active = false.  `ob` is the
+// block's 34 output bytes.
+__device__ __forceinline__ void quant_q8_0_part(float4 v, bool active, int part, uint8_t* ob) {
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    if (!active) return;
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = amax != 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    const int q0 = clampi(__float2int_rn(__fmul_rn(v.x, id)), -128, 127);
+    const int q1 = clampi(__float2int_rn(__fmul_rn(v.y, id)), -128, 127);
+    const int q2 = clampi(__float2int_rn(__fmul_rn(v.z, id)), -128, 127);
+    const int q3 = clampi(__float2int_rn(__fmul_rn(v.w, id)), -128, 127);
+    if (part == 0) st_u16(ob, f2h_bits(d));
+    st_u16(ob + 2 + 4 * part, (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8));
+    st_u16(ob + 4 + 4 * part, (uint32_t)(q2 & 0xFF) | ((uint32_t)(q3 & 0xFF) << 8));
+}
+
+// Q8_K ([minfer] s3.2, quantize_row_q8_k_buf): per 256 values amax, f32
+// d = amax/127, codes saturated to [-128, 127], bsums[g] = exact sum of the 16
+// saturated codes of group g.  One warp per super-block, eight values per lane
+// (v0, v1 = values 8*lane .. 8*lane+7): lanes 2g and 2g+1 hold group g.  `ob`
+// is the super-block's 292 output bytes (4-byte aligned).
+__device__ __forceinline__ void quant_q8_K_lane(float4 v0, float4 v1, int lane, uint8_t* ob) {
+    float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                       fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = amax != 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t w0 = 0, w1 = 0;
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int q = clampi(__float2int_rn(__fmul_rn(vv[i], id)), -128, 127);
+        sum += q;
+        if (i < 4) w0 |= (uint32_t)(q & 0xFF) << (8 * i);
+        else w1 |= (uint32_t)(q & 0xFF) << (8 * (i - 4));
+    }
+    const int bsum = sum + __shfl_xor_sync(0xffffffffu, sum, 1);   // group lane/2
+    const int bsum_next = __shfl_down_sync(0xffffffffu, bsum, 2);  // group lane/2 + 1
+    if (lane == 0) *reinterpret_cast<float*>(ob) = d;
+    *reinterpret_cast<uint32_t*>(ob + 4 + 8 * lane) = w0;
+    *reinterpret_cast<uint32_t*>(ob + 8 + 8 * lane) = w1;
+    if ((lane & 3) == 0)
+        *reinterpret_cast<uint32_t*>(ob + 260 + lane) =
+            ((uint32_t)bsum & 0xFFFFu) | ((uint32_t)(bsum_next & 0xFFFF) << 16);
+}
+
 // ---------------------------------------------------------------- super-units (Q8_0, Q4_0 weights)
 // Eight consecutive 32-value blocks form a "super-unit": 272 bytes for Q8_0
 // (17 chunks of 16 B), 144 bytes for Q4_0 (9 chunks).  When a row holds whole

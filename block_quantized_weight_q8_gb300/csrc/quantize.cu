@@ -13,12 +13,6 @@
 
 namespace qmm {
 
-__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
-__device__ __forceinline__ uint32_t f2h_bits(float f) { return (uint32_t)__half_as_ushort(__float2half_rn(f)); }
-__device__ __forceinline__ void st_u16(uint8_t* p, uint32_t v) {
-    *reinterpret_cast<unsigned short*>(p) = (unsigned short)(v & 0xFFFFu);
-}
-
 // ---------------------------------------------------------------- Q8_0 activations
 // [minfer] "10 . CPU matmul: quantized weights x Q8_0 activations" s3.2 (the
 // activation quantizers): per 32 values amax = max|x|, d = amax/127 stored as
@@ -36,24 +30,9 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __rest
     }
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t b = gt >> 3;
-    const int part = (int)(gt & 7);
     const bool active = b < nblocks;
-    const float4 v = active ? x[b * 8 + part] : make_float4(0.f, 0.f, 0.f, 0.f);
-    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    if (!active) return;
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float id = amax != 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-    const int q0 = clampi(__float2int_rn(__fmul_rn(v.x, id)), -128, 127);
-    const int q1 = clampi(__float2int_rn(__fmul_rn(v.y, id)), -128, 127);
-    const int q2 = clampi(__float2int_rn(__fmul_rn(v.z, id)), -128, 127);
-    const int q3 = clampi(__float2int_rn(__fmul_rn(v.w, id)), -128, 127);
-    uint8_t* ob = out + b * 34;
-    if (part == 0) st_u16(ob, f2h_bits(d));
-    st_u16(ob + 2 + 4 * part, (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8));
-    st_u16(ob + 4 + 4 * part, (uint32_t)(q2 & 0xFF) | ((uint32_t)(q3 & 0xFF) << 8));
+    const float4 v = active ? x[gt] : make_float4(0.f, 0.f, 0.f, 0.f);
+    quant_q8_0_part(v, active, (int)(gt & 7), out + (active ? b * 34 : 0));
 }
 
 // ---------------------------------------------------------------- Q8_K activations
@@ -70,32 +49,7 @@ __global__ void __launch_bounds__(256) quantize_q8_K_kernel(const float4* __rest
     const int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (b >= nblocks) return;  // whole warps leave together
-    const float4 v0 = x[b * 64 + 2 * lane], v1 = x[b * 64 + 2 * lane + 1];
-    float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
-                       fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float id = amax != 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t w0 = 0, w1 = 0;
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-        const int q = clampi(__float2int_rn(__fmul_rn(vv[i], id)), -128, 127);
-        sum += q;
-        if (i < 4) w0 |= (uint32_t)(q & 0xFF) << (8 * i);
-        else w1 |= (uint32_t)(q & 0xFF) << (8 * (i - 4));
-    }
-    const int bsum = sum + __shfl_xor_sync(0xffffffffu, sum, 1);   // group lane/2
-    const int bsum_next = __shfl_down_sync(0xffffffffu, bsum, 2);  // group lane/2 + 1
-    uint8_t* ob = out + b * 292;
-    if (lane == 0) *reinterpret_cast<float*>(ob) = d;
-    *reinterpret_cast<uint32_t*>(ob + 4 + 8 * lane) = w0;
-    *reinterpret_cast<uint32_t*>(ob + 8 + 8 * lane) = w1;
-    if ((lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(ob + 260 + lane) =
-            ((uint32_t)bsum & 0xFFFFu) | ((uint32_t)(bsum_next & 0xFFFF) << 16);
+    quant_q8_K_lane(x[b * 64 + 2 * lane], x[b * 64 + 2 * lane + 1], lane, out + b * 292);
 }
 
 // ---------------------------------------------------------------- Q4_0 weights

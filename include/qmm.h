@@ -22,6 +22,17 @@
  *             asynchronous call.  Nothing is allocated on any call.
  *   Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *             default stream).  Calls are asynchronous on it; none synchronizes.
+ *   Chaining. The matvec, linear and matmul kernels are launched as
+ *             programmatic dependent launches: each lets the next kernel on
+ *             the stream launch early, and may itself start streaming W before
+ *             the kernel ahead of it has finished (W is read-only to every
+ *             call).  Everything else it reads, and everything it writes, waits
+ *             for that kernel to complete.  A kernel that writes W therefore
+ *             must not both directly precede a multiply and release its
+ *             dependents early (griddepcontrol.launch_dependents); ordinary
+ *             kernels, and this library's weight and activation quantizers,
+ *             never release early, so a multiply right after them sees all of
+ *             W.
  *   Errors.   Every call returns a qmm_status.  Arguments are checked on the
  *             host before anything is launched; a failed check launches
  *             nothing.  A launch failure returns QMM_E_CUDA.  No call aborts,
