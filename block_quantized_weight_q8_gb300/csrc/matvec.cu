@@ -134,13 +134,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
     float* ad = reinterpret_cast<float*>(aq + qbytes);
     int* as = reinterpret_cast<int*>(ad + nd);
     uint8_t* xs = reinterpret_cast<uint8_t*>(as + (SU ? nd : (F::ACT == QMM_Q8_0 ? nd : K / 16)));
-    xs = reinterpret_cast<uint8_t*>(((uintptr_t)xs + 15u) & ~(uintptr_t)15u);  // FUSE: the quantized row
+    xs = reinterpret_cast<uint8_t*>(((uintptr_t)xs + 15u) & ~(uintptr_t)15u);  // FUSE, Q8_K: the quantized row
     uint8_t* slots = smem + act_bytes + (size_t)warp * depth * slot_bytes;
 
     const int units = K / F::BV;
     const uint64_t rb = (uint64_t)units * F::BB;
-    const int r_begin = (int)(((int64_t)N * blockIdx.x) / gridDim.x);
-    const int r_end = (int)(((int64_t)N * (blockIdx.x + 1)) / gridDim.x);
+    // an even split of the rows: the first N % grid CTAs take one row more
+    const int rq = N / (int)gridDim.x, rr = N - rq * (int)gridDim.x;
+    const int r_begin = (int)blockIdx.x * rq + min((int)blockIdx.x, rr);
+    const int r_end = r_begin + rq + ((int)blockIdx.x < rr ? 1 : 0);
     const int nitems = (r_end - r_begin + item_rows - 1) / item_rows;
     const int my_items = nitems > warp ? (nitems - warp + nw - 1) / nw : 0;
     const uint64_t total = (uint64_t)N * rb;
@@ -161,28 +163,40 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
     if (pdl) pdl_wait();  // the activation row comes from the previous kernel
     {
         const int nthr = blockDim.x;
-        if constexpr (FUSE) {
-            // x is read in rounds of four 16-byte loads per thread, all issued
-            // before any is used, so a row of up to 4 * 16 * blockDim bytes costs
-            // one memory round trip
-            const float4* x4 = reinterpret_cast<const float4*>(x);
-            if constexpr (F::ACT == QMM_Q8_0) {
-                const int items = (K / 32) * 8;
-                for (int base = warp * 32; base < items; base += 4 * nthr) {
-                    float4 v[4];
+        if constexpr (F::ACT == QMM_Q8_0) {
+            // one thread per activation block: read (or, with FUSE, quantize)
+            // its 32 codes and put them in the layout the decoder reads
+            const int nb = K / 32;
+            for (int b = tid; b < nb; b += nthr) {
+                uint32_t w[8], dbits;
+                if constexpr (FUSE) {
+                    const float4* x4 = reinterpret_cast<const float4*>(x) + (size_t)b * 8;
+                    float4 v[8];
 #pragma unroll
-                    for (int r = 0; r < 4; r++) {
-                        const int gt = base + r * nthr + lane;
-                        v[r] = gt < items ? x4[gt] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
+                    for (int i = 0; i < 8; i++) v[i] = x4[i];
+                    quant_q8_0_block(v, &dbits, w);
+                    if (blockIdx.x == 0 && xq_out != nullptr) {
+                        unsigned short* o = reinterpret_cast<unsigned short*>(xq_out + (size_t)b * 34);
+                        o[0] = (unsigned short)dbits;
 #pragma unroll
-                    for (int r = 0; r < 4; r++) {
-                        const int gt = base + r * nthr + lane;
-                        const bool active = gt < items;
-                        quant_q8_0_part(v[r], active, gt & 7, xs + (active ? (gt >> 3) * 34 : 0));
+                        for (int i = 0; i < 8; i++) {
+                            o[1 + 2 * i] = (unsigned short)(w[i] & 0xFFFFu);
+                            o[2 + 2 * i] = (unsigned short)(w[i] >> 16);
+                        }
                     }
+                } else {
+                    const unsigned short* p = reinterpret_cast<const unsigned short*>(xq + (size_t)b * 34);
+                    dbits = p[0];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) w[i] = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
                 }
-            } else {
+                if constexpr (SU) su_put_block<WT == QMM_Q4_0>(w, dbits, b, nsu, aq, ad, as);
+                else act_put_q8_0_block(w, dbits, b, nb, aq, ad, as);
+            }
+        } else {
+            if constexpr (FUSE) {
+                // one warp per super-block, both rounds of loads issued first
+                const float4* x4 = reinterpret_cast<const float4*>(x);
                 for (int b0 = warp; b0 < nd; b0 += 2 * nw) {
                     const int b1 = b0 + nw;
                     const float4 v0 = x4[b0 * 64 + 2 * lane], v1 = x4[b0 * 64 + 2 * lane + 1];
@@ -191,25 +205,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
                     quant_q8_K_lane(v0, v1, lane, xs + b0 * 292);
                     if (b1 < nd) quant_q8_K_lane(v2, v3, lane, xs + b1 * 292);
                 }
+                __syncthreads();
+                if (blockIdx.x == 0 && xq_out != nullptr) {
+                    const int halves = nd * 292 / 2;
+                    for (int i = tid; i < halves; i += nthr)
+                        reinterpret_cast<unsigned short*>(xq_out)[i] = reinterpret_cast<const unsigned short*>(xs)[i];
+                }
+                xq = xs;
             }
-            __syncthreads();
-            if (blockIdx.x == 0 && xq_out != nullptr) {
-                const int halves = (F::ACT == QMM_Q8_0 ? (K / 32) * 34 : (K / 256) * 292) / 2;
-                for (int i = tid; i < halves; i += nthr)
-                    reinterpret_cast<unsigned short*>(xq_out)[i] = reinterpret_cast<const unsigned short*>(xs)[i];
-            }
-            xq = xs;
-        }
-        if constexpr (SU) {
-            if constexpr (WT == QMM_Q8_0) {
-                for (int i = tid; i < nsu * 17; i += nthr) su_prep_q8_0_chunk(xq, nsu, i, aq);
-                for (int b = tid; b < nd; b += nthr) su_prep_block<false>(xq, nsu, b, aq, ad, as);
-            } else {
-                for (int b = tid; b < nd; b += nthr) su_prep_block<true>(xq, nsu, b, aq, ad, as);
-            }
-        } else if constexpr (F::ACT == QMM_Q8_0) {
-            for (int b = tid; b < nd; b += nthr) unpack_q8_0_block(xq, K, b, aq, ad, as);
-        } else {
             for (int i = tid; i < nd * 73; i += nthr) unpack_q8_K_word(xq, nd, i, aq, ad, as);
         }
         __syncthreads();
@@ -370,7 +373,8 @@ static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, bool 
     if (sb > 0x7FFFFFFFull) return QMM_E_SHAPE;
     p->slot_bytes = (uint32_t)sb;
     uint32_t act = matvec_act_bytes(WT, F::ACT, (int)K, p->su);
-    if (fuse) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);  // the quantized row
+    // a fused Q8_K row is quantized into shared memory first (Q8_0 goes straight to its layout)
+    if (fuse && F::ACT == QMM_Q8_K) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);
     const uint32_t bar_max = align_up(8u * kMaxWarps * 2, 128u);
     if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + sb) return QMM_E_SHAPE;
     const uint64_t budget = (uint64_t)dev.max_smem_optin - bar_max - act;

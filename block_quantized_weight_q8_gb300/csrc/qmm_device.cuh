@@ -346,6 +346,18 @@ __device__ __forceinline__ void q6_K_isums(const SmemBytes& w, uint32_t o, const
 // at least 2-byte aligned) into the chunk-major ActView arrays, one item per
 // call so that any set of threads can share the work; the caller synchronizes
 // those threads afterwards.
+// block b (f16 scale bits, 32 codes as 8 words) into the chunk-major Q8_0 view
+__device__ __forceinline__ void act_put_q8_0_block(const uint32_t w[8], uint32_t dbits, int b, int nb, uint8_t* q,
+                                                   float* d, int* s) {
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) sum = dp4a(w[i], 0x01010101u, sum);
+    d[b] = h2f(dbits);
+    s[b] = sum;
+    *reinterpret_cast<uint4*>(q + (size_t)b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(q + ((size_t)nb + b) * 16) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 __device__ __forceinline__ void unpack_q8_0_block(const uint8_t* __restrict__ row, int K, int b, uint8_t* q, float* d,
                                                   int* s) {
     const int nb = K / 32;
@@ -484,60 +496,67 @@ __device__ __forceinline__ void quant_q8_K_lane(float4 v0, float4 v1, int lane, 
 //         elements j and j+16); plane p, chunk c at ((9p + c)*nsu + u)*16.
 //   d[b]: f32 activation scale of block b; s[b]: int32 sum of its 32 codes.
 
-// Q8_0 activation item i of nsu*17 (one 16-byte chunk); row at least 2-byte aligned
-__device__ __forceinline__ void su_prep_q8_0_chunk(const uint8_t* __restrict__ row, int nsu, int i, uint8_t* q) {
-    const int u = i / 17, c = i - 17 * u;
-    const uint8_t* src = row + 272 * u + 16 * c;
-    uint32_t w[4];
-    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src);
-        w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
-    } else {
-        const unsigned short* p = reinterpret_cast<const unsigned short*>(src);
-#pragma unroll
-        for (int j = 0; j < 4; j++) w[j] = (uint32_t)p[2 * j] | ((uint32_t)p[2 * j + 1] << 16);
-    }
-    // zero the d field of every block b whose first byte 34b falls in this chunk
-#pragma unroll
-    for (int b = 0; b < 8; b++) {
-        const int pos = 34 * b - 16 * c;
-#pragma unroll
-        for (int j = 0; j < 4; j++)
-            if (pos >= 4 * j && pos < 4 * j + 4) w[j] &= (pos & 2) ? 0x0000FFFFu : 0xFFFF0000u;
-    }
-    *reinterpret_cast<uint4*>(q + ((size_t)c * nsu + u) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// block b of a Q8_0 activation row: its f32 scale and code sum; for Q4_0 also
-// scatters the codes into the two planes
+// Writes block b of a Q8_0 activation row -- its f16 scale bits and its 32
+// codes as 8 little-endian words -- into the super-unit arrays of a Q8_0
+// (PLANES = false) or Q4_0 (PLANES = true) weight, with its f32 scale and code
+// sum.  Every byte of the arrays belongs to exactly one block, so one call per
+// block fills them.  All stores are 16-bit at even offsets within a chunk.
 template <bool PLANES>
-__device__ __forceinline__ void su_prep_block(const uint8_t* __restrict__ row, int nsu, int b, uint8_t* q, float* d,
-                                              int* s) {
-    const unsigned short* p = reinterpret_cast<const unsigned short*>(row + 34 * b);
-    d[b] = h2f(p[0]);
-    uint32_t w[8];
+__device__ __forceinline__ void su_put_block(const uint32_t w[8], uint32_t dbits, int b, int nsu, uint8_t* q,
+                                             float* d, int* s) {
     int sum = 0;
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-        w[i] = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
-        sum = dp4a(w[i], 0x01010101u, sum);
-    }
+    for (int i = 0; i < 8; i++) sum = dp4a(w[i], 0x01010101u, sum);
+    d[b] = h2f(dbits);
     s[b] = sum;
-    if constexpr (PLANES) {
-        const int u = b >> 3, bb = b & 7;
+    const int u = b >> 3, bb = b & 7;
+    if constexpr (!PLANES) {
+        // bytes 34bb, 34bb+1: the weight's d field (zero); 34bb + 2 + j: code j
+        const int y0 = 34 * bb;
+        *reinterpret_cast<unsigned short*>(q + ((size_t)(y0 >> 4) * nsu + u) * 16 + (y0 & 15)) = 0;
+#pragma unroll
+        for (int h = 0; h < 16; h++) {
+            const int y = y0 + 2 + 2 * h;
+            *reinterpret_cast<unsigned short*>(q + ((size_t)(y >> 4) * nsu + u) * 16 + (y & 15)) =
+                (unsigned short)((w[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
+        }
+    } else {
 #pragma unroll
         for (int pl = 0; pl < 2; pl++) {
             const int y0 = 18 * bb;  // the weight's d field: zero in both planes
-            *reinterpret_cast<unsigned short*>(q + ((size_t)(9 * pl + y0 / 16) * nsu + u) * 16 + (y0 & 15)) = 0;
+            *reinterpret_cast<unsigned short*>(q + ((size_t)(9 * pl + (y0 >> 4)) * nsu + u) * 16 + (y0 & 15)) = 0;
 #pragma unroll
             for (int h = 0; h < 8; h++) {
-                const int y = 18 * bb + 2 + 2 * h;  // even, so the pair never straddles a chunk
+                const int y = y0 + 2 + 2 * h;
                 const int code = 16 * pl + 2 * h;
-                const uint32_t pair = (w[code >> 2] >> (16 * ((code >> 1) & 1))) & 0xFFFFu;
-                *reinterpret_cast<unsigned short*>(q + ((size_t)(9 * pl + y / 16) * nsu + u) * 16 + (y & 15)) =
-                    (unsigned short)pair;
+                *reinterpret_cast<unsigned short*>(q + ((size_t)(9 * pl + (y >> 4)) * nsu + u) * 16 + (y & 15)) =
+                    (unsigned short)((w[code >> 2] >> (16 * ((code >> 1) & 1))) & 0xFFFFu);
             }
         }
+    }
+}
+
+// One thread quantizes one Q8_0 block of 32 values v (the same IEEE-rounded
+// steps as quant_q8_0_part, so the same bytes): f16 scale bits and the codes as
+// 8 little-endian words.
+__device__ __forceinline__ void quant_q8_0_block(const float4 v[8], uint32_t* dbits, uint32_t w[8]) {
+    // max over the block, seeded with the first values so that it is the same
+    // set-maximum (NaN rules included) as the reduction in quant_q8_0_part
+    float amax = fmaxf(fmaxf(fabsf(v[0].x), fabsf(v[0].y)), fmaxf(fabsf(v[0].z), fabsf(v[0].w)));
+#pragma unroll
+    for (int i = 1; i < 8; i++)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = amax != 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    *dbits = f2h_bits(d);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int q0 = clampi(__float2int_rn(__fmul_rn(v[i].x, id)), -128, 127);
+        const int q1 = clampi(__float2int_rn(__fmul_rn(v[i].y, id)), -128, 127);
+        const int q2 = clampi(__float2int_rn(__fmul_rn(v[i].z, id)), -128, 127);
+        const int q3 = clampi(__float2int_rn(__fmul_rn(v[i].w, id)), -128, 127);
+        w[i] = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) | ((uint32_t)(q2 & 0xFF) << 16) |
+               ((uint32_t)(q3 & 0xFF) << 24);
     }
 }
 
