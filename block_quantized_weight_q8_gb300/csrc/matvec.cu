@@ -35,7 +35,10 @@ struct MatvecPlan {
     bool su;              // decode whole super-units (Q8_0 / Q4_0 with K % 256 == 0)
     int nw;               // warps per CTA
     int lpr;              // lanes per row (power of two, 1..32)
-    int item_rows;        // rows per item (whole passes of 32 / lpr rows)
+    int pieces;           // segments per row
+    int piece_units;      // units per segment (the last segment of a row may have fewer)
+    int item_segs;        // segments per item (whole passes of 32 / lpr segments)
+    uint32_t part_off;    // shared offset of the per-segment partial sums (pieces > 1)
     int depth;            // slots in each warp's ring
     uint32_t slot_bytes;  // bytes per slot (the item's 16-byte aligned superset)
     uint32_t act_bytes;   // shared bytes before the first slot (barriers, activation)
@@ -76,30 +79,52 @@ __device__ __forceinline__ float unit_contrib(const SmemBytes& w, uint32_t o, co
     }
 }
 
-// Issues the bulk copy of item `it` (rows [r0, r1) of W, as their 16-byte
-// aligned superset, the last < 16 bytes of W excepted) into a slot.
-__device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t rb, uint64_t total_al, int r0, int r1,
+// Rows cut into `pieces` segments of `piece_units` units (the last may be
+// shorter); segment s = row s / pieces, piece s % pieces.  A unit is a block,
+// a super-block or a super-unit (ubytes each).  Segments are consecutive in W.
+template <bool SPLIT>
+struct SegGeom {
+    uint64_t rb;      // row bytes
+    int nunit;        // units per row
+    int pieces;       // 1 unless SPLIT
+    int piece_units;
+    int ubytes;
+    __device__ __forceinline__ uint64_t off(int s) const {  // byte offset of segment s in W
+        if constexpr (!SPLIT) return (uint64_t)s * rb;
+        const int row = s / pieces, piece = s - row * pieces;
+        const int u = min(piece * piece_units, nunit);
+        return (uint64_t)row * rb + (uint64_t)u * ubytes;
+    }
+};
+
+// Issues the bulk copy of the bytes [g0, g1) of W, as their 16-byte aligned
+// superset (the last < 16 bytes of W excepted), into a slot.
+__device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t g0, uint64_t g1, uint64_t total_al,
                                            uint8_t* slot, uint32_t bar, uint64_t pol) {
-    const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
-    uint64_t a1 = ((uint64_t)r1 * rb + 15ull) & ~15ull;
+    const uint64_t a0 = g0 & ~15ull;
+    uint64_t a1 = (g1 + 15ull) & ~15ull;
     if (a1 > total_al) a1 = total_al;
     const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
     mbar_arrive_expect_tx(bar, bytes);
     if (bytes) bulk_g2s(smem_u32(slot), W + a0, bytes, bar, pol);
 }
 
-// The decode matvec.  Each CTA owns an even share of the rows, cut into items
-// of `item_rows` rows (whole passes of 32 / lpr rows).  Warp w of the CTA takes
-// items w, w + nw, w + 2nw, ... and streams them through its own ring of
+// The decode matvec.  Each CTA owns an even share of the rows.  A row is one
+// segment, or `pieces` segments when it is long enough that one segment would
+// leave lanes idle; the CTA's segments are cut into items of `item_segs`
+// consecutive segments (whole passes of 32 / lpr segments).  Warp w of the CTA
+// takes items w, w + nw, w + 2nw, ... and streams them through its own ring of
 // `depth` shared-memory slots with 1-D bulk copies (cp.async.bulk completing
 // on the slot's mbarrier, evict-first in L2).  A warp refills a slot as soon as
 // it has decoded it, so no warp waits for another and no CTA-wide barrier sits
-// in the stream.  Lanes take the units of a row (a block, a super-block or,
+// in the stream.  Lanes take the units of a segment (a block, a super-block or,
 // with SU, a super-unit of 8 blocks) in steps of `lpr`, decode them from shared
 // memory, take the exact integer block dots with dp4a, fold each into fp32 once
-// per block and reduce with shuffles in a fixed order; every y[o] is written by
-// one lane, identically on every run ([minfer] "10 . CPU matmul: quantized
-// weights x Q8_0 activations" s3.3: row ownership, no split reduction).
+// per block and reduce with shuffles in a fixed order.  A one-segment row is
+// written by that lane; otherwise the segments' partial sums meet in shared
+// memory and one thread adds them in piece order.  Either way every y[o] comes
+// from one fixed order of operations, identical on every run ([minfer] "10 .
+// CPU matmul: quantized weights x Q8_0 activations" s3.3: row ownership).
 //
 // With pdl set the kernel is one link of a programmatic-dependent-launch chain:
 // it lets its successor launch at once and streams the first item of each warp
@@ -113,12 +138,13 @@ __device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t rb, uint64
 // arithmetic as the standalone quantizer, so the codes are the same bytes);
 // CTA 0 also stores the quantized row to xq_out when that is not null.  One
 // launch then does the whole quantize + multiply of a decode token.
-template <int WT, bool SU, bool FUSE>
+template <int WT, bool SU, bool FUSE, bool SPLIT>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t* __restrict__ W,
                                                                   const uint8_t* __restrict__ xq,
                                                                   const float* __restrict__ x, uint8_t* xq_out,
                                                                   float* __restrict__ y, int N, int K, int lpr,
-                                                                  int item_rows, int depth, uint32_t slot_bytes,
+                                                                  int pieces, int piece_units, int item_segs,
+                                                                  int depth, uint32_t slot_bytes, uint32_t part_off,
                                                                   uint32_t act_bytes, int pdl) {
     using F = Fmt<WT>;
     if (pdl) pdl_launch_dependents();
@@ -139,11 +165,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
 
     const int units = K / F::BV;
     const uint64_t rb = (uint64_t)units * F::BB;
+    if constexpr (!SPLIT) pieces = 1;
+    const SegGeom<SPLIT> geo{rb, SU ? nsu : units, pieces, piece_units, SU ? (WT == QMM_Q4_0 ? 144 : 272) : F::BB};
     // an even split of the rows: the first N % grid CTAs take one row more
     const int rq = N / (int)gridDim.x, rr = N - rq * (int)gridDim.x;
     const int r_begin = (int)blockIdx.x * rq + min((int)blockIdx.x, rr);
     const int r_end = r_begin + rq + ((int)blockIdx.x < rr ? 1 : 0);
-    const int nitems = (r_end - r_begin + item_rows - 1) / item_rows;
+    const int s_begin = r_begin * pieces, s_end = r_end * pieces;  // this CTA's segments
+    const int nitems = (s_end - s_begin + item_segs - 1) / item_segs;
     const int my_items = nitems > warp ? (nitems - warp + nw - 1) / nw : 0;
     const uint64_t total = (uint64_t)N * rb;
     const uint64_t total_al = total & ~15ull;
@@ -154,8 +183,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
         fence_mbar_init();
         pol = policy_evict_first();
         if (my_items > 0) {
-            const int r0 = r_begin + warp * item_rows;
-            issue_item(W, rb, total_al, r0, min(r0 + item_rows, r_end), slots, smem_u32(&full[0]), pol);
+            const int s0 = s_begin + warp * item_segs;
+            issue_item(W, geo.off(s0), geo.off(min(s0 + item_segs, s_end)), total_al, slots, smem_u32(&full[0]), pol);
         }
     }
     __syncwarp();
@@ -219,56 +248,80 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
     }
     if (lane == 0) {
         for (int k = 1; k < depth && k < my_items; k++) {
-            const int r0 = r_begin + (warp + k * nw) * item_rows;
-            issue_item(W, rb, total_al, r0, min(r0 + item_rows, r_end), slots + (size_t)k * slot_bytes,
+            const int s0 = s_begin + (warp + k * nw) * item_segs;
+            issue_item(W, geo.off(s0), geo.off(min(s0 + item_segs, s_end)), total_al, slots + (size_t)k * slot_bytes,
                        smem_u32(&full[k]), pol);
         }
     }
 
     const ActView act{aq, ad, as, nd};
-    const int rows_per_pass = 32 / lpr;
-    const int rsub = lane / lpr, li = lane % lpr;
+    float* part = reinterpret_cast<float*>(smem + part_off);  // pieces > 1: one partial per segment
+    const int segs_per_pass = 32 / lpr;
+    const int ssub = lane / lpr, li = lane % lpr;
+    bool failed = false;
     for (int k = 0; k < my_items; k++) {
         const int slot = k % depth;
         const bool ok = mbar_wait_bounded(smem_u32(&full[slot]), (uint32_t)(k / depth) & 1u, kWaitLimitNs);
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane == 0) atomicOr(&g_matvec_error, kErrTimeout);
-            return;
+            failed = true;
+            break;
         }
-        const int r0 = r_begin + (warp + k * nw) * item_rows;
-        const int r1 = min(r0 + item_rows, r_end);
-        const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
+        const int s0 = s_begin + (warp + k * nw) * item_segs;
+        const int s1 = min(s0 + item_segs, s_end);
+        const uint64_t a0 = geo.off(s0) & ~15ull;
         uint8_t* sbuf = slots + (size_t)slot * slot_bytes;
         const SmemBytes wv{sbuf};
-        for (int rr = r0; rr < r1; rr += rows_per_pass) {
-            const int row = rr + rsub;
-            if (row == N - 1 && total > total_al) {
-                // the last < 16 bytes of W lie in the last row: not reachable by a
-                // 16-byte bulk copy, so this warp fetches them itself
+        for (int ss = s0; ss < s1; ss += segs_per_pass) {
+            const int seg = ss + ssub;
+            if (seg == (SPLIT ? N * pieces : N) - 1 && total > total_al) {
+                // the last < 16 bytes of W lie in the last segment: not reachable
+                // by a 16-byte bulk copy, so this warp fetches them itself
                 for (uint64_t i = total_al + li; i < total; i += lpr) sbuf[i - a0] = W[i];
             }
             __syncwarp();
             float acc = 0.0f;
-            if (row < r1) {
-                const uint32_t ro = (uint32_t)((uint64_t)row * rb - a0);
+            if (seg < s1) {
+                int u0 = 0, un = geo.nunit;
+                if constexpr (SPLIT) {
+                    const int piece = seg - (seg / pieces) * pieces;
+                    u0 = piece * piece_units;
+                    un = min(piece_units, geo.nunit - u0);
+                }
+                const uint32_t so = (uint32_t)(geo.off(seg) - a0);
                 if constexpr (SU) {
-                    for (int u = li; u < nsu; u += lpr) {
-                        if constexpr (WT == QMM_Q8_0) acc += su_q8_0(sbuf + ro + 272u * u, aq, nsu, u, ad + 8 * u);
-                        else acc += su_q4_0(sbuf + ro + 144u * u, aq, nsu, u, ad + 8 * u, as + 8 * u);
+                    for (int u = li; u < un; u += lpr) {
+                        const int ug = u0 + u;
+                        if constexpr (WT == QMM_Q8_0) acc += su_q8_0(sbuf + so + 272u * u, aq, nsu, ug, ad + 8 * ug);
+                        else acc += su_q4_0(sbuf + so + 144u * u, aq, nsu, ug, ad + 8 * ug, as + 8 * ug);
                     }
                 } else {
 #pragma unroll 4
-                    for (int u = li; u < units; u += lpr)
-                        acc += unit_contrib<WT>(wv, ro + (uint32_t)(u * F::BB), act, u);
+                    for (int u = li; u < un; u += lpr)
+                        acc += unit_contrib<WT>(wv, so + (uint32_t)(u * F::BB), act, u0 + u);
                 }
             }
             for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (row < r1 && li == 0) y[row] = acc;
+            if (seg < s1 && li == 0) {
+                if constexpr (SPLIT) part[seg - s_begin] = acc;
+                else y[seg] = acc;
+            }
         }
         __syncwarp();
         if (lane == 0 && k + depth < my_items) {
-            const int q0 = r_begin + (warp + (k + depth) * nw) * item_rows;
-            issue_item(W, rb, total_al, q0, min(q0 + item_rows, r_end), sbuf, smem_u32(&full[slot]), pol);
+            const int q0 = s_begin + (warp + (k + depth) * nw) * item_segs;
+            issue_item(W, geo.off(q0), geo.off(min(q0 + item_segs, s_end)), total_al, sbuf, smem_u32(&full[slot]),
+                       pol);
+        }
+    }
+    if constexpr (SPLIT) {
+        // a row's pieces were taken by different warps: add them in piece order
+        if (!__syncthreads_or(failed ? 1 : 0)) {
+            for (int r = r_begin + tid; r < r_end; r += blockDim.x) {
+                float v = 0.0f;
+                for (int p = 0; p < pieces; p++) v += part[(r - r_begin) * pieces + p];
+                y[r] = v;
+            }
         }
     }
 }
@@ -350,34 +403,54 @@ __host__ inline uint32_t matvec_act_bytes(int wt, int act, int K, bool su) {
     return align_up((uint32_t)((wt == QMM_Q4_0 ? 288 : 272) * nsu + 8 * nd), 128u);
 }
 
-// Picks the launch shape for (format, N, K).  Lanes per row cover the row's
-// units (a pass = 32 / lpr rows); an item is one pass, or several when a pass
-// is under 2 KB.  Each warp keeps two items in flight when 12 or more warps fit
-// that way, else one item with 16 warps (more warps beat a deeper ring there).
-// One CTA per SM.
+// Picks the launch shape for (format, N, K).  A row is cut into the fewest
+// segments that keep the most lanes busy (a segment of U units gets the
+// smallest power of two >= U lanes; at most 32).  Lanes per segment cover its
+// units (a pass = 32 / lpr segments); an item is one pass, or several when a
+// pass is under 4 KB.  Each warp keeps two items in flight when 12 or more warps
+// fit that way, else one item with 16 warps (more warps beat a deeper ring
+// there).  One CTA per SM.
 template <int WT>
 static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, bool fuse, MatvecPlan* p) {
     using F = Fmt<WT>;
     p->su = (WT == QMM_Q8_0 || WT == QMM_Q4_0) && K % 256 == 0;
     const int nunit = p->su ? (int)(K / 256) : (int)(K / F::BV);
-    int lpr = 1;
-    while (lpr < 32 && lpr < nunit) lpr <<= 1;
-    p->lpr = lpr;
-    const uint64_t rb = (uint64_t)(K / F::BV) * F::BB;
-    const int rpp = 32 / lpr;
-    const uint64_t pass_bytes = (uint64_t)rpp * rb;
+    const int ubytes = p->su ? (WT == QMM_Q4_0 ? 144 : 272) : F::BB;
+    int best_p = 1, best_l = 32;
+    double best_use = -1.0;
+    for (int cap = 32; cap >= 8; cap >>= 1) {
+        const int P = (nunit + cap - 1) / cap, U = (nunit + P - 1) / P;
+        int l = 1;
+        while (l < U) l <<= 1;
+        const double use = (double)nunit / ((double)P * l);
+        if (use > best_use + 1e-9) best_use = use, best_p = P, best_l = l;
+    }
+    p->pieces = best_p;
+    p->piece_units = (nunit + best_p - 1) / best_p;
+    p->lpr = best_l;
+    const uint64_t seg_bytes = (uint64_t)p->piece_units * ubytes;
+    const int spp = 32 / p->lpr;
+    const uint64_t pass_bytes = (uint64_t)spp * seg_bytes;
     int npass = (int)(4096u / pass_bytes);
     if (npass < 1) npass = 1;
-    p->item_rows = npass * rpp;
+    p->item_segs = npass * spp;
     const uint64_t sb = align_up((uint32_t)(npass * pass_bytes + 32), 128u);
     if (sb > 0x7FFFFFFFull) return QMM_E_SHAPE;
     p->slot_bytes = (uint32_t)sb;
+    int64_t grid = dev.sms;
+    const int64_t items = (N * p->pieces + p->item_segs - 1) / p->item_segs;
+    if (grid > items) grid = items;
+    if (grid > N) grid = N;
+    if (grid < 1) grid = 1;
+    p->grid = (int)grid;
     uint32_t act = matvec_act_bytes(WT, F::ACT, (int)K, p->su);
     // a fused Q8_K row is quantized into shared memory first (Q8_0 goes straight to its layout)
     if (fuse && F::ACT == QMM_Q8_K) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);
+    const uint64_t rows_max = (uint64_t)((N + grid - 1) / grid);
+    const uint64_t part_bytes = p->pieces > 1 ? align_up((uint32_t)(rows_max * p->pieces * 4), 128u) : 0;
     const uint32_t bar_max = align_up(8u * kMaxWarps * 2, 128u);
-    if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + sb) return QMM_E_SHAPE;
-    const uint64_t budget = (uint64_t)dev.max_smem_optin - bar_max - act;
+    if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + part_bytes + sb) return QMM_E_SHAPE;
+    const uint64_t budget = (uint64_t)dev.max_smem_optin - bar_max - act - part_bytes;
     int nw = (int)(budget / (2 * sb));
     if (nw >= 12) {
         p->depth = 2;
@@ -388,23 +461,19 @@ static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, bool 
     if (nw > kMaxWarps) nw = kMaxWarps;
     if (nw < 1) return QMM_E_SHAPE;
     p->nw = nw;
-    p->act_bytes = align_up(8u * nw * p->depth, 128u) + act;
+    p->part_off = align_up(8u * nw * p->depth, 128u) + act;
+    p->act_bytes = p->part_off + (uint32_t)part_bytes;
     p->smem = p->act_bytes + (uint32_t)(nw * p->depth) * p->slot_bytes;
-    int64_t grid = dev.sms;
-    const int64_t items = (N + p->item_rows - 1) / p->item_rows;
-    if (grid > items) grid = items;
-    if (grid < 1) grid = 1;
-    p->grid = (int)grid;
     return QMM_OK;
 }
 
-template <int WT, bool SU, bool FUSE>
-static qmm_status launch_matvec_su(const void* W, const void* xq, const float* x, void* xq_out, float* y, int64_t N,
+template <int WT, bool SU, bool FUSE, bool SPLIT>
+static qmm_status launch_matvec_k(const void* W, const void* xq, const float* x, void* xq_out, float* y, int64_t N,
                                    int64_t K, const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream,
                                    bool pdl) {
     static bool attr_set[64] = {false};
     if (!attr_set[dev.device]) {
-        if (cudaFuncSetAttribute(matvec_kernel<WT, SU, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(matvec_kernel<WT, SU, FUSE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dev.max_smem_optin) != cudaSuccess)
             return QMM_E_CUDA;
         attr_set[dev.device] = true;
@@ -419,10 +488,19 @@ static qmm_status launch_matvec_su(const void* W, const void* xq, const float* x
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, SU, FUSE>, (const uint8_t*)W,
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, SU, FUSE, SPLIT>, (const uint8_t*)W,
                                              (const uint8_t*)xq, x, (uint8_t*)xq_out, y, (int)N, (int)K, p.lpr,
-                                             p.item_rows, p.depth, p.slot_bytes, p.act_bytes, pdl ? 1 : 0);
+                                             p.pieces, p.piece_units, p.item_segs, p.depth, p.slot_bytes, p.part_off,
+                                             p.act_bytes, pdl ? 1 : 0);
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
+
+template <int WT, bool SU, bool FUSE>
+static qmm_status launch_matvec_su(const void* W, const void* xq, const float* x, void* xq_out, float* y, int64_t N,
+                                   int64_t K, const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream,
+                                   bool pdl) {
+    if (p.pieces > 1) return launch_matvec_k<WT, SU, FUSE, true>(W, xq, x, xq_out, y, N, K, p, dev, stream, pdl);
+    return launch_matvec_k<WT, SU, FUSE, false>(W, xq, x, xq_out, y, N, K, p, dev, stream, pdl);
 }
 
 // x == nullptr: multiply the quantized row xq.  Otherwise quantize x in the
