@@ -443,11 +443,24 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
         qmm.qmm_quantize_q8_K(xd, qd, 1, 12288, stream=sh)
         qmm.matvec("q6_K", s[6][4], qd, outs["W_down"], 4096, 12288, stream=sh)
 
+    # the same layer through qmm_linear_*: each multiply quantizes its own input row in-kernel
+    scratch = torch.empty(qmm.qmm_row_bytes("q8_K", 12288), dtype=torch.uint8, device=dev)
+    xin = {"Wq": xh, "Wk": xh, "Wv": xh, "W_gate": xh, "W_up": xh, "Wo": xo, "W_down": xd}
+
+    def layer_linear(i):
+        for (label, wtype, N, K, W) in sets[i % C]:
+            qmm.linear(wtype, W, xin[label], scratch, scratch.numel(), outs[label], 1, N, K, stream=sh)
+
     t_layer = timed_graph(layer, 8)
+    t_lin = timed_graph(layer_linear, 8)
     res["q4_K_M_layer_4096"] = {"layer_us": round(t_layer * 1e6, 3), "GB/s": round(layer_bytes / t_layer / 1e9, 1),
                                 "frac_hbm": round(layer_bytes / t_layer / 1e9 / hbm, 4), "weight_bytes": layer_bytes,
                                 "equiv_tok_s_36_layers_matmuls_only": round(1.0 / (36 * t_layer), 1),
-                                "launches_per_layer": 10, "copies": C}
+                                "launches_per_layer": 10, "copies": C,
+                                "how": "3 shared qmm_quantize_q8_K + 7 qmm_matvec",
+                                "linear_layer_us": round(t_lin * 1e6, 3),
+                                "linear_GB/s": round(layer_bytes / t_lin / 1e9, 1),
+                                "linear_launches_per_layer": 7}
     del sets, mats
 
     # prefill
@@ -472,6 +485,22 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
         pre["M=%d" % M] = {"us": round(t * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
                            "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4),
                            "frac_hbm_weight_stream": round(W.numel() / t / 1e9 / hbm, 4)}
+    # context: the GPU's own int8 and fp16 GEMMs (cuBLAS through torch) on the M=512 shape
+    try:
+        M = 512
+        a8 = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev)
+        b8 = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev).t()
+        ah = torch.randn(M, K, dtype=torch.float16, device=dev)
+        bh = torch.randn(K, N, dtype=torch.float16, device=dev)
+        t8 = timed_graph(lambda i: torch._int_mm(a8, b8), 2)
+        t16 = timed_graph(lambda i: torch.matmul(ah, bh), 2)
+        pre["context_cublas_M=512"] = {"int8_TOPS": round(2.0 * M * N * K / t8 / 1e12, 1),
+                                       "fp16_TFLOPS": round(2.0 * M * N * K / t16 / 1e12, 1),
+                                       "note": "torch._int_mm / fp16 matmul on the same shape: the int8 tensor "
+                                               "path of this GPU, and the fp16 path the prefill kernel uses"}
+        del a8, b8, ah, bh
+    except Exception as ex:  # context only
+        pre["context_cublas_M=512"] = {"error": str(ex)[:120]}
     res["q4_0_prefill_12288x4096"] = pre
     return res
 
