@@ -1,0 +1,101 @@
+"""Edge cases of the decode path on the GPU, against the CPU oracle.
+
+The largest K the library accepts (65536: every format's row is cut into segments whose
+partial sums meet in shared memory), rows whose last segment is short, rows whose blocks do
+not group into 16-byte aligned super-units, and the quantize-inside-the-matvec path of
+qmm_linear_* on all of these, with its stored activation row compared byte for byte."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+import block_quantized_weight_q8_gb300 as qmm  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+WTYPES = ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("these tests need a CUDA GPU")
+    qmm.build()
+    qmm.load()
+    yield
+    assert qmm.qmm_device_status(clear=True) == 0
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def act_name(wtype):
+    return "q8_0" if wtype in ("q4_0", "q8_0") else "q8_K"
+
+
+def assert_rows_close(y, ref, tol=TOL):
+    y = np.asarray(y, dtype=np.float64).reshape(ref.shape)
+    ref = np.asarray(ref, dtype=np.float64)
+    norm = np.linalg.norm(ref, axis=-1, keepdims=True)
+    err = np.abs(y - ref)
+    bad = err > tol * norm + 1e-30
+    assert not bad.any(), "max err/norm %.3g at %s" % ((err / np.maximum(norm, 1e-30)).max(),
+                                                     np.argwhere(bad)[:3].tolist())
+
+
+def check_matvec_and_linear(wtype, M, N, K, seed):
+    w = workloads.weights_f32(N, K, seed, row_jitter=True)
+    x = workloads.activations_f32(M, K, seed + 1)
+    W = oracle.quantize(wtype, w)
+    X = oracle.quantize(act_name(wtype), x)
+    ref = oracle.matmul(wtype, W, X, M, N, K, nthreads=8)
+    Wd = dev(W)
+    xrb = qmm.qmm_row_bytes(act_name(wtype), K)
+    # the multiply on quantized rows, one token at a time
+    for t in range(M):
+        y = torch.empty(N, dtype=torch.float32, device="cuda")
+        qmm.matvec(wtype, Wd, dev(X.reshape(M, -1)[t]), y, N, K)
+        assert_rows_close(host(y), ref[t])
+    # quantize + multiply through the linear entry point
+    scratch = torch.empty(M * xrb, dtype=torch.uint8, device="cuda")
+    Y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    qmm.linear(wtype, Wd, dev(x), scratch, scratch.numel(), Y, M, N, K)
+    assert_rows_close(host(Y), ref)
+    assert np.array_equal(host(scratch), X.reshape(-1))
+
+
+@pytest.mark.parametrize("wtype", WTYPES)
+def test_max_k(wtype):
+    """K = 65536, the header's limit: 256 units per row for every format."""
+    check_matvec_and_linear(wtype, 1, 19, 65536, seed=70)
+
+
+@pytest.mark.parametrize("wtype,K", [("q8_0", 4128), ("q4_0", 4128), ("q8_0", 4160), ("q4_0", 96),
+                                     ("q4_K", 4352), ("q6_K", 4352), ("q2_K", 4352), ("q6_K", 12288)])
+def test_short_last_segment(wtype, K):
+    """Rows cut into segments with a shorter last one (129 Q8_0 blocks: 16 segments of 8 and one
+    of 1; 17 super-blocks: 3 segments of 6, 6, 5), and rows of blocks that do not form aligned
+    super-units (K % 256 != 0)."""
+    check_matvec_and_linear(wtype, 2, 301, K, seed=80 + K)
+
+
+@pytest.mark.parametrize("wtype", WTYPES)
+def test_one_row_per_cta_and_idle_warps(wtype):
+    """Fewer rows than SMs x warps: most warps of most CTAs have no item."""
+    K = 256 if wtype in ("q4_K", "q6_K", "q2_K") else 64
+    check_matvec_and_linear(wtype, 3, 150, K, seed=90)
+
+
+def test_linear_token_rows_of_odd_alignment():
+    """Q8_0 rows of 34 * 3 bytes: token t's quantized row starts 2 bytes past a 16-byte boundary
+    for odd t, so the in-kernel quantizer stores it with 16-bit writes."""
+    check_matvec_and_linear("q8_0", 5, 67, 96, seed=95)
