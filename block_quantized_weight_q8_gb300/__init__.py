@@ -47,6 +47,7 @@ SIGNATURES = {
     "qmm_linear_q2_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
     "qmm_linear_noalloc": ("tpppiiiq", ctypes.c_int),
+    "qmm_linear_group": ("ttppppspiiq", ctypes.c_int),
     "qmm_blocksums": ("tpppiiiq", ctypes.c_int),
     "qmm_device_status": ("c", ctypes.c_int),
 }
@@ -202,6 +203,20 @@ def qmm_linear_noalloc(wtype, W, x, y, M, N, K, stream=None):
     """qmm_linear_<wtype> without a workspace argument: the library's own 1 MiB device array holds the
     quantized rows (see include/qmm.h for the limit and the sharing rules)."""
     _call("qmm_linear_noalloc", _type(wtype), ptr(W), ptr(x), ptr(y), int(M), int(N), int(K), stream_handle(stream))
+
+
+def qmm_linear_group(wtype, Ws, Ns, x, scratch, scratch_bytes, ys, M, K, stream=None):
+    """qmm_linear_<wtype> for several matrices Ws (rows Ns) on the same rows x, outputs ys, one launch
+    per token (see include/qmm.h)."""
+    G = len(Ws)
+    if not (len(Ns) == G and len(ys) == G):
+        raise ValueError("Ws, Ns and ys must have the same length")
+    w_arr = (ctypes.c_void_p * max(G, 1))(*[ptr(w) for w in Ws])
+    n_arr = (ctypes.c_int64 * max(G, 1))(*[int(n) for n in Ns])
+    y_arr = (ctypes.c_void_p * max(G, 1))(*[ptr(y) for y in ys])
+    _call("qmm_linear_group", _type(wtype), G, ctypes.cast(w_arr, ctypes.c_void_p), ctypes.cast(n_arr, ctypes.c_void_p),
+          ptr(x), ptr(scratch), int(scratch_bytes), ctypes.cast(y_arr, ctypes.c_void_p), int(M), int(K),
+          stream_handle(stream))
 
 
 def qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=None):

@@ -10,6 +10,10 @@ qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int6
                            bool pdl);
 qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq_out, float* y, int64_t N, int64_t K,
                                  cudaStream_t stream, bool pdl);
+qmm_status matvec_group_fused_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
+                                       const float* x, void* xq_out, int64_t K, cudaStream_t stream, bool pdl);
+qmm_status matvec_group_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
+                                 const void* xq, int64_t K, cudaStream_t stream, bool pdl);
 qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                               cudaStream_t stream, bool pdl);
 
@@ -50,12 +54,52 @@ static qmm_status linear(int wt, const void* W, const float* x, void* scratch, s
     return QMM_OK;
 }
 
+// G matrices on the same token rows: one launch per token, each CTA quantizing
+// the row it needs; the separate quantizer first when the row does not fit.
+static qmm_status linear_group(int wt, int G, const void* const* W, const int64_t* N, const float* x, void* scratch,
+                               size_t scratch_bytes, float* const* y, int64_t M, int64_t K, cudaStream_t stream) {
+    const int act = act_type_of(wt);
+    if (act < 0) return QMM_E_TYPE;
+    if (G < 1 || G > 8) return QMM_E_SHAPE;
+    if (!W || !N || !x || !scratch || !y) return QMM_E_NULL;
+    for (int g = 0; g < G; g++) {
+        if (!W[g] || !y[g]) return QMM_E_NULL;
+        const qmm_status st = check_shape(wt, M, N[g], K);
+        if (st != QMM_OK) return st;
+        if (!aligned16(W[g]) || !aligned16(y[g])) return QMM_E_ALIGN;
+    }
+    if (!aligned16(x) || !aligned16(scratch)) return QMM_E_ALIGN;
+    const size_t xrb = row_bytes_of(act, K);
+    if (scratch_bytes < (size_t)M * xrb) return QMM_E_SCRATCH;
+    float* yt[8];
+    bool fused = true;
+    for (int64_t t = 0; t < M; t++) {
+        for (int g = 0; g < G; g++) yt[g] = y[g] + t * N[g];
+        qmm_status st = QMM_E_SHAPE;
+        if (fused)
+            st = matvec_group_fused_dispatch(wt, G, W, N, yt, x + t * K, (uint8_t*)scratch + t * xrb, K, stream, true);
+        if (st == QMM_E_SHAPE && t == 0) {
+            fused = false;
+            st = quantize_act_launch(act, x, scratch, M, K, stream, true);
+            if (st != QMM_OK) return st;
+        }
+        if (!fused) st = matvec_group_dispatch(wt, G, W, N, yt, (const uint8_t*)scratch + t * xrb, K, stream, true);
+        if (st != QMM_OK) return st;
+    }
+    return QMM_OK;
+}
+
 }  // namespace qmm
 
 using namespace qmm;
 
 extern "C" {
 unsigned qmm_internal_matvec_error(int clear);
+
+qmm_status qmm_linear_group(int wtype, int G, const void* const* W, const int64_t* N, const float* x, void* xq_scratch,
+                            size_t scratch_bytes, float* const* y, int64_t M, int64_t K, qmm_stream_t stream) {
+    return linear_group(wtype, G, W, N, x, xq_scratch, scratch_bytes, y, M, K, (cudaStream_t)stream);
+}
 unsigned qmm_internal_matmul_error(int clear);
 
 size_t qmm_block_bytes(int type) { return block_bytes_of(type); }

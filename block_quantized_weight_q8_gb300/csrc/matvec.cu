@@ -30,6 +30,17 @@ static __device__ unsigned int g_matvec_error = 0;
 constexpr int kThreads = 256;  // blocksums kernel
 
 constexpr int kMaxWarps = 16;  // matvec CTA: up to 16 warps, each with its own ring
+constexpr int kMaxGroup = 8;   // weight matrices sharing one activation row in one launch
+
+// The matrices of one launch (all of one format and K): CTAs
+// [cta_end[g-1], cta_end[g]) own matrix g and split its N[g] rows evenly.
+struct MatSet {
+    const uint8_t* W[kMaxGroup];
+    float* y[kMaxGroup];
+    int N[kMaxGroup];
+    int cta_end[kMaxGroup];
+    int G;
+};
 
 struct MatvecPlan {
     bool su;              // decode whole super-units (Q8_0 / Q4_0 with K % 256 == 0)
@@ -139,10 +150,10 @@ __device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t g0, uint64
 // CTA 0 also stores the quantized row to xq_out when that is not null.  One
 // launch then does the whole quantize + multiply of a decode token.
 template <int WT, bool SU, bool FUSE, bool SPLIT>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t* __restrict__ W,
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_constant__ MatSet set,
                                                                   const uint8_t* __restrict__ xq,
                                                                   const float* __restrict__ x, uint8_t* xq_out,
-                                                                  float* __restrict__ y, int N, int K, int lpr,
+                                                                  int K, int lpr,
                                                                   int pieces, int piece_units, int item_segs,
                                                                   int depth, uint32_t slot_bytes, uint32_t part_off,
                                                                   uint32_t act_bytes, int pdl) {
@@ -151,6 +162,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nw = blockDim.x >> 5;
+    // this CTA's matrix, and its place among the CTAs of that matrix
+    int g = 0;
+    while (g + 1 < set.G && (int)blockIdx.x >= set.cta_end[g]) g++;
+    const int cta0 = g ? set.cta_end[g - 1] : 0;
+    const int ncta = set.cta_end[g] - cta0, bl = (int)blockIdx.x - cta0;
+    const uint8_t* __restrict__ W = set.W[g];
+    float* __restrict__ y = set.y[g];
+    const int N = set.N[g];
     // [barriers: nw * depth][activation][slots: nw * depth * slot_bytes]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem) + warp * depth;
     uint8_t* aq = smem + align_up(8u * nw * depth, 128u);
@@ -167,10 +186,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const uint8_t
     const uint64_t rb = (uint64_t)units * F::BB;
     if constexpr (!SPLIT) pieces = 1;
     const SegGeom<SPLIT> geo{rb, SU ? nsu : units, pieces, piece_units, SU ? (WT == QMM_Q4_0 ? 144 : 272) : F::BB};
-    // an even split of the rows: the first N % grid CTAs take one row more
-    const int rq = N / (int)gridDim.x, rr = N - rq * (int)gridDim.x;
-    const int r_begin = (int)blockIdx.x * rq + min((int)blockIdx.x, rr);
-    const int r_end = r_begin + rq + ((int)blockIdx.x < rr ? 1 : 0);
+    // an even split of the matrix's rows: its first N % ncta CTAs take one row more
+    const int rq = N / ncta, rr = N - rq * ncta;
+    const int r_begin = bl * rq + min(bl, rr);
+    const int r_end = r_begin + rq + (bl < rr ? 1 : 0);
     const int s_begin = r_begin * pieces, s_end = r_end * pieces;  // this CTA's segments
     const int nitems = (s_end - s_begin + item_segs - 1) / item_segs;
     const int my_items = nitems > warp ? (nitems - warp + nw - 1) / nw : 0;
@@ -403,15 +422,17 @@ __host__ inline uint32_t matvec_act_bytes(int wt, int act, int K, bool su) {
     return align_up((uint32_t)((wt == QMM_Q4_0 ? 288 : 272) * nsu + 8 * nd), 128u);
 }
 
-// Picks the launch shape for (format, N, K).  A row is cut into the fewest
-// segments that keep the most lanes busy (a segment of U units gets the
-// smallest power of two >= U lanes; at most 32).  Lanes per segment cover its
-// units (a pass = 32 / lpr segments); an item is one pass, or several when a
-// pass is under 4 KB.  Each warp keeps two items in flight when 12 or more warps
-// fit that way, else one item with 16 warps (more warps beat a deeper ring
-// there).  One CTA per SM.
+// Picks the launch shape for G matrices of one format and K (G = 1: a plain
+// matvec).  A row is cut into the fewest segments that keep the most lanes busy
+// (a segment of U units gets the smallest power of two >= U lanes; at most 32).
+// Lanes per segment cover its units (a pass = 32 / lpr segments); an item is
+// one pass, or several when a pass is under 4 KB.  The SMs are shared among the
+// matrices in proportion to their rows, one CTA per SM.  Each warp keeps two
+// items in flight when 12 or more warps fit that way, else one item with 16
+// warps (more warps beat a deeper ring there).
 template <int WT>
-static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, bool fuse, MatvecPlan* p) {
+static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceInfo& dev, bool fuse, MatvecPlan* p,
+                              int* cta_end) {
     using F = Fmt<WT>;
     p->su = (WT == QMM_Q8_0 || WT == QMM_Q4_0) && K % 256 == 0;
     const int nunit = p->su ? (int)(K / 256) : (int)(K / F::BV);
@@ -437,16 +458,46 @@ static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, bool 
     const uint64_t sb = align_up((uint32_t)(npass * pass_bytes + 32), 128u);
     if (sb > 0x7FFFFFFFull) return QMM_E_SHAPE;
     p->slot_bytes = (uint32_t)sb;
-    int64_t grid = dev.sms;
-    const int64_t items = (N * p->pieces + p->item_segs - 1) / p->item_segs;
-    if (grid > items) grid = items;
-    if (grid > N) grid = N;
-    if (grid < 1) grid = 1;
-    p->grid = (int)grid;
+
+    // CTAs per matrix: a share of the SMs proportional to its rows, at least one,
+    // at most one per item and per row
+    int64_t total_rows = 0, cap[kMaxGroup];
+    for (int g = 0; g < G; g++) {
+        total_rows += Ns[g];
+        cap[g] = (Ns[g] * p->pieces + p->item_segs - 1) / p->item_segs;
+        if (cap[g] > Ns[g]) cap[g] = Ns[g];
+    }
+    int grid[kMaxGroup];
+    int64_t sum = 0;
+    for (int g = 0; g < G; g++) {
+        int64_t c = (int64_t)((double)dev.sms * (double)Ns[g] / (double)total_rows + 0.5);
+        if (c < 1) c = 1;
+        if (c > cap[g]) c = cap[g];
+        grid[g] = (int)c;
+        sum += c;
+    }
+    // trim an overshoot from the largest shares (the SMs run one CTA each)
+    while (sum > dev.sms) {
+        int gm = -1;
+        for (int g = 0; g < G; g++)
+            if (grid[g] > 1 && (gm < 0 || grid[g] > grid[gm])) gm = g;
+        if (gm < 0) break;
+        grid[gm]--;
+        sum--;
+    }
+    uint64_t rows_max = 1;
+    int acc = 0;
+    for (int g = 0; g < G; g++) {
+        acc += grid[g];
+        cta_end[g] = acc;
+        const uint64_t r = (uint64_t)((Ns[g] + grid[g] - 1) / grid[g]);
+        if (r > rows_max) rows_max = r;
+    }
+    p->grid = acc;
+
     uint32_t act = matvec_act_bytes(WT, F::ACT, (int)K, p->su);
     // a fused Q8_K row is quantized into shared memory first (Q8_0 goes straight to its layout)
     if (fuse && F::ACT == QMM_Q8_K) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);
-    const uint64_t rows_max = (uint64_t)((N + grid - 1) / grid);
     const uint64_t part_bytes = p->pieces > 1 ? align_up((uint32_t)(rows_max * p->pieces * 4), 128u) : 0;
     const uint32_t bar_max = align_up(8u * kMaxWarps * 2, 128u);
     if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + part_bytes + sb) return QMM_E_SHAPE;
@@ -468,9 +519,8 @@ static qmm_status plan_matvec(int64_t N, int64_t K, const DeviceInfo& dev, bool 
 }
 
 template <int WT, bool SU, bool FUSE, bool SPLIT>
-static qmm_status launch_matvec_k(const void* W, const void* xq, const float* x, void* xq_out, float* y, int64_t N,
-                                   int64_t K, const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream,
-                                   bool pdl) {
+static qmm_status launch_matvec_k(const MatSet& set, const void* xq, const float* x, void* xq_out, int64_t K,
+                                   const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
     static bool attr_set[64] = {false};
     if (!attr_set[dev.device]) {
         if (cudaFuncSetAttribute(matvec_kernel<WT, SU, FUSE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -488,64 +538,83 @@ static qmm_status launch_matvec_k(const void* W, const void* xq, const float* x,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, SU, FUSE, SPLIT>, (const uint8_t*)W,
-                                             (const uint8_t*)xq, x, (uint8_t*)xq_out, y, (int)N, (int)K, p.lpr,
-                                             p.pieces, p.piece_units, p.item_segs, p.depth, p.slot_bytes, p.part_off,
-                                             p.act_bytes, pdl ? 1 : 0);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, matvec_kernel<WT, SU, FUSE, SPLIT>, set, (const uint8_t*)xq, x,
+                                             (uint8_t*)xq_out, (int)K, p.lpr, p.pieces, p.piece_units, p.item_segs,
+                                             p.depth, p.slot_bytes, p.part_off, p.act_bytes, pdl ? 1 : 0);
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
 template <int WT, bool SU, bool FUSE>
-static qmm_status launch_matvec_su(const void* W, const void* xq, const float* x, void* xq_out, float* y, int64_t N,
-                                   int64_t K, const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream,
-                                   bool pdl) {
-    if (p.pieces > 1) return launch_matvec_k<WT, SU, FUSE, true>(W, xq, x, xq_out, y, N, K, p, dev, stream, pdl);
-    return launch_matvec_k<WT, SU, FUSE, false>(W, xq, x, xq_out, y, N, K, p, dev, stream, pdl);
+static qmm_status launch_matvec_su(const MatSet& set, const void* xq, const float* x, void* xq_out, int64_t K,
+                                   const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
+    if (p.pieces > 1) return launch_matvec_k<WT, SU, FUSE, true>(set, xq, x, xq_out, K, p, dev, stream, pdl);
+    return launch_matvec_k<WT, SU, FUSE, false>(set, xq, x, xq_out, K, p, dev, stream, pdl);
 }
 
-// x == nullptr: multiply the quantized row xq.  Otherwise quantize x in the
-// kernel (xq then names where CTA 0 stores the quantized row, or is null).
+// G matrices W[g] (N[g] rows each) against one activation row.  x == nullptr:
+// multiply the quantized row xq.  Otherwise quantize x in the kernel (xq then
+// names where CTA 0 stores the quantized row, or is null).
 template <int WT>
-static qmm_status launch_matvec(const void* W, const void* xq, const float* x, float* y, int64_t N, int64_t K,
-                                cudaStream_t stream, bool pdl) {
+static qmm_status launch_matvec(const void* const* W, const int64_t* N, float* const* y, int G, const void* xq,
+                                const float* x, int64_t K, cudaStream_t stream, bool pdl) {
+    if (G < 1 || G > kMaxGroup) return QMM_E_SHAPE;
     DeviceInfo dev;
     qmm_status st = current_device(&dev);
     if (st != QMM_OK) return st;
     MatvecPlan p;
+    MatSet set = {};
     const bool fuse = x != nullptr;
-    st = plan_matvec<WT>(N, K, dev, fuse, &p);
+    st = plan_matvec<WT>(N, G, K, dev, fuse, &p, set.cta_end);
     if (st != QMM_OK) return st;
+    set.G = G;
+    for (int g = 0; g < G; g++) {
+        set.W[g] = (const uint8_t*)W[g];
+        set.y[g] = y[g];
+        set.N[g] = (int)N[g];
+    }
     if (fuse) {
         if constexpr (WT == QMM_Q8_0 || WT == QMM_Q4_0) {
-            if (p.su) return launch_matvec_su<WT, true, true>(W, nullptr, x, (void*)xq, y, N, K, p, dev, stream, pdl);
+            if (p.su) return launch_matvec_su<WT, true, true>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
         }
-        return launch_matvec_su<WT, false, true>(W, nullptr, x, (void*)xq, y, N, K, p, dev, stream, pdl);
+        return launch_matvec_su<WT, false, true>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
     }
     if constexpr (WT == QMM_Q8_0 || WT == QMM_Q4_0) {
-        if (p.su) return launch_matvec_su<WT, true, false>(W, xq, nullptr, nullptr, y, N, K, p, dev, stream, pdl);
+        if (p.su) return launch_matvec_su<WT, true, false>(set, xq, nullptr, nullptr, K, p, dev, stream, pdl);
     }
-    return launch_matvec_su<WT, false, false>(W, xq, nullptr, nullptr, y, N, K, p, dev, stream, pdl);
+    return launch_matvec_su<WT, false, false>(set, xq, nullptr, nullptr, K, p, dev, stream, pdl);
 }
 
 // Public calls require 16-byte aligned bases; internal per-token calls pass rows
 // of a larger buffer, which the kernel accepts at their natural alignment (W
 // 16 bytes for the bulk copies, an activation row 2 bytes, y 4 bytes; an f32
 // row x to quantize in the kernel 16 bytes).
-static qmm_status matvec_checked(int wt, const void* W, const void* xq, const float* x, float* y, int64_t N,
-                                 int64_t K, cudaStream_t stream, bool pdl, bool public_call) {
-    if (!W || (!xq && !x) || !y) return QMM_E_NULL;
-    qmm_status st = check_shape(wt, 1, N, K);
-    if (st != QMM_OK) return st;
-    if (public_call && (!aligned16(W) || !aligned16(xq) || !aligned16(y))) return QMM_E_ALIGN;
-    if (!aligned16(W) || ((uintptr_t)xq & 1u) || ((uintptr_t)y & 3u) || !aligned16(x)) return QMM_E_ALIGN;
+static qmm_status matvec_group_checked(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
+                                       const void* xq, const float* x, int64_t K, cudaStream_t stream, bool pdl,
+                                       bool public_call) {
+    if (G < 1 || G > kMaxGroup) return QMM_E_SHAPE;
+    if (!W || !N || !y || (!xq && !x)) return QMM_E_NULL;
+    for (int g = 0; g < G; g++) {
+        if (!W[g] || !y[g]) return QMM_E_NULL;
+        qmm_status st = check_shape(wt, 1, N[g], K);
+        if (st != QMM_OK) return st;
+        if (public_call && (!aligned16(W[g]) || !aligned16(y[g]))) return QMM_E_ALIGN;
+        if (!aligned16(W[g]) || ((uintptr_t)y[g] & 3u)) return QMM_E_ALIGN;
+    }
+    if (public_call && !aligned16(xq)) return QMM_E_ALIGN;
+    if (((uintptr_t)xq & 1u) || !aligned16(x)) return QMM_E_ALIGN;
     switch (wt) {
-    case QMM_Q4_0: return launch_matvec<QMM_Q4_0>(W, xq, x, y, N, K, stream, pdl);
-    case QMM_Q8_0: return launch_matvec<QMM_Q8_0>(W, xq, x, y, N, K, stream, pdl);
-    case QMM_Q4_K: return launch_matvec<QMM_Q4_K>(W, xq, x, y, N, K, stream, pdl);
-    case QMM_Q6_K: return launch_matvec<QMM_Q6_K>(W, xq, x, y, N, K, stream, pdl);
-    case QMM_Q2_K: return launch_matvec<QMM_Q2_K>(W, xq, x, y, N, K, stream, pdl);
+    case QMM_Q4_0: return launch_matvec<QMM_Q4_0>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q8_0: return launch_matvec<QMM_Q8_0>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q4_K: return launch_matvec<QMM_Q4_K>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q6_K: return launch_matvec<QMM_Q6_K>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q2_K: return launch_matvec<QMM_Q2_K>(W, N, y, G, xq, x, K, stream, pdl);
     default: return QMM_E_TYPE;
     }
+}
+
+static qmm_status matvec_checked(int wt, const void* W, const void* xq, const float* x, float* y, int64_t N,
+                                 int64_t K, cudaStream_t stream, bool pdl, bool public_call) {
+    return matvec_group_checked(wt, 1, &W, &N, &y, xq, x, K, stream, pdl, public_call);
 }
 
 qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
@@ -560,6 +629,19 @@ qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq
                                  cudaStream_t stream, bool pdl) {
     if (!x) return QMM_E_NULL;
     return matvec_checked(wt, W, xq_out, x, y, N, K, stream, pdl, false);
+}
+
+// The same for G matrices sharing the row (xq_out as above).
+qmm_status matvec_group_fused_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
+                                       const float* x, void* xq_out, int64_t K, cudaStream_t stream, bool pdl) {
+    if (!x) return QMM_E_NULL;
+    return matvec_group_checked(wt, G, W, N, y, xq_out, x, K, stream, pdl, false);
+}
+
+// G matrices against one quantized row (internal: alignment as for per-token rows).
+qmm_status matvec_group_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
+                                 const void* xq, int64_t K, cudaStream_t stream, bool pdl) {
+    return matvec_group_checked(wt, G, W, N, y, xq, nullptr, K, stream, pdl, false);
 }
 
 template <int WT>

@@ -160,7 +160,11 @@ QMM_API qmm_status qmm_matvec_q2_K(const void* W, const void* xq, float* y, int6
  * weight type in one place, so no caller can pair the wrong formats.  Quantizes
  * x (f32 [M][K]) into the caller's scratch (at least M * qmm_row_bytes(
  * qmm_act_type(wtype), K) bytes, 16-byte aligned), then computes y (f32 [M][N]).
- * With M = 1 the matvec starts streaming W while x is being quantized. */
+ * A token row is quantized inside the multiply kernel (every CTA quantizes the
+ * row it needs, with the same arithmetic as qmm_quantize_q8_0/q8_K, and one CTA
+ * stores it to the scratch), so a token is one launch; a row too large for that
+ * kernel's shared memory is quantized by the separate quantizer first.  Q4_0 with
+ * M >= 8 and K % 256 == 0 quantizes all rows, then runs the prefill matmul. */
 QMM_API qmm_status qmm_linear_q4_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
                            int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_linear_q8_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
@@ -193,6 +197,22 @@ QMM_API qmm_status qmm_linear_q2_K(const void* W, const float* x, void* xq_scrat
  * Errors as for qmm_linear_<wtype>, plus QMM_E_TYPE for a non-weight type. */
 QMM_API qmm_status qmm_linear_noalloc(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t N,
                                       int64_t K, qmm_stream_t stream);
+
+/* ---- several weight matrices on one input row, one launch per token ------ */
+/* No counterpart on the pages: an addition for the projections of a decoder
+ * layer that read the same input row (Q, K and V; gate and up).  For each of
+ * the G (1..8) matrices W[g] (N[g] rows of qmm_row_bytes(wtype, K) bytes; all of
+ * one weight type and K), y[g] (f32 [M][N[g]]) = the qmm_linear_<wtype> result
+ * for W[g], bit for bit.  W, N and y are HOST arrays of G entries (device
+ * pointers for W[g] and y[g]).  The SMs are shared among the matrices in
+ * proportion to their rows and each token row is quantized once per CTA, so the
+ * G products cost one launch per token instead of G.  Scratch as for
+ * qmm_linear_<wtype>: it receives the quantized rows.
+ * Errors as for qmm_linear_<wtype>; QMM_E_SHAPE also for G outside 1..8;
+ * QMM_E_TYPE for a non-weight type. */
+QMM_API qmm_status qmm_linear_group(int wtype, int G, const void* const* W, const int64_t* N, const float* x,
+                                    void* xq_scratch, size_t scratch_bytes, float* const* y, int64_t M, int64_t K,
+                                    qmm_stream_t stream);
 
 /* ---- prefill matmul, M tokens (hot path) -------------------------------- */
 /* Y[t][o] = sum_b d_w[o,b] * d_x[t,b] * isum[t,o,b] for M tokens at once: the

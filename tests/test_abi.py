@@ -113,6 +113,28 @@ def test_linear_rejects_bad_arguments(lib):
     assert g(A, A, A, 34 * 8 - 1, A, 1, 64, 256, None) == 5
 
 
+def test_linear_group_rejects_bad_arguments(lib):
+    import ctypes
+    f = lib.qmm_linear_group
+    W = (ctypes.c_void_p * 2)(A, A)
+    N = (ctypes.c_int64 * 2)(64, 32)
+    Y = (ctypes.c_void_p * 2)(A, A)
+    need = 2 * qmm.qmm_row_bytes("q8_K", 512)
+    args = lambda wt, G, w, n, y, sb, M, K: f(wt, G, ctypes.cast(w, ctypes.c_void_p), ctypes.cast(n, ctypes.c_void_p),
+                                               A, A, sb, ctypes.cast(y, ctypes.c_void_p), M, K, None)
+    assert args(qmm.QMM_Q4_K, 2, W, N, Y, need - 1, 2, 512) == 5          # scratch too small
+    assert args(qmm.QMM_Q4_K, 0, W, N, Y, need, 2, 512) == 2              # no matrices
+    assert args(qmm.QMM_Q4_K, 9, W, N, Y, need, 2, 512) == 2              # more than 8
+    assert args(qmm.QMM_Q8_K, 2, W, N, Y, need, 2, 512) == 3              # not a weight type
+    assert args(qmm.QMM_Q4_K, 2, W, N, Y, need, 2, 500) == 2              # K not a multiple of 256
+    Wn = (ctypes.c_void_p * 2)(A, None)
+    assert args(qmm.QMM_Q4_K, 2, Wn, N, Y, need, 2, 512) == 1             # a NULL matrix
+    Nz = (ctypes.c_int64 * 2)(64, 0)
+    assert args(qmm.QMM_Q4_K, 2, W, Nz, Y, need, 2, 512) == 2             # an empty matrix
+    Yu = (ctypes.c_void_p * 2)(A, U)
+    assert args(qmm.QMM_Q4_K, 2, W, N, Yu, need, 2, 512) == 4             # unaligned output
+
+
 def test_matmul_and_blocksums_reject_bad_arguments(lib):
     assert lib.qmm_matmul_q4_0(A, A, A, 0, 64, 256, None) == 2
     assert lib.qmm_matmul_q4_0(A, A, None, 4, 64, 256, None) == 1

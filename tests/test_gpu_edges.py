@@ -99,3 +99,30 @@ def test_linear_token_rows_of_odd_alignment():
     """Q8_0 rows of 34 * 3 bytes: token t's quantized row starts 2 bytes past a 16-byte boundary
     for odd t, so the in-kernel quantizer stores it with 16-bit writes."""
     check_matvec_and_linear("q8_0", 5, 67, 96, seed=95)
+
+
+@pytest.mark.parametrize("wtype,Ns,K,M", [("q4_K", (300, 77, 1024), 4096, 1), ("q4_K", (4096, 1024, 1024), 4096, 2),
+                                          ("q8_0", (129, 4096), 4096, 1), ("q4_0", (64, 33, 5, 700), 896, 3),
+                                          ("q6_K", (512, 257), 12288, 1), ("q2_K", (12288,), 4096, 1)])
+def test_linear_group_matches_oracle_and_linear(wtype, Ns, K, M):
+    """qmm_linear_group: every matrix's output equals the oracle within tolerance and qmm_linear_<w> on
+    that matrix alone bit for bit; the scratch holds the quantized rows."""
+    x = workloads.activations_f32(M, K, seed=100 + K)
+    X = oracle.quantize(act_name(wtype), x)
+    xrb = qmm.qmm_row_bytes(act_name(wtype), K)
+    Ws, refs = [], []
+    for g, N in enumerate(Ns):
+        W = oracle.quantize(wtype, workloads.weights_f32(N, K, seed=200 + g, row_jitter=True))
+        Ws.append(dev(W))
+        refs.append(oracle.matmul(wtype, W, X, M, N, K, nthreads=8))
+    ys = [torch.empty(M, N, dtype=torch.float32, device="cuda") for N in Ns]
+    scratch = torch.empty(M * xrb, dtype=torch.uint8, device="cuda")
+    xd = dev(x)
+    qmm.qmm_linear_group(wtype, Ws, Ns, xd, scratch, scratch.numel(), ys, M, K)
+    assert np.array_equal(host(scratch), X.reshape(-1))
+    for g, N in enumerate(Ns):
+        got = host(ys[g])
+        assert_rows_close(got, refs[g])
+        y1 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        qmm.linear(wtype, Ws[g], xd, scratch, scratch.numel(), y1, M, N, K)
+        assert np.array_equal(host(y1).view(np.uint32), got.view(np.uint32))
