@@ -451,8 +451,21 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
         for (label, wtype, N, K, W) in sets[i % C]:
             qmm.linear(wtype, W, xin[label], scratch, scratch.numel(), outs[label], 1, N, K, stream=sh)
 
+    # the same layer with the projections that read one row grouped: Q, K, V in one launch, gate and up
+    # in another (qmm_linear_group), Wo and W_down on their own
+    by = {m[0]: i for i, m in enumerate(mats)}
+
+    def layer_group(i):
+        s = sets[i % C]
+        for names, xin_ in ((("Wq", "Wk", "Wv"), xh), (("Wo",), xo), (("W_gate", "W_up"), xh), (("W_down",), xd)):
+            ms = [s[by[n]] for n in names]
+            K = ms[0][3]
+            qmm.qmm_linear_group(ms[0][1], [m[4] for m in ms], [m[2] for m in ms], xin_, scratch, scratch.numel(),
+                                 [outs[n] for n in names], 1, K, stream=sh)
+
     t_layer = timed_graph(layer, 8)
     t_lin = timed_graph(layer_linear, 8)
+    t_grp = timed_graph(layer_group, 8)
     res["q4_K_M_layer_4096"] = {"layer_us": round(t_layer * 1e6, 3), "GB/s": round(layer_bytes / t_layer / 1e9, 1),
                                 "frac_hbm": round(layer_bytes / t_layer / 1e9 / hbm, 4), "weight_bytes": layer_bytes,
                                 "equiv_tok_s_36_layers_matmuls_only": round(1.0 / (36 * t_layer), 1),
@@ -460,7 +473,12 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
                                 "how": "3 shared qmm_quantize_q8_K + 7 qmm_matvec",
                                 "linear_layer_us": round(t_lin * 1e6, 3),
                                 "linear_GB/s": round(layer_bytes / t_lin / 1e9, 1),
-                                "linear_launches_per_layer": 7}
+                                "linear_launches_per_layer": 7,
+                                "group_layer_us": round(t_grp * 1e6, 3),
+                                "group_GB/s": round(layer_bytes / t_grp / 1e9, 1),
+                                "group_frac_hbm": round(layer_bytes / t_grp / 1e9 / hbm, 4),
+                                "group_launches_per_layer": 4,
+                                "group_equiv_tok_s_36_layers_matmuls_only": round(1.0 / (36 * t_grp), 1)}
     del sets, mats
 
     # prefill

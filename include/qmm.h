@@ -202,8 +202,10 @@ QMM_API qmm_status qmm_linear_noalloc(int wtype, const void* W, const float* x, 
 /* No counterpart on the pages: an addition for the projections of a decoder
  * layer that read the same input row (Q, K and V; gate and up).  For each of
  * the G (1..8) matrices W[g] (N[g] rows of qmm_row_bytes(wtype, K) bytes; all of
- * one weight type and K), y[g] (f32 [M][N[g]]) = the qmm_linear_<wtype> result
- * for W[g], bit for bit.  W, N and y are HOST arrays of G entries (device
+ * one weight type and K), y[g] (f32 [M][N[g]]) holds for each token the result
+ * qmm_linear_<wtype> gives for that token alone (M = 1), bit for bit.  (With
+ * M >= 8, qmm_linear_q4_0 itself takes the prefill matmul, which adds in another
+ * order.)  W, N and y are HOST arrays of G entries (device
  * pointers for W[g] and y[g]).  The SMs are shared among the matrices in
  * proportion to their rows and each token row is quantized once per CTA, so the
  * G products cost one launch per token instead of G.  Scratch as for
