@@ -31,6 +31,7 @@ constexpr int kThreads = 256;  // blocksums kernel
 
 constexpr int kMaxWarps = 16;  // matvec CTA: up to 16 warps, each with its own ring
 constexpr int kMaxGroup = 8;   // weight matrices sharing one activation row in one launch
+constexpr uint64_t kSmallCtaBytes = 24 * 1024;  // weight bytes per CTA under which two CTAs share an SM
 
 // The matrices of one launch (all of one format and K): CTAs
 // [cta_end[g-1], cta_end[g]) own matrix g and split its N[g] rows evenly.
@@ -409,6 +410,10 @@ qmm_status current_device(DeviceInfo* info) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return QMM_E_CUDA;
         if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return QMM_E_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+            return QMM_E_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+            return QMM_E_CUDA;
         cache[dev] = d;
     }
     *info = cache[dev];
@@ -501,15 +506,31 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     const uint64_t part_bytes = p->pieces > 1 ? align_up((uint32_t)(rows_max * p->pieces * 4), 128u) : 0;
     const uint32_t bar_max = align_up(8u * kMaxWarps * 2, 128u);
     if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + part_bytes + sb) return QMM_E_SHAPE;
-    const uint64_t budget = (uint64_t)dev.max_smem_optin - bar_max - act - part_bytes;
+    // A CTA with little to stream (a small matrix) gets at most 8 warps and half
+    // an SM's shared memory: two CTAs then fit on an SM, so the CTAs of the next
+    // launch in a chain start while this launch's CTAs are still finishing.
+    uint64_t cta_bytes = 0;
+    for (int g = 0; g < G; g++) {
+        const uint64_t b = (uint64_t)((Ns[g] + grid[g] - 1) / grid[g]) * (uint64_t)(K / F::BV) * F::BB;
+        if (b > cta_bytes) cta_bytes = b;
+    }
+    uint64_t smem_cap = (uint64_t)dev.max_smem_optin;
+    int nw_cap = kMaxWarps;
+    const uint64_t half_sm = (uint64_t)dev.smem_per_sm / 2 - (uint64_t)dev.smem_reserved;
+    if (cta_bytes <= kSmallCtaBytes && half_sm >= (uint64_t)bar_max + act + part_bytes + 2 * sb &&
+        half_sm < smem_cap) {
+        smem_cap = half_sm;
+        nw_cap = kMaxWarps / 2;
+    }
+    const uint64_t budget = smem_cap - bar_max - act - part_bytes;
     int nw = (int)(budget / (2 * sb));
-    if (nw >= 12) {
+    if (nw >= 12 || (nw_cap < kMaxWarps && nw >= 1)) {
         p->depth = 2;
     } else {
         p->depth = 1;
         nw = (int)(budget / sb);
     }
-    if (nw > kMaxWarps) nw = kMaxWarps;
+    if (nw > nw_cap) nw = nw_cap;
     if (nw < 1) return QMM_E_SHAPE;
     p->nw = nw;
     p->part_off = align_up(8u * nw * p->depth, 128u) + act;
@@ -525,6 +546,10 @@ static qmm_status launch_matvec_k(const MatSet& set, const void* xq, const float
     if (!attr_set[dev.device]) {
         if (cudaFuncSetAttribute(matvec_kernel<WT, SU, FUSE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dev.max_smem_optin) != cudaSuccess)
+            return QMM_E_CUDA;
+        // all of the SM's unified memory as shared memory, so that two small CTAs fit
+        if (cudaFuncSetAttribute(matvec_kernel<WT, SU, FUSE, SPLIT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return QMM_E_CUDA;
         attr_set[dev.device] = true;
     }

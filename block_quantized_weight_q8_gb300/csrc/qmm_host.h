@@ -59,6 +59,8 @@ struct DeviceInfo {
     int device = -1;
     int sms = 0;
     int max_smem_optin = 0;
+    int smem_per_sm = 0;    // shared memory of one SM, all resident CTAs together
+    int smem_reserved = 0;  // shared memory the system keeps per resident CTA
 };
 
 // Properties of the current device (cached per device id).
