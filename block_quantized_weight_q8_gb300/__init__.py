@@ -46,6 +46,9 @@ SIGNATURES = {
     "qmm_linear_q6_K": ("pppspiiiq", ctypes.c_int),
     "qmm_linear_q2_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
+    "qmm_matmul_q4_K": ("pppiiiq", ctypes.c_int),
+    "qmm_matmul_q6_K": ("pppiiiq", ctypes.c_int),
+    "qmm_matmul_q2_K": ("pppiiiq", ctypes.c_int),
     "qmm_linear_noalloc": ("tpppiiiq", ctypes.c_int),
     "qmm_linear_group": ("ttppppspiiq", ctypes.c_int),
     "qmm_blocksums": ("tpppiiiq", ctypes.c_int),
@@ -221,6 +224,11 @@ def qmm_linear_group(wtype, Ws, Ns, x, scratch, scratch_bytes, ys, M, K, stream=
 
 def qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=None):
     _call("qmm_matmul_q4_0", ptr(W), ptr(xq), ptr(Y), int(M), int(N), int(K), stream_handle(stream))
+
+
+def matmul(wtype, W, xq, Y, M, N, K, stream=None):
+    """qmm_matmul_<wtype>: Y[M][N] for M quantized activation rows (Q8_0 for q4_0, Q8_K for the K-quants)."""
+    _call("qmm_matmul_" + wtype, ptr(W), ptr(xq), ptr(Y), int(M), int(N), int(K), stream_handle(stream))
 
 
 def qmm_blocksums(wtype, W, xq, s, M, N, K, stream=None):

@@ -8,6 +8,9 @@ namespace qmm {
 qmm_status quantize_act_launch(int act, const float* x, void* xq, int64_t M, int64_t K, cudaStream_t stream, bool pdl);
 qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
                            bool pdl);
+qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                            cudaStream_t stream, bool pdl);
+bool kq_uses_tensor_cores(int64_t M, int64_t K);
 qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq_out, float* y, int64_t N, int64_t K,
                                  cudaStream_t stream, bool pdl);
 qmm_status matvec_group_fused_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
@@ -33,6 +36,11 @@ static qmm_status linear(int wt, const void* W, const float* x, void* scratch, s
         st = quantize_act_launch(act, x, scratch, M, K, stream, true);
         if (st != QMM_OK) return st;
         return matmul_q4_0_launch(W, scratch, y, M, N, K, stream, true);
+    }
+    if (act == QMM_Q8_K && kq_uses_tensor_cores(M, K)) {  // K-quant prefill on the tensor cores
+        st = quantize_act_launch(act, x, scratch, M, K, stream, true);
+        if (st != QMM_OK) return st;
+        return matmul_kq_launch(wt, W, scratch, y, M, N, K, stream, true);
     }
     // one launch per token that quantizes its row and multiplies; a row too
     // large for that kernel's shared memory is quantized by its own kernel first
@@ -95,6 +103,7 @@ using namespace qmm;
 
 extern "C" {
 unsigned qmm_internal_matvec_error(int clear);
+unsigned qmm_internal_matmul_kq_error(int clear);
 
 qmm_status qmm_linear_group(int wtype, int G, const void* const* W, const int64_t* N, const float* x, void* xq_scratch,
                             size_t scratch_bytes, float* const* y, int64_t M, int64_t K, qmm_stream_t stream) {
@@ -144,7 +153,8 @@ qmm_status qmm_linear_q2_K(const void* W, const float* x, void* s, size_t sb, fl
 
 qmm_status qmm_device_status(int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return QMM_E_CUDA;
-    const unsigned e = qmm_internal_matvec_error(clear) | qmm_internal_matmul_error(clear);
+    const unsigned e =
+        qmm_internal_matvec_error(clear) | qmm_internal_matmul_error(clear) | qmm_internal_matmul_kq_error(clear);
     if (cudaGetLastError() != cudaSuccess) return QMM_E_CUDA;
     return e ? QMM_E_TIMEOUT : QMM_OK;
 }

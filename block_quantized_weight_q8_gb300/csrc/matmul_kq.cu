@@ -1,0 +1,711 @@
+// matmul_kq.cu -- the prefill matmul Y[M][N] for K-quant weights (Q4_K, Q2_K,
+// Q6_K) x Q8_K activations, M tokens at once, on the 5th-generation tensor cores.
+//
+// Per 256-value super-block the pages' K-quant dot is ([minfer] "10 . CPU
+// matmul: quantized weights x Q8_0 activations" s3.2, the K-quant dot walked;
+// [ggml] "ggml Q4_0 vec_dot Walkthrough" s1.2):
+//   value = sum_s sc_s * sum_{i in s} q_i a_i       (integer)
+//   min   = sum_g f_g * bsum_g                       (integer)
+//   y    += (d_w d_x) * value - (c_w d_x) * min
+// with, per format, f_g and c_w:
+//   Q4_K  (8 sub-blocks of 32, 6-bit sc/m)  f_g = m_{g/2},  c_w = dmin
+//   Q2_K  (16 groups of 16, 4-bit sc/m)     f_g = m_g,      c_w = dmin
+//   Q6_K  (16 groups of 16, int8 sc)        f_g = 32 sc_g,  c_w = d   (codes q in 0..63 stand for q - 32)
+// Both integers come out of tcgen05.mma .kind::f16 exactly: the weight operand
+// holds sc * q per element (Q4_K <= 63*15, Q2_K <= 15*3: exact fp16 integers;
+// Q6_K's sc*q reaches 127*63, so it goes in two exact parts, sc*(q & 7) and
+// 8*sc*(q >> 3)), the activation operand the int8 codes; the min term is one
+// more K = 16 MMA of f_g against the 16 group sums bsum_g (|bsum_g| <= 2048,
+// exact in fp16).  Each super-block's two sums land in TMEM and are folded into
+// fp32 registers once per super-block by d_w*d_x and c_w*d_x, in super-block
+// order, as the scalar kernel folds them.
+//
+// One CTA per tile of 128 weight rows x 128 tokens:
+//   warp 0    TMEM allocation; one thread issues, per 32-value block, the MMAs
+//             into the super-block's accumulator, and per super-block the min
+//             MMA into a second accumulator (2 super-blocks in flight, 512 columns)
+//   warps 1-4 weight converters, warps 5-8 activation converters: each thread
+//             owns one weight row / token, copies its super-block bytes into
+//             shared memory with 16-byte cp.async (chunk-major per thread, one
+//             super-block ahead), decodes them and writes fp16 operands in the
+//             UMMA K-major core-matrix layout, plus the min operands and scales
+//   warps 9-24 epilogue: per super-block tcgen05.ld of both sums, the fp32 fold,
+//             and at the end the token-major store
+// Shapes: K a multiple of 2048 (so that every row of W and of the activation is
+// a whole number of 16-byte chunks) and M >= 8; others run one matvec per token.
+// All waits are bounded; a timeout records QMM_E_TIMEOUT, every warp still
+// reaches the end, and TMEM is freed.
+#include "qmm_device.cuh"
+#include "qmm_host.h"
+#include "tc_device.cuh"
+
+namespace qmm {
+
+static __device__ unsigned int g_matmul_kq_error = 0;
+
+qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
+                           bool pdl);
+
+namespace kq {
+
+constexpr int BM = 128, BN = 128;
+constexpr int RAWX = 304;                 // a Q8_K super-block (292 B) as whole 16-byte chunks
+constexpr int NCX = RAWX / 16;            // 19
+constexpr int SC_SLOTS = 4;               // super-blocks of scales in flight
+constexpr int OP_BYTES = BM * 32 * 2;     // 8192: one 32-value block of one fp16 operand
+constexpr int MIN_BYTES = BM * 16 * 2;    // 4096: one 16-value min operand
+constexpr int NUM_CONV_WARPS = 8, NUM_EPI_WARPS = 16;
+constexpr int CONV0 = 1, EPI0 = CONV0 + NUM_CONV_WARPS;
+constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 800
+constexpr int TMEM_COLS = 512;            // 2 super-blocks x (value, min) x 128 columns
+
+template <int WT> struct Fmt;
+template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, RAWW = 144, SPLIT = 0, OP_SLOTS = 4; };
+template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, RAWW = 96, SPLIT = 0, OP_SLOTS = 4; };
+template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, RAWW = 224, SPLIT = 1, OP_SLOTS = 3; };
+
+template <int WT>
+struct Layout {
+    using F = Fmt<WT>;
+    static constexpr int NCW = F::RAWW / 16;
+    static constexpr int RAW_STAGE = BM * F::RAWW + BN * RAWX;
+    static constexpr int OFF_RAW = 0;                                          // 2 stages
+    static constexpr int OFF_OPA = OFF_RAW + 2 * RAW_STAGE;                    // A (Q6_K: sc*(q&7))
+    static constexpr int OFF_OPH = OFF_OPA + F::OP_SLOTS * OP_BYTES;           // Q6_K: 8*sc*(q>>3)
+    static constexpr int OFF_OPB = OFF_OPH + F::SPLIT * F::OP_SLOTS * OP_BYTES;  // activation codes
+    static constexpr int OFF_MINA = OFF_OPB + F::OP_SLOTS * OP_BYTES;          // 2 slots of f_g
+    static constexpr int OFF_MINB = OFF_MINA + 2 * MIN_BYTES;                  // 2 slots of bsum_g
+    static constexpr int OFF_SCD = OFF_MINB + 2 * MIN_BYTES;                   // d_w per row
+    static constexpr int OFF_SCC = OFF_SCD + SC_SLOTS * BM * 4;                // c_w per row
+    static constexpr int OFF_SCX = OFF_SCC + SC_SLOTS * BM * 4;                // d_x per token
+    static constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;
+    // op_full[S] mma_done[S] acc_full[2] acc_empty[2] sc_empty[SC_SLOTS]
+    static constexpr int NBARS = 2 * F::OP_SLOTS + 4 + SC_SLOTS;
+    static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+    static constexpr int SMEM = OFF_TMEM + 16;
+};
+static_assert(Layout<QMM_Q6_K>::SMEM <= 232448, "Q6_K layout exceeds shared memory");
+static_assert(Layout<QMM_Q4_K>::SMEM <= 232448, "Q4_K layout exceeds shared memory");
+
+template <int WT>
+struct Bars {
+    static constexpr int S = Fmt<WT>::OP_SLOTS;
+    uint32_t base;
+    __device__ uint32_t op_full(int i) const { return base + 8u * i; }
+    __device__ uint32_t op_empty(int i) const { return base + 8u * (S + i); }  // MMA of the slot's block done
+    __device__ uint32_t acc_full(int i) const { return base + 8u * (2 * S + i); }
+    __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * S + 2 + i); }
+    __device__ uint32_t sc_empty(int i) const { return base + 8u * (2 * S + 4 + i); }
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
+    atomicOr(&g_matmul_kq_error, kErrTimeout);
+    *abort_flag = 1;
+    return false;
+}
+
+// 16-byte global -> shared copy (both addresses 16-byte aligned), completing per thread
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Byte offset of element k (0..15) of row r in a 16-value K-major operand:
+// core matrix (r/8, k/8) at ((r/8)*2 + k/8)*128.
+__device__ __forceinline__ uint32_t min_off(int r, int kq) { return (uint32_t)(((r >> 3) * 2 + kq) * 128 + (r & 7) * 16); }
+
+// fp16 bits of small integers
+__device__ __forceinline__ uint32_t h2_of(int lo, int hi) {
+    const __half2 h = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// A thread's raw super-block in shared memory, chunk-major across the 128
+// threads of its role: chunk c at (c*128 + r)*16.  OFF is the (uniform) byte
+// offset of the super-block's first byte within chunk 0.
+struct Raw {
+    const uint8_t* p;  // this thread's chunk 0
+    __device__ __forceinline__ uint4 chunk(int c) const { return *reinterpret_cast<const uint4*>(p + c * 2048); }
+};
+__device__ __forceinline__ uint32_t comp(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+
+// NW little-endian words starting at super-block byte P (P + OFF even), from
+// chunks loaded here; all indices are compile-time after unrolling.
+template <int OFF, int P, int NW>
+__device__ __forceinline__ void words(const Raw& raw, uint32_t* out) {
+    constexpr int B0 = OFF + P;                 // raw byte of the first word
+    constexpr int A0 = B0 & ~3;                 // aligned word below it
+    constexpr int SH = (B0 & 3) * 8;            // 0 or 16
+    constexpr int NA = NW + (SH ? 1 : 0);       // aligned words needed
+    constexpr int C0 = A0 / 16, C1 = (A0 + 4 * NA - 1) / 16;
+    uint4 ch[C1 - C0 + 1];
+#pragma unroll
+    for (int c = C0; c <= C1; c++) ch[c - C0] = raw.chunk(c);
+    uint32_t a[NA];
+#pragma unroll
+    for (int i = 0; i < NA; i++) {
+        const int wb = A0 + 4 * i;
+        a[i] = comp(ch[wb / 16 - C0], (wb % 16) / 4);
+    }
+#pragma unroll
+    for (int i = 0; i < NW; i++) out[i] = SH ? __funnelshift_r(a[i], a[i + 1], SH) : a[i];
+}
+
+// 4 unsigned bytes of w (each < 1024) -> 2 fp16 pairs, times the fp16 pair s
+__device__ __forceinline__ void bytes4_to_h(uint32_t w, uint32_t s, uint32_t* h01, uint32_t* h23) {
+    const uint32_t m1024 = 0x64006400u;
+    *h01 = h2_mul(h2_sub(bytes_to_h2(w, 0x5140), m1024), s);
+    *h23 = h2_mul(h2_sub(bytes_to_h2(w, 0x7362), m1024), s);
+}
+// 8 words of unsigned byte codes (32 values of one block) times per-element fp16
+// scale pairs (s_lo for values 0..15, s_hi for 16..31) into the operand row r
+__device__ __forceinline__ void put_block(uint8_t* op, int r, const uint32_t* q, uint32_t s_lo, uint32_t s_hi) {
+#pragma unroll
+    for (int kq = 0; kq < 4; kq++) {  // values 8kq..8kq+7: words 2kq, 2kq+1
+        const uint32_t s = kq < 2 ? s_lo : s_hi;
+        uint4 v;
+        bytes4_to_h(q[2 * kq], s, &v.x, &v.y);
+        bytes4_to_h(q[2 * kq + 1], s, &v.z, &v.w);
+        *reinterpret_cast<uint4*>(op + op_off(r, kq)) = v;
+    }
+}
+// 16 fp16 values (as 8 pairs) into the min operand row r
+__device__ __forceinline__ void put_min(uint8_t* op, int r, const uint32_t* h) {
+    *reinterpret_cast<uint4*>(op + min_off(r, 0)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(op + min_off(r, 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+}
+__device__ __forceinline__ uint32_t hpair(int v) { return h2_of(v, v); }
+
+// ------------------------------------------------------------------ weight decoders
+// Per super-block header: the scale fields, decoded once.
+struct Hdr {
+    uint32_t d_bits, c_bits;  // f16 d and c_w (dmin, or d for Q6_K)
+    int sc[16];               // per group of 16 values (Q4_K: sub-block s -> groups 2s, 2s+1)
+    int f[16];                // the min operand f_g
+};
+
+// Q4_K: d@0, dmin@2, 12 bytes of 6-bit scales/mins @4 (GGUF packing, a reading), qs@16
+template <int OFF>
+__device__ __forceinline__ void hdr_q4_K(const Raw& raw, Hdr& h) {
+    uint32_t w[4];
+    words<OFF, 0, 4>(raw, w);
+    h.d_bits = w[0] & 0xFFFFu;
+    h.c_bits = w[0] >> 16;
+    const uint32_t sc_lo = w[1] & 0x3F3F3F3Fu, mn_lo = w[2] & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (w[3] & 0x0F0F0F0Fu) | ((w[1] >> 2) & 0x30303030u);
+    const uint32_t mn_hi = ((w[3] >> 4) & 0x0F0F0F0Fu) | ((w[2] >> 2) & 0x30303030u);
+#pragma unroll
+    for (int s = 0; s < 8; s++) {
+        const int sc = (int)byte_of(s < 4 ? sc_lo : sc_hi, s & 3), m = (int)byte_of(s < 4 ? mn_lo : mn_hi, s & 3);
+        h.sc[2 * s] = h.sc[2 * s + 1] = sc;
+        h.f[2 * s] = h.f[2 * s + 1] = m;
+    }
+}
+// block j = sub-block j: low (j even) or high (j odd) nibbles of qs[32(j/2) .. +32]
+template <int OFF>
+__device__ __forceinline__ void blk_q4_K(const Raw& raw, const Hdr& h, int j, uint8_t* opA, int r) {
+    uint32_t q[8];
+    switch (j >> 1) {
+    case 0: words<OFF, 16, 8>(raw, q); break;
+    case 1: words<OFF, 48, 8>(raw, q); break;
+    case 2: words<OFF, 80, 8>(raw, q); break;
+    default: words<OFF, 112, 8>(raw, q); break;
+    }
+    const int sh = (j & 1) * 4;
+#pragma unroll
+    for (int i = 0; i < 8; i++) q[i] = (q[i] >> sh) & 0x0F0F0F0Fu;
+    const uint32_t s = hpair(h.sc[2 * j]);
+    put_block(opA, r, q, s, s);
+}
+
+// Q2_K: scales[16]@0 (sc low nibble, m high), qs[64]@16, d@80, dmin@82;
+// value 128h + 32s + l is (qs[32h + l] >> 2s) & 3 (GGUF order, a reading)
+template <int OFF>
+__device__ __forceinline__ void hdr_q2_K(const Raw& raw, Hdr& h) {
+    uint32_t w[4], dd[1];
+    words<OFF, 0, 4>(raw, w);
+    words<OFF, 80, 1>(raw, dd);
+    h.d_bits = dd[0] & 0xFFFFu;
+    h.c_bits = dd[0] >> 16;
+#pragma unroll
+    for (int g = 0; g < 16; g++) {
+        const uint32_t b = byte_of(w[g >> 2], g & 3);
+        h.sc[g] = (int)(b & 15u);
+        h.f[g] = (int)(b >> 4);
+    }
+}
+template <int OFF>
+__device__ __forceinline__ void blk_q2_K(const Raw& raw, const Hdr& h, int j, uint8_t* opA, int r) {
+    uint32_t q[8];
+    if (j < 4) words<OFF, 16, 8>(raw, q);
+    else words<OFF, 48, 8>(raw, q);
+    const int sh = 2 * (j & 3);
+#pragma unroll
+    for (int i = 0; i < 8; i++) q[i] = (q[i] >> sh) & 0x03030303u;
+    put_block(opA, r, q, hpair(h.sc[2 * j]), hpair(h.sc[2 * j + 1]));
+}
+
+// Q6_K (GGUF layout, a reading): ql[128]@0, qh[64]@128, int8 scales[16]@192,
+// d@208; values 128n + l, +32, +64, +96 take their low 4 bits from ql[64n+l]&15,
+// ql[64n+l+32]&15, ql[64n+l]>>4, ql[64n+l+32]>>4 and their high 2 bits from
+// qh[32n+l] bits 0-1, 2-3, 4-5, 6-7.  Block j = 4n + part.
+template <int OFF>
+__device__ __forceinline__ void hdr_q6_K(const Raw& raw, Hdr& h) {
+    uint32_t w[4], dd[1];
+    words<OFF, 192, 4>(raw, w);
+    words<OFF, 206, 1>(raw, dd);  // bytes 206..209: d in the high half (no read past byte 209)
+    h.d_bits = dd[0] >> 16;
+    h.c_bits = h.d_bits;
+#pragma unroll
+    for (int g = 0; g < 16; g++) {
+        h.sc[g] = (int)(int8_t)byte_of(w[g >> 2], g & 3);
+        h.f[g] = 32 * h.sc[g];
+    }
+}
+template <int OFF>
+__device__ __forceinline__ void blk_q6_K(const Raw& raw, const Hdr& h, int j, uint8_t* opA, uint8_t* opH, int r) {
+    uint32_t ql[8], qh[8];
+    switch (j) {  // ql run: 64n + 32*(part & 1); qh run: 128 + 32n
+    case 0: case 2: words<OFF, 0, 8>(raw, ql); words<OFF, 128, 8>(raw, qh); break;
+    case 1: case 3: words<OFF, 32, 8>(raw, ql); words<OFF, 128, 8>(raw, qh); break;
+    case 4: case 6: words<OFF, 64, 8>(raw, ql); words<OFF, 160, 8>(raw, qh); break;
+    default: words<OFF, 96, 8>(raw, ql); words<OFF, 160, 8>(raw, qh); break;
+    }
+    const int part = j & 3;
+    const int lsh = (part >> 1) * 4, hsh = 2 * part;
+    uint32_t lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const uint32_t q = ((ql[i] >> lsh) & 0x0F0F0F0Fu) | (((qh[i] >> hsh) & 0x03030303u) << 4);  // 0..63
+        lo[i] = q & 0x07070707u;
+        hi[i] = (q >> 3) & 0x07070707u;
+    }
+    const int g0 = 2 * j, g1 = 2 * j + 1;
+    put_block(opA, r, lo, hpair(h.sc[g0]), hpair(h.sc[g1]));
+    put_block(opH, r, hi, hpair(8 * h.sc[g0]), hpair(8 * h.sc[g1]));
+}
+
+// ------------------------------------------------------------------ activation decoder
+// Q8_K: f32 d@0, int8 qs[256]@4, int16 bsums[16]@260
+template <int OFF>
+__device__ __forceinline__ void blk_x(const Raw& raw, int j, uint8_t* opB, int r) {
+    uint32_t q[8];
+    switch (j) {
+    case 0: words<OFF, 4, 8>(raw, q); break;
+    case 1: words<OFF, 36, 8>(raw, q); break;
+    case 2: words<OFF, 68, 8>(raw, q); break;
+    case 3: words<OFF, 100, 8>(raw, q); break;
+    case 4: words<OFF, 132, 8>(raw, q); break;
+    case 5: words<OFF, 164, 8>(raw, q); break;
+    case 6: words<OFF, 196, 8>(raw, q); break;
+    default: words<OFF, 228, 8>(raw, q); break;
+    }
+    const uint32_t m1152 = 0x64806480u;  // 1024 + (a + 128) - 1152 = a
+#pragma unroll
+    for (int kq = 0; kq < 4; kq++) {
+        const uint32_t w0 = q[2 * kq] ^ 0x80808080u, w1 = q[2 * kq + 1] ^ 0x80808080u;
+        uint4 v;
+        v.x = h2_sub(bytes_to_h2(w0, 0x5140), m1152);
+        v.y = h2_sub(bytes_to_h2(w0, 0x7362), m1152);
+        v.z = h2_sub(bytes_to_h2(w1, 0x5140), m1152);
+        v.w = h2_sub(bytes_to_h2(w1, 0x7362), m1152);
+        *reinterpret_cast<uint4*>(opB + op_off(r, kq)) = v;
+    }
+}
+template <int OFF>
+__device__ __forceinline__ void hdr_x(const Raw& raw, uint32_t* d_bits, uint32_t* bs /* 8 words */) {
+    uint32_t w[1];
+    words<OFF, 0, 1>(raw, w);
+    *d_bits = w[0];
+    words<OFF, 260, 8>(raw, bs);
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int WT>
+__global__ void __launch_bounds__(THREADS, 1)
+    matmul_kq_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq, float* __restrict__ Y, int M,
+                     int N, int K, int pdl) {
+    using F = Fmt<WT>;
+    using L = Layout<WT>;
+    constexpr int S = F::OP_SLOTS;
+    if (pdl) pdl_launch_dependents();
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = smem_u32(smem);
+    if (sbase & 127u) {  // operand tiles need 128-byte alignment
+        if (threadIdx.x == 0) atomicOr(&g_matmul_kq_error, kErrTimeout);
+        return;
+    }
+    const Bars<WT> bars{sbase + L::OFF_BAR};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_TMEM + 8);
+    float* scd = reinterpret_cast<float*>(smem + L::OFF_SCD);
+    float* scc = reinterpret_cast<float*>(smem + L::OFF_SCC);
+    float* scx = reinterpret_cast<float*>(smem + L::OFF_SCX);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o0 = blockIdx.x * BM, t0 = blockIdx.y * BN;
+    const int nsb = K / 256;
+    const uint64_t rb = (uint64_t)nsb * F::BB, xrb = (uint64_t)nsb * 292;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; i++) {
+            mbar_init(bars.op_full(i), NUM_CONV_WARPS);
+            mbar_init(bars.op_empty(i), 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(bars.acc_full(i), 1);
+            mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
+        }
+        for (int i = 0; i < SC_SLOTS; i++) mbar_init(bars.sc_empty(i), NUM_EPI_WARPS);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc_f16(BM, BN);
+            const uint64_t a0 = smem_desc(sbase + L::OFF_OPA, 128, 512);
+            const uint64_t h0 = smem_desc(sbase + L::OFF_OPH, 128, 512);
+            const uint64_t b0 = smem_desc(sbase + L::OFF_OPB, 128, 512);
+            const uint64_t ma0 = smem_desc(sbase + L::OFF_MINA, 128, 256);
+            const uint64_t mb0 = smem_desc(sbase + L::OFF_MINB, 128, 256);
+            for (int sb = 0; sb < nsb; sb++) {
+                const int as = sb & 1;
+                if (sb >= 2 && !wait_or_abort(bars.acc_empty(as), ((sb >> 1) - 1) & 1, abort_flag)) break;
+                const uint32_t dv = tmem + (uint32_t)(as * 128), dm = tmem + (uint32_t)(256 + as * 128);
+                bool ok = true;
+                for (int j = 0; j < 8; j++) {
+                    const int b = sb * 8 + j, os = b % S;
+                    if (!wait_or_abort(bars.op_full(os), (b / S) & 1, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t so = (uint64_t)(os * (OP_BYTES >> 4));
+                    mma_f16(dv, a0 + so, b0 + so, idesc, j > 0 ? 1u : 0u);
+                    mma_f16(dv, a0 + so + (256 >> 4), b0 + so + (256 >> 4), idesc, 1u);
+                    if (F::SPLIT) {
+                        mma_f16(dv, h0 + so, b0 + so, idesc, 1u);
+                        mma_f16(dv, h0 + so + (256 >> 4), b0 + so + (256 >> 4), idesc, 1u);
+                    }
+                    if (j == 7) {
+                        const uint64_t mo = (uint64_t)(as * (MIN_BYTES >> 4));
+                        mma_f16(dm, ma0 + mo, mb0 + mo, idesc, 0u);
+                    }
+                    mma_commit(bars.op_empty(os));
+                    if (j == 7) mma_commit(bars.acc_full(as));
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp < EPI0) {
+        // ------------------------------------------------------------ converters
+        const bool is_w = warp < CONV0 + NUM_CONV_WARPS / 2;
+        const int r = (warp - (is_w ? CONV0 : CONV0 + NUM_CONV_WARPS / 2)) * 32 + lane;  // row or token
+        const uint8_t* src;
+        if (is_w) {
+            src = W + (uint64_t)min(o0 + r, N - 1) * rb;
+        } else {
+            if (pdl) pdl_wait();  // the activation comes from the previous kernel
+            src = xq + (uint64_t)min(t0 + r, M - 1) * xrb;
+        }
+        const int BBs = is_w ? F::BB : 292, NC = is_w ? L::NCW : NCX;
+        const uint32_t raw_role = is_w ? 0u : (uint32_t)(BM * F::RAWW);
+        auto prefetch = [&](int sb) {
+            if (sb < nsb) {
+                const uint64_t a = ((uint64_t)sb * BBs) & ~15ull;
+                const uint32_t dst = sbase + L::OFF_RAW + (uint32_t)((sb & 1) * L::RAW_STAGE) + raw_role + (uint32_t)r * 16u;
+                for (int c = 0; c < NC; c++) cp_async16(dst + (uint32_t)c * 2048u, src + a + 16 * c);
+            }
+            cp_async_commit();  // possibly empty: one group per super-block keeps the count uniform
+        };
+        prefetch(0);
+        prefetch(1);
+        for (int sb = 0; sb < nsb; sb++) {
+            cp_async_wait<1>();  // this super-block's group is complete (the next may still fly)
+            const Raw raw{smem + L::OFF_RAW + (sb & 1) * L::RAW_STAGE + raw_role + r * 16};
+            const int off = (int)(((uint64_t)sb * BBs) & 15u);
+            const int ss = sb % SC_SLOTS, as = sb & 1;
+            if (sb >= SC_SLOTS && !wait_or_abort(bars.sc_empty(ss), ((sb / SC_SLOTS) - 1) & 1, abort_flag)) break;
+            Hdr h;
+            uint32_t xd = 0, bs[8];
+            if (is_w) {
+                if constexpr (WT == QMM_Q4_K) {
+                    hdr_q4_K<0>(raw, h);
+                } else if constexpr (WT == QMM_Q2_K) {
+                    switch (off) {
+                    case 0: hdr_q2_K<0>(raw, h); break;
+                    case 4: hdr_q2_K<4>(raw, h); break;
+                    case 8: hdr_q2_K<8>(raw, h); break;
+                    default: hdr_q2_K<12>(raw, h); break;
+                    }
+                } else {
+                    switch (off) {
+                    case 0: hdr_q6_K<0>(raw, h); break;
+                    case 2: hdr_q6_K<2>(raw, h); break;
+                    case 4: hdr_q6_K<4>(raw, h); break;
+                    case 6: hdr_q6_K<6>(raw, h); break;
+                    case 8: hdr_q6_K<8>(raw, h); break;
+                    case 10: hdr_q6_K<10>(raw, h); break;
+                    case 12: hdr_q6_K<12>(raw, h); break;
+                    default: hdr_q6_K<14>(raw, h); break;
+                    }
+                }
+                scd[ss * BM + r] = h2f(h.d_bits);
+                scc[ss * BM + r] = h2f(h.c_bits);
+            } else {
+                switch (off) {
+                case 0: hdr_x<0>(raw, &xd, bs); break;
+                case 4: hdr_x<4>(raw, &xd, bs); break;
+                case 8: hdr_x<8>(raw, &xd, bs); break;
+                default: hdr_x<12>(raw, &xd, bs); break;
+                }
+                scx[ss * BN + r] = __uint_as_float(xd);
+            }
+            bool ok = true;
+            for (int j = 0; j < 8; j++) {
+                const int b = sb * 8 + j, os = b % S;
+                if (b >= S && !wait_or_abort(bars.op_empty(os), ((b / S) - 1) & 1, abort_flag)) { ok = false; break; }
+                uint8_t* opA = smem + L::OFF_OPA + os * OP_BYTES;
+                if (is_w) {
+                    if constexpr (WT == QMM_Q4_K) {
+                        blk_q4_K<0>(raw, h, j, opA, r);
+                    } else if constexpr (WT == QMM_Q2_K) {
+                        switch (off) {
+                        case 0: blk_q2_K<0>(raw, h, j, opA, r); break;
+                        case 4: blk_q2_K<4>(raw, h, j, opA, r); break;
+                        case 8: blk_q2_K<8>(raw, h, j, opA, r); break;
+                        default: blk_q2_K<12>(raw, h, j, opA, r); break;
+                        }
+                    } else {
+                        uint8_t* opH = smem + L::OFF_OPH + os * OP_BYTES;
+                        switch (off) {
+                        case 0: blk_q6_K<0>(raw, h, j, opA, opH, r); break;
+                        case 2: blk_q6_K<2>(raw, h, j, opA, opH, r); break;
+                        case 4: blk_q6_K<4>(raw, h, j, opA, opH, r); break;
+                        case 6: blk_q6_K<6>(raw, h, j, opA, opH, r); break;
+                        case 8: blk_q6_K<8>(raw, h, j, opA, opH, r); break;
+                        case 10: blk_q6_K<10>(raw, h, j, opA, opH, r); break;
+                        case 12: blk_q6_K<12>(raw, h, j, opA, opH, r); break;
+                        default: blk_q6_K<14>(raw, h, j, opA, opH, r); break;
+                        }
+                    }
+                } else {
+                    uint8_t* opB = smem + L::OFF_OPB + os * OP_BYTES;
+                    switch (off) {
+                    case 0: blk_x<0>(raw, j, opB, r); break;
+                    case 4: blk_x<4>(raw, j, opB, r); break;
+                    case 8: blk_x<8>(raw, j, opB, r); break;
+                    default: blk_x<12>(raw, j, opB, r); break;
+                    }
+                }
+                if (j == 7) {
+                    // the min operands of this super-block; their slot was last read by
+                    // the min MMA of super-block sb - 2, complete once its acc_full fired
+                    if (sb >= 2 && !wait_or_abort(bars.acc_full(as), ((sb - 2) >> 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t hv[8];
+                    if (is_w) {
+#pragma unroll
+                        for (int i = 0; i < 8; i++) hv[i] = h2_of(h.f[2 * i], h.f[2 * i + 1]);
+                        put_min(smem + L::OFF_MINA + as * MIN_BYTES, r, hv);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; i++) hv[i] = h2_of((int)(int16_t)(bs[i] & 0xFFFFu), (int)(int16_t)(bs[i] >> 16));
+                        put_min(smem + L::OFF_MINB + as * MIN_BYTES, r, hv);
+                    }
+                }
+                fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.op_full(os));
+            }
+            if (!ok) break;
+            prefetch(sb + 2);  // this stage's bytes are all read
+        }
+        cp_async_wait<0>();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - EPI0;
+        const int quad = warp & 3, cg = e >> 2;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cg * 32);
+        uint64_t acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) acc[j] = 0;
+        for (int sb = 0; sb < nsb; sb++) {
+            const int as = sb & 1, ss = sb % SC_SLOTS;
+            if (!wait_or_abort(bars.acc_full(as), (sb >> 1) & 1, abort_flag)) break;
+            tc_fence_after();
+            const float dw = scd[ss * BM + row], cw = scc[ss * BM + row];
+            const uint64_t dw2 = f2_pack(__float_as_uint(dw), __float_as_uint(dw));
+            const uint64_t cw2 = f2_pack(__float_as_uint(-cw), __float_as_uint(-cw));
+            const uint64_t* dxs = reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                uint32_t v[16], m[16];
+                tmem_ld16(lane_base + (uint32_t)(as * 128 + 16 * hh), v);
+                tmem_ld16(lane_base + (uint32_t)(256 + as * 128 + 16 * hh), m);
+                tmem_ld_wait();
+                if (hh == 1) {  // both sums are in registers: the accumulators may be reused
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.acc_empty(as));
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) {
+                    const uint64_t dx = dxs[8 * hh + jj];
+                    if constexpr (WT == QMM_Q6_K) {
+                        // one scale for both sums: the exact integer value - 32*min first
+                        const float a0 = __uint_as_float(v[2 * jj]) - __uint_as_float(m[2 * jj]);
+                        const float a1 = __uint_as_float(v[2 * jj + 1]) - __uint_as_float(m[2 * jj + 1]);
+                        acc[8 * hh + jj] = f2_fma(f2_pack(__float_as_uint(a0), __float_as_uint(a1)), f2_mul(dw2, dx),
+                                                  acc[8 * hh + jj]);
+                    } else {
+                        // the pages' order: subtract the min term, then add the value term
+                        acc[8 * hh + jj] = f2_fma(f2_pack(m[2 * jj], m[2 * jj + 1]), f2_mul(cw2, dx), acc[8 * hh + jj]);
+                        acc[8 * hh + jj] = f2_fma(f2_pack(v[2 * jj], v[2 * jj + 1]), f2_mul(dw2, dx), acc[8 * hh + jj]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.sc_empty(ss));
+        }
+        if (pdl) pdl_wait();  // Y may be read or written by the previous kernel
+        const int o = o0 + row;
+        if (!*abort_flag && o < N) {
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                const int t = t0 + cg * 32 + j;
+                const uint32_t bits = (j & 1) ? (uint32_t)(acc[j >> 1] >> 32) : (uint32_t)acc[j >> 1];
+                if (t < M) Y[(size_t)t * N + o] = __uint_as_float(bits);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace kq
+}  // namespace qmm
+
+// ------------------------------------------------------------------ host side
+namespace qmm {
+
+// The tensor-core path needs every row of W and of the activation to be whole
+// 16-byte chunks (K a multiple of 2048) and enough tokens to fill a tile
+// reasonably; other shapes run one matvec per token.
+static bool kq_tensor_core_shape(int64_t M, int64_t K) { return K % 2048 == 0 && M >= 8; }
+
+template <int WT>
+static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                            cudaStream_t stream, bool pdl) {
+    using L = kq::Layout<WT>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMM_E_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kq::matmul_kq_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) !=
+            cudaSuccess)
+            return QMM_E_CUDA;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + kq::BM - 1) / kq::BM), (unsigned)((M + kq::BN - 1) / kq::BN));
+    cfg.blockDim = dim3(kq::THREADS);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kq::matmul_kq_kernel<WT>, (const uint8_t*)W, (const uint8_t*)xq, Y,
+                                             (int)M, (int)N, (int)K, pdl ? 1 : 0);
+    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
+
+// Y[M][N] for a K-quant W against M Q8_K rows (internal: arguments checked).
+qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                            cudaStream_t stream, bool pdl) {
+    if (!kq_tensor_core_shape(M, K)) {
+        const size_t xrb = row_bytes_of(QMM_Q8_K, K);
+        for (int64_t t = 0; t < M; t++) {
+            qmm_status st = matvec_dispatch(wt, W, (const uint8_t*)xq + t * xrb, Y + t * N, N, K, stream, pdl);
+            if (st != QMM_OK) return st;
+        }
+        return QMM_OK;
+    }
+    if ((N + kq::BM - 1) / kq::BM > 0x7FFFFFFF || (M + kq::BN - 1) / kq::BN > 65535) return QMM_E_SHAPE;
+    switch (wt) {
+    case QMM_Q4_K: return launch_kq<QMM_Q4_K>(W, xq, Y, M, N, K, stream, pdl);
+    case QMM_Q2_K: return launch_kq<QMM_Q2_K>(W, xq, Y, M, N, K, stream, pdl);
+    case QMM_Q6_K: return launch_kq<QMM_Q6_K>(W, xq, Y, M, N, K, stream, pdl);
+    default: return QMM_E_TYPE;
+    }
+}
+
+bool kq_uses_tensor_cores(int64_t M, int64_t K) { return kq_tensor_core_shape(M, K); }
+
+static qmm_status matmul_kq_checked(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                                    qmm_stream_t stream) {
+    if (!W || !xq || !Y) return QMM_E_NULL;
+    qmm_status st = check_shape(wt, M, N, K);
+    if (st != QMM_OK) return st;
+    if (!aligned16(W) || !aligned16(xq) || !aligned16(Y)) return QMM_E_ALIGN;
+    return matmul_kq_launch(wt, W, xq, Y, M, N, K, (cudaStream_t)stream, true);
+}
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+qmm_status qmm_matmul_q4_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_kq_checked(QMM_Q4_K, W, xq, Y, M, N, K, stream);
+}
+qmm_status qmm_matmul_q2_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_kq_checked(QMM_Q2_K, W, xq, Y, M, N, K, stream);
+}
+qmm_status qmm_matmul_q6_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_kq_checked(QMM_Q6_K, W, xq, Y, M, N, K, stream);
+}
+
+unsigned qmm_internal_matmul_kq_error(int clear) {
+    unsigned v = 0;
+    cudaMemcpyFromSymbol(&v, g_matmul_kq_error, sizeof(v));
+    if (clear) {
+        const unsigned z = 0;
+        cudaMemcpyToSymbol(g_matmul_kq_error, &z, sizeof(z));
+    }
+    return v;
+}
+
+}  // extern "C"

@@ -225,6 +225,22 @@ QMM_API qmm_status qmm_linear_group(int wtype, int G, const void* const* W, cons
  * W: N rows of Q4_0; xq: [M][K/32] Q8_0 blocks; Y: f32 [M][N]. */
 QMM_API qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream);
+/* The same for the K-quants against Q8_K rows ([minfer] s3.2, the K-quant dot
+ * walked; [ggml] s1.2).  Per 256-value super-block the integer value term
+ * (sum of sc * code dots, Q6_K in two exact parts) and the integer min term
+ * (f_g * bsum_g: Q4_K m_{g/2}, Q2_K m_g, Q6_K 32 sc_g) run on the tensor cores
+ * with integer-valued operands; each super-block then folds into fp32:
+ * y -= (dmin_w*d_x) * min; y += (d_w*d_x) * value (Q4_K, Q2_K), or
+ * y += (d_w*d_x) * (value - min) (Q6_K).  Results agree with the scalar order
+ * within 1e-5 of the row's L2 norm.  K a multiple of 2048 and M >= 8 take this
+ * path; other shapes run one matvec per token (same results as qmm_matvec).
+ * W: N rows of the format; xq: [M][K/256] Q8_K blocks; Y: f32 [M][N]. */
+QMM_API qmm_status qmm_matmul_q4_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream);
+QMM_API qmm_status qmm_matmul_q6_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream);
+QMM_API qmm_status qmm_matmul_q2_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream);
 
 /* ---- verification hooks (not on the hot path) --------------------------- */
 /* The exact int32 block sums the kernels fold, for bit-exact checking:

@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("qmm_quantize_q8_0", "qmm_quantize_q8_K", "qmm_matvec_q4_0", "qmm_matvec_q8_0",
-                 "qmm_matvec_q4_K", "qmm_matvec_q6_K", "qmm_matvec_q2_K", "qmm_matmul_q4_0",
+                 "qmm_matvec_q4_K", "qmm_matvec_q6_K", "qmm_matvec_q2_K", "qmm_matmul_q4_0", "qmm_matmul_q4_K",
+                 "qmm_matmul_q6_K", "qmm_matmul_q2_K",
                  "qmm_linear_q4_0", "qmm_blocksums", "qmm_status_str", "qmm_row_bytes"):
         assert want in names
     assert set(names) == set(qmm.SIGNATURES), set(names) ^ set(qmm.SIGNATURES)
@@ -140,6 +141,11 @@ def test_matmul_and_blocksums_reject_bad_arguments(lib):
     assert lib.qmm_matmul_q4_0(A, A, None, 4, 64, 256, None) == 1
     assert lib.qmm_matmul_q4_0(A, U, A, 4, 64, 256, None) == 4
     assert lib.qmm_matmul_q4_0(A, A, A, 4, 64, 48, None) == 2
+    for f in (lib.qmm_matmul_q4_K, lib.qmm_matmul_q6_K, lib.qmm_matmul_q2_K):
+        assert f(A, A, A, 0, 64, 2048, None) == 2
+        assert f(A, A, None, 8, 64, 2048, None) == 1
+        assert f(A, U, A, 8, 64, 2048, None) == 4
+        assert f(A, A, A, 8, 64, 1000, None) == 2
     assert lib.qmm_blocksums(7, A, A, A, 1, 1, 256, None) == 3
     assert lib.qmm_blocksums(qmm.QMM_Q8_K, A, A, A, 1, 1, 256, None) == 3   # not a weight type
     assert lib.qmm_blocksums(qmm.QMM_Q4_K, A, A, A, 1, 1, 128, None) == 2
