@@ -503,6 +503,24 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
         pre["M=%d" % M] = {"us": round(t * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
                            "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4),
                            "frac_hbm_weight_stream": round(W.numel() / t / 1e9 / hbm, 4)}
+    # the K-quant prefill at the decoder layer's shapes (M = 512): W_gate/W_up (Q4_K), W_down (Q6_K),
+    # and the Q2_K matrix
+    kq = {}
+    for wtype, Nk, Kk in (("q4_K", 12288, 4096), ("q6_K", 4096, 12288), ("q2_K", 12288, 4096)):
+        M = 512
+        Wk = quantized_weights(wtype, Nk, Kk, cfg["seed"])
+        xk = to_dev(workloads.activations_f32(M, Kk, cfg["seed"] + 3))
+        xqk = torch.empty(M * qmm.qmm_row_bytes("q8_K", Kk), dtype=torch.uint8, device=dev)
+        Yk = torch.empty(M, Nk, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            qmm.qmm_quantize_q8_K(xk, xqk, M, Kk, stream=sh)
+        tk = timed_graph(lambda i: qmm.matmul(wtype, Wk, xqk, Yk, M, Nk, Kk, stream=sh), 2)
+        tops = 2.0 * M * Nk * Kk / tk / 1e12
+        kq["%s_%dx%dx%d" % (wtype, M, Nk, Kk)] = {"us": round(tk * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
+                                                  "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4)}
+        del Wk, xk, xqk, Yk
+    pre["k_quants_M=512"] = kq
+
     # context: the GPU's own int8 and fp16 GEMMs (cuBLAS through torch) on the M=512 shape
     try:
         M = 512

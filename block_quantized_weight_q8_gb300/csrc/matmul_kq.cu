@@ -60,9 +60,11 @@ constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 800
 constexpr int TMEM_COLS = 512;            // 2 super-blocks x (value, min) x 128 columns
 
 template <int WT> struct Fmt;
-template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, RAWW = 144, SPLIT = 0, OP_SLOTS = 4; };
-template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, RAWW = 96, SPLIT = 0, OP_SLOTS = 4; };
-template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, RAWW = 224, SPLIT = 1, OP_SLOTS = 3; };
+// BB bytes per super-block, RAWW its 16-byte aligned superset, SPLIT: two
+// weight operands, OP_SLOTS blocks in flight, GROUP blocks converted together
+template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, RAWW = 144, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
+template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, RAWW = 96, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
+template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, RAWW = 224, SPLIT = 1, OP_SLOTS = 3, GROUP = 1; };
 
 template <int WT>
 struct Layout {
@@ -186,49 +188,50 @@ __device__ __forceinline__ void put_min(uint8_t* op, int r, const uint32_t* h) {
 __device__ __forceinline__ uint32_t hpair(int v) { return h2_of(v, v); }
 
 // ------------------------------------------------------------------ weight decoders
-// Per super-block header: the scale fields, decoded once.
+// Per super-block header, kept packed in registers (no arrays indexed at run
+// time): the f16 d and c_w, and four words of per-group scale bytes.
 struct Hdr {
     uint32_t d_bits, c_bits;  // f16 d and c_w (dmin, or d for Q6_K)
-    int sc[16];               // per group of 16 values (Q4_K: sub-block s -> groups 2s, 2s+1)
-    int f[16];                // the min operand f_g
+    uint32_t w0, w1, w2, w3;  // per format, see below
 };
+__device__ __forceinline__ uint32_t pick4(const Hdr& h, int i) { return i == 0 ? h.w0 : i == 1 ? h.w1 : i == 2 ? h.w2 : h.w3; }
 
-// Q4_K: d@0, dmin@2, 12 bytes of 6-bit scales/mins @4 (GGUF packing, a reading), qs@16
+// Q4_K: d@0, dmin@2, 12 bytes of 6-bit scales/mins @4 (GGUF packing, a reading), qs@16.
+// w0 = sc of sub-blocks 0..3, w1 = sc 4..7, w2 = m 0..3, w3 = m 4..7 (one byte each)
 template <int OFF>
 __device__ __forceinline__ void hdr_q4_K(const Raw& raw, Hdr& h) {
     uint32_t w[4];
     words<OFF, 0, 4>(raw, w);
     h.d_bits = w[0] & 0xFFFFu;
     h.c_bits = w[0] >> 16;
-    const uint32_t sc_lo = w[1] & 0x3F3F3F3Fu, mn_lo = w[2] & 0x3F3F3F3Fu;
-    const uint32_t sc_hi = (w[3] & 0x0F0F0F0Fu) | ((w[1] >> 2) & 0x30303030u);
-    const uint32_t mn_hi = ((w[3] >> 4) & 0x0F0F0F0Fu) | ((w[2] >> 2) & 0x30303030u);
-#pragma unroll
-    for (int s = 0; s < 8; s++) {
-        const int sc = (int)byte_of(s < 4 ? sc_lo : sc_hi, s & 3), m = (int)byte_of(s < 4 ? mn_lo : mn_hi, s & 3);
-        h.sc[2 * s] = h.sc[2 * s + 1] = sc;
-        h.f[2 * s] = h.f[2 * s + 1] = m;
-    }
+    h.w0 = w[1] & 0x3F3F3F3Fu;
+    h.w2 = w[2] & 0x3F3F3F3Fu;
+    h.w1 = (w[3] & 0x0F0F0F0Fu) | ((w[1] >> 2) & 0x30303030u);
+    h.w3 = ((w[3] >> 4) & 0x0F0F0F0Fu) | ((w[2] >> 2) & 0x30303030u);
 }
+__device__ __forceinline__ int sc_q4_K(const Hdr& h, int s) { return (int)byte_of(s < 4 ? h.w0 : h.w1, s & 3); }
+__device__ __forceinline__ int f_q4_K(const Hdr& h, int g) { return (int)byte_of((g >> 1) < 4 ? h.w2 : h.w3, (g >> 1) & 3); }
 // block j = sub-block j: low (j even) or high (j odd) nibbles of qs[32(j/2) .. +32]
 template <int OFF>
-__device__ __forceinline__ void blk_q4_K(const Raw& raw, const Hdr& h, int j, uint8_t* opA, int r) {
-    uint32_t q[8];
+__device__ __forceinline__ void ld_q4_K(const Raw& raw, int j, uint32_t* q) {
     switch (j >> 1) {
     case 0: words<OFF, 16, 8>(raw, q); break;
     case 1: words<OFF, 48, 8>(raw, q); break;
     case 2: words<OFF, 80, 8>(raw, q); break;
     default: words<OFF, 112, 8>(raw, q); break;
     }
+}
+__device__ __forceinline__ void st_q4_K(const Hdr& h, int j, uint32_t* q, uint8_t* opA, int r) {
     const int sh = (j & 1) * 4;
 #pragma unroll
     for (int i = 0; i < 8; i++) q[i] = (q[i] >> sh) & 0x0F0F0F0Fu;
-    const uint32_t s = hpair(h.sc[2 * j]);
+    const uint32_t s = hpair(sc_q4_K(h, j));
     put_block(opA, r, q, s, s);
 }
 
 // Q2_K: scales[16]@0 (sc low nibble, m high), qs[64]@16, d@80, dmin@82;
-// value 128h + 32s + l is (qs[32h + l] >> 2s) & 3 (GGUF order, a reading)
+// value 128h + 32s + l is (qs[32h + l] >> 2s) & 3 (GGUF order, a reading).
+// w0..w3 = the 16 scale bytes.
 template <int OFF>
 __device__ __forceinline__ void hdr_q2_K(const Raw& raw, Hdr& h) {
     uint32_t w[4], dd[1];
@@ -236,28 +239,27 @@ __device__ __forceinline__ void hdr_q2_K(const Raw& raw, Hdr& h) {
     words<OFF, 80, 1>(raw, dd);
     h.d_bits = dd[0] & 0xFFFFu;
     h.c_bits = dd[0] >> 16;
-#pragma unroll
-    for (int g = 0; g < 16; g++) {
-        const uint32_t b = byte_of(w[g >> 2], g & 3);
-        h.sc[g] = (int)(b & 15u);
-        h.f[g] = (int)(b >> 4);
-    }
+    h.w0 = w[0], h.w1 = w[1], h.w2 = w[2], h.w3 = w[3];
 }
+__device__ __forceinline__ int sc_q2_K(const Hdr& h, int g) { return (int)(byte_of(pick4(h, g >> 2), g & 3) & 15u); }
+__device__ __forceinline__ int f_q2_K(const Hdr& h, int g) { return (int)(byte_of(pick4(h, g >> 2), g & 3) >> 4); }
 template <int OFF>
-__device__ __forceinline__ void blk_q2_K(const Raw& raw, const Hdr& h, int j, uint8_t* opA, int r) {
-    uint32_t q[8];
+__device__ __forceinline__ void ld_q2_K(const Raw& raw, int j, uint32_t* q) {
     if (j < 4) words<OFF, 16, 8>(raw, q);
     else words<OFF, 48, 8>(raw, q);
+}
+__device__ __forceinline__ void st_q2_K(const Hdr& h, int j, uint32_t* q, uint8_t* opA, int r) {
     const int sh = 2 * (j & 3);
 #pragma unroll
     for (int i = 0; i < 8; i++) q[i] = (q[i] >> sh) & 0x03030303u;
-    put_block(opA, r, q, hpair(h.sc[2 * j]), hpair(h.sc[2 * j + 1]));
+    put_block(opA, r, q, hpair(sc_q2_K(h, 2 * j)), hpair(sc_q2_K(h, 2 * j + 1)));
 }
 
 // Q6_K (GGUF layout, a reading): ql[128]@0, qh[64]@128, int8 scales[16]@192,
 // d@208; values 128n + l, +32, +64, +96 take their low 4 bits from ql[64n+l]&15,
 // ql[64n+l+32]&15, ql[64n+l]>>4, ql[64n+l+32]>>4 and their high 2 bits from
-// qh[32n+l] bits 0-1, 2-3, 4-5, 6-7.  Block j = 4n + part.
+// qh[32n+l] bits 0-1, 2-3, 4-5, 6-7.  Block j = 4n + part.  w0..w3 = the 16
+// int8 scales.
 template <int OFF>
 __device__ __forceinline__ void hdr_q6_K(const Raw& raw, Hdr& h) {
     uint32_t w[4], dd[1];
@@ -265,21 +267,20 @@ __device__ __forceinline__ void hdr_q6_K(const Raw& raw, Hdr& h) {
     words<OFF, 206, 1>(raw, dd);  // bytes 206..209: d in the high half (no read past byte 209)
     h.d_bits = dd[0] >> 16;
     h.c_bits = h.d_bits;
-#pragma unroll
-    for (int g = 0; g < 16; g++) {
-        h.sc[g] = (int)(int8_t)byte_of(w[g >> 2], g & 3);
-        h.f[g] = 32 * h.sc[g];
-    }
+    h.w0 = w[0], h.w1 = w[1], h.w2 = w[2], h.w3 = w[3];
 }
+__device__ __forceinline__ int sc_q6_K(const Hdr& h, int g) { return (int)(int8_t)byte_of(pick4(h, g >> 2), g & 3); }
 template <int OFF>
-__device__ __forceinline__ void blk_q6_K(const Raw& raw, const Hdr& h, int j, uint8_t* opA, uint8_t* opH, int r) {
-    uint32_t ql[8], qh[8];
+__device__ __forceinline__ void ld_q6_K(const Raw& raw, int j, uint32_t* ql, uint32_t* qh) {
     switch (j) {  // ql run: 64n + 32*(part & 1); qh run: 128 + 32n
     case 0: case 2: words<OFF, 0, 8>(raw, ql); words<OFF, 128, 8>(raw, qh); break;
     case 1: case 3: words<OFF, 32, 8>(raw, ql); words<OFF, 128, 8>(raw, qh); break;
     case 4: case 6: words<OFF, 64, 8>(raw, ql); words<OFF, 160, 8>(raw, qh); break;
     default: words<OFF, 96, 8>(raw, ql); words<OFF, 160, 8>(raw, qh); break;
     }
+}
+__device__ __forceinline__ void st_q6_K(const Hdr& h, int j, const uint32_t* ql, const uint32_t* qh, uint8_t* opA,
+                                        uint8_t* opH, int r) {
     const int part = j & 3;
     const int lsh = (part >> 1) * 4, hsh = 2 * part;
     uint32_t lo[8], hi[8];
@@ -289,16 +290,26 @@ __device__ __forceinline__ void blk_q6_K(const Raw& raw, const Hdr& h, int j, ui
         lo[i] = q & 0x07070707u;
         hi[i] = (q >> 3) & 0x07070707u;
     }
-    const int g0 = 2 * j, g1 = 2 * j + 1;
-    put_block(opA, r, lo, hpair(h.sc[g0]), hpair(h.sc[g1]));
-    put_block(opH, r, hi, hpair(8 * h.sc[g0]), hpair(8 * h.sc[g1]));
+    const int s0 = sc_q6_K(h, 2 * j), s1 = sc_q6_K(h, 2 * j + 1);
+    put_block(opA, r, lo, hpair(s0), hpair(s1));
+    put_block(opH, r, hi, hpair(8 * s0), hpair(8 * s1));
+}
+
+// the min operand f_g of a weight row, as 8 fp16 pairs
+template <int WT>
+__device__ __forceinline__ void min_row(const Hdr& h, uint32_t* hv) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        if constexpr (WT == QMM_Q4_K) hv[i] = h2_of(f_q4_K(h, 2 * i), f_q4_K(h, 2 * i + 1));
+        else if constexpr (WT == QMM_Q2_K) hv[i] = h2_of(f_q2_K(h, 2 * i), f_q2_K(h, 2 * i + 1));
+        else hv[i] = h2_of(32 * sc_q6_K(h, 2 * i), 32 * sc_q6_K(h, 2 * i + 1));
+    }
 }
 
 // ------------------------------------------------------------------ activation decoder
 // Q8_K: f32 d@0, int8 qs[256]@4, int16 bsums[16]@260
 template <int OFF>
-__device__ __forceinline__ void blk_x(const Raw& raw, int j, uint8_t* opB, int r) {
-    uint32_t q[8];
+__device__ __forceinline__ void ld_x(const Raw& raw, int j, uint32_t* q) {
     switch (j) {
     case 0: words<OFF, 4, 8>(raw, q); break;
     case 1: words<OFF, 36, 8>(raw, q); break;
@@ -309,6 +320,8 @@ __device__ __forceinline__ void blk_x(const Raw& raw, int j, uint8_t* opB, int r
     case 6: words<OFF, 196, 8>(raw, q); break;
     default: words<OFF, 228, 8>(raw, q); break;
     }
+}
+__device__ __forceinline__ void st_x(const uint32_t* q, uint8_t* opB, int r) {
     const uint32_t m1152 = 0x64806480u;  // 1024 + (a + 128) - 1152 = a
 #pragma unroll
     for (int kq = 0; kq < 4; kq++) {
@@ -480,43 +493,74 @@ __global__ void __launch_bounds__(THREADS, 1)
                 scx[ss * BN + r] = __uint_as_float(xd);
             }
             bool ok = true;
-            for (int j = 0; j < 8; j++) {
-                const int b = sb * 8 + j, os = b % S;
-                if (b >= S && !wait_or_abort(bars.op_empty(os), ((b / S) - 1) & 1, abort_flag)) { ok = false; break; }
-                uint8_t* opA = smem + L::OFF_OPA + os * OP_BYTES;
+            // blocks in groups of G: all of a group's loads are issued before its
+            // stores, so the group's decode chains overlap
+            constexpr int G = F::GROUP;
+            for (int jg = 0; jg < 8; jg += G) {
+                int osl[G];
+#pragma unroll
+                for (int u = 0; u < G; u++) {
+                    const int b = sb * 8 + jg + u;
+                    osl[u] = b % S;
+                    if (b >= S && !wait_or_abort(bars.op_empty(osl[u]), ((b / S) - 1) & 1, abort_flag)) ok = false;
+                }
+                if (!ok) break;
                 if (is_w) {
-                    if constexpr (WT == QMM_Q4_K) {
-                        blk_q4_K<0>(raw, h, j, opA, r);
-                    } else if constexpr (WT == QMM_Q2_K) {
-                        switch (off) {
-                        case 0: blk_q2_K<0>(raw, h, j, opA, r); break;
-                        case 4: blk_q2_K<4>(raw, h, j, opA, r); break;
-                        case 8: blk_q2_K<8>(raw, h, j, opA, r); break;
-                        default: blk_q2_K<12>(raw, h, j, opA, r); break;
+                    if constexpr (WT == QMM_Q6_K) {
+                        uint32_t ql[G][8], qh[G][8];
+#pragma unroll
+                        for (int u = 0; u < G; u++) {
+                            switch (off) {
+                            case 0: ld_q6_K<0>(raw, jg + u, ql[u], qh[u]); break;
+                            case 2: ld_q6_K<2>(raw, jg + u, ql[u], qh[u]); break;
+                            case 4: ld_q6_K<4>(raw, jg + u, ql[u], qh[u]); break;
+                            case 6: ld_q6_K<6>(raw, jg + u, ql[u], qh[u]); break;
+                            case 8: ld_q6_K<8>(raw, jg + u, ql[u], qh[u]); break;
+                            case 10: ld_q6_K<10>(raw, jg + u, ql[u], qh[u]); break;
+                            case 12: ld_q6_K<12>(raw, jg + u, ql[u], qh[u]); break;
+                            default: ld_q6_K<14>(raw, jg + u, ql[u], qh[u]); break;
+                            }
                         }
+#pragma unroll
+                        for (int u = 0; u < G; u++)
+                            st_q6_K(h, jg + u, ql[u], qh[u], smem + L::OFF_OPA + osl[u] * OP_BYTES,
+                                    smem + L::OFF_OPH + osl[u] * OP_BYTES, r);
                     } else {
-                        uint8_t* opH = smem + L::OFF_OPH + os * OP_BYTES;
-                        switch (off) {
-                        case 0: blk_q6_K<0>(raw, h, j, opA, opH, r); break;
-                        case 2: blk_q6_K<2>(raw, h, j, opA, opH, r); break;
-                        case 4: blk_q6_K<4>(raw, h, j, opA, opH, r); break;
-                        case 6: blk_q6_K<6>(raw, h, j, opA, opH, r); break;
-                        case 8: blk_q6_K<8>(raw, h, j, opA, opH, r); break;
-                        case 10: blk_q6_K<10>(raw, h, j, opA, opH, r); break;
-                        case 12: blk_q6_K<12>(raw, h, j, opA, opH, r); break;
-                        default: blk_q6_K<14>(raw, h, j, opA, opH, r); break;
+                        uint32_t q[G][8];
+#pragma unroll
+                        for (int u = 0; u < G; u++) {
+                            if constexpr (WT == QMM_Q4_K) {
+                                ld_q4_K<0>(raw, jg + u, q[u]);
+                            } else {
+                                switch (off) {
+                                case 0: ld_q2_K<0>(raw, jg + u, q[u]); break;
+                                case 4: ld_q2_K<4>(raw, jg + u, q[u]); break;
+                                case 8: ld_q2_K<8>(raw, jg + u, q[u]); break;
+                                default: ld_q2_K<12>(raw, jg + u, q[u]); break;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < G; u++) {
+                            if constexpr (WT == QMM_Q4_K) st_q4_K(h, jg + u, q[u], smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
+                            else st_q2_K(h, jg + u, q[u], smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
                         }
                     }
                 } else {
-                    uint8_t* opB = smem + L::OFF_OPB + os * OP_BYTES;
-                    switch (off) {
-                    case 0: blk_x<0>(raw, j, opB, r); break;
-                    case 4: blk_x<4>(raw, j, opB, r); break;
-                    case 8: blk_x<8>(raw, j, opB, r); break;
-                    default: blk_x<12>(raw, j, opB, r); break;
+                    uint32_t q[G][8];
+#pragma unroll
+                    for (int u = 0; u < G; u++) {
+                        switch (off) {
+                        case 0: ld_x<0>(raw, jg + u, q[u]); break;
+                        case 4: ld_x<4>(raw, jg + u, q[u]); break;
+                        case 8: ld_x<8>(raw, jg + u, q[u]); break;
+                        default: ld_x<12>(raw, jg + u, q[u]); break;
+                        }
                     }
+#pragma unroll
+                    for (int u = 0; u < G; u++) st_x(q[u], smem + L::OFF_OPB + osl[u] * OP_BYTES, r);
                 }
-                if (j == 7) {
+                if (jg + G == 8) {
                     // the min operands of this super-block; their slot was last read by
                     // the min MMA of super-block sb - 2, complete once its acc_full fired
                     if (sb >= 2 && !wait_or_abort(bars.acc_full(as), ((sb - 2) >> 1) & 1, abort_flag)) {
@@ -525,8 +569,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     uint32_t hv[8];
                     if (is_w) {
-#pragma unroll
-                        for (int i = 0; i < 8; i++) hv[i] = h2_of(h.f[2 * i], h.f[2 * i + 1]);
+                        min_row<WT>(h, hv);
                         put_min(smem + L::OFF_MINA + as * MIN_BYTES, r, hv);
                     } else {
 #pragma unroll
@@ -536,7 +579,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bars.op_full(os));
+                if (lane == 0) {
+#pragma unroll
+                    for (int u = 0; u < G; u++) mbar_arrive(bars.op_full(osl[u]));
+                }
             }
             if (!ok) break;
             prefetch(sb + 2);  // this stage's bytes are all read
@@ -560,29 +606,29 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t cw2 = f2_pack(__float_as_uint(-cw), __float_as_uint(-cw));
             const uint64_t* dxs = reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
 #pragma unroll
-            for (int hh = 0; hh < 2; hh++) {
-                uint32_t v[16], m[16];
-                tmem_ld16(lane_base + (uint32_t)(as * 128 + 16 * hh), v);
-                tmem_ld16(lane_base + (uint32_t)(256 + as * 128 + 16 * hh), m);
+            for (int qq = 0; qq < 4; qq++) {  // 8 columns at a time
+                uint32_t v[8], m[8];
+                tmem_ld8(lane_base + (uint32_t)(as * 128 + 8 * qq), v);
+                tmem_ld8(lane_base + (uint32_t)(256 + as * 128 + 8 * qq), m);
                 tmem_ld_wait();
-                if (hh == 1) {  // both sums are in registers: the accumulators may be reused
+                if (qq == 3) {  // both sums are in registers: the accumulators may be reused
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bars.acc_empty(as));
                 }
 #pragma unroll
-                for (int jj = 0; jj < 8; jj++) {
-                    const uint64_t dx = dxs[8 * hh + jj];
+                for (int jj = 0; jj < 4; jj++) {
+                    const uint64_t dx = dxs[4 * qq + jj];
+                    uint64_t& a = acc[4 * qq + jj];
                     if constexpr (WT == QMM_Q6_K) {
                         // one scale for both sums: the exact integer value - 32*min first
                         const float a0 = __uint_as_float(v[2 * jj]) - __uint_as_float(m[2 * jj]);
                         const float a1 = __uint_as_float(v[2 * jj + 1]) - __uint_as_float(m[2 * jj + 1]);
-                        acc[8 * hh + jj] = f2_fma(f2_pack(__float_as_uint(a0), __float_as_uint(a1)), f2_mul(dw2, dx),
-                                                  acc[8 * hh + jj]);
+                        a = f2_fma(f2_pack(__float_as_uint(a0), __float_as_uint(a1)), f2_mul(dw2, dx), a);
                     } else {
                         // the pages' order: subtract the min term, then add the value term
-                        acc[8 * hh + jj] = f2_fma(f2_pack(m[2 * jj], m[2 * jj + 1]), f2_mul(cw2, dx), acc[8 * hh + jj]);
-                        acc[8 * hh + jj] = f2_fma(f2_pack(v[2 * jj], v[2 * jj + 1]), f2_mul(dw2, dx), acc[8 * hh + jj]);
+                        a = f2_fma(f2_pack(m[2 * jj], m[2 * jj + 1]), f2_mul(cw2, dx), a);
+                        a = f2_fma(f2_pack(v[2 * jj], v[2 * jj + 1]), f2_mul(dw2, dx), a);
                     }
                 }
             }

@@ -81,6 +81,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
         : "r"(taddr));
 }
 
+// 8 consecutive TMEM columns of this warp's 32 lanes into 8 registers.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* v) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr));
+}
+
 // fp16 bits of (1024 + byte) for two bytes picked by `sel` from x, next to 0x64.
 __device__ __forceinline__ uint32_t bytes_to_h2(uint32_t x, uint32_t sel) { return __byte_perm(x, 0x64646464u, sel); }
 __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
