@@ -46,6 +46,7 @@ SIGNATURES = {
     "qmm_linear_q6_K": ("pppspiiiq", ctypes.c_int),
     "qmm_linear_q2_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
+    "qmm_get_rows": ("tpppiiiq", ctypes.c_int),
     "qmm_matmul_q4_K": ("pppiiiq", ctypes.c_int),
     "qmm_matmul_q6_K": ("pppiiiq", ctypes.c_int),
     "qmm_matmul_q2_K": ("pppiiiq", ctypes.c_int),
@@ -229,6 +230,11 @@ def qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=None):
 def matmul(wtype, W, xq, Y, M, N, K, stream=None):
     """qmm_matmul_<wtype>: Y[M][N] for M quantized activation rows (Q8_0 for q4_0, Q8_K for the K-quants)."""
     _call("qmm_matmul_" + wtype, ptr(W), ptr(xq), ptr(Y), int(M), int(N), int(K), stream_handle(stream))
+
+
+def qmm_get_rows(wtype, W, ids, out, R, N, K, stream=None):
+    """out[r] = dequantized row ids[r] of W (ids: int32 device tensor)."""
+    _call("qmm_get_rows", _type(wtype), ptr(W), ptr(ids), ptr(out), int(R), int(N), int(K), stream_handle(stream))
 
 
 def qmm_blocksums(wtype, W, xq, s, M, N, K, stream=None):

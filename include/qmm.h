@@ -242,6 +242,18 @@ QMM_API qmm_status qmm_matmul_q6_K(const void* W, const void* xq, float* Y, int6
 QMM_API qmm_status qmm_matmul_q2_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream);
 
+/* ---- embedding lookup ----------------------------------------------------- */
+/* out[r][k] = value k of row ids[r] of W, dequantized ([minfer] s3.2, "The
+ * embedding 'matmul'": each token id's row walked block by block, scale x code).
+ * Each value is computed in f32 with at most one rounding (Q4_0 d*(n-8), Q8_0
+ * d*q, Q6_K (d*sc)*(q-32): exact; Q4_K and Q2_K fma(d*sc, q, -(dmin*m)): one
+ * rounding), so it equals the exact dequantized value rounded once to f32.
+ * W: N rows of wtype (a weight type); ids: int32 [R] device array; out: f32
+ * [R][K].  An id outside [0, N) gives a zero row and makes qmm_device_status()
+ * return QMM_E_SHAPE. */
+QMM_API qmm_status qmm_get_rows(int wtype, const void* W, const int32_t* ids, float* out, int64_t R, int64_t N,
+                                int64_t K, qmm_stream_t stream);
+
 /* ---- verification hooks (not on the hot path) --------------------------- */
 /* The exact int32 block sums the kernels fold, for bit-exact checking:
  * s[t][o][b] for every token t, row o and block b; Q4_0/Q8_0 give one int32 per

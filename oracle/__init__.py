@@ -144,6 +144,18 @@ def dequantize(t, q: np.ndarray, K: int) -> np.ndarray:
     return out
 
 
+def get_rows(t, W: np.ndarray, ids, K: int) -> np.ndarray:
+    """The embedding lookup ([minfer] s3.2, "The embedding 'matmul'"): for each token id, that row
+    of the quantized matrix dequantized block by block, exact (float64).  An id outside the matrix
+    is an error here; the device entry point writes a zero row and reports it."""
+    rb = row_bytes(t, K)
+    W = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1, rb)
+    ids = np.asarray(ids, dtype=np.int64)
+    if ids.size and (ids.min() < 0 or ids.max() >= W.shape[0]):
+        raise IndexError("token id outside the matrix")
+    return dequantize(t, W[ids], K)
+
+
 def codes(t, q: np.ndarray, K: int) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     rows = q.size // row_bytes(t, K)

@@ -136,6 +136,16 @@ def test_linear_group_rejects_bad_arguments(lib):
     assert args(qmm.QMM_Q4_K, 2, W, N, Yu, need, 2, 512) == 4             # unaligned output
 
 
+def test_get_rows_rejects_bad_arguments(lib):
+    f = lib.qmm_get_rows
+    assert f(qmm.QMM_Q8_K, A, A, A, 1, 4, 256, None) == 3     # not a weight type
+    assert f(qmm.QMM_Q4_0, None, A, A, 1, 4, 256, None) == 1
+    assert f(qmm.QMM_Q4_0, A, A, A, 0, 4, 256, None) == 2
+    assert f(qmm.QMM_Q4_K, A, A, A, 1, 4, 128, None) == 2
+    assert f(qmm.QMM_Q4_0, A, A + 2, A, 1, 4, 256, None) == 4  # ids not 4-byte aligned
+    assert f(qmm.QMM_Q4_0, A, A, U, 1, 4, 256, None) == 4
+
+
 def test_matmul_and_blocksums_reject_bad_arguments(lib):
     assert lib.qmm_matmul_q4_0(A, A, A, 0, 64, 256, None) == 2
     assert lib.qmm_matmul_q4_0(A, A, None, 4, 64, 256, None) == 1

@@ -3,7 +3,8 @@
 The largest K the library accepts (65536: every format's row is cut into segments whose
 partial sums meet in shared memory), rows whose last segment is short, rows whose blocks do
 not group into 16-byte aligned super-units, and the quantize-inside-the-matvec path of
-qmm_linear_* on all of these, with its stored activation row compared byte for byte."""
+qmm_linear_* on all of these, with its stored activation row compared byte for byte; the
+grouped linear; and the embedding lookup qmm_get_rows."""
 import numpy as np
 import pytest
 
@@ -126,3 +127,31 @@ def test_linear_group_matches_oracle_and_linear(wtype, Ns, K, M):
         y1 = torch.empty(M, N, dtype=torch.float32, device="cuda")
         qmm.linear(wtype, Ws[g], xd, scratch, scratch.numel(), y1, M, N, K)
         assert np.array_equal(host(y1).view(np.uint32), got.view(np.uint32))
+
+
+@pytest.mark.parametrize("wtype,N,K", [("q4_0", 300, 896), ("q8_0", 129, 4096), ("q4_K", 77, 4096), ("q6_K", 50, 12288),
+                                       ("q2_K", 33, 768)])
+def test_get_rows_bitexact(wtype, N, K):
+    """qmm_get_rows equals the oracle's exact dequantized rows rounded once to f32, bit for bit; ids repeat
+    and cover the first and last rows."""
+    W = oracle.quantize(wtype, workloads.weights_f32(N, K, seed=300 + N, row_jitter=True))
+    ids = np.array([0, N - 1, 5 % N, 5 % N, N // 2, 1 % N, N - 2], dtype=np.int32)
+    want = oracle.get_rows(wtype, W, ids, K).astype(np.float32)
+    out = torch.empty(len(ids), K, dtype=torch.float32, device="cuda")
+    qmm.qmm_get_rows(wtype, dev(W), dev(ids), out, len(ids), N, K)
+    got = host(out)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), np.argwhere(got != want)[:5].tolist()
+
+
+def test_get_rows_index_out_of_range_is_reported():
+    """An id outside [0, N) gives a zero row and QMM_E_SHAPE from qmm_device_status."""
+    N, K = 16, 256
+    W = oracle.quantize("q8_0", workloads.weights_f32(N, K, seed=9))
+    ids = np.array([3, N, -1], dtype=np.int32)
+    out = torch.full((3, K), 7.0, dtype=torch.float32, device="cuda")
+    assert qmm.qmm_device_status(clear=True) == 0
+    qmm.qmm_get_rows("q8_0", dev(W), dev(ids), out, 3, N, K)
+    got = host(out)
+    assert np.array_equal(got[0], oracle.get_rows("q8_0", W, [3], K)[0].astype(np.float32))
+    assert np.all(got[1:] == 0.0)
+    assert qmm.qmm_device_status(clear=True) == 2   # QMM_E_SHAPE

@@ -432,3 +432,19 @@ def test_token_major_output(orc):
     for t in range(M):
         yt = orc.matmul("q4_0", W, X[t:t + 1], 1, N, K)
         assert np.array_equal(y[t], yt[0])
+
+
+def test_get_rows_returns_the_rows_asked_for(orc):
+    """[minfer] s3.2, "The embedding 'matmul'": token id r reads row r.  Rows of integers with
+    |max| = 127 quantize to Q8_0 with d = 1 exactly, so each looked-up row is its source row, in
+    the order the ids give, repeats included."""
+    N, K = 9, 64
+    rng = np.random.default_rng(5)
+    w = rng.integers(-126, 127, size=(N, K)).astype(np.float32)
+    w[:, 0] = w[:, 32] = 127.0    # one 127 in each 32-value block
+    w[np.arange(N), 1 + np.arange(N)] = -100.0 - np.arange(N)   # every row distinct
+    W = orc.quantize("q8_0", w)
+    ids = [4, 0, 8, 4, 2]
+    assert np.array_equal(orc.get_rows("q8_0", W, ids, K), w[ids].astype(np.float64))
+    with pytest.raises(IndexError):
+        orc.get_rows("q8_0", W, [N], K)
