@@ -7,7 +7,7 @@ product: the two share no code.  The arithmetic lives in ``qmm_oracle.c`` (plain
 scalar C, -O2 -ffp-contract=off); this module only compiles it with gcc and
 marshals numpy arrays through ctypes.
 
-Type codes: 0 Q4_0, 1 Q8_0, 2 Q4_K, 3 Q6_K, 4 Q2_K, 5 Q8_K.
+Type codes: 0 Q4_0, 1 Q8_0, 2 Q4_K, 3 Q6_K, 4 Q2_K, 5 Q8_K, 6 Q4_1, 7 Q5_0, 8 Q5_1, 9 Q5_K.
 """
 from __future__ import annotations
 
@@ -22,8 +22,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "qmm_oracle.c")
 LIB = os.path.join(HERE, "_build", "liboracle.so")
 
-Q4_0, Q8_0, Q4_K, Q6_K, Q2_K, Q8_K = range(6)
-TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q2_K": Q2_K, "q8_K": Q8_K}
+Q4_0, Q8_0, Q4_K, Q6_K, Q2_K, Q8_K, Q4_1, Q5_0, Q5_1, Q5_K = range(10)
+TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "q4_K": Q4_K, "q6_K": Q6_K, "q2_K": Q2_K, "q8_K": Q8_K,
+         "q4_1": Q4_1, "q5_0": Q5_0, "q5_1": Q5_1, "q5_K": Q5_K}
 
 _lock = threading.Lock()
 _lib = None
@@ -54,7 +55,8 @@ def load(path: str):
     L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
     L.orc_f16_to_f32.restype = ctypes.c_float
     for name in ("orc_quantize_q8_0", "orc_quantize_q8_K", "orc_quantize_q4_0",
-                 "orc_quantize_q4_K", "orc_quantize_q6_K", "orc_quantize_q2_K"):
+                 "orc_quantize_q4_K", "orc_quantize_q6_K", "orc_quantize_q2_K", "orc_quantize_q4_1",
+                 "orc_quantize_q5_0", "orc_quantize_q5_1", "orc_quantize_q5_K"):
         getattr(L, name).argtypes = [p, p, i64]
         getattr(L, name).restype = None
     L.orc_dequantize.argtypes = [i32, p, p, i64]
@@ -130,7 +132,9 @@ def quantize(t, x: np.ndarray) -> np.ndarray:
         raise ValueError("K must be a multiple of the block size")
     out = np.zeros((rows, row_bytes(t, K)), dtype=np.uint8)
     fn = {Q8_0: "orc_quantize_q8_0", Q8_K: "orc_quantize_q8_K", Q4_0: "orc_quantize_q4_0",
-          Q4_K: "orc_quantize_q4_K", Q6_K: "orc_quantize_q6_K", Q2_K: "orc_quantize_q2_K"}[t]
+          Q4_K: "orc_quantize_q4_K", Q6_K: "orc_quantize_q6_K", Q2_K: "orc_quantize_q2_K",
+          Q4_1: "orc_quantize_q4_1", Q5_0: "orc_quantize_q5_0", Q5_1: "orc_quantize_q5_1",
+          Q5_K: "orc_quantize_q5_K"}[t]
     getattr(lib(), fn)(_ptr(x2), _ptr(out), rows * K)
     return out
 

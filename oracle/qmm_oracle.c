@@ -31,6 +31,12 @@
  *     min/max (Q4_K, Q2_K) and signed-extreme (Q6_K) schemes.  These are
  *     "parity unpinned" against any external source: they are pinned only by
  *     their encode/decode round trips and the brute-force dot products.
+ *   - Q4_1 (20 B), Q5_0 (22 B), Q5_1 (24 B) and Q5_K (176 B) follow the GGUF
+ *     byte layouts (the pages give the 22/24/176-B sizes and that Q5_0/Q5_1
+ *     add a plane of high bits).  Q4_1/Q5_0/Q5_1 pair with Q8_0 activations
+ *     like every 32-value type; their min term uses the exact integer sum of
+ *     the activation block's codes.  Their quantizers are the Q4_0 idea on 5
+ *     bits (Q5_0) and a plain min/max grid (Q4_1, Q5_1, and Q5_K as Q4_K).
  */
 #include <math.h>
 #include <pthread.h>
@@ -44,11 +50,18 @@
 #define ORC_Q6_K 3
 #define ORC_Q2_K 4
 #define ORC_Q8_K 5
+#define ORC_Q4_1 6
+#define ORC_Q5_0 7
+#define ORC_Q5_1 8
+#define ORC_Q5_K 9
 
 /* ------------------------------------------------------------------------- */
 /* Block sizes.  [minfer] s2.3 (block.rs constants: 18, 34, 144, 210);       */
 /* [ggml] s1.1 (block_q8_0 = 34 B, block_q4_0 = 18 B), s1.2 (block_q2_K =   */
 /* 84 B).  Q8_K is the 292-B f32-d layout (see the readings above).          */
+/* [minfer] s1 (the data-flow diagram: 18/22/24/34/144/176/210 B per block)  */
+/* and s3.2 (Q5_0/Q5_1 "22/24 B blocks", dot_q5_k_q8_k over 176-B rows).     */
+/* Q4_1's 20 B (f16 d, f16 m, 16 B of nibbles) is the GGUF layout.           */
 /* ------------------------------------------------------------------------- */
 int orc_block_bytes(int type) {
     switch (type) {
@@ -58,14 +71,18 @@ int orc_block_bytes(int type) {
     case ORC_Q6_K: return 128 + 64 + 16 + 2;
     case ORC_Q2_K: return 16 + 64 + 2 + 2;
     case ORC_Q8_K: return 4 + 256 + 2 * 16;
+    case ORC_Q4_1: return 2 + 2 + 16;
+    case ORC_Q5_0: return 2 + 4 + 16;
+    case ORC_Q5_1: return 2 + 2 + 4 + 16;
+    case ORC_Q5_K: return 2 + 2 + 12 + 32 + 128;
     default: return 0;
     }
 }
 
 int orc_block_values(int type) {
     switch (type) {
-    case ORC_Q4_0: case ORC_Q8_0: return 32;
-    case ORC_Q4_K: case ORC_Q6_K: case ORC_Q2_K: case ORC_Q8_K: return 256;
+    case ORC_Q4_0: case ORC_Q8_0: case ORC_Q4_1: case ORC_Q5_0: case ORC_Q5_1: return 32;
+    case ORC_Q4_K: case ORC_Q6_K: case ORC_Q2_K: case ORC_Q8_K: case ORC_Q5_K: return 256;
     default: return 0;
     }
 }
@@ -73,7 +90,7 @@ int orc_block_values(int type) {
 /* The activation format each weight type pairs with: [minfer] s2.4 and s3.2
  * (cpu_quant_matmul_f32): K-quant weights take Q8_K, all others Q8_0. */
 int orc_act_type(int wtype) {
-    return (wtype == ORC_Q4_K || wtype == ORC_Q6_K || wtype == ORC_Q2_K) ? ORC_Q8_K : ORC_Q8_0;
+    return (wtype == ORC_Q4_K || wtype == ORC_Q6_K || wtype == ORC_Q2_K || wtype == ORC_Q5_K) ? ORC_Q8_K : ORC_Q8_0;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -419,6 +436,149 @@ void orc_quantize_q6_K(const float* x, uint8_t* out, int64_t n) {
 }
 
 /* ------------------------------------------------------------------------- */
+/* 32-value formats with a min or a fifth bit ([minfer] s3.2: "Q5_0/Q5_1 add */
+/* their high-bit planes (22/24 B blocks)"; layouts are GGUF readings):      */
+/*   Q4_1  f16 d @0, f16 m @2, qs[16] @4        value d*q + m,   q in 0..15  */
+/*   Q5_0  f16 d @0, qh[4] @2, qs[16] @6        value d*(q-16),  q in 0..31  */
+/*   Q5_1  f16 d @0, f16 m @2, qh[4] @4, qs[16] @8   value d*q + m, 0..31    */
+/* Nibbles as in Q4_0 (byte j: element j low, j+16 high); bit i of the       */
+/* little-endian 32-bit qh is the fifth bit of element i.                    */
+/* ------------------------------------------------------------------------- */
+static void pack_nibbles(const uint8_t code[32], uint8_t* qs) {
+    for (int j = 0; j < 16; j++) qs[j] = (uint8_t)((code[j] & 15) | ((code[j + 16] & 15) << 4));
+}
+
+static void pack_high_bits(const uint8_t code[32], uint8_t* qh) {
+    uint32_t h = 0;
+    for (int i = 0; i < 32; i++) h |= (uint32_t)((code[i] >> 4) & 1) << i;
+    for (int k = 0; k < 4; k++) qh[k] = (uint8_t)(h >> (8 * k));
+}
+
+/* Reading: a min/max grid.  m = min x, d = (max x - m) / levels, and each code
+ * the nearest grid step (x - m)/d rounded half up, clamped to levels; computed
+ * with the f32 d and m, stored as f16. */
+static void quantize_minmax_32(const float* xb, int levels, float* d_out, float* m_out, uint8_t code[32]) {
+    float lo = xb[0], hi = xb[0];
+    for (int i = 1; i < 32; i++) {
+        if (xb[i] < lo) lo = xb[i];
+        if (xb[i] > hi) hi = xb[i];
+    }
+    float d = (hi - lo) / (float)levels;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    for (int i = 0; i < 32; i++) {
+        float t = (xb[i] - lo) * id + 0.5f;  /* >= 0.5, so truncation is floor */
+        code[i] = (uint8_t)clampi((int)t, 0, levels);
+    }
+    *d_out = d;
+    *m_out = lo;
+}
+
+void orc_quantize_q4_1(const float* x, uint8_t* out, int64_t n) {
+    for (int64_t b = 0; b < n / 32; b++) {
+        uint8_t* ob = out + b * 20;
+        float d, m;
+        uint8_t code[32];
+        quantize_minmax_32(x + b * 32, 15, &d, &m, code);
+        wr16(ob, orc_f32_to_f16(d));
+        wr16(ob + 2, orc_f32_to_f16(m));
+        pack_nibbles(code, ob + 4);
+    }
+}
+
+void orc_quantize_q5_1(const float* x, uint8_t* out, int64_t n) {
+    for (int64_t b = 0; b < n / 32; b++) {
+        uint8_t* ob = out + b * 24;
+        float d, m;
+        uint8_t code[32];
+        quantize_minmax_32(x + b * 32, 31, &d, &m, code);
+        wr16(ob, orc_f32_to_f16(d));
+        wr16(ob + 2, orc_f32_to_f16(m));
+        pack_high_bits(code, ob + 4);
+        pack_nibbles(code, ob + 8);
+    }
+}
+
+/* Reading: the Q4_0 scheme on 5 bits.  m = the value of largest magnitude (the
+ * first on a tie), d = m / -16, codes min(31, trunc(x/d + 16.5)). */
+void orc_quantize_q5_0(const float* x, uint8_t* out, int64_t n) {
+    for (int64_t b = 0; b < n / 32; b++) {
+        const float* xb = x + b * 32;
+        uint8_t* ob = out + b * 22;
+        float amax = 0.0f, m = 0.0f;
+        for (int i = 0; i < 32; i++) {
+            if (fabsf(xb[i]) > amax) { amax = fabsf(xb[i]); m = xb[i]; }
+        }
+        float d = m / -16.0f;
+        float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+        wr16(ob, orc_f32_to_f16(d));
+        uint8_t code[32];
+        for (int i = 0; i < 32; i++) {
+            float t = xb[i] * id + 16.5f;
+            code[i] = (uint8_t)clampi((int)t, 0, 31);
+        }
+        pack_high_bits(code, ob + 2);
+        pack_nibbles(code, ob + 6);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Q5_K: 176 B per 256 values ([minfer] s1 and s3.2 give the size and the    */
+/* dot_q5_k_q8_k arm).  Reading, GGUF layout: f16 d @0, f16 dmin @2, the     */
+/* Q4_K 12-byte scale/min packing @4, qh[32] @16, qs[128] @48.  For chunk j  */
+/* = 0..3 and lane l: element 64j+l has low nibble qs[32j+l] & 15 and fifth  */
+/* bit (qh[l] >> 2j) & 1; element 64j+32+l has qs[32j+l] >> 4 and bit 2j+1.  */
+/* A weight decodes as d*sc_s*q - dmin*m_s.  Quantizer: the Q4_K scheme with */
+/* codes 0..31.                                                              */
+/* ------------------------------------------------------------------------- */
+void orc_quantize_q5_K(const float* x, uint8_t* out, int64_t n) {
+    for (int64_t b = 0; b < n / 256; b++) {
+        const float* xb = x + b * 256;
+        uint8_t* ob = out + b * 176;
+        float scl[8], mns[8];
+        float maxscl = 0.0f, maxmin = 0.0f;
+        for (int s = 0; s < 8; s++) {
+            float lo = xb[32 * s], hi = xb[32 * s];
+            for (int i = 1; i < 32; i++) {
+                float v = xb[32 * s + i];
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+            }
+            mns[s] = lo < 0.0f ? -lo : 0.0f;
+            scl[s] = (hi + mns[s]) / 31.0f;
+            if (scl[s] > maxscl) maxscl = scl[s];
+            if (mns[s] > maxmin) maxmin = mns[s];
+        }
+        float d = maxscl / 63.0f, dmin = maxmin / 63.0f;
+        uint16_t dh = orc_f32_to_f16(d), dmh = orc_f32_to_f16(dmin);
+        wr16(ob, dh);
+        wr16(ob + 2, dmh);
+        int sc[8], mn[8];
+        for (int s = 0; s < 8; s++) {
+            sc[s] = d > 0.0f ? clampi(rne(scl[s] / d), 0, 63) : 0;
+            mn[s] = dmin > 0.0f ? clampi(rne(mns[s] / dmin), 0, 63) : 0;
+        }
+        q4_K_pack_scales(sc, mn, ob + 4);
+        float df = orc_f16_to_f32(dh), dmf = orc_f16_to_f32(dmh);
+        uint8_t q[256];
+        for (int s = 0; s < 8; s++) {
+            float ds = df * (float)sc[s];
+            float dm = dmf * (float)mn[s];
+            for (int i = 0; i < 32; i++) {
+                float v = xb[32 * s + i];
+                q[32 * s + i] = (uint8_t)(ds > 0.0f ? clampi(rne((v + dm) / ds), 0, 31) : 0);
+            }
+        }
+        memset(ob + 16, 0, 32);
+        for (int j = 0; j < 4; j++)
+            for (int l = 0; l < 32; l++) {
+                int lo = q[64 * j + l], hi = q[64 * j + 32 + l];
+                ob[48 + 32 * j + l] = (uint8_t)((lo & 15) | ((hi & 15) << 4));
+                ob[16 + l] |= (uint8_t)(((lo >> 4) << (2 * j)) | ((hi >> 4) << (2 * j + 1)));
+            }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Decoding a block to its integer codes (and scale factors).  These are the */
 /* per-format decode formulas above, read back out of the bytes.             */
 /* ------------------------------------------------------------------------- */
@@ -439,6 +599,24 @@ static int q4_K_code(const uint8_t* blk, int e) {   /* 0..15 */
 static int q2_K_code(const uint8_t* blk, int e) {   /* 0..3 */
     int h = e / 128, s = (e % 128) / 32, l = e % 32;
     return (blk[16 + 32 * h + l] >> (2 * s)) & 3;
+}
+
+/* the stored 4-bit code of element i of a 32-value block whose nibbles start at qs */
+static int nibble_code(const uint8_t* qs, int i) { return i < 16 ? (qs[i] & 0x0F) : (qs[i - 16] >> 4); }
+
+/* the fifth bit of element i: bit i of the little-endian 32-bit word at qh */
+static int fifth_bit(const uint8_t* qh, int i) { return (qh[i / 8] >> (i % 8)) & 1; }
+
+static int q4_1_code(const uint8_t* blk, int i) { return nibble_code(blk + 4, i); }                           /* 0..15 */
+static int q5_0_code(const uint8_t* blk, int i) { return nibble_code(blk + 6, i) | (fifth_bit(blk + 2, i) << 4); } /* 0..31 */
+static int q5_1_code(const uint8_t* blk, int i) { return nibble_code(blk + 8, i) | (fifth_bit(blk + 4, i) << 4); } /* 0..31 */
+
+static int q5_K_code(const uint8_t* blk, int e) {   /* 0..31 */
+    int j = e / 64, r = e % 64, l = r % 32;
+    uint8_t byte = blk[48 + 32 * j + l];
+    int low = r < 32 ? (byte & 0x0F) : (byte >> 4);
+    int high = (blk[16 + l] >> (2 * j + (r >= 32))) & 1;
+    return low | (high << 4);
 }
 
 static int q6_K_code(const uint8_t* blk, int e) {   /* 0..63 (stored code, before -32) */
@@ -495,13 +673,32 @@ void orc_dequantize(int type, const uint8_t* in, double* out, int64_t n) {
             for (int e = 0; e < 256; e++)
                 o[e] = d * (int8_t)blk[192 + e / 16] * (q6_K_code(blk, e) - 32);
         } break;
+        case ORC_Q4_1: {
+            double d = orc_f16_to_f32(rd16(blk)), m = orc_f16_to_f32(rd16(blk + 2));
+            for (int i = 0; i < 32; i++) o[i] = d * q4_1_code(blk, i) + m;
+        } break;
+        case ORC_Q5_0: {
+            double d = orc_f16_to_f32(rd16(blk));
+            for (int i = 0; i < 32; i++) o[i] = d * (q5_0_code(blk, i) - 16);
+        } break;
+        case ORC_Q5_1: {
+            double d = orc_f16_to_f32(rd16(blk)), m = orc_f16_to_f32(rd16(blk + 2));
+            for (int i = 0; i < 32; i++) o[i] = d * q5_1_code(blk, i) + m;
+        } break;
+        case ORC_Q5_K: {
+            double d = orc_f16_to_f32(rd16(blk)), dmin = orc_f16_to_f32(rd16(blk + 2));
+            int sc[8], mn[8];
+            orc_q4_K_unpack_scales(blk + 4, sc, mn);
+            for (int e = 0; e < 256; e++) o[e] = d * sc[e / 32] * q5_K_code(blk, e) - dmin * mn[e / 32];
+        } break;
         default: break;
         }
     }
 }
 
 /* Raw integer codes (test helper): the value each element's code stands for
- * before scaling: Q4_0 q-8, Q8_0/Q8_K q, Q4_K/Q2_K q, Q6_K q-32. */
+ * before scaling: Q4_0 q-8, Q8_0/Q8_K q, Q4_K/Q2_K q, Q6_K q-32, Q4_1/Q5_1/Q5_K q
+ * (their min is added, or subtracted, separately), Q5_0 q-16. */
 void orc_codes(int type, const uint8_t* in, int32_t* out, int64_t n) {
     int bv = orc_block_values(type), bb = orc_block_bytes(type);
     for (int64_t b = 0; b < n / bv; b++) {
@@ -515,6 +712,10 @@ void orc_codes(int type, const uint8_t* in, int32_t* out, int64_t n) {
             case ORC_Q4_K: o[e] = q4_K_code(blk, e); break;
             case ORC_Q2_K: o[e] = q2_K_code(blk, e); break;
             case ORC_Q6_K: o[e] = q6_K_code(blk, e) - 32; break;
+            case ORC_Q4_1: o[e] = q4_1_code(blk, e); break;
+            case ORC_Q5_0: o[e] = q5_0_code(blk, e) - 16; break;
+            case ORC_Q5_1: o[e] = q5_1_code(blk, e); break;
+            case ORC_Q5_K: o[e] = q5_K_code(blk, e); break;
             default: o[e] = 0;
             }
         }
@@ -531,7 +732,17 @@ void orc_codes(int type, const uint8_t* in, int32_t* out, int64_t n) {
 /*   Q2_K  value = sum_g sc_g * sum_{i in g} q_i*a_i,  min = sum_g m_g*bsum_g */
 /*   Q6_K  value = sum_g sc_g * sum_{i in g} q_i*a_i (q the stored 0..63),   */
 /*         min   = sum_g sc_g * bsum_g; the dot's integer is value - 32*min.  */
+/*   Q4_1, Q5_1  isum = sum_i q_i*a_i (q unsigned); the min contributes      */
+/*         m * sum_i a_i, the activation block's own code sum               */
+/*   Q5_0  isum = sum_i (q_i - 16)*a_i                                       */
+/*   Q5_K  value = sum_s sc_s * sum_{i in s} q_i*a_i, min as Q4_K            */
 /* ------------------------------------------------------------------------- */
+static int32_t act_block_sum(const uint8_t* ab) {
+    int32_t s = 0;
+    for (int j = 0; j < 32; j++) s += (int8_t)ab[2 + j];
+    return s;
+}
+
 static int32_t blk32_isum(int wtype, const uint8_t* wb, const uint8_t* ab) {
     int32_t si = 0;
     if (wtype == ORC_Q4_0) {
@@ -543,8 +754,13 @@ static int32_t blk32_isum(int wtype, const uint8_t* wb, const uint8_t* ab) {
             si += v0 * (int8_t)ab[2 + j];
             si += v1 * (int8_t)ab[2 + j + 16];
         }
-    } else { /* Q8_0 */
+    } else if (wtype == ORC_Q8_0) {
         for (int j = 0; j < 32; j++) si += (int8_t)wb[2 + j] * (int8_t)ab[2 + j];
+    } else { /* Q4_1, Q5_0, Q5_1: element by element */
+        for (int i = 0; i < 32; i++) {
+            int c = wtype == ORC_Q4_1 ? q4_1_code(wb, i) : wtype == ORC_Q5_0 ? q5_0_code(wb, i) - 16 : q5_1_code(wb, i);
+            si += c * (int8_t)ab[2 + i];
+        }
     }
     return si;
 }
@@ -569,6 +785,15 @@ static void kblk_isums(int wtype, const uint8_t* wb, const uint8_t* ab, int32_t*
             sumi2 += s_hi * sc[2 * j + 1];
         }
         v = sumi1 + sumi2;
+    } else if (wtype == ORC_Q5_K) {
+        int sc[8], mn[8];
+        orc_q4_K_unpack_scales(wb + 4, sc, mn);
+        for (int s = 0; s < 8; s++) {
+            int32_t si = 0;
+            for (int i = 0; i < 32; i++) si += q5_K_code(wb, 32 * s + i) * a[32 * s + i];
+            v += sc[s] * si;
+            m += mn[s] * (bs[2 * s] + bs[2 * s + 1]);
+        }
     } else if (wtype == ORC_Q2_K) {
         for (int g = 0; g < 16; g++) {
             int32_t s = 0;
@@ -609,6 +834,8 @@ void orc_blocksums_row(int wtype, const uint8_t* wrow, const uint8_t* xrow, int6
 /*        ([minfer] s3.2, the K-quant dot walked)                            */
 /*  Q2_K: the same two-term fold with its own (value, min) ([ggml] s1.2)     */
 /*  Q6_K: d = dw*dx; sumf += d*(value - 32*min)  (reading)                   */
+/*  Q4_1/Q5_1: s += (float)isum*dw*dx; s += (float)asum*mw*dx   (reading)     */
+/*  Q5_0: as Q4_0; Q5_K: as Q4_K                                             */
 /* ------------------------------------------------------------------------- */
 float orc_dot_row(int wtype, const uint8_t* wrow, const uint8_t* xrow, int64_t K) {
     int at = orc_act_type(wtype);
@@ -622,6 +849,10 @@ float orc_dot_row(int wtype, const uint8_t* wrow, const uint8_t* xrow, int64_t K
             float dy = orc_f16_to_f32(rd16(a));
             int32_t si = blk32_isum(wtype, w, a);
             s += (float)si * dx * dy;
+            if (wtype == ORC_Q4_1 || wtype == ORC_Q5_1) {
+                float mx = orc_f16_to_f32(rd16(w + 2));
+                s += (float)act_block_sum(a) * mx * dy;
+            }
         }
         return s;
     }
@@ -631,7 +862,7 @@ float orc_dot_row(int wtype, const uint8_t* wrow, const uint8_t* xrow, int64_t K
         float ad = rdf32(a);
         int32_t value, minterm;
         kblk_isums(wtype, w, a, &value, &minterm);
-        if (wtype == ORC_Q4_K) {
+        if (wtype == ORC_Q4_K || wtype == ORC_Q5_K) {
             float d = orc_f16_to_f32(rd16(w)) * ad;
             float dmin = orc_f16_to_f32(rd16(w + 2)) * ad;
             s -= dmin * (float)minterm;
@@ -661,6 +892,9 @@ double orc_dot_row_exact(int wtype, const uint8_t* wrow, const uint8_t* xrow, in
             const uint8_t* a = xrow + b * ab;
             s += (double)orc_f16_to_f32(rd16(w)) * (double)orc_f16_to_f32(rd16(a)) *
                  (double)blk32_isum(wtype, w, a);
+            if (wtype == ORC_Q4_1 || wtype == ORC_Q5_1)
+                s += (double)orc_f16_to_f32(rd16(w + 2)) * (double)orc_f16_to_f32(rd16(a)) *
+                     (double)act_block_sum(a);
         }
         return s;
     }
@@ -670,7 +904,7 @@ double orc_dot_row_exact(int wtype, const uint8_t* wrow, const uint8_t* xrow, in
         double ad = rdf32(a);
         int32_t value, minterm;
         kblk_isums(wtype, w, a, &value, &minterm);
-        if (wtype == ORC_Q4_K)
+        if (wtype == ORC_Q4_K || wtype == ORC_Q5_K)
             s += ad * ((double)orc_f16_to_f32(rd16(w)) * value - (double)orc_f16_to_f32(rd16(w + 2)) * minterm);
         else if (wtype == ORC_Q2_K)
             s += ad * ((double)orc_f16_to_f32(rd16(w + 80)) * value -

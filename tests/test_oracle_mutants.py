@@ -18,7 +18,8 @@ MUTANTS = [
     ("q4_0 dot drops the -8", "int v0 = (wb[2 + j] & 0x0F) - 8;", "int v0 = (wb[2 + j] & 0x0F);"),
     ("q4_K min term sign", "s -= dmin * (float)minterm;\n            s += d * (float)value;\n        } else if (wtype == ORC_Q2_K)",
      "s += dmin * (float)minterm;\n            s += d * (float)value;\n        } else if (wtype == ORC_Q2_K)"),
-    ("q4_K bsum pair index", "m += mn[s] * (bs[2 * s] + bs[2 * s + 1]);", "m += mn[s] * (bs[2 * s] + bs[2 * s]);"),
+    ("q4_K bsum pair index", "for (int s = 0; s < 8; s++) m += mn[s] * (bs[2 * s] + bs[2 * s + 1]);",
+     "for (int s = 0; s < 8; s++) m += mn[s] * (bs[2 * s] + bs[2 * s]);"),
     ("q8_0 scale 128/amax", "float id = (amax != 0.0f) ? 127.0f / amax : 0.0f;\n        for (int i = 0; i < 32; i++) {",
      "float id = (amax != 0.0f) ? 128.0f / amax : 0.0f;\n        for (int i = 0; i < 32; i++) {"),
     ("f16 ties round up", "if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;", "if (rest >= 0x1000u) h += 1u;"),
@@ -32,6 +33,14 @@ MUTANTS = [
     ("q8_K bsums skip a code", "for (int i = 0; i < 16; i++) {\n                float v = xb[g * 16 + i] * id;\n                int q = clampi(rne(v), -128, 127);\n                ob[4 + g * 16 + i] = (uint8_t)(int8_t)q;\n                sum += q;",
      "for (int i = 0; i < 16; i++) {\n                float v = xb[g * 16 + i] * id;\n                int q = clampi(rne(v), -128, 127);\n                ob[4 + g * 16 + i] = (uint8_t)(int8_t)q;\n                if (i) sum += q;"),
     ("q8_0 rounds half away from zero", "float r = nearbyintf(v);", "float r = roundf(v);"),
+    ("fifth bit read transposed", "return (qh[i / 8] >> (i % 8)) & 1;", "return (qh[i % 4] >> (i / 4)) & 1;"),
+    ("q4_1 drops the min term", "s += (float)act_block_sum(a) * mx * dy;", "s += 0.0f * mx * dy;"),
+    ("q5_K fifth bit shift", "int high = (blk[16 + l] >> (2 * j + (r >= 32))) & 1;",
+     "int high = (blk[16 + l] >> (j + (r >= 32))) & 1;"),
+    ("q5_1 high bits at the q5_0 offset", "nibble_code(blk + 8, i) | (fifth_bit(blk + 4, i) << 4)",
+     "nibble_code(blk + 8, i) | (fifth_bit(blk + 2, i) << 4)"),
+    ("q5_0 rounding offset", "float t = xb[i] * id + 16.5f;", "float t = xb[i] * id + 16.0f;"),
+    ("q5_K quantizer 15 levels", "scl[s] = (hi + mns[s]) / 31.0f;", "scl[s] = (hi + mns[s]) / 15.0f;"),
 ]
 
 PINS = [name for name in dir(pins) if name.startswith("test_")]

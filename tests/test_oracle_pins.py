@@ -11,7 +11,8 @@ import pytest
 from conftest import read_golden
 import workloads
 
-QTYPES = ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K"]
+QTYPES = ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K", "q4_1", "q5_0", "q5_1", "q5_K"]
+KQUANTS = ("q4_K", "q6_K", "q2_K", "q5_K")
 
 
 def f16(v):
@@ -59,10 +60,12 @@ def test_block_sizes(orc):
 
 
 def test_pairing_rule(orc):
-    """[minfer] s2.4/s3.2: K-quant weights pair with Q8_K, the 32-value types with Q8_0."""
-    assert orc.act_type("q4_0") == orc.Q8_0 and orc.act_type("q8_0") == orc.Q8_0
-    for t in ("q4_K", "q6_K", "q2_K"):
-        assert orc.act_type(t) == orc.Q8_K
+    """[minfer] s2.4/s3.2: K-quant weights pair with Q8_K (the Q4_K/Q5_K/Q6_K arms call
+    dot_q*_k_q8_k), the 32-value types with Q8_0 (dot_<T>_q8_0)."""
+    for t in ("q4_0", "q8_0", "q4_1", "q5_0", "q5_1"):
+        assert orc.act_type(t) == orc.Q8_0, t
+    for t in KQUANTS:
+        assert orc.act_type(t) == orc.Q8_K, t
 
 
 def _q4_0_block(d_bits, qs):
@@ -294,6 +297,69 @@ def test_q4_K_handmade_block(orc):
         assert codes[e] == c and vals[e] == want, (e, codes[e], vals[e], want)
 
 
+def test_q5_q4_1_handmade_blocks(orc):
+    """Hand-built Q5_0, Q5_1, Q4_1 and Q5_K blocks decode to the values worked out by hand:
+    the fifth-bit plane, the nibble pairing and the min of each layout (GGUF readings; sizes
+    [minfer] s1, s3.2)."""
+    blocks = []
+    for row in read_golden("q5_q4_1_handmade.txt"):
+        if row[0] == "blk":
+            blocks.append((row[1], np.zeros(int(row[2]), dtype=np.uint8), []))
+        elif row[0] == "byte":
+            blocks[-1][1][int(row[1])] = int(row[2], 0)
+        elif row[0] == "elem":
+            blocks[-1][2].append((int(row[1]), int(row[2]), float(row[3])))
+    assert [b[0] for b in blocks] == ["q5_0", "q5_1", "q4_1", "q5_K"]
+    for t, blk, elems in blocks:
+        bv = orc.block_values(t)
+        vals = orc.dequantize(t, blk, bv)[0]
+        codes = orc.codes(t, blk, bv)[0]
+        for e, code, want in elems:
+            stored = codes[e] + 16 if t == "q5_0" else codes[e]
+            assert stored == code and vals[e] == want, (t, e, stored, code, vals[e], want)
+
+
+def test_q5_q4_1_integer_grids_are_exact(orc):
+    """Textbook special case of the 32-value quantizers (readings): a block that is already an
+    integer grid comes back exactly.  Q4_1 on c + {0..15} and Q5_1 on c + {0..31} have d = 1,
+    m = c; Q5_0 on {-16..15} has its extreme -16 at code 0 and d = 1.  Each block is a
+    permutation, so a misplaced nibble or high bit changes a value."""
+    g = np.random.default_rng(8)
+    for t, levels, c in (("q4_1", 16, 3.0), ("q5_1", 32, -5.0), ("q5_0", 32, -16.0)):
+        base = np.arange(32) % levels
+        x = np.stack([g.permutation(base) for _ in range(6)]).astype(np.float32) + np.float32(c)
+        v = orc.dequantize(t, orc.quantize(t, x), 32)
+        assert np.array_equal(v.reshape(x.shape), x.astype(np.float64)), t
+
+
+@pytest.mark.parametrize("wtype", ["q4_1", "q5_0", "q5_1"])
+def test_32_value_roundtrip(orc, wtype):
+    """The 32-value quantizers (readings): every code in range; min/max grids reconstruct each
+    value within half a step plus the f16 rounding of d and m; Q5_0's extreme sits at code -16
+    (the Q4_0 idea, [ggml] s1.1) and the rest within half a step except the clipped end."""
+    w = workloads.weights_f32(16, 512, seed=23, row_jitter=True)
+    q = orc.quantize(wtype, w)
+    v = orc.dequantize(wtype, q, 512).reshape(-1, 32)
+    codes = orc.codes(wtype, q, 512).reshape(-1, 32)
+    wb = w.reshape(-1, 32).astype(np.float64)
+    lo, hi = {"q4_1": (0, 15), "q5_0": (-16, 15), "q5_1": (0, 31)}[wtype]
+    assert codes.min() >= lo and codes.max() <= hi
+    if wtype == "q5_0":
+        r = np.arange(wb.shape[0])
+        imax = np.abs(wb).argmax(axis=1)
+        assert np.all(codes[r, imax] == -16)
+        d32 = wb[r, imax] / -16
+        dh = q.reshape(-1, 22)[:, 0:2].copy().view(np.float16).astype(np.float64)[:, 0]
+        t = wb / d32[:, None]                  # the code each value wants, before clipping
+        ok = t < 15.5
+        bound = 0.5 * np.abs(dh)[:, None] + np.abs(t) * np.abs(dh - d32)[:, None] + 1e-6 * np.abs(wb)
+        assert np.all((np.abs(v - wb) <= bound)[ok])
+    else:
+        step = (wb.max(axis=1) - wb.min(axis=1)) / (hi - lo)
+        bound = 0.5 * step * (1 + 2e-3) + 2 ** -11 * np.abs(wb.min(axis=1)) + 1e-7
+        assert np.all(np.abs(v - wb) <= bound[:, None]), np.abs(v - wb).max()
+
+
 def test_q4_K_scale_packing_roundtrip(orc):
     """The 12-byte packing (reading: GGUF) is a bijection on eight 6-bit scales and mins:
     every value 0..63 in every slot survives pack (via the quantizer) and unpack.  Checked by
@@ -319,7 +385,7 @@ def test_q4_K_scale_packing_roundtrip(orc):
     assert len(seen) == 512
 
 
-@pytest.mark.parametrize("wtype", ["q4_K", "q2_K", "q6_K"])
+@pytest.mark.parametrize("wtype", ["q4_K", "q2_K", "q6_K", "q5_K"])
 def test_kquant_roundtrip(orc, wtype):
     """K-quant weight quantizers (readings): codes in range and every value reconstructed
     within the grid's step plus the rounding of its stored scale and min.  A wrong pack or
@@ -328,17 +394,17 @@ def test_kquant_roundtrip(orc, wtype):
     q = orc.quantize(wtype, w)
     v = orc.dequantize(wtype, q, 1024)
     codes = orc.codes(wtype, q, 1024)
-    lo, hi = {"q4_K": (0, 15), "q2_K": (0, 3), "q6_K": (-32, 31)}[wtype]
+    lo, hi = {"q4_K": (0, 15), "q2_K": (0, 3), "q6_K": (-32, 31), "q5_K": (0, 31)}[wtype]
     assert codes.min() >= lo and codes.max() <= hi
     err = np.abs(v - w)
-    gsz = 32 if wtype == "q4_K" else 16
+    gsz = 32 if wtype in ("q4_K", "q5_K") else 16
     rng_ = w.reshape(-1, gsz).max(axis=1) - np.minimum(w.reshape(-1, gsz).min(axis=1), 0)
-    levels = {"q4_K": 15, "q2_K": 3, "q6_K": 63}[wtype]
+    levels = {"q4_K": 15, "q2_K": 3, "q6_K": 63, "q5_K": 31}[wtype]
     step = rng_ / levels
     # a step and a half covers the grid offset from the rounded 6/4-bit scale and min
     assert np.all(err.reshape(-1, gsz) <= 1.5 * step[:, None] + 1e-6), err.max()
     rel = np.linalg.norm(v - w) / np.linalg.norm(w)
-    assert rel < {"q4_K": 0.12, "q2_K": 0.45, "q6_K": 0.03}[wtype], rel
+    assert rel < {"q4_K": 0.12, "q2_K": 0.45, "q6_K": 0.03, "q5_K": 0.06}[wtype], rel
 
 
 def test_q6_K_extreme_code(orc):
@@ -366,7 +432,7 @@ def test_factorized_equals_bruteforce(orc, wtype):
     double rounding, and the pages' fp32 fold is within fp32 accumulation error of it.  The
     brute force decodes every element on its own path, so a wrong nibble pairing, a dropped
     min term, a sign slip or a transposed operand in the kernel arithmetic fails here."""
-    bv = 256 if wtype in ("q4_K", "q6_K", "q2_K") else 32
+    bv = 256 if wtype in KQUANTS else 32
     for K in sorted({bv, 2 * bv, 512 if bv == 32 else 768}):
         for N in (1, 3, 7):
             M = 3
@@ -396,12 +462,15 @@ def test_blocksums_consistent(orc, wtype):
     wb = W.reshape(N, -1, orc.block_bytes(wtype))
     xb = X.reshape(M, -1, orc.block_bytes(orc.act_type(wtype)))
     h = lambda a: a.copy().view(np.float16).astype(np.float64)[..., 0]
-    if wtype in ("q4_0", "q8_0"):
+    if wtype not in KQUANTS:
         dw, dx = h(wb[:, :, 0:2]), h(xb[:, :, 0:2])
         y = np.einsum("tob,ob,tb->to", s, dw, dx)
+        if wtype in ("q4_1", "q5_1"):   # the min meets the activation block's code sum
+            asum = xb[:, :, 2:34].view(np.int8).astype(np.float64).sum(axis=2)
+            y += np.einsum("tb,ob,tb->to", asum, h(wb[:, :, 2:4]), dx)
     else:
         dx = xb[:, :, 0:4].copy().view(np.float32).astype(np.float64)[..., 0]
-        off = {"q4_K": (0, 2), "q2_K": (80, 82), "q6_K": (208, None)}[wtype]
+        off = {"q4_K": (0, 2), "q2_K": (80, 82), "q6_K": (208, None), "q5_K": (0, 2)}[wtype]
         dw = h(wb[:, :, off[0]:off[0] + 2])
         v, m = s[:, :, 0::2], s[:, :, 1::2]
         if wtype == "q6_K":
