@@ -147,7 +147,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ helpers
 def act_of(wtype):
-    return "q8_0" if wtype in ("q4_0", "q8_0") else "q8_K"
+    return "q8_0" if wtype in ("q4_0", "q8_0", "q4_1", "q5_0", "q5_1") else "q8_K"
 
 
 def load_peaks():

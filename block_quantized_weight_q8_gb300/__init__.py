@@ -13,10 +13,10 @@ import os
 
 from .buildlib import LIB, build  # noqa: F401
 
-QMM_Q4_0, QMM_Q8_0, QMM_Q4_K, QMM_Q6_K, QMM_Q2_K, QMM_Q8_K = range(6)
+QMM_Q4_0, QMM_Q8_0, QMM_Q4_K, QMM_Q6_K, QMM_Q2_K, QMM_Q8_K, QMM_Q4_1, QMM_Q5_0, QMM_Q5_1, QMM_Q5_K = range(10)
 TYPES = {"q4_0": QMM_Q4_0, "q8_0": QMM_Q8_0, "q4_K": QMM_Q4_K, "q6_K": QMM_Q6_K, "q2_K": QMM_Q2_K,
-         "q8_K": QMM_Q8_K}
-WEIGHT_TYPES = ("q4_0", "q8_0", "q4_K", "q6_K", "q2_K")
+         "q8_K": QMM_Q8_K, "q4_1": QMM_Q4_1, "q5_0": QMM_Q5_0, "q5_1": QMM_Q5_1, "q5_K": QMM_Q5_K}
+WEIGHT_TYPES = ("q4_0", "q8_0", "q4_K", "q6_K", "q2_K", "q4_1", "q5_0", "q5_1", "q5_K")
 
 STATUS = {0: "QMM_OK", 1: "QMM_E_NULL", 2: "QMM_E_SHAPE", 3: "QMM_E_TYPE", 4: "QMM_E_ALIGN",
           5: "QMM_E_SCRATCH", 6: "QMM_E_CUDA", 7: "QMM_E_TIMEOUT"}
@@ -40,11 +40,19 @@ SIGNATURES = {
     "qmm_matvec_q4_K": ("pppiiq", ctypes.c_int),
     "qmm_matvec_q6_K": ("pppiiq", ctypes.c_int),
     "qmm_matvec_q2_K": ("pppiiq", ctypes.c_int),
+    "qmm_matvec_q4_1": ("pppiiq", ctypes.c_int),
+    "qmm_matvec_q5_0": ("pppiiq", ctypes.c_int),
+    "qmm_matvec_q5_1": ("pppiiq", ctypes.c_int),
+    "qmm_matvec_q5_K": ("pppiiq", ctypes.c_int),
     "qmm_linear_q4_0": ("pppspiiiq", ctypes.c_int),
     "qmm_linear_q8_0": ("pppspiiiq", ctypes.c_int),
     "qmm_linear_q4_K": ("pppspiiiq", ctypes.c_int),
     "qmm_linear_q6_K": ("pppspiiiq", ctypes.c_int),
     "qmm_linear_q2_K": ("pppspiiiq", ctypes.c_int),
+    "qmm_linear_q4_1": ("pppspiiiq", ctypes.c_int),
+    "qmm_linear_q5_0": ("pppspiiiq", ctypes.c_int),
+    "qmm_linear_q5_1": ("pppspiiiq", ctypes.c_int),
+    "qmm_linear_q5_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
     "qmm_get_rows": ("tpppiiiq", ctypes.c_int),
     "qmm_matmul_q4_K": ("pppiiiq", ctypes.c_int),
@@ -177,6 +185,10 @@ qmm_matvec_q8_0 = _mv("qmm_matvec_q8_0")
 qmm_matvec_q4_K = _mv("qmm_matvec_q4_K")
 qmm_matvec_q6_K = _mv("qmm_matvec_q6_K")
 qmm_matvec_q2_K = _mv("qmm_matvec_q2_K")
+qmm_matvec_q4_1 = _mv("qmm_matvec_q4_1")
+qmm_matvec_q5_0 = _mv("qmm_matvec_q5_0")
+qmm_matvec_q5_1 = _mv("qmm_matvec_q5_1")
+qmm_matvec_q5_K = _mv("qmm_matvec_q5_K")
 
 
 def matvec(wtype, W, xq, y, N, K, stream=None):
@@ -196,6 +208,10 @@ qmm_linear_q8_0 = _lin("qmm_linear_q8_0")
 qmm_linear_q4_K = _lin("qmm_linear_q4_K")
 qmm_linear_q6_K = _lin("qmm_linear_q6_K")
 qmm_linear_q2_K = _lin("qmm_linear_q2_K")
+qmm_linear_q4_1 = _lin("qmm_linear_q4_1")
+qmm_linear_q5_0 = _lin("qmm_linear_q5_0")
+qmm_linear_q5_1 = _lin("qmm_linear_q5_1")
+qmm_linear_q5_K = _lin("qmm_linear_q5_K")
 
 
 def linear(wtype, W, x, scratch, scratch_bytes, y, M, N, K, stream=None):

@@ -10,7 +10,7 @@ qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int6
                            bool pdl);
 qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                             cudaStream_t stream, bool pdl);
-bool kq_uses_tensor_cores(int64_t M, int64_t K);
+bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K);
 qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq_out, float* y, int64_t N, int64_t K,
                                  cudaStream_t stream, bool pdl);
 qmm_status matvec_group_fused_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
@@ -37,7 +37,7 @@ static qmm_status linear(int wt, const void* W, const float* x, void* scratch, s
         if (st != QMM_OK) return st;
         return matmul_q4_0_launch(W, scratch, y, M, N, K, stream, true);
     }
-    if (act == QMM_Q8_K && kq_uses_tensor_cores(M, K)) {  // K-quant prefill on the tensor cores
+    if (kq_uses_tensor_cores(wt, M, K)) {  // K-quant prefill on the tensor cores
         st = quantize_act_launch(act, x, scratch, M, K, stream, true);
         if (st != QMM_OK) return st;
         return matmul_kq_launch(wt, W, scratch, y, M, N, K, stream, true);
@@ -150,6 +150,23 @@ qmm_status qmm_linear_q6_K(const void* W, const float* x, void* s, size_t sb, fl
 qmm_status qmm_linear_q2_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
     return linear(QMM_Q2_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+
+qmm_status qmm_linear_q4_1(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q4_1, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_linear_q5_0(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q5_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_linear_q5_1(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q5_1, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_linear_q5_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return linear(QMM_Q5_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 
 qmm_status qmm_device_status(int clear) {

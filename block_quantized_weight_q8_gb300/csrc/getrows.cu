@@ -9,7 +9,9 @@
 //   Q4_0  d * (n - 8), Q8_0  d * q                       exact products
 //   Q4_K  fma(d*sc, q, -(dmin*m)), Q2_K the same         d*sc and dmin*m exact
 //   Q6_K  (d*sc) * (q - 32)                             exact (18 + 6 bits)
-// Layouts as in the decoders (GGUF readings for the K-quants).
+//   Q4_1, Q5_1  fma(d, q, m)      Q5_0  d * (q - 16)      Q5_K as Q4_K
+// Layouts as in the decoders (GGUF readings for the K-quants and the types
+// with a fifth bit or a min).
 #include "qmm_device.cuh"
 #include "qmm_host.h"
 
@@ -67,6 +69,53 @@ __device__ __forceinline__ void dequant32(const uint8_t* __restrict__ row, int s
             const float dl = d * (float)(g & 15u), ml = dmin * (float)(g >> 4);
 #pragma unroll
             for (int j = 0; j < 16; j++) v[16 * half + j] = fmaf(dl, (float)((q[16 * half + j] >> sh) & 3), -ml);
+        }
+    } else if constexpr (WT == QMM_Q4_1 || WT == QMM_Q5_0 || WT == QMM_Q5_1) {
+        constexpr int BB = Fmt<WT>::BB;
+        constexpr int QS = WT == QMM_Q4_1 ? 4 : (WT == QMM_Q5_0 ? 6 : 8);  // nibbles
+        constexpr int QH = WT == QMM_Q5_0 ? 2 : 4;                          // fifth bits
+        const uint8_t* b = row + BB * s;
+        const float d = h2f(ld_u16(b));
+        const float m = WT == QMM_Q5_0 ? 0.0f : h2f(ld_u16(b + 2));
+        uint32_t qh = 0;
+        if constexpr (WT != QMM_Q4_1) qh = ld_u16(b + QH) | (ld_u16(b + QH + 2) << 16);
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const uint32_t byte = b[QS + j];
+            int lo = (int)(byte & 15u), hi = (int)(byte >> 4);
+            if constexpr (WT != QMM_Q4_1) {
+                lo |= (int)((qh >> j) & 1u) << 4;
+                hi |= (int)((qh >> (j + 16)) & 1u) << 4;
+            }
+            if constexpr (WT == QMM_Q5_0) {
+                v[j] = d * (float)(lo - 16);
+                v[j + 16] = d * (float)(hi - 16);
+            } else {
+                v[j] = fmaf(d, (float)lo, m);
+                v[j + 16] = fmaf(d, (float)hi, m);
+            }
+        }
+    } else if constexpr (WT == QMM_Q5_K) {
+        const uint8_t* b = row + 176 * (s >> 3);
+        const int sb = s & 7;
+        const float d = h2f(ld_u16(b)), dmin = h2f(ld_u16(b + 2));
+        const uint8_t* sc = b + 4;
+        int scale, mn;
+        if (sb < 4) {
+            scale = sc[sb] & 63;
+            mn = sc[sb + 4] & 63;
+        } else {
+            scale = (sc[sb + 4] & 15) | ((sc[sb - 4] >> 6) << 4);
+            mn = (sc[sb + 4] >> 4) | ((sc[sb] >> 6) << 4);
+        }
+        const float dl = d * (float)scale, ml = dmin * (float)mn;
+        const uint8_t* q = b + 48 + 32 * (sb >> 1);
+        const uint8_t* qh = b + 16;
+        const int sh = (sb & 1) * 4;  // sub-block sb: nibble (sb & 1), fifth bit sb of qh[l]
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            const int code = ((q[j] >> sh) & 15) | (((qh[j] >> sb) & 1) << 4);
+            v[j] = fmaf(dl, (float)code, -ml);
         }
     } else {  // Q6_K
         const uint8_t* b = row + 210 * (s >> 3);
@@ -149,6 +198,10 @@ qmm_status qmm_get_rows(int wtype, const void* W, const int32_t* ids, float* out
     case QMM_Q4_K: return launch_getrows<QMM_Q4_K>(W, ids, out, R, N, K, cs);
     case QMM_Q6_K: return launch_getrows<QMM_Q6_K>(W, ids, out, R, N, K, cs);
     case QMM_Q2_K: return launch_getrows<QMM_Q2_K>(W, ids, out, R, N, K, cs);
+    case QMM_Q4_1: return launch_getrows<QMM_Q4_1>(W, ids, out, R, N, K, cs);
+    case QMM_Q5_0: return launch_getrows<QMM_Q5_0>(W, ids, out, R, N, K, cs);
+    case QMM_Q5_1: return launch_getrows<QMM_Q5_1>(W, ids, out, R, N, K, cs);
+    case QMM_Q5_K: return launch_getrows<QMM_Q5_K>(W, ids, out, R, N, K, cs);
     default: return QMM_E_TYPE;
     }
 }

@@ -22,7 +22,7 @@ qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int6
                            bool pdl);
 qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                             cudaStream_t stream, bool pdl);
-bool kq_uses_tensor_cores(int64_t M, int64_t K);
+bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K);
 qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq_out, float* y, int64_t N, int64_t K,
                                  cudaStream_t stream, bool pdl);
 qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
@@ -78,7 +78,7 @@ qmm_status qmm_linear_noalloc(int wtype, const void* W, const float* x, float* y
         if (st != QMM_OK) return st;
         return matmul_q4_0_launch(W, scratch, y, M, N, K, cs, true);
     }
-    if (act == QMM_Q8_K && kq_uses_tensor_cores(M, K)) {  // K-quant prefill on the tensor cores
+    if (kq_uses_tensor_cores(wtype, M, K)) {  // K-quant prefill on the tensor cores
         st = quantize_act_launch(act, x, scratch, M, K, cs, true);
         if (st != QMM_OK) return st;
         return matmul_kq_launch(wtype, W, scratch, y, M, N, K, cs, true);

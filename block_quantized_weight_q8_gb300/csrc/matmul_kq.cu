@@ -694,10 +694,12 @@ static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, 
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
+bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K);
+
 // Y[M][N] for a K-quant W against M Q8_K rows (internal: arguments checked).
 qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                             cudaStream_t stream, bool pdl) {
-    if (!kq_tensor_core_shape(M, K)) {
+    if (!kq_uses_tensor_cores(wt, M, K)) {  // per token: small M, ragged K, or no tensor-core kernel
         const size_t xrb = row_bytes_of(QMM_Q8_K, K);
         for (int64_t t = 0; t < M; t++) {
             qmm_status st = matvec_dispatch(wt, W, (const uint8_t*)xq + t * xrb, Y + t * N, N, K, stream, pdl);
@@ -714,7 +716,9 @@ qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int
     }
 }
 
-bool kq_uses_tensor_cores(int64_t M, int64_t K) { return kq_tensor_core_shape(M, K); }
+bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K) {
+    return (wt == QMM_Q4_K || wt == QMM_Q2_K || wt == QMM_Q6_K) && kq_tensor_core_shape(M, K);
+}
 
 static qmm_status matmul_kq_checked(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                                     qmm_stream_t stream) {

@@ -1,5 +1,6 @@
 // matvec.cu -- the decode matvec (one token): y[o] = row o of the block-quantized
-// W against one Q8_0 / Q8_K activation row, for Q4_0, Q8_0, Q4_K, Q6_K and Q2_K.
+// W against one Q8_0 / Q8_K activation row, for Q4_0, Q8_0, Q4_K, Q6_K and Q2_K,
+// and Q4_1, Q5_0, Q5_1, Q5_K.
 //
 // Design (GB300): the kernel is HBM-bound, so it is built around keeping the
 // weight stream in flight.  Each CTA owns a contiguous range of rows (an even
@@ -69,10 +70,17 @@ __host__ __device__ inline uint32_t act_region_bytes(int act, int K) {
 
 template <int WT>
 __device__ __forceinline__ float unit_contrib(const SmemBytes& w, uint32_t o, const ActView& a, int u) {
-    if constexpr (WT == QMM_Q4_0 || WT == QMM_Q8_0) {
+    if constexpr (WT == QMM_Q4_0 || WT == QMM_Q8_0 || WT == QMM_Q5_0) {
         uint32_t db;
-        const int isum = (WT == QMM_Q4_0) ? q4_0_isum(w, o, a, u, &db) : q8_0_isum(w, o, a, u, &db);
+        const int isum = (WT == QMM_Q4_0)   ? q4_0_isum(w, o, a, u, &db)
+                         : (WT == QMM_Q8_0) ? q8_0_isum(w, o, a, u, &db)
+                                            : q5_0_isum(w, o, a, u, &db);
         return (float)isum * h2f(db) * a.d[u];
+    } else if constexpr (WT == QMM_Q4_1 || WT == QMM_Q5_1) {
+        uint32_t dm;
+        const int isum = (WT == QMM_Q4_1) ? q4_1_isum(w, o, a, u, &dm) : q5_1_isum(w, o, a, u, &dm);
+        // d*dx*sum(q*a) + m*dx*sum(a): the min meets the activation block's code sum
+        return (float)isum * h2f(dm & 0xFFFFu) * a.d[u] + (float)a.s[u] * h2f(dm >> 16) * a.d[u];
     } else if constexpr (WT == QMM_Q6_K) {
         int v, m;
         uint32_t db;
@@ -83,6 +91,7 @@ __device__ __forceinline__ float unit_contrib(const SmemBytes& w, uint32_t o, co
         int v, m;
         uint32_t db, dmb;
         if constexpr (WT == QMM_Q4_K) q4_K_isums(w, o, a, u, &v, &m, &db, &dmb);
+        else if constexpr (WT == QMM_Q5_K) q5_K_isums(w, o, a, u, &v, &m, &db, &dmb);
         else q2_K_isums(w, o, a, u, &v, &m, &db, &dmb);
         const float d = h2f(db) * a.d[u];
         const float dmin = h2f(dmb) * a.d[u];
@@ -389,7 +398,11 @@ __global__ void __launch_bounds__(kThreads) blocksums_kernel(const uint8_t* __re
         else if constexpr (WT == QMM_Q8_0) v = q8_0_isum(wv, o, act, u, &db);
         else if constexpr (WT == QMM_Q4_K) q4_K_isums(wv, o, act, u, &v, &m, &db, &dmb);
         else if constexpr (WT == QMM_Q2_K) q2_K_isums(wv, o, act, u, &v, &m, &db, &dmb);
-        else q6_K_isums(wv, o, act, u, &v, &m, &db);
+        else if constexpr (WT == QMM_Q6_K) q6_K_isums(wv, o, act, u, &v, &m, &db);
+        else if constexpr (WT == QMM_Q4_1) v = q4_1_isum(wv, o, act, u, &db);
+        else if constexpr (WT == QMM_Q5_0) v = q5_0_isum(wv, o, act, u, &db);
+        else if constexpr (WT == QMM_Q5_1) v = q5_1_isum(wv, o, act, u, &db);
+        else q5_K_isums(wv, o, act, u, &v, &m, &db, &dmb);
         if constexpr (F::ACT == QMM_Q8_0) {
             dst[u] = v;
         } else {
@@ -633,6 +646,10 @@ static qmm_status matvec_group_checked(int wt, int G, const void* const* W, cons
     case QMM_Q4_K: return launch_matvec<QMM_Q4_K>(W, N, y, G, xq, x, K, stream, pdl);
     case QMM_Q6_K: return launch_matvec<QMM_Q6_K>(W, N, y, G, xq, x, K, stream, pdl);
     case QMM_Q2_K: return launch_matvec<QMM_Q2_K>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q4_1: return launch_matvec<QMM_Q4_1>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q5_0: return launch_matvec<QMM_Q5_0>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q5_1: return launch_matvec<QMM_Q5_1>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q5_K: return launch_matvec<QMM_Q5_K>(W, N, y, G, xq, x, K, stream, pdl);
     default: return QMM_E_TYPE;
     }
 }
@@ -714,6 +731,18 @@ qmm_status qmm_matvec_q6_K(const void* W, const void* xq, float* y, int64_t N, i
 qmm_status qmm_matvec_q2_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
     return matvec_checked(QMM_Q2_K, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
 }
+qmm_status qmm_matvec_q4_1(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q4_1, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
+}
+qmm_status qmm_matvec_q5_0(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q5_0, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
+}
+qmm_status qmm_matvec_q5_1(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q5_1, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
+}
+qmm_status qmm_matvec_q5_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream) {
+    return matvec_checked(QMM_Q5_K, W, xq, nullptr, y, N, K, (cudaStream_t)stream, true, true);
+}
 
 qmm_status qmm_blocksums(int wtype, const void* W, const void* xq, int32_t* s, int64_t M, int64_t N, int64_t K,
                          qmm_stream_t stream) {
@@ -729,6 +758,10 @@ qmm_status qmm_blocksums(int wtype, const void* W, const void* xq, int32_t* s, i
     case QMM_Q4_K: return launch_blocksums<QMM_Q4_K>(W, xq, s, M, N, K, cs);
     case QMM_Q6_K: return launch_blocksums<QMM_Q6_K>(W, xq, s, M, N, K, cs);
     case QMM_Q2_K: return launch_blocksums<QMM_Q2_K>(W, xq, s, M, N, K, cs);
+    case QMM_Q4_1: return launch_blocksums<QMM_Q4_1>(W, xq, s, M, N, K, cs);
+    case QMM_Q5_0: return launch_blocksums<QMM_Q5_0>(W, xq, s, M, N, K, cs);
+    case QMM_Q5_1: return launch_blocksums<QMM_Q5_1>(W, xq, s, M, N, K, cs);
+    case QMM_Q5_K: return launch_blocksums<QMM_Q5_K>(W, xq, s, M, N, K, cs);
     default: return QMM_E_TYPE;
     }
 }

@@ -24,6 +24,10 @@ template <> struct Fmt<QMM_Q8_0> { static constexpr int BB = 34, BV = 32, ACT = 
 template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, BV = 256, ACT = QMM_Q8_K; };
 template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, BV = 256, ACT = QMM_Q8_K; };
 template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, BV = 256, ACT = QMM_Q8_K; };
+template <> struct Fmt<QMM_Q4_1> { static constexpr int BB = 20, BV = 32, ACT = QMM_Q8_0; };
+template <> struct Fmt<QMM_Q5_0> { static constexpr int BB = 22, BV = 32, ACT = QMM_Q8_0; };
+template <> struct Fmt<QMM_Q5_1> { static constexpr int BB = 24, BV = 32, ACT = QMM_Q8_0; };
+template <> struct Fmt<QMM_Q5_K> { static constexpr int BB = 176, BV = 256, ACT = QMM_Q8_K; };
 
 constexpr int Q8_0_BB = 34;
 constexpr int Q8_K_BB = 292;
@@ -336,6 +340,113 @@ __device__ __forceinline__ void q6_K_isums(const SmemBytes& w, uint32_t o, const
             v += (int)(int8_t)byte_of(scw[g >> 2], g & 3) * acc0;
             v += (int)(int8_t)byte_of(scw[(g + 1) >> 2], (g + 1) & 3) * acc1;
         }
+    }
+    *value = v;
+    *minterm = m;
+}
+
+// ---------------------------------------------------------------- formats with a fifth bit or a min
+// GGUF layouts (readings; the pages give the 22/24/176-byte sizes and that the
+// five-bit types add a plane of high bits):
+//   Q4_1  f16 d, f16 m, qs[16]           value d*q + m
+//   Q5_0  f16 d, qh[4], qs[16]           value d*(q - 16)
+//   Q5_1  f16 d, f16 m, qh[4], qs[16]    value d*q + m
+//   Q5_K  f16 d, f16 dmin, scales[12], qh[32], qs[128]   value d*sc_s*q - dmin*m_s
+// Nibbles as in Q4_0; bit i of the 32-bit qh is the fifth bit of element i.
+
+// bits 0..3 of x moved to bit 0 of bytes 0..3 (the four partial products of the
+// multiply land on disjoint bit ranges, so nothing carries)
+__device__ __forceinline__ uint32_t spread4(uint32_t x) { return ((x & 15u) * 0x00204081u) & 0x01010101u; }
+
+// sum_j q_j * a_j of a 32-value block given its four nibble words and (for the
+// five-bit types) the 32-bit plane of fifth bits
+template <bool FIVE>
+__device__ __forceinline__ int nib_isum(const uint32_t qs[4], uint32_t qh, const ActView& a, int b) {
+    const uint4 lo = a.chunk(b, 0), hi = a.chunk(b, 1);
+    const uint32_t al[4] = {lo.x, lo.y, lo.z, lo.w}, ah[4] = {hi.x, hi.y, hi.z, hi.w};
+    int s0 = 0, s1 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        uint32_t ql = qs[i] & 0x0F0F0F0Fu, qu = (qs[i] >> 4) & 0x0F0F0F0Fu;
+        if constexpr (FIVE) {
+            ql |= spread4(qh >> (4 * i)) << 4;
+            qu |= spread4(qh >> (16 + 4 * i)) << 4;
+        }
+        s0 = dp4a(ql, al[i], s0);
+        s1 = dp4a(qu, ah[i], s1);
+    }
+    return s0 + s1;
+}
+
+// Q4_1 x Q8_0: isum = sum q*a; the caller adds m * dx * sum(a).  20-byte blocks
+// in 16-byte aligned rows: 4-byte aligned.
+__device__ __forceinline__ int q4_1_isum(const SmemBytes& w, uint32_t o, const ActView& a, int b, uint32_t* dm_bits) {
+    *dm_bits = w.w32(o);
+    uint32_t qs[4];
+    w.words_aligned<4>(o + 4, qs);
+    return nib_isum<false>(qs, 0u, a, b);
+}
+
+// Q5_0 x Q8_0: isum = sum (q - 16)*a, the -16 applied once as -16*sum(a).
+// 22-byte blocks: 2-byte aligned.
+__device__ __forceinline__ int q5_0_isum(const SmemBytes& w, uint32_t o, const ActView& a, int b, uint32_t* d_bits) {
+    *d_bits = w.u16(o);
+    uint32_t v[5];
+    w.words<5>(o + 2, v);
+    const uint32_t qs[4] = {v[1], v[2], v[3], v[4]};
+    return nib_isum<true>(qs, v[0], a, b) - 16 * a.s[b];
+}
+
+// Q5_1 x Q8_0: isum = sum q*a; the caller adds m * dx * sum(a).  24-byte blocks:
+// 8-byte aligned.
+__device__ __forceinline__ int q5_1_isum(const SmemBytes& w, uint32_t o, const ActView& a, int b, uint32_t* dm_bits) {
+    *dm_bits = w.w32(o);
+    const uint32_t qh = w.w32(o + 4);
+    uint32_t qs[4];
+    w.words_aligned<4>(o + 8, qs);
+    return nib_isum<true>(qs, qh, a, b);
+}
+
+// Q5_K x Q8_K: the Q4_K dot with five-bit codes: element 64j + l takes bit 2j
+// of qh[l], element 64j + 32 + l bit 2j + 1.  176-byte super-blocks: 16-byte
+// aligned.
+__device__ __forceinline__ void q5_K_isums(const SmemBytes& w, uint32_t o, const ActView& a, int u, int* value,
+                                           int* minterm, uint32_t* d_bits, uint32_t* dmin_bits) {
+    const uint4 h = *reinterpret_cast<const uint4*>(w.base + o);
+    *d_bits = h.x & 0xFFFFu;
+    *dmin_bits = h.x >> 16;
+    const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
+    const uint32_t mn_lo = h.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+    const uint32_t mn_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+    int m = 0;
+#pragma unroll
+    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_lo, s) * (a.bsum(u, 2 * s) + a.bsum(u, 2 * s + 1));
+#pragma unroll
+    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_hi, s) * (a.bsum(u, 8 + 2 * s) + a.bsum(u, 9 + 2 * s));
+    const uint4 h0 = *reinterpret_cast<const uint4*>(w.base + o + 16);
+    const uint4 h1 = *reinterpret_cast<const uint4*>(w.base + o + 32);
+    const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    int v = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const uint4 q0 = *reinterpret_cast<const uint4*>(w.base + o + 48 + 32 * j);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(w.base + o + 64 + 32 * j);
+        const uint32_t q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint4 l0 = a.chunk(u, 4 * j), l1 = a.chunk(u, 4 * j + 1);
+        const uint4 g0 = a.chunk(u, 4 * j + 2), g1 = a.chunk(u, 4 * j + 3);
+        const uint32_t al[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+        const uint32_t ah[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        int s_lo = 0, s_hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t lo = (q[i] & 0x0F0F0F0Fu) | (((qh[i] >> (2 * j)) & 0x01010101u) << 4);
+            const uint32_t hi = ((q[i] >> 4) & 0x0F0F0F0Fu) | (((qh[i] >> (2 * j + 1)) & 0x01010101u) << 4);
+            s_lo = dp4a(lo, al[i], s_lo);
+            s_hi = dp4a(hi, ah[i], s_hi);
+        }
+        const uint32_t scw = j < 2 ? sc_lo : sc_hi;
+        v += s_lo * (int)byte_of(scw, (2 * j) & 3) + s_hi * (int)byte_of(scw, (2 * j + 1) & 3);
     }
     *value = v;
     *minterm = m;

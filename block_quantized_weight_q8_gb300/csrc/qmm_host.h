@@ -16,8 +16,8 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 inline int block_values_of(int t) {
     switch (t) {
-    case QMM_Q4_0: case QMM_Q8_0: return 32;
-    case QMM_Q4_K: case QMM_Q6_K: case QMM_Q2_K: case QMM_Q8_K: return 256;
+    case QMM_Q4_0: case QMM_Q8_0: case QMM_Q4_1: case QMM_Q5_0: case QMM_Q5_1: return 32;
+    case QMM_Q4_K: case QMM_Q6_K: case QMM_Q2_K: case QMM_Q8_K: case QMM_Q5_K: return 256;
     default: return 0;
     }
 }
@@ -29,13 +29,17 @@ inline size_t block_bytes_of(int t) {
     case QMM_Q6_K: return 210;
     case QMM_Q2_K: return 84;
     case QMM_Q8_K: return 292;
+    case QMM_Q4_1: return 20;
+    case QMM_Q5_0: return 22;
+    case QMM_Q5_1: return 24;
+    case QMM_Q5_K: return 176;
     default: return 0;
     }
 }
 inline int act_type_of(int wt) {
     switch (wt) {
-    case QMM_Q4_0: case QMM_Q8_0: return QMM_Q8_0;
-    case QMM_Q4_K: case QMM_Q6_K: case QMM_Q2_K: return QMM_Q8_K;
+    case QMM_Q4_0: case QMM_Q8_0: case QMM_Q4_1: case QMM_Q5_0: case QMM_Q5_1: return QMM_Q8_0;
+    case QMM_Q4_K: case QMM_Q6_K: case QMM_Q2_K: case QMM_Q5_K: return QMM_Q8_K;
     default: return -1;
     }
 }

@@ -84,8 +84,22 @@ typedef enum {
  *         value d*sc_g*(q-32) per 16-value group       (GGUF layout, a reading)
  *   Q2_K: scales[16] @0 (sc low, m high nibble), qs[64] @16, f16 d @80,
  *         f16 dmin @82; value d*sc_g*q - dmin*m_g                   [ggml] s1.2
- *   Q8_K: f32 d @0, int8 qs[256] @4, int16 bsums[16] @260 (activations only) */
-typedef enum { QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_Q4_K = 2, QMM_Q6_K = 3, QMM_Q2_K = 4, QMM_Q8_K = 5 } qmm_type;
+ *   Q8_K: f32 d @0, int8 qs[256] @4, int16 bsums[16] @260 (activations only)
+ * Q4_1 20 B / 32, Q5_0 22 B / 32, Q5_1 24 B / 32, Q5_K 176 B / 256 ([minfer] s1
+ * and s3.2 give the 22/24/176-B sizes and that the five-bit types add a plane of
+ * high bits; the byte layouts are GGUF's, a reading):
+ *   Q4_1: f16 d @0, f16 m @2, qs[16] @4; value d*q + m (q the nibble)
+ *   Q5_0: f16 d @0, qh[4] @2, qs[16] @6; value d*(q-16)
+ *   Q5_1: f16 d @0, f16 m @2, qh[4] @4, qs[16] @8; value d*q + m
+ *         (q = nibble as in Q4_0, plus bit i of the 32-bit qh as bit 4 of element i)
+ *   Q5_K: f16 d @0, f16 dmin @2, scales @4 (the Q4_K packing), qh[32] @16,
+ *         qs[128] @48; element 64j+l (64j+32+l) is the low (high) nibble of
+ *         qs[32j+l] plus bit 2j (2j+1) of qh[l] as bit 4; value d*sc_s*q - dmin*m_s
+ * Q4_1, Q5_0 and Q5_1 pair with Q8_0 activations, Q5_K with Q8_K. */
+typedef enum {
+    QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_Q4_K = 2, QMM_Q6_K = 3, QMM_Q2_K = 4, QMM_Q8_K = 5,
+    QMM_Q4_1 = 6, QMM_Q5_0 = 7, QMM_Q5_1 = 8, QMM_Q5_K = 9
+} qmm_type;
 
 typedef void* qmm_stream_t; /* a cudaStream_t */
 
@@ -145,6 +159,11 @@ QMM_API qmm_status qmm_quantize_q2_K(const float* w, void* wq, int64_t N, int64_
  *     min_term = sum of m * (activation group sums from bsums)
  *     ([minfer] s3.2, the K-quant dot walked; [ggml] s1.2).
  *   Q6_K (x in Q8_K): y += (d_w*d_x) * sum_g sc_g * sum (q-32)*a (reading).
+ *   Q5_0 (x in Q8_0): as Q4_0 with isum_b = sum (q-16)*a.
+ *   Q4_1, Q5_1 (x in Q8_0): y += (float)isum_b * d_w * d_x + (float)asum_b *
+ *     m_w * d_x, isum_b = sum q*a and asum_b the exact sum of the activation
+ *     block's codes (the min meets it: sum (d q + m) a = d sum q a + m sum a).
+ *   Q5_K (x in Q8_K): as Q4_K with five-bit codes.
  * W: N rows; xq: one activation row; y: f32 [N].  The fp32 fold per thread and
  * the reduction across threads follow a fixed order, which differs from a
  * left-to-right scalar sum; results agree with one within 1e-5 of the row's
@@ -154,6 +173,10 @@ QMM_API qmm_status qmm_matvec_q8_0(const void* W, const void* xq, float* y, int6
 QMM_API qmm_status qmm_matvec_q4_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_matvec_q6_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_matvec_q2_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_matvec_q4_1(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_matvec_q5_0(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_matvec_q5_1(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_matvec_q5_K(const void* W, const void* xq, float* y, int64_t N, int64_t K, qmm_stream_t stream);
 
 /* ---- quantize + matvec with the pairing fixed (hot path) ---------------- */
 /* [minfer] s3.2 (cpu_quant_matmul_f32): the activation format is chosen by the
@@ -164,7 +187,9 @@ QMM_API qmm_status qmm_matvec_q2_K(const void* W, const void* xq, float* y, int6
  * row it needs, with the same arithmetic as qmm_quantize_q8_0/q8_K, and one CTA
  * stores it to the scratch), so a token is one launch; a row too large for that
  * kernel's shared memory is quantized by the separate quantizer first.  Q4_0 with
- * M >= 8 and K % 256 == 0 quantizes all rows, then runs the prefill matmul. */
+ * M >= 8 and K % 256 == 0, and Q4_K / Q6_K / Q2_K with M >= 8 and K % 2048 == 0,
+ * quantize all rows, then run the prefill matmul.  The other types multiply
+ * token by token at every M. */
 QMM_API qmm_status qmm_linear_q4_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
                            int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_linear_q8_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
@@ -174,6 +199,14 @@ QMM_API qmm_status qmm_linear_q4_K(const void* W, const float* x, void* xq_scrat
 QMM_API qmm_status qmm_linear_q6_K(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
                            int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_linear_q2_K(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_q4_1(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_q5_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_q5_1(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
+                           int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_q5_K(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
                            int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
 
 /* ---- quantize + multiply without a caller workspace ---------------------- */
@@ -246,8 +279,9 @@ QMM_API qmm_status qmm_matmul_q2_K(const void* W, const void* xq, float* Y, int6
 /* out[r][k] = value k of row ids[r] of W, dequantized ([minfer] s3.2, "The
  * embedding 'matmul'": each token id's row walked block by block, scale x code).
  * Each value is computed in f32 with at most one rounding (Q4_0 d*(n-8), Q8_0
- * d*q, Q6_K (d*sc)*(q-32): exact; Q4_K and Q2_K fma(d*sc, q, -(dmin*m)): one
- * rounding), so it equals the exact dequantized value rounded once to f32.
+ * d*q, Q6_K (d*sc)*(q-32), Q5_0 d*(q-16): exact; Q4_K, Q5_K and Q2_K
+ * fma(d*sc, q, -(dmin*m)), Q4_1 and Q5_1 fma(d, q, m): one rounding), so it
+ * equals the exact dequantized value rounded once to f32.
  * W: N rows of wtype (a weight type); ids: int32 [R] device array; out: f32
  * [R][K].  An id outside [0, N) gives a zero row and makes qmm_device_status()
  * return QMM_E_SHAPE. */
@@ -261,7 +295,8 @@ QMM_API qmm_status qmm_get_rows(int wtype, const void* W, const int32_t* ids, fl
  * (value term, min term) -- Q4_K: (sum_s sc_s*dot_s, sum_s m_s*(bsum_2s +
  * bsum_2s+1)); Q2_K: (sum_g sc_g*dot_g, sum_g m_g*bsum_g); Q6_K: (sum_g sc_g *
  * dot_g with the stored codes 0..63, sum_g sc_g*bsum_g), whose integer is
- * value - 32*min.  s: int32 [M][N][per-row count], computed by the same device
+ * value - 32*min; Q5_K as Q4_K.  Q5_0 gives sum (q-16)*a per block, Q4_1 and
+ * Q5_1 sum q*a (their min meets the activation's own code sum).  s: int32 [M][N][per-row count], computed by the same device
  * decode routines the matvec uses. */
 QMM_API qmm_status qmm_blocksums(int wtype, const void* W, const void* xq, int32_t* s, int64_t M, int64_t N, int64_t K,
                          qmm_stream_t stream);

@@ -54,9 +54,13 @@ def test_header_compiles_as_c(tmp_path):
 
 def test_formats(lib):
     sizes = {"q4_0": (18, 32), "q8_0": (34, 32), "q4_K": (144, 256), "q6_K": (210, 256), "q2_K": (84, 256),
-             "q8_K": (292, 256)}
+             "q8_K": (292, 256), "q4_1": (20, 32), "q5_0": (22, 32), "q5_1": (24, 32), "q5_K": (176, 256)}
     for t, (bb, bv) in sizes.items():
         assert qmm.qmm_block_bytes(t) == bb and qmm.qmm_block_values(t) == bv
+    for t in ("q4_1", "q5_0", "q5_1"):
+        assert qmm.qmm_act_type(t) == qmm.QMM_Q8_0
+    assert qmm.qmm_act_type("q5_K") == qmm.QMM_Q8_K
+    assert qmm.qmm_block_bytes(10) == 0
     assert qmm.qmm_row_bytes("q4_0", 896) == 504
     assert qmm.qmm_row_bytes("q8_0", 4096) == 4352
     assert qmm.qmm_row_bytes("q4_K", 4096) == 16 * 144
@@ -156,7 +160,7 @@ def test_matmul_and_blocksums_reject_bad_arguments(lib):
         assert f(A, A, None, 8, 64, 2048, None) == 1
         assert f(A, U, A, 8, 64, 2048, None) == 4
         assert f(A, A, A, 8, 64, 1000, None) == 2
-    assert lib.qmm_blocksums(7, A, A, A, 1, 1, 256, None) == 3
+    assert lib.qmm_blocksums(10, A, A, A, 1, 1, 256, None) == 3
     assert lib.qmm_blocksums(qmm.QMM_Q8_K, A, A, A, 1, 1, 256, None) == 3   # not a weight type
     assert lib.qmm_blocksums(qmm.QMM_Q4_K, A, A, A, 1, 1, 128, None) == 2
 

@@ -17,7 +17,7 @@ import block_quantized_weight_q8_gb300 as qmm  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
-WTYPES = ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K"]
+WTYPES = ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K", "q4_1", "q5_0", "q5_1", "q5_K"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,7 +40,7 @@ def host(t):
 
 
 def act_name(wtype):
-    return "q8_0" if wtype in ("q4_0", "q8_0") else "q8_K"
+    return "q8_0" if wtype in ("q4_0", "q8_0", "q4_1", "q5_0", "q5_1") else "q8_K"
 
 
 def assert_rows_close(y, ref, tol=TOL):
@@ -81,7 +81,8 @@ def test_max_k(wtype):
 
 
 @pytest.mark.parametrize("wtype,K", [("q8_0", 4128), ("q4_0", 4128), ("q8_0", 4160), ("q4_0", 96),
-                                     ("q4_K", 4352), ("q6_K", 4352), ("q2_K", 4352), ("q6_K", 12288)])
+                                     ("q4_K", 4352), ("q6_K", 4352), ("q2_K", 4352), ("q6_K", 12288),
+                                     ("q4_1", 4160), ("q5_0", 4128), ("q5_1", 4096), ("q5_K", 4352)])
 def test_short_last_segment(wtype, K):
     """Rows cut into segments with a shorter last one (129 Q8_0 blocks: 16 segments of 8 and one
     of 1; 17 super-blocks: 3 segments of 6, 6, 5), and rows of blocks that do not form aligned
@@ -92,7 +93,7 @@ def test_short_last_segment(wtype, K):
 @pytest.mark.parametrize("wtype", WTYPES)
 def test_one_row_per_cta_and_idle_warps(wtype):
     """Fewer rows than SMs x warps: most warps of most CTAs have no item."""
-    K = 256 if wtype in ("q4_K", "q6_K", "q2_K") else 64
+    K = 256 if wtype in ("q4_K", "q6_K", "q2_K", "q5_K") else 64
     check_matvec_and_linear(wtype, 3, 150, K, seed=90)
 
 
@@ -104,7 +105,8 @@ def test_linear_token_rows_of_odd_alignment():
 
 @pytest.mark.parametrize("wtype,Ns,K,M", [("q4_K", (300, 77, 1024), 4096, 1), ("q4_K", (4096, 1024, 1024), 4096, 2),
                                           ("q8_0", (129, 4096), 4096, 1), ("q4_0", (64, 33, 5, 700), 896, 3),
-                                          ("q6_K", (512, 257), 12288, 1), ("q2_K", (12288,), 4096, 1)])
+                                          ("q6_K", (512, 257), 12288, 1), ("q2_K", (12288,), 4096, 1),
+                                          ("q5_1", (64, 33), 896, 2), ("q5_K", (300, 77), 4096, 1)])
 def test_linear_group_matches_oracle_and_linear(wtype, Ns, K, M):
     """qmm_linear_group: every matrix's output equals the oracle within tolerance and qmm_linear_<w> on
     that matrix alone bit for bit; the scratch holds the quantized rows."""
@@ -130,7 +132,8 @@ def test_linear_group_matches_oracle_and_linear(wtype, Ns, K, M):
 
 
 @pytest.mark.parametrize("wtype,N,K", [("q4_0", 300, 896), ("q8_0", 129, 4096), ("q4_K", 77, 4096), ("q6_K", 50, 12288),
-                                       ("q2_K", 33, 768)])
+                                       ("q2_K", 33, 768), ("q4_1", 40, 896), ("q5_0", 41, 4096), ("q5_1", 9, 96),
+                                       ("q5_K", 20, 4096)])
 def test_get_rows_bitexact(wtype, N, K):
     """qmm_get_rows equals the oracle's exact dequantized rows rounded once to f32, bit for bit; ids repeat
     and cover the first and last rows."""

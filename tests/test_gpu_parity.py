@@ -16,7 +16,7 @@ import block_quantized_weight_q8_gb300 as qmm  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
-WTYPES = ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K"]
+WTYPES = ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K", "q4_1", "q5_0", "q5_1", "q5_K"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -47,11 +47,11 @@ def f32(*shape):
 
 
 def bv(t):
-    return 256 if t in ("q4_K", "q6_K", "q2_K", "q8_K") else 32
+    return 256 if t in ("q4_K", "q6_K", "q2_K", "q8_K", "q5_K") else 32
 
 
 def act_name(wtype):
-    return "q8_0" if wtype in ("q4_0", "q8_0") else "q8_K"
+    return "q8_0" if wtype in ("q4_0", "q8_0", "q4_1", "q5_0", "q5_1") else "q8_K"
 
 
 def assert_rows_close(y, ref, tol=TOL):
@@ -149,7 +149,8 @@ def test_matvec_matches_oracle(wtype, N, K):
 
 
 @pytest.mark.parametrize("wtype,N,K", [("q4_0", 7, 32), ("q4_0", 3, 96), ("q8_0", 5, 32), ("q6_K", 3, 256),
-                                       ("q2_K", 1, 256), ("q6_K", 1, 768), ("q4_0", 1, 32)])
+                                       ("q2_K", 1, 256), ("q6_K", 1, 768), ("q4_0", 1, 32), ("q4_1", 3, 32),
+                                       ("q5_0", 5, 96), ("q5_1", 1, 32), ("q5_0", 1, 32), ("q5_K", 3, 256)])
 def test_matvec_unaligned_tail(wtype, N, K):
     """W of N * row_bytes bytes that is not a multiple of 16: the last bytes take the plain path."""
     W, X = make_inputs(wtype, 1, N, K, seed=5000 + N)

@@ -37,9 +37,10 @@ def _close(y, ref):
 
 
 @pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 1, 12288, 4096), ("q4_0", 1, 4864, 896), ("q4_K", 1, 4096, 4096),
-                                         ("q6_K", 1, 1024, 12288), ("q2_K", 3, 777, 1024), ("q4_0", 5, 300, 1024)])
+                                         ("q6_K", 1, 1024, 12288), ("q2_K", 3, 777, 1024), ("q4_0", 5, 300, 1024),
+                                         ("q5_1", 2, 500, 4096), ("q5_K", 1, 4096, 4096)])
 def test_noalloc_matches_linear_twice(lib, wtype, M, N, K):
-    act = "q8_0" if wtype in ("q4_0", "q8_0") else "q8_K"
+    act = "q8_0" if wtype in ("q4_0", "q8_0", "q4_1", "q5_0", "q5_1") else "q8_K"
     W = torch.from_numpy(oracle.quantize(wtype, workloads.weights_f32(N, K, seed=31, row_jitter=True))).cuda()
     sb = M * qmm.qmm_row_bytes(act, K)
     scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
