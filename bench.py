@@ -390,7 +390,8 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     # single matvecs
-    for name in ("q4_0_matvec_4864x896", "q2_K_matvec_12288x4096"):
+    for name in ("q4_0_matvec_4864x896", "q2_K_matvec_12288x4096", "q4_1_matvec_12288x4096",
+                 "q5_0_matvec_12288x4096", "q5_1_matvec_12288x4096", "q5_K_matvec_12288x4096"):
         cfg = workloads.WORKLOADS[name]
         wtype, N, K = cfg["wtype"], cfg["N"], cfg["K"]
         W0 = quantized_weights(wtype, N, K, cfg["seed"])

@@ -35,6 +35,10 @@ SIGNATURES = {
     "qmm_quantize_q4_K": ("ppiiq", ctypes.c_int),
     "qmm_quantize_q6_K": ("ppiiq", ctypes.c_int),
     "qmm_quantize_q2_K": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q4_1": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q5_0": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q5_1": ("ppiiq", ctypes.c_int),
+    "qmm_quantize_q5_K": ("ppiiq", ctypes.c_int),
     "qmm_matvec_q4_0": ("pppiiq", ctypes.c_int),
     "qmm_matvec_q8_0": ("pppiiq", ctypes.c_int),
     "qmm_matvec_q4_K": ("pppiiq", ctypes.c_int),

@@ -1,5 +1,6 @@
 // quantize.cu -- the activation quantizers (Q8_0, Q8_K) on the hot path, and
-// the weight quantizers (Q4_0, Q4_K, Q6_K, Q2_K) used to prepare inputs.
+// the weight quantizers (Q4_0, Q4_K, Q6_K, Q2_K, Q4_1, Q5_0, Q5_1, Q5_K) used
+// to prepare inputs.
 //
 // Every float operation is written with an explicitly IEEE-rounded intrinsic
 // (__fdiv_rn, __fmul_rn, __fadd_rn, __float2int_rn, __float2half_rn), so that
@@ -276,6 +277,133 @@ qmm_status quantize_act_launch(int act, const float* x, void* xq, int64_t M, int
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
+// ---------------------------------------------------------------- Q4_1 / Q5_1 weights
+// A reading (the pages give no quantizer for them): a min/max grid per block of
+// 32, m = min x, d = (max x - m) / levels, codes min(levels, trunc((x - m) *
+// (1/d) + 0.5)) with the f32 d and m, both stored as f16.  Layouts (GGUF): Q4_1
+// d @0, m @2, nibbles @4; Q5_1 d @0, m @2, fifth bits @4, nibbles @8.
+template <int LEVELS, int BB, int QH, int QS>
+__global__ void quantize_minmax_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t nblocks) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const float* xb = x + b * 32;
+    float lo = xb[0], hi = xb[0];
+    for (int i = 1; i < 32; i++) {
+        const float v = xb[i];
+        if (v < lo) lo = v;
+        if (v > hi) hi = v;
+    }
+    const float d = __fdiv_rn(__fsub_rn(hi, lo), (float)LEVELS);
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    uint8_t* ob = out + b * BB;
+    st_u16(ob, f2h_bits(d));
+    st_u16(ob + 2, f2h_bits(lo));
+    uint32_t qh = 0;
+    for (int j = 0; j < 16; j++) {
+        const int c0 = clampi(__float2int_rz(__fadd_rn(__fmul_rn(__fsub_rn(xb[j], lo), id), 0.5f)), 0, LEVELS);
+        const int c1 = clampi(__float2int_rz(__fadd_rn(__fmul_rn(__fsub_rn(xb[j + 16], lo), id), 0.5f)), 0, LEVELS);
+        ob[QS + j] = (uint8_t)((c0 & 15) | ((c1 & 15) << 4));
+        qh |= (uint32_t)(c0 >> 4) << j;
+        qh |= (uint32_t)(c1 >> 4) << (j + 16);
+    }
+    if constexpr (QH >= 0) {
+        st_u16(ob + QH, qh & 0xFFFFu);
+        st_u16(ob + QH + 2, qh >> 16);
+    }
+}
+
+// ---------------------------------------------------------------- Q5_0 weights
+// A reading: the Q4_0 scheme on five bits.  m = the value of largest magnitude
+// (first on a tie), d = m / -16, codes min(31, trunc(x * (1/d) + 16.5)).
+// Layout (GGUF): d @0, fifth bits @2, nibbles @6.
+__global__ void quantize_q5_0_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t nblocks) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const float* xb = x + b * 32;
+    float amax = 0.0f, m = 0.0f;
+    for (int i = 0; i < 32; i++) {
+        const float v = xb[i];
+        if (fabsf(v) > amax) { amax = fabsf(v); m = v; }
+    }
+    const float d = __fdiv_rn(m, -16.0f);
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    uint8_t* ob = out + b * 22;
+    st_u16(ob, f2h_bits(d));
+    uint32_t qh = 0;
+    for (int j = 0; j < 16; j++) {
+        const int c0 = clampi(__float2int_rz(__fadd_rn(__fmul_rn(xb[j], id), 16.5f)), 0, 31);
+        const int c1 = clampi(__float2int_rz(__fadd_rn(__fmul_rn(xb[j + 16], id), 16.5f)), 0, 31);
+        ob[6 + j] = (uint8_t)((c0 & 15) | ((c1 & 15) << 4));
+        qh |= (uint32_t)(c0 >> 4) << j;
+        qh |= (uint32_t)(c1 >> 4) << (j + 16);
+    }
+    st_u16(ob + 2, qh & 0xFFFFu);
+    st_u16(ob + 4, qh >> 16);
+}
+
+// ---------------------------------------------------------------- Q5_K weights
+// A reading: the Q4_K scheme with codes 0..31 (scale_s = (max x + min_s)/31).
+// Layout (GGUF): d @0, dmin @2, packed scales @4, qh[32] @16, qs[128] @48;
+// element 64j + l: low nibble of qs[32j + l], fifth bit 2j of qh[l]; element
+// 64j + 32 + l: high nibble, bit 2j + 1.
+__global__ void quantize_q5_K_kernel(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t nblocks) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const float* xb = x + b * 256;
+    uint8_t* ob = out + b * 176;
+    float scl[8], mns[8];
+    float maxscl = 0.0f, maxmin = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 8; s++) {
+        float lo = xb[32 * s], hi = xb[32 * s];
+        for (int i = 1; i < 32; i++) {
+            const float v = xb[32 * s + i];
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        mns[s] = lo < 0.0f ? -lo : 0.0f;
+        scl[s] = __fdiv_rn(__fadd_rn(hi, mns[s]), 31.0f);
+        if (scl[s] > maxscl) maxscl = scl[s];
+        if (mns[s] > maxmin) maxmin = mns[s];
+    }
+    const float d = __fdiv_rn(maxscl, 63.0f), dmin = __fdiv_rn(maxmin, 63.0f);
+    const uint32_t dh = f2h_bits(d), dmh = f2h_bits(dmin);
+    st_u16(ob, dh);
+    st_u16(ob + 2, dmh);
+    int sc[8], mn[8];
+#pragma unroll
+    for (int s = 0; s < 8; s++) {
+        sc[s] = d > 0.0f ? clampi(__float2int_rn(__fdiv_rn(scl[s], d)), 0, 63) : 0;
+        mn[s] = dmin > 0.0f ? clampi(__float2int_rn(__fdiv_rn(mns[s], dmin)), 0, 63) : 0;
+    }
+#pragma unroll
+    for (int s = 0; s < 4; s++) {
+        ob[4 + s] = (uint8_t)((sc[s] & 63) | ((sc[s + 4] >> 4) << 6));
+        ob[8 + s] = (uint8_t)((mn[s] & 63) | ((mn[s + 4] >> 4) << 6));
+        ob[12 + s] = (uint8_t)((sc[s + 4] & 15) | ((mn[s + 4] & 15) << 4));
+    }
+    const float df = h2f(dh), dmf = h2f(dmh);
+    float ds[8], dm[8];
+#pragma unroll
+    for (int s = 0; s < 8; s++) {
+        ds[s] = __fmul_rn(df, (float)sc[s]);
+        dm[s] = __fmul_rn(dmf, (float)mn[s]);
+    }
+    for (int l = 0; l < 32; l++) {
+        uint32_t qh = 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int s0 = 2 * j, s1 = 2 * j + 1;
+            const float v0 = xb[64 * j + l], v1 = xb[64 * j + 32 + l];
+            const int c0 = ds[s0] > 0.0f ? clampi(__float2int_rn(__fdiv_rn(__fadd_rn(v0, dm[s0]), ds[s0])), 0, 31) : 0;
+            const int c1 = ds[s1] > 0.0f ? clampi(__float2int_rn(__fdiv_rn(__fadd_rn(v1, dm[s1]), ds[s1])), 0, 31) : 0;
+            ob[48 + 32 * j + l] = (uint8_t)((c0 & 15) | ((c1 & 15) << 4));
+            qh |= (uint32_t)((c0 >> 4) << (2 * j)) | (uint32_t)((c1 >> 4) << (2 * j + 1));
+        }
+        ob[16 + l] = (uint8_t)qh;
+    }
+}
+
 template <class Kern>
 static qmm_status launch_weight_quant(Kern kern, int t, const float* w, void* wq, int64_t N, int64_t K,
                                       cudaStream_t stream) {
@@ -317,6 +445,18 @@ qmm_status qmm_quantize_q6_K(const float* w, void* wq, int64_t N, int64_t K, qmm
 }
 qmm_status qmm_quantize_q2_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream) {
     return launch_weight_quant(quantize_q2_K_kernel, QMM_Q2_K, w, wq, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_quantize_q4_1(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream) {
+    return launch_weight_quant(quantize_minmax_kernel<15, 20, -1, 4>, QMM_Q4_1, w, wq, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_quantize_q5_0(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream) {
+    return launch_weight_quant(quantize_q5_0_kernel, QMM_Q5_0, w, wq, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_quantize_q5_1(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream) {
+    return launch_weight_quant(quantize_minmax_kernel<31, 24, 4, 8>, QMM_Q5_1, w, wq, N, K, (cudaStream_t)stream);
+}
+qmm_status qmm_quantize_q5_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream) {
+    return launch_weight_quant(quantize_q5_K_kernel, QMM_Q5_K, w, wq, N, K, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -143,11 +143,20 @@ QMM_API qmm_status qmm_quantize_q8_K(const float* x, void* xq, int64_t M, int64_
  *   Q6_K (reading): per group the signed extreme m_g, s_g = m_g / -32;
  *     d = max|s_g| / 127 (f16), int8 sc_g = rne(s_g/d), codes
  *     rne(x / (f16(d)*sc_g)) in -32..31, stored +32.
+ *   Q4_1, Q5_1 (reading): m = min x, d = (max x - m) / 15 (31), codes
+ *     min(15 (31), trunc((x - m) * (1/d) + 0.5)); d and m stored as f16.
+ *   Q5_0 (reading): the Q4_0 scheme on five bits: d = m / -16, codes
+ *     min(31, trunc(x / d + 16.5)).
+ *   Q5_K (reading): the Q4_K scheme with (max x + min_s)/31 and codes 0..31.
  * Q8_0 weights use qmm_quantize_q8_0. */
 QMM_API qmm_status qmm_quantize_q4_0(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_quantize_q4_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_quantize_q6_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_quantize_q2_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_quantize_q4_1(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_quantize_q5_0(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_quantize_q5_1(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_quantize_q5_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream);
 
 /* ---- decode matvec, one token (hot path) -------------------------------- */
 /* y[o] = sum over blocks b of the row's block dot, folded in fp32:

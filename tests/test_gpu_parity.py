@@ -98,7 +98,7 @@ def test_activation_quantizer_bitexact(t, M, K):
 
 
 # ------------------------------------------------------------------ weight quantizers
-@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_K", "q6_K", "q2_K", "q4_1", "q5_0", "q5_1", "q5_K"])
 @pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (33, 1024)])
 def test_weight_quantizer_bitexact(t, N, K):
     w = workloads.weights_f32(N, K, seed=2000 + N, row_jitter=True)
@@ -234,7 +234,9 @@ def _full_matvec(name):
     assert_rows_close(host(y), ref)
 
 
-@pytest.mark.parametrize("name", ["q4_0_matvec_4864x896", "q8_0_matvec_12288x4096", "q2_K_matvec_12288x4096"])
+@pytest.mark.parametrize("name", ["q4_0_matvec_4864x896", "q8_0_matvec_12288x4096", "q2_K_matvec_12288x4096",
+                                  "q4_1_matvec_12288x4096", "q5_0_matvec_12288x4096", "q5_1_matvec_12288x4096",
+                                  "q5_K_matvec_12288x4096"])
 def test_full_size_matvec(name):
     _full_matvec(name)
 

@@ -17,6 +17,8 @@ Shapes (N rows x K input dim, M tokens):
                     W_gate, W_up 12288x4096 in Q4_K; W_down 4096x12288 in Q6_K
   q2_K matvec       12288 x 4096, M=1
   q4_0 prefill      M in {128, 512, 2048} x 12288 x 4096
+  q4_1 / q5_0 / q5_1 / q5_K matvecs   12288 x 4096, M=1 (the other formats the
+                    pages list, on the FFN shape)
 """
 from __future__ import annotations
 
@@ -44,6 +46,10 @@ WORKLOADS = {
     "q2_K_matvec_12288x4096": dict(kind="matvec", wtype="q2_K", M=1, N=12288, K=4096, seed=0xC0FFEE + 3),
     "q4_0_prefill_512x12288x4096": dict(kind="matmul", wtype="q4_0", M=512, N=12288, K=4096,
                                         seed=0xC0FFEE + 4, M_sweep=(128, 512, 2048)),
+    "q4_1_matvec_12288x4096": dict(kind="matvec", wtype="q4_1", M=1, N=12288, K=4096, seed=0xC0FFEE + 5),
+    "q5_0_matvec_12288x4096": dict(kind="matvec", wtype="q5_0", M=1, N=12288, K=4096, seed=0xC0FFEE + 6),
+    "q5_1_matvec_12288x4096": dict(kind="matvec", wtype="q5_1", M=1, N=12288, K=4096, seed=0xC0FFEE + 7),
+    "q5_K_matvec_12288x4096": dict(kind="matvec", wtype="q5_K", M=1, N=12288, K=4096, seed=0xC0FFEE + 8),
 }
 
 
