@@ -78,6 +78,13 @@ def load(path: str):
     L.orc_blocksums.restype = None
     L.orc_matmul_exact.argtypes = [i32, p, p, p, i64, i64, i64, i32]
     L.orc_matmul_exact.restype = None
+    L.orc_kv_row_bytes.argtypes = [i32]
+    L.orc_kv_quantize.argtypes = [p, p, i64, i32]
+    L.orc_kv_quantize.restype = None
+    L.orc_kv_scores.argtypes = [p, p, p, i32, i32, i64, i32, ctypes.c_float]
+    L.orc_kv_scores.restype = None
+    L.orc_kv_wsum.argtypes = [p, p, p, i32, i32, i64, i32]
+    L.orc_kv_wsum.restype = None
     return L
 
 
@@ -214,3 +221,38 @@ def dot_row(wtype, wrow, xrow, K) -> float:
     wrow = np.ascontiguousarray(wrow, dtype=np.uint8)
     xrow = np.ascontiguousarray(xrow, dtype=np.uint8)
     return float(lib().orc_dot_row(_t(wtype), _ptr(wrow), _ptr(xrow), K))
+
+
+# ---- the Q8 KV cache ([krafla] "Architecture", Attention: "Q8 cache")
+def kv_row_bytes(hd: int) -> int:
+    """Bytes of one quantized head vector: f32 scale + hd int8 codes."""
+    return int(lib().orc_kv_row_bytes(hd))
+
+
+def kv_quantize(x: np.ndarray, hd: int) -> np.ndarray:
+    """f32 [..., hd] head vectors -> uint8 [rows, 4 + hd] (f32 d, int8 codes), the activations' rule."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, hd)
+    out = np.zeros((x.shape[0], kv_row_bytes(hd)), dtype=np.uint8)
+    lib().orc_kv_quantize(_ptr(x), _ptr(out), x.shape[0], hd)
+    return out
+
+
+def kv_scores(q8: np.ndarray, k8: np.ndarray, Hq: int, Hkv: int, P: int, hd: int, scale: float = 1.0) -> np.ndarray:
+    """f32 [Hq, P]: ((dq * dk) * isum) * scale, query head h against KV head h // (Hq // Hkv);
+    k8 holds row (p, kvh) at index p * Hkv + kvh."""
+    q8 = np.ascontiguousarray(q8, dtype=np.uint8)
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8)
+    assert q8.size == Hq * kv_row_bytes(hd) and k8.size >= P * Hkv * kv_row_bytes(hd) and Hq % Hkv == 0
+    out = np.zeros((Hq, P), dtype=np.float32)
+    lib().orc_kv_scores(_ptr(q8), _ptr(k8), _ptr(out), Hq, Hkv, P, hd, ctypes.c_float(scale))
+    return out
+
+
+def kv_wsum(w: np.ndarray, v8: np.ndarray, Hq: int, Hkv: int, P: int, hd: int) -> np.ndarray:
+    """float64 [Hq, hd]: sum_p w[h, p] * dv[p, kvh] * v[p, kvh, :], exact up to binary64 rounding."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    v8 = np.ascontiguousarray(v8, dtype=np.uint8)
+    assert w.size == Hq * P and v8.size >= P * Hkv * kv_row_bytes(hd) and Hq % Hkv == 0
+    out = np.zeros((Hq, hd), dtype=np.float64)
+    lib().orc_kv_wsum(_ptr(w), _ptr(v8), _ptr(out), Hq, Hkv, P, hd)
+    return out

@@ -1001,3 +1001,71 @@ void orc_matmul_exact(int wtype, const uint8_t* W, const uint8_t* X, double* out
             out[t * N + o] = bruteforce ? orc_dot_row_bruteforce(wtype, W + o * ws, X + t * xs, K)
                                         : orc_dot_row_exact(wtype, W + o * ws, X + t * xs, K);
 }
+
+/* ------------------------------------------------------------------------- */
+/* The Q8 KV cache.  [krafla] "Architecture", Attention ("Q8 cache"): each    */
+/* position's K and V are stored per KV head as int8 codes with one float     */
+/* scale, quantized by the activations' rule; each query head is quantized   */
+/* the same way; the scores are integer dot products, and the V sum widens    */
+/* the int8 values to float as it goes (head_dim 64: 68 bytes per head).      */
+/* Readings:                                                                  */
+/*   - a row is one head vector of hd values: f32 d @0, int8 codes @4         */
+/*     (4 + hd bytes); the rule is the Q8_0 one (amax, d = amax/127, codes    */
+/*     nearest-even of x*127/amax) over the whole head vector;               */
+/*   - the cache holds row (p, kvh) at (p*Hkv + kvh) * (4 + hd): a position's */
+/*     heads side by side, positions appended in order;                       */
+/*   - query head h reads KV head h / (Hq/Hkv) (heads that share a KV head    */
+/*     are consecutive);                                                      */
+/*   - a score is ((dq * dk) * isum) * scale in f32 (isum exact: |isum| <=    */
+/*     hd * 128 * 128 < 2^24), scale the caller's factor (1/sqrt(hd) for      */
+/*     attention);                                                            */
+/*   - the V sum out[h][i] = sum_p w[h][p] * dv[p] * v[p][i] is given here    */
+/*     exactly (binary64): the device sums in f32, so it is checked against   */
+/*     an error bound, not bit for bit.                                       */
+/* ------------------------------------------------------------------------- */
+int orc_kv_row_bytes(int hd) { return 4 + hd; }
+
+void orc_kv_quantize(const float* x, uint8_t* out, int64_t rows, int hd) {
+    for (int64_t r = 0; r < rows; r++) {
+        const float* xr = x + r * hd;
+        uint8_t* o = out + r * (4 + hd);
+        float amax = 0.0f;
+        for (int i = 0; i < hd; i++) {
+            float a = fabsf(xr[i]);
+            if (a > amax) amax = a;
+        }
+        wrf32(o, amax / 127.0f);
+        float id = (amax != 0.0f) ? 127.0f / amax : 0.0f;
+        for (int i = 0; i < hd; i++) o[4 + i] = (uint8_t)(int8_t)clampi(rne(xr[i] * id), -128, 127);
+    }
+}
+
+void orc_kv_scores(const uint8_t* q, const uint8_t* kc, float* s, int Hq, int Hkv, int64_t P, int hd, float scale) {
+    const int G = Hq / Hkv, rb = 4 + hd;
+    for (int h = 0; h < Hq; h++) {
+        const uint8_t* qr = q + (int64_t)h * rb;
+        const int kvh = h / G;
+        for (int64_t p = 0; p < P; p++) {
+            const uint8_t* kr = kc + (p * Hkv + kvh) * rb;
+            int32_t isum = 0;
+            for (int i = 0; i < hd; i++) isum += (int8_t)qr[4 + i] * (int8_t)kr[4 + i];
+            float dd = rdf32(qr) * rdf32(kr);
+            s[(int64_t)h * P + p] = (dd * (float)isum) * scale;
+        }
+    }
+}
+
+void orc_kv_wsum(const float* w, const uint8_t* vc, double* out, int Hq, int Hkv, int64_t P, int hd) {
+    const int G = Hq / Hkv, rb = 4 + hd;
+    for (int h = 0; h < Hq; h++) {
+        const int kvh = h / G;
+        for (int i = 0; i < hd; i++) {
+            double acc = 0.0;
+            for (int64_t p = 0; p < P; p++) {
+                const uint8_t* vr = vc + (p * Hkv + kvh) * rb;
+                acc += (double)w[(int64_t)h * P + p] * (double)rdf32(vr) * (double)(int8_t)vr[4 + i];
+            }
+            out[(int64_t)h * hd + i] = acc;
+        }
+    }
+}

@@ -41,6 +41,11 @@ MUTANTS = [
      "nibble_code(blk + 8, i) | (fifth_bit(blk + 2, i) << 4)"),
     ("q5_0 rounding offset", "float t = xb[i] * id + 16.5f;", "float t = xb[i] * id + 16.0f;"),
     ("q5_K quantizer 15 levels", "scl[s] = (hi + mns[s]) / 31.0f;", "scl[s] = (hi + mns[s]) / 15.0f;"),
+    ("kv heads interleaved", "const int kvh = h / G;\n        for (int64_t p = 0; p < P; p++) {\n            const uint8_t* kr",
+     "const int kvh = h % Hkv;\n        for (int64_t p = 0; p < P; p++) {\n            const uint8_t* kr"),
+    ("kv cache head-major", "const uint8_t* vr = vc + (p * Hkv + kvh) * rb;", "const uint8_t* vr = vc + (kvh * P + p) * rb;"),
+    ("kv scale 128/amax", "float id = (amax != 0.0f) ? 127.0f / amax : 0.0f;\n        for (int i = 0; i < hd; i++)",
+     "float id = (amax != 0.0f) ? 128.0f / amax : 0.0f;\n        for (int i = 0; i < hd; i++)"),
 ]
 
 PINS = [name for name in dir(pins) if name.startswith("test_")]

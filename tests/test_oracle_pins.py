@@ -517,3 +517,74 @@ def test_get_rows_returns_the_rows_asked_for(orc):
     assert np.array_equal(orc.get_rows("q8_0", W, ids, K), w[ids].astype(np.float64))
     with pytest.raises(IndexError):
         orc.get_rows("q8_0", W, [N], K)
+
+
+# --------------------------------------------------------------------------- Q8 KV cache
+def test_kv_row_size(orc):
+    """[krafla] "Architecture", Attention: 68 bytes per head at head_dim 64 against 256 in f32,
+    about 3.8x smaller."""
+    for _, hd, b8, b32, shrink in read_golden("kv_cache.txt"):
+        assert orc.kv_row_bytes(int(hd)) == int(b8)
+        assert 4 * int(hd) == int(b32) and round(int(b32) / int(b8), 1) == float(shrink)
+
+
+def test_kv_quantize_is_the_activation_rule(orc):
+    """[krafla] "Architecture", Attention: K, V and the query heads use the activations'
+    quantization rule.  Over 256 values that rule, with its f32 scale, is Q8_K's: codes and d
+    equal Q8_K's bytes; over 32 values the codes equal Q8_0's and Q8_0's f16 scale is the
+    f16 rounding of the f32 d."""
+    x = workloads.activations_f32(6, 256, seed=41)
+    x[0] = 0.0
+    kv = orc.kv_quantize(x, 256)
+    q8k = orc.quantize("q8_K", x).reshape(6, 292)
+    assert np.array_equal(kv[:, 0:4], q8k[:, 0:4]) and np.array_equal(kv[:, 4:], q8k[:, 4:260])
+    x32 = x[:, :32]
+    kv32 = orc.kv_quantize(x32, 32)
+    q80 = orc.quantize("q8_0", x32).reshape(6, 34)
+    assert np.array_equal(kv32[:, 4:], q80[:, 2:])
+    d = kv32[:, 0:4].copy().view(np.float32)[:, 0]
+    assert np.array_equal(d.astype(np.float16).view(np.uint16), q80[:, 0:2].copy().view(np.uint16)[:, 0])
+
+
+def _kv_integer_case(g, rows, hd):
+    """Integer head vectors with |max| = 127 in each: scale exactly 1, codes = the integers."""
+    v = g.integers(-127, 128, size=(rows, hd)).astype(np.float32)
+    v[:, 0] = 127.0
+    return v
+
+
+def test_kv_scores_integer_case_and_head_mapping(orc):
+    """Integer head vectors with scale 1: each score is the exact integer dot (numpy int64) times
+    the power-of-two factor.  Heads sharing a KV head are consecutive (a reading): with KV head
+    1's codes zeroed except the forced 127, query heads 2 and 3 score only that element."""
+    g = np.random.default_rng(42)
+    Hq, Hkv, P, hd = 4, 2, 5, 64
+    q = _kv_integer_case(g, Hq, hd)
+    k = _kv_integer_case(g, P * Hkv, hd)
+    k.reshape(P, Hkv, hd)[:, 1, 1:] = 0.0
+    q8, k8 = orc.kv_quantize(q, hd), orc.kv_quantize(k, hd)
+    s = orc.kv_scores(q8, k8, Hq, Hkv, P, hd, scale=0.125)
+    kk = k.reshape(P, Hkv, hd).astype(np.int64)
+    for h in range(Hq):
+        want = kk[:, h // 2, :] @ q[h].astype(np.int64)
+        assert np.array_equal(s[h].astype(np.float64), want * 0.125), h
+    assert np.array_equal(s[2:].astype(np.float64), 127.0 * 127.0 * 0.125 * np.ones((2, P)))
+
+
+def test_kv_wsum_matches_dequantized_einsum(orc):
+    """The V sum equals a float64 einsum of the softmax-like weights and the dequantized V rows
+    (a library product), with heads mapped as for the scores."""
+    g = np.random.default_rng(43)
+    Hq, Hkv, P, hd = 8, 2, 37, 32
+    v = g.standard_normal((P * Hkv, hd)).astype(np.float32)
+    v8 = orc.kv_quantize(v, hd)
+    w = g.random((Hq, P)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    got = orc.kv_wsum(w, v8, Hq, Hkv, P, hd)
+    dv = v8[:, 0:4].copy().view(np.float32)[:, 0].astype(np.float64)
+    vq = v8[:, 4:].view(np.int8).astype(np.float64) * dv[:, None]
+    vq = vq.reshape(P, Hkv, hd)
+    want = np.stack([w[h].astype(np.float64) @ vq[:, h // (Hq // Hkv), :] for h in range(Hq)])
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-15)
+    # the dequantized rows are within half a step of the f32 inputs
+    assert np.all(np.abs(vq.reshape(-1, hd) - v) <= dv[:, None] / 2 * (1 + 1e-6) + 1e-12)
