@@ -59,6 +59,11 @@ SIGNATURES = {
     "qmm_linear_q5_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
     "qmm_get_rows": ("tpppiiiq", ctypes.c_int),
+    "qmm_kv_row_bytes": ("i", ctypes.c_size_t),
+    "qmm_kv_quantize": ("ppiiq", ctypes.c_int),
+    "qmm_kv_scores": ("pppiiiifq", ctypes.c_int),
+    "qmm_kv_wsum_scratch_bytes": ("iii", ctypes.c_size_t),
+    "qmm_kv_wsum": ("pppps" + "iiiiq", ctypes.c_int),
     "qmm_matmul_q4_K": ("pppiiiq", ctypes.c_int),
     "qmm_matmul_q6_K": ("pppiiiq", ctypes.c_int),
     "qmm_matmul_q2_K": ("pppiiiq", ctypes.c_int),
@@ -68,7 +73,7 @@ SIGNATURES = {
     "qmm_device_status": ("c", ctypes.c_int),
 }
 _CT = {"p": ctypes.c_void_p, "i": ctypes.c_int64, "s": ctypes.c_size_t, "t": ctypes.c_int, "c": ctypes.c_int,
-       "q": ctypes.c_void_p}
+       "q": ctypes.c_void_p, "f": ctypes.c_float}
 
 _lib = None
 
@@ -255,6 +260,32 @@ def matmul(wtype, W, xq, Y, M, N, K, stream=None):
 def qmm_get_rows(wtype, W, ids, out, R, N, K, stream=None):
     """out[r] = dequantized row ids[r] of W (ids: int32 device tensor)."""
     _call("qmm_get_rows", _type(wtype), ptr(W), ptr(ids), ptr(out), int(R), int(N), int(K), stream_handle(stream))
+
+
+# ---- the Q8 KV cache
+def qmm_kv_row_bytes(hd):
+    return int(load().qmm_kv_row_bytes(int(hd)))
+
+
+def qmm_kv_quantize(x, out, rows, hd, stream=None):
+    """rows head vectors (f32 [rows][hd]) into quantized rows (f32 d + int8 codes) at out."""
+    _call("qmm_kv_quantize", ptr(x), ptr(out), int(rows), int(hd), stream_handle(stream))
+
+
+def qmm_kv_scores(q, kc, scores, Hq, Hkv, P, hd, scale, stream=None):
+    """scores[h][p] for the quantized query rows q against positions 0..P-1 of the K cache kc."""
+    _call("qmm_kv_scores", ptr(q), ptr(kc), ptr(scores), int(Hq), int(Hkv), int(P), int(hd), float(scale),
+          stream_handle(stream))
+
+
+def qmm_kv_wsum_scratch_bytes(Hq, P, hd):
+    return int(load().qmm_kv_wsum_scratch_bytes(int(Hq), int(P), int(hd)))
+
+
+def qmm_kv_wsum(w, vc, out, scratch, scratch_bytes, Hq, Hkv, P, hd, stream=None):
+    """out[h] = sum_p w[h][p] * (dequantized V row of position p, KV head h / (Hq/Hkv))."""
+    _call("qmm_kv_wsum", ptr(w), ptr(vc), ptr(out), ptr(scratch), int(scratch_bytes), int(Hq), int(Hkv), int(P),
+          int(hd), stream_handle(stream))
 
 
 def qmm_blocksums(wtype, W, xq, s, M, N, K, stream=None):

@@ -297,6 +297,46 @@ QMM_API qmm_status qmm_matmul_q2_K(const void* W, const void* xq, float* Y, int6
 QMM_API qmm_status qmm_get_rows(int wtype, const void* W, const int32_t* ids, float* out, int64_t R, int64_t N,
                                 int64_t K, qmm_stream_t stream);
 
+/* ---- the Q8 KV cache of decode attention --------------------------------- */
+/* [krafla] "Architecture", Attention ("Q8 cache"): each position's K and V are
+ * kept per KV head as int8 codes with one float scale, quantized by the
+ * activations' rule, and each query head is quantized the same way; a score is
+ * an integer dot product, and the V sum widens the int8 values to float as it
+ * goes.  Readings where the page is silent:
+ *   row     one head vector of hd values: f32 d @0, int8 codes @4 (4 + hd bytes,
+ *           68 at hd = 64); d = amax/127, codes rne(x * 127/amax) saturated to
+ *           int8 (0 for an all-zero vector) -- over 256 values exactly a Q8_K
+ *           block's d and codes
+ *   cache   row (p, kvh) at byte (p*Hkv + kvh) * (4 + hd): appending position p
+ *           writes Hkv consecutive rows
+ *   heads   query head h reads KV head h / (Hq/Hkv)
+ * hd: a multiple of 16 in 16..256; Hq a multiple of Hkv with Hq/Hkv <= 8; P >= 1.
+ * Pointers: 4-byte aligned (the V-sum scratch 16-byte aligned).  Errors:
+ * QMM_E_NULL, QMM_E_SHAPE, QMM_E_ALIGN, QMM_E_SCRATCH, QMM_E_CUDA, as above. */
+QMM_API size_t qmm_kv_row_bytes(int64_t hd);  /* 4 + hd; 0 for an unsupported hd */
+
+/* rows head vectors x (f32 [rows][hd]) into rows quantized rows at out; the
+ * codes and d are bit-identical to a scalar implementation of the rule. */
+QMM_API qmm_status qmm_kv_quantize(const float* x, void* out, int64_t rows, int64_t hd, qmm_stream_t stream);
+
+/* scores[h][p] = ((dq_h * dk_p) * isum) * scale for the Hq quantized query rows q
+ * against positions 0..P-1 of the K cache kc, with isum the exact int32 dot of
+ * the codes and every float step rounded once (so the result is bit-identical
+ * to a scalar implementation); scale is the caller's factor (1/sqrt(hd) for
+ * attention).  scores: f32 [Hq][P]. */
+QMM_API qmm_status qmm_kv_scores(const void* q, const void* kc, float* scores, int64_t Hq, int64_t Hkv, int64_t P,
+                                 int64_t hd, float scale, qmm_stream_t stream);
+
+/* out[h][i] = sum_p w[h][p] * dv_p * v_p[i] over positions 0..P-1 of the V cache
+ * vc, w f32 [Hq][P] (the attention weights), out f32 [Hq][hd].  Summed in f32:
+ * each thread runs an FMA chain over a fixed chunk of 128 positions into the
+ * scratch, then the chunks are added in order, so the result is the same on
+ * every GPU and within (P + 2) * 2^-24 * sum_p |w dv v| of the exact sum.
+ * scratch: at least qmm_kv_wsum_scratch_bytes(Hq, P, hd) bytes. */
+QMM_API size_t qmm_kv_wsum_scratch_bytes(int64_t Hq, int64_t P, int64_t hd);
+QMM_API qmm_status qmm_kv_wsum(const float* w, const void* vc, float* out, void* scratch, size_t scratch_bytes,
+                               int64_t Hq, int64_t Hkv, int64_t P, int64_t hd, qmm_stream_t stream);
+
 /* ---- verification hooks (not on the hot path) --------------------------- */
 /* The exact int32 block sums the kernels fold, for bit-exact checking:
  * s[t][o][b] for every token t, row o and block b; Q4_0/Q8_0 give one int32 per

@@ -31,7 +31,9 @@ def test_header_declares_the_boundary():
     for want in ("qmm_quantize_q8_0", "qmm_quantize_q8_K", "qmm_matvec_q4_0", "qmm_matvec_q8_0",
                  "qmm_matvec_q4_K", "qmm_matvec_q6_K", "qmm_matvec_q2_K", "qmm_matmul_q4_0", "qmm_matmul_q4_K",
                  "qmm_matmul_q6_K", "qmm_matmul_q2_K",
-                 "qmm_linear_q4_0", "qmm_blocksums", "qmm_status_str", "qmm_row_bytes"):
+                 "qmm_linear_q4_0", "qmm_blocksums", "qmm_status_str", "qmm_row_bytes", "qmm_matvec_q4_1",
+                 "qmm_matvec_q5_0", "qmm_matvec_q5_1", "qmm_matvec_q5_K", "qmm_get_rows", "qmm_kv_quantize",
+                 "qmm_kv_scores", "qmm_kv_wsum"):
         assert want in names
     assert set(names) == set(qmm.SIGNATURES), set(names) ^ set(qmm.SIGNATURES)
 
@@ -148,6 +150,31 @@ def test_get_rows_rejects_bad_arguments(lib):
     assert f(qmm.QMM_Q4_K, A, A, A, 1, 4, 128, None) == 2
     assert f(qmm.QMM_Q4_0, A, A + 2, A, 1, 4, 256, None) == 4  # ids not 4-byte aligned
     assert f(qmm.QMM_Q4_0, A, A, U, 1, 4, 256, None) == 4
+
+
+def test_kv_cache_calls_reject_bad_arguments(lib):
+    assert qmm.qmm_kv_row_bytes(64) == 68 and qmm.qmm_kv_row_bytes(128) == 132
+    assert qmm.qmm_kv_row_bytes(72) == 0 and qmm.qmm_kv_row_bytes(512) == 0 and qmm.qmm_kv_row_bytes(0) == 0
+    q = lib.qmm_kv_quantize
+    assert q(None, A, 4, 64, None) == 1
+    assert q(A, A, 0, 64, None) == 2
+    assert q(A, A, 4, 60, None) == 2
+    assert q(A + 2, A, 4, 64, None) == 4
+    s = lib.qmm_kv_scores
+    f = ctypes.c_float(0.125)
+    assert s(A, A, None, 32, 8, 100, 128, f, None) == 1
+    assert s(A, A, A, 32, 6, 100, 128, f, None) == 2    # Hq not a multiple of Hkv
+    assert s(A, A, A, 32, 2, 100, 128, f, None) == 2    # 16 query heads per KV head
+    assert s(A, A, A, 32, 8, 0, 128, f, None) == 2
+    assert s(A, A, A, 32, 8, 100, 120, f, None) == 2
+    assert s(A, A + 1, A, 32, 8, 100, 128, f, None) == 4
+    need = qmm.qmm_kv_wsum_scratch_bytes(32, 300, 128)
+    assert need == 32 * 3 * 128 * 4
+    w = lib.qmm_kv_wsum
+    assert w(A, A, A, None, need, 32, 8, 300, 128, None) == 1
+    assert w(A, A, A, A, need - 4, 32, 8, 300, 128, None) == 5
+    assert w(A, A, A, A + 4, need, 32, 8, 300, 128, None) == 4  # scratch must be 16-byte aligned
+    assert w(A, A, A, A, need, 32, 8, 300, 100, None) == 2
 
 
 def test_matmul_and_blocksums_reject_bad_arguments(lib):

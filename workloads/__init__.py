@@ -19,6 +19,10 @@ Shapes (N rows x K input dim, M tokens):
   q4_0 prefill      M in {128, 512, 2048} x 12288 x 4096
   q4_1 / q5_0 / q5_1 / q5_K matvecs   12288 x 4096, M=1 (the other formats the
                     pages list, on the FFN shape)
+  Q8 KV cache       32 query heads, 8 KV heads, head_dim 128, 4096 cached
+                    positions (an 8B-class layer at the page's 4096-position
+                    context): q, K, V ~ the activation recipe; the attention
+                    weights a softmax of N(0, 2^2) logits per query head
 """
 from __future__ import annotations
 
@@ -50,6 +54,7 @@ WORKLOADS = {
     "q5_0_matvec_12288x4096": dict(kind="matvec", wtype="q5_0", M=1, N=12288, K=4096, seed=0xC0FFEE + 6),
     "q5_1_matvec_12288x4096": dict(kind="matvec", wtype="q5_1", M=1, N=12288, K=4096, seed=0xC0FFEE + 7),
     "q5_K_matvec_12288x4096": dict(kind="matvec", wtype="q5_K", M=1, N=12288, K=4096, seed=0xC0FFEE + 8),
+    "q8_kv_cache_32x8x4096x128": dict(kind="kv", Hq=32, Hkv=8, P=4096, hd=128, seed=0xC0FFEE + 9),
 }
 
 
@@ -79,3 +84,15 @@ def activations_f32(M: int, K: int, seed: int, stream: int = 0) -> np.ndarray:
 
 def uniform_f32(shape, lo: float, hi: float, seed: int) -> np.ndarray:
     return rng(seed, 99).uniform(lo, hi, size=shape).astype(np.float32)
+
+
+def kv_inputs(Hq: int, Hkv: int, P: int, hd: int, seed: int):
+    """Decode-attention inputs: q f32 [Hq, hd], K and V f32 [P * Hkv, hd] (row p * Hkv + kvh),
+    attention weights f32 [Hq, P] (each row a softmax of N(0, 4) logits, summing to 1)."""
+    q = activations_f32(Hq, hd, seed, stream=0)
+    k = activations_f32(P * Hkv, hd, seed, stream=1)
+    v = activations_f32(P * Hkv, hd, seed, stream=2)
+    z = rng(seed, 6).standard_normal((Hq, P)) * 2.0
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    w = (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+    return q, k, v, w
