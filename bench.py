@@ -482,6 +482,48 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
                                 "group_equiv_tok_s_36_layers_matmuls_only": round(1.0 / (36 * t_grp), 1)}
     del sets, mats
 
+    # the Q8 KV cache of one decode-attention layer: quantize the query heads, score every cached
+    # position against them, and sum the V rows under the attention weights (the softmax between the
+    # two is not part of the library: its output is an input here).  Enough copies of the caches
+    # that a replay cycle streams more than L2 holds.
+    cfg = workloads.WORKLOADS["q8_kv_cache_32x8x4096x128"]
+    Hq, Hkv, P, hd = cfg["Hq"], cfg["Hkv"], cfg["P"], cfg["hd"]
+    q, k, v, w = workloads.kv_inputs(Hq, Hkv, P, hd, cfg["seed"])
+    rb = qmm.qmm_kv_row_bytes(hd)
+    kc = torch.empty(P * Hkv * rb, dtype=torch.uint8, device=dev)
+    vc = torch.empty_like(kc)
+    with torch.cuda.stream(stream):
+        qmm.qmm_kv_quantize(to_dev(k), kc, P * Hkv, hd, stream=sh)
+        qmm.qmm_kv_quantize(to_dev(v), vc, P * Hkv, hd, stream=sh)
+    stream.synchronize()
+    cache_bytes = 2 * kc.numel()
+    C = max(2, int(np.ceil(2.5 * 129e6 / cache_bytes)))
+    kcs = [kc] + [kc.clone() for _ in range(C - 1)]
+    vcs = [vc] + [vc.clone() for _ in range(C - 1)]
+    qx, wd = to_dev(q), to_dev(w)
+    q8 = torch.empty(Hq * rb, dtype=torch.uint8, device=dev)
+    scores = torch.empty(Hq, P, dtype=torch.float32, device=dev)
+    out = torch.empty(Hq, hd, dtype=torch.float32, device=dev)
+    sbk = qmm.qmm_kv_wsum_scratch_bytes(Hq, P, hd)
+    kscratch = torch.empty(sbk, dtype=torch.uint8, device=dev)
+    scale = float(1.0 / np.sqrt(hd))
+
+    def attn(i):
+        qmm.qmm_kv_quantize(qx, q8, Hq, hd, stream=sh)
+        qmm.qmm_kv_scores(q8, kcs[i % C], scores, Hq, Hkv, P, hd, scale, stream=sh)
+        qmm.qmm_kv_wsum(wd, vcs[i % C], out, kscratch, sbk, Hq, Hkv, P, hd, stream=sh)
+
+    t_attn = timed_graph(attn, 8)
+    t_sc = timed_graph(lambda i: qmm.qmm_kv_scores(q8, kcs[i % C], scores, Hq, Hkv, P, hd, scale, stream=sh), 8)
+    t_ws = timed_graph(lambda i: qmm.qmm_kv_wsum(wd, vcs[i % C], out, kscratch, sbk, Hq, Hkv, P, hd, stream=sh), 8)
+    res["q8_kv_cache_32x8x4096x128"] = {
+        "us": round(t_attn * 1e6, 3), "cache_bytes": cache_bytes, "cache_GB/s": round(cache_bytes / t_attn / 1e9, 1),
+        "frac_hbm": round(cache_bytes / t_attn / 1e9 / hbm, 4), "launches": 4, "copies": C,
+        "scores_us": round(t_sc * 1e6, 3), "scores_K_GB/s": round(kc.numel() / t_sc / 1e9, 1),
+        "wsum_us": round(t_ws * 1e6, 3), "wsum_V_GB/s": round(vc.numel() / t_ws / 1e9, 1),
+        "how": "qmm_kv_quantize (32 query heads) + qmm_kv_scores + qmm_kv_wsum (2 launches)"}
+    del kcs, vcs
+
     # prefill
     cfg = workloads.WORKLOADS["q4_0_prefill_512x12288x4096"]
     N, K = cfg["N"], cfg["K"]
