@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
     uint8_t* aq = smem + align_up(8u * nw * depth, 128u);
     const int nd = F::ACT == QMM_Q8_0 ? K / 32 : K / 256;
     const int nsu = K / 256;
-    const int qbytes = SU ? (WT == QMM_Q4_0 ? 288 * nsu : 272 * nsu) : K;
+    const int qbytes = SU ? SuFmt<has_su<WT>() ? WT : QMM_Q8_0>::A * nsu : K;
     float* ad = reinterpret_cast<float*>(aq + qbytes);
     int* as = reinterpret_cast<int*>(ad + nd);
     uint8_t* xs = reinterpret_cast<uint8_t*>(as + (SU ? nd : (F::ACT == QMM_Q8_0 ? nd : K / 16)));
@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
     const int units = K / F::BV;
     const uint64_t rb = (uint64_t)units * F::BB;
     if constexpr (!SPLIT) pieces = 1;
-    const SegGeom<SPLIT> geo{rb, SU ? nsu : units, pieces, piece_units, SU ? (WT == QMM_Q4_0 ? 144 : 272) : F::BB};
+    const SegGeom<SPLIT> geo{rb, SU ? nsu : units, pieces, piece_units,
+                             SU ? SuFmt<has_su<WT>() ? WT : QMM_Q8_0>::W : F::BB};
     // an even split of the matrix's rows: its first N % ncta CTAs take one row more
     const int rq = N / ncta, rr = N - rq * ncta;
     const int r_begin = bl * rq + min(bl, rr);
@@ -248,8 +249,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
 #pragma unroll
                     for (int i = 0; i < 8; i++) w[i] = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
                 }
-                if constexpr (SU) su_put_block<WT == QMM_Q4_0>(w, dbits, b, nsu, aq, ad, as);
-                else act_put_q8_0_block(w, dbits, b, nb, aq, ad, as);
+                if constexpr (SU && (WT == QMM_Q8_0 || WT == QMM_Q4_0))
+                    su_put_block<WT == QMM_Q4_0>(w, dbits, b, nsu, aq, ad, as);
+                else if constexpr (SU)
+                    su_put_halves(w, dbits, b, nsu, aq, ad, as);
+                else
+                    act_put_q8_0_block(w, dbits, b, nb, aq, ad, as);
             }
         } else {
             if constexpr (FUSE) {
@@ -322,7 +327,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                     for (int u = li; u < un; u += lpr) {
                         const int ug = u0 + u;
                         if constexpr (WT == QMM_Q8_0) acc += su_q8_0(sbuf + so + 272u * u, aq, nsu, ug, ad + 8 * ug);
-                        else acc += su_q4_0(sbuf + so + 144u * u, aq, nsu, ug, ad + 8 * ug, as + 8 * ug);
+                        else if constexpr (WT == QMM_Q4_0)
+                            acc += su_q4_0(sbuf + so + 144u * u, aq, nsu, ug, ad + 8 * ug, as + 8 * ug);
+                        else if constexpr (has_su<WT>())
+                            acc += su_q45<WT>(sbuf + so + (uint32_t)SuFmt<WT>::W * u, aq, nsu, ug, ad + 8 * ug,
+                                              as + 8 * ug);
                     }
                 } else {
 #pragma unroll 4
@@ -437,7 +446,8 @@ qmm_status current_device(DeviceInfo* info) {
 __host__ inline uint32_t matvec_act_bytes(int wt, int act, int K, bool su) {
     if (!su) return act_region_bytes(act, K);
     const int nsu = K / 256, nd = K / 32;
-    return align_up((uint32_t)((wt == QMM_Q4_0 ? 288 : 272) * nsu + 8 * nd), 128u);
+    const int per = wt == QMM_Q4_0 ? 288 : (wt == QMM_Q8_0 ? 272 : 256);
+    return align_up((uint32_t)(per * nsu + 8 * nd), 128u);
 }
 
 // Picks the launch shape for G matrices of one format and K (G = 1: a plain
@@ -452,9 +462,9 @@ template <int WT>
 static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceInfo& dev, bool fuse, MatvecPlan* p,
                               int* cta_end) {
     using F = Fmt<WT>;
-    p->su = (WT == QMM_Q8_0 || WT == QMM_Q4_0) && K % 256 == 0;
+    p->su = has_su<WT>() && K % 256 == 0;
     const int nunit = p->su ? (int)(K / 256) : (int)(K / F::BV);
-    const int ubytes = p->su ? (WT == QMM_Q4_0 ? 144 : 272) : F::BB;
+    const int ubytes = p->su ? 8 * F::BB : F::BB;
     int best_p = 1, best_l = 32;
     double best_use = -1.0;
     for (int cap = 32; cap >= 8; cap >>= 1) {
@@ -611,12 +621,12 @@ static qmm_status launch_matvec(const void* const* W, const int64_t* N, float* c
         set.N[g] = (int)N[g];
     }
     if (fuse) {
-        if constexpr (WT == QMM_Q8_0 || WT == QMM_Q4_0) {
+        if constexpr (has_su<WT>()) {
             if (p.su) return launch_matvec_su<WT, true, true>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
         }
         return launch_matvec_su<WT, false, true>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
     }
-    if constexpr (WT == QMM_Q8_0 || WT == QMM_Q4_0) {
+    if constexpr (has_su<WT>()) {
         if (p.su) return launch_matvec_su<WT, true, false>(set, xq, nullptr, nullptr, K, p, dev, stream, pdl);
     }
     return launch_matvec_su<WT, false, false>(set, xq, nullptr, nullptr, K, p, dev, stream, pdl);

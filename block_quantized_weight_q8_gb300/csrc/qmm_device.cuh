@@ -647,6 +647,101 @@ __device__ __forceinline__ void su_put_block(const uint32_t w[8], uint32_t dbits
     }
 }
 
+// ---------------------------------------------------------------- super-units of Q4_1, Q5_0, Q5_1
+// Eight blocks (160, 176, 192 bytes) start on a 16-byte boundary when K % 256
+// == 0.  The activation for them: block bb of super-unit u keeps its codes
+// 0..15 in chunk 2bb and 16..31 in chunk 2bb+1, chunk c at (c*nsu + u)*16.
+template <int WT> struct SuFmt;
+template <> struct SuFmt<QMM_Q8_0> { static constexpr int W = 272, A = 272; };
+template <> struct SuFmt<QMM_Q4_0> { static constexpr int W = 144, A = 288; };
+template <> struct SuFmt<QMM_Q4_1> { static constexpr int W = 160, A = 256; };
+template <> struct SuFmt<QMM_Q5_0> { static constexpr int W = 176, A = 256; };
+template <> struct SuFmt<QMM_Q5_1> { static constexpr int W = 192, A = 256; };
+template <int WT>
+__host__ __device__ constexpr bool has_su() {
+    return WT == QMM_Q8_0 || WT == QMM_Q4_0 || WT == QMM_Q4_1 || WT == QMM_Q5_0 || WT == QMM_Q5_1;
+}
+
+__device__ __forceinline__ void su_put_halves(const uint32_t w[8], uint32_t dbits, int b, int nsu, uint8_t* q,
+                                              float* d, int* s) {
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) sum = dp4a(w[i], 0x01010101u, sum);
+    d[b] = h2f(dbits);
+    s[b] = sum;
+    const int u = b >> 3, bb = b & 7;
+    *reinterpret_cast<uint4*>(q + ((size_t)(2 * bb) * nsu + u) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(q + ((size_t)(2 * bb + 1) * nsu + u) * 16) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// the 4 bytes at even byte offset `off` of a super-unit held as words ww[]
+template <int OFF>
+__device__ __forceinline__ uint32_t su_word(const uint32_t* ww) {
+    if constexpr (OFF % 4 == 0) return ww[OFF / 4];
+    else return __funnelshift_r(ww[OFF / 4], ww[OFF / 4 + 1], 16);
+}
+
+// One block bb of a Q4_1 / Q5_0 / Q5_1 super-unit: its f32 contribution
+// (the per-block fold of the per-block decoders above).
+template <int WT, int BB>
+__device__ __forceinline__ float su_block5(const uint32_t* ww, const uint8_t* q, int nsu, int u, float dx, int asum) {
+    constexpr int O = Fmt<WT>::BB * BB;  // byte offset of the block
+    constexpr int QS = WT == QMM_Q4_1 ? 4 : (WT == QMM_Q5_0 ? 6 : 8);
+    uint32_t qs[4], qh = 0;
+    qs[0] = su_word<O + QS>(ww);
+    qs[1] = su_word<O + QS + 4>(ww);
+    qs[2] = su_word<O + QS + 8>(ww);
+    qs[3] = su_word<O + QS + 12>(ww);
+    if constexpr (WT == QMM_Q5_0) qh = su_word<O + 2>(ww);
+    if constexpr (WT == QMM_Q5_1) qh = su_word<O + 4>(ww);
+    const uint4 lo = *reinterpret_cast<const uint4*>(q + ((size_t)(2 * BB) * nsu + u) * 16);
+    const uint4 hi = *reinterpret_cast<const uint4*>(q + ((size_t)(2 * BB + 1) * nsu + u) * 16);
+    const uint32_t al[4] = {lo.x, lo.y, lo.z, lo.w}, ah[4] = {hi.x, hi.y, hi.z, hi.w};
+    int s0 = 0, s1 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        uint32_t ql = qs[i] & 0x0F0F0F0Fu, qu = (qs[i] >> 4) & 0x0F0F0F0Fu;
+        if constexpr (WT != QMM_Q4_1) {
+            ql |= spread4(qh >> (4 * i)) << 4;
+            qu |= spread4(qh >> (16 + 4 * i)) << 4;
+        }
+        s0 = dp4a(ql, al[i], s0);
+        s1 = dp4a(qu, ah[i], s1);
+    }
+    if constexpr (WT == QMM_Q5_0) {
+        const uint32_t db = (O % 4 == 0) ? (ww[O / 4] & 0xFFFFu) : (ww[O / 4] >> 16);
+        return (float)(s0 + s1 - 16 * asum) * h2f(db) * dx;
+    } else {
+        const uint32_t dm = ww[O / 4];  // O % 4 == 0 for the 20- and 24-byte blocks
+        return (float)(s0 + s1) * h2f(dm & 0xFFFFu) * dx + (float)asum * h2f(dm >> 16) * dx;
+    }
+}
+
+// The f32 fold of one Q4_1 / Q5_0 / Q5_1 super-unit: the 8 blocks' contributions
+// added in block order.  w: the super-unit in shared memory (16-byte aligned).
+template <int WT>
+__device__ __forceinline__ float su_q45(const uint8_t* w, const uint8_t* q, int nsu, int u, const float* d,
+                                        const int* asum) {
+    constexpr int NW = SuFmt<WT>::W / 4;
+    uint32_t ww[NW + 1];
+#pragma unroll
+    for (int c = 0; c < NW / 4; c++) {
+        const uint4 v = *reinterpret_cast<const uint4*>(w + 16 * c);
+        ww[4 * c] = v.x, ww[4 * c + 1] = v.y, ww[4 * c + 2] = v.z, ww[4 * c + 3] = v.w;
+    }
+    ww[NW] = 0u;  // never selected: a funnel shift past the last block reads no real byte
+    float acc = 0.0f;
+    acc += su_block5<WT, 0>(ww, q, nsu, u, d[0], asum[0]);
+    acc += su_block5<WT, 1>(ww, q, nsu, u, d[1], asum[1]);
+    acc += su_block5<WT, 2>(ww, q, nsu, u, d[2], asum[2]);
+    acc += su_block5<WT, 3>(ww, q, nsu, u, d[3], asum[3]);
+    acc += su_block5<WT, 4>(ww, q, nsu, u, d[4], asum[4]);
+    acc += su_block5<WT, 5>(ww, q, nsu, u, d[5], asum[5]);
+    acc += su_block5<WT, 6>(ww, q, nsu, u, d[6], asum[6]);
+    acc += su_block5<WT, 7>(ww, q, nsu, u, d[7], asum[7]);
+    return acc;
+}
+
 // One thread quantizes one Q8_0 block of 32 values v (the same IEEE-rounded
 // steps as quant_q8_0_part, so the same bytes): f16 scale bits and the codes as
 // 8 little-endian words.
