@@ -32,6 +32,7 @@ constexpr int kThreads = 256;  // blocksums kernel
 
 constexpr int kMaxWarps = 16;  // matvec CTA: up to 16 warps, each with its own ring
 constexpr int kMaxGroup = 8;   // weight matrices sharing one activation row in one launch
+constexpr int kMaxDepth = 8;   // bulk-copy slots per warp
 constexpr uint64_t kSmallCtaBytes = 24 * 1024;  // weight bytes per CTA under which two CTAs share an SM
 
 // The matrices of one launch (all of one format and K): CTAs
@@ -477,6 +478,10 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     p->pieces = best_p;
     p->piece_units = (nunit + best_p - 1) / best_p;
     p->lpr = best_l;
+    // Q4_0 super-units: two per lane (two independent chains per lane, and a
+    // warp's per-pass overhead over twice the bytes) measured 6% faster at
+    // 12288 x 4096; the other formats were slower that way
+    if (WT == QMM_Q4_0 && p->su && p->lpr >= 16 && p->piece_units >= p->lpr) p->lpr >>= 1;
     const uint64_t seg_bytes = (uint64_t)p->piece_units * ubytes;
     const int spp = 32 / p->lpr;
     const uint64_t pass_bytes = (uint64_t)spp * seg_bytes;
@@ -527,7 +532,7 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     // a fused Q8_K row is quantized into shared memory first (Q8_0 goes straight to its layout)
     if (fuse && F::ACT == QMM_Q8_K) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);
     const uint64_t part_bytes = p->pieces > 1 ? align_up((uint32_t)(rows_max * p->pieces * 4), 128u) : 0;
-    const uint32_t bar_max = align_up(8u * kMaxWarps * 2, 128u);
+    const uint32_t bar_max = align_up(8u * kMaxWarps * kMaxDepth, 128u);
     if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + part_bytes + sb) return QMM_E_SHAPE;
     // A CTA with little to stream (a small matrix) gets at most 8 warps and half
     // an SM's shared memory: two CTAs then fit on an SM, so the CTAs of the next
@@ -555,6 +560,16 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     }
     if (nw > nw_cap) nw = nw_cap;
     if (nw < 1) return QMM_E_SHAPE;
+    // a deeper ring when the shared memory holds more of a warp's items: with
+    // only a few items per warp, a ring of two makes each warp wait for several
+    // full memory round trips, where all of its items could be in flight at once
+    {
+        const uint64_t items_cta = (rows_max * (uint64_t)p->pieces + p->item_segs - 1) / p->item_segs;
+        const int ipw = (int)((items_cta + nw - 1) / nw);
+        uint64_t dmax = budget / ((uint64_t)nw * sb);
+        if (dmax > (uint64_t)kMaxDepth) dmax = kMaxDepth;
+        if (ipw > p->depth && (int)dmax > p->depth) p->depth = ipw < (int)dmax ? ipw : (int)dmax;
+    }
     p->nw = nw;
     p->part_off = align_up(8u * nw * p->depth, 128u) + act;
     p->act_bytes = p->part_off + (uint32_t)part_bytes;

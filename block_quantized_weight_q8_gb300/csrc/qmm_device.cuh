@@ -64,6 +64,18 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return (w >> (8 * k)) & 0xFFu; }
+// two-way dot products: a holds two signed 16-bit values, b four signed bytes;
+// lo pairs a with bytes 0, 1 of b, hi with bytes 2, 3
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 // ---------------------------------------------------------------- mbarrier + bulk copy
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -171,16 +183,19 @@ struct SmemBytes {
 //             consecutive 16-byte words -- no bank conflicts
 //   d[n]      f32 block scales (Q8_0: from f16; Q8_K: as stored)
 //   s         Q8_0: int32 sum of each block's 32 codes, s[u] (for the Q4_0 -8);
-//             Q8_K: int32 bsums, group g of block u at s[g*n + u].
+//             Q8_K: the bsums as packed int16 pairs (groups 2k, 2k+1 in one
+//             word, as the block stores them), pair k of block u at s[k*n + u].
 struct ActView {
     const uint8_t* q;
     const float* d;
     const int* s;
     int n;
     __device__ __forceinline__ uint4 chunk(int u, int c) const {
-        return *reinterpret_cast<const uint4*>(q + ((size_t)c * n + u) * 16);
+        return *reinterpret_cast<const uint4*>(q + ((uint32_t)c * n + u) * 16);
     }
-    __device__ __forceinline__ int bsum(int u, int g) const { return s[g * n + u]; }
+    __device__ __forceinline__ uint32_t bpair(int u, int k) const {
+        return reinterpret_cast<const uint32_t*>(s)[k * n + u];
+    }
 };
 
 // ---------------------------------------------------------------- block decoders
@@ -236,11 +251,16 @@ __device__ __forceinline__ void q4_K_isums(const SmemBytes& w, uint32_t o, const
     const uint32_t mn_lo = h.z & 0x3F3F3F3Fu;                                   // m 0..3
     const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);   // sc 4..7
     const uint32_t mn_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);  // m 4..7
+    // m_s * (bsum_2s + bsum_2s+1): pair s against the bytes (m_s, m_s)
     int m = 0;
-#pragma unroll
-    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_lo, s) * (a.bsum(u, 2 * s) + a.bsum(u, 2 * s + 1));
-#pragma unroll
-    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_hi, s) * (a.bsum(u, 8 + 2 * s) + a.bsum(u, 9 + 2 * s));
+    m = dp2a_lo(a.bpair(u, 0), __byte_perm(mn_lo, 0, 0x1100), m);
+    m = dp2a_hi(a.bpair(u, 1), __byte_perm(mn_lo, 0, 0x1100), m);
+    m = dp2a_lo(a.bpair(u, 2), __byte_perm(mn_lo, 0, 0x3322), m);
+    m = dp2a_hi(a.bpair(u, 3), __byte_perm(mn_lo, 0, 0x3322), m);
+    m = dp2a_lo(a.bpair(u, 4), __byte_perm(mn_hi, 0, 0x1100), m);
+    m = dp2a_hi(a.bpair(u, 5), __byte_perm(mn_hi, 0, 0x1100), m);
+    m = dp2a_lo(a.bpair(u, 6), __byte_perm(mn_hi, 0, 0x3322), m);
+    m = dp2a_hi(a.bpair(u, 7), __byte_perm(mn_hi, 0, 0x3322), m);
     int v = 0;
 #pragma unroll
     for (int j = 0; j < 4; j++) {
@@ -266,7 +286,11 @@ __device__ __forceinline__ void q4_K_isums(const SmemBytes& w, uint32_t o, const
 
 // Q2_K x Q8_K ([ggml] s1.2): value = sum_g sc_g * sum_{i in g} q_i a_i,
 // min = sum_g m_g * bsum_g; element 128h + 32s + l is (qs[32h + l] >> 2s) & 3
-// (GGUF order, a reading).  84-byte blocks in 4-byte aligned rows: aligned.
+// (GGUF order, a reading).  The codes of shift s are taken in place, masked to
+// 4^s * q (bytes up to 192: an unsigned x signed dp4a), and the power of four is
+// divided out once per shift: every such sum is an exact multiple of it.  The
+// min term is four pairs of two-way dots of the bsum pairs against the m
+// nibbles.  84-byte blocks in 4-byte aligned rows: aligned words.
 __device__ __forceinline__ void q2_K_isums(const SmemBytes& w, uint32_t o, const ActView& a, int u, int* value,
                                            int* minterm, uint32_t* d_bits, uint32_t* dmin_bits) {
     uint32_t scw[4];
@@ -274,9 +298,16 @@ __device__ __forceinline__ void q2_K_isums(const SmemBytes& w, uint32_t o, const
     const uint32_t dd = w.w32(o + 80);
     *d_bits = dd & 0xFFFFu;
     *dmin_bits = dd >> 16;
-    int m = 0, v = 0;
+    int m = 0;
+    uint32_t scl[4];
 #pragma unroll
-    for (int g = 0; g < 16; g++) m += (int)(byte_of(scw[g >> 2], g & 3) >> 4) * a.bsum(u, g);
+    for (int k = 0; k < 4; k++) {
+        const uint32_t mw = (scw[k] >> 4) & 0x0F0F0F0Fu;
+        m = dp2a_lo(a.bpair(u, 2 * k), mw, m);
+        m = dp2a_hi(a.bpair(u, 2 * k + 1), mw, m);
+        scl[k] = scw[k] & 0x0F0F0F0Fu;
+    }
+    int vs[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int h = 0; h < 2; h++) {
         uint32_t q[8];
@@ -284,22 +315,23 @@ __device__ __forceinline__ void q2_K_isums(const SmemBytes& w, uint32_t o, const
 #pragma unroll
         for (int s = 0; s < 4; s++) {
             const uint4 a0 = a.chunk(u, 8 * h + 2 * s), a1 = a.chunk(u, 8 * h + 2 * s + 1);
-            const uint32_t sh = 2u * s;
+            const uint32_t mask = 0x03030303u << (2 * s);
             int g0 = 0, g1 = 0;
-            g0 = dp4a((q[0] >> sh) & 0x03030303u, a0.x, g0);
-            g0 = dp4a((q[1] >> sh) & 0x03030303u, a0.y, g0);
-            g0 = dp4a((q[2] >> sh) & 0x03030303u, a0.z, g0);
-            g0 = dp4a((q[3] >> sh) & 0x03030303u, a0.w, g0);
-            g1 = dp4a((q[4] >> sh) & 0x03030303u, a1.x, g1);
-            g1 = dp4a((q[5] >> sh) & 0x03030303u, a1.y, g1);
-            g1 = dp4a((q[6] >> sh) & 0x03030303u, a1.z, g1);
-            g1 = dp4a((q[7] >> sh) & 0x03030303u, a1.w, g1);
+            g0 = dp4a_us(q[0] & mask, a0.x, g0);
+            g0 = dp4a_us(q[1] & mask, a0.y, g0);
+            g0 = dp4a_us(q[2] & mask, a0.z, g0);
+            g0 = dp4a_us(q[3] & mask, a0.w, g0);
+            g1 = dp4a_us(q[4] & mask, a1.x, g1);
+            g1 = dp4a_us(q[5] & mask, a1.y, g1);
+            g1 = dp4a_us(q[6] & mask, a1.z, g1);
+            g1 = dp4a_us(q[7] & mask, a1.w, g1);
             const int g = 8 * h + 2 * s;
-            v += (int)(byte_of(scw[g >> 2], g & 3) & 15u) * g0;
-            v += (int)(byte_of(scw[(g + 1) >> 2], (g + 1) & 3) & 15u) * g1;
+            // byte g & 3 of the scale word, zero-extended (selector 4 takes a zero byte)
+            vs[s] += (int)__byte_perm(scl[g >> 2], 0, 0x4440u | (g & 3)) * g0;
+            vs[s] += (int)__byte_perm(scl[(g + 1) >> 2], 0, 0x4440u | ((g + 1) & 3)) * g1;
         }
     }
-    *value = v;
+    *value = vs[0] + (vs[1] >> 2) + (vs[2] >> 4) + (vs[3] >> 6);
     *minterm = m;
 }
 
@@ -313,7 +345,10 @@ __device__ __forceinline__ void q6_K_isums(const SmemBytes& w, uint32_t o, const
     *d_bits = w.u16(o + 208);
     int m = 0, v = 0;
 #pragma unroll
-    for (int g = 0; g < 16; g++) m += (int)(int8_t)byte_of(scw[g >> 2], g & 3) * a.bsum(u, g);
+    for (int k = 0; k < 4; k++) {  // sum_g sc_g * bsum_g: signed scale bytes against the bsum pairs
+        m = dp2a_lo(a.bpair(u, 2 * k), scw[k], m);
+        m = dp2a_hi(a.bpair(u, 2 * k + 1), scw[k], m);
+    }
 #pragma unroll
     for (int n = 0; n < 2; n++) {
         uint32_t A[8], B[8], H[8];
@@ -419,11 +454,16 @@ __device__ __forceinline__ void q5_K_isums(const SmemBytes& w, uint32_t o, const
     const uint32_t mn_lo = h.z & 0x3F3F3F3Fu;
     const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
     const uint32_t mn_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+    // m_s * (bsum_2s + bsum_2s+1): pair s against the bytes (m_s, m_s)
     int m = 0;
-#pragma unroll
-    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_lo, s) * (a.bsum(u, 2 * s) + a.bsum(u, 2 * s + 1));
-#pragma unroll
-    for (int s = 0; s < 4; s++) m += (int)byte_of(mn_hi, s) * (a.bsum(u, 8 + 2 * s) + a.bsum(u, 9 + 2 * s));
+    m = dp2a_lo(a.bpair(u, 0), __byte_perm(mn_lo, 0, 0x1100), m);
+    m = dp2a_hi(a.bpair(u, 1), __byte_perm(mn_lo, 0, 0x1100), m);
+    m = dp2a_lo(a.bpair(u, 2), __byte_perm(mn_lo, 0, 0x3322), m);
+    m = dp2a_hi(a.bpair(u, 3), __byte_perm(mn_lo, 0, 0x3322), m);
+    m = dp2a_lo(a.bpair(u, 4), __byte_perm(mn_hi, 0, 0x1100), m);
+    m = dp2a_hi(a.bpair(u, 5), __byte_perm(mn_hi, 0, 0x1100), m);
+    m = dp2a_lo(a.bpair(u, 6), __byte_perm(mn_hi, 0, 0x3322), m);
+    m = dp2a_hi(a.bpair(u, 7), __byte_perm(mn_hi, 0, 0x3322), m);
     const uint4 h0 = *reinterpret_cast<const uint4*>(w.base + o + 16);
     const uint4 h1 = *reinterpret_cast<const uint4*>(w.base + o + 32);
     const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
@@ -465,8 +505,8 @@ __device__ __forceinline__ void act_put_q8_0_block(const uint32_t w[8], uint32_t
     for (int i = 0; i < 8; i++) sum = dp4a(w[i], 0x01010101u, sum);
     d[b] = h2f(dbits);
     s[b] = sum;
-    *reinterpret_cast<uint4*>(q + (size_t)b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(q + ((size_t)nb + b) * 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    *reinterpret_cast<uint4*>(q + (uint32_t)b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(q + ((uint32_t)nb + b) * 16) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 __device__ __forceinline__ void unpack_q8_0_block(const uint8_t* __restrict__ row, int K, int b, uint8_t* q, float* d,
@@ -481,8 +521,8 @@ __device__ __forceinline__ void unpack_q8_0_block(const uint8_t* __restrict__ ro
         wv[i] = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
         sum = dp4a(wv[i], 0x01010101u, sum);
     }
-    *reinterpret_cast<uint4*>(q + (size_t)b * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-    *reinterpret_cast<uint4*>(q + ((size_t)nb + b) * 16) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    *reinterpret_cast<uint4*>(q + (uint32_t)b * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    *reinterpret_cast<uint4*>(q + ((uint32_t)nb + b) * 16) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
     s[b] = sum;
 }
 
@@ -496,11 +536,9 @@ __device__ __forceinline__ void unpack_q8_K_word(const uint8_t* __restrict__ row
         d[u] = __uint_as_float(wv);
     } else if (k <= 64) {
         const int c = (k - 1) >> 2, wi = (k - 1) & 3;
-        *reinterpret_cast<uint32_t*>(q + ((size_t)c * ns + u) * 16 + 4 * wi) = wv;
+        *reinterpret_cast<uint32_t*>(q + ((uint32_t)c * ns + u) * 16 + 4 * wi) = wv;
     } else {
-        const int g = 2 * (k - 65);
-        s[g * ns + u] = (int)(int16_t)(wv & 0xFFFFu);
-        s[(g + 1) * ns + u] = (int)(int16_t)(wv >> 16);
+        reinterpret_cast<uint32_t*>(s)[(k - 65) * ns + u] = wv;  // the bsum pair of groups 2(k-65), +1
     }
 }
 
@@ -624,23 +662,23 @@ __device__ __forceinline__ void su_put_block(const uint32_t w[8], uint32_t dbits
     if constexpr (!PLANES) {
         // bytes 34bb, 34bb+1: the weight's d field (zero); 34bb + 2 + j: code j
         const int y0 = 34 * bb;
-        *reinterpret_cast<unsigned short*>(q + ((size_t)(y0 >> 4) * nsu + u) * 16 + (y0 & 15)) = 0;
+        *reinterpret_cast<unsigned short*>(q + ((uint32_t)(y0 >> 4) * nsu + u) * 16 + (y0 & 15)) = 0;
 #pragma unroll
         for (int h = 0; h < 16; h++) {
             const int y = y0 + 2 + 2 * h;
-            *reinterpret_cast<unsigned short*>(q + ((size_t)(y >> 4) * nsu + u) * 16 + (y & 15)) =
+            *reinterpret_cast<unsigned short*>(q + ((uint32_t)(y >> 4) * nsu + u) * 16 + (y & 15)) =
                 (unsigned short)((w[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
         }
     } else {
 #pragma unroll
         for (int pl = 0; pl < 2; pl++) {
             const int y0 = 18 * bb;  // the weight's d field: zero in both planes
-            *reinterpret_cast<unsigned short*>(q + ((size_t)(9 * pl + (y0 >> 4)) * nsu + u) * 16 + (y0 & 15)) = 0;
+            *reinterpret_cast<unsigned short*>(q + ((uint32_t)(9 * pl + (y0 >> 4)) * nsu + u) * 16 + (y0 & 15)) = 0;
 #pragma unroll
             for (int h = 0; h < 8; h++) {
                 const int y = y0 + 2 + 2 * h;
                 const int code = 16 * pl + 2 * h;
-                *reinterpret_cast<unsigned short*>(q + ((size_t)(9 * pl + (y >> 4)) * nsu + u) * 16 + (y & 15)) =
+                *reinterpret_cast<unsigned short*>(q + ((uint32_t)(9 * pl + (y >> 4)) * nsu + u) * 16 + (y & 15)) =
                     (unsigned short)((w[code >> 2] >> (16 * ((code >> 1) & 1))) & 0xFFFFu);
             }
         }
@@ -670,8 +708,8 @@ __device__ __forceinline__ void su_put_halves(const uint32_t w[8], uint32_t dbit
     d[b] = h2f(dbits);
     s[b] = sum;
     const int u = b >> 3, bb = b & 7;
-    *reinterpret_cast<uint4*>(q + ((size_t)(2 * bb) * nsu + u) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(q + ((size_t)(2 * bb + 1) * nsu + u) * 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    *reinterpret_cast<uint4*>(q + ((uint32_t)(2 * bb) * nsu + u) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(q + ((uint32_t)(2 * bb + 1) * nsu + u) * 16) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // the 4 bytes at even byte offset `off` of a super-unit held as words ww[]
@@ -694,8 +732,8 @@ __device__ __forceinline__ float su_block5(const uint32_t* ww, const uint8_t* q,
     qs[3] = su_word<O + QS + 12>(ww);
     if constexpr (WT == QMM_Q5_0) qh = su_word<O + 2>(ww);
     if constexpr (WT == QMM_Q5_1) qh = su_word<O + 4>(ww);
-    const uint4 lo = *reinterpret_cast<const uint4*>(q + ((size_t)(2 * BB) * nsu + u) * 16);
-    const uint4 hi = *reinterpret_cast<const uint4*>(q + ((size_t)(2 * BB + 1) * nsu + u) * 16);
+    const uint4 lo = *reinterpret_cast<const uint4*>(q + ((uint32_t)(2 * BB) * nsu + u) * 16);
+    const uint4 hi = *reinterpret_cast<const uint4*>(q + ((uint32_t)(2 * BB + 1) * nsu + u) * 16);
     const uint32_t al[4] = {lo.x, lo.y, lo.z, lo.w}, ah[4] = {hi.x, hi.y, hi.z, hi.w};
     int s0 = 0, s1 = 0;
 #pragma unroll
@@ -778,7 +816,7 @@ __device__ __forceinline__ float su_q8_0(const uint8_t* w, const uint8_t* q, int
 #pragma unroll
     for (int c = 0; c < 17; c++) {
         const uint4 wc = *reinterpret_cast<const uint4*>(w + 16 * c);
-        const uint4 ac = *reinterpret_cast<const uint4*>(q + ((size_t)c * nsu + u) * 16);
+        const uint4 ac = *reinterpret_cast<const uint4*>(q + ((uint32_t)c * nsu + u) * 16);
         const uint32_t ww[4] = {wc.x, wc.y, wc.z, wc.w}, aa[4] = {ac.x, ac.y, ac.z, ac.w};
 #pragma unroll
         for (int j = 0; j < 4; j++) {
@@ -807,8 +845,8 @@ __device__ __forceinline__ float su_q4_0(const uint8_t* w, const uint8_t* q, int
 #pragma unroll
     for (int c = 0; c < 9; c++) {
         const uint4 wc = *reinterpret_cast<const uint4*>(w + 16 * c);
-        const uint4 lo = *reinterpret_cast<const uint4*>(q + ((size_t)c * nsu + u) * 16);
-        const uint4 hi = *reinterpret_cast<const uint4*>(q + ((size_t)(9 + c) * nsu + u) * 16);
+        const uint4 lo = *reinterpret_cast<const uint4*>(q + ((uint32_t)c * nsu + u) * 16);
+        const uint4 hi = *reinterpret_cast<const uint4*>(q + ((uint32_t)(9 + c) * nsu + u) * 16);
         const uint32_t ww[4] = {wc.x, wc.y, wc.z, wc.w}, al[4] = {lo.x, lo.y, lo.z, lo.w},
                        ah[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
