@@ -7,7 +7,7 @@
 // A row is one head vector of hd values: f32 d @0, int8 codes @4 (4 + hd bytes;
 // 68 at hd = 64).  The cache holds row (p, kvh) at (p*Hkv + kvh) * (4 + hd), so
 // appending a position writes Hkv consecutive rows.  Query head h reads KV head
-// h / (Hq/Hkv).
+// h / (Hq/Hkv) ([krafla] "Architecture", "Data flow for one token").
 //
 //   kv_quantize   one warp per row: amax, d = amax/127, codes rne(x*127/amax)
 //   kv_scores     a CTA per (128 positions, KV head): the K rows of the tile and

@@ -309,7 +309,8 @@ QMM_API qmm_status qmm_get_rows(int wtype, const void* W, const int32_t* ids, fl
  *           block's d and codes
  *   cache   row (p, kvh) at byte (p*Hkv + kvh) * (4 + hd): appending position p
  *           writes Hkv consecutive rows
- *   heads   query head h reads KV head h / (Hq/Hkv)
+ *   heads   query head h reads KV head h / (Hq/Hkv) (the page's "Data flow for
+ *           one token": GQA head h -> kv head h / (n_heads / n_kv_heads))
  * hd: a multiple of 16 in 16..256; Hq a multiple of Hkv with Hq/Hkv <= 8; P >= 1.
  * Pointers: 4-byte aligned (the V-sum scratch 16-byte aligned).  Errors:
  * QMM_E_NULL, QMM_E_SHAPE, QMM_E_ALIGN, QMM_E_SCRATCH, QMM_E_CUDA, as above. */

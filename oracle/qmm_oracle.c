@@ -1014,8 +1014,9 @@ void orc_matmul_exact(int wtype, const uint8_t* W, const uint8_t* X, double* out
 /*     nearest-even of x*127/amax) over the whole head vector;               */
 /*   - the cache holds row (p, kvh) at (p*Hkv + kvh) * (4 + hd): a position's */
 /*     heads side by side, positions appended in order;                       */
-/*   - query head h reads KV head h / (Hq/Hkv) (heads that share a KV head    */
-/*     are consecutive);                                                      */
+/*   - query head h reads KV head h / (Hq/Hkv): [krafla] "Architecture",      */
+/*     "Data flow for one token" (GQA head h -> kv head h / (n_heads /        */
+/*     n_kv_heads)), not a reading;                                           */
 /*   - a score is ((dq * dk) * isum) * scale in f32 (isum exact: |isum| <=    */
 /*     hd * 128 * 128 < 2^24), scale the caller's factor (1/sqrt(hd) for      */
 /*     attention);                                                            */

@@ -555,8 +555,9 @@ def _kv_integer_case(g, rows, hd):
 
 def test_kv_scores_integer_case_and_head_mapping(orc):
     """Integer head vectors with scale 1: each score is the exact integer dot (numpy int64) times
-    the power-of-two factor.  Heads sharing a KV head are consecutive (a reading): with KV head
-    1's codes zeroed except the forced 127, query heads 2 and 3 score only that element."""
+    the power-of-two factor.  Query head h reads KV head h // (Hq // Hkv) ([krafla] "Architecture",
+    "Data flow for one token"): with KV head 1's codes zeroed except the forced 127, query heads 2
+    and 3 score only that element."""
     g = np.random.default_rng(42)
     Hq, Hkv, P, hd = 4, 2, 5, 64
     q = _kv_integer_case(g, Hq, hd)
