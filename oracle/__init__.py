@@ -78,6 +78,8 @@ def load(path: str):
     L.orc_blocksums.restype = None
     L.orc_matmul_exact.argtypes = [i32, p, p, p, i64, i64, i64, i32]
     L.orc_matmul_exact.restype = None
+    L.orc_rmsnorm.argtypes = [p, p, ctypes.c_float, p, i64, i64]
+    L.orc_rmsnorm.restype = None
     L.orc_kv_row_bytes.argtypes = [i32]
     L.orc_kv_quantize.argtypes = [p, p, i64, i32]
     L.orc_kv_quantize.restype = None
@@ -255,4 +257,18 @@ def kv_wsum(w: np.ndarray, v8: np.ndarray, Hq: int, Hkv: int, P: int, hd: int) -
     assert w.size == Hq * P and v8.size >= P * Hkv * kv_row_bytes(hd) and Hq % Hkv == 0
     out = np.zeros((Hq, hd), dtype=np.float64)
     lib().orc_kv_wsum(_ptr(w), _ptr(v8), _ptr(out), Hq, Hkv, P, hd)
+    return out
+
+
+# ---- RMSNorm ahead of the quantizer ([krafla] "Architecture", "Data flow for one token")
+def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """f32 [M, K]: (x * s) * w with s = 1/sqrt(ss/K + eps) in f32, ss in the fixed order of
+    qmm_oracle.c (8-value sequential partials, then a stride-doubling tree)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    M, K = x2.shape
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    assert w.size == K and K % 8 == 0
+    out = np.zeros((M, K), dtype=np.float32)
+    lib().orc_rmsnorm(_ptr(x2), _ptr(w), ctypes.c_float(eps), _ptr(out), M, K)
     return out

@@ -43,6 +43,9 @@ MUTANTS = [
     ("q5_K quantizer 15 levels", "scl[s] = (hi + mns[s]) / 31.0f;", "scl[s] = (hi + mns[s]) / 15.0f;"),
     ("kv heads interleaved", "const int kvh = h / G;\n        for (int64_t p = 0; p < P; p++) {\n            const uint8_t* kr",
      "const int kvh = h % Hkv;\n        for (int64_t p = 0; p < P; p++) {\n            const uint8_t* kr"),
+    ("rmsnorm drops eps", "const float sc = 1.0f / sqrtf(mean + eps);", "const float sc = 1.0f / sqrtf(mean);"),
+    ("rmsnorm ignores w", "h[t * K + i] = (xr[i] * sc) * w[i];", "h[t * K + i] = xr[i] * sc;"),
+    ("rmsnorm mean over K-1", "const float mean = p[0] / (float)K;", "const float mean = p[0] / (float)(K - 1);"),
     ("kv cache head-major", "const uint8_t* vr = vc + (p * Hkv + kvh) * rb;", "const uint8_t* vr = vc + (kvh * P + p) * rb;"),
     ("kv scale 128/amax", "float id = (amax != 0.0f) ? 127.0f / amax : 0.0f;\n        for (int i = 0; i < hd; i++)",
      "float id = (amax != 0.0f) ? 128.0f / amax : 0.0f;\n        for (int i = 0; i < hd; i++)"),

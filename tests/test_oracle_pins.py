@@ -589,3 +589,30 @@ def test_kv_wsum_matches_dequantized_einsum(orc):
     assert np.allclose(got, want, rtol=1e-13, atol=1e-15)
     # the dequantized rows are within half a step of the f32 inputs
     assert np.all(np.abs(vq.reshape(-1, hd) - v) <= dv[:, None] / 2 * (1 + 1e-6) + 1e-12)
+
+
+# --------------------------------------------------------------------------- RMSNorm
+def test_rmsnorm_matches_float64(orc):
+    """h = rmsnorm(x) ahead of the quantizer ([krafla] "Architecture", "Data flow for one token"),
+    reading x * w / sqrt(mean(x^2) + eps): the f32 result is within 2e-6 of a float64 evaluation
+    per element (the fixed-order f32 sum of squares and five single roundings), for an eps that
+    matters and one that does not."""
+    g = np.random.default_rng(60)
+    for K, eps in ((4096, 1e-6), (896, 0.5), (256, 1e-5)):
+        x = workloads.activations_f32(3, K, seed=K)
+        w = g.uniform(0.25, 2.0, size=K).astype(np.float32)
+        h = orc.rmsnorm(x, w, eps)
+        x64 = x.astype(np.float64)
+        ref = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + eps) * w
+        assert np.all(np.abs(h - ref) <= 2e-6 * np.abs(ref) + 1e-30), np.max(np.abs(h - ref) / np.abs(ref))
+
+
+def test_rmsnorm_exact_cases(orc):
+    """A constant power-of-two vector with eps = 0 normalizes to -w exactly, and scaling x by a
+    power of two leaves h unchanged bit for bit (every step scales exactly)."""
+    K = 512
+    w = np.random.default_rng(61).uniform(0.5, 1.5, size=K).astype(np.float32)
+    x = np.full((1, K), -0.5, dtype=np.float32)
+    assert np.array_equal(orc.rmsnorm(x, w, 0.0)[0], -w)
+    y = workloads.activations_f32(2, K, seed=62)
+    assert np.array_equal(orc.rmsnorm(y, w, 0.0).view(np.uint32), orc.rmsnorm(y * 4, w, 0.0).view(np.uint32))
