@@ -464,9 +464,27 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
             qmm.qmm_linear_group(ms[0][1], [m[4] for m in ms], [m[2] for m in ms], xin_, scratch, scratch.numel(),
                                  [outs[n] for n in names], 1, K, stream=sh)
 
+    # the same four launches with each group's RMSNorm inside it: h = rmsnorm(x) ; qa = quantize(h)
+    # feeding Q, K, V (and gate, up) from one launch, as the layer's data flow reads
+    gam = to_dev(np.random.default_rng(cfg["seed"]).uniform(0.5, 1.5, size=4096).astype(np.float32))
+
+    def layer_norm(i):
+        s = sets[i % C]
+        for names, xin_, normed in ((("Wq", "Wk", "Wv"), xh, True), (("Wo",), xo, False),
+                                    (("W_gate", "W_up"), xh, True), (("W_down",), xd, False)):
+            ms = [s[by[n]] for n in names]
+            K = ms[0][3]
+            if normed:
+                qmm.qmm_linear_norm(ms[0][1], [m[4] for m in ms], [m[2] for m in ms], xin_, gam, 1e-6, scratch,
+                                    scratch.numel(), [outs[n] for n in names], 1, K, stream=sh)
+            else:
+                qmm.qmm_linear_group(ms[0][1], [m[4] for m in ms], [m[2] for m in ms], xin_, scratch,
+                                     scratch.numel(), [outs[n] for n in names], 1, K, stream=sh)
+
     t_layer = timed_graph(layer, 8)
     t_lin = timed_graph(layer_linear, 8)
     t_grp = timed_graph(layer_group, 8)
+    t_nrm = timed_graph(layer_norm, 8)
     res["q4_K_M_layer_4096"] = {"layer_us": round(t_layer * 1e6, 3), "GB/s": round(layer_bytes / t_layer / 1e9, 1),
                                 "frac_hbm": round(layer_bytes / t_layer / 1e9 / hbm, 4), "weight_bytes": layer_bytes,
                                 "equiv_tok_s_36_layers_matmuls_only": round(1.0 / (36 * t_layer), 1),
@@ -479,7 +497,10 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
                                 "group_GB/s": round(layer_bytes / t_grp / 1e9, 1),
                                 "group_frac_hbm": round(layer_bytes / t_grp / 1e9 / hbm, 4),
                                 "group_launches_per_layer": 4,
-                                "group_equiv_tok_s_36_layers_matmuls_only": round(1.0 / (36 * t_grp), 1)}
+                                "group_equiv_tok_s_36_layers_matmuls_only": round(1.0 / (36 * t_grp), 1),
+                                "group_with_rmsnorm_layer_us": round(t_nrm * 1e6, 3),
+                                "group_with_rmsnorm_GB/s": round(layer_bytes / t_nrm / 1e9, 1),
+                                "group_with_rmsnorm_note": "QKV and gate+up launches also RMSNorm their row"}
     del sets, mats
 
     # the Q8 KV cache of one decode-attention layer: quantize the query heads, score every cached

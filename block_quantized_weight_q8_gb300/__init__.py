@@ -59,6 +59,8 @@ SIGNATURES = {
     "qmm_linear_q5_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
     "qmm_get_rows": ("tpppiiiq", ctypes.c_int),
+    "qmm_rmsnorm_quantize": ("tppfpiiq", ctypes.c_int),
+    "qmm_linear_norm": ("ttppppfpspiiq", ctypes.c_int),
     "qmm_kv_row_bytes": ("i", ctypes.c_size_t),
     "qmm_kv_quantize": ("ppiiq", ctypes.c_int),
     "qmm_kv_scores": ("pppiiiifq", ctypes.c_int),
@@ -246,6 +248,24 @@ def qmm_linear_group(wtype, Ws, Ns, x, scratch, scratch_bytes, ys, M, K, stream=
     _call("qmm_linear_group", _type(wtype), G, ctypes.cast(w_arr, ctypes.c_void_p), ctypes.cast(n_arr, ctypes.c_void_p),
           ptr(x), ptr(scratch), int(scratch_bytes), ctypes.cast(y_arr, ctypes.c_void_p), int(M), int(K),
           stream_handle(stream))
+
+
+def qmm_rmsnorm_quantize(act, x, w, eps, xq, M, K, stream=None):
+    """Quantize the RMSNormed rows (x * s) * w to act ("q8_0" or "q8_K")."""
+    _call("qmm_rmsnorm_quantize", _type(act), ptr(x), ptr(w), float(eps), ptr(xq), int(M), int(K), stream_handle(stream))
+
+
+def qmm_linear_norm(wtype, Ws, Ns, x, w, eps, scratch, scratch_bytes, ys, M, K, stream=None):
+    """qmm_linear_group on the RMSNormed rows of x (norm weight w, eps)."""
+    G = len(Ws)
+    if not (len(Ns) == G and len(ys) == G):
+        raise ValueError("Ws, Ns and ys must have the same length")
+    w_arr = (ctypes.c_void_p * max(G, 1))(*[ptr(m) for m in Ws])
+    n_arr = (ctypes.c_int64 * max(G, 1))(*[int(n) for n in Ns])
+    y_arr = (ctypes.c_void_p * max(G, 1))(*[ptr(y) for y in ys])
+    _call("qmm_linear_norm", _type(wtype), G, ctypes.cast(w_arr, ctypes.c_void_p), ctypes.cast(n_arr, ctypes.c_void_p),
+          ptr(x), ptr(w), float(eps), ptr(scratch), int(scratch_bytes), ctypes.cast(y_arr, ctypes.c_void_p), int(M),
+          int(K), stream_handle(stream))
 
 
 def qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=None):

@@ -19,6 +19,11 @@ qmm_status matvec_group_dispatch(int wt, int G, const void* const* W, const int6
                                  const void* xq, int64_t K, cudaStream_t stream, bool pdl);
 qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                               cudaStream_t stream, bool pdl);
+qmm_status rmsnorm_quantize_launch(int act, const float* x, const float* w, float eps, void* xq, int64_t M, int64_t K,
+                                   cudaStream_t stream, bool pdl);
+qmm_status matvec_group_norm_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
+                                      const float* x, const float* gamma, float eps, void* xq_out, int64_t K,
+                                      cudaStream_t stream, bool pdl);
 
 // [minfer] "10 . CPU matmul: quantized weights x Q8_0 activations" s3.2
 // (cpu_quant_matmul_f32): the weight type alone decides the activation format;
@@ -97,6 +102,57 @@ static qmm_status linear_group(int wt, int G, const void* const* W, const int64_
     return QMM_OK;
 }
 
+// [krafla] "Architecture", "Data flow for one token": h = rmsnorm(x) ; qa =
+// quantize_q8(h) ; then the matvecs that read qa.  A token is one launch (each
+// CTA norms and quantizes the row itself); a prefill that takes the tensor-core
+// matmul norms and quantizes all rows first; a row too large for the fused
+// kernel's shared memory is normed and quantized by its own kernel.
+static qmm_status linear_norm(int wt, int G, const void* const* W, const int64_t* N, const float* x, const float* w,
+                              float eps, void* scratch, size_t scratch_bytes, float* const* y, int64_t M, int64_t K,
+                              cudaStream_t stream) {
+    const int act = act_type_of(wt);
+    if (act < 0) return QMM_E_TYPE;
+    if (G < 1 || G > 8) return QMM_E_SHAPE;
+    if (!W || !N || !x || !w || !scratch || !y) return QMM_E_NULL;
+    for (int g = 0; g < G; g++) {
+        if (!W[g] || !y[g]) return QMM_E_NULL;
+        const qmm_status st = check_shape(wt, M, N[g], K);
+        if (st != QMM_OK) return st;
+        if (!aligned16(W[g]) || !aligned16(y[g])) return QMM_E_ALIGN;
+    }
+    if (!aligned16(x) || !aligned16(w) || !aligned16(scratch)) return QMM_E_ALIGN;
+    const size_t xrb = row_bytes_of(act, K);
+    if (scratch_bytes < (size_t)M * xrb) return QMM_E_SCRATCH;
+    qmm_status st;
+    if (M > 1 && (wt == QMM_Q4_0 || kq_uses_tensor_cores(wt, M, K))) {
+        st = rmsnorm_quantize_launch(act, x, w, eps, scratch, M, K, stream, true);
+        if (st != QMM_OK) return st;
+        for (int g = 0; g < G; g++) {
+            st = wt == QMM_Q4_0 ? matmul_q4_0_launch(W[g], scratch, y[g], M, N[g], K, stream, true)
+                                : matmul_kq_launch(wt, W[g], scratch, y[g], M, N[g], K, stream, true);
+            if (st != QMM_OK) return st;
+        }
+        return QMM_OK;
+    }
+    float* yt[8];
+    bool fused = true;
+    for (int64_t t = 0; t < M; t++) {
+        for (int g = 0; g < G; g++) yt[g] = y[g] + t * N[g];
+        st = QMM_E_SHAPE;
+        if (fused)
+            st = matvec_group_norm_dispatch(wt, G, W, N, yt, x + t * K, w, eps, (uint8_t*)scratch + t * xrb, K,
+                                            stream, true);
+        if (st == QMM_E_SHAPE && t == 0) {
+            fused = false;
+            st = rmsnorm_quantize_launch(act, x, w, eps, scratch, M, K, stream, true);
+            if (st != QMM_OK) return st;
+        }
+        if (!fused) st = matvec_group_dispatch(wt, G, W, N, yt, (const uint8_t*)scratch + t * xrb, K, stream, true);
+        if (st != QMM_OK) return st;
+    }
+    return QMM_OK;
+}
+
 }  // namespace qmm
 
 using namespace qmm;
@@ -111,6 +167,12 @@ qmm_status qmm_linear_group(int wtype, int G, const void* const* W, const int64_
     return linear_group(wtype, G, W, N, x, xq_scratch, scratch_bytes, y, M, K, (cudaStream_t)stream);
 }
 unsigned qmm_internal_matmul_error(int clear);
+
+qmm_status qmm_linear_norm(int wtype, int G, const void* const* W, const int64_t* N, const float* x, const float* w,
+                           float eps, void* xq_scratch, size_t scratch_bytes, float* const* y, int64_t M, int64_t K,
+                           qmm_stream_t stream) {
+    return linear_norm(wtype, G, W, N, x, w, eps, xq_scratch, scratch_bytes, y, M, K, (cudaStream_t)stream);
+}
 
 size_t qmm_block_bytes(int type) { return block_bytes_of(type); }
 int qmm_block_values(int type) { return block_values_of(type); }

@@ -43,6 +43,9 @@ struct MatSet {
     int N[kMaxGroup];
     int cta_end[kMaxGroup];
     int G;
+    const float* gamma;  // fused quantize: RMSNorm the row first with this weight (null: no norm)
+    float eps;
+    uint32_t norm_off;   // shared-memory offset of the norm's K/8 partial sums
 };
 
 struct MatvecPlan {
@@ -57,6 +60,7 @@ struct MatvecPlan {
     uint32_t slot_bytes;  // bytes per slot (the item's 16-byte aligned superset)
     uint32_t act_bytes;   // shared bytes before the first slot (barriers, activation)
     uint32_t smem;        // total dynamic shared memory
+    uint32_t norm_off;    // a normed row's partial sums
     int grid;
 };
 
@@ -223,6 +227,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
     if (pdl) pdl_wait();  // the activation row comes from the previous kernel
     {
         const int nthr = blockDim.x;
+        float sn = 1.0f;  // the RMSNorm scale of the row, when the fused quantize norms it first
+        if constexpr (FUSE) {
+            if (set.gamma != nullptr) sn = rms_scale(x, K, reinterpret_cast<float*>(smem + set.norm_off), set.eps);
+        }
         if constexpr (F::ACT == QMM_Q8_0) {
             // one thread per activation block: read (or, with FUSE, quantize)
             // its 32 codes and put them in the layout the decoder reads
@@ -234,6 +242,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                     float4 v[8];
 #pragma unroll
                     for (int i = 0; i < 8; i++) v[i] = x4[i];
+                    if (set.gamma != nullptr) {
+                        const float4* g4 = reinterpret_cast<const float4*>(set.gamma) + (size_t)b * 8;
+#pragma unroll
+                        for (int i = 0; i < 8; i++) v[i] = norm4(v[i], sn, g4[i]);
+                    }
                     quant_q8_0_block(v, &dbits, w);
                     if (blockIdx.x == 0 && xq_out != nullptr) {
                         unsigned short* o = reinterpret_cast<unsigned short*>(xq_out + (size_t)b * 34);
@@ -263,9 +276,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                 const float4* x4 = reinterpret_cast<const float4*>(x);
                 for (int b0 = warp; b0 < nd; b0 += 2 * nw) {
                     const int b1 = b0 + nw;
-                    const float4 v0 = x4[b0 * 64 + 2 * lane], v1 = x4[b0 * 64 + 2 * lane + 1];
+                    float4 v0 = x4[b0 * 64 + 2 * lane], v1 = x4[b0 * 64 + 2 * lane + 1];
                     float4 v2 = make_float4(0.f, 0.f, 0.f, 0.f), v3 = v2;
                     if (b1 < nd) v2 = x4[b1 * 64 + 2 * lane], v3 = x4[b1 * 64 + 2 * lane + 1];
+                    if (set.gamma != nullptr) {
+                        const float4* g4 = reinterpret_cast<const float4*>(set.gamma);
+                        v0 = norm4(v0, sn, g4[b0 * 64 + 2 * lane]);
+                        v1 = norm4(v1, sn, g4[b0 * 64 + 2 * lane + 1]);
+                        if (b1 < nd) {
+                            v2 = norm4(v2, sn, g4[b1 * 64 + 2 * lane]);
+                            v3 = norm4(v3, sn, g4[b1 * 64 + 2 * lane + 1]);
+                        }
+                    }
                     quant_q8_K_lane(v0, v1, lane, xs + b0 * 292);
                     if (b1 < nd) quant_q8_K_lane(v2, v3, lane, xs + b1 * 292);
                 }
@@ -460,8 +482,8 @@ __host__ inline uint32_t matvec_act_bytes(int wt, int act, int K, bool su) {
 // items in flight when 12 or more warps fit that way, else one item with 16
 // warps (more warps beat a deeper ring there).
 template <int WT>
-static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceInfo& dev, bool fuse, MatvecPlan* p,
-                              int* cta_end) {
+static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceInfo& dev, bool fuse, bool norm,
+                              MatvecPlan* p, int* cta_end) {
     using F = Fmt<WT>;
     p->su = has_su<WT>() && K % 256 == 0;
     const int nunit = p->su ? (int)(K / 256) : (int)(K / F::BV);
@@ -531,6 +553,9 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     uint32_t act = matvec_act_bytes(WT, F::ACT, (int)K, p->su);
     // a fused Q8_K row is quantized into shared memory first (Q8_0 goes straight to its layout)
     if (fuse && F::ACT == QMM_Q8_K) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);
+    // a normed row: the K/8 partial sums of squares after the activation
+    const uint32_t norm_rel = act;
+    if (norm) act += align_up(4u * (uint32_t)(K / 8), 128u);
     const uint64_t part_bytes = p->pieces > 1 ? align_up((uint32_t)(rows_max * p->pieces * 4), 128u) : 0;
     const uint32_t bar_max = align_up(8u * kMaxWarps * kMaxDepth, 128u);
     if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + part_bytes + sb) return QMM_E_SHAPE;
@@ -572,6 +597,7 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     }
     p->nw = nw;
     p->part_off = align_up(8u * nw * p->depth, 128u) + act;
+    p->norm_off = align_up(8u * nw * p->depth, 128u) + norm_rel;
     p->act_bytes = p->part_off + (uint32_t)part_bytes;
     p->smem = p->act_bytes + (uint32_t)(nw * p->depth) * p->slot_bytes;
     return QMM_OK;
@@ -619,7 +645,8 @@ static qmm_status launch_matvec_su(const MatSet& set, const void* xq, const floa
 // names where CTA 0 stores the quantized row, or is null).
 template <int WT>
 static qmm_status launch_matvec(const void* const* W, const int64_t* N, float* const* y, int G, const void* xq,
-                                const float* x, int64_t K, cudaStream_t stream, bool pdl) {
+                                const float* x, int64_t K, cudaStream_t stream, bool pdl, const float* gamma,
+                                float eps) {
     if (G < 1 || G > kMaxGroup) return QMM_E_SHAPE;
     DeviceInfo dev;
     qmm_status st = current_device(&dev);
@@ -627,9 +654,12 @@ static qmm_status launch_matvec(const void* const* W, const int64_t* N, float* c
     MatvecPlan p;
     MatSet set = {};
     const bool fuse = x != nullptr;
-    st = plan_matvec<WT>(N, G, K, dev, fuse, &p, set.cta_end);
+    st = plan_matvec<WT>(N, G, K, dev, fuse, fuse && gamma != nullptr, &p, set.cta_end);
     if (st != QMM_OK) return st;
     set.G = G;
+    set.gamma = fuse ? gamma : nullptr;
+    set.eps = eps;
+    set.norm_off = p.norm_off;
     for (int g = 0; g < G; g++) {
         set.W[g] = (const uint8_t*)W[g];
         set.y[g] = y[g];
@@ -653,7 +683,7 @@ static qmm_status launch_matvec(const void* const* W, const int64_t* N, float* c
 // row x to quantize in the kernel 16 bytes).
 static qmm_status matvec_group_checked(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
                                        const void* xq, const float* x, int64_t K, cudaStream_t stream, bool pdl,
-                                       bool public_call) {
+                                       bool public_call, const float* gamma = nullptr, float eps = 0.0f) {
     if (G < 1 || G > kMaxGroup) return QMM_E_SHAPE;
     if (!W || !N || !y || (!xq && !x)) return QMM_E_NULL;
     for (int g = 0; g < G; g++) {
@@ -664,17 +694,17 @@ static qmm_status matvec_group_checked(int wt, int G, const void* const* W, cons
         if (!aligned16(W[g]) || ((uintptr_t)y[g] & 3u)) return QMM_E_ALIGN;
     }
     if (public_call && !aligned16(xq)) return QMM_E_ALIGN;
-    if (((uintptr_t)xq & 1u) || !aligned16(x)) return QMM_E_ALIGN;
+    if (((uintptr_t)xq & 1u) || !aligned16(x) || !aligned16(gamma)) return QMM_E_ALIGN;
     switch (wt) {
-    case QMM_Q4_0: return launch_matvec<QMM_Q4_0>(W, N, y, G, xq, x, K, stream, pdl);
-    case QMM_Q8_0: return launch_matvec<QMM_Q8_0>(W, N, y, G, xq, x, K, stream, pdl);
-    case QMM_Q4_K: return launch_matvec<QMM_Q4_K>(W, N, y, G, xq, x, K, stream, pdl);
-    case QMM_Q6_K: return launch_matvec<QMM_Q6_K>(W, N, y, G, xq, x, K, stream, pdl);
-    case QMM_Q2_K: return launch_matvec<QMM_Q2_K>(W, N, y, G, xq, x, K, stream, pdl);
-    case QMM_Q4_1: return launch_matvec<QMM_Q4_1>(W, N, y, G, xq, x, K, stream, pdl);
-    case QMM_Q5_0: return launch_matvec<QMM_Q5_0>(W, N, y, G, xq, x, K, stream, pdl);
-    case QMM_Q5_1: return launch_matvec<QMM_Q5_1>(W, N, y, G, xq, x, K, stream, pdl);
-    case QMM_Q5_K: return launch_matvec<QMM_Q5_K>(W, N, y, G, xq, x, K, stream, pdl);
+    case QMM_Q4_0: return launch_matvec<QMM_Q4_0>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
+    case QMM_Q8_0: return launch_matvec<QMM_Q8_0>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
+    case QMM_Q4_K: return launch_matvec<QMM_Q4_K>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
+    case QMM_Q6_K: return launch_matvec<QMM_Q6_K>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
+    case QMM_Q2_K: return launch_matvec<QMM_Q2_K>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
+    case QMM_Q4_1: return launch_matvec<QMM_Q4_1>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
+    case QMM_Q5_0: return launch_matvec<QMM_Q5_0>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
+    case QMM_Q5_1: return launch_matvec<QMM_Q5_1>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
+    case QMM_Q5_K: return launch_matvec<QMM_Q5_K>(W, N, y, G, xq, x, K, stream, pdl, gamma, eps);
     default: return QMM_E_TYPE;
     }
 }
@@ -703,6 +733,14 @@ qmm_status matvec_group_fused_dispatch(int wt, int G, const void* const* W, cons
                                        const float* x, void* xq_out, int64_t K, cudaStream_t stream, bool pdl) {
     if (!x) return QMM_E_NULL;
     return matvec_group_checked(wt, G, W, N, y, xq_out, x, K, stream, pdl, false);
+}
+
+// The same with the row RMSNormed by gamma (eps) before it is quantized.
+qmm_status matvec_group_norm_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
+                                      const float* x, const float* gamma, float eps, void* xq_out, int64_t K,
+                                      cudaStream_t stream, bool pdl) {
+    if (!x || !gamma) return QMM_E_NULL;
+    return matvec_group_checked(wt, G, W, N, y, xq_out, x, K, stream, pdl, false, gamma, eps);
 }
 
 // G matrices against one quantized row (internal: alignment as for per-token rows).

@@ -685,6 +685,44 @@ __device__ __forceinline__ void su_put_block(const uint32_t w[8], uint32_t dbits
     }
 }
 
+// ---------------------------------------------------------------- RMSNorm ahead of the quantizer
+// [krafla] "Architecture", "Data flow for one token": h = rmsnorm(x) ; qa =
+// quantize_q8(h).  h_i = (x_i * s) * w_i with s = 1/sqrt(ss/K + eps), each step
+// rounded once; ss in one fixed order -- 8-value sequential partials, then a
+// stride-doubling tree (step 1, 2, 4, ...: p[i] += p[i + step] for i a multiple
+// of 2*step) -- so that the codes of h are the same on every run and in the
+// scalar implementation of the same steps.  Every thread of the CTA calls it;
+// p: K/8 floats of shared memory; x 16-byte aligned, K % 8 == 0.
+__device__ __forceinline__ float rms_scale(const float* x, int K, float* p, float eps) {
+    const int n8 = K / 8;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+        const float4 a = x4[2 * i], b = x4[2 * i + 1];
+        float s = __fmul_rn(a.x, a.x);
+        s = __fadd_rn(s, __fmul_rn(a.y, a.y));
+        s = __fadd_rn(s, __fmul_rn(a.z, a.z));
+        s = __fadd_rn(s, __fmul_rn(a.w, a.w));
+        s = __fadd_rn(s, __fmul_rn(b.x, b.x));
+        s = __fadd_rn(s, __fmul_rn(b.y, b.y));
+        s = __fadd_rn(s, __fmul_rn(b.z, b.z));
+        s = __fadd_rn(s, __fmul_rn(b.w, b.w));
+        p[i] = s;
+    }
+    __syncthreads();
+    for (int step = 1; step < n8; step <<= 1) {
+        for (int i = 2 * step * (int)threadIdx.x; i + step < n8; i += 2 * step * (int)blockDim.x)
+            p[i] = __fadd_rn(p[i], p[i + step]);
+        __syncthreads();
+    }
+    const float mean = __fdiv_rn(p[0], (float)K);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+}
+
+__device__ __forceinline__ float4 norm4(float4 v, float s, float4 w) {
+    return make_float4(__fmul_rn(__fmul_rn(v.x, s), w.x), __fmul_rn(__fmul_rn(v.y, s), w.y),
+                       __fmul_rn(__fmul_rn(v.z, s), w.z), __fmul_rn(__fmul_rn(v.w, s), w.w));
+}
+
 // ---------------------------------------------------------------- super-units of Q4_1, Q5_0, Q5_1
 // Eight blocks (160, 176, 192 bytes) start on a 16-byte boundary when K % 256
 // == 0.  The activation for them: block bb of super-unit u keeps its codes

@@ -404,6 +404,60 @@ __global__ void quantize_q5_K_kernel(const float* __restrict__ x, uint8_t* __res
     }
 }
 
+// ---------------------------------------------------------------- RMSNorm + quantize
+// [krafla] "Architecture", "Data flow for one token": h = rmsnorm(x) ; qa =
+// quantize_q8(h).  One CTA per row: the norm's scale (rms_scale, a fixed-order
+// sum of squares), then h = (x * s) * w handed to the same per-block quantizer
+// arithmetic as quantize_q8_0_kernel / quantize_q8_K_kernel.
+__global__ void __launch_bounds__(256) rmsnorm_quantize_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                                               float eps, uint8_t* __restrict__ out, int K, int act,
+                                                               int pdl) {
+    extern __shared__ float rq_part[];
+    if (pdl) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
+    const float* xr = x + (int64_t)blockIdx.x * K;
+    const float sn = rms_scale(xr, K, rq_part, eps);
+    const float4* x4 = reinterpret_cast<const float4*>(xr);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (act == QMM_Q8_0) {
+        uint8_t* orow = out + (int64_t)blockIdx.x * (K / 32) * 34;
+        const int n4 = K / 4, n4r = (n4 + 31) / 32 * 32;  // whole warps: the 8-lane shuffles need them
+        for (int gt = warp * 32 + lane; gt < n4r; gt += blockDim.x) {
+            const bool active = gt < n4;
+            const float4 v = active ? norm4(x4[gt], sn, w4[gt]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            quant_q8_0_part(v, active, gt & 7, orow + (active ? (gt >> 3) * 34 : 0));
+        }
+    } else {
+        uint8_t* orow = out + (int64_t)blockIdx.x * (K / 256) * 292;
+        for (int b = warp; b < K / 256; b += blockDim.x >> 5) {
+            const float4 v0 = norm4(x4[b * 64 + 2 * lane], sn, w4[b * 64 + 2 * lane]);
+            const float4 v1 = norm4(x4[b * 64 + 2 * lane + 1], sn, w4[b * 64 + 2 * lane + 1]);
+            quant_q8_K_lane(v0, v1, lane, orow + b * 292);
+        }
+    }
+}
+
+qmm_status rmsnorm_quantize_launch(int act, const float* x, const float* w, float eps, void* xq, int64_t M, int64_t K,
+                                   cudaStream_t stream, bool pdl) {
+    if (M > 0x7FFFFFFFLL) return QMM_E_SHAPE;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)M);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = (size_t)(K / 8) * sizeof(float);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, rmsnorm_quantize_kernel, x, w, eps, (uint8_t*)xq, (int)K, act, pdl ? 1 : 0);
+    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
+
 template <class Kern>
 static qmm_status launch_weight_quant(Kern kern, int t, const float* w, void* wq, int64_t N, int64_t K,
                                       cudaStream_t stream) {
@@ -432,6 +486,17 @@ qmm_status qmm_quantize_q8_K(const float* x, void* xq, int64_t M, int64_t K, qmm
     qmm_status st = check_quant_args(QMM_Q8_K, x, xq, M, K);
     if (st != QMM_OK) return st;
     return quantize_act_launch(QMM_Q8_K, x, xq, M, K, (cudaStream_t)stream, false);
+}
+
+qmm_status qmm_rmsnorm_quantize(int act, const float* x, const float* w, float eps, void* xq, int64_t M, int64_t K,
+                                qmm_stream_t stream) {
+    if (act != QMM_Q8_0 && act != QMM_Q8_K) return QMM_E_TYPE;
+    qmm_status st = check_quant_args(act, x, xq, M, K);
+    if (st != QMM_OK) return st;
+    if (!w) return QMM_E_NULL;
+    if (K > kMaxK) return QMM_E_SHAPE;
+    if (!aligned16(w)) return QMM_E_ALIGN;
+    return rmsnorm_quantize_launch(act, x, w, eps, xq, M, K, (cudaStream_t)stream, false);
 }
 
 qmm_status qmm_quantize_q4_0(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream) {

@@ -258,6 +258,30 @@ QMM_API qmm_status qmm_linear_group(int wtype, int G, const void* const* W, cons
                                     void* xq_scratch, size_t scratch_bytes, float* const* y, int64_t M, int64_t K,
                                     qmm_stream_t stream);
 
+/* ---- RMSNorm fused ahead of the quantizer --------------------------------- */
+/* [krafla] "Architecture", "Data flow for one token": h = rmsnorm(x) ; qa =
+ * quantize_q8(h), then the matvecs that read qa.  The page gives no formula;
+ * reading: h_i = (x_i * s) * w_i, s = 1 / sqrt(ss / K + eps), every step an f32
+ * operation rounded once, and ss summed in one fixed order -- 8-value
+ * sequential partials, then a stride-doubling tree over them (step 1, 2, 4, ...:
+ * p[i] += p[i + step] for every multiple i of 2*step with i + step < K/8) -- so
+ * the codes of h are bit-identical to a scalar implementation of the same
+ * steps.  A model whose norm scales by 1 + w passes that vector as w.
+ *
+ * qmm_rmsnorm_quantize: act QMM_Q8_0 or QMM_Q8_K; x f32 [M][K], w f32 [K]
+ * (16-byte aligned), xq as for qmm_quantize_q8_0/q8_K; K <= 65536.
+ * qmm_linear_norm: qmm_linear_group on the normed rows (G = 1 for one matrix),
+ * the quantized normed rows left in the scratch.  A decode token is one launch
+ * (every CTA norms and quantizes the row itself); a prefill that takes the
+ * tensor-core matmul (Q4_0, or Q4_K/Q6_K/Q2_K with M >= 8 and K % 2048 == 0)
+ * norms and quantizes all rows first.  Errors as for qmm_linear_group, plus
+ * QMM_E_NULL for w. */
+QMM_API qmm_status qmm_rmsnorm_quantize(int act, const float* x, const float* w, float eps, void* xq, int64_t M,
+                                        int64_t K, qmm_stream_t stream);
+QMM_API qmm_status qmm_linear_norm(int wtype, int G, const void* const* W, const int64_t* N, const float* x,
+                                   const float* w, float eps, void* xq_scratch, size_t scratch_bytes, float* const* y,
+                                   int64_t M, int64_t K, qmm_stream_t stream);
+
 /* ---- prefill matmul, M tokens (hot path) -------------------------------- */
 /* Y[t][o] = sum_b d_w[o,b] * d_x[t,b] * isum[t,o,b] for M tokens at once: the
  * weights are read once per tile of tokens and reused across them ([krafla]

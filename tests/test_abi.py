@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
                  "qmm_matmul_q6_K", "qmm_matmul_q2_K",
                  "qmm_linear_q4_0", "qmm_blocksums", "qmm_status_str", "qmm_row_bytes", "qmm_matvec_q4_1",
                  "qmm_matvec_q5_0", "qmm_matvec_q5_1", "qmm_matvec_q5_K", "qmm_get_rows", "qmm_kv_quantize",
-                 "qmm_kv_scores", "qmm_kv_wsum"):
+                 "qmm_kv_scores", "qmm_kv_wsum", "qmm_rmsnorm_quantize", "qmm_linear_norm"):
         assert want in names
     assert set(names) == set(qmm.SIGNATURES), set(names) ^ set(qmm.SIGNATURES)
 
@@ -150,6 +150,26 @@ def test_get_rows_rejects_bad_arguments(lib):
     assert f(qmm.QMM_Q4_K, A, A, A, 1, 4, 128, None) == 2
     assert f(qmm.QMM_Q4_0, A, A + 2, A, 1, 4, 256, None) == 4  # ids not 4-byte aligned
     assert f(qmm.QMM_Q4_0, A, A, U, 1, 4, 256, None) == 4
+
+
+def test_norm_calls_reject_bad_arguments(lib):
+    f = lib.qmm_rmsnorm_quantize
+    e = ctypes.c_float(1e-6)
+    assert f(qmm.QMM_Q4_0, A, A, e, A, 1, 256, None) == 3     # not an activation type
+    assert f(qmm.QMM_Q8_0, A, None, e, A, 1, 256, None) == 1
+    assert f(qmm.QMM_Q8_K, A, A, e, A, 1, 96, None) == 2
+    assert f(qmm.QMM_Q8_0, A, A, e, A, 1, 131072, None) == 2  # beyond the 65536 limit
+    assert f(qmm.QMM_Q8_0, A, U, e, A, 1, 256, None) == 4
+    W = (ctypes.c_void_p * 2)(A, A)
+    N = (ctypes.c_int64 * 2)(64, 32)
+    Y = (ctypes.c_void_p * 2)(A, A)
+    g = lib.qmm_linear_norm
+    need = 2 * qmm.qmm_row_bytes("q8_K", 512)
+    assert g(qmm.QMM_Q4_K, 2, W, N, A, None, e, A, need, Y, 2, 512, None) == 1
+    assert g(qmm.QMM_Q4_K, 2, W, N, A, U, e, A, need, Y, 2, 512, None) == 4
+    assert g(qmm.QMM_Q4_K, 2, W, N, A, A, e, A, need - 1, Y, 2, 512, None) == 5
+    assert g(qmm.QMM_Q4_K, 9, W, N, A, A, e, A, need, Y, 2, 512, None) == 2
+    assert g(qmm.QMM_Q8_K, 2, W, N, A, A, e, A, need, Y, 2, 512, None) == 3
 
 
 def test_kv_cache_calls_reject_bad_arguments(lib):
