@@ -161,6 +161,7 @@ extern "C" {
 unsigned qmm_internal_matvec_error(int clear);
 unsigned qmm_internal_matmul_kq_error(int clear);
 unsigned qmm_internal_getrows_error(int clear);
+unsigned qmm_internal_kv_error(int clear);
 
 qmm_status qmm_linear_group(int wtype, int G, const void* const* W, const int64_t* N, const float* x, void* xq_scratch,
                             size_t scratch_bytes, float* const* y, int64_t M, int64_t K, qmm_stream_t stream) {
@@ -234,7 +235,8 @@ qmm_status qmm_linear_q5_K(const void* W, const float* x, void* s, size_t sb, fl
 qmm_status qmm_device_status(int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return QMM_E_CUDA;
     const unsigned e = qmm_internal_matvec_error(clear) | qmm_internal_matmul_error(clear) |
-                       qmm_internal_matmul_kq_error(clear) | qmm_internal_getrows_error(clear);
+                       qmm_internal_matmul_kq_error(clear) | qmm_internal_getrows_error(clear) |
+                       qmm_internal_kv_error(clear);
     if (cudaGetLastError() != cudaSuccess) return QMM_E_CUDA;
     if (e & 1u) return QMM_E_TIMEOUT;  // a device wait ran out of time
     if (e & 2u) return QMM_E_SHAPE;    // qmm_get_rows met an index outside [0, N)

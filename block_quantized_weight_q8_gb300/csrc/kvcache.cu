@@ -10,30 +10,28 @@
 // h / (Hq/Hkv) ([krafla] "Architecture", "Data flow for one token").
 //
 //   kv_quantize   one warp per row: amax, d = amax/127, codes rne(x*127/amax)
-//   kv_scores     a CTA per (128 positions, KV head): the K rows of the tile and
-//                 the group's query rows staged in shared memory, eight lanes per
-//                 position computing the group's G integer dots with dp4a and
-//                 meeting through shuffles; score = ((dq*dk) * isum) * scale, each
-//                 step rounded once
-//   kv_wsum       pass 1: a CTA per (128-position chunk, KV head): the chunk's V
-//                 rows and the group's weights staged in shared memory; thread
-//                 groups each take every groups-th position of the chunk, one
-//                 thread per 4 columns converting each V word once and running
-//                 an f32 FMA chain for every query head of the group; the groups'
-//                 sums are added in group order; pass 2: a warp per output adds
-//                 the chunks' partial sums, lane l taking chunks l, l + 32, ... in
-//                 order, then a fixed butterfly.  The grouping depends only on
-//                 hd, Hq/Hkv and P, so the result does not depend on the GPU.
-// The rows of one KV head sit Hkv rows apart and are only 4-byte aligned, so the
-// tiles are staged with 4-byte asynchronous copies (cp.async): every copy of a
-// tile is in flight at once, then one wait.
+//   kv_scores     a CTA per range of positions, every KV head: one contiguous,
+//                 16-byte aligned range of the cache, fetched by one bulk copy;
+//                 eight lanes per row computing the group's G integer dots with
+//                 dp4a and meeting through a transposing shuffle reduction;
+//                 score = ((dq*dk) * isum) * scale, each step rounded once
+//   kv_wsum       pass 1: a CTA per 32-position chunk (every KV head, or a group
+//                 of them when the rows do not fit), one bulk copy; one thread
+//                 per (KV head, 4 columns) converting each V word once and
+//                 running the f32 FMA chains of its query heads over the chunk's
+//                 positions in order; pass 2: per output, 8 warps each add every
+//                 8th chunk's sum in order, then the 8 in warp order.  The order
+//                 depends only on P, so the result does not depend on the GPU.
+// A ragged last tile, or a cache that is not 16-byte aligned, is staged with
+// 4-byte asynchronous copies (cp.async) instead: all in flight, then one wait.
+#include <type_traits>
+
 #include "qmm_device.cuh"
 #include "qmm_host.h"
 
 namespace qmm {
 
-constexpr int kKvRows = 128;    // positions per CTA of the score kernel
-constexpr int kKvChunk = 128;   // positions per partial sum of the V sum
+constexpr int kKvChunk = 32;    // positions per partial sum of the V sum
 constexpr int kKvMaxGroup = 8;  // query heads per KV head
 constexpr int kKvMaxHd = 256;
 
@@ -55,6 +53,7 @@ __device__ __forceinline__ void stage_rows(uint32_t* dst, int dst_stride, const 
 
 __global__ void __launch_bounds__(256) kv_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ out,
                                                           int64_t rows, int hd) {
+    pdl_wait();
     const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (r >= rows) return;  // whole warps leave together
@@ -67,75 +66,130 @@ __global__ void __launch_bounds__(256) kv_quantize_kernel(const float* __restric
     const float id = amax != 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
     if (lane == 0) *reinterpret_cast<float*>(o) = __fdiv_rn(amax, 127.0f);
     for (int i = lane; i < hd; i += 32) o[4 + i] = (uint8_t)(int8_t)clampi(__float2int_rn(__fmul_rn(xr[i], id)), -128, 127);
+    pdl_launch_dependents();
 }
 
-// Shared-memory row stride (words) for rows read by 8 lanes each, 4 rows per
-// warp: s = 8 (mod 32) puts the four rows' words in distinct bank octets.
-__host__ __device__ inline int kv_smem_stride(int nwd) { return nwd <= 8 ? 8 : 8 + (nwd - 8 + 31) / 32 * 32; }
+static __device__ unsigned int g_kv_error = 0;
 
-// grid (tiles of kKvRows positions, Hkv); 8 lanes per position, 256 threads.
-// Lane j of a position's octet takes code words j, j + 8, ... (at most 8 of
-// them, hd <= 256) and holds the group's query words for them in registers; the
-// G partial dots meet through three xor shuffles.  GT is G rounded up to 1, 2,
-// 4 or 8.
-template <int GT>
+// Positions per score CTA: a multiple of 4 (so the tile of TP * Hkv rows of
+// 4 + hd bytes is a multiple of 16 bytes) with at least 128 rows.
+__host__ __device__ inline int kv_score_positions(int Hkv) {
+    int tp = (128 + Hkv - 1) / Hkv;
+    tp = (tp + 3) / 4 * 4;
+    return tp < 4 ? 4 : tp;
+}
+
+// grid: tiles of TP positions, every KV head of them -- one contiguous range of
+// the cache, fetched by one bulk copy (or, for a ragged last tile or an
+// unaligned cache, by 4-byte asynchronous copies).  256 threads = 32 octets;
+// octet o takes the tile's rows o, o + 32, ...; lane j of an octet takes a
+// contiguous run of the row's code words and holds the matching query words of
+// the row's KV-head group in registers (reloaded when the octet's KV head
+// changes, never when Hkv divides 32).  The G partial dots meet through three xor
+// shuffles.  GT is G rounded up to 1, 2, 4 or 8; WT the code words per lane,
+// ceil(hd/32) rounded up to 1, 2, 4 or 8.
+template <int GT, int WT>
 __global__ void __launch_bounds__(256) kv_scores_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ kc,
                                                         float* __restrict__ scores, int G, int Hkv, int64_t P, int hd,
-                                                        float scale) {
-    extern __shared__ __align__(16) uint32_t kv_smem[];
-    const int nwd = (4 + hd) / 4, st = kv_smem_stride(nwd);
-    uint32_t* qs = kv_smem;            // G rows
-    uint32_t* ks = kv_smem + G * st;   // kKvRows rows
-    const int kvh = blockIdx.y;
-    const int64_t p0 = (int64_t)blockIdx.x * kKvRows;
-    const int rows = P - p0 < kKvRows ? (int)(P - p0) : kKvRows;
+                                                        float scale, int TP, int bulk) {
+    extern __shared__ __align__(16) uint8_t kv_tile[];
+    pdl_wait();
+    uint64_t* bar = reinterpret_cast<uint64_t*>(kv_tile);
+    uint32_t* ks = reinterpret_cast<uint32_t*>(kv_tile + 16);
+    const int nwd = (4 + hd) / 4, nq = hd / 4, wpl = (nq + 7) / 8;
     const int64_t rb = 4 + hd;
-    stage_rows(qs, st, q + (int64_t)kvh * G * rb, rb, G, nwd);
-    stage_rows(ks, st, kc + (p0 * Hkv + kvh) * rb, Hkv * rb, rows, nwd);
-    cp_async_wait_all();
-    __syncthreads();
-    const int j = threadIdx.x & 7;
-    uint32_t qw[GT][8];
-#pragma unroll
-    for (int g = 0; g < GT; g++)
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-            const int w = 1 + j + 8 * k;
-            qw[g][k] = (g < G && w < nwd) ? qs[g * st + w] : 0u;
+    const int64_t p0 = (int64_t)blockIdx.x * TP;
+    const int np = P - p0 < TP ? (int)(P - p0) : TP;
+    const int R = np * Hkv;
+    const uint8_t* src = kc + p0 * Hkv * rb;
+    const bool use_bulk = bulk && np == TP;
+    if (use_bulk) {
+        if (threadIdx.x == 0) {
+            mbar_init(smem_u32(bar), 1);
+            fence_mbar_init();
+            const uint32_t bytes = (uint32_t)(R * rb);
+            mbar_arrive_expect_tx(smem_u32(bar), bytes);
+            bulk_g2s(smem_u32(ks), src, bytes, smem_u32(bar), policy_evict_first());
         }
-    const float dq = j < G ? __uint_as_float(qs[j * st]) : 0.0f;
-    // the 32 octets take rows octet, octet + 32, ...
-    for (int r = threadIdx.x >> 3; r - (int)(threadIdx.x >> 3) < kKvRows; r += 32) {
-        const uint32_t* kr = ks + r * st;
+        __syncthreads();
+        const bool ok = mbar_wait_bounded(smem_u32(bar), 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) {  // every thread leaves together, so no shuffle misses a lane
+            if (threadIdx.x == 0) atomicOr(&g_kv_error, kErrTimeout);
+            return;
+        }
+    } else {
+        const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src);
+        for (int i = threadIdx.x; i < R * nwd; i += blockDim.x) cp_async4(ks + i, s4 + i);
+        cp_async_wait_all();
+        __syncthreads();
+    }
+    const int j = threadIdx.x & 7, oct = threadIdx.x >> 3;
+    const int w0 = 1 + j * wpl;  // this lane's first code word
+    // after the octet's transposing reduction lane j holds the dot of head gl
+    // of the group (bit k of j picks the upper half at round k)
+    int gl = 0;
+#pragma unroll
+    for (int m = 1, n = GT; n > 1; m <<= 1, n >>= 1)
+        if (j & m) gl += n >> 1;
+    uint32_t qw[GT][WT];
+    int cur = -1;
+    float dq = 0.0f;
+    // row r = oct + 32 it: position pl, KV head kvh, stepped without a division per row
+    const int dpl = 32 / Hkv, dkv = 32 - dpl * Hkv;
+    int pl = oct / Hkv, kvh = oct - pl * Hkv;
+    const int iters = (R + 31) / 32;  // the same count for every octet: the shuffles need whole warps
+    for (int it = 0; it < iters; it++, pl += dpl, kvh += dkv) {
+        if (kvh >= Hkv) kvh -= Hkv, pl += 1;
+        const int r = oct + 32 * it;
+        const bool live = r < R;
+        if (live && kvh != cur) {  // uniform per octet: its rows' KV head
+            const uint32_t* qg = reinterpret_cast<const uint32_t*>(q + (int64_t)kvh * G * rb);
+#pragma unroll
+            for (int g = 0; g < GT; g++)
+#pragma unroll
+                for (int k = 0; k < WT; k++)
+                    qw[g][k] = (g < G && k < wpl && w0 + k < nwd) ? __ldg(qg + g * nwd + w0 + k) : 0u;
+            dq = gl < G ? __uint_as_float(__ldg(qg + gl * nwd)) : 0.0f;
+            cur = kvh;
+        }
+        const uint32_t* kr = ks + r * nwd;
         int acc[GT];
 #pragma unroll
         for (int g = 0; g < GT; g++) acc[g] = 0;
-        if (r < rows) {
+        if (live) {
 #pragma unroll
-            for (int k = 0; k < 8; k++) {
-                const int w = 1 + j + 8 * k;
-                if (w < nwd) {
-                    const uint32_t kw = kr[w];
+            for (int k = 0; k < WT; k++) {
+                if (k < wpl && w0 + k < nwd) {
+                    const uint32_t kw = kr[w0 + k];
 #pragma unroll
                     for (int g = 0; g < GT; g++) acc[g] = dp4a(kw, qw[g][k], acc[g]);
                 }
             }
         }
+        // transposing reduction: at each round a lane keeps half of its sums and
+        // trades the other half with its partner, so GT - 1 shuffles leave one
+        // sum per lane; the remaining rounds add single values
+        int m = 1;
 #pragma unroll
-        for (int g = 0; g < GT; g++) {
-            acc[g] += __shfl_xor_sync(0xFFFFFFFFu, acc[g], 1);
-            acc[g] += __shfl_xor_sync(0xFFFFFFFFu, acc[g], 2);
-            acc[g] += __shfl_xor_sync(0xFFFFFFFFu, acc[g], 4);
+        for (int n = GT; n > 1; n >>= 1, m <<= 1) {
+            const bool hi = (j & m) != 0;
+#pragma unroll
+            for (int i = 0; i < n / 2; i++) {
+                const int send = hi ? acc[i] : acc[i + n / 2];
+                const int keep = hi ? acc[i + n / 2] : acc[i];
+                acc[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, m);
+            }
         }
-        if (r < rows && j < G) {
-            int a = acc[0];
-#pragma unroll
-            for (int g = 1; g < GT; g++)
-                if (g == j) a = acc[g];
+        for (; m < 8; m <<= 1) acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], m);
+        if (live && j < GT && gl < G) {
             const float dk = __uint_as_float(kr[0]);
-            scores[(int64_t)(kvh * G + j) * P + p0 + r] = __fmul_rn(__fmul_rn(__fmul_rn(dq, dk), (float)a), scale);
+            scores[(int64_t)(kvh * G + gl) * P + p0 + pl] =
+                __fmul_rn(__fmul_rn(__fmul_rn(dq, dk), (float)acc[0]), scale);
         }
     }
+    // the next kernel may launch once every CTA is here (or has left): launched
+    // earlier, its waiting CTAs would take the slots this grid's later waves need
+    pdl_launch_dependents();
 }
 
 // int8 byte k of v as an exact float: the biased byte (v ^ 0x80 per byte,
@@ -144,44 +198,77 @@ __device__ __forceinline__ float i8_to_f(uint32_t vb, int k) {
     return __fsub_rn(__uint_as_float(__byte_perm(vb, 0x4B000000u, 0x7640u + (uint32_t)k)), 8388736.0f);
 }
 
-// pass 1: grid (chunks, Hkv).  One thread per column quad in each of `groups`
-// thread groups; group k walks the chunk's positions k, k + groups, ...,
-// converting each V word once and running the G heads' f32 FMA chains; then
-// the groups' sums are added in group order.  GT as for the scores.
+// pass 1: grid (chunks of kKvChunk positions, groups of hg KV heads).  The
+// chunk's rows of those heads are staged in shared memory (one bulk copy when
+// the group is every head and the range is aligned, else 4-byte asynchronous
+// copies of each position's run of hg rows), with the weights of their query
+// heads.  One thread per (KV head, column quad) walks the chunk's positions in
+// order, converting each V word once and running the f32 FMA chains of the
+// group's GT (>= G) query heads.  Partial sums: part[(c * Hq + h) * hd + i].
 template <int GT>
 __global__ void __launch_bounds__(512) kv_wsum_partial_kernel(const float* __restrict__ w, const uint8_t* __restrict__ vc,
                                                               float* __restrict__ part, int G, int Hkv, int64_t P,
-                                                              int hd, int groups, int gthreads) {
-    extern __shared__ __align__(16) uint32_t kv_smem[];
+                                                              int hd, int hg, int bulk) {
+    extern __shared__ __align__(16) uint8_t kv_tile[];
+    pdl_wait();
+    uint64_t* bar = reinterpret_cast<uint64_t*>(kv_tile);
     const int nq = hd / 4, nwd = nq + 1;
-    const int kvh = blockIdx.y;
-    const int c = blockIdx.x, nc = gridDim.x;
+    const int64_t rb = 4 + hd;
+    const int c = blockIdx.x, kv0 = blockIdx.y * hg;
+    const int hn = Hkv - kv0 < hg ? Hkv - kv0 : hg;  // KV heads in this group
     const int64_t pa = (int64_t)c * kKvChunk;
     const int n = P - pa < kKvChunk ? (int)(P - pa) : kKvChunk;
-    const int64_t rb = 4 + hd;
-    uint32_t* vs = kv_smem;                                         // n rows of nwd words
-    float* ws = reinterpret_cast<float*>(kv_smem + kKvChunk * nwd);  // G rows of n weights
-    float4* red = reinterpret_cast<float4*>(ws + G * kKvChunk);      // groups x G x nq partial sums
-    stage_rows(vs, nwd, vc + (pa * Hkv + kvh) * rb, Hkv * rb, n, nwd);
-    for (int g = 0; g < G; g++)
-        for (int j = threadIdx.x; j < n; j += blockDim.x) cp_async4(ws + g * kKvChunk + j, w + (kvh * G + g) * P + pa + j);
+    const int Hq = Hkv * G;
+    uint32_t* vs = reinterpret_cast<uint32_t*>(kv_tile + 16);                 // n positions x hn rows
+    float* ws = reinterpret_cast<float*>(vs + (size_t)kKvChunk * hg * nwd);    // hn*G heads x kKvChunk weights
+    const uint8_t* src = vc + (pa * Hkv + kv0) * rb;
+    const bool use_bulk = bulk && hn == Hkv && n == kKvChunk;
+    if (use_bulk && threadIdx.x == 0) {
+        mbar_init(smem_u32(bar), 1);
+        fence_mbar_init();
+        const uint32_t bytes = (uint32_t)((int64_t)n * Hkv * rb);
+        mbar_arrive_expect_tx(smem_u32(bar), bytes);
+        bulk_g2s(smem_u32(vs), src, bytes, smem_u32(bar), policy_evict_first());
+    }
+    if (!use_bulk) {  // position p's hn rows are one run of hn * nwd words
+        const int run = hn * nwd;
+        for (int i = threadIdx.x; i < n * run; i += blockDim.x) {
+            const int pp = i / run, k = i - pp * run;
+            cp_async4(vs + (size_t)pp * run + k,
+                      reinterpret_cast<const uint32_t*>(src + (int64_t)pp * Hkv * rb) + k);
+        }
+    }
+    for (int i = threadIdx.x; i < hn * G * n; i += blockDim.x) {
+        const int hh = i / n, j = i - hh * n;
+        cp_async4(ws + hh * kKvChunk + j, w + (int64_t)(kv0 * G + hh) * P + pa + j);
+    }
     cp_async_wait_all();
     __syncthreads();
-    const int grp = threadIdx.x / gthreads, quad = threadIdx.x - grp * gthreads;
-    if (quad < nq) {
+    if (use_bulk) {
+        const bool ok = mbar_wait_bounded(smem_u32(bar), 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) atomicOr(&g_kv_error, kErrTimeout);
+            return;
+        }
+    }
+    const int run = hn * nwd;
+    for (int t = threadIdx.x; t < hn * nq; t += blockDim.x) {
+        const int kh = t / nq, quad = t - kh * nq;
         float4 a[GT];
 #pragma unroll
         for (int g = 0; g < GT; g++) a[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t* col = vs + kh * nwd;
+        const float* wk = ws + kh * G * kKvChunk;
 #pragma unroll 2
-        for (int j = grp; j < n; j += groups) {
-            const uint32_t* row = vs + j * nwd;
+        for (int j = 0; j < n; j++) {
+            const uint32_t* row = col + j * run;
             const float dv = __uint_as_float(row[0]);
             const uint32_t vb = row[1 + quad] ^ 0x80808080u;
             const float v0 = i8_to_f(vb, 0), v1 = i8_to_f(vb, 1), v2 = i8_to_f(vb, 2), v3 = i8_to_f(vb, 3);
 #pragma unroll
             for (int g = 0; g < GT; g++) {
                 if (g < G) {
-                    const float coef = __fmul_rn(ws[g * kKvChunk + j], dv);
+                    const float coef = __fmul_rn(wk[g * kKvChunk + j], dv);
                     a[g].x = __fmaf_rn(coef, v0, a[g].x);
                     a[g].y = __fmaf_rn(coef, v1, a[g].y);
                     a[g].z = __fmaf_rn(coef, v2, a[g].z);
@@ -190,53 +277,71 @@ __global__ void __launch_bounds__(512) kv_wsum_partial_kernel(const float* __res
             }
         }
 #pragma unroll
-        for (int g = 0; g < GT; g++)
-            if (g < G) red[(grp * G + g) * nq + quad] = a[g];
-    }
-    __syncthreads();
-    for (int t2 = threadIdx.x; t2 < G * nq; t2 += blockDim.x) {
-        float4 sum = red[t2];
-        for (int k = 1; k < groups; k++) {
-            const float4 v = red[k * G * nq + t2];
-            sum.x = __fadd_rn(sum.x, v.x);
-            sum.y = __fadd_rn(sum.y, v.y);
-            sum.z = __fadd_rn(sum.z, v.z);
-            sum.w = __fadd_rn(sum.w, v.w);
+        for (int g = 0; g < GT; g++) {
+            if (g < G) {
+                const int h = (kv0 + kh) * G + g;
+                *reinterpret_cast<float4*>(part + ((int64_t)c * Hq + h) * hd + 4 * quad) = a[g];
+            }
         }
-        const int g = t2 / nq, quad2 = t2 - g * nq;
-        *reinterpret_cast<float4*>(part + (((int64_t)kvh * nc + c) * G + g) * hd + 4 * quad2) = sum;
     }
+    pdl_launch_dependents();
 }
 
-// pass 2: one warp per output (h, i).  Lane l adds chunks l, l + 32, ... in
-// order, then the 32 lane sums meet in a fixed butterfly: the order depends on
-// the chunk count alone.
+// pass 2: a CTA of 8 warps per 32 consecutive outputs (lane = output, so every
+// load is one coalesced 128-byte row of a chunk's sums).  Warp k adds chunks k,
+// k + 8, ... in order; then the 8 warp sums are added in warp order.  The order
+// depends on the chunk count alone.
 __global__ void __launch_bounds__(256) kv_wsum_reduce_kernel(const float* __restrict__ part, float* __restrict__ out,
-                                                             int G, int Hq, int nc, int hd) {
-    const int64_t o = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (o >= (int64_t)Hq * hd) return;  // whole warps leave together
-    const int h = (int)(o / hd), i = (int)(o - (int64_t)h * hd);
-    const int kvh = h / G, g = h - kvh * G;
-    const float* src = part + ((int64_t)kvh * nc * G + g) * hd + i;
-    const int64_t step = (int64_t)G * hd;
+                                                             int Hq, int nc, int hd) {
+    __shared__ float red[8][32];
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t outs = (int64_t)Hq * hd;
+    const int64_t o = (int64_t)blockIdx.x * 32 + lane;
     float s = 0.0f;
-#pragma unroll 4
-    for (int c = lane; c < nc; c += 32) s = __fadd_rn(s, src[c * step]);
+    if (o < outs) {
+#pragma unroll 8
+        for (int c = warp; c < nc; c += 8) s = __fadd_rn(s, part[(int64_t)c * outs + o]);
+    }
+    red[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0 && o < outs) {
+        float t = red[0][lane];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, off));
-    if (lane == 0) out[o] = s;
+        for (int k = 1; k < 8; k++) t = __fadd_rn(t, red[k][lane]);
+        out[o] = t;
+    }
+    pdl_launch_dependents();
 }
 
 static bool kv_hd_ok(int64_t hd) { return hd >= 16 && hd <= kKvMaxHd && hd % 16 == 0; }
 
 static qmm_status kv_heads_ok(int64_t Hq, int64_t Hkv, int64_t P) {
-    if (Hq < 1 || Hkv < 1 || P < 1 || Hq % Hkv || Hq / Hkv > kKvMaxGroup || Hkv > 65535) return QMM_E_SHAPE;
+    if (Hq < 1 || Hkv < 1 || P < 1 || Hq % Hkv || Hq / Hkv > kKvMaxGroup || Hkv > 128) return QMM_E_SHAPE;
     if (P > 0x7FFFFFFFLL || P * Hq > ((int64_t)1 << 40)) return QMM_E_SHAPE;
     return QMM_OK;
 }
 
 static bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
+
+// A programmatic dependent launch: the kernel waits for its predecessor's
+// memory before it reads anything, and lets its successor launch when its own
+// work is done.
+template <typename... KArgs, typename... Args>
+static qmm_status launch_pdl(void (*kern)(KArgs...), dim3 grid, int block, size_t smem, cudaStream_t stream,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
 
 }  // namespace qmm
 
@@ -246,14 +351,24 @@ extern "C" {
 
 size_t qmm_kv_row_bytes(int64_t hd) { return kv_hd_ok(hd) ? (size_t)(4 + hd) : 0; }
 
+unsigned qmm_internal_kv_error(int clear) {
+    unsigned v = 0;
+    cudaMemcpyFromSymbol(&v, g_kv_error, sizeof(v));
+    if (clear) {
+        const unsigned z = 0;
+        cudaMemcpyToSymbol(g_kv_error, &z, sizeof(z));
+    }
+    return v;
+}
+
 qmm_status qmm_kv_quantize(const float* x, void* out, int64_t rows, int64_t hd, qmm_stream_t stream) {
     if (!x || !out) return QMM_E_NULL;
     if (rows < 1 || !kv_hd_ok(hd) || rows > ((int64_t)1 << 36)) return QMM_E_SHAPE;
     if (!aligned4(x) || !aligned4(out)) return QMM_E_ALIGN;
     const int64_t grid = (rows * 32 + 255) / 256;
     if (grid > 0x7FFFFFFFLL) return QMM_E_SHAPE;
-    kv_quantize_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(x, (uint8_t*)out, rows, (int)hd);
-    return launch_status();
+    return launch_pdl(kv_quantize_kernel, dim3((unsigned)grid), 256, 0, (cudaStream_t)stream, x, (uint8_t*)out, rows,
+                      (int)hd);
 }
 
 qmm_status qmm_kv_scores(const void* q, const void* kc, float* scores, int64_t Hq, int64_t Hkv, int64_t P, int64_t hd,
@@ -264,15 +379,34 @@ qmm_status qmm_kv_scores(const void* q, const void* kc, float* scores, int64_t H
     if (st != QMM_OK) return st;
     if (!aligned4(q) || !aligned4(kc) || !aligned4(scores)) return QMM_E_ALIGN;
     const int G = (int)(Hq / Hkv);
-    const size_t smem = (size_t)(G + kKvRows) * (size_t)kv_smem_stride((int)(4 + hd) / 4) * 4;
-    const dim3 grid((unsigned)((P + kKvRows - 1) / kKvRows), (unsigned)Hkv);
+    const int TP = kv_score_positions((int)Hkv);
+    const size_t smem = 16 + (size_t)TP * (size_t)Hkv * (size_t)(4 + hd);
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != QMM_OK) return st;
+    if (smem > (size_t)dev.max_smem_optin) return QMM_E_SHAPE;
+    const int bulk = aligned16(kc) ? 1 : 0;
+    const dim3 grid((unsigned)((P + TP - 1) / TP));
     cudaStream_t cs = (cudaStream_t)stream;
     const uint8_t *qb = (const uint8_t*)q, *kb = (const uint8_t*)kc;
-    if (G == 1) kv_scores_kernel<1><<<grid, 256, smem, cs>>>(qb, kb, scores, G, (int)Hkv, P, (int)hd, scale);
-    else if (G == 2) kv_scores_kernel<2><<<grid, 256, smem, cs>>>(qb, kb, scores, G, (int)Hkv, P, (int)hd, scale);
-    else if (G <= 4) kv_scores_kernel<4><<<grid, 256, smem, cs>>>(qb, kb, scores, G, (int)Hkv, P, (int)hd, scale);
-    else kv_scores_kernel<8><<<grid, 256, smem, cs>>>(qb, kb, scores, G, (int)Hkv, P, (int)hd, scale);
-    return launch_status();
+    auto go = [&](auto kern) -> qmm_status {
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return QMM_E_CUDA;
+        return launch_pdl(kern, grid, 256, smem, cs, qb, kb, scores, G, (int)Hkv, P, (int)hd, scale, TP, bulk);
+    };
+    const int wpl = ((int)hd / 4 + 7) / 8;
+    auto by_w = [&](auto g_tag) -> qmm_status {
+        constexpr int GT = decltype(g_tag)::value;
+        if (wpl <= 1) return go(kv_scores_kernel<GT, 1>);
+        if (wpl <= 2) return go(kv_scores_kernel<GT, 2>);
+        if (wpl <= 4) return go(kv_scores_kernel<GT, 4>);
+        return go(kv_scores_kernel<GT, 8>);
+    };
+    if (G == 1) return by_w(std::integral_constant<int, 1>());
+    if (G == 2) return by_w(std::integral_constant<int, 2>());
+    if (G <= 4) return by_w(std::integral_constant<int, 4>());
+    return by_w(std::integral_constant<int, 8>());
 }
 
 size_t qmm_kv_wsum_scratch_bytes(int64_t Hq, int64_t P, int64_t hd) {
@@ -291,30 +425,39 @@ qmm_status qmm_kv_wsum(const float* w, const void* vc, float* out, void* scratch
     const int G = (int)(Hq / Hkv);
     const int64_t nc = (P + kKvChunk - 1) / kKvChunk;
     if (nc > 0x7FFFFFFFLL) return QMM_E_SHAPE;
-    const int nq = (int)(hd / 4);
-    const int gthreads = (nq + 31) / 32 * 32;
-    int groups = 512 / gthreads;
-    if (groups > 16) groups = 16;
-    // the staged chunk, its weights and the groups' sums within the default 48 KB
-    // (one group always fits: at most 33280 + 4096 + 8192 bytes)
-    const size_t base = (size_t)kKvChunk * (size_t)(4 + hd) + (size_t)G * kKvChunk * sizeof(float);
-    while (groups > 1 && base + (size_t)groups * G * nq * 16 > 48 * 1024) groups--;
-    const size_t smem = base + (size_t)groups * G * nq * 16;
+    const int nq = (int)(hd / 4), nwd = nq + 1;
+    // KV heads per CTA: all of them when the chunk's rows and weights fit in
+    // about 100 KB of shared memory (then one bulk copy fetches the rows)
+    const size_t per_head = (size_t)kKvChunk * nwd * 4 + (size_t)G * kKvChunk * 4;
+    int hg = (int)((100 * 1024 - 16) / per_head);
+    if (hg > Hkv) hg = (int)Hkv;
+    if (hg < 1) hg = 1;
+    const size_t smem = 16 + (size_t)hg * per_head;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != QMM_OK) return st;
+    if (smem > (size_t)dev.max_smem_optin) return QMM_E_SHAPE;
+    const int bulk = (aligned16(vc) && hg == Hkv) ? 1 : 0;
+    int nt = (hg * nq + 31) / 32 * 32;
+    if (nt > 512) nt = 512;
     cudaStream_t cs = (cudaStream_t)stream;
-    const dim3 grid((unsigned)nc, (unsigned)Hkv);
-    const int nt = groups * gthreads;
+    const dim3 grid((unsigned)nc, (unsigned)((Hkv + hg - 1) / hg));
     const uint8_t* vb = (const uint8_t*)vc;
     float* pt = (float*)scratch;
-    if (G == 1) kv_wsum_partial_kernel<1><<<grid, nt, smem, cs>>>(w, vb, pt, G, (int)Hkv, P, (int)hd, groups, gthreads);
-    else if (G == 2) kv_wsum_partial_kernel<2><<<grid, nt, smem, cs>>>(w, vb, pt, G, (int)Hkv, P, (int)hd, groups, gthreads);
-    else if (G <= 4) kv_wsum_partial_kernel<4><<<grid, nt, smem, cs>>>(w, vb, pt, G, (int)Hkv, P, (int)hd, groups, gthreads);
-    else kv_wsum_partial_kernel<8><<<grid, nt, smem, cs>>>(w, vb, pt, G, (int)Hkv, P, (int)hd, groups, gthreads);
-    st = launch_status();
+    auto go = [&](auto kern) -> qmm_status {
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return QMM_E_CUDA;
+        return launch_pdl(kern, grid, nt, smem, cs, w, vb, pt, G, (int)Hkv, P, (int)hd, hg, bulk);
+    };
+    if (G == 1) st = go(kv_wsum_partial_kernel<1>);
+    else if (G == 2) st = go(kv_wsum_partial_kernel<2>);
+    else if (G <= 4) st = go(kv_wsum_partial_kernel<4>);
+    else st = go(kv_wsum_partial_kernel<8>);
     if (st != QMM_OK) return st;
     const int64_t outs = Hq * hd;
-    kv_wsum_reduce_kernel<<<(unsigned)((outs * 32 + 255) / 256), 256, 0, cs>>>((const float*)scratch, out, G, (int)Hq,
-                                                                               (int)nc, (int)hd);
-    return launch_status();
+    return launch_pdl(kv_wsum_reduce_kernel, dim3((unsigned)((outs + 31) / 32)), 256, 0, cs, (const float*)scratch, out,
+                      (int)Hq, (int)nc, (int)hd);
 }
 
 }  // extern "C"

@@ -354,10 +354,9 @@ QMM_API qmm_status qmm_kv_scores(const void* q, const void* kc, float* scores, i
 
 /* out[h][i] = sum_p w[h][p] * dv_p * v_p[i] over positions 0..P-1 of the V cache
  * vc, w f32 [Hq][P] (the attention weights), out f32 [Hq][hd].  Summed in f32
- * in an order fixed by hd, Hq/Hkv and P alone (FMA chains over interleaved
- * positions of 128-position chunks, the chunk sums in the scratch, then a fixed
- * tree), so the result is the same on every GPU and within (P + 2) * 2^-24 *
- * sum_p |w dv v| of the exact sum.
+ * in an order fixed by P alone (an FMA chain over each 32-position chunk in
+ * order, the chunk sums in the scratch, then a fixed tree), so the result is the
+ * same on every GPU and within (P + 2) * 2^-24 * sum_p |w dv v| of the exact sum.
  * scratch: at least qmm_kv_wsum_scratch_bytes(Hq, P, hd) bytes. */
 QMM_API size_t qmm_kv_wsum_scratch_bytes(int64_t Hq, int64_t P, int64_t hd);
 QMM_API qmm_status qmm_kv_wsum(const float* w, const void* vc, float* out, void* scratch, size_t scratch_bytes,

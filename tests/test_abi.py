@@ -189,7 +189,7 @@ def test_kv_cache_calls_reject_bad_arguments(lib):
     assert s(A, A, A, 32, 8, 100, 120, f, None) == 2
     assert s(A, A + 1, A, 32, 8, 100, 128, f, None) == 4
     need = qmm.qmm_kv_wsum_scratch_bytes(32, 300, 128)
-    assert need == 32 * 3 * 128 * 4
+    assert need == 32 * 10 * 128 * 4                           # 32-position chunks
     w = lib.qmm_kv_wsum
     assert w(A, A, A, None, need, 32, 8, 300, 128, None) == 1
     assert w(A, A, A, A, need - 4, 32, 8, 300, 128, None) == 5
