@@ -159,12 +159,14 @@ __device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t g0, uint64
 // write y.  Few copies are in flight while the activation is read, so its
 // loads are not queued behind the whole weight stream.
 //
-// With FUSE the kernel takes the f32 activation row x instead of xq and
+// With FUSE (1) the kernel takes the f32 activation row x instead of xq and
 // quantizes it itself (every CTA, into shared memory, with the same per-block
 // arithmetic as the standalone quantizer, so the codes are the same bytes);
 // CTA 0 also stores the quantized row to xq_out when that is not null.  One
-// launch then does the whole quantize + multiply of a decode token.
-template <int WT, bool SU, bool FUSE, bool SPLIT>
+// launch then does the whole quantize + multiply of a decode token.  FUSE 2
+// RMSNorms the row first (set.gamma, set.eps); a mode of its own, so the plain
+// fused kernel carries none of it.
+template <int WT, bool SU, int FUSE, bool SPLIT>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_constant__ MatSet set,
                                                                   const uint8_t* __restrict__ xq,
                                                                   const float* __restrict__ x, uint8_t* xq_out,
@@ -228,9 +230,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
     {
         const int nthr = blockDim.x;
         float sn = 1.0f;  // the RMSNorm scale of the row, when the fused quantize norms it first
-        if constexpr (FUSE) {
-            if (set.gamma != nullptr) sn = rms_scale(x, K, reinterpret_cast<float*>(smem + set.norm_off), set.eps);
-        }
+        if constexpr (FUSE == 2) sn = rms_scale(x, K, reinterpret_cast<float*>(smem + set.norm_off), set.eps);
         if constexpr (F::ACT == QMM_Q8_0) {
             // one thread per activation block: read (or, with FUSE, quantize)
             // its 32 codes and put them in the layout the decoder reads
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                     float4 v[8];
 #pragma unroll
                     for (int i = 0; i < 8; i++) v[i] = x4[i];
-                    if (set.gamma != nullptr) {
+                    if constexpr (FUSE == 2) {
                         const float4* g4 = reinterpret_cast<const float4*>(set.gamma) + (size_t)b * 8;
 #pragma unroll
                         for (int i = 0; i < 8; i++) v[i] = norm4(v[i], sn, g4[i]);
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                     float4 v0 = x4[b0 * 64 + 2 * lane], v1 = x4[b0 * 64 + 2 * lane + 1];
                     float4 v2 = make_float4(0.f, 0.f, 0.f, 0.f), v3 = v2;
                     if (b1 < nd) v2 = x4[b1 * 64 + 2 * lane], v3 = x4[b1 * 64 + 2 * lane + 1];
-                    if (set.gamma != nullptr) {
+                    if constexpr (FUSE == 2) {
                         const float4* g4 = reinterpret_cast<const float4*>(set.gamma);
                         v0 = norm4(v0, sn, g4[b0 * 64 + 2 * lane]);
                         v1 = norm4(v1, sn, g4[b0 * 64 + 2 * lane + 1]);
@@ -555,7 +555,8 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     if (fuse && F::ACT == QMM_Q8_K) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);
     // a normed row: the K/8 partial sums of squares after the activation
     const uint32_t norm_rel = act;
-    if (norm) act += align_up(4u * (uint32_t)(K / 8), 128u);
+    // (sized for any block of up to kMaxWarps warps)
+    if (norm) act += align_up(4u * (uint32_t)rms_scratch_bound((int)K, kMaxWarps * 32), 128u);
     const uint64_t part_bytes = p->pieces > 1 ? align_up((uint32_t)(rows_max * p->pieces * 4), 128u) : 0;
     const uint32_t bar_max = align_up(8u * kMaxWarps * kMaxDepth, 128u);
     if ((uint64_t)dev.max_smem_optin < (uint64_t)bar_max + act + part_bytes + sb) return QMM_E_SHAPE;
@@ -603,7 +604,7 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     return QMM_OK;
 }
 
-template <int WT, bool SU, bool FUSE, bool SPLIT>
+template <int WT, bool SU, int FUSE, bool SPLIT>
 static qmm_status launch_matvec_k(const MatSet& set, const void* xq, const float* x, void* xq_out, int64_t K,
                                    const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
     static bool attr_set[64] = {false};
@@ -633,7 +634,7 @@ static qmm_status launch_matvec_k(const MatSet& set, const void* xq, const float
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
-template <int WT, bool SU, bool FUSE>
+template <int WT, bool SU, int FUSE>
 static qmm_status launch_matvec_su(const MatSet& set, const void* xq, const float* x, void* xq_out, int64_t K,
                                    const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
     if (p.pieces > 1) return launch_matvec_k<WT, SU, FUSE, true>(set, xq, x, xq_out, K, p, dev, stream, pdl);
@@ -665,16 +666,22 @@ static qmm_status launch_matvec(const void* const* W, const int64_t* N, float* c
         set.y[g] = y[g];
         set.N[g] = (int)N[g];
     }
-    if (fuse) {
+    if (fuse && gamma != nullptr) {  // RMSNorm, quantize and multiply
         if constexpr (has_su<WT>()) {
-            if (p.su) return launch_matvec_su<WT, true, true>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
+            if (p.su) return launch_matvec_su<WT, true, 2>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
         }
-        return launch_matvec_su<WT, false, true>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
+        return launch_matvec_su<WT, false, 2>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
+    }
+    if (fuse) {  // quantize and multiply
+        if constexpr (has_su<WT>()) {
+            if (p.su) return launch_matvec_su<WT, true, 1>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
+        }
+        return launch_matvec_su<WT, false, 1>(set, nullptr, x, (void*)xq, K, p, dev, stream, pdl);
     }
     if constexpr (has_su<WT>()) {
-        if (p.su) return launch_matvec_su<WT, true, false>(set, xq, nullptr, nullptr, K, p, dev, stream, pdl);
+        if (p.su) return launch_matvec_su<WT, true, 0>(set, xq, nullptr, nullptr, K, p, dev, stream, pdl);
     }
-    return launch_matvec_su<WT, false, false>(set, xq, nullptr, nullptr, K, p, dev, stream, pdl);
+    return launch_matvec_su<WT, false, 0>(set, xq, nullptr, nullptr, K, p, dev, stream, pdl);
 }
 
 // Public calls require 16-byte aligned bases; internal per-token calls pass rows

@@ -691,30 +691,64 @@ __device__ __forceinline__ void su_put_block(const uint32_t w[8], uint32_t dbits
 // rounded once; ss in one fixed order -- 8-value sequential partials, then a
 // stride-doubling tree (step 1, 2, 4, ...: p[i] += p[i + step] for i a multiple
 // of 2*step) -- so that the codes of h are the same on every run and in the
-// scalar implementation of the same steps.  Every thread of the CTA calls it;
-// p: K/8 floats of shared memory; x 16-byte aligned, K % 8 == 0.
+// scalar implementation of the same steps.
+//
+// The tree runs as: thread t owns the aligned run of m partials [t*m, t*m + m)
+// (m a power of two, m * threads >= K/8) and sums it pairwise; lanes then meet
+// by xor shuffles and warps through one shared-memory step.  Partials past K/8
+// are zeros, which leaves every sum unchanged (ss >= 0), so this is the same
+// tree.  Every thread of the CTA calls it; p: rms_scratch_floats(K, threads)
+// floats of shared memory; x 16-byte aligned, K % 8 == 0.
+__host__ __device__ inline int rms_run(int K, int nthr) {
+    int m = 1;
+    while (m * nthr < K / 8) m <<= 1;
+    return m;
+}
+__host__ __device__ inline int rms_scratch_floats(int K, int nthr) { return rms_run(K, nthr) * nthr + 33; }
+// a bound for any block of up to max_threads threads: m * threads < 2 * K/8 when m > 1
+__host__ __device__ inline int rms_scratch_bound(int K, int max_threads) {
+    return (2 * (K / 8) > max_threads ? 2 * (K / 8) : max_threads) + 33;
+}
+
+__device__ __forceinline__ float sq8(const float4* x4, int i) {
+    const float4 a = x4[2 * i], b = x4[2 * i + 1];
+    float s = __fmul_rn(a.x, a.x);
+    s = __fadd_rn(s, __fmul_rn(a.y, a.y));
+    s = __fadd_rn(s, __fmul_rn(a.z, a.z));
+    s = __fadd_rn(s, __fmul_rn(a.w, a.w));
+    s = __fadd_rn(s, __fmul_rn(b.x, b.x));
+    s = __fadd_rn(s, __fmul_rn(b.y, b.y));
+    s = __fadd_rn(s, __fmul_rn(b.z, b.z));
+    return __fadd_rn(s, __fmul_rn(b.w, b.w));
+}
+
 __device__ __forceinline__ float rms_scale(const float* x, int K, float* p, float eps) {
-    const int n8 = K / 8;
+    const int n8 = K / 8, nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m = rms_run(K, nthr);
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-        const float4 a = x4[2 * i], b = x4[2 * i + 1];
-        float s = __fmul_rn(a.x, a.x);
-        s = __fadd_rn(s, __fmul_rn(a.y, a.y));
-        s = __fadd_rn(s, __fmul_rn(a.z, a.z));
-        s = __fadd_rn(s, __fmul_rn(a.w, a.w));
-        s = __fadd_rn(s, __fmul_rn(b.x, b.x));
-        s = __fadd_rn(s, __fmul_rn(b.y, b.y));
-        s = __fadd_rn(s, __fmul_rn(b.z, b.z));
-        s = __fadd_rn(s, __fmul_rn(b.w, b.w));
-        p[i] = s;
+    float v;
+    if (m == 1) {
+        v = tid < n8 ? sq8(x4, tid) : 0.0f;
+    } else {
+        float* pt = p + tid * m;
+        for (int i = 0; i < m; i++) pt[i] = tid * m + i < n8 ? sq8(x4, tid * m + i) : 0.0f;
+        for (int step = 1; step < m; step <<= 1)
+            for (int i = 0; i < m; i += 2 * step) pt[i] = __fadd_rn(pt[i], pt[i + step]);
+        v = pt[0];
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+    float* wsum = p + m * nthr;
+    if (lane == 0) wsum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float u = lane < (nthr >> 5) ? wsum[lane] : 0.0f;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) u = __fadd_rn(u, __shfl_xor_sync(0xFFFFFFFFu, u, off));
+        if (lane == 0) wsum[32] = u;
     }
     __syncthreads();
-    for (int step = 1; step < n8; step <<= 1) {
-        for (int i = 2 * step * (int)threadIdx.x; i + step < n8; i += 2 * step * (int)blockDim.x)
-            p[i] = __fadd_rn(p[i], p[i + step]);
-        __syncthreads();
-    }
-    const float mean = __fdiv_rn(p[0], (float)K);
+    const float mean = __fdiv_rn(wsum[32], (float)K);
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 }
 

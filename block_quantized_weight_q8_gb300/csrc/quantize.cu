@@ -446,7 +446,11 @@ qmm_status rmsnorm_quantize_launch(int act, const float* x, const float* w, floa
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)M);
     cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = (size_t)(K / 8) * sizeof(float);
+    cfg.dynamicSmemBytes = (size_t)rms_scratch_floats((int)K, 256) * sizeof(float);
+    if (cfg.dynamicSmemBytes > 48 * 1024 &&
+        cudaFuncSetAttribute(rmsnorm_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)cfg.dynamicSmemBytes) != cudaSuccess)
+        return QMM_E_CUDA;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
