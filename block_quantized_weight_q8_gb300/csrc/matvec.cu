@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                 }
                 xq = xs;
             }
-            for (int i = tid; i < nd * 73; i += nthr) unpack_q8_K_word(xq, nd, i, aq, ad, as);
+            unpack_q8_K_row_by(xq, nd, aq, ad, as, tid, nthr);
         }
         __syncthreads();
     }

@@ -528,10 +528,9 @@ __device__ __forceinline__ void unpack_q8_0_block(const uint8_t* __restrict__ ro
 
 // item i of ns * 73: word k = i % 73 of super-block u = i / 73 (d, 64 code
 // words, 8 bsum words)
-__device__ __forceinline__ void unpack_q8_K_word(const uint8_t* __restrict__ row, int ns, int i, uint8_t* q, float* d,
-                                                 int* s) {
-    const int u = i / 73, k = i % 73;
-    const uint32_t wv = *reinterpret_cast<const uint32_t*>(row + 292 * u + 4 * k);
+// word wv = word k (0..72) of Q8_K block u into the view: the f32 scale, a
+// quarter chunk of codes, or a bsum pair
+__device__ __forceinline__ void put_q8_K_word(uint32_t wv, int u, int k, int ns, uint8_t* q, float* d, int* s) {
     if (k == 0) {
         d[u] = __uint_as_float(wv);
     } else if (k <= 64) {
@@ -539,6 +538,34 @@ __device__ __forceinline__ void unpack_q8_K_word(const uint8_t* __restrict__ row
         *reinterpret_cast<uint32_t*>(q + ((uint32_t)c * ns + u) * 16 + 4 * wi) = wv;
     } else {
         reinterpret_cast<uint32_t*>(s)[(k - 65) * ns + u] = wv;  // the bsum pair of groups 2(k-65), +1
+    }
+}
+
+__device__ __forceinline__ void unpack_q8_K_word(const uint8_t* __restrict__ row, int ns, int i, uint8_t* q, float* d,
+                                                 int* s) {
+    const int u = i / 73, k = i % 73;
+    put_q8_K_word(*reinterpret_cast<const uint32_t*>(row + 292 * u + 4 * k), u, k, ns, q, d, s);
+}
+
+// The whole Q8_K row by the threads tid, tid + nthr, ...: each thread issues up
+// to four of its loads before it stores any, so the row costs one memory round
+// trip rather than one per word a thread handles (eight at a time raised the
+// register pressure of the kernels that call it and was slower).
+__device__ __forceinline__ void unpack_q8_K_row_by(const uint8_t* __restrict__ row, int ns, uint8_t* q, float* d,
+                                                   int* s, int tid, int nthr) {
+    const int total = ns * 73;
+    for (int i0 = tid; i0 < total; i0 += 4 * nthr) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int i = i0 + k * nthr;
+            wv[k] = i < total ? *reinterpret_cast<const uint32_t*>(row + 292 * (i / 73) + 4 * (i % 73)) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int i = i0 + k * nthr;
+            if (i < total) put_q8_K_word(wv[k], i / 73, i % 73, ns, q, d, s);
+        }
     }
 }
 
@@ -550,7 +577,7 @@ __device__ __forceinline__ void unpack_q8_0_row(const uint8_t* __restrict__ row,
 __device__ __forceinline__ void unpack_q8_K_row(const uint8_t* __restrict__ row, int K, uint8_t* q, float* d,
                                                 int* s) {
     const int ns = K / 256;
-    for (int i = threadIdx.x; i < ns * 73; i += blockDim.x) unpack_q8_K_word(row, ns, i, q, d, s);
+    unpack_q8_K_row_by(row, ns, q, d, s, threadIdx.x, blockDim.x);
 }
 
 // ---------------------------------------------------------------- activation quantizers
