@@ -195,8 +195,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
     const int qbytes = SU ? SuFmt<has_su<WT>() ? WT : QMM_Q8_0>::A * nsu : K;
     float* ad = reinterpret_cast<float*>(aq + qbytes);
     int* as = reinterpret_cast<int*>(ad + nd);
-    uint8_t* xs = reinterpret_cast<uint8_t*>(as + (SU ? nd : (F::ACT == QMM_Q8_0 ? nd : K / 16)));
-    xs = reinterpret_cast<uint8_t*>(((uintptr_t)xs + 15u) & ~(uintptr_t)15u);  // FUSE, Q8_K: the quantized row
     uint8_t* slots = smem + act_bytes + (size_t)warp * depth * slot_bytes;
 
     const int units = K / F::BV;
@@ -288,18 +286,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                             v3 = norm4(v3, sn, g4[b1 * 64 + 2 * lane + 1]);
                         }
                     }
-                    quant_q8_K_lane(v0, v1, lane, xs + b0 * 292);
-                    if (b1 < nd) quant_q8_K_lane(v2, v3, lane, xs + b1 * 292);
+                    // straight into the decoder's layout; CTA 0 also stores the row
+                    uint8_t* ob = blockIdx.x == 0 ? xq_out : nullptr;
+                    quant_q8_K_lane_put(v0, v1, lane, b0, nd, aq, ad, as, ob ? ob + b0 * 292 : nullptr);
+                    if (b1 < nd) quant_q8_K_lane_put(v2, v3, lane, b1, nd, aq, ad, as, ob ? ob + b1 * 292 : nullptr);
                 }
-                __syncthreads();
-                if (blockIdx.x == 0 && xq_out != nullptr) {
-                    const int halves = nd * 292 / 2;
-                    for (int i = tid; i < halves; i += nthr)
-                        reinterpret_cast<unsigned short*>(xq_out)[i] = reinterpret_cast<const unsigned short*>(xs)[i];
-                }
-                xq = xs;
+            } else {
+                unpack_q8_K_row_by(xq, nd, aq, ad, as, tid, nthr);
             }
-            unpack_q8_K_row_by(xq, nd, aq, ad, as, tid, nthr);
         }
         __syncthreads();
     }
@@ -551,8 +545,6 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     p->grid = acc;
 
     uint32_t act = matvec_act_bytes(WT, F::ACT, (int)K, p->su);
-    // a fused Q8_K row is quantized into shared memory first (Q8_0 goes straight to its layout)
-    if (fuse && F::ACT == QMM_Q8_K) act += align_up((uint32_t)row_bytes_of(F::ACT, K) + 16u, 128u);
     // a normed row: the K/8 partial sums of squares after the activation
     const uint32_t norm_rel = act;
     // (sized for any block of up to kMaxWarps warps)

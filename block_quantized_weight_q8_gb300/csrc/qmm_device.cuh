@@ -622,7 +622,10 @@ __device__ __forceinline__ void quant_q8_0_part(float4 v, bool active, int part,
 // saturated codes of group g.  One warp per super-block, eight values per lane
 // (v0, v1 = values 8*lane .. 8*lane+7): lanes 2g and 2g+1 hold group g.  `ob`
 // is the super-block's 292 output bytes (4-byte aligned).
-__device__ __forceinline__ void quant_q8_K_lane(float4 v0, float4 v1, int lane, uint8_t* ob) {
+// The arithmetic of one lane: its 8 codes as two words, the block's f32 scale,
+// and (lanes 4k) the bsum pair of groups 2k, 2k + 1.
+__device__ __forceinline__ void quant_q8_K_core(float4 v0, float4 v1, float* d_out, uint32_t* w0_out,
+                                                uint32_t* w1_out, uint32_t* pair_out) {
     float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
                        fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
 #pragma unroll
@@ -641,12 +644,40 @@ __device__ __forceinline__ void quant_q8_K_lane(float4 v0, float4 v1, int lane, 
     }
     const int bsum = sum + __shfl_xor_sync(0xffffffffu, sum, 1);   // group lane/2
     const int bsum_next = __shfl_down_sync(0xffffffffu, bsum, 2);  // group lane/2 + 1
+    *d_out = d;
+    *w0_out = w0;
+    *w1_out = w1;
+    *pair_out = ((uint32_t)bsum & 0xFFFFu) | ((uint32_t)(bsum_next & 0xFFFF) << 16);
+}
+
+// the 292-byte Q8_K block at ob
+__device__ __forceinline__ void store_q8_K_block(int lane, float d, uint32_t w0, uint32_t w1, uint32_t pair,
+                                                 uint8_t* ob) {
     if (lane == 0) *reinterpret_cast<float*>(ob) = d;
     *reinterpret_cast<uint32_t*>(ob + 4 + 8 * lane) = w0;
     *reinterpret_cast<uint32_t*>(ob + 8 + 8 * lane) = w1;
-    if ((lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(ob + 260 + lane) =
-            ((uint32_t)bsum & 0xFFFFu) | ((uint32_t)(bsum_next & 0xFFFF) << 16);
+    if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(ob + 260 + lane) = pair;
+}
+
+__device__ __forceinline__ void quant_q8_K_lane(float4 v0, float4 v1, int lane, uint8_t* ob) {
+    float d;
+    uint32_t w0, w1, pair;
+    quant_q8_K_core(v0, v1, &d, &w0, &w1, &pair);
+    store_q8_K_block(lane, d, w0, w1, pair, ob);
+}
+
+// The same block straight into the decoder's view (block u of ns): the codes of
+// lane l (8l .. 8l + 7) are half of chunk l / 2; also the 292-byte block at ob
+// when ob is not null.
+__device__ __forceinline__ void quant_q8_K_lane_put(float4 v0, float4 v1, int lane, int u, int ns, uint8_t* q,
+                                                    float* dv, int* s, uint8_t* ob) {
+    float d;
+    uint32_t w0, w1, pair;
+    quant_q8_K_core(v0, v1, &d, &w0, &w1, &pair);
+    if (lane == 0) dv[u] = d;
+    *reinterpret_cast<uint2*>(q + ((uint32_t)(lane >> 1) * ns + u) * 16 + (lane & 1) * 8) = make_uint2(w0, w1);
+    if ((lane & 3) == 0) reinterpret_cast<uint32_t*>(s)[(lane >> 2) * ns + u] = pair;
+    if (ob != nullptr) store_q8_K_block(lane, d, w0, w1, pair, ob);
 }
 
 // ---------------------------------------------------------------- super-units (Q8_0, Q4_0 weights)
