@@ -159,6 +159,57 @@ __device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t g0, uint64
 // write y.  Few copies are in flight while the activation is read, so its
 // loads are not queued behind the whole weight stream.
 //
+// A Q8_0 activation block (f16 scale bits, 8 code words) into the layout the
+// decoder of WT reads.
+template <int WT, bool SU>
+__device__ __forceinline__ void put_act_block(const uint32_t w[8], uint32_t dbits, int b, int nb, int nsu, uint8_t* aq,
+                                              float* ad, int* as) {
+    if constexpr (SU && (WT == QMM_Q8_0 || WT == QMM_Q4_0))
+        su_put_block<WT == QMM_Q4_0>(w, dbits, b, nsu, aq, ad, as);
+    else if constexpr (SU)
+        su_put_halves(w, dbits, b, nsu, aq, ad, as);
+    else
+        act_put_q8_0_block(w, dbits, b, nb, aq, ad, as);
+}
+
+// the 34-byte block b of the quantized row (16-bit stores: rows of a larger
+// buffer are only 2-byte aligned)
+__device__ __forceinline__ void store_q8_0_block(uint8_t* xq_out, int b, uint32_t dbits, const uint32_t w[8]) {
+    unsigned short* o = reinterpret_cast<unsigned short*>(xq_out + (size_t)b * 34);
+    o[0] = (unsigned short)dbits;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        o[1 + 2 * i] = (unsigned short)(w[i] & 0xFFFFu);
+        o[2 + 2 * i] = (unsigned short)(w[i] >> 16);
+    }
+}
+
+// The fused quantize of the whole row in one pass, LPB lanes per block (the
+// caller has checked K/32 * LPB <= threads).  FUSE 2 norms each value first.
+template <int WT, bool SU, int FUSE, int LPB>
+__device__ __forceinline__ void fused_q8_0_lanes(const float* x, const float* gamma, float sn, uint8_t* xq_out, int K,
+                                                 int nsu, uint8_t* aq, float* ad, int* as) {
+    constexpr int NV = 8 / LPB;
+    const int nb = K / 32, tid = threadIdx.x;
+    const int b = tid / LPB, part = tid - b * LPB;
+    const bool active = b < nb;
+    const size_t off = (size_t)(active ? b : 0) * 8 + (size_t)part * NV;
+    float4 v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) v[i] = active ? reinterpret_cast<const float4*>(x)[off + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (FUSE == 2) {
+#pragma unroll
+        for (int i = 0; i < NV; i++)
+            if (active) v[i] = norm4(v[i], sn, reinterpret_cast<const float4*>(gamma)[off + i]);
+    }
+    uint32_t w[8], dbits;
+    quant_q8_0_block_lanes<LPB>(v, part, &dbits, w);
+    if (active && part == 0) {
+        if (blockIdx.x == 0 && xq_out != nullptr) store_q8_0_block(xq_out, b, dbits, w);
+        put_act_block<WT, SU>(w, dbits, b, nb, nsu, aq, ad, as);
+    }
+}
+
 // With FUSE (1) the kernel takes the f32 activation row x instead of xq and
 // quantizes it itself (every CTA, into shared memory, with the same per-block
 // arithmetic as the standalone quantizer, so the codes are the same bytes);
@@ -231,9 +282,16 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
         if constexpr (FUSE == 2) sn = rms_scale(x, K, reinterpret_cast<float*>(smem + set.norm_off), set.eps);
         if constexpr (F::ACT == QMM_Q8_0) {
             // one thread per activation block: read (or, with FUSE, quantize)
-            // its 32 codes and put them in the layout the decoder reads
+            // its 32 codes and put them in the layout the decoder reads; a
+            // fused quantize that fits in one pass takes 4 or 2 lanes per block
             const int nb = K / 32;
-            for (int b = tid; b < nb; b += nthr) {
+            int lpb = 1;
+            if constexpr (FUSE) lpb = nb * 4 <= nthr ? 4 : (nb * 2 <= nthr ? 2 : 1);
+            if constexpr (FUSE) {
+                if (lpb == 4) fused_q8_0_lanes<WT, SU, FUSE, 4>(x, set.gamma, sn, xq_out, K, nsu, aq, ad, as);
+                if (lpb == 2) fused_q8_0_lanes<WT, SU, FUSE, 2>(x, set.gamma, sn, xq_out, K, nsu, aq, ad, as);
+            }
+            for (int b = tid; lpb == 1 && b < nb; b += nthr) {
                 uint32_t w[8], dbits;
                 if constexpr (FUSE) {
                     const float4* x4 = reinterpret_cast<const float4*>(x) + (size_t)b * 8;
@@ -246,27 +304,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                         for (int i = 0; i < 8; i++) v[i] = norm4(v[i], sn, g4[i]);
                     }
                     quant_q8_0_block(v, &dbits, w);
-                    if (blockIdx.x == 0 && xq_out != nullptr) {
-                        unsigned short* o = reinterpret_cast<unsigned short*>(xq_out + (size_t)b * 34);
-                        o[0] = (unsigned short)dbits;
-#pragma unroll
-                        for (int i = 0; i < 8; i++) {
-                            o[1 + 2 * i] = (unsigned short)(w[i] & 0xFFFFu);
-                            o[2 + 2 * i] = (unsigned short)(w[i] >> 16);
-                        }
-                    }
+                    if (blockIdx.x == 0 && xq_out != nullptr) store_q8_0_block(xq_out, b, dbits, w);
                 } else {
                     const unsigned short* p = reinterpret_cast<const unsigned short*>(xq + (size_t)b * 34);
                     dbits = p[0];
 #pragma unroll
                     for (int i = 0; i < 8; i++) w[i] = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
                 }
-                if constexpr (SU && (WT == QMM_Q8_0 || WT == QMM_Q4_0))
-                    su_put_block<WT == QMM_Q4_0>(w, dbits, b, nsu, aq, ad, as);
-                else if constexpr (SU)
-                    su_put_halves(w, dbits, b, nsu, aq, ad, as);
-                else
-                    act_put_q8_0_block(w, dbits, b, nb, aq, ad, as);
+                put_act_block<WT, SU>(w, dbits, b, nb, nsu, aq, ad, as);
             }
         } else {
             if constexpr (FUSE) {

@@ -934,6 +934,42 @@ __device__ __forceinline__ void quant_q8_0_block(const float4 v[8], uint32_t* db
     }
 }
 
+// One Q8_0 block quantized by LPB consecutive lanes of a warp (8 / LPB float4
+// each): the same bytes as quant_q8_0_block (the maximum is exact in any order,
+// NaN rules included), with the 8 code words gathered in the group's first lane
+// (part 0).  Every lane of the warp calls it.
+template <int LPB>
+__device__ __forceinline__ void quant_q8_0_block_lanes(const float4* v, int part, uint32_t* dbits, uint32_t w[8]) {
+    constexpr int NV = 8 / LPB;
+    float amax = fmaxf(fmaxf(fabsf(v[0].x), fabsf(v[0].y)), fmaxf(fabsf(v[0].z), fabsf(v[0].w)));
+#pragma unroll
+    for (int i = 1; i < NV; i++)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+#pragma unroll
+    for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = amax != 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    *dbits = f2h_bits(d);
+    uint32_t mine[NV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+        const int q0 = clampi(__float2int_rn(__fmul_rn(v[i].x, id)), -128, 127);
+        const int q1 = clampi(__float2int_rn(__fmul_rn(v[i].y, id)), -128, 127);
+        const int q2 = clampi(__float2int_rn(__fmul_rn(v[i].z, id)), -128, 127);
+        const int q3 = clampi(__float2int_rn(__fmul_rn(v[i].w, id)), -128, 127);
+        mine[i] = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) | ((uint32_t)(q2 & 0xFF) << 16) |
+                  ((uint32_t)(q3 & 0xFF) << 24);
+        w[i] = mine[i];
+    }
+#pragma unroll
+    for (int src = 1; src < LPB; src++)
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, mine[i], src);
+            if (part == 0) w[src * NV + i] = t;
+        }
+}
+
 // The f32 fold of one super-unit: for each of its 8 blocks, isum * d_w * d_x
 // added in block order ([minfer] "10 . CPU matmul: quantized weights x Q8_0
 // activations" s3.2, the Q8_0 kernel).  w: the super-unit in shared memory
