@@ -570,7 +570,7 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
     # the K-quant prefill at the decoder layer's shapes (M = 512): W_gate/W_up (Q4_K), W_down (Q6_K),
     # and the Q2_K matrix
     kq = {}
-    for wtype, Nk, Kk in (("q4_K", 12288, 4096), ("q6_K", 4096, 12288), ("q2_K", 12288, 4096)):
+    for wtype, Nk, Kk in (("q4_K", 12288, 4096), ("q6_K", 4096, 12288), ("q2_K", 12288, 4096), ("q5_K", 12288, 4096)):
         M = 512
         Wk = quantized_weights(wtype, Nk, Kk, cfg["seed"])
         xk = to_dev(workloads.activations_f32(M, Kk, cfg["seed"] + 3))

@@ -68,6 +68,7 @@ SIGNATURES = {
     "qmm_kv_wsum": ("pppps" + "iiiiq", ctypes.c_int),
     "qmm_matmul_q4_K": ("pppiiiq", ctypes.c_int),
     "qmm_matmul_q6_K": ("pppiiiq", ctypes.c_int),
+    "qmm_matmul_q5_K": ("pppiiiq", ctypes.c_int),
     "qmm_matmul_q2_K": ("pppiiiq", ctypes.c_int),
     "qmm_linear_noalloc": ("tpppiiiq", ctypes.c_int),
     "qmm_linear_group": ("ttppppspiiq", ctypes.c_int),

@@ -65,6 +65,7 @@ template <int WT> struct Fmt;
 template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, RAWW = 144, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
 template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, RAWW = 96, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
 template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, RAWW = 224, SPLIT = 1, OP_SLOTS = 3, GROUP = 1; };
+template <> struct Fmt<QMM_Q5_K> { static constexpr int BB = 176, RAWW = 176, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
 
 template <int WT>
 struct Layout {
@@ -88,6 +89,7 @@ struct Layout {
 };
 static_assert(Layout<QMM_Q6_K>::SMEM <= 232448, "Q6_K layout exceeds shared memory");
 static_assert(Layout<QMM_Q4_K>::SMEM <= 232448, "Q4_K layout exceeds shared memory");
+static_assert(Layout<QMM_Q5_K>::SMEM <= 232448, "Q5_K layout exceeds shared memory");
 
 template <int WT>
 struct Bars {
@@ -229,6 +231,27 @@ __device__ __forceinline__ void st_q4_K(const Hdr& h, int j, uint32_t* q, uint8_
     put_block(opA, r, q, s, s);
 }
 
+// Q5_K: the Q4_K header (d, dmin, packed scales and mins) @0, qh[32]@16,
+// qs[128]@48 (GGUF layout, a reading).  Sub-block j takes the low (j even) or
+// high (j odd) nibbles of qs[32(j/2) .. +32] and bit j of each qh[l] as bit 4:
+// codes 0..31, so sc*q <= 63*31 is still an exact fp16 integer.
+template <int OFF>
+__device__ __forceinline__ void ld_q5_K(const Raw& raw, int j, uint32_t* q) {
+    switch (j >> 1) {
+    case 0: words<OFF, 48, 8>(raw, q); break;
+    case 1: words<OFF, 80, 8>(raw, q); break;
+    case 2: words<OFF, 112, 8>(raw, q); break;
+    default: words<OFF, 144, 8>(raw, q); break;
+    }
+}
+__device__ __forceinline__ void st_q5_K(const Hdr& h, int j, uint32_t* q, const uint32_t* qh, uint8_t* opA, int r) {
+    const int sh = (j & 1) * 4;
+#pragma unroll
+    for (int i = 0; i < 8; i++) q[i] = ((q[i] >> sh) & 0x0F0F0F0Fu) | (((qh[i] >> j) & 0x01010101u) << 4);
+    const uint32_t s = hpair(sc_q4_K(h, j));
+    put_block(opA, r, q, s, s);
+}
+
 // Q2_K: scales[16]@0 (sc low nibble, m high), qs[64]@16, d@80, dmin@82;
 // value 128h + 32s + l is (qs[32h + l] >> 2s) & 3 (GGUF order, a reading).
 // w0..w3 = the 16 scale bytes.
@@ -300,7 +323,7 @@ template <int WT>
 __device__ __forceinline__ void min_row(const Hdr& h, uint32_t* hv) {
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-        if constexpr (WT == QMM_Q4_K) hv[i] = h2_of(f_q4_K(h, 2 * i), f_q4_K(h, 2 * i + 1));
+        if constexpr (WT == QMM_Q4_K || WT == QMM_Q5_K) hv[i] = h2_of(f_q4_K(h, 2 * i), f_q4_K(h, 2 * i + 1));
         else if constexpr (WT == QMM_Q2_K) hv[i] = h2_of(f_q2_K(h, 2 * i), f_q2_K(h, 2 * i + 1));
         else hv[i] = h2_of(32 * sc_q6_K(h, 2 * i), 32 * sc_q6_K(h, 2 * i + 1));
     }
@@ -460,7 +483,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             Hdr h;
             uint32_t xd = 0, bs[8];
             if (is_w) {
-                if constexpr (WT == QMM_Q4_K) {
+                if constexpr (WT == QMM_Q4_K || WT == QMM_Q5_K) {
                     hdr_q4_K<0>(raw, h);
                 } else if constexpr (WT == QMM_Q2_K) {
                     switch (off) {
@@ -525,6 +548,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int u = 0; u < G; u++)
                             st_q6_K(h, jg + u, ql[u], qh[u], smem + L::OFF_OPA + osl[u] * OP_BYTES,
                                     smem + L::OFF_OPH + osl[u] * OP_BYTES, r);
+                    } else if constexpr (WT == QMM_Q5_K) {
+                        uint32_t q[G][8], qh[8];
+                        words<0, 16, 8>(raw, qh);  // the fifth bits of every sub-block
+#pragma unroll
+                        for (int u = 0; u < G; u++) ld_q5_K<0>(raw, jg + u, q[u]);
+#pragma unroll
+                        for (int u = 0; u < G; u++) st_q5_K(h, jg + u, q[u], qh, smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
                     } else {
                         uint32_t q[G][8];
 #pragma unroll
@@ -712,12 +742,13 @@ qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int
     case QMM_Q4_K: return launch_kq<QMM_Q4_K>(W, xq, Y, M, N, K, stream, pdl);
     case QMM_Q2_K: return launch_kq<QMM_Q2_K>(W, xq, Y, M, N, K, stream, pdl);
     case QMM_Q6_K: return launch_kq<QMM_Q6_K>(W, xq, Y, M, N, K, stream, pdl);
+    case QMM_Q5_K: return launch_kq<QMM_Q5_K>(W, xq, Y, M, N, K, stream, pdl);
     default: return QMM_E_TYPE;
     }
 }
 
 bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K) {
-    return (wt == QMM_Q4_K || wt == QMM_Q2_K || wt == QMM_Q6_K) && kq_tensor_core_shape(M, K);
+    return (wt == QMM_Q4_K || wt == QMM_Q2_K || wt == QMM_Q6_K || wt == QMM_Q5_K) && kq_tensor_core_shape(M, K);
 }
 
 static qmm_status matmul_kq_checked(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
@@ -746,6 +777,10 @@ qmm_status qmm_matmul_q2_K(const void* W, const void* xq, float* Y, int64_t M, i
 qmm_status qmm_matmul_q6_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
     return matmul_kq_checked(QMM_Q6_K, W, xq, Y, M, N, K, stream);
+}
+qmm_status qmm_matmul_q5_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_kq_checked(QMM_Q5_K, W, xq, Y, M, N, K, stream);
 }
 
 unsigned qmm_internal_matmul_kq_error(int clear) {

@@ -196,7 +196,7 @@ QMM_API qmm_status qmm_matvec_q5_K(const void* W, const void* xq, float* y, int6
  * row it needs, with the same arithmetic as qmm_quantize_q8_0/q8_K, and one CTA
  * stores it to the scratch), so a token is one launch; a row too large for that
  * kernel's shared memory is quantized by the separate quantizer first.  Q4_0 with
- * M >= 8 and K % 256 == 0, and Q4_K / Q6_K / Q2_K with M >= 8 and K % 2048 == 0,
+ * M >= 8 and K % 256 == 0, and Q4_K / Q6_K / Q2_K / Q5_K with M >= 8 and K % 2048 == 0,
  * quantize all rows, then run the prefill matmul.  The other types multiply
  * token by token at every M. */
 QMM_API qmm_status qmm_linear_q4_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
@@ -273,7 +273,7 @@ QMM_API qmm_status qmm_linear_group(int wtype, int G, const void* const* W, cons
  * qmm_linear_norm: qmm_linear_group on the normed rows (G = 1 for one matrix),
  * the quantized normed rows left in the scratch.  A decode token is one launch
  * (every CTA norms and quantizes the row itself); a prefill that takes the
- * tensor-core matmul (Q4_0, or Q4_K/Q6_K/Q2_K with M >= 8 and K % 2048 == 0)
+ * tensor-core matmul (Q4_0, or Q4_K/Q6_K/Q2_K/Q5_K with M >= 8 and K % 2048 == 0)
  * norms and quantizes all rows first.  Errors as for qmm_linear_group, plus
  * QMM_E_NULL for w. */
 QMM_API qmm_status qmm_rmsnorm_quantize(int act, const float* x, const float* w, float eps, void* xq, int64_t M,
@@ -294,9 +294,10 @@ QMM_API qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int6
 /* The same for the K-quants against Q8_K rows ([minfer] s3.2, the K-quant dot
  * walked; [ggml] s1.2).  Per 256-value super-block the integer value term
  * (sum of sc * code dots, Q6_K in two exact parts) and the integer min term
- * (f_g * bsum_g: Q4_K m_{g/2}, Q2_K m_g, Q6_K 32 sc_g) run on the tensor cores
- * with integer-valued operands; each super-block then folds into fp32:
- * y -= (dmin_w*d_x) * min; y += (d_w*d_x) * value (Q4_K, Q2_K), or
+ * (f_g * bsum_g: Q4_K and Q5_K m_{g/2}, Q2_K m_g, Q6_K 32 sc_g) run on the
+ * tensor cores with integer-valued operands (Q5_K: sc * q <= 63 * 31, exact in
+ * fp16); each super-block then folds into fp32:
+ * y -= (dmin_w*d_x) * min; y += (d_w*d_x) * value (Q4_K, Q5_K, Q2_K), or
  * y += (d_w*d_x) * (value - min) (Q6_K).  Results agree with the scalar order
  * within 1e-5 of the row's L2 norm.  K a multiple of 2048 and M >= 8 take this
  * path; other shapes run one matvec per token (same results as qmm_matvec).
@@ -306,6 +307,8 @@ QMM_API qmm_status qmm_matmul_q4_K(const void* W, const void* xq, float* Y, int6
 QMM_API qmm_status qmm_matmul_q6_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream);
 QMM_API qmm_status qmm_matmul_q2_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream);
+QMM_API qmm_status qmm_matmul_q5_K(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream);
 
 /* ---- embedding lookup ----------------------------------------------------- */

@@ -15,7 +15,7 @@ import block_quantized_weight_q8_gb300 as qmm  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
-KQ = ["q4_K", "q6_K", "q2_K"]
+KQ = ["q4_K", "q6_K", "q2_K", "q5_K"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -78,7 +78,8 @@ def test_linear_kq_many_tokens(wtype):
     assert_rows_close(host(Y), ref)
 
 
-@pytest.mark.parametrize("wtype,N,K", [("q4_K", 4096, 4096), ("q6_K", 4096, 12288), ("q2_K", 12288, 4096)])
+@pytest.mark.parametrize("wtype,N,K", [("q4_K", 4096, 4096), ("q6_K", 4096, 12288), ("q2_K", 12288, 4096),
+                                       ("q5_K", 12288, 4096)])
 def test_full_size_kq_prefill_sampled(wtype, N, K):
     """M = 512 at the layer's shapes; rows and tokens sampled for the oracle."""
     M = 512
