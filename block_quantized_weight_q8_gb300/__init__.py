@@ -59,6 +59,7 @@ SIGNATURES = {
     "qmm_linear_q5_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
     "qmm_get_rows": ("tpppiiiq", ctypes.c_int),
+    "qmm_linear_host": ("tppppsppiiiq", ctypes.c_int),
     "qmm_rmsnorm_quantize": ("tppfpiiq", ctypes.c_int),
     "qmm_linear_norm": ("ttppppfpspiiq", ctypes.c_int),
     "qmm_kv_row_bytes": ("i", ctypes.c_size_t),
@@ -229,6 +230,13 @@ qmm_linear_q5_K = _lin("qmm_linear_q5_K")
 def linear(wtype, W, x, scratch, scratch_bytes, y, M, N, K, stream=None):
     _call("qmm_linear_" + wtype, ptr(W), ptr(x), ptr(scratch), int(scratch_bytes), ptr(y), int(M), int(N), int(K),
           stream_handle(stream))
+
+
+def qmm_linear_host(wtype, W, x_host, x_dev, scratch, scratch_bytes, y_dev, y_host, M, N, K, stream=None):
+    """qmm_linear_<wtype> with host buffers: x_host (pinned) -> x_dev, the multiply, y_dev -> y_host, queued on
+    the stream (synchronize it before reading y_host)."""
+    _call("qmm_linear_host", _type(wtype), ptr(W), ptr(x_host), ptr(x_dev), ptr(scratch), int(scratch_bytes), ptr(y_dev),
+          ptr(y_host), int(M), int(N), int(K), stream_handle(stream))
 
 
 def qmm_linear_noalloc(wtype, W, x, y, M, N, K, stream=None):

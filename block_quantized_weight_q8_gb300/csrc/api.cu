@@ -169,6 +169,28 @@ qmm_status qmm_linear_group(int wtype, int G, const void* const* W, const int64_
 }
 unsigned qmm_internal_matmul_error(int clear);
 
+// qmm_linear_<wtype> with host buffers: x from the caller's (pinned) host
+// memory in, y back out, both copies and the multiply queued on one stream.
+qmm_status qmm_linear_host(int wtype, const void* W, const float* x_host, float* x_dev, void* xq_scratch,
+                           size_t scratch_bytes, float* y_dev, float* y_host, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    if (!x_host || !y_host) return QMM_E_NULL;
+    qmm_status st = check_shape(wtype, M, N, K);
+    if (st != QMM_OK) return st;
+    if (act_type_of(wtype) < 0) return QMM_E_TYPE;
+    if (!x_dev || !y_dev) return QMM_E_NULL;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(x_dev, x_host, (size_t)M * (size_t)K * sizeof(float), cudaMemcpyHostToDevice, cs) !=
+        cudaSuccess)
+        return QMM_E_CUDA;
+    st = linear(wtype, W, x_dev, xq_scratch, scratch_bytes, y_dev, M, N, K, cs);
+    if (st != QMM_OK) return st;
+    if (cudaMemcpyAsync(y_host, y_dev, (size_t)M * (size_t)N * sizeof(float), cudaMemcpyDeviceToHost, cs) !=
+        cudaSuccess)
+        return QMM_E_CUDA;
+    return QMM_OK;
+}
+
 qmm_status qmm_linear_norm(int wtype, int G, const void* const* W, const int64_t* N, const float* x, const float* w,
                            float eps, void* xq_scratch, size_t scratch_bytes, float* const* y, int64_t M, int64_t K,
                            qmm_stream_t stream) {

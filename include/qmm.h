@@ -218,6 +218,18 @@ QMM_API qmm_status qmm_linear_q5_1(const void* W, const float* x, void* xq_scrat
 QMM_API qmm_status qmm_linear_q5_K(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
                            int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
 
+/* ---- quantize + multiply with host buffers -------------------------------- */
+/* qmm_linear_<wtype> for a caller whose input and output live in host memory:
+ * copies x_host (f32 [M][K]) to x_dev, runs qmm_linear_<wtype> (x_dev, the
+ * scratch and y_dev as there), and copies y_dev (f32 [M][N]) back to y_host, all
+ * queued on the stream in that order (cudaMemcpyAsync; asynchronous only when
+ * the host buffers are pinned).  The caller synchronizes the stream before it
+ * reads y_host.  Errors as for qmm_linear_<wtype>; QMM_E_NULL for a null host
+ * buffer; QMM_E_CUDA when a copy cannot be queued. */
+QMM_API qmm_status qmm_linear_host(int wtype, const void* W, const float* x_host, float* x_dev, void* xq_scratch,
+                                   size_t scratch_bytes, float* y_dev, float* y_host, int64_t M, int64_t N, int64_t K,
+                                   qmm_stream_t stream);
+
 /* ---- quantize + multiply without a caller workspace ---------------------- */
 /* No counterpart on the pages: an addition for callers that cannot give the
  * library a device buffer (a plugin inside an application that owns all device

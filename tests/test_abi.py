@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
                  "qmm_matmul_q6_K", "qmm_matmul_q2_K",
                  "qmm_linear_q4_0", "qmm_blocksums", "qmm_status_str", "qmm_row_bytes", "qmm_matvec_q4_1",
                  "qmm_matvec_q5_0", "qmm_matvec_q5_1", "qmm_matvec_q5_K", "qmm_get_rows", "qmm_kv_quantize",
-                 "qmm_kv_scores", "qmm_kv_wsum", "qmm_rmsnorm_quantize", "qmm_linear_norm"):
+                 "qmm_kv_scores", "qmm_kv_wsum", "qmm_rmsnorm_quantize", "qmm_linear_norm", "qmm_linear_host"):
         assert want in names
     assert set(names) == set(qmm.SIGNATURES), set(names) ^ set(qmm.SIGNATURES)
 
@@ -150,6 +150,15 @@ def test_get_rows_rejects_bad_arguments(lib):
     assert f(qmm.QMM_Q4_K, A, A, A, 1, 4, 128, None) == 2
     assert f(qmm.QMM_Q4_0, A, A + 2, A, 1, 4, 256, None) == 4  # ids not 4-byte aligned
     assert f(qmm.QMM_Q4_0, A, A, U, 1, 4, 256, None) == 4
+
+
+def test_linear_host_rejects_bad_arguments(lib):
+    f = lib.qmm_linear_host
+    need = qmm.qmm_row_bytes("q8_0", 256)
+    assert f(qmm.QMM_Q8_0, A, None, A, A, need, A, A, 1, 64, 256, None) == 1   # no host x
+    assert f(qmm.QMM_Q8_0, A, A, A, A, need, A, None, 1, 64, 256, None) == 1   # no host y
+    assert f(qmm.QMM_Q8_0, A, A, A, A, need, A, A, 1, 64, 100, None) == 2
+    assert f(qmm.QMM_Q8_K, A, A, A, A, need, A, A, 1, 64, 256, None) in (2, 3)
 
 
 def test_norm_calls_reject_bad_arguments(lib):

@@ -158,3 +158,21 @@ def test_get_rows_index_out_of_range_is_reported():
     assert np.array_equal(got[0], oracle.get_rows("q8_0", W, [3], K)[0].astype(np.float32))
     assert np.all(got[1:] == 0.0)
     assert qmm.qmm_device_status(clear=True) == 2   # QMM_E_SHAPE
+
+
+def test_linear_host_matches_linear():
+    """qmm_linear_host (pinned x in, the multiply, y out on one stream) gives qmm_linear_<w>'s result bit for bit."""
+    wtype, M, N, K = "q4_K", 2, 300, 4096
+    W = dev(oracle.quantize(wtype, workloads.weights_f32(N, K, seed=71)))
+    x = workloads.activations_f32(M, K, seed=72)
+    x_host = torch.from_numpy(x).pin_memory()
+    y_host = torch.empty(M, N, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty(M, K, dtype=torch.float32, device="cuda")
+    sb = M * qmm.qmm_row_bytes("q8_K", K)
+    scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
+    y_dev = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    qmm.qmm_linear_host(wtype, W, x_host, x_dev, scratch, sb, y_dev, y_host, M, N, K)
+    torch.cuda.synchronize()
+    y2 = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    qmm.linear(wtype, W, dev(x), scratch, sb, y2, M, N, K)
+    assert np.array_equal(y_host.numpy().view(np.uint32), host(y2).view(np.uint32))
