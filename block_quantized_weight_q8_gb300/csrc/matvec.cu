@@ -543,6 +543,11 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
     // warp's per-pass overhead over twice the bytes) measured 6% faster at
     // 12288 x 4096; the other formats were slower that way
     if (WT == QMM_Q4_0 && p->su && p->lpr >= 16 && p->piece_units >= p->lpr) p->lpr >>= 1;
+    // short rows of 32-value blocks (no super-units): 4 lanes per row, several
+    // blocks per lane and 8 rows per pass, rather than one row per 32-lane pass
+    // of short dependency chains (Q4_0 4864 x 896: 4.02 -> 2.22 us; 8 lanes gave
+    // 2.85, 2 lanes 2.35)
+    if (!p->su && F::BV == 32 && p->pieces == 1 && nunit >= 8 && nunit <= 32) p->lpr = 4;
     const uint64_t seg_bytes = (uint64_t)p->piece_units * ubytes;
     const int spp = 32 / p->lpr;
     const uint64_t pass_bytes = (uint64_t)spp * seg_bytes;
