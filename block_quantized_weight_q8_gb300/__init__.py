@@ -58,6 +58,7 @@ SIGNATURES = {
     "qmm_linear_q5_1": ("pppspiiiq", ctypes.c_int),
     "qmm_linear_q5_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
+    "qmm_matmul_q8_0": ("pppiiiq", ctypes.c_int),
     "qmm_get_rows": ("tpppiiiq", ctypes.c_int),
     "qmm_linear_host": ("tppppsppiiiq", ctypes.c_int),
     "qmm_rmsnorm_quantize": ("tppfpiiq", ctypes.c_int),

@@ -8,17 +8,15 @@ namespace qmm {
 qmm_status quantize_act_launch(int act, const float* x, void* xq, int64_t M, int64_t K, cudaStream_t stream, bool pdl);
 qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
                            bool pdl);
-qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                            cudaStream_t stream, bool pdl);
-bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K);
 qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq_out, float* y, int64_t N, int64_t K,
                                  cudaStream_t stream, bool pdl);
 qmm_status matvec_group_fused_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
                                        const float* x, void* xq_out, int64_t K, cudaStream_t stream, bool pdl);
 qmm_status matvec_group_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
                                  const void* xq, int64_t K, cudaStream_t stream, bool pdl);
-qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t stream, bool pdl);
+bool prefill_on_tensor_cores(int wt, int64_t M, int64_t K);
+qmm_status prefill_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                          cudaStream_t stream, bool pdl);
 qmm_status rmsnorm_quantize_launch(int act, const float* x, const float* w, float eps, void* xq, int64_t M, int64_t K,
                                    cudaStream_t stream, bool pdl);
 qmm_status matvec_group_norm_dispatch(int wt, int G, const void* const* W, const int64_t* N, float* const* y,
@@ -37,15 +35,10 @@ static qmm_status linear(int wt, const void* W, const float* x, void* scratch, s
     const int act = act_type_of(wt);
     const size_t xrb = row_bytes_of(act, K);
     if (scratch_bytes < (size_t)M * xrb) return QMM_E_SCRATCH;
-    if (wt == QMM_Q4_0 && M > 1) {
+    if (prefill_on_tensor_cores(wt, M, K)) {  // quantize all rows once, then the tensor-core prefill
         st = quantize_act_launch(act, x, scratch, M, K, stream, true);
         if (st != QMM_OK) return st;
-        return matmul_q4_0_launch(W, scratch, y, M, N, K, stream, true);
-    }
-    if (kq_uses_tensor_cores(wt, M, K)) {  // K-quant prefill on the tensor cores
-        st = quantize_act_launch(act, x, scratch, M, K, stream, true);
-        if (st != QMM_OK) return st;
-        return matmul_kq_launch(wt, W, scratch, y, M, N, K, stream, true);
+        return prefill_launch(wt, W, scratch, y, M, N, K, stream, true);
     }
     // one launch per token that quantizes its row and multiplies; a row too
     // large for that kernel's shared memory is quantized by its own kernel first
@@ -84,6 +77,15 @@ static qmm_status linear_group(int wt, int G, const void* const* W, const int64_
     if (!aligned16(x) || !aligned16(scratch)) return QMM_E_ALIGN;
     const size_t xrb = row_bytes_of(act, K);
     if (scratch_bytes < (size_t)M * xrb) return QMM_E_SCRATCH;
+    if (prefill_on_tensor_cores(wt, M, K)) {  // all rows quantized once, then one prefill per matrix
+        qmm_status st = quantize_act_launch(act, x, scratch, M, K, stream, true);
+        if (st != QMM_OK) return st;
+        for (int g = 0; g < G; g++) {
+            st = prefill_launch(wt, W[g], scratch, y[g], M, N[g], K, stream, true);
+            if (st != QMM_OK) return st;
+        }
+        return QMM_OK;
+    }
     float* yt[8];
     bool fused = true;
     for (int64_t t = 0; t < M; t++) {
@@ -124,12 +126,11 @@ static qmm_status linear_norm(int wt, int G, const void* const* W, const int64_t
     const size_t xrb = row_bytes_of(act, K);
     if (scratch_bytes < (size_t)M * xrb) return QMM_E_SCRATCH;
     qmm_status st;
-    if (M > 1 && (wt == QMM_Q4_0 || kq_uses_tensor_cores(wt, M, K))) {
+    if (prefill_on_tensor_cores(wt, M, K)) {
         st = rmsnorm_quantize_launch(act, x, w, eps, scratch, M, K, stream, true);
         if (st != QMM_OK) return st;
         for (int g = 0; g < G; g++) {
-            st = wt == QMM_Q4_0 ? matmul_q4_0_launch(W[g], scratch, y[g], M, N[g], K, stream, true)
-                                : matmul_kq_launch(wt, W[g], scratch, y[g], M, N[g], K, stream, true);
+            st = prefill_launch(wt, W[g], scratch, y[g], M, N[g], K, stream, true);
             if (st != QMM_OK) return st;
         }
         return QMM_OK;

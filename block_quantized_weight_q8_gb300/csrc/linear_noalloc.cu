@@ -20,13 +20,11 @@ namespace qmm {
 qmm_status quantize_act_launch(int act, const float* x, void* xq, int64_t M, int64_t K, cudaStream_t stream, bool pdl);
 qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
                            bool pdl);
-qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                            cudaStream_t stream, bool pdl);
-bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K);
 qmm_status matvec_fused_dispatch(int wt, const void* W, const float* x, void* xq_out, float* y, int64_t N, int64_t K,
                                  cudaStream_t stream, bool pdl);
-qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t stream, bool pdl);
+bool prefill_on_tensor_cores(int wt, int64_t M, int64_t K);
+qmm_status prefill_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                          cudaStream_t stream, bool pdl);
 
 // 1 MiB: room for 240 Q8_0 rows or 224 Q8_K rows at K = 4096.
 constexpr size_t kNoAllocScratchBytes = (size_t)1 << 20;
@@ -73,15 +71,10 @@ qmm_status qmm_linear_noalloc(int wtype, const void* W, const float* x, float* y
     st = noalloc_scratch(&scratch);
     if (st != QMM_OK) return st;
     cudaStream_t cs = (cudaStream_t)stream;
-    if (wtype == QMM_Q4_0 && M > 1) {
+    if (prefill_on_tensor_cores(wtype, M, K)) {  // quantize all rows once, then the tensor-core prefill
         st = quantize_act_launch(act, x, scratch, M, K, cs, true);
         if (st != QMM_OK) return st;
-        return matmul_q4_0_launch(W, scratch, y, M, N, K, cs, true);
-    }
-    if (kq_uses_tensor_cores(wtype, M, K)) {  // K-quant prefill on the tensor cores
-        st = quantize_act_launch(act, x, scratch, M, K, cs, true);
-        if (st != QMM_OK) return st;
-        return matmul_kq_launch(wtype, W, scratch, y, M, N, K, cs, true);
+        return prefill_launch(wtype, W, scratch, y, M, N, K, cs, true);
     }
     // one launch per token that quantizes its row and multiplies; a row too
     // large for that kernel's shared memory is quantized by its own kernel first

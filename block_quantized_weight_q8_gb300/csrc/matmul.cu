@@ -42,6 +42,9 @@ static __device__ unsigned int g_matmul_error = 0;
 
 qmm_status matvec_dispatch(int wt, const void* W, const void* xq, float* y, int64_t N, int64_t K, cudaStream_t stream,
                            bool pdl);
+qmm_status matmul_kq_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                            cudaStream_t stream, bool pdl);
+bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K);
 
 namespace mm {
 
@@ -50,32 +53,40 @@ constexpr int BN = 128;            // tokens per tile (MMA N, TMEM columns per a
 constexpr int KB = 8;              // Q blocks per raw stage (256 K values)
 constexpr int RAW_STAGES = 2;
 constexpr int OP_SLOTS = 4;        // converted blocks in flight
-constexpr int SC_SLOTS = 32;       // block scales in flight (outlive the operands)
 constexpr int NACC = 4;            // TMEM accumulators (4 x 128 columns = all 512)
 static_assert(OP_SLOTS == NACC, "one barrier tracks both an operand slot and its accumulator");
-constexpr int W_RAW = BM * KB * 18;   // 18432
 constexpr int X_RAW = BN * KB * 34;   // 34816
-constexpr int RAW_BYTES = W_RAW + X_RAW;
 constexpr int OP_A = BM * 32 * 2;     // 8192: fp16 weights of one block
 constexpr int OP_B = BN * 32 * 2;     // 8192: fp16 activations of one block
 constexpr int NUM_CONV_WARPS = 8, NUM_EPI_WARPS = 16;  // converters: 4 for weights, 4 for activations
 constexpr int THREADS = (2 + NUM_CONV_WARPS + NUM_EPI_WARPS) * 32;  // 832
 constexpr int TMEM_COLS = NACC * BN;  // 512
 
-// shared memory layout (offsets from the 1024-byte aligned dynamic shared memory base)
-constexpr int OFF_RAW = 0;
-constexpr int OFF_OPA = OFF_RAW + RAW_STAGES * RAW_BYTES;       // 106496
-constexpr int OFF_OPB = OFF_OPA + OP_SLOTS * OP_A;              // 139264
-constexpr int OFF_SCW = OFF_OPB + OP_SLOTS * OP_B;              // 172032
-constexpr int OFF_SCX = OFF_SCW + SC_SLOTS * BM * 4;            // 176128
-constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;            // 180224
-// barriers: raw_full[2] raw_empty[2] op_full[4] mma_done[4] sc_empty[32] acc_empty[4]
-constexpr int NBARS = 2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + NACC;
-constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
-constexpr int SMEM_BYTES = OFF_TMEM + 16;
+// Shared memory layout per weight format (offsets from the 1024-byte aligned
+// dynamic shared memory base).  Q4_0 weight blocks are 18 bytes, Q8_0 34; the
+// larger raw stages of Q8_0 leave room for 16 scale slots instead of 32.
+template <int WT>
+struct Lay {
+    static constexpr int WB = WT == QMM_Q8_0 ? 34 : 18;
+    static constexpr int SC_SLOTS = WT == QMM_Q8_0 ? 16 : 32;  // block scales in flight (outlive the operands)
+    static constexpr int W_RAW = BM * KB * WB;
+    static constexpr int RAW_BYTES = W_RAW + X_RAW;
+    static constexpr int OFF_RAW = 0;
+    static constexpr int OFF_OPA = OFF_RAW + RAW_STAGES * RAW_BYTES;
+    static constexpr int OFF_OPB = OFF_OPA + OP_SLOTS * OP_A;
+    static constexpr int OFF_SCW = OFF_OPB + OP_SLOTS * OP_B;
+    static constexpr int OFF_SCX = OFF_SCW + SC_SLOTS * BM * 4;
+    static constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;
+    // barriers: raw_full[2] raw_empty[2] op_full[4] mma_done[4] sc_empty[SC_SLOTS] acc_empty[4]
+    static constexpr int NBARS = 2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + NACC;
+    static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+    static constexpr int SMEM_BYTES = OFF_TMEM + 16;
+};
+static_assert(Lay<QMM_Q4_0>::SMEM_BYTES <= 232448 && Lay<QMM_Q8_0>::SMEM_BYTES <= 232448, "prefill smem");
 
 struct Bars {
     uint32_t base;
+    int sc;  // scale slots
     __device__ uint32_t raw_full(int i) const { return base + 8u * i; }
     __device__ uint32_t raw_empty(int i) const { return base + 8u * (RAW_STAGES + i); }
     __device__ uint32_t op_full(int i) const { return base + 8u * (2 * RAW_STAGES + i); }
@@ -85,7 +96,7 @@ struct Bars {
     __device__ uint32_t op_empty(int i) const { return mma_done(i); }
     __device__ uint32_t acc_full(int i) const { return mma_done(i); }
     __device__ uint32_t sc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + i); }
-    __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + i); }
+    __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + sc + i); }
 };
 
 // wait with a time limit; on failure set the error word and the CTA's abort flag.
@@ -100,8 +111,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return false;
 }
 
+template <int WT>
 __global__ void __launch_bounds__(THREADS, 1)
-    matmul_q4_0_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+    matmul_q_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                        float* __restrict__ Y, int M, int N, int K, int pdl) {
     if (pdl) pdl_launch_dependents();
     // used directly (not re-aligned by integer arithmetic) so that the compiler
@@ -112,7 +124,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (threadIdx.x == 0) atomicOr(&g_matmul_error, kErrTimeout);
         return;
     }
-    const Bars bars{sbase + OFF_BAR};
+    using L = Lay<WT>;
+    constexpr int OFF_RAW = L::OFF_RAW, OFF_OPA = L::OFF_OPA, OFF_OPB = L::OFF_OPB, OFF_SCW = L::OFF_SCW,
+                  OFF_SCX = L::OFF_SCX, OFF_TMEM = L::OFF_TMEM, SC_SLOTS = L::SC_SLOTS, W_RAW = L::W_RAW,
+                  RAW_BYTES = L::RAW_BYTES, WB = L::WB;
+    const Bars bars{sbase + L::OFF_BAR, SC_SLOTS};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_TMEM + 8);
     const float* scw = reinterpret_cast<const float*>(smem + OFF_SCW);
@@ -158,7 +174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 const uint32_t dst = sbase + OFF_RAW + s * RAW_BYTES;
                 mbar_arrive_expect_tx(bars.raw_full(s), RAW_BYTES);
-                tma_load_2d(dst, &wmap, c * (KB * 18 / 2), o0, bars.raw_full(s));
+                tma_load_2d(dst, &wmap, c * (KB * WB / 2), o0, bars.raw_full(s));
                 tma_load_2d(dst + W_RAW, &xmap, c * (KB * 34 / 2), t0, bars.raw_full(s));
             }
         }
@@ -189,8 +205,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < nchunks; c++) {
             const int s = c % RAW_STAGES;
             if (!wait_or_abort(bars.raw_full(s), (c / RAW_STAGES) & 1, abort_flag)) break;
-            if (is_w) {
-                // this weight row's 8 blocks: 144 bytes, 16-byte aligned
+            if (WT == QMM_Q4_0 && is_w) {
+                // this Q4_0 weight row's 8 blocks: 144 bytes, 16-byte aligned
                 uint32_t raw[36];
                 const uint4* src = reinterpret_cast<const uint4*>(smem + OFF_RAW + s * RAW_BYTES + r * (KB * 18));
 #pragma unroll
@@ -235,9 +251,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) mbar_arrive(bars.op_full(os));
                 }
             } else {
-                // this token's 8 blocks: 272 bytes, 16-byte aligned, read as two windows of
-                // 144 bytes (bytes 0..143 hold blocks 0-3, bytes 128..271 hold blocks 4-7)
-                const uint8_t* row = smem + OFF_RAW + s * RAW_BYTES + W_RAW + r * (KB * 34);
+                // this token's (or Q8_0 weight row's) 8 blocks: 272 bytes, 16-byte aligned,
+                // read as two windows of 144 bytes (bytes 0..143 hold blocks 0-3, bytes
+                // 128..271 hold blocks 4-7)
+                const uint8_t* row = smem + OFF_RAW + s * RAW_BYTES + (is_w ? 0 : W_RAW) + r * (KB * 34);
+                uint8_t* const opbase = smem + (is_w ? OFF_OPA : OFF_OPB);
+                float* const scbase = reinterpret_cast<float*>(smem + (is_w ? OFF_SCW : OFF_SCX));
 #pragma unroll
                 for (int h = 0; h < 2; h++) {
                     uint32_t raw[36];
@@ -264,7 +283,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint32_t dbits =
                             __funnelshift_r(raw[off / 4], raw[off / 4 + 1], 8 * (off % 4)) & 0xFFFFu;
                         const uint32_t m128 = 0x64806480u;  // (1152, 1152): 1024 + (a + 128) - 1152 = a
-                        uint8_t* Bop = smem + OFF_OPB + os * OP_B;
+                        static_assert(OP_A == OP_B && BM == BN, "one converter for both operands");
+                        uint8_t* Bop = opbase + os * OP_B;
 #pragma unroll
                         for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7: code words 2kq, 2kq+1
                             const int q0 = off + 2 + 8 * kq, q1 = q0 + 4;
@@ -279,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             v.w = h2_sub(bytes_to_h2(w1, 0x7362), m128);
                             *reinterpret_cast<uint4*>(Bop + op_off(r, kq)) = v;
                         }
-                        reinterpret_cast<float*>(smem + OFF_SCX)[ss * BN + r] = h2f(dbits);
+                        scbase[ss * BN + r] = h2f(dbits);
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bars.op_full(os));
@@ -382,34 +402,36 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uin
 // enough tokens to fill a tile reasonably; other shapes run one matvec per token.
 static bool tensor_core_shape(int64_t M, int64_t K) { return K % 256 == 0 && M >= 8; }
 
-qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t stream, bool pdl) {
+template <int WT>
+static qmm_status matmul_q_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                                  cudaStream_t stream, bool pdl) {
+    using L = mm::Lay<WT>;
     if (!tensor_core_shape(M, K)) {
         const size_t xrb = row_bytes_of(QMM_Q8_0, K);
         for (int64_t t = 0; t < M; t++) {
-            qmm_status st = matvec_dispatch(QMM_Q4_0, W, (const uint8_t*)xq + t * xrb, Y + t * N, N, K, stream, pdl);
+            qmm_status st = matvec_dispatch(WT, W, (const uint8_t*)xq + t * xrb, Y + t * N, N, K, stream, pdl);
             if (st != QMM_OK) return st;
         }
         return QMM_OK;
     }
     if ((N + mm::BM - 1) / mm::BM > 0x7FFFFFFF || (M + mm::BN - 1) / mm::BN > 65535) return QMM_E_SHAPE;
     CUtensorMap wmap, xmap;
-    if (!make_map(&wmap, W, row_bytes_of(QMM_Q4_0, K), (uint64_t)N, mm::KB * 18) ||
+    if (!make_map(&wmap, W, row_bytes_of(WT, K), (uint64_t)N, mm::KB * L::WB) ||
         !make_map(&xmap, xq, row_bytes_of(QMM_Q8_0, K), (uint64_t)M, mm::KB * 34))
         return QMM_E_CUDA;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMM_E_CUDA;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(mm::matmul_q4_0_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 mm::SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(mm::matmul_q_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::SMEM_BYTES) != cudaSuccess)
             return QMM_E_CUDA;
         attr_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + mm::BN - 1) / mm::BN));
     cfg.blockDim = dim3(mm::THREADS);
-    cfg.dynamicSmemBytes = mm::SMEM_BYTES;
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -417,8 +439,35 @@ qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, mm::matmul_q4_0_kernel, wmap, xmap, Y, (int)M, (int)N, (int)K, pdl ? 1 : 0);
+        cudaLaunchKernelEx(&cfg, mm::matmul_q_kernel<WT>, wmap, xmap, Y, (int)M, (int)N, (int)K, pdl ? 1 : 0);
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
+
+qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t stream, bool pdl) {
+    return matmul_q_launch<QMM_Q4_0>(W, xq, Y, M, N, K, stream, pdl);
+}
+
+qmm_status matmul_q8_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t stream, bool pdl) {
+    return matmul_q_launch<QMM_Q8_0>(W, xq, Y, M, N, K, stream, pdl);
+}
+
+// Whether an M-token multiply of this weight type takes a tensor-core prefill
+// kernel (after one quantization of all M rows) rather than a launch per token.
+// Q4_0 takes it for every M > 1 (its launcher runs per-token matvecs itself on
+// shapes the tiles do not take); Q8_0 only on shapes the tiles take.
+bool prefill_on_tensor_cores(int wt, int64_t M, int64_t K) {
+    if (wt == QMM_Q4_0) return M > 1;
+    if (wt == QMM_Q8_0) return M > 1 && tensor_core_shape(M, K);
+    return kq_uses_tensor_cores(wt, M, K);
+}
+
+qmm_status prefill_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                          cudaStream_t stream, bool pdl) {
+    if (wt == QMM_Q4_0) return matmul_q_launch<QMM_Q4_0>(W, xq, Y, M, N, K, stream, pdl);
+    if (wt == QMM_Q8_0) return matmul_q_launch<QMM_Q8_0>(W, xq, Y, M, N, K, stream, pdl);
+    return matmul_kq_launch(wt, W, xq, Y, M, N, K, stream, pdl);
 }
 
 }  // namespace qmm
@@ -434,6 +483,15 @@ qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, i
     if (st != QMM_OK) return st;
     if (!aligned16(W) || !aligned16(xq) || !aligned16(Y)) return QMM_E_ALIGN;
     return matmul_q4_0_launch(W, xq, Y, M, N, K, (cudaStream_t)stream, true);
+}
+
+qmm_status qmm_matmul_q8_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    if (!W || !xq || !Y) return QMM_E_NULL;
+    qmm_status st = check_shape(QMM_Q8_0, M, N, K);
+    if (st != QMM_OK) return st;
+    if (!aligned16(W) || !aligned16(xq) || !aligned16(Y)) return QMM_E_ALIGN;
+    return matmul_q8_0_launch(W, xq, Y, M, N, K, (cudaStream_t)stream, true);
 }
 
 unsigned qmm_internal_matmul_error(int clear) {

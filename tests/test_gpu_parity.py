@@ -204,14 +204,64 @@ def test_linear_matches_quantize_then_matvec(wtype, M):
 
 
 # ------------------------------------------------------------------ prefill matmul
+@pytest.mark.parametrize("wtype", ["q4_0", "q8_0"])
 @pytest.mark.parametrize("M,N,K", [(1, 64, 256), (3, 100, 512), (17, 300, 1024), (128, 256, 4096),
-                                   (130, 390, 2048)])
-def test_matmul_q4_0_matches_oracle(M, N, K):
-    W, X = make_inputs("q4_0", M, N, K, seed=9000 + M)
-    ref = oracle.matmul("q4_0", W, X, M, N, K, nthreads=8)
+                                   (130, 390, 2048), (8, 129, 256), (255, 17, 768)])
+def test_matmul_q_matches_oracle(wtype, M, N, K):
+    """The 32-value-block prefill (Q4_0 or Q8_0 weights x Q8_0 rows): several tiles in both directions,
+    ragged last tiles of rows and tokens, a single output row, and the per-token fallback shapes."""
+    W, X = make_inputs(wtype, M, N, K, seed=9000 + M)
+    ref = oracle.matmul(wtype, W, X, M, N, K, nthreads=8)
     Y = f32(M, N)
-    qmm.qmm_matmul_q4_0(dev(W), dev(X), Y, M, N, K)
+    qmm.matmul(wtype, dev(W), dev(X), Y, M, N, K)
     assert_rows_close(host(Y), ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 128, 256), (130, 300, 1024)])
+def test_matmul_q8_0_integer_sums_exact(M, N, K):
+    """Integer-valued rows with a +-127 in every block quantize to d = 1 and codes equal to the values,
+    so Y is the plain integer matrix product (at most 1024 * 127 * 127 < 2^24: exact in f32) and must
+    match it bit for bit: each block's sum of 32 products up to 127 * 127 is exact on the tensor cores."""
+    g = np.random.default_rng(77 + M)
+    w = g.integers(-127, 128, size=(N, K)).astype(np.float32)
+    x = g.integers(-127, 128, size=(M, K)).astype(np.float32)
+    w[:, ::32] = np.where(g.random((N, K // 32)) < 0.5, 127.0, -127.0)
+    x[:, ::32] = np.where(g.random((M, K // 32)) < 0.5, 127.0, -127.0)
+    w[0, :] = 127.0  # the largest block sums, both signs
+    x[0, :] = 127.0
+    x[1, :] = -127.0
+    W = oracle.quantize("q8_0", w)
+    X = oracle.quantize("q8_0", x)
+    want = (x.astype(np.int64) @ w.astype(np.int64).T).astype(np.float32)
+    Y = f32(M, N)
+    qmm.matmul("q8_0", dev(W), dev(X), Y, M, N, K)
+    assert np.array_equal(host(Y), want)
+    # and through the quantize + multiply entry point, with the GPU quantizer
+    Y2 = f32(M, N)
+    xrb = qmm.qmm_row_bytes("q8_0", K)
+    scratch = u8(M * xrb)
+    qmm.linear("q8_0", dev(W), dev(x), scratch, scratch.numel(), Y2, M, N, K)
+    assert np.array_equal(host(scratch), X.reshape(-1))
+    assert np.array_equal(host(Y2), want)
+
+
+@pytest.mark.parametrize("M", [8, 64])
+def test_linear_q8_0_prefill_route(M):
+    """qmm_linear_q8_0 with M >= 8 quantizes all rows, then runs the prefill: bit for bit the same as
+    qmm_quantize_q8_0 followed by qmm_matmul_q8_0."""
+    N, K = 300, 2048
+    W, _ = make_inputs("q8_0", 1, N, K, seed=4242)
+    x = workloads.activations_f32(M, K, seed=4243)
+    Wd, xd = dev(W), dev(x)
+    xrb = qmm.qmm_row_bytes("q8_0", K)
+    s1, s2 = u8(M * xrb), u8(M * xrb)
+    y1, y2 = f32(M, N), f32(M, N)
+    qmm.linear("q8_0", Wd, xd, s1, s1.numel(), y1, M, N, K)
+    qmm.qmm_quantize_q8_0(xd, s2, M, K)
+    qmm.matmul("q8_0", Wd, s2, y2, M, N, K)
+    assert np.array_equal(host(s1), host(s2))
+    assert np.array_equal(host(y1).view(np.uint32), host(y2).view(np.uint32))
+    assert_rows_close(host(y1), oracle.matmul("q8_0", W, oracle.quantize("q8_0", x), M, N, K, nthreads=8))
 
 
 # ------------------------------------------------------------------ full workload sizes
@@ -254,23 +304,23 @@ def test_full_size_layer_set():
         assert_rows_close(host(y), ref)
 
 
-@pytest.mark.parametrize("M", [128, 512, 2048])
-def test_full_size_prefill_sampled(M):
+@pytest.mark.parametrize("wtype,M", [("q4_0", 128), ("q4_0", 512), ("q4_0", 2048), ("q8_0", 512)])
+def test_full_size_prefill_sampled(wtype, M):
     cfg = workloads.WORKLOADS["q4_0_prefill_512x12288x4096"]
     N, K = cfg["N"], cfg["K"]
     w = workloads.weights_f32(N, K, cfg["seed"])
     x = workloads.activations_f32(M, K, cfg["seed"])
-    W = oracle.quantize("q4_0", w)
+    W = oracle.quantize(wtype, w)
     X = oracle.quantize("q8_0", x)
     Y = f32(M, N)
-    qmm.qmm_matmul_q4_0(dev(W), dev(X), Y, M, N, K)
+    qmm.matmul(wtype, dev(W), dev(X), Y, M, N, K)
     got = host(Y)
     g = np.random.default_rng(M)
     tokens = np.unique(np.concatenate([[0, M - 1], g.integers(0, M, 6)]))
     rows = np.unique(np.concatenate([[0, N - 1], g.integers(0, N, 200)]))
     Wr = W.reshape(N, -1)[rows]
     for t in tokens:
-        ref_full = oracle.matmul("q4_0", W, X.reshape(M, -1)[t:t + 1], 1, N, K, nthreads=16)[0]
+        ref_full = oracle.matmul(wtype, W, X.reshape(M, -1)[t:t + 1], 1, N, K, nthreads=16)[0]
         assert_rows_close(got[t], ref_full)
-        ref_rows = oracle.matmul("q4_0", Wr, X.reshape(M, -1)[t:t + 1], 1, len(rows), K)[0]
+        ref_rows = oracle.matmul(wtype, Wr, X.reshape(M, -1)[t:t + 1], 1, len(rows), K)[0]
         assert np.array_equal(ref_rows, ref_full[rows])
