@@ -1,5 +1,5 @@
-// matmul.cu -- the prefill matmul Y[M][N] for Q4_0 weights x Q8_0 activations,
-// M tokens at once, on the 5th-generation tensor cores.
+// matmul.cu -- the prefill matmul Y[M][N] for Q4_0 or Q8_0 weights x Q8_0
+// activations, M tokens at once, on the 5th-generation tensor cores.
 //
 // Y[t][o] = sum_b d_w[o,b] * d_x[t,b] * isum[t,o,b] ([krafla] "Architecture",
 // Batched prompt prefill; [kvad] "Batched prefill, and i8mm"): the weights are
@@ -8,26 +8,30 @@
 // sm_103a has no int8 tensor-core MMA (ptxas rejects tcgen05.mma .kind::i8 for
 // this target), so the integer codes go through .kind::f16 with fp16 operands:
 // every Q4_0 code (-8..7) and Q8_0 code (-128..127) is an exact fp16 value, all
-// products are exact, and each 32-wide block's sum (|sum| <= 32*8*128 < 2^24) is
+// products are exact, and each 32-wide block's sum (|sum| <= 32*128*128 < 2^24) is
 // exact in the fp32 accumulator -- the MMA computes the same integer isum the
 // scalar kernel does ([minfer] s3.2: the integer dot is exact; [ggml] s2).
 // Each block's sum is then folded into an fp32 accumulator once, scaled by
 // d_w * d_x, exactly as the pages' kernels fold per block.
 //
-// One CTA per output tile of 128 weight rows x 128 tokens:
+// One CTA per output tile of 128 weight rows x 128 tokens, 28 warps:
 //   warp 0   producer: 2-D TMA loads of the raw weight bytes (128 rows x 8 blocks)
 //            and the raw activation bytes (128 tokens x 8 blocks) into a ring of
 //            raw stages; also owns the tensor-memory allocation
-//   warp 1   MMA issuer: per block, two tcgen05.mma (K = 16 each) into one of four
-//            128-column TMEM accumulators, then tcgen05.commit
-//   warps 2-9 converters (2-5 weight rows, 6-9 tokens): each thread loads its
-//            row of the raw stage into registers with 16-byte loads, then writes
-//            each block as fp16 operands in the UMMA K-major core-matrix layout
-//            (8 rows x 16 bytes per core matrix) plus its f32 scale
-//   warps 10-25 epilogue: tcgen05.ld of each block's exact sums (32 tokens of one
+//   warp 1   MMA issuer: per pair of blocks, two tcgen05.mma (K = 16 each) per
+//            block into its own 128-column TMEM accumulator, then one
+//            tcgen05.commit for the pair
+//   warps 2-4, 6-8, 10-11  converters (four for weight rows, four for tokens):
+//            each thread loads its row of the raw stage into registers with
+//            16-byte loads, then writes each block as fp16 operands in the UMMA
+//            K-major core-matrix layout (8 rows x 16 bytes per core matrix) plus
+//            its f32 scale; warps 5 and 9 stay idle so that the MMA issuer's
+//            scheduler carries no converter work
+//   warps 12-27 epilogue: tcgen05.ld of each block's exact sums (32 tokens of one
 //            weight row per thread), y += v * (d_w*d_x) in registers in block
 //            order, then the token-major store
-// All waits are bounded; a timeout records QMM_E_TIMEOUT, every warp still
+// Blocks move between the roles in pairs (one barrier handshake per two blocks);
+// all waits are bounded; a timeout records QMM_E_TIMEOUT, every warp still
 // reaches the end, and TMEM is freed.
 #include <cuda.h>
 #include <mutex>
@@ -52,51 +56,64 @@ constexpr int BM = 128;            // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;            // tokens per tile (MMA N, TMEM columns per accumulator)
 constexpr int KB = 8;              // Q blocks per raw stage (256 K values)
 constexpr int RAW_STAGES = 2;
-constexpr int OP_SLOTS = 4;        // converted blocks in flight
-constexpr int NACC = 4;            // TMEM accumulators (4 x 128 columns = all 512)
-static_assert(OP_SLOTS == NACC, "one barrier tracks both an operand slot and its accumulator");
+constexpr int ACC_PAIRS = 2;       // accumulator pairs: two blocks' sums per handshake (4 x 128 columns)
 constexpr int X_RAW = BN * KB * 34;   // 34816
 constexpr int OP_A = BM * 32 * 2;     // 8192: fp16 weights of one block
 constexpr int OP_B = BN * 32 * 2;     // 8192: fp16 activations of one block
 constexpr int NUM_CONV_WARPS = 8, NUM_EPI_WARPS = 16;  // converters: 4 for weights, 4 for activations
-constexpr int THREADS = (2 + NUM_CONV_WARPS + NUM_EPI_WARPS) * 32;  // 832
-constexpr int TMEM_COLS = NACC * BN;  // 512
+// Warps 0-11: producer (0), MMA issuer (1), converters (2-4, 6-8, 10-11), two
+// idle warps (5, 9) that keep the MMA issuer's scheduler free of converter work;
+// warps 12-27: epilogue (warp % 4 is the TMEM lane quadrant it may read).
+constexpr int EPI0 = 12;
+constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 896
+constexpr int TMEM_COLS = 2 * ACC_PAIRS * BN;  // 512: four 128-column accumulators
+
+__device__ __forceinline__ int converter_index(int warp) {  // 0..7, or -1 for other warps
+    return (warp >= 2 && warp < EPI0 && warp != 5 && warp != 9) ? warp - 2 - (warp > 5) - (warp > 9) : -1;
+}
 
 // Shared memory layout per weight format (offsets from the 1024-byte aligned
 // dynamic shared memory base).  Q4_0 weight blocks are 18 bytes, Q8_0 34; the
-// larger raw stages of Q8_0 leave room for 16 scale slots instead of 32.
+// larger raw stages of Q8_0 leave room for 16 scale slots instead of 32.  (A
+// third operand pair for Q4_0, in place of 16 scale slots, measured no faster.)
 template <int WT>
 struct Lay {
     static constexpr int WB = WT == QMM_Q8_0 ? 34 : 18;
+    static constexpr int PAIRS = 2;                             // operand pair slots (converted blocks in flight / 2)
+    static constexpr int OPS = 2 * PAIRS;
     static constexpr int SC_SLOTS = WT == QMM_Q8_0 ? 16 : 32;  // block scales in flight (outlive the operands)
+    static constexpr int SCP = SC_SLOTS / 2;                   // ... in pairs
     static constexpr int W_RAW = BM * KB * WB;
     static constexpr int RAW_BYTES = W_RAW + X_RAW;
     static constexpr int OFF_RAW = 0;
     static constexpr int OFF_OPA = OFF_RAW + RAW_STAGES * RAW_BYTES;
-    static constexpr int OFF_OPB = OFF_OPA + OP_SLOTS * OP_A;
-    static constexpr int OFF_SCW = OFF_OPB + OP_SLOTS * OP_B;
+    static constexpr int OFF_OPB = OFF_OPA + OPS * OP_A;
+    static constexpr int OFF_SCW = OFF_OPB + OPS * OP_B;
     static constexpr int OFF_SCX = OFF_SCW + SC_SLOTS * BM * 4;
     static constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;
-    // barriers: raw_full[2] raw_empty[2] op_full[4] mma_done[4] sc_empty[SC_SLOTS] acc_empty[4]
-    static constexpr int NBARS = 2 * RAW_STAGES + 2 * OP_SLOTS + SC_SLOTS + NACC;
+    // barriers: raw_full[2] raw_empty[2] op_full[PAIRS] op_empty[PAIRS] acc_full[2] acc_empty[2] sc_empty[SCP]
+    static constexpr int NBARS = 2 * RAW_STAGES + 2 * PAIRS + 2 * ACC_PAIRS + SCP;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM + 16;
 };
 static_assert(Lay<QMM_Q4_0>::SMEM_BYTES <= 232448 && Lay<QMM_Q8_0>::SMEM_BYTES <= 232448, "prefill smem");
+static_assert(KB % 4 == 0, "pairs must not straddle the activation converter's 4-block windows");
 
 struct Bars {
     uint32_t base;
-    int sc;  // scale slots
+    int pairs;  // operand pair slots
     __device__ uint32_t raw_full(int i) const { return base + 8u * i; }
     __device__ uint32_t raw_empty(int i) const { return base + 8u * (RAW_STAGES + i); }
+    // operand pair slot i: written by the converters / read by the tensor core (one tcgen05.commit)
     __device__ uint32_t op_full(int i) const { return base + 8u * (2 * RAW_STAGES + i); }
-    // MMA of the block in slot i complete: its operands may be overwritten and its
-    // accumulator read (one tcgen05.commit serves both)
-    __device__ uint32_t mma_done(int i) const { return base + 8u * (2 * RAW_STAGES + OP_SLOTS + i); }
-    __device__ uint32_t op_empty(int i) const { return mma_done(i); }
-    __device__ uint32_t acc_full(int i) const { return mma_done(i); }
-    __device__ uint32_t sc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + i); }
-    __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * OP_SLOTS + sc + i); }
+    __device__ uint32_t op_empty(int i) const { return base + 8u * (2 * RAW_STAGES + pairs + i); }
+    // accumulator pair i: both blocks' sums complete (one tcgen05.commit) / read into registers
+    __device__ uint32_t acc_full(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * pairs + i); }
+    __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * pairs + ACC_PAIRS + i); }
+    // scale pair slot i read by the epilogue
+    __device__ uint32_t sc_empty(int i) const {
+        return base + 8u * (2 * RAW_STAGES + 2 * pairs + 2 * ACC_PAIRS + i);
+    }
 };
 
 // wait with a time limit; on failure set the error word and the CTA's abort flag.
@@ -114,7 +131,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 template <int WT>
 __global__ void __launch_bounds__(THREADS, 1)
     matmul_q_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                       float* __restrict__ Y, int M, int N, int K, int pdl) {
+                    float* __restrict__ Y, int M, int N, int K, int pdl) {
     if (pdl) pdl_launch_dependents();
     // used directly (not re-aligned by integer arithmetic) so that the compiler
     // keeps every access in the shared state space
@@ -125,14 +142,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         return;
     }
     using L = Lay<WT>;
-    constexpr int OFF_RAW = L::OFF_RAW, OFF_OPA = L::OFF_OPA, OFF_OPB = L::OFF_OPB, OFF_SCW = L::OFF_SCW,
-                  OFF_SCX = L::OFF_SCX, OFF_TMEM = L::OFF_TMEM, SC_SLOTS = L::SC_SLOTS, W_RAW = L::W_RAW,
-                  RAW_BYTES = L::RAW_BYTES, WB = L::WB;
-    const Bars bars{sbase + L::OFF_BAR, SC_SLOTS};
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_TMEM + 8);
-    const float* scw = reinterpret_cast<const float*>(smem + OFF_SCW);
-    const float* scx = reinterpret_cast<const float*>(smem + OFF_SCX);
+    constexpr int SC_SLOTS = L::SC_SLOTS, SCP = L::SCP, W_RAW = L::W_RAW, RAW_BYTES = L::RAW_BYTES, WB = L::WB,
+                  PAIRS = L::PAIRS;
+    const Bars bars{sbase + L::OFF_BAR, PAIRS};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_TMEM + 8);
+    const float* scw = reinterpret_cast<const float*>(smem + L::OFF_SCW);
+    const float* scx = reinterpret_cast<const float*>(smem + L::OFF_SCX);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int o0 = blockIdx.x * BM, t0 = blockIdx.y * BN;
@@ -144,12 +160,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bars.raw_full(i), 1);
             mbar_init(bars.raw_empty(i), NUM_CONV_WARPS);
         }
-        for (int i = 0; i < OP_SLOTS; i++) {
+        for (int i = 0; i < PAIRS; i++) {
             mbar_init(bars.op_full(i), NUM_CONV_WARPS);
-            mbar_init(bars.mma_done(i), 1);
+            mbar_init(bars.op_empty(i), 1);
         }
-        for (int i = 0; i < SC_SLOTS; i++) mbar_init(bars.sc_empty(i), NUM_EPI_WARPS);
-        for (int i = 0; i < NACC; i++) mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
+        for (int i = 0; i < ACC_PAIRS; i++) {
+            mbar_init(bars.acc_full(i), 1);
+            mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
+        }
+        for (int i = 0; i < SCP; i++) mbar_init(bars.sc_empty(i), NUM_EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -163,6 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int cw = converter_index(warp);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -172,7 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int s = c % RAW_STAGES;
                 if (c >= RAW_STAGES && !wait_or_abort(bars.raw_empty(s), ((c / RAW_STAGES) - 1) & 1, abort_flag))
                     break;
-                const uint32_t dst = sbase + OFF_RAW + s * RAW_BYTES;
+                const uint32_t dst = sbase + L::OFF_RAW + s * RAW_BYTES;
                 mbar_arrive_expect_tx(bars.raw_full(s), RAW_BYTES);
                 tma_load_2d(dst, &wmap, c * (KB * WB / 2), o0, bars.raw_full(s));
                 tma_load_2d(dst + W_RAW, &xmap, c * (KB * 34 / 2), t0, bars.raw_full(s));
@@ -183,32 +203,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             const uint32_t idesc = instr_desc_f16(BM, BN);
             // descriptors of slot 0; slot os adds os * OP_A (>> 4) to the address field
-            const uint64_t a0 = smem_desc(sbase + OFF_OPA, 128, 512);
-            const uint64_t b0 = smem_desc(sbase + OFF_OPB, 128, 512);
-            for (int b = 0; b < nb; b++) {
-                const int os = b % OP_SLOTS, ac = b % NACC;
-                if (!wait_or_abort(bars.op_full(os), (b / OP_SLOTS) & 1, abort_flag)) break;
-                if (b >= NACC && !wait_or_abort(bars.acc_empty(ac), ((b / NACC) - 1) & 1, abort_flag)) break;
+            const uint64_t a0 = smem_desc(sbase + L::OFF_OPA, 128, 512);
+            const uint64_t b0 = smem_desc(sbase + L::OFF_OPB, 128, 512);
+            for (int p = 0; p < nb / 2; p++) {  // blocks 2p and 2p+1 per handshake
+                const int ps = p % PAIRS, ap = p % ACC_PAIRS;
+                if (!wait_or_abort(bars.op_full(ps), (p / PAIRS) & 1, abort_flag)) break;
+                if (p >= ACC_PAIRS && !wait_or_abort(bars.acc_empty(ap), ((p / ACC_PAIRS) - 1) & 1, abort_flag))
+                    break;
                 tc_fence_after();
-                const uint64_t ad = a0 + (uint64_t)(os * (OP_A >> 4));
-                const uint64_t bd = b0 + (uint64_t)(os * (OP_B >> 4));
-                const uint32_t d = tmem + (uint32_t)(ac * BN);
-                mma_f16(d, ad, bd, idesc, 0);                    // K 0..15: core matrices 0, 1
-                mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1);  // K 16..31: core matrices 2, 3
-                mma_commit(bars.mma_done(os));
+#pragma unroll
+                for (int i = 0; i < 2; i++) {
+                    const int os = 2 * ps + i;
+                    const uint64_t ad = a0 + (uint64_t)(os * (OP_A >> 4));
+                    const uint64_t bd = b0 + (uint64_t)(os * (OP_B >> 4));
+                    const uint32_t d = tmem + (uint32_t)((2 * ap + i) * BN);
+                    mma_f16(d, ad, bd, idesc, 0);                            // K 0..15: core matrices 0, 1
+                    mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1);  // K 16..31: core matrices 2, 3
+                }
+                mma_commit(bars.op_empty(ps));
+                mma_commit(bars.acc_full(ap));
             }
         }
-    } else if (warp < 2 + NUM_CONV_WARPS) {
+    } else if (cw >= 0) {
         // ------------------------------------------------------------ converters
-        const bool is_w = warp < 2 + NUM_CONV_WARPS / 2;
-        const int r = (warp - (is_w ? 2 : 2 + NUM_CONV_WARPS / 2)) * 32 + lane;  // weight row or token, 0..127
+        // Blocks go in pairs: the slots of pair p are taken (operands freed by the
+        // MMAs of pair p - PAIRS, scales by the epilogue of pair p - SCP) before
+        // its first block, and handed to the MMA issuer after its second.
+        const bool is_w = cw < NUM_CONV_WARPS / 2;
+        const int r = (cw % (NUM_CONV_WARPS / 2)) * 32 + lane;  // weight row or token, 0..127
         for (int c = 0; c < nchunks; c++) {
             const int s = c % RAW_STAGES;
             if (!wait_or_abort(bars.raw_full(s), (c / RAW_STAGES) & 1, abort_flag)) break;
             if (WT == QMM_Q4_0 && is_w) {
                 // this Q4_0 weight row's 8 blocks: 144 bytes, 16-byte aligned
                 uint32_t raw[36];
-                const uint4* src = reinterpret_cast<const uint4*>(smem + OFF_RAW + s * RAW_BYTES + r * (KB * 18));
+                const uint4* src = reinterpret_cast<const uint4*>(smem + L::OFF_RAW + s * RAW_BYTES + r * (KB * 18));
 #pragma unroll
                 for (int i = 0; i < 9; i++) {
                     const uint4 v = src[i];
@@ -218,9 +247,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) mbar_arrive(bars.raw_empty(s));
 #pragma unroll
                 for (int lb = 0; lb < KB; lb++) {
-                    const int b = c * KB + lb, os = b % OP_SLOTS, ss = b % SC_SLOTS;
-                    if (b >= OP_SLOTS && !wait_or_abort(bars.op_empty(os), ((b / OP_SLOTS) - 1) & 1, abort_flag)) break;
-                    if (b >= SC_SLOTS && !wait_or_abort(bars.sc_empty(ss), ((b / SC_SLOTS) - 1) & 1, abort_flag)) break;
+                    const int b = c * KB + lb, p = b >> 1, ps = p % PAIRS, os = 2 * ps + (b & 1), ss = b % SC_SLOTS;
+                    if ((b & 1) == 0) {
+                        if (p >= PAIRS && !wait_or_abort(bars.op_empty(ps), ((p / PAIRS) - 1) & 1, abort_flag)) break;
+                        if (p >= SCP && !wait_or_abort(bars.sc_empty(p % SCP), ((p / SCP) - 1) & 1, abort_flag))
+                            break;
+                    }
                     // block lb: f16 d at byte 18*lb, nibbles at 18*lb + 2 (element j low, j+16 high)
                     const int off = 18 * lb;
                     const uint32_t dbits = __funnelshift_r(raw[off / 4], raw[off / 4 + 1], 8 * (off % 4)) & 0xFFFFu;
@@ -233,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         hi[i] = (q >> 4) & 0x0F0F0F0Fu;
                     }
                     const uint32_t m8 = 0x64086408u;  // (1032, 1032): 1024 + n - 1032 = n - 8
-                    uint8_t* A = smem + OFF_OPA + os * OP_A;
+                    uint8_t* A = smem + L::OFF_OPA + os * OP_A;
 #pragma unroll
                     for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7
                         const uint32_t w0 = kq < 2 ? lo[2 * kq] : hi[2 * (kq - 2)];
@@ -245,18 +277,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                         v.w = h2_sub(bytes_to_h2(w1, 0x7362), m8);
                         *reinterpret_cast<uint4*>(A + op_off(r, kq)) = v;
                     }
-                    reinterpret_cast<float*>(smem + OFF_SCW)[ss * BM + r] = h2f(dbits);
-                    fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bars.op_full(os));
+                    reinterpret_cast<float*>(smem + L::OFF_SCW)[ss * BM + r] = h2f(dbits);
+                    if (b & 1) {
+                        fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.op_full(ps));
+                    }
                 }
             } else {
                 // this token's (or Q8_0 weight row's) 8 blocks: 272 bytes, 16-byte aligned,
                 // read as two windows of 144 bytes (bytes 0..143 hold blocks 0-3, bytes
                 // 128..271 hold blocks 4-7)
-                const uint8_t* row = smem + OFF_RAW + s * RAW_BYTES + (is_w ? 0 : W_RAW) + r * (KB * 34);
-                uint8_t* const opbase = smem + (is_w ? OFF_OPA : OFF_OPB);
-                float* const scbase = reinterpret_cast<float*>(smem + (is_w ? OFF_SCW : OFF_SCX));
+                const uint8_t* row = smem + L::OFF_RAW + s * RAW_BYTES + (is_w ? 0 : W_RAW) + r * (KB * 34);
+                uint8_t* const opbase = smem + (is_w ? L::OFF_OPA : L::OFF_OPB);
+                float* const scbase = reinterpret_cast<float*>(smem + (is_w ? L::OFF_SCW : L::OFF_SCX));
 #pragma unroll
                 for (int h = 0; h < 2; h++) {
                     uint32_t raw[36];
@@ -273,11 +307,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int lq = 0; lq < KB / 2; lq++) {
                         const int lb = 4 * h + lq;
-                        const int b = c * KB + lb, os = b % OP_SLOTS, ss = b % SC_SLOTS;
-                        if (b >= OP_SLOTS && !wait_or_abort(bars.op_empty(os), ((b / OP_SLOTS) - 1) & 1, abort_flag))
-                            break;
-                        if (b >= SC_SLOTS && !wait_or_abort(bars.sc_empty(ss), ((b / SC_SLOTS) - 1) & 1, abort_flag))
-                            break;
+                        const int b = c * KB + lb, p = b >> 1, ps = p % PAIRS, os = 2 * ps + (b & 1),
+                                  ss = b % SC_SLOTS;
+                        if ((b & 1) == 0) {
+                            if (p >= PAIRS &&
+                                !wait_or_abort(bars.op_empty(ps), ((p / PAIRS) - 1) & 1, abort_flag))
+                                break;
+                            if (p >= SCP && !wait_or_abort(bars.sc_empty(p % SCP), ((p / SCP) - 1) & 1, abort_flag))
+                                break;
+                        }
                         // block lb: f16 d at byte 34*lb, 32 int8 codes at 34*lb + 2 (window-relative)
                         const int off = 34 * lb - 128 * h;
                         const uint32_t dbits =
@@ -300,48 +338,54 @@ __global__ void __launch_bounds__(THREADS, 1)
                             *reinterpret_cast<uint4*>(Bop + op_off(r, kq)) = v;
                         }
                         scbase[ss * BN + r] = h2f(dbits);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bars.op_full(os));
+                        if (b & 1) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bars.op_full(ps));
+                        }
                     }
                 }
             }
         }
-    } else {
+    } else if (warp >= EPI0) {
         // ------------------------------------------------------------ epilogue
-        const int e = warp - (2 + NUM_CONV_WARPS);  // 0..15
-        const int quad = warp & 3;                    // TMEM lane quadrant this warp may access
-        const int cg = e >> 2;                        // which 32 columns (tokens)
-        const int row = quad * 32 + lane;             // weight row within the tile
-        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const int e = warp - EPI0;        // 0..15
+        const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+        const int cg = e >> 2;            // which 32 columns (tokens)
+        const int row = quad * 32 + lane;  // weight row within the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cg * 32);
         uint64_t acc[16];  // running sums of tokens 2j, 2j+1 as packed f32 pairs
 #pragma unroll
         for (int j = 0; j < 16; j++) acc[j] = 0;
-        for (int b = 0; b < nb; b++) {
-            const int ac = b % NACC, ss = b % SC_SLOTS;
-            if (!wait_or_abort(bars.acc_full(ac), (b / NACC) & 1, abort_flag)) break;
+        for (int p = 0; p < nb / 2; p++) {
+            const int ap = p % ACC_PAIRS;
+            if (!wait_or_abort(bars.acc_full(ap), (p / ACC_PAIRS) & 1, abort_flag)) break;
             tc_fence_after();
-            const uint32_t dwb = __float_as_uint(scw[ss * BM + row]);
-            const uint64_t dw2 = f2_pack(dwb, dwb);
-            const uint64_t* dxs = reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
+#pragma unroll 1
+            for (int i = 0; i < 2; i++) {  // blocks 2p, 2p+1 in block order (not unrolled: registers)
+                const int ss = (2 * p + i) % SC_SLOTS, ac = 2 * ap + i;
+                const uint32_t dwb = __float_as_uint(scw[ss * BM + row]);
+                const uint64_t dw2 = f2_pack(dwb, dwb);
+                const uint64_t* dxs = reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
 #pragma unroll
-            for (int h = 0; h < 2; h++) {
-                uint32_t v[16];
-                tmem_ld16(lane_base + (uint32_t)(ac * BN + cg * 32 + 16 * h), v);
-                tmem_ld_wait();
-                if (h == 1) {  // the block's sums are in registers: the accumulator may be reused
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bars.acc_empty(ac));
-                }
+                for (int h = 0; h < 2; h++) {
+                    uint32_t v[16];
+                    tmem_ld16(lane_base + (uint32_t)(ac * BN + 16 * h), v);
+                    tmem_ld_wait();
+                    if (i == 1 && h == 1) {  // both blocks' sums are in registers: the accumulators may be reused
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.acc_empty(ap));
+                    }
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const uint64_t sc = f2_mul(dw2, dxs[8 * h + j]);  // (d_w*d_x[t], d_w*d_x[t+1])
-                    acc[8 * h + j] = f2_fma(f2_pack(v[2 * j], v[2 * j + 1]), sc, acc[8 * h + j]);
+                    for (int j = 0; j < 8; j++) {
+                        const uint64_t sc = f2_mul(dw2, dxs[8 * h + j]);  // (d_w*d_x[t], d_w*d_x[t+1])
+                        acc[8 * h + j] = f2_fma(f2_pack(v[2 * j], v[2 * j + 1]), sc, acc[8 * h + j]);
+                    }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.sc_empty(ss));
+            if (lane == 0) mbar_arrive(bars.sc_empty(p % SCP));
         }
         if (pdl) pdl_wait();  // Y may be read or written by the previous kernel
         const int o = o0 + row;
