@@ -567,20 +567,22 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
         pre["M=%d" % M] = {"us": round(t * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
                            "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4),
                            "frac_hbm_weight_stream": round(W.numel() / t / 1e9 / hbm, 4)}
-    # Q8_0 weights on the same prefill kernel (the weight converter takes the activation converter's path)
+    # the other 32-value weight formats on the same prefill kernel
     M = 512
-    W8 = quantized_weights("q8_0", N, K, cfg["seed"])
     x = to_dev(workloads.activations_f32(M, K, cfg["seed"] + M))
     xq = torch.empty(M * qmm.qmm_row_bytes("q8_0", K), dtype=torch.uint8, device=dev)
     Y = torch.empty(M, N, dtype=torch.float32, device=dev)
     with torch.cuda.stream(stream):
         qmm.qmm_quantize_q8_0(x, xq, M, K, stream=sh)
-    t = timed_graph(lambda i: qmm.matmul("q8_0", W8, xq, Y, M, N, K, stream=sh), 2)
-    tops = 2.0 * M * N * K / t / 1e12
-    pre["q8_0_weights_M=512"] = {"us": round(t * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
-                                 "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4),
-                                 "frac_hbm_weight_stream": round(W8.numel() / t / 1e9 / hbm, 4)}
-    del W8, x, xq, Y
+    for wtype in ("q8_0", "q4_1", "q5_0", "q5_1"):
+        W8 = quantized_weights(wtype, N, K, cfg["seed"])
+        t = timed_graph(lambda i: qmm.matmul(wtype, W8, xq, Y, M, N, K, stream=sh), 2)
+        tops = 2.0 * M * N * K / t / 1e12
+        pre["%s_weights_M=512" % wtype] = {"us": round(t * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
+                                           "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4),
+                                           "frac_hbm_weight_stream": round(W8.numel() / t / 1e9 / hbm, 4)}
+        del W8
+    del x, xq, Y
     # the K-quant prefill at the decoder layer's shapes (M = 512): W_gate/W_up (Q4_K), W_down (Q6_K),
     # and the Q2_K matrix
     kq = {}

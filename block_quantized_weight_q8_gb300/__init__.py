@@ -59,6 +59,9 @@ SIGNATURES = {
     "qmm_linear_q5_K": ("pppspiiiq", ctypes.c_int),
     "qmm_matmul_q4_0": ("pppiiiq", ctypes.c_int),
     "qmm_matmul_q8_0": ("pppiiiq", ctypes.c_int),
+    "qmm_matmul_q4_1": ("pppiiiq", ctypes.c_int),
+    "qmm_matmul_q5_0": ("pppiiiq", ctypes.c_int),
+    "qmm_matmul_q5_1": ("pppiiiq", ctypes.c_int),
     "qmm_get_rows": ("tpppiiiq", ctypes.c_int),
     "qmm_linear_host": ("tppppsppiiiq", ctypes.c_int),
     "qmm_rmsnorm_quantize": ("tppfpiiq", ctypes.c_int),
@@ -283,7 +286,8 @@ def qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=None):
 
 
 def matmul(wtype, W, xq, Y, M, N, K, stream=None):
-    """qmm_matmul_<wtype>: Y[M][N] for M quantized activation rows (Q8_0 for q4_0, Q8_K for the K-quants)."""
+    """qmm_matmul_<wtype>: Y[M][N] for M quantized activation rows (Q8_0 for the 32-value formats, Q8_K for
+    the K-quants)."""
     _call("qmm_matmul_" + wtype, ptr(W), ptr(xq), ptr(Y), int(M), int(N), int(K), stream_handle(stream))
 
 

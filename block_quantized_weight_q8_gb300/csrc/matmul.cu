@@ -72,16 +72,23 @@ __device__ __forceinline__ int converter_index(int warp) {  // 0..7, or -1 for o
     return (warp >= 2 && warp < EPI0 && warp != 5 && warp != 9) ? warp - 2 - (warp > 5) - (warp > 9) : -1;
 }
 
+// Weight block bytes of the 32-value formats (Q4_0 18, Q8_0 34, Q4_1 20, Q5_0 22, Q5_1 24).
+__host__ __device__ constexpr int block_bytes32(int wt) {
+    return wt == QMM_Q8_0 ? 34 : wt == QMM_Q4_1 ? 20 : wt == QMM_Q5_0 ? 22 : wt == QMM_Q5_1 ? 24 : 18;
+}
+
 // Shared memory layout per weight format (offsets from the 1024-byte aligned
-// dynamic shared memory base).  Q4_0 weight blocks are 18 bytes, Q8_0 34; the
-// larger raw stages of Q8_0 leave room for 16 scale slots instead of 32.  (A
-// third operand pair for Q4_0, in place of 16 scale slots, measured no faster.)
+// dynamic shared memory base).  Q4_0 keeps 32 scale slots; the larger raw stages
+// of the other formats leave room for 16.  (A third operand pair for Q4_0, in
+// place of 16 scale slots, measured no faster.)  Q4_1 and Q5_1 also carry each
+// row's m_w and each token's d_x * sum(a) per block, for the min term.
 template <int WT>
 struct Lay {
-    static constexpr int WB = WT == QMM_Q8_0 ? 34 : 18;
+    static constexpr int WB = block_bytes32(WT);
+    static constexpr bool HAS_MIN = WT == QMM_Q4_1 || WT == QMM_Q5_1;
     static constexpr int PAIRS = 2;                             // operand pair slots (converted blocks in flight / 2)
     static constexpr int OPS = 2 * PAIRS;
-    static constexpr int SC_SLOTS = WT == QMM_Q8_0 ? 16 : 32;  // block scales in flight (outlive the operands)
+    static constexpr int SC_SLOTS = WT == QMM_Q4_0 ? 32 : 16;  // block scales in flight (outlive the operands)
     static constexpr int SCP = SC_SLOTS / 2;                   // ... in pairs
     static constexpr int W_RAW = BM * KB * WB;
     static constexpr int RAW_BYTES = W_RAW + X_RAW;
@@ -90,13 +97,18 @@ struct Lay {
     static constexpr int OFF_OPB = OFF_OPA + OPS * OP_A;
     static constexpr int OFF_SCW = OFF_OPB + OPS * OP_B;
     static constexpr int OFF_SCX = OFF_SCW + SC_SLOTS * BM * 4;
-    static constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;
+    static constexpr int OFF_SCM = OFF_SCX + SC_SLOTS * BN * 4;            // m_w per row (min formats)
+    static constexpr int OFF_SCS = OFF_SCM + (HAS_MIN ? SC_SLOTS * BM * 4 : 0);  // d_x * sum(a) per token
+    static constexpr int OFF_BAR = OFF_SCS + (HAS_MIN ? SC_SLOTS * BN * 4 : 0);
     // barriers: raw_full[2] raw_empty[2] op_full[PAIRS] op_empty[PAIRS] acc_full[2] acc_empty[2] sc_empty[SCP]
     static constexpr int NBARS = 2 * RAW_STAGES + 2 * PAIRS + 2 * ACC_PAIRS + SCP;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM + 16;
 };
-static_assert(Lay<QMM_Q4_0>::SMEM_BYTES <= 232448 && Lay<QMM_Q8_0>::SMEM_BYTES <= 232448, "prefill smem");
+static_assert(Lay<QMM_Q4_0>::SMEM_BYTES <= 232448 && Lay<QMM_Q8_0>::SMEM_BYTES <= 232448 &&
+                  Lay<QMM_Q4_1>::SMEM_BYTES <= 232448 && Lay<QMM_Q5_0>::SMEM_BYTES <= 232448 &&
+                  Lay<QMM_Q5_1>::SMEM_BYTES <= 232448,
+              "prefill smem");
 static_assert(KB % 4 == 0, "pairs must not straddle the activation converter's 4-block windows");
 
 struct Bars {
@@ -149,6 +161,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_TMEM + 8);
     const float* scw = reinterpret_cast<const float*>(smem + L::OFF_SCW);
     const float* scx = reinterpret_cast<const float*>(smem + L::OFF_SCX);
+    const float* scm = reinterpret_cast<const float*>(smem + L::OFF_SCM);
+    const float* scs = reinterpret_cast<const float*>(smem + L::OFF_SCS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int o0 = blockIdx.x * BM, t0 = blockIdx.y * BN;
@@ -243,8 +257,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint4 v = src[i];
                     raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.raw_empty(s));
 #pragma unroll
                 for (int lb = 0; lb < KB; lb++) {
                     const int b = c * KB + lb, p = b >> 1, ps = p % PAIRS, os = 2 * ps + (b & 1), ss = b % SC_SLOTS;
@@ -284,6 +296,84 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (lane == 0) mbar_arrive(bars.op_full(ps));
                     }
                 }
+            } else if (is_w && (WT == QMM_Q4_1 || WT == QMM_Q5_0 || WT == QMM_Q5_1)) {
+                // this weight row's 8 blocks (160, 176 or 192 bytes, 16-byte aligned), read as two
+                // windows of 4 blocks starting at the 16-byte boundary at or below each window's
+                // first byte.  Q4_1: d, m, qs@4; Q5_0: d, qh@2, qs@6; Q5_1: d, m, qh@4, qs@8;
+                // element j is the low nibble of qs[j], element j+16 the high one, and bit e of
+                // qh is element e's fifth bit.
+                constexpr int OFF_Q = WT == QMM_Q4_1 ? 4 : WT == QMM_Q5_0 ? 6 : 8;
+                constexpr int OFF_H = WT == QMM_Q5_0 ? 2 : 4;
+                constexpr bool FIVE = WT != QMM_Q4_1;
+                // fp16 bits of (1024 + byte) minus 1024 (codes 0..31) or 1040 (Q5_0: code - 16)
+                constexpr uint32_t magic = WT == QMM_Q5_0 ? 0x64106410u : 0x64006400u;
+                const uint8_t* rowp = smem + L::OFF_RAW + s * RAW_BYTES + r * (KB * WB);
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int start = 4 * WB * h, base16 = start & ~15, off0 = start - base16;
+                    const int nv = (off0 + 4 * WB + 15) / 16;  // 16-byte loads: 5 or 6
+                    uint32_t raw[25];
+                    raw[24] = 0;
+                    const uint4* src = reinterpret_cast<const uint4*>(rowp + base16);
+#pragma unroll
+                    for (int i = 0; i < 6; i++) {
+                        if (i < nv) {
+                            const uint4 v = src[i];
+                            raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
+                        } else {
+                            raw[4 * i] = raw[4 * i + 1] = raw[4 * i + 2] = raw[4 * i + 3] = 0;
+                        }
+                    }
+#pragma unroll
+                    for (int lq = 0; lq < KB / 2; lq++) {
+                        const int lb = 4 * h + lq;
+                        const int b = c * KB + lb, p = b >> 1, ps = p % PAIRS, os = 2 * ps + (b & 1),
+                                  ss = b % SC_SLOTS;
+                        if ((b & 1) == 0) {
+                            if (p >= PAIRS &&
+                                !wait_or_abort(bars.op_empty(ps), ((p / PAIRS) - 1) & 1, abort_flag))
+                                break;
+                            if (p >= SCP && !wait_or_abort(bars.sc_empty(p % SCP), ((p / SCP) - 1) & 1, abort_flag))
+                                break;
+                        }
+                        const int off = off0 + WB * lq;  // the block's first byte in the window
+                        auto word_at = [&](int o) -> uint32_t {
+                            return (o % 4 == 0) ? raw[o / 4] : __funnelshift_r(raw[o / 4], raw[o / 4 + 1], 8 * (o % 4));
+                        };
+                        const uint32_t dm = word_at(off);  // d in the low half, m (Q4_1, Q5_1) in the high half
+                        const uint32_t qh = FIVE ? word_at(off + OFF_H) : 0u;
+                        uint32_t lo[4], hi[4];
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const uint32_t q = word_at(off + OFF_Q + 4 * i);
+                            lo[i] = q & 0x0F0F0F0Fu;
+                            hi[i] = (q >> 4) & 0x0F0F0F0Fu;
+                            if (FIVE) {
+                                lo[i] |= spread4(qh >> (4 * i)) << 4;
+                                hi[i] |= spread4(qh >> (16 + 4 * i)) << 4;
+                            }
+                        }
+                        uint8_t* A = smem + L::OFF_OPA + os * OP_A;
+#pragma unroll
+                        for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7
+                            const uint32_t w0 = kq < 2 ? lo[2 * kq] : hi[2 * (kq - 2)];
+                            const uint32_t w1 = kq < 2 ? lo[2 * kq + 1] : hi[2 * (kq - 2) + 1];
+                            uint4 v;
+                            v.x = h2_sub(bytes_to_h2(w0, 0x5140), magic);
+                            v.y = h2_sub(bytes_to_h2(w0, 0x7362), magic);
+                            v.z = h2_sub(bytes_to_h2(w1, 0x5140), magic);
+                            v.w = h2_sub(bytes_to_h2(w1, 0x7362), magic);
+                            *reinterpret_cast<uint4*>(A + op_off(r, kq)) = v;
+                        }
+                        reinterpret_cast<float*>(smem + L::OFF_SCW)[ss * BM + r] = h2f(dm & 0xFFFFu);
+                        if (L::HAS_MIN) reinterpret_cast<float*>(smem + L::OFF_SCM)[ss * BM + r] = h2f(dm >> 16);
+                        if (b & 1) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bars.op_full(ps));
+                        }
+                    }
+                }
             } else {
                 // this token's (or Q8_0 weight row's) 8 blocks: 272 bytes, 16-byte aligned,
                 // read as two windows of 144 bytes (bytes 0..143 hold blocks 0-3, bytes
@@ -299,10 +389,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int i = 0; i < 9; i++) {
                         const uint4 v = src[i];
                         raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
-                    }
-                    if (h == 1) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bars.raw_empty(s));
                     }
 #pragma unroll
                     for (int lq = 0; lq < KB / 2; lq++) {
@@ -323,13 +409,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint32_t m128 = 0x64806480u;  // (1152, 1152): 1024 + (a + 128) - 1152 = a
                         static_assert(OP_A == OP_B && BM == BN, "one converter for both operands");
                         uint8_t* Bop = opbase + os * OP_B;
+                        int asum = 0;  // sum of the block's codes (min formats: the token's m_w term)
 #pragma unroll
                         for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7: code words 2kq, 2kq+1
                             const int q0 = off + 2 + 8 * kq, q1 = q0 + 4;
-                            const uint32_t w0 =
-                                __funnelshift_r(raw[q0 / 4], raw[q0 / 4 + 1], 8 * (q0 % 4)) ^ 0x80808080u;
-                            const uint32_t w1 =
-                                __funnelshift_r(raw[q1 / 4], raw[q1 / 4 + 1], 8 * (q1 % 4)) ^ 0x80808080u;
+                            const uint32_t c0 = __funnelshift_r(raw[q0 / 4], raw[q0 / 4 + 1], 8 * (q0 % 4));
+                            const uint32_t c1 = __funnelshift_r(raw[q1 / 4], raw[q1 / 4 + 1], 8 * (q1 % 4));
+                            if (L::HAS_MIN) asum = __dp4a((int)c1, 0x01010101, __dp4a((int)c0, 0x01010101, asum));
+                            const uint32_t w0 = c0 ^ 0x80808080u, w1 = c1 ^ 0x80808080u;
                             uint4 v;
                             v.x = h2_sub(bytes_to_h2(w0, 0x5140), m128);
                             v.y = h2_sub(bytes_to_h2(w0, 0x7362), m128);
@@ -338,6 +425,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             *reinterpret_cast<uint4*>(Bop + op_off(r, kq)) = v;
                         }
                         scbase[ss * BN + r] = h2f(dbits);
+                        if (L::HAS_MIN && !is_w)
+                            reinterpret_cast<float*>(smem + L::OFF_SCS)[ss * BN + r] = h2f(dbits) * (float)asum;
                         if (b & 1) {
                             fence_proxy_async_smem();
                             __syncwarp();
@@ -346,6 +435,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
+            // The raw stage goes back to the producer only once every value read from it
+            // has been used: released right after the loads, the next chunk's TMA was seen
+            // to overwrite a window whose loads the weight converter had just issued.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.raw_empty(s));
         }
     } else if (warp >= EPI0) {
         // ------------------------------------------------------------ epilogue
@@ -367,6 +461,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t dwb = __float_as_uint(scw[ss * BM + row]);
                 const uint64_t dw2 = f2_pack(dwb, dwb);
                 const uint64_t* dxs = reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
+                // min formats: y += m_w * (d_x * sum(a)) after the block's value term
+                const uint32_t mwb = L::HAS_MIN ? __float_as_uint(scm[ss * BM + row]) : 0u;
+                const uint64_t mw2 = f2_pack(mwb, mwb);
+                const uint64_t* css = reinterpret_cast<const uint64_t*>(scs + ss * BN + cg * 32);
 #pragma unroll
                 for (int h = 0; h < 2; h++) {
                     uint32_t v[16];
@@ -381,6 +479,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int j = 0; j < 8; j++) {
                         const uint64_t sc = f2_mul(dw2, dxs[8 * h + j]);  // (d_w*d_x[t], d_w*d_x[t+1])
                         acc[8 * h + j] = f2_fma(f2_pack(v[2 * j], v[2 * j + 1]), sc, acc[8 * h + j]);
+                        if (L::HAS_MIN) acc[8 * h + j] = f2_fma(mw2, css[8 * h + j], acc[8 * h + j]);
                     }
                 }
             }
@@ -500,18 +599,24 @@ qmm_status matmul_q8_0_launch(const void* W, const void* xq, float* Y, int64_t M
 // Whether an M-token multiply of this weight type takes a tensor-core prefill
 // kernel (after one quantization of all M rows) rather than a launch per token.
 // Q4_0 takes it for every M > 1 (its launcher runs per-token matvecs itself on
-// shapes the tiles do not take); Q8_0 only on shapes the tiles take.
+// shapes the tiles do not take); the other 32-value formats only on shapes the
+// tiles take.
 bool prefill_on_tensor_cores(int wt, int64_t M, int64_t K) {
     if (wt == QMM_Q4_0) return M > 1;
-    if (wt == QMM_Q8_0) return M > 1 && tensor_core_shape(M, K);
+    if (wt == QMM_Q8_0 || wt == QMM_Q4_1 || wt == QMM_Q5_0 || wt == QMM_Q5_1) return M > 1 && tensor_core_shape(M, K);
     return kq_uses_tensor_cores(wt, M, K);
 }
 
 qmm_status prefill_launch(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                           cudaStream_t stream, bool pdl) {
-    if (wt == QMM_Q4_0) return matmul_q_launch<QMM_Q4_0>(W, xq, Y, M, N, K, stream, pdl);
-    if (wt == QMM_Q8_0) return matmul_q_launch<QMM_Q8_0>(W, xq, Y, M, N, K, stream, pdl);
-    return matmul_kq_launch(wt, W, xq, Y, M, N, K, stream, pdl);
+    switch (wt) {
+    case QMM_Q4_0: return matmul_q_launch<QMM_Q4_0>(W, xq, Y, M, N, K, stream, pdl);
+    case QMM_Q8_0: return matmul_q_launch<QMM_Q8_0>(W, xq, Y, M, N, K, stream, pdl);
+    case QMM_Q4_1: return matmul_q_launch<QMM_Q4_1>(W, xq, Y, M, N, K, stream, pdl);
+    case QMM_Q5_0: return matmul_q_launch<QMM_Q5_0>(W, xq, Y, M, N, K, stream, pdl);
+    case QMM_Q5_1: return matmul_q_launch<QMM_Q5_1>(W, xq, Y, M, N, K, stream, pdl);
+    default: return matmul_kq_launch(wt, W, xq, Y, M, N, K, stream, pdl);
+    }
 }
 
 }  // namespace qmm
@@ -529,13 +634,30 @@ qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, i
     return matmul_q4_0_launch(W, xq, Y, M, N, K, (cudaStream_t)stream, true);
 }
 
-qmm_status qmm_matmul_q8_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                           qmm_stream_t stream) {
+static qmm_status matmul_public(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                                qmm_stream_t stream) {
     if (!W || !xq || !Y) return QMM_E_NULL;
-    qmm_status st = check_shape(QMM_Q8_0, M, N, K);
+    qmm_status st = check_shape(wt, M, N, K);
     if (st != QMM_OK) return st;
     if (!aligned16(W) || !aligned16(xq) || !aligned16(Y)) return QMM_E_ALIGN;
-    return matmul_q8_0_launch(W, xq, Y, M, N, K, (cudaStream_t)stream, true);
+    return prefill_launch(wt, W, xq, Y, M, N, K, (cudaStream_t)stream, true);
+}
+
+qmm_status qmm_matmul_q8_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_public(QMM_Q8_0, W, xq, Y, M, N, K, stream);
+}
+qmm_status qmm_matmul_q4_1(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_public(QMM_Q4_1, W, xq, Y, M, N, K, stream);
+}
+qmm_status qmm_matmul_q5_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_public(QMM_Q5_0, W, xq, Y, M, N, K, stream);
+}
+qmm_status qmm_matmul_q5_1(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_public(QMM_Q5_1, W, xq, Y, M, N, K, stream);
 }
 
 unsigned qmm_internal_matmul_error(int clear) {

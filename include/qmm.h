@@ -195,11 +195,12 @@ QMM_API qmm_status qmm_matvec_q5_K(const void* W, const void* xq, float* y, int6
  * A token row is quantized inside the multiply kernel (every CTA quantizes the
  * row it needs, with the same arithmetic as qmm_quantize_q8_0/q8_K, and one CTA
  * stores it to the scratch), so a token is one launch; a row too large for that
- * kernel's shared memory is quantized by the separate quantizer first.  Q4_0 and
- * Q8_0 with M >= 8 and K % 256 == 0, and Q4_K / Q6_K / Q2_K / Q5_K with M >= 8
- * and K % 2048 == 0, quantize all rows, then run the prefill matmul (Q4_0 with
- * 1 < M < 8 also quantizes all rows first, then multiplies token by token).  The
- * other types multiply token by token at every M. */
+ * kernel's shared memory is quantized by the separate quantizer first.  The
+ * 32-value formats (Q4_0, Q8_0, Q4_1, Q5_0, Q5_1) with M >= 8 and K % 256 == 0,
+ * and Q4_K / Q6_K / Q2_K / Q5_K with M >= 8 and K % 2048 == 0, quantize all rows,
+ * then run the prefill matmul (Q4_0 with 1 < M < 8 also quantizes all rows
+ * first, then multiplies token by token).  Other shapes multiply token by
+ * token. */
 QMM_API qmm_status qmm_linear_q4_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
                            int64_t M, int64_t N, int64_t K, qmm_stream_t stream);
 QMM_API qmm_status qmm_linear_q8_0(const void* W, const float* x, void* xq_scratch, size_t scratch_bytes, float* y,
@@ -287,8 +288,8 @@ QMM_API qmm_status qmm_linear_group(int wtype, int G, const void* const* W, cons
  * qmm_linear_norm: qmm_linear_group on the normed rows (G = 1 for one matrix),
  * the quantized normed rows left in the scratch.  A decode token is one launch
  * (every CTA norms and quantizes the row itself); a prefill that takes the
- * tensor-core matmul (Q4_0 with M > 1; Q8_0 with M >= 8 and K % 256 == 0;
- * Q4_K/Q6_K/Q2_K/Q5_K with M >= 8 and K % 2048 == 0)
+ * tensor-core matmul (Q4_0 with M > 1; Q8_0/Q4_1/Q5_0/Q5_1 with M >= 8 and
+ * K % 256 == 0; Q4_K/Q6_K/Q2_K/Q5_K with M >= 8 and K % 2048 == 0)
  * norms and quantizes all rows first.  Errors as for qmm_linear_group, plus
  * QMM_E_NULL for w. */
 QMM_API qmm_status qmm_rmsnorm_quantize(int act, const float* x, const float* w, float eps, void* xq, int64_t M,
@@ -303,13 +304,23 @@ QMM_API qmm_status qmm_linear_norm(int wtype, int G, const void* const* W, const
  * "Batched prompt prefill"; [kvad] "Batched prefill, and i8mm").  The integer
  * block sums run on the tensor cores with integer-valued operands (exact), and
  * each 32-wide block's sum is rescaled into fp32 by d_w*d_x.
- * W: N rows of Q4_0 (or Q8_0); xq: [M][K/32] Q8_0 blocks; Y: f32 [M][N].
- * K a multiple of 256 and M >= 8 take this path; other shapes run one matvec
- * per token (same results as qmm_matvec).  Q8_0 x Q8_0 block sums reach
- * 32 * 127 * 127 < 2^24, still exact in the fp32 accumulator. */
+ * W: N rows of Q4_0 (or Q8_0, Q4_1, Q5_0, Q5_1); xq: [M][K/32] Q8_0 blocks;
+ * Y: f32 [M][N].  K a multiple of 256 and M >= 8 take this path; other shapes
+ * run one matvec per token (same results as qmm_matvec).  Q8_0 x Q8_0 block sums
+ * reach 32 * 127 * 127 < 2^24 and five-bit ones 32 * 31 * 127, exact in the fp32
+ * accumulator.  Q4_1 and Q5_1 add each block's min term after its value term:
+ * y += (d_w*d_x) * isum; y += m_w * (d_x * sum(a)), with sum(a) the exact
+ * integer sum of the token's block codes.  Results agree with the scalar order
+ * within 1e-5 of the row's L2 norm. */
 QMM_API qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream);
 QMM_API qmm_status qmm_matmul_q8_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream);
+QMM_API qmm_status qmm_matmul_q4_1(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream);
+QMM_API qmm_status qmm_matmul_q5_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream);
+QMM_API qmm_status qmm_matmul_q5_1(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream);
 /* The same for the K-quants against Q8_K rows ([minfer] s3.2, the K-quant dot
  * walked; [ggml] s1.2).  Per 256-value super-block the integer value term

@@ -204,12 +204,12 @@ def test_linear_matches_quantize_then_matvec(wtype, M):
 
 
 # ------------------------------------------------------------------ prefill matmul
-@pytest.mark.parametrize("wtype", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("wtype", ["q4_0", "q8_0", "q4_1", "q5_0", "q5_1"])
 @pytest.mark.parametrize("M,N,K", [(1, 64, 256), (3, 100, 512), (17, 300, 1024), (128, 256, 4096),
                                    (130, 390, 2048), (8, 129, 256), (255, 17, 768)])
 def test_matmul_q_matches_oracle(wtype, M, N, K):
-    """The 32-value-block prefill (Q4_0 or Q8_0 weights x Q8_0 rows): several tiles in both directions,
-    ragged last tiles of rows and tokens, a single output row, and the per-token fallback shapes."""
+    """The 32-value-block prefill (Q4_0, Q8_0, Q4_1, Q5_0 or Q5_1 weights x Q8_0 rows): several tiles in
+    both directions, ragged last tiles of rows and tokens, and the per-token fallback shapes."""
     W, X = make_inputs(wtype, M, N, K, seed=9000 + M)
     ref = oracle.matmul(wtype, W, X, M, N, K, nthreads=8)
     Y = f32(M, N)
@@ -217,51 +217,63 @@ def test_matmul_q_matches_oracle(wtype, M, N, K):
     assert_rows_close(host(Y), ref)
 
 
+# integer weight ranges whose quantization gives d = 1 (and m = 0) exactly, codes equal to the values,
+# given the extremes each block is forced to hold
+INT_RANGES = {"q8_0": (-127, 127, (127, -127)), "q5_0": (-16, 15, (-16,)), "q4_1": (0, 15, (0, 15)),
+              "q5_1": (0, 31, (0, 31))}
+
+
+@pytest.mark.parametrize("wtype", ["q8_0", "q5_0", "q4_1", "q5_1"])
 @pytest.mark.parametrize("M,N,K", [(8, 128, 256), (130, 300, 1024)])
-def test_matmul_q8_0_integer_sums_exact(M, N, K):
-    """Integer-valued rows with a +-127 in every block quantize to d = 1 and codes equal to the values,
-    so Y is the plain integer matrix product (at most 1024 * 127 * 127 < 2^24: exact in f32) and must
-    match it bit for bit: each block's sum of 32 products up to 127 * 127 is exact on the tensor cores."""
+def test_matmul_integer_sums_exact(wtype, M, N, K):
+    """Integer-valued rows quantize to d = 1 (m = 0) with codes equal to the values (weights: the format's
+    code range with its extremes in every block; activations: -127..127 with a +-127 in every block), so
+    Y is the plain integer matrix product (at most 1024 * 127 * 127 < 2^24: exact in f32) and must match
+    it bit for bit: each block's sum of 32 products is exact on the tensor cores."""
+    lo, hi, ext = INT_RANGES[wtype]
     g = np.random.default_rng(77 + M)
-    w = g.integers(-127, 128, size=(N, K)).astype(np.float32)
+    w = g.integers(lo, hi + 1, size=(N, K)).astype(np.float32)
     x = g.integers(-127, 128, size=(M, K)).astype(np.float32)
-    w[:, ::32] = np.where(g.random((N, K // 32)) < 0.5, 127.0, -127.0)
+    for i, e in enumerate(ext):  # the extremes at the start of every block (the first max-|x| wins)
+        w[:, i::32] = e
     x[:, ::32] = np.where(g.random((M, K // 32)) < 0.5, 127.0, -127.0)
-    w[0, :] = 127.0  # the largest block sums, both signs
+    w[0, len(ext):] = hi if abs(hi) >= abs(lo) else lo  # the largest block sums, both signs
     x[0, :] = 127.0
     x[1, :] = -127.0
-    W = oracle.quantize("q8_0", w)
+    W = oracle.quantize(wtype, w)
     X = oracle.quantize("q8_0", x)
+    assert np.array_equal(oracle.get_rows(wtype, W, np.arange(N, dtype=np.int32), K), w)  # d = 1, codes = values
     want = (x.astype(np.int64) @ w.astype(np.int64).T).astype(np.float32)
     Y = f32(M, N)
-    qmm.matmul("q8_0", dev(W), dev(X), Y, M, N, K)
+    qmm.matmul(wtype, dev(W), dev(X), Y, M, N, K)
     assert np.array_equal(host(Y), want)
     # and through the quantize + multiply entry point, with the GPU quantizer
     Y2 = f32(M, N)
     xrb = qmm.qmm_row_bytes("q8_0", K)
     scratch = u8(M * xrb)
-    qmm.linear("q8_0", dev(W), dev(x), scratch, scratch.numel(), Y2, M, N, K)
+    qmm.linear(wtype, dev(W), dev(x), scratch, scratch.numel(), Y2, M, N, K)
     assert np.array_equal(host(scratch), X.reshape(-1))
     assert np.array_equal(host(Y2), want)
 
 
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_1", "q5_0", "q5_1"])
 @pytest.mark.parametrize("M", [8, 64])
-def test_linear_q8_0_prefill_route(M):
-    """qmm_linear_q8_0 with M >= 8 quantizes all rows, then runs the prefill: bit for bit the same as
-    qmm_quantize_q8_0 followed by qmm_matmul_q8_0."""
+def test_linear_prefill_route(wtype, M):
+    """qmm_linear_<w> with M >= 8 quantizes all rows, then runs the prefill: bit for bit the same as
+    qmm_quantize_q8_0 followed by qmm_matmul_<w>."""
     N, K = 300, 2048
-    W, _ = make_inputs("q8_0", 1, N, K, seed=4242)
+    W, _ = make_inputs(wtype, 1, N, K, seed=4242)
     x = workloads.activations_f32(M, K, seed=4243)
     Wd, xd = dev(W), dev(x)
     xrb = qmm.qmm_row_bytes("q8_0", K)
     s1, s2 = u8(M * xrb), u8(M * xrb)
     y1, y2 = f32(M, N), f32(M, N)
-    qmm.linear("q8_0", Wd, xd, s1, s1.numel(), y1, M, N, K)
+    qmm.linear(wtype, Wd, xd, s1, s1.numel(), y1, M, N, K)
     qmm.qmm_quantize_q8_0(xd, s2, M, K)
-    qmm.matmul("q8_0", Wd, s2, y2, M, N, K)
+    qmm.matmul(wtype, Wd, s2, y2, M, N, K)
     assert np.array_equal(host(s1), host(s2))
     assert np.array_equal(host(y1).view(np.uint32), host(y2).view(np.uint32))
-    assert_rows_close(host(y1), oracle.matmul("q8_0", W, oracle.quantize("q8_0", x), M, N, K, nthreads=8))
+    assert_rows_close(host(y1), oracle.matmul(wtype, W, oracle.quantize("q8_0", x), M, N, K, nthreads=8))
 
 
 # ------------------------------------------------------------------ full workload sizes
@@ -304,7 +316,8 @@ def test_full_size_layer_set():
         assert_rows_close(host(y), ref)
 
 
-@pytest.mark.parametrize("wtype,M", [("q4_0", 128), ("q4_0", 512), ("q4_0", 2048), ("q8_0", 512)])
+@pytest.mark.parametrize("wtype,M", [("q4_0", 128), ("q4_0", 512), ("q4_0", 2048), ("q8_0", 512), ("q4_1", 512),
+                                     ("q5_0", 512), ("q5_1", 512)])
 def test_full_size_prefill_sampled(wtype, M):
     cfg = workloads.WORKLOADS["q4_0_prefill_512x12288x4096"]
     N, K = cfg["N"], cfg["K"]
