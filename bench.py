@@ -333,8 +333,9 @@ def run_gpu(args, rank, local_rank, world):
     e2e_value, _ = aggregate(wbytes * e2e_steps, e2e_secs, world, dev)
     e2e = {"value": round(e2e_value / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": 4 * K,
            "d2h_bytes_per_step": 4 * N, "steps": e2e_steps,
-           "note": "qmm_linear_host per step (pinned x in, quantize + multiply, y out, one stream), "
-                   "eager calls through the binding, host copies inside the timed region"}
+           "note": "qmm_linear_host per step, eager calls through the binding: x (16 KB) read from pinned host "
+                   "memory by the quantize kernel over the host link, the multiply, y (48 KB) written by it into "
+                   "pinned host memory; both transfers inside the timed region, one stream"}
     del Ws, W0
 
     # ---------------- other workloads

@@ -154,6 +154,21 @@ static qmm_status linear_norm(int wt, int G, const void* const* W, const int64_t
     return QMM_OK;
 }
 
+// The device address of a pinned (page-locked, mapped) host buffer, or null for
+// pageable, managed or device memory.
+static const void* mapped_host(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the error this query may leave behind
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Outputs (M * N f32 values) up to which qmm_linear_host writes y straight into
+// the caller's pinned host buffer: 256 KB.
+constexpr int64_t kDirectHostOutputs = 65536;
+
 }  // namespace qmm
 
 using namespace qmm;
@@ -171,16 +186,37 @@ qmm_status qmm_linear_group(int wtype, int G, const void* const* W, const int64_
 unsigned qmm_internal_matmul_error(int clear);
 
 // qmm_linear_<wtype> with host buffers: x from the caller's (pinned) host
-// memory in, y back out, both copies and the multiply queued on one stream.
+// memory in, y back out, all queued on one stream.
 qmm_status qmm_linear_host(int wtype, const void* W, const float* x_host, float* x_dev, void* xq_scratch,
                            size_t scratch_bytes, float* y_dev, float* y_host, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
     if (!x_host || !y_host) return QMM_E_NULL;
     qmm_status st = check_shape(wtype, M, N, K);
     if (st != QMM_OK) return st;
-    if (act_type_of(wtype) < 0) return QMM_E_TYPE;
-    if (!x_dev || !y_dev) return QMM_E_NULL;
+    const int act = act_type_of(wtype);
+    if (act < 0) return QMM_E_TYPE;
     cudaStream_t cs = (cudaStream_t)stream;
+    // Pinned host buffers are mapped into the device's address space: for a small
+    // output the quantizer reads x over the host link and the multiply writes y
+    // there, with no copy-engine transfer (each of which costs several
+    // microseconds of latency on the stream for a few kilobytes).
+    const float* xm = static_cast<const float*>(mapped_host(x_host));
+    float* ym = static_cast<float*>(const_cast<void*>(mapped_host(y_host)));
+    if (xm && ym && M * N <= kDirectHostOutputs && aligned16(xm) && aligned16(ym)) {
+        if (!W || !xq_scratch) return QMM_E_NULL;
+        if (!aligned16(W) || !aligned16(xq_scratch)) return QMM_E_ALIGN;
+        const size_t xrb = row_bytes_of(act, K);
+        if (scratch_bytes < (size_t)M * xrb) return QMM_E_SCRATCH;
+        st = quantize_act_launch(act, xm, xq_scratch, M, K, cs, true);
+        if (st != QMM_OK) return st;
+        if (prefill_on_tensor_cores(wtype, M, K)) return prefill_launch(wtype, W, xq_scratch, ym, M, N, K, cs, true);
+        for (int64_t t = 0; t < M; t++) {
+            st = matvec_dispatch(wtype, W, (const uint8_t*)xq_scratch + t * xrb, ym + t * N, N, K, cs, true);
+            if (st != QMM_OK) return st;
+        }
+        return QMM_OK;
+    }
+    if (!x_dev || !y_dev) return QMM_E_NULL;
     if (cudaMemcpyAsync(x_dev, x_host, (size_t)M * (size_t)K * sizeof(float), cudaMemcpyHostToDevice, cs) !=
         cudaSuccess)
         return QMM_E_CUDA;

@@ -222,12 +222,18 @@ QMM_API qmm_status qmm_linear_q5_K(const void* W, const float* x, void* xq_scrat
 
 /* ---- quantize + multiply with host buffers -------------------------------- */
 /* qmm_linear_<wtype> for a caller whose input and output live in host memory:
- * copies x_host (f32 [M][K]) to x_dev, runs qmm_linear_<wtype> (x_dev, the
- * scratch and y_dev as there), and copies y_dev (f32 [M][N]) back to y_host, all
- * queued on the stream in that order (cudaMemcpyAsync; asynchronous only when
- * the host buffers are pinned).  The caller synchronizes the stream before it
- * reads y_host.  Errors as for qmm_linear_<wtype>; QMM_E_NULL for a null host
- * buffer; QMM_E_CUDA when a copy cannot be queued. */
+ * x_host (f32 [M][K]) in, y_host (f32 [M][N]) out, everything queued on the
+ * stream; the caller synchronizes the stream before it reads y_host.  Results
+ * equal qmm_linear_<wtype>'s bit for bit.
+ *   - Both host buffers pinned (page-locked and mapped, e.g. cudaHostAlloc),
+ *     16-byte aligned, and M * N <= 65536: the activation quantizer reads x_host
+ *     over the host link into the scratch and the multiply writes y_host
+ *     directly; x_dev and y_dev are not touched (they may be NULL).
+ *   - Otherwise: x_host is copied to x_dev, qmm_linear_<wtype> runs (x_dev, the
+ *     scratch and y_dev as there), and y_dev is copied back to y_host
+ *     (cudaMemcpyAsync; asynchronous only when the host buffers are pinned).
+ * Errors as for qmm_linear_<wtype>; QMM_E_NULL for a null host buffer (or a null
+ * x_dev / y_dev on the copying path); QMM_E_CUDA when a copy cannot be queued. */
 QMM_API qmm_status qmm_linear_host(int wtype, const void* W, const float* x_host, float* x_dev, void* xq_scratch,
                                    size_t scratch_bytes, float* y_dev, float* y_host, int64_t M, int64_t N, int64_t K,
                                    qmm_stream_t stream);

@@ -160,15 +160,21 @@ def test_get_rows_index_out_of_range_is_reported():
     assert qmm.qmm_device_status(clear=True) == 2   # QMM_E_SHAPE
 
 
-def test_linear_host_matches_linear():
-    """qmm_linear_host (pinned x in, the multiply, y out on one stream) gives qmm_linear_<w>'s result bit for bit."""
-    wtype, M, N, K = "q4_K", 2, 300, 4096
+@pytest.mark.parametrize("wtype,M,N,K,pinned", [("q4_K", 2, 300, 4096, True), ("q8_0", 1, 12288, 4096, True),
+                                                 ("q4_0", 16, 300, 1024, True), ("q8_0", 1, 70000, 256, True),
+                                                 ("q4_K", 2, 300, 4096, False)])
+def test_linear_host_matches_linear(wtype, M, N, K, pinned):
+    """qmm_linear_host (x in from host memory, the multiply, y out on one stream) gives qmm_linear_<w>'s result
+    bit for bit: pinned buffers with a small output take the direct path (the kernels read x and write y in
+    host memory), a large output or pageable buffers the copying one."""
     W = dev(oracle.quantize(wtype, workloads.weights_f32(N, K, seed=71)))
     x = workloads.activations_f32(M, K, seed=72)
-    x_host = torch.from_numpy(x).pin_memory()
-    y_host = torch.empty(M, N, dtype=torch.float32).pin_memory()
+    x_host = torch.from_numpy(x)
+    y_host = torch.full((M, N), float("nan"), dtype=torch.float32)
+    if pinned:
+        x_host, y_host = x_host.pin_memory(), y_host.pin_memory()
     x_dev = torch.empty(M, K, dtype=torch.float32, device="cuda")
-    sb = M * qmm.qmm_row_bytes("q8_K", K)
+    sb = M * qmm.qmm_row_bytes(act_name(wtype), K)
     scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
     y_dev = torch.empty(M, N, dtype=torch.float32, device="cuda")
     qmm.qmm_linear_host(wtype, W, x_host, x_dev, scratch, sb, y_dev, y_host, M, N, K)
