@@ -586,16 +586,6 @@ static qmm_status matmul_q_launch(const void* W, const void* xq, float* Y, int64
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 
-qmm_status matmul_q4_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t stream, bool pdl) {
-    return matmul_q_launch<QMM_Q4_0>(W, xq, Y, M, N, K, stream, pdl);
-}
-
-qmm_status matmul_q8_0_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                              cudaStream_t stream, bool pdl) {
-    return matmul_q_launch<QMM_Q8_0>(W, xq, Y, M, N, K, stream, pdl);
-}
-
 // Whether an M-token multiply of this weight type takes a tensor-core prefill
 // kernel (after one quantization of all M rows) rather than a launch per token.
 // Q4_0 takes it for every M > 1 (its launcher runs per-token matvecs itself on
@@ -625,14 +615,6 @@ using namespace qmm;
 
 extern "C" {
 
-qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                           qmm_stream_t stream) {
-    if (!W || !xq || !Y) return QMM_E_NULL;
-    qmm_status st = check_shape(QMM_Q4_0, M, N, K);
-    if (st != QMM_OK) return st;
-    if (!aligned16(W) || !aligned16(xq) || !aligned16(Y)) return QMM_E_ALIGN;
-    return matmul_q4_0_launch(W, xq, Y, M, N, K, (cudaStream_t)stream, true);
-}
 
 static qmm_status matmul_public(int wt, const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                                 qmm_stream_t stream) {
@@ -643,6 +625,10 @@ static qmm_status matmul_public(int wt, const void* W, const void* xq, float* Y,
     return prefill_launch(wt, W, xq, Y, M, N, K, (cudaStream_t)stream, true);
 }
 
+qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                           qmm_stream_t stream) {
+    return matmul_public(QMM_Q4_0, W, xq, Y, M, N, K, stream);
+}
 qmm_status qmm_matmul_q8_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
     return matmul_public(QMM_Q8_0, W, xq, Y, M, N, K, stream);
