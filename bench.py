@@ -649,9 +649,33 @@ def cpu_sample(nthreads: int, target_s: float):
 def cpu_baseline(args):
     nthreads = os.cpu_count() or 1
     gbs, secs, reps, rows = cpu_sample(nthreads, args.cpu_seconds)
+    # the same on one thread, a shorter sample: the rows split over threads is bit-identical, so this
+    # is the single-core rate of the same computation
+    gbs1, secs1, reps1, _ = cpu_sample(1, max(1.0, args.cpu_seconds / 3))
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": "%d full steps of the %s workload (quantize + %d-row matvec), %.1f s, rows split over %d "
-                      "threads" % (reps, HEADLINE, rows, secs, nthreads)}
+                      "threads" % (reps, HEADLINE, rows, secs, nthreads),
+            "one_thread": {"value": round(gbs1, 3), "unit": "GB/s", "sample": "%d full steps, %.1f s" % (reps1, secs1)},
+            "cpu": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name as the OS reports it (or the machine type)."""
+    arm = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+                if key in ("cpu implementer", "cpu part") and key not in arm:
+                    arm[key] = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    if arm:  # Arm cores report their implementer and part numbers (0x41 / 0xd4f: Neoverse V2)
+        return "Arm implementer %s part %s" % (arm.get("cpu implementer", "?"), arm.get("cpu part", "?"))
+    import platform
+    return platform.machine() or "unknown"
 
 
 def run_reference(args, rank, world):
