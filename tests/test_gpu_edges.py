@@ -106,7 +106,9 @@ def test_linear_token_rows_of_odd_alignment():
 @pytest.mark.parametrize("wtype,Ns,K,M", [("q4_K", (300, 77, 1024), 4096, 1), ("q4_K", (4096, 1024, 1024), 4096, 2),
                                           ("q8_0", (129, 4096), 4096, 1), ("q4_0", (64, 33, 5, 700), 896, 3),
                                           ("q6_K", (512, 257), 12288, 1), ("q2_K", (12288,), 4096, 1),
-                                          ("q5_1", (64, 33), 896, 2), ("q5_K", (300, 77), 4096, 1)])
+                                          ("q5_1", (64, 33), 896, 2), ("q5_K", (300, 77), 4096, 1),
+                                          ("q4_0", (300, 77), 1024, 16), ("q4_K", (300, 77), 2048, 16),
+                                          ("q5_0", (64, 33), 512, 9)])
 def test_linear_group_matches_oracle_and_linear(wtype, Ns, K, M):
     """qmm_linear_group: every matrix's output equals the oracle within tolerance and qmm_linear_<w> on
     that matrix alone bit for bit; the scratch holds the quantized rows."""

@@ -70,7 +70,8 @@ def test_rmsnorm_quantize_bitexact(act, M, K, eps):
                                           ("q6_K", (257,), 12288, 2), ("q2_K", (129, 64), 1024, 1),
                                           ("q4_0", (64, 33), 896, 3), ("q5_1", (100,), 512, 1),
                                           ("q5_K", (333, 20), 4096, 2), ("q4_K", (512, 300), 4096, 16),
-                                          ("q4_0", (512,), 4096, 16)])
+                                          ("q4_0", (512,), 4096, 16), ("q8_0", (300, 77), 2048, 16),
+                                          ("q5_1", (130,), 1024, 9)])
 def test_linear_norm_matches_oracle(wtype, Ns, K, M):
     """Decode tokens (one fused launch each) and the prefill route (M = 16: norm-quantize all rows,
     then the tensor-core matmul) against the oracle on the same f32 inputs; the scratch holds the
