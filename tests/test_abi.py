@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
                  "qmm_matmul_q6_K", "qmm_matmul_q2_K",
                  "qmm_linear_q4_0", "qmm_blocksums", "qmm_status_str", "qmm_row_bytes", "qmm_matvec_q4_1",
                  "qmm_matvec_q5_0", "qmm_matvec_q5_1", "qmm_matvec_q5_K", "qmm_get_rows", "qmm_kv_quantize",
-                 "qmm_kv_scores", "qmm_kv_wsum", "qmm_rmsnorm_quantize", "qmm_linear_norm", "qmm_linear_host"):
+                 "qmm_kv_scores", "qmm_kv_wsum", "qmm_rmsnorm_quantize", "qmm_linear_norm", "qmm_linear_host",
+                 "qmm_matmul_q8_0", "qmm_matmul_q4_1", "qmm_matmul_q5_0", "qmm_matmul_q5_1", "qmm_matmul_q5_K"):
         assert want in names
     assert set(names) == set(qmm.SIGNATURES), set(names) ^ set(qmm.SIGNATURES)
 
@@ -211,7 +212,12 @@ def test_matmul_and_blocksums_reject_bad_arguments(lib):
     assert lib.qmm_matmul_q4_0(A, A, None, 4, 64, 256, None) == 1
     assert lib.qmm_matmul_q4_0(A, U, A, 4, 64, 256, None) == 4
     assert lib.qmm_matmul_q4_0(A, A, A, 4, 64, 48, None) == 2
-    for f in (lib.qmm_matmul_q4_K, lib.qmm_matmul_q6_K, lib.qmm_matmul_q2_K):
+    for f in (lib.qmm_matmul_q8_0, lib.qmm_matmul_q4_1, lib.qmm_matmul_q5_0, lib.qmm_matmul_q5_1):
+        assert f(A, A, A, 0, 64, 256, None) == 2
+        assert f(None, A, A, 8, 64, 256, None) == 1
+        assert f(A, U, A, 8, 64, 256, None) == 4
+        assert f(A, A, A, 8, 64, 48, None) == 2
+    for f in (lib.qmm_matmul_q4_K, lib.qmm_matmul_q6_K, lib.qmm_matmul_q2_K, lib.qmm_matmul_q5_K):
         assert f(A, A, A, 0, 64, 2048, None) == 2
         assert f(A, A, None, 8, 64, 2048, None) == 1
         assert f(A, U, A, 8, 64, 2048, None) == 4
