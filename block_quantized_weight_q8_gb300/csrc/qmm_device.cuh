@@ -550,10 +550,39 @@ __device__ __forceinline__ void unpack_q8_K_word(const uint8_t* __restrict__ row
 // The whole Q8_K row by the threads tid, tid + nthr, ...: each thread issues up
 // to four of its loads before it stores any, so the row costs one memory round
 // trip rather than one per word a thread handles (eight at a time raised the
-// register pressure of the kernels that call it and was slower).
+// register pressure of the kernels that call it and was slower).  A 16-byte
+// aligned row of a multiple of four super-blocks is read in 16-byte chunks.
 __device__ __forceinline__ void unpack_q8_K_row_by(const uint8_t* __restrict__ row, int ns, uint8_t* q, float* d,
                                                    int* s, int tid, int nthr) {
     const int total = ns * 73;
+    if (ns % 4 == 0 && ((uintptr_t)row & 15u) == 0) {
+        // four super-blocks are 73 whole 16-byte chunks: each thread loads two
+        // chunks (eight words) before it stores any, so a long row (K = 12288:
+        // 876 chunks) is still one memory round trip
+        const int nchunk = total / 4;
+        const uint4* rv = reinterpret_cast<const uint4*>(row);
+        for (int j0 = tid; j0 < nchunk; j0 += 2 * nthr) {
+            uint4 cv[2];
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                const int j = j0 + k * nthr;
+                cv[k] = j < nchunk ? rv[j] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                const int j = j0 + k * nthr;
+                if (j < nchunk) {
+                    const uint32_t w[4] = {cv[k].x, cv[k].y, cv[k].z, cv[k].w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int i = 4 * j + e;
+                        put_q8_K_word(w[e], i / 73, i % 73, ns, q, d, s);
+                    }
+                }
+            }
+        }
+        return;
+    }
     for (int i0 = tid; i0 < total; i0 += 4 * nthr) {
         uint32_t wv[4];
 #pragma unroll
