@@ -66,3 +66,15 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_threads_and_one_core():
+    """The bench line's CPU baseline: the oracle on every host core and on one, with the CPU named."""
+    sys.path.insert(0, ROOT)
+    import argparse
+
+    import bench
+    d = bench.cpu_baseline(argparse.Namespace(cpu_seconds=0.3))
+    assert d["kind"] == "oracle" and d["unit"] == "GB/s" and d["cores"] >= 1 and d["value"] > 0
+    assert d["one_thread"]["value"] > 0 and d["one_thread"]["unit"] == "GB/s"
+    assert isinstance(d["cpu"], str) and d["cpu"]
