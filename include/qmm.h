@@ -3,9 +3,23 @@
  * GB300 (sm_103a).
  *
  * y = W . x where W stays in its block-quantized form (Q4_0, Q8_0, Q4_K, Q6_K,
- * Q2_K) and is never dequantized as a whole, x is quantized on the fly to Q8_0
- * or Q8_K, and every block is an exact integer dot product whose per-block
- * scales (and K-quant mins) are folded into an fp32 accumulator once per block.
+ * Q2_K; also Q4_1, Q5_0, Q5_1, Q5_K) and is never dequantized as a whole, x is
+ * quantized on the fly to Q8_0 or Q8_K, and every block is an exact integer dot
+ * product whose per-block scales (and mins) are folded into an fp32
+ * accumulator once per block.
+ *
+ * A decode token and a prefill, with device buffers (error checks elided):
+ *
+ *   size_t wb = qmm_row_bytes(QMM_Q8_0, K) * N;          // W: N rows of Q8_0
+ *   size_t sb = qmm_row_bytes(qmm_act_type(QMM_Q8_0), K); // one quantized row
+ *   // x: f32 [1][K], y: f32 [1][N], scratch: sb bytes, all 16-byte aligned
+ *   qmm_linear_q8_0(W, x, scratch, sb, y, 1, N, K, stream);
+ *   // M tokens: scratch of M * sb bytes; M >= 8 runs on the tensor cores
+ *   qmm_linear_q8_0(W, X, scratch, M * sb, Y, M, N, K, stream);
+ *   // or quantize once and reuse the rows: qmm_quantize_q8_0(X, xq, M, K,
+ *   // stream); qmm_matmul_q8_0(W, xq, Y, M, N, K, stream);
+ *   // results are ready when the stream reaches them; a device-side timeout
+ *   // is read back with qmm_device_status(1).
  *
  * Pages the operations follow (cited by title and section):
  *   [minfer] "10 . CPU matmul: quantized weights x Q8_0 activations"
