@@ -26,8 +26,8 @@ qmm_status matvec_group_norm_dispatch(int wt, int G, const void* const* W, const
 // [minfer] "10 . CPU matmul: quantized weights x Q8_0 activations" s3.2
 // (cpu_quant_matmul_f32): the weight type alone decides the activation format;
 // quantize once into the caller's scratch, then multiply.
-static qmm_status linear(int wt, const void* W, const float* x, void* scratch, size_t scratch_bytes, float* y,
-                         int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+qmm_status linear_impl(int wt, const void* W, const float* x, void* scratch, size_t scratch_bytes, float* y,
+                       int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     if (!W || !x || !scratch || !y) return QMM_E_NULL;
     qmm_status st = check_shape(wt, M, N, K);
     if (st != QMM_OK) return st;
@@ -220,7 +220,7 @@ qmm_status qmm_linear_host(int wtype, const void* W, const float* x_host, float*
     if (cudaMemcpyAsync(x_dev, x_host, (size_t)M * (size_t)K * sizeof(float), cudaMemcpyHostToDevice, cs) !=
         cudaSuccess)
         return QMM_E_CUDA;
-    st = linear(wtype, W, x_dev, xq_scratch, scratch_bytes, y_dev, M, N, K, cs);
+    st = linear_impl(wtype, W, x_dev, xq_scratch, scratch_bytes, y_dev, M, N, K, cs);
     if (st != QMM_OK) return st;
     if (cudaMemcpyAsync(y_host, y_dev, (size_t)M * (size_t)N * sizeof(float), cudaMemcpyDeviceToHost, cs) !=
         cudaSuccess)
@@ -255,40 +255,40 @@ const char* qmm_status_str(qmm_status s) {
 
 qmm_status qmm_linear_q4_0(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q4_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q4_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 qmm_status qmm_linear_q8_0(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q8_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q8_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 qmm_status qmm_linear_q4_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q4_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q4_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 qmm_status qmm_linear_q6_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q6_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q6_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 qmm_status qmm_linear_q2_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q2_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q2_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 
 qmm_status qmm_linear_q4_1(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q4_1, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q4_1, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 qmm_status qmm_linear_q5_0(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q5_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q5_0, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 qmm_status qmm_linear_q5_1(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q5_1, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q5_1, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 qmm_status qmm_linear_q5_K(const void* W, const float* x, void* s, size_t sb, float* y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream) {
-    return linear(QMM_Q5_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
+    return linear_impl(QMM_Q5_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 
 qmm_status qmm_device_status(int clear) {

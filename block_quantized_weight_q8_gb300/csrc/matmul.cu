@@ -562,15 +562,16 @@ static qmm_status matmul_q_launch(const void* W, const void* xq, float* Y, int64
     if (!make_map(&wmap, W, row_bytes_of(WT, K), (uint64_t)N, mm::KB * L::WB) ||
         !make_map(&xmap, xq, row_bytes_of(QMM_Q8_0, K), (uint64_t)M, mm::KB * 34))
         return QMM_E_CUDA;
-    static bool attr_set[64] = {false};
+    static PerDeviceOnce attr_once;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMM_E_CUDA;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(mm::matmul_q_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::SMEM_BYTES) != cudaSuccess)
-            return QMM_E_CUDA;
-        attr_set[dev] = true;
-    }
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_E_CUDA;
+    const qmm_status ast = attr_once.run(dev, [] {
+        return cudaFuncSetAttribute(mm::matmul_q_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    L::SMEM_BYTES) == cudaSuccess
+                   ? QMM_OK
+                   : QMM_E_CUDA;
+    });
+    if (ast != QMM_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + mm::BN - 1) / mm::BN));
     cfg.blockDim = dim3(mm::THREADS);

@@ -700,15 +700,16 @@ template <int WT>
 static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                             cudaStream_t stream, bool pdl) {
     using L = kq::Layout<WT>;
-    static bool attr_set[64] = {false};
+    static PerDeviceOnce attr_once;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMM_E_CUDA;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(kq::matmul_kq_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) !=
-            cudaSuccess)
-            return QMM_E_CUDA;
-        attr_set[dev] = true;
-    }
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_E_CUDA;
+    const qmm_status ast = attr_once.run(dev, [] {
+        return cudaFuncSetAttribute(kq::matmul_kq_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) ==
+                       cudaSuccess
+                   ? QMM_OK
+                   : QMM_E_CUDA;
+    });
+    if (ast != QMM_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + kq::BM - 1) / kq::BM), (unsigned)((M + kq::BN - 1) / kq::BN));
     cfg.blockDim = dim3(kq::THREADS);

@@ -486,9 +486,10 @@ __global__ void __launch_bounds__(kThreads) blocksums_kernel(const uint8_t* __re
 // ------------------------------------------------------------------ host side
 qmm_status current_device(DeviceInfo* info) {
     static DeviceInfo cache[64];
+    static PerDeviceOnce once;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QMM_E_CUDA;
-    if (cache[dev].device != dev) {
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_E_CUDA;
+    const qmm_status st = once.run(dev, [&] {
         DeviceInfo d;
         d.device = dev;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return QMM_E_CUDA;
@@ -499,7 +500,9 @@ qmm_status current_device(DeviceInfo* info) {
         if (cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
             return QMM_E_CUDA;
         cache[dev] = d;
-    }
+        return QMM_OK;
+    });
+    if (st != QMM_OK) return st;
     *info = cache[dev];
     return QMM_OK;
 }
@@ -649,8 +652,8 @@ static qmm_status plan_matvec(const int64_t* Ns, int G, int64_t K, const DeviceI
 template <int WT, bool SU, int FUSE, bool SPLIT>
 static qmm_status launch_matvec_k(const MatSet& set, const void* xq, const float* x, void* xq_out, int64_t K,
                                    const MatvecPlan& p, const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
-    static bool attr_set[64] = {false};
-    if (!attr_set[dev.device]) {
+    static PerDeviceOnce attr_once;
+    const qmm_status ast = attr_once.run(dev.device, [&] {
         if (cudaFuncSetAttribute(matvec_kernel<WT, SU, FUSE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dev.max_smem_optin) != cudaSuccess)
             return QMM_E_CUDA;
@@ -658,8 +661,9 @@ static qmm_status launch_matvec_k(const MatSet& set, const void* xq, const float
         if (cudaFuncSetAttribute(matvec_kernel<WT, SU, FUSE, SPLIT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return QMM_E_CUDA;
-        attr_set[dev.device] = true;
-    }
+        return QMM_OK;
+    });
+    if (ast != QMM_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3((unsigned)(p.nw * 32));

@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "qmm.h"
 
 namespace qmm {
@@ -69,6 +72,35 @@ struct DeviceInfo {
 
 // Properties of the current device (cached per device id).
 qmm_status current_device(DeviceInfo* info);
+
+// Per-device one-time set-up (kernel attributes, cached device properties)
+// that host threads may reach concurrently: the first caller on a device runs
+// it under a lock, later callers see the finished flag; a set-up that fails is
+// tried again on the next call.
+class PerDeviceOnce {
+  public:
+    template <class F>
+    qmm_status run(int dev, F&& setup) {
+        if (dev < 0 || dev >= kDevices) return QMM_E_CUDA;
+        if (done_[dev].load(std::memory_order_acquire)) return QMM_OK;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (done_[dev].load(std::memory_order_relaxed)) return QMM_OK;
+        const qmm_status st = setup();
+        if (st == QMM_OK) done_[dev].store(true, std::memory_order_release);
+        return st;
+    }
+
+  private:
+    static constexpr int kDevices = 64;
+    std::atomic<bool> done_[kDevices] = {};
+    std::mutex mu_;
+};
+
+// The quantize + multiply with a caller scratch buffer (qmm_linear_<wtype>),
+// also used by the entry points that supply their own scratch.  wt must be a
+// weight type.
+qmm_status linear_impl(int wt, const void* W, const float* x, void* scratch, size_t scratch_bytes, float* y,
+                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 inline qmm_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_E_CUDA;

@@ -21,8 +21,7 @@
  *   [krafla] "Architecture" (jonpark0.github.io/krafla)
  *   [kvad]   "kvad -- the same ideas, at scale" (kvad.eu/docs/internals/engine)
  *
- * Readings taken where the pages are silent or garbled (each also listed in
- * the design notes):
+ * Readings taken where the pages are silent or garbled:
  *   - Q8_K activation blocks are 292 B: f32 d, int8 qs[256], int16 bsums[16].
  *   - The Q8_K inverse scale is 127/amax, the same expression as Q8_0.
  *   - Q4_0 codes are min(15, trunc(x*id + 8.5)) with d = m / -8.

@@ -3,9 +3,12 @@ device workspace (for example a plugin that only receives its input and output b
 application that owns the device memory, or a loop that must never call cudaMalloc).  It keeps the
 quantized activation in the library's own fixed 1 MiB device array instead.
 
-Checked through the C ABI against qmm_linear_<wtype> (the call that takes a caller workspace), on
-two calls in a row, within the tolerance the other GPU tests use.  This file is collected last so a
-run that stops at the first failure has already run every other test; it also passes on its own."""
+Checked through the C ABI on two calls in a row: bit for bit against qmm_linear_<wtype> (the call
+that takes a caller workspace and runs the same kernels), and against the CPU oracle within the
+tolerance the other GPU tests use.  The cases cover both routes: a launch per token (M < 8) and the
+tensor-core prefill (M >= 8), whose TMA tensor maps are then built over the library's array.  This
+file is collected last so a run that stops at the first failure has already run every other test;
+it also passes on its own."""
 import ctypes
 
 import numpy as np
@@ -38,23 +41,29 @@ def _close(y, ref):
 
 @pytest.mark.parametrize("wtype,M,N,K", [("q8_0", 1, 12288, 4096), ("q4_0", 1, 4864, 896), ("q4_K", 1, 4096, 4096),
                                          ("q6_K", 1, 1024, 12288), ("q2_K", 3, 777, 1024), ("q4_0", 5, 300, 1024),
-                                         ("q5_1", 2, 500, 4096), ("q5_K", 1, 4096, 4096)])
+                                         ("q5_1", 2, 500, 4096), ("q5_K", 1, 4096, 4096),
+                                         ("q4_0", 16, 300, 1024), ("q8_0", 8, 500, 4096), ("q4_K", 8, 300, 2048),
+                                         ("q6_K", 9, 200, 4096), ("q5_0", 200, 129, 4096)])
 def test_noalloc_matches_linear_twice(lib, wtype, M, N, K):
     act = "q8_0" if wtype in ("q4_0", "q8_0", "q4_1", "q5_0", "q5_1") else "q8_K"
-    W = torch.from_numpy(oracle.quantize(wtype, workloads.weights_f32(N, K, seed=31, row_jitter=True))).cuda()
+    Wq = oracle.quantize(wtype, workloads.weights_f32(N, K, seed=31, row_jitter=True))
+    W = torch.from_numpy(Wq).cuda()
     sb = M * qmm.qmm_row_bytes(act, K)
+    assert sb <= 1 << 20
     scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     f = lib.qmm_linear_noalloc
     lin = getattr(lib, "qmm_linear_" + wtype)
     for call in range(2):  # the shared array keeps the previous call's contents: both must be right
-        x = torch.from_numpy(workloads.activations_f32(M, K, seed=100 + call)).cuda()
+        xh = workloads.activations_f32(M, K, seed=100 + call)
+        x = torch.from_numpy(xh).cuda()
         y_ref = torch.empty(M, N, dtype=torch.float32, device="cuda")
         y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
         assert lin(W.data_ptr(), x.data_ptr(), scratch.data_ptr(), sb, y_ref.data_ptr(), M, N, K, stream) == 0
         assert f(qmm.TYPES[wtype], W.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, K, stream) == 0
         torch.cuda.synchronize()
-        _close(y.cpu().numpy(), y_ref.cpu().numpy())
+        assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
+        _close(y.cpu().numpy(), oracle.matmul(wtype, Wq, oracle.quantize(act, xh), M, N, K, nthreads=8))
     assert qmm.qmm_device_status(clear=True) == 0
 
 
