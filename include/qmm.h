@@ -296,12 +296,15 @@ QMM_API qmm_status qmm_linear_group(int wtype, int G, const void* const* W, cons
 /* ---- RMSNorm fused ahead of the quantizer --------------------------------- */
 /* [krafla] "Architecture", "Data flow for one token": h = rmsnorm(x) ; qa =
  * quantize_q8(h), then the matvecs that read qa.  The page gives no formula;
- * reading: h_i = (x_i * s) * w_i, s = 1 / sqrt(ss / K + eps), every step an f32
- * operation rounded once, and ss summed in one fixed order -- 8-value
- * sequential partials, then a stride-doubling tree over them (step 1, 2, 4, ...:
- * p[i] += p[i + step] for every multiple i of 2*step with i + step < K/8) -- so
- * the codes of h are bit-identical to a scalar implementation of the same
- * steps.  A model whose norm scales by 1 + w passes that vector as w.
+ * reading: h_i = (x_i * s) * w_i, s = 1 / sqrt(ss / K + eps), ss = sum of x_i^2,
+ * every step an f32 operation rounded once.  The kernels sum ss in f32 in one
+ * fixed order (8-value sequential partials, then a pairwise tree), so results
+ * are identical run to run; that sum is within (8 + log2 K) units in the last
+ * place of the exact one.  Since h and its block maximum scale together, the
+ * codes agree with those of an exactly summed ss except where h_i * 127/amax
+ * lies within a few roundings of a tie (there by at most 1), and each block's
+ * d agrees to within that relative bound.  A model whose norm scales by 1 + w
+ * passes that vector as w.
  *
  * qmm_rmsnorm_quantize: act QMM_Q8_0 or QMM_Q8_K; x f32 [M][K], w f32 [K]
  * (16-byte aligned), xq as for qmm_quantize_q8_0/q8_K; K <= 65536.

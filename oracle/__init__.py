@@ -262,13 +262,13 @@ def kv_wsum(w: np.ndarray, v8: np.ndarray, Hq: int, Hkv: int, P: int, hd: int) -
 
 # ---- RMSNorm ahead of the quantizer ([krafla] "Architecture", "Data flow for one token")
 def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
-    """f32 [M, K]: (x * s) * w with s = 1/sqrt(ss/K + eps) in f32, ss in the fixed order of
-    qmm_oracle.c (8-value sequential partials, then a stride-doubling tree)."""
+    """f32 [M, K]: (x * s) * w with s = 1/sqrt(ss/K + eps) in f32, ss = sum of x^2 taken left to
+    right in binary64 and rounded once to f32."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     x2 = x.reshape(-1, x.shape[-1])
     M, K = x2.shape
     w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
-    assert w.size == K and K % 8 == 0
+    assert w.size == K
     out = np.zeros((M, K), dtype=np.float32)
     lib().orc_rmsnorm(_ptr(x2), _ptr(w), ctypes.c_float(eps), _ptr(out), M, K)
     return out

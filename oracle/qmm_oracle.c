@@ -1073,31 +1073,20 @@ void orc_kv_wsum(const float* w, const uint8_t* vc, double* out, int Hq, int Hkv
 /* ------------------------------------------------------------------------- */
 /* RMSNorm ahead of the activation quantizer: [krafla] "Architecture",       */
 /* "Data flow for one token" (h = rmsnorm(x) ; qa = quantize_q8(h)).  The     */
-/* page gives no formula; reading, the usual one in f32:                      */
-/*   h_i = (x_i * s) * w_i,  s = 1 / sqrt(ss / K + eps),                      */
-/* each operation rounded once.  Because the codes of h are compared bit for  */
-/* bit, the sum of squares ss has one fixed order (a reading too): partial    */
-/* sums of 8 consecutive squares, in order, then those K/8 partials added by  */
-/* a stride-doubling tree (step 1, 2, 4, ...: p[i] += p[i + step] for every   */
-/* i that is a multiple of 2*step with i + step < K/8).  A model whose norm   */
-/* scales by 1 + w passes that vector as w.                                   */
+/* page gives no formula; reading, the usual definition                       */
+/*   h_i = (x_i * s) * w_i,  s = 1 / sqrt(ss / K + eps),  ss = sum_i x_i^2.   */
+/* ss is the plain sum of squares, left to right, in binary64 (the square of  */
+/* an f32 is exact there) and rounded once to f32; every later step is an f32 */
+/* operation rounded once.  A model whose norm scales by 1 + w passes that    */
+/* vector as w.                                                               */
 /* ------------------------------------------------------------------------- */
 void orc_rmsnorm(const float* x, const float* w, float eps, float* h, int64_t M, int64_t K) {
-    const int64_t n8 = K / 8;
-    float* p = (float*)malloc(sizeof(float) * (size_t)(n8 > 0 ? n8 : 1));
-    if (!p) return;
     for (int64_t t = 0; t < M; t++) {
         const float* xr = x + t * K;
-        for (int64_t i = 0; i < n8; i++) {
-            float s = xr[8 * i] * xr[8 * i];
-            for (int j = 1; j < 8; j++) s = s + xr[8 * i + j] * xr[8 * i + j];
-            p[i] = s;
-        }
-        for (int64_t step = 1; step < n8; step *= 2)
-            for (int64_t i = 0; i + step < n8; i += 2 * step) p[i] = p[i] + p[i + step];
-        const float mean = p[0] / (float)K;
+        double ss = 0.0;
+        for (int64_t i = 0; i < K; i++) ss += (double)xr[i] * (double)xr[i];
+        const float mean = (float)ss / (float)K;
         const float sc = 1.0f / sqrtf(mean + eps);
         for (int64_t i = 0; i < K; i++) h[t * K + i] = (xr[i] * sc) * w[i];
     }
-    free(p);
 }

@@ -1,7 +1,12 @@
 """RMSNorm fused ahead of the quantizer ([krafla] "Architecture", "Data flow for one token":
-h = rmsnorm(x) ; qa = quantize_q8(h)) on the GPU against the CPU oracle: the quantized normed
-rows bit-exact (both sides sum the squares in the same fixed order), the products within 1e-5
-of each token row's L2 norm."""
+h = rmsnorm(x) ; qa = quantize_q8(h)) on the GPU against the CPU oracle.
+
+The oracle sums the squares left to right in binary64 (the plain definition); the kernels sum them
+in f32 in their own order, so the two scales s differ by a few units in the last place.  The codes
+rne(h_i * 127/amax) do not depend on s beyond rounding (h and amax scale together), so they must be
+bit-exact except where h_i * 127/amax lies within a few roundings of a tie, where +-1 is allowed and
+counted; each block's d = amax/127 follows s and may differ by the derived bound.  The products are
+within 1e-5 of each token row's L2 norm."""
 import numpy as np
 import pytest
 
@@ -46,6 +51,60 @@ def assert_rows_close(y, ref, tol=TOL):
     assert not bad.any(), (np.abs(y - ref) / np.maximum(norm, 1e-30)).max()
 
 
+# |t' - t| for t = h_i * 127/amax, |t| <= 127: h_i and amax each carry at most four roundings of
+# 2^-24 relative on either side, id and the product one more each: about 11 * 2^-24 * 127 = 8.3e-5.
+CODE_TIE_MARGIN = 2e-4
+
+
+def scale_margin(K):
+    """Relative bound on the difference of d = amax/127 between the two sums of squares: the kernel's
+    f32 sum (sequential runs of 8, then a tree of depth log2(K/8)) is within (8 + log2 K) * 2^-24 of
+    the exact sum, the oracle's within 2^-24; s = 1/sqrt(ss/K + eps) halves that and adds four
+    roundings per side; amax and the division add three more.  Doubled for safety."""
+    u = 2.0 ** -24
+    return 2 * (0.5 * (9 + np.log2(K)) + 8 + 6) * u
+
+
+def normed_codes_differences(act, got, h):
+    """Compares the GPU's quantized normed rows `got` (bytes) with the oracle's quantization of the
+    oracle's h.  Returns the number of codes that took the +-1 allowance near a tie."""
+    M, K = h.shape
+    bv, bb, off = (32, 34, 2) if act == "q8_0" else (256, 292, 4)
+    want = oracle.quantize(act, h).reshape(M, K // bv, bb)
+    got = np.asarray(got, dtype=np.uint8).reshape(M, K // bv, bb)
+    cw = want[:, :, off:off + bv].view(np.int8).astype(np.int32)
+    cg = got[:, :, off:off + bv].view(np.int8).astype(np.int32)
+    hb = h.reshape(M, K // bv, bv).astype(np.float32)
+    amax = np.abs(hb).max(axis=2, keepdims=True)
+    with np.errstate(divide="ignore"):
+        idv = np.where(amax > 0, np.float32(127.0) / amax, np.float32(0.0)).astype(np.float32)
+    t = (hb * idv).astype(np.float32).astype(np.float64)
+    near = np.abs(t - np.floor(t) - 0.5) <= CODE_TIE_MARGIN
+    diff = cg - cw
+    assert np.all(diff[~near] == 0), "codes differ away from a tie: %s" % np.argwhere((diff != 0) & ~near)[:5]
+    assert np.all(np.abs(diff) <= 1)
+    dm = scale_margin(K)
+    a32 = amax[:, :, 0].astype(np.float64)
+    if act == "q8_0":
+        dwant = want[:, :, 0:2].copy().view(np.uint16)[:, :, 0].astype(np.int64)
+        dgot = got[:, :, 0:2].copy().view(np.uint16)[:, :, 0].astype(np.int64)
+        d32 = (amax[:, :, 0] / np.float32(127.0)).astype(np.float32).astype(np.float64)
+        v = dwant.astype(np.uint16).view(np.float16).astype(np.float64)
+        up = (dwant + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+        dn = np.maximum(dwant - 1, 0).astype(np.uint16).view(np.float16).astype(np.float64)
+        near_d = (np.abs(d32 - (v + up) / 2) <= dm * d32) | (np.abs(d32 - (v + dn) / 2) <= dm * d32)
+        dd = dgot - dwant
+        assert np.all(dd[~near_d] == 0) and np.all(np.abs(dd) <= 1)
+    else:
+        dwant = want[:, :, 0:4].copy().view(np.float32)[:, :, 0].astype(np.float64)
+        dgot = got[:, :, 0:4].copy().view(np.float32)[:, :, 0].astype(np.float64)
+        assert np.all(np.abs(dgot - dwant) <= dm * dwant)
+        bs_got = got[:, :, 260:292].copy().view(np.int16).astype(np.int32)
+        assert np.array_equal(bs_got, cg.reshape(M, K // bv, 16, 16).sum(axis=3))  # bsums of its own codes
+    assert np.all(cg[a32 == 0] == 0)  # an all-zero block stays all zero
+    return int((diff != 0).sum())
+
+
 def norm_weight(K, seed):
     return np.random.default_rng(seed).uniform(0.5, 1.5, size=K).astype(np.float32)
 
@@ -59,11 +118,11 @@ def test_rmsnorm_quantize_bitexact(act, M, K, eps):
         x[1] = 0.0 if eps > 0 else 1.0      # an all-zero row (eps keeps the scale finite)
         x[2] = -0.5                          # a constant row
     w = norm_weight(K, K)
-    want = oracle.quantize(act, oracle.rmsnorm(x, w, eps))
-    out = torch.empty(want.size, dtype=torch.uint8, device="cuda")
+    h = oracle.rmsnorm(x, w, eps)
+    out = torch.empty(M * qmm.qmm_row_bytes(act, K), dtype=torch.uint8, device="cuda")
     qmm.qmm_rmsnorm_quantize(act, dev(x), dev(w), eps, out, M, K)
-    got = host(out).reshape(want.shape)
-    assert np.array_equal(got, want), np.argwhere(got != want)[:5].tolist()
+    flips = normed_codes_differences(act, host(out), h)
+    print("%s M=%d K=%d: %d of %d codes took the +-1 allowance near a tie" % (act, M, K, flips, M * K))
 
 
 @pytest.mark.parametrize("wtype,Ns,K,M", [("q8_0", (12288,), 4096, 1), ("q4_K", (300, 77, 1024), 4096, 1),
@@ -79,7 +138,8 @@ def test_linear_norm_matches_oracle(wtype, Ns, K, M):
     eps = 1e-6
     x = workloads.activations_f32(M, K, seed=950 + K)
     w = norm_weight(K, 7)
-    X = oracle.quantize(act_name(wtype), oracle.rmsnorm(x, w, eps))
+    h = oracle.rmsnorm(x, w, eps)
+    X = oracle.quantize(act_name(wtype), h)
     Ws, refs = [], []
     for g, N in enumerate(Ns):
         Wq = oracle.quantize(wtype, workloads.weights_f32(N, K, seed=960 + g, row_jitter=True))
@@ -89,7 +149,8 @@ def test_linear_norm_matches_oracle(wtype, Ns, K, M):
     sb = M * qmm.qmm_row_bytes(act_name(wtype), K)
     scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
     qmm.qmm_linear_norm(wtype, Ws, Ns, dev(x), dev(w), eps, scratch, sb, ys, M, K)
-    assert np.array_equal(host(scratch), X.reshape(-1))
+    flips = normed_codes_differences(act_name(wtype), host(scratch), h)
+    print("%s M=%d K=%d: %d codes took the +-1 allowance near a tie" % (wtype, M, K, flips))
     for g in range(len(Ns)):
         assert_rows_close(host(ys[g]), refs[g])
 

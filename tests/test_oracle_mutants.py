@@ -45,7 +45,10 @@ MUTANTS = [
      "const int kvh = h % Hkv;\n        for (int64_t p = 0; p < P; p++) {\n            const uint8_t* kr"),
     ("rmsnorm drops eps", "const float sc = 1.0f / sqrtf(mean + eps);", "const float sc = 1.0f / sqrtf(mean);"),
     ("rmsnorm ignores w", "h[t * K + i] = (xr[i] * sc) * w[i];", "h[t * K + i] = xr[i] * sc;"),
-    ("rmsnorm mean over K-1", "const float mean = p[0] / (float)K;", "const float mean = p[0] / (float)(K - 1);"),
+    ("rmsnorm mean over K-1", "const float mean = (float)ss / (float)K;",
+     "const float mean = (float)ss / (float)(K - 1);"),
+    ("rmsnorm sums |x|, not x^2", "ss += (double)xr[i] * (double)xr[i];", "ss += fabs((double)xr[i]);"),
+    ("rmsnorm skips the last value", "for (int64_t i = 0; i < K; i++) ss +=", "for (int64_t i = 1; i < K; i++) ss +="),
     ("kv cache head-major", "const uint8_t* vr = vc + (p * Hkv + kvh) * rb;", "const uint8_t* vr = vc + (kvh * P + p) * rb;"),
     ("kv scale 128/amax", "float id = (amax != 0.0f) ? 127.0f / amax : 0.0f;\n        for (int i = 0; i < hd; i++)",
      "float id = (amax != 0.0f) ? 128.0f / amax : 0.0f;\n        for (int i = 0; i < hd; i++)"),

@@ -594,9 +594,9 @@ def test_kv_wsum_matches_dequantized_einsum(orc):
 # --------------------------------------------------------------------------- RMSNorm
 def test_rmsnorm_matches_float64(orc):
     """h = rmsnorm(x) ahead of the quantizer ([krafla] "Architecture", "Data flow for one token"),
-    reading x * w / sqrt(mean(x^2) + eps): the f32 result is within 2e-6 of a float64 evaluation
-    per element (the fixed-order f32 sum of squares and five single roundings), for an eps that
-    matters and one that does not."""
+    reading x * w / sqrt(mean(x^2) + eps): the f32 result is within 6e-7 of a float64 evaluation
+    per element (8 single roundings of 2^-24 after a binary64 sum of squares that is exact to far
+    below that), for an eps that matters and one that does not."""
     g = np.random.default_rng(60)
     for K, eps in ((4096, 1e-6), (896, 0.5), (256, 1e-5)):
         x = workloads.activations_f32(3, K, seed=K)
@@ -604,7 +604,7 @@ def test_rmsnorm_matches_float64(orc):
         h = orc.rmsnorm(x, w, eps)
         x64 = x.astype(np.float64)
         ref = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + eps) * w
-        assert np.all(np.abs(h - ref) <= 2e-6 * np.abs(ref) + 1e-30), np.max(np.abs(h - ref) / np.abs(ref))
+        assert np.all(np.abs(h - ref) <= 6e-7 * np.abs(ref) + 1e-30), np.max(np.abs(h - ref) / np.abs(ref))
 
 
 def test_rmsnorm_exact_cases(orc):
