@@ -208,6 +208,16 @@ class Timer:
         return e0.elapsed_time(e1) / 1000.0  # seconds
 
 
+def timed_regions(timer, region, world, device, min_seconds: float):
+    """Times region() (one bracketed timed region each) repeatedly until at least min_seconds of
+    device time is timed; every rank runs the same number of regions.  Returns (seconds, regions)."""
+    first = timer.run(region, 1)
+    want = int(np.ceil(min_seconds / max(first, 1e-7)))
+    regions = max(1, min(100000, int(reduce_max(want, world, device))))
+    secs = sum(timer.run(region, 1) for _ in range(regions))
+    return secs, regions
+
+
 def make_graph(torch, stream, body, count: int):
     """Capture `count` calls of body(i) into one CUDA graph on `stream`."""
     g = torch.cuda.CUDAGraph()
@@ -250,8 +260,6 @@ def run_gpu(args, rank, local_rank, world):
     def copies_for(nbytes):
         return max(2, int(np.ceil(2.5 * L2_BYTES / nbytes)))
 
-    graph_steps = 64
-
     # ---------------- headline: Q8_0 decode step (quantize + matvec)
     cfg = workloads.WORKLOADS[HEADLINE]
     N, K = cfg["N"], cfg["K"]
@@ -268,30 +276,36 @@ def run_gpu(args, rank, local_rank, world):
     def step(i):
         qmm.qmm_linear_q8_0(Ws[i % C], x, xq, xrb, y, 1, N, K, stream=sh)
 
+    # One timed region is exactly --steps steps: a CUDA graph of G = min(steps, 64) calls replayed
+    # steps // G times, then a graph of the remaining steps % G calls.
+    G = min(args.steps, 64)
+    full, rest = divmod(args.steps, G)
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
             step(i)
-        graph = make_graph(torch, stream, step, graph_steps)
+        graph = make_graph(torch, stream, step, G)
+        graph_rest = make_graph(torch, stream, lambda i: step(full * G + i), rest) if rest else None
     torch.cuda.synchronize()
 
-    def replay(n_steps):
-        full, rest = divmod(n_steps, graph_steps)
+    def region(_):
         for _ in range(full):
             graph.replay()
-        for i in range(rest):
-            step(i)
+        if graph_rest is not None:
+            graph_rest.replay()
 
     with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup // graph_steps)):
+        for _ in range(max(1, args.warmup // G)):  # at least one full replay of each graph
             graph.replay()
-        secs = timer.run(lambda i: replay(args.steps), 1)
-    value, tmax = aggregate(wbytes * args.steps, secs, world, dev)
-    ms_per_step = tmax / args.steps * 1e3
-    launches = 1 * args.steps  # the step is one kernel: it quantizes x itself, then multiplies
+        if graph_rest is not None:
+            graph_rest.replay()
+        secs, regions = timed_regions(timer, region, world, dev, args.min_timed_s)
+    value, tmax = aggregate(wbytes * args.steps * regions, secs, world, dev)
+    ms_per_step = tmax / (args.steps * regions) * 1e3
+    launches = 1 * args.steps  # per timed region: the step is one kernel (it quantizes x, then multiplies)
 
     # the step's kernel is the dominant (only) kernel: roofline from the step's own timing.
     # Algorithmic bytes per launch: W, the f32 x, the quantized row stored once, y.
-    step_s = secs / args.steps
+    step_s = secs / (args.steps * regions)
     algo_bytes = wbytes + 4 * K + xrb + 4 * N
     achieved = algo_bytes / step_s / 1e9
 
@@ -300,11 +314,10 @@ def run_gpu(args, rank, local_rank, world):
         qmm.qmm_matvec_q8_0(Ws[i % C], xq, y, N, K, stream=sh)
 
     with torch.cuda.stream(stream):
-        mv_graph = make_graph(torch, stream, mv, graph_steps)
+        mv_graph = make_graph(torch, stream, mv, 64)
         mv_graph.replay()
-        reps = max(4, (args.steps + graph_steps - 1) // graph_steps)
-        mv_secs = timer.run(lambda i: mv_graph.replay(), reps)
-    mv_launch_s = mv_secs / (reps * graph_steps)
+        mv_secs, mv_regions = timed_regions(timer, lambda i: mv_graph.replay(), 1, dev, args.min_timed_s)
+    mv_launch_s = mv_secs / (mv_regions * 64)
     traffic, traffic_src = profiled_traffic()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
@@ -329,10 +342,11 @@ def run_gpu(args, rank, local_rank, world):
     with torch.cuda.stream(stream):
         for i in range(3):
             e2e_step(i)
-        e2e_secs = timer.run(e2e_step, e2e_steps)
-    e2e_value, _ = aggregate(wbytes * e2e_steps, e2e_secs, world, dev)
+        e2e_secs, e2e_regions = timed_regions(timer, lambda _: [e2e_step(i) for i in range(e2e_steps)], world, dev,
+                                              args.min_timed_s)
+    e2e_value, _ = aggregate(wbytes * e2e_steps * e2e_regions, e2e_secs, world, dev)
     e2e = {"value": round(e2e_value / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": 4 * K,
-           "d2h_bytes_per_step": 4 * N, "steps": e2e_steps,
+           "d2h_bytes_per_step": 4 * N, "steps": e2e_steps, "timed_regions": e2e_regions,
            "note": "qmm_linear_host per step, eager calls through the binding: x (16 KB) read from pinned host "
                    "memory by the quantize kernel over the host link, the multiply, y (48 KB) written by it into "
                    "pinned host memory; both transfers inside the timed region, one stream"}
@@ -351,16 +365,22 @@ def run_gpu(args, rank, local_rank, world):
         line = {
             "metric": METRIC, "value": round(value / 1e9, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "timed_regions": regions,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic (seeded N(0,0.02) weights quantized on the GPU; N(0,1) activation with 1% x20)",
             "config": {"workload": HEADLINE, "wtype": "q8_0", "M": 1, "N": N, "K": K, "weight_bytes": wbytes,
                        "step": "qmm_linear_q8_0: one kernel per token (each CTA quantizes x to Q8_0, then the "
                                "matvec), chained launches, CUDA graph",
+                       "timing": "each timed region is exactly `steps` steps, bracketed by barrier + synchronize "
+                                 "and CUDA events on the launching stream; regions repeat until at least %.0f ms "
+                                 "is timed (%d regions); value and ms_per_step over all of them" % (
+                                     args.min_timed_s * 1e3, regions),
                        "l2": "weights rotate over %d resident copies (%.0f MB > 2x the 129 MB L2)" % (
                            C, C * wbytes / 1e6),
                        "parallelism": "replicas: each rank streams its own weights" if world > 1 else "1 GPU"},
             "roofline": roofline,
             "gpu_launches": launches,
+            "gpu_launches_all_regions": launches * regions,
             "e2e": e2e,
             "clocks": clock_info,
             "configs": extra,
@@ -550,7 +570,10 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
     cfg = workloads.WORKLOADS["q4_0_prefill_512x12288x4096"]
     N, K = cfg["N"], cfg["K"]
     W = quantized_weights("q4_0", N, K, cfg["seed"])
-    pre = {}
+    # weight copies rotate so that each launch finds its W in HBM, not in the 129 MB L2
+    Cw = copies_for(W.numel())
+    Wr = [W] + [W.clone() for _ in range(Cw - 1)]
+    pre = {"weights": "%d rotating copies of W per timing (%.0f MB)" % (Cw, Cw * W.numel() / 1e6)}
     for M in cfg["M_sweep"]:
         x = to_dev(workloads.activations_f32(M, K, cfg["seed"] + M))
         xrb = qmm.qmm_row_bytes("q8_0", K)
@@ -560,9 +583,9 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
             qmm.qmm_quantize_q8_0(x, xq, M, K, stream=sh)
 
         def mm(i):
-            qmm.qmm_matmul_q4_0(W, xq, Y, M, N, K, stream=sh)
+            qmm.qmm_matmul_q4_0(Wr[i % Cw], xq, Y, M, N, K, stream=sh)
 
-        t = timed_graph(mm, 2)
+        t = timed_graph(mm, Cw)
         ops = 2.0 * M * N * K
         tops = ops / t / 1e12
         pre["M=%d" % M] = {"us": round(t * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
@@ -575,14 +598,17 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
     Y = torch.empty(M, N, dtype=torch.float32, device=dev)
     with torch.cuda.stream(stream):
         qmm.qmm_quantize_q8_0(x, xq, M, K, stream=sh)
+    del Wr
     for wtype in ("q8_0", "q4_1", "q5_0", "q5_1"):
         W8 = quantized_weights(wtype, N, K, cfg["seed"])
-        t = timed_graph(lambda i: qmm.matmul(wtype, W8, xq, Y, M, N, K, stream=sh), 2)
+        C8 = copies_for(W8.numel())
+        W8r = [W8] + [W8.clone() for _ in range(C8 - 1)]
+        t = timed_graph(lambda i: qmm.matmul(wtype, W8r[i % C8], xq, Y, M, N, K, stream=sh), C8)
         tops = 2.0 * M * N * K / t / 1e12
         pre["%s_weights_M=512" % wtype] = {"us": round(t * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
                                            "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4),
                                            "frac_hbm_weight_stream": round(W8.numel() / t / 1e9 / hbm, 4)}
-        del W8
+        del W8, W8r
     del x, xq, Y
     # the K-quant prefill at the decoder layer's shapes (M = 512): W_gate/W_up (Q4_K), W_down (Q6_K),
     # and the Q2_K matrix
@@ -595,11 +621,14 @@ def other_workloads(args, torch, qmm, dev, stream, timer, peaks, world, quantize
         Yk = torch.empty(M, Nk, dtype=torch.float32, device=dev)
         with torch.cuda.stream(stream):
             qmm.qmm_quantize_q8_K(xk, xqk, M, Kk, stream=sh)
-        tk = timed_graph(lambda i: qmm.matmul(wtype, Wk, xqk, Yk, M, Nk, Kk, stream=sh), 2)
+        Ck = copies_for(Wk.numel())
+        Wkr = [Wk] + [Wk.clone() for _ in range(Ck - 1)]
+        tk = timed_graph(lambda i: qmm.matmul(wtype, Wkr[i % Ck], xqk, Yk, M, Nk, Kk, stream=sh), Ck)
         tops = 2.0 * M * Nk * Kk / tk / 1e12
         kq["%s_%dx%dx%d" % (wtype, M, Nk, Kk)] = {"us": round(tk * 1e6, 2), "int8_equiv_TOPS": round(tops, 2),
-                                                  "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4)}
-        del Wk, xk, xqk, Yk
+                                                  "frac_bf16_dense_peak": round(tops / peaks["bf16_tflops"], 4),
+                                                  "frac_hbm_weight_stream": round(Wk.numel() / tk / 1e9 / hbm, 4)}
+        del Wk, Wkr, xk, xqk, Yk
     pre["k_quants_M=512"] = kq
 
     # context: the GPU's own int8 and fp16 GEMMs (cuBLAS through torch) on the M=512 shape
@@ -724,6 +753,8 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--min-timed-s", type=float, default=0.05,
+                    help="repeat the timed region of --steps steps until this much device time is timed")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -78,10 +78,11 @@ SIGNATURES = {
     "qmm_linear_noalloc": ("tpppiiiq", ctypes.c_int),
     "qmm_linear_group": ("ttppppspiiq", ctypes.c_int),
     "qmm_blocksums": ("tpppiiiq", ctypes.c_int),
+    "qmm_test_wait_timeout": ("uq", ctypes.c_int),
     "qmm_device_status": ("c", ctypes.c_int),
 }
 _CT = {"p": ctypes.c_void_p, "i": ctypes.c_int64, "s": ctypes.c_size_t, "t": ctypes.c_int, "c": ctypes.c_int,
-       "q": ctypes.c_void_p, "f": ctypes.c_float}
+       "q": ctypes.c_void_p, "f": ctypes.c_float, "u": ctypes.c_uint64}
 
 _lib = None
 
@@ -324,6 +325,10 @@ def qmm_kv_wsum(w, vc, out, scratch, scratch_bytes, Hq, Hkv, P, hd, stream=None)
 
 def qmm_blocksums(wtype, W, xq, s, M, N, K, stream=None):
     _call("qmm_blocksums", _type(wtype), ptr(W), ptr(xq), ptr(s), int(M), int(N), int(K), stream_handle(stream))
+
+
+def qmm_test_wait_timeout(limit_ns: int, stream=None):
+    _call("qmm_test_wait_timeout", int(limit_ns), stream_handle(stream))
 
 
 def qmm_device_status(clear: bool = False) -> int:

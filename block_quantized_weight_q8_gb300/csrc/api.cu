@@ -165,6 +165,19 @@ static const void* mapped_host(const void* p) {
     return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
+static __device__ unsigned int g_test_error = 0;
+
+// The failure-path test: one thread waits on an mbarrier that nothing arrives
+// at, with the library's bounded wait, and records the timeout.
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+        if (!mbar_wait_bounded(smem_u32(&bar), 0, limit_ns)) atomicOr(&g_test_error, kErrTimeout);
+    }
+}
+
 // Outputs (M * N f32 values) up to which qmm_linear_host writes y straight into
 // the caller's pinned host buffer: 256 KB.
 constexpr int64_t kDirectHostOutputs = 65536;
@@ -291,11 +304,24 @@ qmm_status qmm_linear_q5_K(const void* W, const float* x, void* s, size_t sb, fl
     return linear_impl(QMM_Q5_K, W, x, s, sb, y, M, N, K, (cudaStream_t)stream);
 }
 
+qmm_status qmm_test_wait_timeout(uint64_t limit_ns, qmm_stream_t stream) {
+    const uint64_t lim = limit_ns < 1000ull ? 1000ull : (limit_ns > 100000000ull ? 100000000ull : limit_ns);
+    wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(lim);
+    return launch_status();
+}
+
 qmm_status qmm_device_status(int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return QMM_E_CUDA;
-    const unsigned e = qmm_internal_matvec_error(clear) | qmm_internal_matmul_error(clear) |
-                       qmm_internal_matmul_kq_error(clear) | qmm_internal_getrows_error(clear) |
-                       qmm_internal_kv_error(clear);
+    unsigned e = qmm_internal_matvec_error(clear) | qmm_internal_matmul_error(clear) |
+                 qmm_internal_matmul_kq_error(clear) | qmm_internal_getrows_error(clear) |
+                 qmm_internal_kv_error(clear);
+    {
+        unsigned v = 0;
+        if (cudaMemcpyFromSymbol(&v, g_test_error, sizeof(v)) != cudaSuccess) return QMM_E_CUDA;
+        e |= v;
+        const unsigned z = 0;
+        if (clear && cudaMemcpyToSymbol(g_test_error, &z, sizeof(z)) != cudaSuccess) return QMM_E_CUDA;
+    }
     if (cudaGetLastError() != cudaSuccess) return QMM_E_CUDA;
     if (e & 1u) return QMM_E_TIMEOUT;  // a device wait ran out of time
     if (e & 2u) return QMM_E_SHAPE;    // qmm_get_rows met an index outside [0, N)

@@ -427,13 +427,27 @@ QMM_API qmm_status qmm_kv_wsum(const float* w, const void* vc, float* out, void*
  * bsum_2s+1)); Q2_K: (sum_g sc_g*dot_g, sum_g m_g*bsum_g); Q6_K: (sum_g sc_g *
  * dot_g with the stored codes 0..63, sum_g sc_g*bsum_g), whose integer is
  * value - 32*min; Q5_K as Q4_K.  Q5_0 gives sum (q-16)*a per block, Q4_1 and
- * Q5_1 sum q*a (their min meets the activation's own code sum).  s: int32 [M][N][per-row count], computed by the same device
- * decode routines the matvec uses. */
+ * Q5_1 sum q*a (their min meets the activation's own code sum).  s: int32
+ * [M][N][per-row count], computed by the matvec's per-block decode routines
+ * (the super-unit decoders it takes when K % 256 == 0 are checked through
+ * outputs that are exact integers instead).  One generic call for every weight
+ * type, where the per-type calls of the multiply would add nine names for a
+ * test hook. */
 QMM_API qmm_status qmm_blocksums(int wtype, const void* W, const void* xq, int32_t* s, int64_t M, int64_t N, int64_t K,
                          qmm_stream_t stream);
 
-/* Reads (and with clear != 0 resets) the device error word that bounded waits
- * set when they run out.  Synchronizes the device.  QMM_OK when no wait ran out. */
+/* A test of the failure path ([krafla] "Architecture", Error handling: status
+ * codes, no library code aborts): launches one thread that waits, through the
+ * same bounded wait every kernel here uses for its copies, on an mbarrier that
+ * nothing arrives at, for limit_ns nanoseconds (clamped to 1 us .. 100 ms).  The
+ * wait runs out, records QMM_E_TIMEOUT in the device error word and returns;
+ * qmm_device_status() then reports QMM_E_TIMEOUT and the context stays usable.
+ * Returns QMM_E_CUDA if the launch fails. */
+QMM_API qmm_status qmm_test_wait_timeout(uint64_t limit_ns, qmm_stream_t stream);
+
+/* Reads (and with clear != 0 resets) the device error words that bounded waits
+ * (QMM_E_TIMEOUT) and qmm_get_rows (QMM_E_SHAPE for an id outside [0, N)) set.
+ * Synchronizes the device.  QMM_OK when nothing was recorded. */
 QMM_API qmm_status qmm_device_status(int clear);
 
 #ifdef __cplusplus

@@ -184,3 +184,23 @@ def test_linear_host_matches_linear(wtype, M, N, K, pinned):
     y2 = torch.empty(M, N, dtype=torch.float32, device="cuda")
     qmm.linear(wtype, W, dev(x), scratch, sb, y2, M, N, K)
     assert np.array_equal(y_host.numpy().view(np.uint32), host(y2).view(np.uint32))
+
+
+# ------------------------------------------------------------------ failure path
+def test_bounded_wait_runs_out_and_reports():
+    """[krafla] "Architecture", Error handling (status codes, nothing aborts): a wait on an
+    mbarrier that nothing arrives at, limited to 1 ms, ends, records QMM_E_TIMEOUT for
+    qmm_device_status, and leaves the context usable (a multiply right after is still correct
+    and the cleared status reads OK)."""
+    assert qmm.qmm_device_status(clear=True) == 0
+    qmm.qmm_test_wait_timeout(1_000_000)
+    assert qmm.qmm_device_status(clear=False) == 7  # QMM_E_TIMEOUT, still set until cleared
+    assert qmm.qmm_device_status(clear=True) == 7
+    assert qmm.qmm_device_status(clear=False) == 0
+    N, K = 300, 1024
+    W = oracle.quantize("q8_0", workloads.weights_f32(N, K, seed=70))
+    X = oracle.quantize("q8_0", workloads.activations_f32(1, K, seed=71))
+    y = torch.empty(N, dtype=torch.float32, device="cuda")
+    qmm.matvec("q8_0", dev(W), dev(X), y, N, K)
+    assert_rows_close(host(y), oracle.matmul("q8_0", W, X, 1, N, K))
+    assert qmm.qmm_device_status(clear=True) == 0

@@ -236,11 +236,11 @@ def test_matmul_deterministic(wtype):
 
 # integer weight ranges whose quantization gives d = 1 (and m = 0) exactly, codes equal to the values,
 # given the extremes each block is forced to hold
-INT_RANGES = {"q8_0": (-127, 127, (127, -127)), "q5_0": (-16, 15, (-16,)), "q4_1": (0, 15, (0, 15)),
-              "q5_1": (0, 31, (0, 31))}
+INT_RANGES = {"q4_0": (-8, 7, (-8,)), "q8_0": (-127, 127, (127, -127)), "q5_0": (-16, 15, (-16,)),
+              "q4_1": (0, 15, (0, 15)), "q5_1": (0, 31, (0, 31))}
 
 
-@pytest.mark.parametrize("wtype", ["q8_0", "q5_0", "q4_1", "q5_1"])
+@pytest.mark.parametrize("wtype", ["q4_0", "q8_0", "q5_0", "q4_1", "q5_1"])
 @pytest.mark.parametrize("M,N,K", [(8, 128, 256), (130, 300, 1024)])
 def test_matmul_integer_sums_exact(wtype, M, N, K):
     """Integer-valued rows quantize to d = 1 (m = 0) with codes equal to the values (weights: the format's
