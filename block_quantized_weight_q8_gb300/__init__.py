@@ -19,7 +19,7 @@ TYPES = {"q4_0": QMM_Q4_0, "q8_0": QMM_Q8_0, "q4_K": QMM_Q4_K, "q6_K": QMM_Q6_K,
 WEIGHT_TYPES = ("q4_0", "q8_0", "q4_K", "q6_K", "q2_K", "q4_1", "q5_0", "q5_1", "q5_K")
 
 STATUS = {0: "QMM_OK", 1: "QMM_E_NULL", 2: "QMM_E_SHAPE", 3: "QMM_E_TYPE", 4: "QMM_E_ALIGN",
-          5: "QMM_E_SCRATCH", 6: "QMM_E_CUDA", 7: "QMM_E_TIMEOUT"}
+          5: "QMM_E_SCRATCH", 6: "QMM_E_CUDA", 7: "QMM_E_TIMEOUT", 8: "QMM_E_BOUNDS"}
 
 # every entry point the header declares, with its argument kinds
 # p: pointer, i: int64, s: size_t, t: int (type code), c: int, q: stream
@@ -93,11 +93,14 @@ class QmmError(RuntimeError):
         super().__init__("%s failed: %s (%s)" % (fn, STATUS.get(status, status), _status_str(status)))
 
 
-def load(path: str = LIB):
-    """Load libqmm.so (built in-tree by build()); raises if it is missing."""
+def load(path: str = None):
+    """Load libqmm.so (built in-tree by build()); raises if it is missing.  The environment
+    variable QMM_LIBRARY names another build of the same library to load instead (the
+    bounds-checked variant, block_quantized_weight_q8_gb300.buildlib.CHECKED_LIB)."""
     global _lib
     if _lib is not None:
         return _lib
+    path = path or os.environ.get("QMM_LIBRARY") or LIB
     if not os.path.exists(path):
         raise ImportError("libqmm.so is not built (%s): run block_quantized_weight_q8_gb300.build()" % path)
     L = ctypes.CDLL(path)

@@ -191,6 +191,7 @@ unsigned qmm_internal_matvec_error(int clear);
 unsigned qmm_internal_matmul_kq_error(int clear);
 unsigned qmm_internal_getrows_error(int clear);
 unsigned qmm_internal_kv_error(int clear);
+unsigned qmm_internal_quantize_error(int clear);
 
 qmm_status qmm_linear_group(int wtype, int G, const void* const* W, const int64_t* N, const float* x, void* xq_scratch,
                             size_t scratch_bytes, float* const* y, int64_t M, int64_t K, qmm_stream_t stream) {
@@ -262,6 +263,7 @@ const char* qmm_status_str(qmm_status s) {
     case QMM_E_SCRATCH: return "the scratch buffer is too small";
     case QMM_E_CUDA: return "a CUDA runtime call or kernel launch failed";
     case QMM_E_TIMEOUT: return "a bounded device wait ran out";
+    case QMM_E_BOUNDS: return "a kernel index fell outside its buffer (bounds-checked build)";
     default: return "unknown status";
     }
 }
@@ -314,7 +316,7 @@ qmm_status qmm_device_status(int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return QMM_E_CUDA;
     unsigned e = qmm_internal_matvec_error(clear) | qmm_internal_matmul_error(clear) |
                  qmm_internal_matmul_kq_error(clear) | qmm_internal_getrows_error(clear) |
-                 qmm_internal_kv_error(clear);
+                 qmm_internal_kv_error(clear) | qmm_internal_quantize_error(clear);
     {
         unsigned v = 0;
         if (cudaMemcpyFromSymbol(&v, g_test_error, sizeof(v)) != cudaSuccess) return QMM_E_CUDA;
@@ -323,8 +325,9 @@ qmm_status qmm_device_status(int clear) {
         if (clear && cudaMemcpyToSymbol(g_test_error, &z, sizeof(z)) != cudaSuccess) return QMM_E_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return QMM_E_CUDA;
-    if (e & 1u) return QMM_E_TIMEOUT;  // a device wait ran out of time
-    if (e & 2u) return QMM_E_SHAPE;    // qmm_get_rows met an index outside [0, N)
+    if (e & kErrTimeout) return QMM_E_TIMEOUT;  // a device wait ran out of time
+    if (e & kErrBounds) return QMM_E_BOUNDS;    // an index check of a bounds-checked build failed
+    if (e & 2u) return QMM_E_SHAPE;             // qmm_get_rows met an index outside [0, N)
     return QMM_OK;
 }
 

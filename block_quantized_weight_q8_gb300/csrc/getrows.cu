@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(256) getrows_kernel(const uint8_t* __restrict_
         } else {
             dequant32<WT>(W + (uint64_t)id * rb, s, v);
         }
+        if (!QMM_IN_BOUNDS(g_getrows_error, r * (int64_t)K + 32 * s + 31, R * (int64_t)K)) continue;
         float4* o = reinterpret_cast<float4*>(out + r * (int64_t)K + 32 * s);
 #pragma unroll
         for (int j = 0; j < 8; j++) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);

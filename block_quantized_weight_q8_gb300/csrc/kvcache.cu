@@ -107,9 +107,12 @@ __global__ void __launch_bounds__(256) kv_scores_kernel(const uint8_t* __restric
         if (threadIdx.x == 0) {
             mbar_init(smem_u32(bar), 1);
             fence_mbar_init();
-            const uint32_t bytes = (uint32_t)(R * rb);
+            uint32_t bytes = (uint32_t)(R * rb);
+            if (!QMM_IN_BOUNDS(g_kv_error, 16 + (int64_t)bytes - 1, dynamic_smem_bytes()) ||
+                !QMM_IN_BOUNDS(g_kv_error, (p0 * Hkv * rb) + bytes - 1, P * Hkv * rb))
+                bytes = 0;  // the tile must fit the shared buffer and lie inside the cache
             mbar_arrive_expect_tx(smem_u32(bar), bytes);
-            bulk_g2s(smem_u32(ks), src, bytes, smem_u32(bar), policy_evict_first());
+            if (bytes) bulk_g2s(smem_u32(ks), src, bytes, smem_u32(bar), policy_evict_first());
         }
         __syncthreads();
         const bool ok = mbar_wait_bounded(smem_u32(bar), 0, kWaitLimitNs);
@@ -119,7 +122,10 @@ __global__ void __launch_bounds__(256) kv_scores_kernel(const uint8_t* __restric
         }
     } else {
         const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src);
-        for (int i = threadIdx.x; i < R * nwd; i += blockDim.x) cp_async4(ks + i, s4 + i);
+        for (int i = threadIdx.x; i < R * nwd; i += blockDim.x)
+            if (QMM_IN_BOUNDS(g_kv_error, p0 * Hkv * rb + 4 * (int64_t)i + 3, P * Hkv * rb) &&
+                QMM_IN_BOUNDS(g_kv_error, 16 + 4 * (int64_t)i + 3, dynamic_smem_bytes()))
+                cp_async4(ks + i, s4 + i);
         cp_async_wait_all();
         __syncthreads();
     }
@@ -183,8 +189,9 @@ __global__ void __launch_bounds__(256) kv_scores_kernel(const uint8_t* __restric
         for (; m < 8; m <<= 1) acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], m);
         if (live && j < GT && gl < G) {
             const float dk = __uint_as_float(kr[0]);
-            scores[(int64_t)(kvh * G + gl) * P + p0 + pl] =
-                __fmul_rn(__fmul_rn(__fmul_rn(dq, dk), (float)acc[0]), scale);
+            if (QMM_IN_BOUNDS(g_kv_error, (int64_t)(kvh * G + gl) * P + p0 + pl, (int64_t)Hkv * G * P))
+                scores[(int64_t)(kvh * G + gl) * P + p0 + pl] =
+                    __fmul_rn(__fmul_rn(__fmul_rn(dq, dk), (float)acc[0]), scale);
         }
     }
     // the next kernel may launch once every CTA is here (or has left): launched
@@ -226,21 +233,24 @@ __global__ void __launch_bounds__(512) kv_wsum_partial_kernel(const float* __res
     if (use_bulk && threadIdx.x == 0) {
         mbar_init(smem_u32(bar), 1);
         fence_mbar_init();
-        const uint32_t bytes = (uint32_t)((int64_t)n * Hkv * rb);
+        uint32_t bytes = (uint32_t)((int64_t)n * Hkv * rb);
+        if (!QMM_IN_BOUNDS(g_kv_error, (pa * Hkv + kv0) * rb + bytes - 1, P * Hkv * rb)) bytes = 0;
         mbar_arrive_expect_tx(smem_u32(bar), bytes);
-        bulk_g2s(smem_u32(vs), src, bytes, smem_u32(bar), policy_evict_first());
+        if (bytes) bulk_g2s(smem_u32(vs), src, bytes, smem_u32(bar), policy_evict_first());
     }
     if (!use_bulk) {  // position p's hn rows are one run of hn * nwd words
         const int run = hn * nwd;
         for (int i = threadIdx.x; i < n * run; i += blockDim.x) {
             const int pp = i / run, k = i - pp * run;
-            cp_async4(vs + (size_t)pp * run + k,
-                      reinterpret_cast<const uint32_t*>(src + (int64_t)pp * Hkv * rb) + k);
+            if (QMM_IN_BOUNDS(g_kv_error, (pa * Hkv + kv0) * rb + (int64_t)pp * Hkv * rb + 4 * k + 3, P * Hkv * rb))
+                cp_async4(vs + (size_t)pp * run + k,
+                          reinterpret_cast<const uint32_t*>(src + (int64_t)pp * Hkv * rb) + k);
         }
     }
     for (int i = threadIdx.x; i < hn * G * n; i += blockDim.x) {
         const int hh = i / n, j = i - hh * n;
-        cp_async4(ws + hh * kKvChunk + j, w + (int64_t)(kv0 * G + hh) * P + pa + j);
+        if (QMM_IN_BOUNDS(g_kv_error, (int64_t)(kv0 * G + hh) * P + pa + j, (int64_t)Hq * P))
+            cp_async4(ws + hh * kKvChunk + j, w + (int64_t)(kv0 * G + hh) * P + pa + j);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -301,7 +311,9 @@ __global__ void __launch_bounds__(256) kv_wsum_reduce_kernel(const float* __rest
     float s = 0.0f;
     if (o < outs) {
 #pragma unroll 8
-        for (int c = warp; c < nc; c += 8) s = __fadd_rn(s, part[(int64_t)c * outs + o]);
+        for (int c = warp; c < nc; c += 8)
+            if (QMM_IN_BOUNDS(g_kv_error, (int64_t)c * outs + o, (int64_t)nc * outs))
+                s = __fadd_rn(s, part[(int64_t)c * outs + o]);
     }
     red[warp][lane] = s;
     __syncthreads();

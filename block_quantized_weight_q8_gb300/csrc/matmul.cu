@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         return;
     }
     using L = Lay<WT>;
+    if (!QMM_IN_BOUNDS(g_matmul_error, L::SMEM_BYTES - 1, dynamic_smem_bytes())) return;  // the layout must fit
     constexpr int SC_SLOTS = L::SC_SLOTS, SCP = L::SCP, W_RAW = L::W_RAW, RAW_BYTES = L::RAW_BYTES, WB = L::WB,
                   PAIRS = L::PAIRS;
     const Bars bars{sbase + L::OFF_BAR, PAIRS};
@@ -493,7 +494,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 32; j++) {
                 const int t = t0 + cg * 32 + j;
                 const uint32_t bits = (j & 1) ? (uint32_t)(acc[j >> 1] >> 32) : (uint32_t)acc[j >> 1];
-                if (t < M) Y[(size_t)t * N + o] = __uint_as_float(bits);
+                if (t < M && QMM_IN_BOUNDS(g_matmul_error, (size_t)t * N + o, (size_t)M * N))
+                    Y[(size_t)t * N + o] = __uint_as_float(bits);
             }
         }
     }

@@ -468,7 +468,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (sb < nsb) {
                 const uint64_t a = ((uint64_t)sb * BBs) & ~15ull;
                 const uint32_t dst = sbase + L::OFF_RAW + (uint32_t)((sb & 1) * L::RAW_STAGE) + raw_role + (uint32_t)r * 16u;
-                for (int c = 0; c < NC; c++) cp_async16(dst + (uint32_t)c * 2048u, src + a + 16 * c);
+                // the chunks stay inside the row (its bytes rounded up to 16: rows are 16-byte multiples)
+                if (QMM_IN_BOUNDS(g_matmul_kq_error, a + 16 * NC - 1, is_w ? (int64_t)rb : (int64_t)xrb))
+                    for (int c = 0; c < NC; c++) cp_async16(dst + (uint32_t)c * 2048u, src + a + 16 * c);
             }
             cp_async_commit();  // possibly empty: one group per super-block keeps the count uniform
         };
@@ -672,7 +674,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 32; j++) {
                 const int t = t0 + cg * 32 + j;
                 const uint32_t bits = (j & 1) ? (uint32_t)(acc[j >> 1] >> 32) : (uint32_t)acc[j >> 1];
-                if (t < M) Y[(size_t)t * N + o] = __uint_as_float(bits);
+                if (t < M && QMM_IN_BOUNDS(g_matmul_kq_error, (size_t)t * N + o, (size_t)M * N))
+                    Y[(size_t)t * N + o] = __uint_as_float(bits);
             }
         }
     }

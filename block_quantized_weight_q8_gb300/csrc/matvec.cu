@@ -126,11 +126,12 @@ struct SegGeom {
 // Issues the bulk copy of the bytes [g0, g1) of W, as their 16-byte aligned
 // superset (the last < 16 bytes of W excepted), into a slot.
 __device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t g0, uint64_t g1, uint64_t total_al,
-                                           uint8_t* slot, uint32_t bar, uint64_t pol) {
+                                           uint8_t* slot, uint32_t bar, uint64_t pol, uint32_t slot_bytes) {
     const uint64_t a0 = g0 & ~15ull;
     uint64_t a1 = (g1 + 15ull) & ~15ull;
     if (a1 > total_al) a1 = total_al;
-    const uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
+    uint32_t bytes = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
+    if (!QMM_IN_BOUNDS(g_matvec_error, bytes, (int64_t)slot_bytes + 1)) bytes = 0;  // the copy must fit its slot
     mbar_arrive_expect_tx(bar, bytes);
     if (bytes) bulk_g2s(smem_u32(slot), W + a0, bytes, bar, pol);
 }
@@ -270,7 +271,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
         pol = policy_evict_first();
         if (my_items > 0) {
             const int s0 = s_begin + warp * item_segs;
-            issue_item(W, geo.off(s0), geo.off(min(s0 + item_segs, s_end)), total_al, slots, smem_u32(&full[0]), pol);
+            issue_item(W, geo.off(s0), geo.off(min(s0 + item_segs, s_end)), total_al, slots, smem_u32(&full[0]), pol,
+                       slot_bytes);
         }
     }
     __syncwarp();
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
         for (int k = 1; k < depth && k < my_items; k++) {
             const int s0 = s_begin + (warp + k * nw) * item_segs;
             issue_item(W, geo.off(s0), geo.off(min(s0 + item_segs, s_end)), total_al, slots + (size_t)k * slot_bytes,
-                       smem_u32(&full[k]), pol);
+                       smem_u32(&full[k]), pol, slot_bytes);
         }
     }
 
@@ -373,7 +375,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
             if (seg == (SPLIT ? N * pieces : N) - 1 && total > total_al) {
                 // the last < 16 bytes of W lie in the last segment: not reachable
                 // by a 16-byte bulk copy, so this warp fetches them itself
-                for (uint64_t i = total_al + li; i < total; i += lpr) sbuf[i - a0] = W[i];
+                for (uint64_t i = total_al + li; i < total; i += lpr)
+                    if (QMM_IN_BOUNDS(g_matvec_error, i - a0, slot_bytes)) sbuf[i - a0] = W[i];
             }
             __syncwarp();
             float acc = 0.0f;
@@ -385,6 +388,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                     un = min(piece_units, geo.nunit - u0);
                 }
                 const uint32_t so = (uint32_t)(geo.off(seg) - a0);
+                // the segment's bytes must lie inside the slot the item was copied to
+                const int64_t seg_end = (int64_t)so + (int64_t)un * (SU ? geo.ubytes : F::BB);
+                if (!QMM_IN_BOUNDS(g_matvec_error, seg_end - 1, slot_bytes)) un = 0;
                 if constexpr (SU) {
                     for (int u = li; u < un; u += lpr) {
                         const int ug = u0 + u;
@@ -403,15 +409,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
             }
             for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (seg < s1 && li == 0) {
-                if constexpr (SPLIT) part[seg - s_begin] = acc;
-                else y[seg] = acc;
+                if constexpr (SPLIT) {
+                    if (QMM_IN_BOUNDS(g_matvec_error, seg - s_begin, s_end - s_begin)) part[seg - s_begin] = acc;
+                } else if (QMM_IN_BOUNDS(g_matvec_error, seg, N)) {
+                    y[seg] = acc;
+                }
             }
         }
         __syncwarp();
         if (lane == 0 && k + depth < my_items) {
             const int q0 = s_begin + (warp + (k + depth) * nw) * item_segs;
             issue_item(W, geo.off(q0), geo.off(min(q0 + item_segs, s_end)), total_al, sbuf, smem_u32(&full[slot]),
-                       pol);
+                       pol, slot_bytes);
         }
     }
     if constexpr (SPLIT) {
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
             for (int r = r_begin + tid; r < r_end; r += blockDim.x) {
                 float v = 0.0f;
                 for (int p = 0; p < pieces; p++) v += part[(r - r_begin) * pieces + p];
-                y[r] = v;
+                if (QMM_IN_BOUNDS(g_matvec_error, r, N)) y[r] = v;
             }
         }
     }
@@ -453,7 +462,8 @@ __global__ void __launch_bounds__(kThreads) blocksums_kernel(const uint8_t* __re
     const int r1 = min(r0 + rows_per_cta, N);
     const uint64_t a0 = ((uint64_t)r0 * rb) & ~15ull;
     const uint64_t g1 = (uint64_t)r1 * rb;
-    for (uint64_t i = a0 + threadIdx.x; i < g1; i += blockDim.x) wbuf[i - a0] = W[i];
+    for (uint64_t i = a0 + threadIdx.x; i < g1; i += blockDim.x)
+        if (QMM_IN_BOUNDS(g_matvec_error, i - a0, (uint64_t)rows_per_cta * rb + 16)) wbuf[i - a0] = W[i];
     __syncthreads();
 
     const ActView act{aq, ad, as, nd};
@@ -463,6 +473,8 @@ __global__ void __launch_bounds__(kThreads) blocksums_kernel(const uint8_t* __re
         const int row = r0 + i / units, u = i % units;
         const uint32_t o = (uint32_t)((uint64_t)row * rb - a0) + (uint32_t)(u * F::BB);
         int32_t* dst = out + ((uint64_t)t * N + row) * per;
+        if (!QMM_IN_BOUNDS(g_matvec_error, ((uint64_t)t * N + row) * per + u * (per / units), (uint64_t)gridDim.y * N * per))
+            continue;
         uint32_t db, dmb;
         int v = 0, m = 0;
         if constexpr (WT == QMM_Q4_0) v = q4_0_isum(wv, o, act, u, &db);

@@ -144,6 +144,29 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate copy
 constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrBounds = 4u;  // an index outside its buffer (bounds-checked builds only)
+
+// Bounds-checked builds (compiled with -DQMM_CHECK_BOUNDS): QMM_IN_BOUNDS(err, i, n)
+// is true when 0 <= i < n; otherwise it records kErrBounds in the translation
+// unit's device error word `err` and is false, so that the access it guards is
+// skipped instead of faulting.  qmm_device_status() reports the record as
+// QMM_E_BOUNDS.  In normal builds it is the constant true and its arguments are
+// not evaluated.
+#ifdef QMM_CHECK_BOUNDS
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t v;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+    return v;
+}
+__device__ __forceinline__ bool in_bounds_or_record(unsigned int* err, int64_t i, int64_t n) {
+    if (i >= 0 && i < n) return true;
+    atomicOr(err, kErrBounds);
+    return false;
+}
+#define QMM_IN_BOUNDS(err, i, n) ::qmm::in_bounds_or_record(&(err), (int64_t)(i), (int64_t)(n))
+#else
+#define QMM_IN_BOUNDS(err, i, n) true
+#endif
 
 // ---------------------------------------------------------------- unaligned byte reader
 // A view of bytes in shared memory at a 2-byte-aligned offset.  word(i) returns

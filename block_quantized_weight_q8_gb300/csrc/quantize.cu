@@ -14,6 +14,8 @@
 
 namespace qmm {
 
+static __device__ unsigned int g_quantize_error = 0;  // bounds records of a bounds-checked build
+
 // ---------------------------------------------------------------- Q8_0 activations
 // [minfer] "10 . CPU matmul: quantized weights x Q8_0 activations" s3.2 (the
 // activation quantizers): per 32 values amax = max|x|, d = amax/127 stored as
@@ -31,7 +33,7 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4* __rest
     }
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t b = gt >> 3;
-    const bool active = b < nblocks;
+    const bool active = b < nblocks && QMM_IN_BOUNDS(g_quantize_error, b * 34 + 33, nblocks * 34);
     const float4 v = active ? x[gt] : make_float4(0.f, 0.f, 0.f, 0.f);
     quant_q8_0_part(v, active, (int)(gt & 7), out + (active ? b * 34 : 0));
 }
@@ -50,6 +52,7 @@ __global__ void __launch_bounds__(256) quantize_q8_K_kernel(const float4* __rest
     const int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (b >= nblocks) return;  // whole warps leave together
+    if (!QMM_IN_BOUNDS(g_quantize_error, b * 292 + 291, nblocks * 292)) return;
     quant_q8_K_lane(x[b * 64 + 2 * lane], x[b * 64 + 2 * lane + 1], lane, out + b * 292);
 }
 
@@ -526,6 +529,16 @@ qmm_status qmm_quantize_q5_1(const float* w, void* wq, int64_t N, int64_t K, qmm
 }
 qmm_status qmm_quantize_q5_K(const float* w, void* wq, int64_t N, int64_t K, qmm_stream_t stream) {
     return launch_weight_quant(quantize_q5_K_kernel, QMM_Q5_K, w, wq, N, K, (cudaStream_t)stream);
+}
+
+unsigned qmm_internal_quantize_error(int clear) {
+    unsigned v = 0;
+    cudaMemcpyFromSymbol(&v, g_quantize_error, sizeof(v));
+    if (clear) {
+        const unsigned z = 0;
+        cudaMemcpyToSymbol(g_quantize_error, &z, sizeof(z));
+    }
+    return v;
 }
 
 }  // extern "C"

@@ -83,7 +83,9 @@ typedef enum {
     QMM_E_ALIGN = 4,    /* a base pointer is not 16-byte aligned */
     QMM_E_SCRATCH = 5,  /* a caller scratch buffer is too small */
     QMM_E_CUDA = 6,     /* a CUDA runtime call or kernel launch failed */
-    QMM_E_TIMEOUT = 7   /* a bounded device wait ran out (see qmm_device_status) */
+    QMM_E_TIMEOUT = 7,  /* a bounded device wait ran out (see qmm_device_status) */
+    QMM_E_BOUNDS = 8    /* a kernel index fell outside its buffer and the access was
+                           skipped: only a library built with -DQMM_CHECK_BOUNDS checks */
 } qmm_status;
 
 /* Block types.  Byte sizes per block: Q4_0 18 B / 32 values, Q8_0 34 B / 32,
@@ -446,8 +448,10 @@ QMM_API qmm_status qmm_blocksums(int wtype, const void* W, const void* xq, int32
 QMM_API qmm_status qmm_test_wait_timeout(uint64_t limit_ns, qmm_stream_t stream);
 
 /* Reads (and with clear != 0 resets) the device error words that bounded waits
- * (QMM_E_TIMEOUT) and qmm_get_rows (QMM_E_SHAPE for an id outside [0, N)) set.
- * Synchronizes the device.  QMM_OK when nothing was recorded. */
+ * (QMM_E_TIMEOUT), qmm_get_rows (QMM_E_SHAPE for an id outside [0, N)) and, in a
+ * bounds-checked build, the kernels' index checks (QMM_E_BOUNDS) set; a timeout
+ * is reported first, then a bounds record.  Synchronizes the device.  QMM_OK
+ * when nothing was recorded. */
 QMM_API qmm_status qmm_device_status(int clear);
 
 #ifdef __cplusplus
