@@ -14,25 +14,26 @@
 // Each block's sum is then folded into an fp32 accumulator once, scaled by
 // d_w * d_x, exactly as the pages' kernels fold per block.
 //
-// One CTA per output tile of 128 weight rows x 128 tokens, 28 warps:
-//   warp 0   producer: 2-D TMA loads of the raw weight bytes (128 rows x 8 blocks)
+// One CTA per output tile of 128 weight rows x 128 tokens, 26 warps:
+//   warp 24  producer: 2-D TMA loads of the raw weight bytes (128 rows x 8 blocks)
 //            and the raw activation bytes (128 tokens x 8 blocks) into a ring of
 //            raw stages; also owns the tensor-memory allocation
-//   warp 1   MMA issuer: per pair of blocks, two tcgen05.mma (K = 16 each) per
-//            block into its own 128-column TMEM accumulator, then one
-//            tcgen05.commit for the pair
-//   warps 2-4, 6-8, 10-11  converters (four for weight rows, four for tokens):
-//            each thread loads its row of the raw stage into registers with
-//            16-byte loads, then writes each block as fp16 operands in the UMMA
-//            K-major core-matrix layout (8 rows x 16 bytes per core matrix) plus
-//            its f32 scale; warps 5 and 9 stay idle so that the MMA issuer's
-//            scheduler carries no converter work
-//   warps 12-27 epilogue: tcgen05.ld of each block's exact sums (32 tokens of one
+//   warp 25  MMA issuer: per block, two tcgen05.mma (K = 16 each) with the
+//            weight operand read from TMEM and the activation operand from shared
+//            memory, into one of three 128-column TMEM accumulators; one
+//            tcgen05.commit frees the operand slot, another hands over the sums
+//   warps 16-19 weight converters: each thread turns its row's blocks into fp16
+//            operands and stores them straight into its TMEM lane (tcgen05.st;
+//            warp % 4 is that lane quadrant), plus the f32 scale
+//   warps 20-23 activation converters: each thread turns its token's blocks
+//            into fp16 operands in the UMMA K-major core-matrix layout (8 rows x
+//            16 bytes per core matrix) in shared memory, plus the f32 scale
+//   warps 0-15 epilogue: tcgen05.ld of each block's exact sums (32 tokens of one
 //            weight row per thread), y += v * (d_w*d_x) in registers in block
 //            order, then the token-major store
-// Blocks move between the roles in pairs (one barrier handshake per two blocks);
-// all waits are bounded; a timeout records QMM_E_TIMEOUT, every warp still
-// reaches the end, and TMEM is freed.
+// The weight operand never passes through shared memory, so the tensor core
+// reads only the activation tile from it.  All waits are bounded; a timeout
+// records QMM_E_TIMEOUT, every warp still reaches the end, and TMEM is freed.
 #include <cuda.h>
 #include <mutex>
 
@@ -56,21 +57,30 @@ constexpr int BM = 128;            // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;            // tokens per tile (MMA N, TMEM columns per accumulator)
 constexpr int KB = 8;              // Q blocks per raw stage (256 K values)
 constexpr int RAW_STAGES = 2;
-constexpr int ACC_PAIRS = 2;       // accumulator pairs: two blocks' sums per handshake (4 x 128 columns)
+constexpr int S_BUFS = 3;          // per-block sum accumulators in TMEM, 128 columns each
+constexpr int OP_SLOTS = 4;        // operand slots: weights in TMEM (16 columns), activations in shared memory
+constexpr int A_COL0 = S_BUFS * BN;  // TMEM column of weight operand slot 0 (after the accumulators)
+constexpr int TMEM_COLS = 512;
+static_assert(A_COL0 + OP_SLOTS * 16 <= TMEM_COLS, "TMEM layout");
+// One tcgen05.commit per block signals "the MMAs of block b are done" on
+// mma_done[b % DONE_RING]: the epilogue waits for it to read block b's sums, the
+// converters to reuse block b's operand slot for block b + OP_SLOTS.  A barrier
+// is reused DONE_RING blocks later, which neither waiter can reach first: the
+// MMAs of block b + DONE_RING need the epilogue to have released block
+// b + DONE_RING - S_BUFS > b, and the converters' operands of that block.
+constexpr int DONE_RING = 8;
+static_assert(DONE_RING >= S_BUFS + 3 && DONE_RING >= OP_SLOTS + 2 && (DONE_RING & (DONE_RING - 1)) == 0,
+              "mma_done ring");
 constexpr int X_RAW = BN * KB * 34;   // 34816
-constexpr int OP_A = BM * 32 * 2;     // 8192: fp16 weights of one block
 constexpr int OP_B = BN * 32 * 2;     // 8192: fp16 activations of one block
-constexpr int NUM_CONV_WARPS = 8, NUM_EPI_WARPS = 16;  // converters: 4 for weights, 4 for activations
-// Warps 0-11: producer (0), MMA issuer (1), converters (2-4, 6-8, 10-11), two
-// idle warps (5, 9) that keep the MMA issuer's scheduler free of converter work;
-// warps 12-27: epilogue (warp % 4 is the TMEM lane quadrant it may read).
-constexpr int EPI0 = 12;
-constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 896
-constexpr int TMEM_COLS = 2 * ACC_PAIRS * BN;  // 512: four 128-column accumulators
-
-__device__ __forceinline__ int converter_index(int warp) {  // 0..7, or -1 for other warps
-    return (warp >= 2 && warp < EPI0 && warp != 5 && warp != 9) ? warp - 2 - (warp > 5) - (warp > 9) : -1;
-}
+constexpr int NUM_EPI_WARPS = 16, NUM_W_WARPS = 4, NUM_X_WARPS = 4;
+constexpr int NUM_CONV_WARPS = NUM_W_WARPS + NUM_X_WARPS;
+// Warps 0-15: epilogue (warp % 4 is the TMEM lane quadrant it may read, warp / 4
+// its 32 tokens); 16-19: weight converters (warp % 4 = the lane quadrant of the
+// 32 rows each writes into TMEM); 20-23: activation converters; 24: TMA producer
+// (and the TMEM allocation); 25: MMA issuer.
+constexpr int W0 = NUM_EPI_WARPS, X0 = W0 + NUM_W_WARPS, TMA_WARP = X0 + NUM_X_WARPS, MMA_WARP = TMA_WARP + 1;
+constexpr int THREADS = (MMA_WARP + 1) * 32;  // 832
 
 // Weight block bytes of the 32-value formats (Q4_0 18, Q8_0 34, Q4_1 20, Q5_0 22, Q5_1 24).
 __host__ __device__ constexpr int block_bytes32(int wt) {
@@ -78,30 +88,31 @@ __host__ __device__ constexpr int block_bytes32(int wt) {
 }
 
 // Shared memory layout per weight format (offsets from the 1024-byte aligned
-// dynamic shared memory base).  Q4_0 keeps 32 scale slots; the larger raw stages
-// of the other formats leave room for 16.  (A third operand pair for Q4_0, in
-// place of 16 scale slots, measured no faster.)  Q4_1 and Q5_1 also carry each
-// row's m_w and each token's d_x * sum(a) per block, for the min term.
+// dynamic shared memory base): the raw stages, the activation operand slots and
+// the per-block scales.  Q4_1 and Q5_1 also carry each row's m_w and each
+// token's d_x * sum(a) per block, for the min term.
 template <int WT>
 struct Lay {
     static constexpr int WB = block_bytes32(WT);
     static constexpr bool HAS_MIN = WT == QMM_Q4_1 || WT == QMM_Q5_1;
-    static constexpr int PAIRS = 2;                             // operand pair slots (converted blocks in flight / 2)
-    static constexpr int OPS = 2 * PAIRS;
-    static constexpr int SC_SLOTS = WT == QMM_Q4_0 ? 32 : 16;  // block scales in flight (outlive the operands)
-    static constexpr int SCP = SC_SLOTS / 2;                   // ... in pairs
+    // Blocks of scales in flight.  A slot is rewritten for block b by a converter
+    // that has waited for the MMAs of block b - OP_SLOTS, which the MMA issuer
+    // started only after the epilogue released the sums of block
+    // b - OP_SLOTS - S_BUFS; the epilogue works in block order, so it had
+    // finished every read of block b - OP_SLOTS - S_BUFS - 1 and earlier.
+    static constexpr int SC_SLOTS = 16;
+    static_assert(SC_SLOTS >= OP_SLOTS + S_BUFS + 1, "scale slots must outlive the epilogue's reads");
     static constexpr int W_RAW = BM * KB * WB;
     static constexpr int RAW_BYTES = W_RAW + X_RAW;
     static constexpr int OFF_RAW = 0;
-    static constexpr int OFF_OPA = OFF_RAW + RAW_STAGES * RAW_BYTES;
-    static constexpr int OFF_OPB = OFF_OPA + OPS * OP_A;
-    static constexpr int OFF_SCW = OFF_OPB + OPS * OP_B;
+    static constexpr int OFF_OPB = OFF_RAW + RAW_STAGES * RAW_BYTES;
+    static constexpr int OFF_SCW = OFF_OPB + OP_SLOTS * OP_B;
     static constexpr int OFF_SCX = OFF_SCW + SC_SLOTS * BM * 4;
     static constexpr int OFF_SCM = OFF_SCX + SC_SLOTS * BN * 4;            // m_w per row (min formats)
     static constexpr int OFF_SCS = OFF_SCM + (HAS_MIN ? SC_SLOTS * BM * 4 : 0);  // d_x * sum(a) per token
     static constexpr int OFF_BAR = OFF_SCS + (HAS_MIN ? SC_SLOTS * BN * 4 : 0);
-    // barriers: raw_full[2] raw_empty[2] op_full[PAIRS] op_empty[PAIRS] acc_full[2] acc_empty[2] sc_empty[SCP]
-    static constexpr int NBARS = 2 * RAW_STAGES + 2 * PAIRS + 2 * ACC_PAIRS + SCP;
+    // barriers: raw_full[2] raw_empty[2] op_full[4] mma_done[8] acc_empty[3]
+    static constexpr int NBARS = 2 * RAW_STAGES + OP_SLOTS + DONE_RING + S_BUFS;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM + 16;
 };
@@ -109,28 +120,21 @@ static_assert(Lay<QMM_Q4_0>::SMEM_BYTES <= 232448 && Lay<QMM_Q8_0>::SMEM_BYTES <
                   Lay<QMM_Q4_1>::SMEM_BYTES <= 232448 && Lay<QMM_Q5_0>::SMEM_BYTES <= 232448 &&
                   Lay<QMM_Q5_1>::SMEM_BYTES <= 232448,
               "prefill smem");
-static_assert(KB % 4 == 0, "pairs must not straddle the activation converter's 4-block windows");
 
 struct Bars {
     uint32_t base;
-    int pairs;  // operand pair slots
     __device__ uint32_t raw_full(int i) const { return base + 8u * i; }
     __device__ uint32_t raw_empty(int i) const { return base + 8u * (RAW_STAGES + i); }
-    // operand pair slot i: written by the converters / read by the tensor core (one tcgen05.commit)
+    // operand slot i written by the converters
     __device__ uint32_t op_full(int i) const { return base + 8u * (2 * RAW_STAGES + i); }
-    __device__ uint32_t op_empty(int i) const { return base + 8u * (2 * RAW_STAGES + pairs + i); }
-    // accumulator pair i: both blocks' sums complete (one tcgen05.commit) / read into registers
-    __device__ uint32_t acc_full(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * pairs + i); }
-    __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + 2 * pairs + ACC_PAIRS + i); }
-    // scale pair slot i read by the epilogue
-    __device__ uint32_t sc_empty(int i) const {
-        return base + 8u * (2 * RAW_STAGES + 2 * pairs + 2 * ACC_PAIRS + i);
-    }
+    // the MMAs of block b done (one tcgen05.commit): barrier b % DONE_RING, phase b / DONE_RING
+    __device__ uint32_t mma_done(int b) const { return base + 8u * (2 * RAW_STAGES + OP_SLOTS + (b & (DONE_RING - 1))); }
+    // accumulator i read into registers by every epilogue warp
+    __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + OP_SLOTS + DONE_RING + i); }
 };
 
 // wait with a time limit; on failure set the error word and the CTA's abort flag.
-// The fast path (phase already complete) is a single try_wait: the roles here
-// share their schedulers with FP32-heavy warps, so every instruction counts.
+// The fast path (phase already complete) is a single try_wait.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
@@ -138,6 +142,149 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     atomicOr(&g_matmul_error, kErrTimeout);
     *abort_flag = 1;
     return false;
+}
+
+// One block of 32 converted values of a row (fp16 pairs in K order: register c
+// holds elements 2c and 2c+1) into its operand slot: weights into this warp's
+// TMEM lanes, activations into the K-major core-matrix layout in shared memory.
+template <bool IS_W>
+__device__ __forceinline__ void put_operand(const uint32_t (&h)[16], uint32_t tmem_a, uint8_t* opb_row) {
+    if constexpr (IS_W) {
+        tc_fence_after();  // after the wait that freed the slot (its last MMA read it)
+        tmem_st16(tmem_a, h);
+        tmem_st_wait();
+        tc_fence_before();
+    } else {
+#pragma unroll
+        for (int kq = 0; kq < 4; kq++)
+            *reinterpret_cast<uint4*>(opb_row + kq * 128) = make_uint4(h[4 * kq], h[4 * kq + 1], h[4 * kq + 2], h[4 * kq + 3]);
+        fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
+    }
+}
+
+// The converter loop of one role.  IS_W: weight rows (WT's block layout) into
+// TMEM; otherwise Q8_0 tokens into shared memory.  Each thread owns one row or
+// token of the tile; per block it waits for the operand slot (freed by the MMAs
+// of block b - OP_SLOTS; that also frees the block's scale slot), converts, and
+// hands the block to the MMA issuer.
+template <int WT, bool IS_W>
+__device__ __forceinline__ void convert_loop(uint8_t* smem, uint32_t sbase, const Bars& bars, uint32_t tmem, int r,
+                                             int nchunks, volatile int* abort_flag) {
+    using L = Lay<WT>;
+    constexpr int SC_SLOTS = L::SC_SLOTS, RAW_BYTES = L::RAW_BYTES, W_RAW = L::W_RAW;
+    constexpr int RB = IS_W ? L::WB : 34;  // raw block bytes of this role
+    static_assert(KB % OP_SLOTS == 0 && SC_SLOTS == 2 * KB && DONE_RING == KB,
+                  "slot indices are fixed per block of a chunk");
+    const int lane = threadIdx.x & 31;
+    const uint32_t tmem_row = tmem + ((uint32_t)(r & ~31) << 16) + (uint32_t)A_COL0;  // this warp's lane quadrant
+    // this thread's row in the activation operand slots (K-major core matrices)
+    uint8_t* const opb_row = smem + L::OFF_OPB + ((r >> 3) * 4) * 128 + (r & 7) * 16;
+    float* const scale_row = reinterpret_cast<float*>(smem + (IS_W ? L::OFF_SCW : L::OFF_SCX)) + r;
+    float* const mw_row = reinterpret_cast<float*>(smem + L::OFF_SCM) + r;
+    float* const asum_row = reinterpret_cast<float*>(smem + L::OFF_SCS) + r;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; c++) {
+        const int s = c % RAW_STAGES;
+        if (!wait_or_abort(bars.raw_full(s), (c / RAW_STAGES) & 1, abort_flag)) break;
+        const uint8_t* row = smem + L::OFF_RAW + s * RAW_BYTES + (IS_W ? 0 : W_RAW) + r * (KB * RB);
+        // the row's 8 blocks, read as two windows of 4 blocks from the 16-byte boundary at or
+        // below each window's first byte (rows of 8 blocks are 16-byte multiples)
+#pragma unroll
+        for (int hw = 0; hw < 2 && ok; hw++) {
+            const int start = 4 * RB * hw, base16 = start & ~15, off0 = start - base16;
+            constexpr int NV = (4 * RB + 15 + 15) / 16;  // 16-byte loads covering a window at any offset
+            uint32_t raw[4 * NV + 1];
+            raw[4 * NV] = 0;
+            const int nv = (off0 + 4 * RB + 15) / 16;
+            const uint4* src = reinterpret_cast<const uint4*>(row + base16);
+#pragma unroll
+            for (int i = 0; i < NV; i++) {
+                const uint4 v = i < nv ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+                raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
+            }
+#pragma unroll
+            for (int lq = 0; lq < KB / 2; lq++) {
+                // block b = c * KB + kb of the chunk: operand slot kb % OP_SLOTS, scale slot
+                // (c & 1) * KB + kb; its slot was last used by block b - OP_SLOTS, whose
+                // mma_done barrier is (kb - OP_SLOTS) mod KB, in phase c (or c - 1)
+                const int kb = 4 * hw + lq, os = kb % OP_SLOTS, ssl = (c & 1) * KB + kb;
+                const int kprev = kb - OP_SLOTS;  // the previous user's block within its chunk
+                const bool freed =
+                    (c == 0 && kprev < 0) ||
+                    wait_or_abort(bars.mma_done((kprev + KB) % KB), (kprev < 0 ? c - 1 : c) & 1, abort_flag);
+                if (!__all_sync(0xffffffffu, freed)) {  // warp-uniform: the TMEM store below is warp-collective
+                    ok = false;
+                    break;
+                }
+                const int off = off0 + RB * lq;  // the block's first byte in the window
+                auto word_at = [&](int o) -> uint32_t {
+                    return (o % 4 == 0) ? raw[o / 4] : __funnelshift_r(raw[o / 4], raw[o / 4 + 1], 8 * (o % 4));
+                };
+                uint32_t h[16];
+                if constexpr (IS_W && WT != QMM_Q8_0) {
+                    // Q4_0: d, qs@2; Q4_1: d, m, qs@4; Q5_0: d, qh@2, qs@6; Q5_1: d, m, qh@4, qs@8;
+                    // element j is the low nibble of qs[j], element j+16 the high one, and bit e of
+                    // qh is element e's fifth bit
+                    constexpr int OFF_Q = WT == QMM_Q4_0 ? 2 : WT == QMM_Q4_1 ? 4 : WT == QMM_Q5_0 ? 6 : 8;
+                    constexpr int OFF_H = WT == QMM_Q5_0 ? 2 : 4;
+                    constexpr bool FIVE = WT == QMM_Q5_0 || WT == QMM_Q5_1;
+                    // fp16 bits of (1024 + code) minus 1032 (Q4_0: code - 8), 1040 (Q5_0: code - 16)
+                    // or 1024 (Q4_1, Q5_1: the code itself)
+                    constexpr uint32_t magic =
+                        WT == QMM_Q4_0 ? 0x64086408u : WT == QMM_Q5_0 ? 0x64106410u : 0x64006400u;
+                    const uint32_t dm = word_at(off);  // d in the low half, m (Q4_1, Q5_1) in the high half
+                    const uint32_t qh = FIVE ? word_at(off + OFF_H) : 0u;
+                    uint32_t lo[4], hi[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const uint32_t q = word_at(off + OFF_Q + 4 * i);
+                        lo[i] = q & 0x0F0F0F0Fu;
+                        hi[i] = (q >> 4) & 0x0F0F0F0Fu;
+                        if (FIVE) {
+                            lo[i] |= spread4(qh >> (4 * i)) << 4;
+                            hi[i] |= spread4(qh >> (16 + 4 * i)) << 4;
+                        }
+                    }
+#pragma unroll
+                    for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7
+                        const uint32_t w0 = kq < 2 ? lo[2 * kq] : hi[2 * (kq - 2)];
+                        const uint32_t w1 = kq < 2 ? lo[2 * kq + 1] : hi[2 * (kq - 2) + 1];
+                        h[4 * kq] = h2_sub(bytes_to_h2(w0, 0x5140), magic);
+                        h[4 * kq + 1] = h2_sub(bytes_to_h2(w0, 0x7362), magic);
+                        h[4 * kq + 2] = h2_sub(bytes_to_h2(w1, 0x5140), magic);
+                        h[4 * kq + 3] = h2_sub(bytes_to_h2(w1, 0x7362), magic);
+                    }
+                    scale_row[ssl * BM] = h2f(dm & 0xFFFFu);
+                    if (L::HAS_MIN) mw_row[ssl * BM] = h2f(dm >> 16);
+                } else {
+                    // a Q8_0 block (activation token or Q8_0 weight row): f16 d, 32 int8 codes
+                    const uint32_t dbits = word_at(off) & 0xFFFFu;
+                    const uint32_t m128 = 0x64806480u;  // (1152, 1152): 1024 + (a + 128) - 1152 = a
+                    int asum = 0;  // sum of the block's codes (min formats: the token's m_w term)
+#pragma unroll
+                    for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7: code words 2kq, 2kq+1
+                        const uint32_t c0 = word_at(off + 2 + 8 * kq), c1 = word_at(off + 6 + 8 * kq);
+                        if (!IS_W && L::HAS_MIN) asum = __dp4a((int)c1, 0x01010101, __dp4a((int)c0, 0x01010101, asum));
+                        const uint32_t w0 = c0 ^ 0x80808080u, w1 = c1 ^ 0x80808080u;
+                        h[4 * kq] = h2_sub(bytes_to_h2(w0, 0x5140), m128);
+                        h[4 * kq + 1] = h2_sub(bytes_to_h2(w0, 0x7362), m128);
+                        h[4 * kq + 2] = h2_sub(bytes_to_h2(w1, 0x5140), m128);
+                        h[4 * kq + 3] = h2_sub(bytes_to_h2(w1, 0x7362), m128);
+                    }
+                    scale_row[ssl * BN] = h2f(dbits);
+                    if (!IS_W && L::HAS_MIN) asum_row[ssl * BN] = h2f(dbits) * (float)asum;
+                }
+                put_operand<IS_W>(h, tmem_row + (uint32_t)(os * 16), opb_row + os * OP_B);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.op_full(os));
+            }
+        }
+        // The raw stage goes back to the producer only once every value read from it
+        // has been used: released right after the loads, the next chunk's TMA was seen
+        // to overwrite a window whose loads a converter had just issued.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.raw_empty(s));
+    }
 }
 
 template <int WT>
@@ -155,9 +302,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     using L = Lay<WT>;
     if (!QMM_IN_BOUNDS(g_matmul_error, L::SMEM_BYTES - 1, dynamic_smem_bytes())) return;  // the layout must fit
-    constexpr int SC_SLOTS = L::SC_SLOTS, SCP = L::SCP, W_RAW = L::W_RAW, RAW_BYTES = L::RAW_BYTES, WB = L::WB,
-                  PAIRS = L::PAIRS;
-    const Bars bars{sbase + L::OFF_BAR, PAIRS};
+    constexpr int SC_SLOTS = L::SC_SLOTS, W_RAW = L::W_RAW, RAW_BYTES = L::RAW_BYTES, WB = L::WB;
+    const Bars bars{sbase + L::OFF_BAR};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_TMEM + 8);
     const float* scw = reinterpret_cast<const float*>(smem + L::OFF_SCW);
@@ -175,19 +321,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bars.raw_full(i), 1);
             mbar_init(bars.raw_empty(i), NUM_CONV_WARPS);
         }
-        for (int i = 0; i < PAIRS; i++) {
-            mbar_init(bars.op_full(i), NUM_CONV_WARPS);
-            mbar_init(bars.op_empty(i), 1);
-        }
-        for (int i = 0; i < ACC_PAIRS; i++) {
-            mbar_init(bars.acc_full(i), 1);
-            mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
-        }
-        for (int i = 0; i < SCP; i++) mbar_init(bars.sc_empty(i), NUM_EPI_WARPS);
+        for (int i = 0; i < OP_SLOTS; i++) mbar_init(bars.op_full(i), NUM_CONV_WARPS);
+        for (int i = 0; i < DONE_RING; i++) mbar_init(bars.mma_done(i), 1);
+        for (int i = 0; i < S_BUFS; i++) mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {  // allocate the TMEM accumulators (whole warp)
+    if (warp == TMA_WARP) {  // allocate the TMEM accumulators and weight operand slots (whole warp)
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
                      : "memory");
@@ -197,9 +337,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int cw = converter_index(warp);
 
-    if (warp == 0) {
+    if (warp == TMA_WARP) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             if (pdl) pdl_wait();  // the activation comes from the previous kernel
@@ -213,279 +352,116 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_2d(dst + W_RAW, &xmap, c * (KB * 34 / 2), t0, bars.raw_full(s));
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = instr_desc_f16(BM, BN);
-            // descriptors of slot 0; slot os adds os * OP_A (>> 4) to the address field
-            const uint64_t a0 = smem_desc(sbase + L::OFF_OPA, 128, 512);
-            const uint64_t b0 = smem_desc(sbase + L::OFF_OPB, 128, 512);
-            for (int p = 0; p < nb / 2; p++) {  // blocks 2p and 2p+1 per handshake
-                const int ps = p % PAIRS, ap = p % ACC_PAIRS;
-                if (!wait_or_abort(bars.op_full(ps), (p / PAIRS) & 1, abort_flag)) break;
-                if (p >= ACC_PAIRS && !wait_or_abort(bars.acc_empty(ap), ((p / ACC_PAIRS) - 1) & 1, abort_flag))
-                    break;
+            const uint64_t b0 = smem_desc(sbase + L::OFF_OPB, 128, 512);  // slot os adds os * OP_B (>> 4)
+            // block b = round * S_BUFS + sb uses accumulator sb; from round 1 on it waits for the
+            // release of round - 1, i.e. phase parity (round - 1) & 1 = s_phase ^ 1
+            int sb = 0, s_phase = 0;
+            for (int b = 0; b < nb; b++) {
+                const int os = b & (OP_SLOTS - 1);
+                if (!wait_or_abort(bars.op_full(os), (b / OP_SLOTS) & 1, abort_flag)) break;
+                if (b >= S_BUFS && !wait_or_abort(bars.acc_empty(sb), s_phase ^ 1, abort_flag)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int i = 0; i < 2; i++) {
-                    const int os = 2 * ps + i;
-                    const uint64_t ad = a0 + (uint64_t)(os * (OP_A >> 4));
-                    const uint64_t bd = b0 + (uint64_t)(os * (OP_B >> 4));
-                    const uint32_t d = tmem + (uint32_t)((2 * ap + i) * BN);
-                    mma_f16(d, ad, bd, idesc, 0);                            // K 0..15: core matrices 0, 1
-                    mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1);  // K 16..31: core matrices 2, 3
-                }
-                mma_commit(bars.op_empty(ps));
-                mma_commit(bars.acc_full(ap));
-            }
-        }
-    } else if (cw >= 0) {
-        // ------------------------------------------------------------ converters
-        // Blocks go in pairs: the slots of pair p are taken (operands freed by the
-        // MMAs of pair p - PAIRS, scales by the epilogue of pair p - SCP) before
-        // its first block, and handed to the MMA issuer after its second.
-        const bool is_w = cw < NUM_CONV_WARPS / 2;
-        const int r = (cw % (NUM_CONV_WARPS / 2)) * 32 + lane;  // weight row or token, 0..127
-        for (int c = 0; c < nchunks; c++) {
-            const int s = c % RAW_STAGES;
-            if (!wait_or_abort(bars.raw_full(s), (c / RAW_STAGES) & 1, abort_flag)) break;
-            if (WT == QMM_Q4_0 && is_w) {
-                // this Q4_0 weight row's 8 blocks: 144 bytes, 16-byte aligned
-                uint32_t raw[36];
-                const uint4* src = reinterpret_cast<const uint4*>(smem + L::OFF_RAW + s * RAW_BYTES + r * (KB * 18));
-#pragma unroll
-                for (int i = 0; i < 9; i++) {
-                    const uint4 v = src[i];
-                    raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
-                }
-#pragma unroll
-                for (int lb = 0; lb < KB; lb++) {
-                    const int b = c * KB + lb, p = b >> 1, ps = p % PAIRS, os = 2 * ps + (b & 1), ss = b % SC_SLOTS;
-                    if ((b & 1) == 0) {
-                        if (p >= PAIRS && !wait_or_abort(bars.op_empty(ps), ((p / PAIRS) - 1) & 1, abort_flag)) break;
-                        if (p >= SCP && !wait_or_abort(bars.sc_empty(p % SCP), ((p / SCP) - 1) & 1, abort_flag))
-                            break;
-                    }
-                    // block lb: f16 d at byte 18*lb, nibbles at 18*lb + 2 (element j low, j+16 high)
-                    const int off = 18 * lb;
-                    const uint32_t dbits = __funnelshift_r(raw[off / 4], raw[off / 4 + 1], 8 * (off % 4)) & 0xFFFFu;
-                    uint32_t lo[4], hi[4];
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int qo = off + 2 + 4 * i;
-                        const uint32_t q = __funnelshift_r(raw[qo / 4], raw[qo / 4 + 1], 8 * (qo % 4));
-                        lo[i] = q & 0x0F0F0F0Fu;
-                        hi[i] = (q >> 4) & 0x0F0F0F0Fu;
-                    }
-                    const uint32_t m8 = 0x64086408u;  // (1032, 1032): 1024 + n - 1032 = n - 8
-                    uint8_t* A = smem + L::OFF_OPA + os * OP_A;
-#pragma unroll
-                    for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7
-                        const uint32_t w0 = kq < 2 ? lo[2 * kq] : hi[2 * (kq - 2)];
-                        const uint32_t w1 = kq < 2 ? lo[2 * kq + 1] : hi[2 * (kq - 2) + 1];
-                        uint4 v;
-                        v.x = h2_sub(bytes_to_h2(w0, 0x5140), m8);
-                        v.y = h2_sub(bytes_to_h2(w0, 0x7362), m8);
-                        v.z = h2_sub(bytes_to_h2(w1, 0x5140), m8);
-                        v.w = h2_sub(bytes_to_h2(w1, 0x7362), m8);
-                        *reinterpret_cast<uint4*>(A + op_off(r, kq)) = v;
-                    }
-                    reinterpret_cast<float*>(smem + L::OFF_SCW)[ss * BM + r] = h2f(dbits);
-                    if (b & 1) {
-                        fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bars.op_full(ps));
-                    }
-                }
-            } else if (is_w && (WT == QMM_Q4_1 || WT == QMM_Q5_0 || WT == QMM_Q5_1)) {
-                // this weight row's 8 blocks (160, 176 or 192 bytes, 16-byte aligned), read as two
-                // windows of 4 blocks starting at the 16-byte boundary at or below each window's
-                // first byte.  Q4_1: d, m, qs@4; Q5_0: d, qh@2, qs@6; Q5_1: d, m, qh@4, qs@8;
-                // element j is the low nibble of qs[j], element j+16 the high one, and bit e of
-                // qh is element e's fifth bit.
-                constexpr int OFF_Q = WT == QMM_Q4_1 ? 4 : WT == QMM_Q5_0 ? 6 : 8;
-                constexpr int OFF_H = WT == QMM_Q5_0 ? 2 : 4;
-                constexpr bool FIVE = WT != QMM_Q4_1;
-                // fp16 bits of (1024 + byte) minus 1024 (codes 0..31) or 1040 (Q5_0: code - 16)
-                constexpr uint32_t magic = WT == QMM_Q5_0 ? 0x64106410u : 0x64006400u;
-                const uint8_t* rowp = smem + L::OFF_RAW + s * RAW_BYTES + r * (KB * WB);
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int start = 4 * WB * h, base16 = start & ~15, off0 = start - base16;
-                    const int nv = (off0 + 4 * WB + 15) / 16;  // 16-byte loads: 5 or 6
-                    uint32_t raw[25];
-                    raw[24] = 0;
-                    const uint4* src = reinterpret_cast<const uint4*>(rowp + base16);
-#pragma unroll
-                    for (int i = 0; i < 6; i++) {
-                        if (i < nv) {
-                            const uint4 v = src[i];
-                            raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
-                        } else {
-                            raw[4 * i] = raw[4 * i + 1] = raw[4 * i + 2] = raw[4 * i + 3] = 0;
-                        }
-                    }
-#pragma unroll
-                    for (int lq = 0; lq < KB / 2; lq++) {
-                        const int lb = 4 * h + lq;
-                        const int b = c * KB + lb, p = b >> 1, ps = p % PAIRS, os = 2 * ps + (b & 1),
-                                  ss = b % SC_SLOTS;
-                        if ((b & 1) == 0) {
-                            if (p >= PAIRS &&
-                                !wait_or_abort(bars.op_empty(ps), ((p / PAIRS) - 1) & 1, abort_flag))
-                                break;
-                            if (p >= SCP && !wait_or_abort(bars.sc_empty(p % SCP), ((p / SCP) - 1) & 1, abort_flag))
-                                break;
-                        }
-                        const int off = off0 + WB * lq;  // the block's first byte in the window
-                        auto word_at = [&](int o) -> uint32_t {
-                            return (o % 4 == 0) ? raw[o / 4] : __funnelshift_r(raw[o / 4], raw[o / 4 + 1], 8 * (o % 4));
-                        };
-                        const uint32_t dm = word_at(off);  // d in the low half, m (Q4_1, Q5_1) in the high half
-                        const uint32_t qh = FIVE ? word_at(off + OFF_H) : 0u;
-                        uint32_t lo[4], hi[4];
-#pragma unroll
-                        for (int i = 0; i < 4; i++) {
-                            const uint32_t q = word_at(off + OFF_Q + 4 * i);
-                            lo[i] = q & 0x0F0F0F0Fu;
-                            hi[i] = (q >> 4) & 0x0F0F0F0Fu;
-                            if (FIVE) {
-                                lo[i] |= spread4(qh >> (4 * i)) << 4;
-                                hi[i] |= spread4(qh >> (16 + 4 * i)) << 4;
-                            }
-                        }
-                        uint8_t* A = smem + L::OFF_OPA + os * OP_A;
-#pragma unroll
-                        for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7
-                            const uint32_t w0 = kq < 2 ? lo[2 * kq] : hi[2 * (kq - 2)];
-                            const uint32_t w1 = kq < 2 ? lo[2 * kq + 1] : hi[2 * (kq - 2) + 1];
-                            uint4 v;
-                            v.x = h2_sub(bytes_to_h2(w0, 0x5140), magic);
-                            v.y = h2_sub(bytes_to_h2(w0, 0x7362), magic);
-                            v.z = h2_sub(bytes_to_h2(w1, 0x5140), magic);
-                            v.w = h2_sub(bytes_to_h2(w1, 0x7362), magic);
-                            *reinterpret_cast<uint4*>(A + op_off(r, kq)) = v;
-                        }
-                        reinterpret_cast<float*>(smem + L::OFF_SCW)[ss * BM + r] = h2f(dm & 0xFFFFu);
-                        if (L::HAS_MIN) reinterpret_cast<float*>(smem + L::OFF_SCM)[ss * BM + r] = h2f(dm >> 16);
-                        if (b & 1) {
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(bars.op_full(ps));
-                        }
-                    }
-                }
-            } else {
-                // this token's (or Q8_0 weight row's) 8 blocks: 272 bytes, 16-byte aligned,
-                // read as two windows of 144 bytes (bytes 0..143 hold blocks 0-3, bytes
-                // 128..271 hold blocks 4-7)
-                const uint8_t* row = smem + L::OFF_RAW + s * RAW_BYTES + (is_w ? 0 : W_RAW) + r * (KB * 34);
-                uint8_t* const opbase = smem + (is_w ? L::OFF_OPA : L::OFF_OPB);
-                float* const scbase = reinterpret_cast<float*>(smem + (is_w ? L::OFF_SCW : L::OFF_SCX));
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    uint32_t raw[36];
-                    const uint4* src = reinterpret_cast<const uint4*>(row + 128 * h);
-#pragma unroll
-                    for (int i = 0; i < 9; i++) {
-                        const uint4 v = src[i];
-                        raw[4 * i] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
-                    }
-#pragma unroll
-                    for (int lq = 0; lq < KB / 2; lq++) {
-                        const int lb = 4 * h + lq;
-                        const int b = c * KB + lb, p = b >> 1, ps = p % PAIRS, os = 2 * ps + (b & 1),
-                                  ss = b % SC_SLOTS;
-                        if ((b & 1) == 0) {
-                            if (p >= PAIRS &&
-                                !wait_or_abort(bars.op_empty(ps), ((p / PAIRS) - 1) & 1, abort_flag))
-                                break;
-                            if (p >= SCP && !wait_or_abort(bars.sc_empty(p % SCP), ((p / SCP) - 1) & 1, abort_flag))
-                                break;
-                        }
-                        // block lb: f16 d at byte 34*lb, 32 int8 codes at 34*lb + 2 (window-relative)
-                        const int off = 34 * lb - 128 * h;
-                        const uint32_t dbits =
-                            __funnelshift_r(raw[off / 4], raw[off / 4 + 1], 8 * (off % 4)) & 0xFFFFu;
-                        const uint32_t m128 = 0x64806480u;  // (1152, 1152): 1024 + (a + 128) - 1152 = a
-                        static_assert(OP_A == OP_B && BM == BN, "one converter for both operands");
-                        uint8_t* Bop = opbase + os * OP_B;
-                        int asum = 0;  // sum of the block's codes (min formats: the token's m_w term)
-#pragma unroll
-                        for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7: code words 2kq, 2kq+1
-                            const int q0 = off + 2 + 8 * kq, q1 = q0 + 4;
-                            const uint32_t c0 = __funnelshift_r(raw[q0 / 4], raw[q0 / 4 + 1], 8 * (q0 % 4));
-                            const uint32_t c1 = __funnelshift_r(raw[q1 / 4], raw[q1 / 4 + 1], 8 * (q1 % 4));
-                            if (L::HAS_MIN) asum = __dp4a((int)c1, 0x01010101, __dp4a((int)c0, 0x01010101, asum));
-                            const uint32_t w0 = c0 ^ 0x80808080u, w1 = c1 ^ 0x80808080u;
-                            uint4 v;
-                            v.x = h2_sub(bytes_to_h2(w0, 0x5140), m128);
-                            v.y = h2_sub(bytes_to_h2(w0, 0x7362), m128);
-                            v.z = h2_sub(bytes_to_h2(w1, 0x5140), m128);
-                            v.w = h2_sub(bytes_to_h2(w1, 0x7362), m128);
-                            *reinterpret_cast<uint4*>(Bop + op_off(r, kq)) = v;
-                        }
-                        scbase[ss * BN + r] = h2f(dbits);
-                        if (L::HAS_MIN && !is_w)
-                            reinterpret_cast<float*>(smem + L::OFF_SCS)[ss * BN + r] = h2f(dbits) * (float)asum;
-                        if (b & 1) {
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(bars.op_full(ps));
-                        }
-                    }
+                const uint32_t a = tmem + (uint32_t)(A_COL0 + os * 16);
+                const uint64_t bd = b0 + (uint64_t)(os * (OP_B >> 4));
+                const uint32_t d = tmem + (uint32_t)(sb * BN);
+                mma_f16_ts(d, a, bd, idesc, 0);                       // K 0..15: columns 0-7, core matrices 0, 1
+                mma_f16_ts(d, a + 8, bd + (256 >> 4), idesc, 1);      // K 16..31: columns 8-15, core matrices 2, 3
+                mma_commit(bars.mma_done(b));
+                if (++sb == S_BUFS) {  // the next round of accumulators: wait for the previous round's release
+                    sb = 0;
+                    s_phase ^= 1;
                 }
             }
-            // The raw stage goes back to the producer only once every value read from it
-            // has been used: released right after the loads, the next chunk's TMA was seen
-            // to overwrite a window whose loads the weight converter had just issued.
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.raw_empty(s));
         }
-    } else if (warp >= EPI0) {
-        // ------------------------------------------------------------ epilogue
-        const int e = warp - EPI0;        // 0..15
+    } else if (warp >= W0 && warp < X0) {
+        // ------------------------------------------------------------ weight converters
+        convert_loop<WT, true>(smem, sbase, bars, tmem, (warp & 3) * 32 + lane, nchunks, abort_flag);
+    } else if (warp >= X0 && warp < TMA_WARP) {
+        // ------------------------------------------------------------ activation converters
+        convert_loop<WT, false>(smem, sbase, bars, tmem, (warp - X0) * 32 + lane, nchunks, abort_flag);
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 0-15)
         const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-        const int cg = e >> 2;            // which 32 columns (tokens)
+        const int cg = warp >> 2;         // which 32 columns (tokens)
         const int row = quad * 32 + lane;  // weight row within the tile
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cg * 32);
-        uint64_t acc[16];  // running sums of tokens 2j, 2j+1 as packed f32 pairs
+        float acc[32];  // running sums of this thread's 32 tokens
 #pragma unroll
-        for (int j = 0; j < 16; j++) acc[j] = 0;
-        for (int p = 0; p < nb / 2; p++) {
-            const int ap = p % ACC_PAIRS;
-            if (!wait_or_abort(bars.acc_full(ap), (p / ACC_PAIRS) & 1, abort_flag)) break;
+        for (int j = 0; j < 32; j++) acc[j] = 0.0f;
+        // running state instead of per-block index arithmetic: the accumulator columns of
+        // block b (S_BUFS of them in turn), its scale slot (SC_SLOTS in turn) and the
+        // mma_done barrier of block b (DONE_RING in turn, phase b / DONE_RING)
+        uint32_t s_cols = lane_base;
+        int sbi = 0, sci = 0, dri = 0;
+        uint32_t d_parity = 0;
+        const float* scw_row = scw + row;
+        const float* scx_cg = scx + cg * 32;
+        const float* scm_row = scm + row;
+        const float* scs_cg = scs + cg * 32;
+        for (int b = 0; b < nb; b++) {  // blocks in order
+            // warp-uniform: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, wait_or_abort(bars.mma_done(dri), d_parity, abort_flag))) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int i = 0; i < 2; i++) {  // blocks 2p, 2p+1 in block order (not unrolled: registers)
-                const int ss = (2 * p + i) % SC_SLOTS, ac = 2 * ap + i;
-                const uint32_t dwb = __float_as_uint(scw[ss * BM + row]);
-                const uint64_t dw2 = f2_pack(dwb, dwb);
-                const uint64_t* dxs = reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
-                // min formats: y += m_w * (d_x * sum(a)) after the block's value term
-                const uint32_t mwb = L::HAS_MIN ? __float_as_uint(scm[ss * BM + row]) : 0u;
-                const uint64_t mw2 = f2_pack(mwb, mwb);
-                const uint64_t* css = reinterpret_cast<const uint64_t*>(scs + ss * BN + cg * 32);
+            const int so = sci * BN;  // scale slot offset (BM == BN)
+            const uint32_t dwb = __float_as_uint(scw_row[so]);
+            const uint64_t dw2 = f2_pack(dwb, dwb);
+            const uint4* dxs = reinterpret_cast<const uint4*>(scx_cg + so);
+            // min formats: y += m_w * (d_x * sum(a)) after the block's value term
+            const float mw = L::HAS_MIN ? scm_row[so] : 0.0f;
+            const uint4* css = reinterpret_cast<const uint4*>(scs_cg + so);
+            // the block's 32 sums in quarters of 8 columns: each quarter's TMEM load is
+            // issued before the previous quarter is folded, so the load of one overlaps
+            // the arithmetic of the other (a wait covers every load issued before it)
+            uint32_t v[2][8];
+            tmem_ld8(s_cols, v[0]);
+            tmem_ld_wait_regs8(v[0]);
 #pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    uint32_t v[16];
-                    tmem_ld16(lane_base + (uint32_t)(ac * BN + 16 * h), v);
-                    tmem_ld_wait();
-                    if (i == 1 && h == 1) {  // both blocks' sums are in registers: the accumulators may be reused
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bars.acc_empty(ap));
-                    }
+            for (int q = 0; q < 4; q++) {
+                if (q < 3) tmem_ld8(s_cols + (uint32_t)(8 * (q + 1)), v[(q + 1) & 1]);
+                const uint32_t* u = v[q & 1];
 #pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        const uint64_t sc = f2_mul(dw2, dxs[8 * h + j]);  // (d_w*d_x[t], d_w*d_x[t+1])
-                        acc[8 * h + j] = f2_fma(f2_pack(v[2 * j], v[2 * j + 1]), sc, acc[8 * h + j]);
-                        if (L::HAS_MIN) acc[8 * h + j] = f2_fma(mw2, css[8 * h + j], acc[8 * h + j]);
+                for (int i = 0; i < 2; i++) {  // tokens t = 8q + 4i .. 8q + 4i + 3
+                    // the scale products d_w*d_x[t] two at a time (the d_x pairs arrive as aligned
+                    // register pairs), then one scalar FMA per sum reading the product's halves:
+                    // no register-pair assembly of the loaded sums
+                    const uint4 dx4 = dxs[2 * q + i];
+                    const uint64_t sc0 = f2_mul(dw2, f2_pack(dx4.x, dx4.y));
+                    const uint64_t sc1 = f2_mul(dw2, f2_pack(dx4.z, dx4.w));
+                    const int t = 8 * q + 4 * i;
+                    acc[t] = fmaf(__uint_as_float(u[4 * i]), __uint_as_float((uint32_t)sc0), acc[t]);
+                    acc[t + 1] = fmaf(__uint_as_float(u[4 * i + 1]), __uint_as_float((uint32_t)(sc0 >> 32)), acc[t + 1]);
+                    acc[t + 2] = fmaf(__uint_as_float(u[4 * i + 2]), __uint_as_float((uint32_t)sc1), acc[t + 2]);
+                    acc[t + 3] = fmaf(__uint_as_float(u[4 * i + 3]), __uint_as_float((uint32_t)(sc1 >> 32)), acc[t + 3]);
+                    if (L::HAS_MIN) {
+                        const uint4 cs4 = css[2 * q + i];
+                        acc[t] = fmaf(mw, __uint_as_float(cs4.x), acc[t]);
+                        acc[t + 1] = fmaf(mw, __uint_as_float(cs4.y), acc[t + 1]);
+                        acc[t + 2] = fmaf(mw, __uint_as_float(cs4.z), acc[t + 2]);
+                        acc[t + 3] = fmaf(mw, __uint_as_float(cs4.w), acc[t + 3]);
                     }
                 }
+                if (q < 3) tmem_ld_wait_regs8(v[(q + 1) & 1]);
+                if (q == 2) {  // all four quarters are in registers: the accumulator may be reused
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.acc_empty(sbi));
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.sc_empty(p % SCP));
+            if (++sbi == S_BUFS) {
+                sbi = 0;
+                s_cols = lane_base;
+            } else {
+                s_cols += BN;
+            }
+            sci = (sci + 1) & (SC_SLOTS - 1);
+            if (++dri == DONE_RING) {
+                dri = 0;
+                d_parity ^= 1u;
+            }
         }
         if (pdl) pdl_wait();  // Y may be read or written by the previous kernel
         const int o = o0 + row;
@@ -493,16 +469,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; j++) {
                 const int t = t0 + cg * 32 + j;
-                const uint32_t bits = (j & 1) ? (uint32_t)(acc[j >> 1] >> 32) : (uint32_t)acc[j >> 1];
                 if (t < M && QMM_IN_BOUNDS(g_matmul_error, (size_t)t * N + o, (size_t)M * N))
-                    Y[(size_t)t * N + o] = __uint_as_float(bits);
+                    Y[(size_t)t * N + o] = acc[j];
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == TMA_WARP) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
     }
