@@ -688,6 +688,79 @@ def cpu_baseline(args):
             "cpu": cpu_model()}
 
 
+def oracle_table(args):
+    """The CPU oracle on every configuration of the benchmark workloads, on one thread and on all of
+    the host's threads (rows split evenly, bit-identical results): the median of 5 timed runs of a
+    quantize + multiply step, with the CPU model.  The prefill runs on a bounded sample of its
+    tokens (all rows, all of K), reported as GOP/s; everything else runs whole."""
+    import oracle
+
+    nthreads = os.cpu_count() or 1
+
+    def median_time(fn, reps=5):
+        fn()  # warm-up (page-in, caches)
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        return float(np.median(ts))
+
+    rows = {}
+    for name in ("q4_0_matvec_4864x896", "q8_0_matvec_12288x4096", "q2_K_matvec_12288x4096"):
+        cfg = workloads.WORKLOADS[name]
+        wt, N, K = cfg["wtype"], cfg["N"], cfg["K"]
+        W = oracle.quantize(wt, workloads.weights_f32(N, K, cfg["seed"]))
+        x = workloads.activations_f32(1, K, cfg["seed"])
+        act = act_of(wt)
+        res = {"weight_bytes": int(W.size)}
+        for nt in (1, nthreads):
+            t = median_time(lambda: oracle.matmul(wt, W, oracle.quantize(act, x), 1, N, K, nthreads=nt))
+            res["ms_%dt" % nt] = round(t * 1e3, 3)
+            res["GB/s_%dt" % nt] = round(W.size / t / 1e9, 2)
+        rows[name] = res
+    # the decoder-layer set: three quantized rows, seven matrices
+    cfg = workloads.WORKLOADS["q4_K_M_layer_4096"]
+    mats = []
+    for i, (label, wt, N, K) in enumerate(cfg["matrices"]):
+        mats.append((label, wt, N, K, oracle.quantize(wt, workloads.weights_f32(N, K, cfg["seed"], stream=i,
+                                                                                  row_jitter=True))))
+    xh = workloads.activations_f32(1, 4096, cfg["seed"])
+    xo = workloads.activations_f32(1, 4096, cfg["seed"] + 1)
+    xd = workloads.activations_f32(1, 12288, cfg["seed"] + 2)
+    layer_bytes = sum(m[4].size for m in mats)
+
+    def layer(nt):
+        qh, qo, qd = oracle.quantize("q8_K", xh), oracle.quantize("q8_K", xo), oracle.quantize("q8_K", xd)
+        for (label, wt, N, K, W) in mats:
+            xq = qd if label == "W_down" else (qo if label == "Wo" else qh)
+            oracle.matmul(wt, W, xq, 1, N, K, nthreads=nt)
+
+    res = {"weight_bytes": int(layer_bytes)}
+    for nt in (1, nthreads):
+        t = median_time(lambda: layer(nt))
+        res["ms_%dt" % nt] = round(t * 1e3, 3)
+        res["GB/s_%dt" % nt] = round(layer_bytes / t / 1e9, 2)
+    rows["q4_K_M_layer_4096"] = res
+    # the prefill: a bounded sample of tokens against all rows, as GOP/s (the work is linear in M)
+    cfg = workloads.WORKLOADS["q4_0_prefill_512x12288x4096"]
+    N, K = cfg["N"], cfg["K"]
+    W = oracle.quantize("q4_0", workloads.weights_f32(N, K, cfg["seed"]))
+    res = {}
+    for nt, Ms in ((1, 2), (nthreads, 16)):
+        x = workloads.activations_f32(Ms, K, cfg["seed"] + 512)
+        t = median_time(lambda: oracle.matmul("q4_0", W, oracle.quantize("q8_0", x), Ms, N, K, nthreads=nt))
+        gops = 2.0 * Ms * N * K / t / 1e9
+        res["GOP/s_%dt" % nt] = round(gops, 2)
+        res["sample_%dt" % nt] = "%d tokens x %d rows x K=%d" % (Ms, N, K)
+        for M in cfg["M_sweep"]:
+            res["est_ms_M=%d_%dt" % (M, nt)] = round(2.0 * M * N * K / (gops * 1e9) * 1e3, 1)
+    rows["q4_0_prefill_12288x4096"] = res
+    line = {"oracle_table": rows, "threads": nthreads, "cpu": cpu_model(), "median_of": 5,
+            "note": "oracle = quantize + multiply, scalar C (-O2 -ffp-contract=off), rows split over threads"}
+    print(json.dumps(line), flush=True)
+
+
 def cpu_model() -> str:
     """The host CPU's model name as the OS reports it (or the machine type)."""
     arm = {}
@@ -753,12 +826,18 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the CPU oracle on every configuration (1 and all threads, median of 5) and exit")
     ap.add_argument("--min-timed-s", type=float, default=0.05,
                     help="repeat the timed region of --steps steps until this much device time is timed")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     rank, local_rank, world = dist_env()
+    if args.oracle_table:
+        if rank == 0:
+            oracle_table(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
