@@ -66,11 +66,16 @@ struct MatvecPlan {
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-// activation region: [codes: K B][scales: 4*nd B][sums: 4*nsum B], 128-byte padded
+// activation region: [codes][scales: 4*nd B][sums], 128-byte padded; Q8_0:
+// K code bytes and nd int32 sums; Q8_K: 16 chunk rows of pitch q8k_pitch(nd)
+// and 8 bsum-pair rows of the same pitch
+__host__ __device__ inline uint32_t act_code_bytes(int act, int K) {
+    return act == QMM_Q8_0 ? (uint32_t)K : 256u * (uint32_t)q8k_pitch(K / 256);
+}
 __host__ __device__ inline uint32_t act_region_bytes(int act, int K) {
     const int nd = act == QMM_Q8_0 ? K / 32 : K / 256;
-    const int nsum = act == QMM_Q8_0 ? K / 32 : K / 16;
-    return align_up((uint32_t)K + 4u * nd + 4u * nsum, 128u);
+    const uint32_t sum_bytes = act == QMM_Q8_0 ? 4u * nd : 32u * (uint32_t)q8k_pitch(nd);
+    return align_up(act_code_bytes(act, K) + 4u * nd + sum_bytes, 128u);
 }
 
 template <int WT>
@@ -244,7 +249,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
     uint8_t* aq = smem + align_up(8u * nw * depth, 128u);
     const int nd = F::ACT == QMM_Q8_0 ? K / 32 : K / 256;
     const int nsu = K / 256;
-    const int qbytes = SU ? SuFmt<has_su<WT>() ? WT : QMM_Q8_0>::A * nsu : K;
+    const int ap = F::ACT == QMM_Q8_0 ? nd : q8k_pitch(nd);  // the view's pitch
+    const int qbytes = SU ? SuFmt<has_su<WT>() ? WT : QMM_Q8_0>::A * nsu : (int)act_code_bytes(F::ACT, K);
     float* ad = reinterpret_cast<float*>(aq + qbytes);
     int* as = reinterpret_cast<int*>(ad + nd);
     uint8_t* slots = smem + act_bytes + (size_t)warp * depth * slot_bytes;
@@ -335,11 +341,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                     }
                     // straight into the decoder's layout; CTA 0 also stores the row
                     uint8_t* ob = blockIdx.x == 0 ? xq_out : nullptr;
-                    quant_q8_K_lane_put(v0, v1, lane, b0, nd, aq, ad, as, ob ? ob + b0 * 292 : nullptr);
-                    if (b1 < nd) quant_q8_K_lane_put(v2, v3, lane, b1, nd, aq, ad, as, ob ? ob + b1 * 292 : nullptr);
+                    quant_q8_K_lane_put(v0, v1, lane, b0, ap, aq, ad, as, ob ? ob + b0 * 292 : nullptr);
+                    if (b1 < nd) quant_q8_K_lane_put(v2, v3, lane, b1, ap, aq, ad, as, ob ? ob + b1 * 292 : nullptr);
                 }
             } else {
-                unpack_q8_K_row_by(xq, nd, aq, ad, as, tid, nthr);
+                unpack_q8_K_row_by(xq, nd, ap, aq, ad, as, tid, nthr);
             }
         }
         __syncthreads();
@@ -352,7 +358,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
         }
     }
 
-    const ActView act{aq, ad, as, nd};
+    const ActView act{aq, ad, as, ap};
     float* part = reinterpret_cast<float*>(smem + part_off);  // pieces > 1: one partial per segment
     const int segs_per_pass = 32 / lpr;
     const int ssub = lane / lpr, li = lane % lpr;
@@ -446,7 +452,8 @@ __global__ void __launch_bounds__(kThreads) blocksums_kernel(const uint8_t* __re
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* aq = smem + 128;
     const int nd = F::ACT == QMM_Q8_0 ? K / 32 : K / 256;
-    float* ad = reinterpret_cast<float*>(aq + K);
+    const int ap = F::ACT == QMM_Q8_0 ? nd : q8k_pitch(nd);
+    float* ad = reinterpret_cast<float*>(aq + act_code_bytes(F::ACT, K));
     int* as = reinterpret_cast<int*>(ad + nd);
     uint8_t* wbuf = smem + act_bytes;
 
@@ -466,7 +473,7 @@ __global__ void __launch_bounds__(kThreads) blocksums_kernel(const uint8_t* __re
         if (QMM_IN_BOUNDS(g_matvec_error, i - a0, (uint64_t)rows_per_cta * rb + 16)) wbuf[i - a0] = W[i];
     __syncthreads();
 
-    const ActView act{aq, ad, as, nd};
+    const ActView act{aq, ad, as, ap};
     const SmemBytes wv{wbuf};
     const int per = F::ACT == QMM_Q8_0 ? units : 2 * units;
     for (int i = threadIdx.x; i < (r1 - r0) * units; i += blockDim.x) {

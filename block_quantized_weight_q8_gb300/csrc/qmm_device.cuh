@@ -201,13 +201,19 @@ struct SmemBytes {
 };
 
 // The activation row, unpacked once per CTA into shared memory, chunk-major:
-//   q         int8 codes as 16-byte chunks, chunk c of block u at (c*n + u)*16
-//             (n = blocks per row), so lanes working on consecutive blocks read
-//             consecutive 16-byte words -- no bank conflicts
-//   d[n]      f32 block scales (Q8_0: from f16; Q8_K: as stored)
+//   q         int8 codes as 16-byte chunks, chunk c of block u at (c*n + u)*16,
+//             so lanes working on consecutive blocks read consecutive 16-byte
+//             words -- no bank conflicts
+//   d[]       f32 block scales (Q8_0: from f16; Q8_K: as stored), d[u]
 //   s         Q8_0: int32 sum of each block's 32 codes, s[u] (for the Q4_0 -8);
 //             Q8_K: the bsums as packed int16 pairs (groups 2k, 2k+1 in one
 //             word, as the block stores them), pair k of block u at s[k*n + u].
+// n is the pitch: the blocks per row for Q8_0; for Q8_K the super-blocks per
+// row made odd (q8k_pitch), because the writers of a Q8_K row put the chunks of
+// one super-block into consecutive lanes, n*16 bytes apart, and with n a
+// multiple of 8 every lane of a store would hit the same four banks.
+__host__ __device__ constexpr int q8k_pitch(int ns) { return ns | 1; }
+
 struct ActView {
     const uint8_t* q;
     const float* d;
@@ -549,74 +555,41 @@ __device__ __forceinline__ void unpack_q8_0_block(const uint8_t* __restrict__ ro
     s[b] = sum;
 }
 
-// item i of ns * 73: word k = i % 73 of super-block u = i / 73 (d, 64 code
-// words, 8 bsum words)
-// word wv = word k (0..72) of Q8_K block u into the view: the f32 scale, a
-// quarter chunk of codes, or a bsum pair
-__device__ __forceinline__ void put_q8_K_word(uint32_t wv, int u, int k, int ns, uint8_t* q, float* d, int* s) {
-    if (k == 0) {
-        d[u] = __uint_as_float(wv);
-    } else if (k <= 64) {
-        const int c = (k - 1) >> 2, wi = (k - 1) & 3;
-        *reinterpret_cast<uint32_t*>(q + ((uint32_t)c * ns + u) * 16 + 4 * wi) = wv;
-    } else {
-        reinterpret_cast<uint32_t*>(s)[(k - 65) * ns + u] = wv;  // the bsum pair of groups 2(k-65), +1
-    }
-}
-
-__device__ __forceinline__ void unpack_q8_K_word(const uint8_t* __restrict__ row, int ns, int i, uint8_t* q, float* d,
-                                                 int* s) {
-    const int u = i / 73, k = i % 73;
-    put_q8_K_word(*reinterpret_cast<const uint32_t*>(row + 292 * u + 4 * k), u, k, ns, q, d, s);
-}
-
-// The whole Q8_K row by the threads tid, tid + nthr, ...: each thread issues up
-// to four of its loads before it stores any, so the row costs one memory round
-// trip rather than one per word a thread handles (eight at a time raised the
-// register pressure of the kernels that call it and was slower).  A 16-byte
-// aligned row of a multiple of four super-blocks is read in 16-byte chunks.
-__device__ __forceinline__ void unpack_q8_K_row_by(const uint8_t* __restrict__ row, int ns, uint8_t* q, float* d,
-                                                   int* s, int tid, int nthr) {
-    const int total = ns * 73;
-    if (ns % 4 == 0 && ((uintptr_t)row & 15u) == 0) {
-        // four super-blocks are 73 whole 16-byte chunks: each thread loads two
-        // chunks (eight words) before it stores any, so a long row (K = 12288:
-        // 876 chunks) is still one memory round trip
-        const int nchunk = total / 4;
-        const uint4* rv = reinterpret_cast<const uint4*>(row);
-        for (int j0 = tid; j0 < nchunk; j0 += 2 * nthr) {
-            uint4 cv[2];
+// The whole Q8_K row by the threads tid, tid + nthr, ...: item t is chunk
+// c = t % 16 of super-block u = t / 16 (its 16 code bytes as four words); the
+// items c < 8 also carry bsum pair c, item 8 the scale.  A thread takes two
+// items and issues all their loads before it stores any, so even a long row
+// (K = 12288: 768 items) is one memory round trip.  The 16 items of a
+// super-block sit in consecutive lanes and their chunks pitch * 16 bytes apart,
+// pitch odd, so a quarter warp's 16-byte stores fall in distinct banks.  Rows
+// need 4-byte alignment only (Q8_K rows are 292 bytes).
+__device__ __forceinline__ void unpack_q8_K_row_by(const uint8_t* __restrict__ row, int ns, int n, uint8_t* q,
+                                                   float* d, int* s, int tid, int nthr) {
+    const int total = ns * 16;
+    const uint32_t* rw = reinterpret_cast<const uint32_t*>(row);
+    for (int t0 = tid; t0 < total; t0 += 2 * nthr) {
+        uint32_t v[2][5];
 #pragma unroll
-            for (int k = 0; k < 2; k++) {
-                const int j = j0 + k * nthr;
-                cv[k] = j < nchunk ? rv[j] : make_uint4(0u, 0u, 0u, 0u);
-            }
+        for (int k = 0; k < 2; k++) {
+            const int t = t0 + k * nthr;
+            const int u = t >> 4, c = t & 15;
+            if (t < total) {
+                const uint32_t* b = rw + 73 * u;
 #pragma unroll
-            for (int k = 0; k < 2; k++) {
-                const int j = j0 + k * nthr;
-                if (j < nchunk) {
-                    const uint32_t w[4] = {cv[k].x, cv[k].y, cv[k].z, cv[k].w};
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int i = 4 * j + e;
-                        put_q8_K_word(w[e], i / 73, i % 73, ns, q, d, s);
-                    }
-                }
+                for (int e = 0; e < 4; e++) v[k][e] = b[1 + 4 * c + e];
+                v[k][4] = c < 8 ? b[65 + c] : (c == 8 ? b[0] : 0u);
             }
         }
-        return;
-    }
-    for (int i0 = tid; i0 < total; i0 += 4 * nthr) {
-        uint32_t wv[4];
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int i = i0 + k * nthr;
-            wv[k] = i < total ? *reinterpret_cast<const uint32_t*>(row + 292 * (i / 73) + 4 * (i % 73)) : 0u;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int i = i0 + k * nthr;
-            if (i < total) put_q8_K_word(wv[k], i / 73, i % 73, ns, q, d, s);
+        for (int k = 0; k < 2; k++) {
+            const int t = t0 + k * nthr;
+            const int u = t >> 4, c = t & 15;
+            if (t < total) {
+                *reinterpret_cast<uint4*>(q + ((uint32_t)c * n + u) * 16) =
+                    make_uint4(v[k][0], v[k][1], v[k][2], v[k][3]);
+                if (c < 8) reinterpret_cast<uint32_t*>(s)[c * n + u] = v[k][4];  // pair of groups 2c, 2c + 1
+                else if (c == 8) d[u] = __uint_as_float(v[k][4]);
+            }
         }
     }
 }
@@ -629,7 +602,7 @@ __device__ __forceinline__ void unpack_q8_0_row(const uint8_t* __restrict__ row,
 __device__ __forceinline__ void unpack_q8_K_row(const uint8_t* __restrict__ row, int K, uint8_t* q, float* d,
                                                 int* s) {
     const int ns = K / 256;
-    unpack_q8_K_row_by(row, ns, q, d, s, threadIdx.x, blockDim.x);
+    unpack_q8_K_row_by(row, ns, q8k_pitch(ns), q, d, s, threadIdx.x, blockDim.x);
 }
 
 // ---------------------------------------------------------------- activation quantizers
@@ -718,17 +691,17 @@ __device__ __forceinline__ void quant_q8_K_lane(float4 v0, float4 v1, int lane, 
     store_q8_K_block(lane, d, w0, w1, pair, ob);
 }
 
-// The same block straight into the decoder's view (block u of ns): the codes of
-// lane l (8l .. 8l + 7) are half of chunk l / 2; also the 292-byte block at ob
-// when ob is not null.
-__device__ __forceinline__ void quant_q8_K_lane_put(float4 v0, float4 v1, int lane, int u, int ns, uint8_t* q,
+// The same block straight into the decoder's view (block u, pitch n): the codes
+// of lane l (8l .. 8l + 7) are half of chunk l / 2; also the 292-byte block at
+// ob when ob is not null.
+__device__ __forceinline__ void quant_q8_K_lane_put(float4 v0, float4 v1, int lane, int u, int n, uint8_t* q,
                                                     float* dv, int* s, uint8_t* ob) {
     float d;
     uint32_t w0, w1, pair;
     quant_q8_K_core(v0, v1, &d, &w0, &w1, &pair);
     if (lane == 0) dv[u] = d;
-    *reinterpret_cast<uint2*>(q + ((uint32_t)(lane >> 1) * ns + u) * 16 + (lane & 1) * 8) = make_uint2(w0, w1);
-    if ((lane & 3) == 0) reinterpret_cast<uint32_t*>(s)[(lane >> 2) * ns + u] = pair;
+    *reinterpret_cast<uint2*>(q + ((uint32_t)(lane >> 1) * n + u) * 16 + (lane & 1) * 8) = make_uint2(w0, w1);
+    if ((lane & 3) == 0) reinterpret_cast<uint32_t*>(s)[(lane >> 2) * n + u] = pair;
     if (ob != nullptr) store_q8_K_block(lane, d, w0, w1, pair, ob);
 }
 
@@ -832,6 +805,20 @@ __device__ __forceinline__ float sq8(const float4* x4, int i) {
     return __fadd_rn(s, __fmul_rn(b.w, b.w));
 }
 
+// the pairwise sum of the run of M partials starting at partial `first`, in
+// registers: every load is issued before the first add
+template <int M>
+__device__ __forceinline__ float rms_run_sum(const float4* x4, int first, int n8) {
+    float p[M];
+#pragma unroll
+    for (int i = 0; i < M; i++) p[i] = first + i < n8 ? sq8(x4, first + i) : 0.0f;
+#pragma unroll
+    for (int step = 1; step < M; step <<= 1)
+#pragma unroll
+        for (int i = 0; i < M; i += 2 * step) p[i] = __fadd_rn(p[i], p[i + step]);
+    return p[0];
+}
+
 __device__ __forceinline__ float rms_scale(const float* x, int K, float* p, float eps) {
     const int n8 = K / 8, nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m = rms_run(K, nthr);
@@ -839,7 +826,15 @@ __device__ __forceinline__ float rms_scale(const float* x, int K, float* p, floa
     float v;
     if (m == 1) {
         v = tid < n8 ? sq8(x4, tid) : 0.0f;
+    } else if (m == 2) {
+        v = rms_run_sum<2>(x4, tid * 2, n8);
+    } else if (m == 4) {
+        v = rms_run_sum<4>(x4, tid * 4, n8);
+    } else if (m == 8) {
+        v = rms_run_sum<8>(x4, tid * 8, n8);
     } else {
+        // longer runs through shared memory (here each load waits for the
+        // previous partial's store)
         float* pt = p + tid * m;
         for (int i = 0; i < m; i++) pt[i] = tid * m + i < n8 ? sq8(x4, tid * m + i) : 0.0f;
         for (int step = 1; step < m; step <<= 1)
