@@ -504,17 +504,17 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// A 2-D map over `rows` rows of `row_bytes` bytes, viewed as 16-bit elements,
-// with boxes of `box_bytes` x 128 rows; rows beyond the end read as zeros.
-static bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes) {
+bool make_row_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                  int elem_bytes) {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {row_bytes / 2, rows};
+    if (!fn || (elem_bytes != 2 && elem_bytes != 8) || row_bytes % elem_bytes || box_bytes % 16) return false;
+    const cuuint64_t dims[2] = {row_bytes / elem_bytes, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_bytes / 2, 128};
+    const cuuint32_t box[2] = {box_bytes / (uint32_t)elem_bytes, 128};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUtensorMapDataType t = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+    return fn(map, t, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -536,8 +536,8 @@ static qmm_status matmul_q_launch(const void* W, const void* xq, float* Y, int64
     }
     if ((N + mm::BM - 1) / mm::BM > 0x7FFFFFFF || (M + mm::BN - 1) / mm::BN > 65535) return QMM_E_SHAPE;
     CUtensorMap wmap, xmap;
-    if (!make_map(&wmap, W, row_bytes_of(WT, K), (uint64_t)N, mm::KB * L::WB) ||
-        !make_map(&xmap, xq, row_bytes_of(QMM_Q8_0, K), (uint64_t)M, mm::KB * 34))
+    if (!make_row_map(&wmap, W, row_bytes_of(WT, K), (uint64_t)N, mm::KB * L::WB, 2) ||
+        !make_row_map(&xmap, xq, row_bytes_of(QMM_Q8_0, K), (uint64_t)M, mm::KB * 34, 2))
         return QMM_E_CUDA;
     static PerDeviceOnce attr_once;
     int dev = 0;

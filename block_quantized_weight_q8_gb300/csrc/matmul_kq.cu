@@ -25,14 +25,18 @@
 //             into the super-block's accumulator, and per super-block the min
 //             MMA into a second accumulator (2 super-blocks in flight, 512 columns)
 //   warps 1-4 weight converters, warps 5-8 activation converters: each thread
-//             owns one weight row / token, copies its super-block bytes into
-//             shared memory with 16-byte cp.async (chunk-major per thread, one
-//             super-block ahead), decodes them and writes fp16 operands in the
-//             UMMA K-major core-matrix layout, plus the min operands and scales
+//             owns one weight row / token.  A role's super-block bytes arrive by
+//             TMA, one 2-D box per super-block (128 rows x the super-block's
+//             16-byte aligned superset, as 8-byte elements) in a ring of two
+//             stages; after reading a stage the role's four warps meet at a
+//             named barrier and one thread loads the box two super-blocks ahead
+//             into it.  Each thread decodes its row and writes fp16 operands in
+//             the UMMA K-major core-matrix layout, plus the min operands and scales
 //   warps 9-24 epilogue: per super-block tcgen05.ld of both sums, the fp32 fold,
 //             and at the end the token-major store
 // Shapes: K a multiple of 2048 (so that every row of W and of the activation is
-// a whole number of 16-byte chunks) and M >= 8; others run one matvec per token.
+// a whole number of 16-byte chunks, as a TMA row pitch must be) and M >= 8;
+// others run one matvec per token.
 // All waits are bounded; a timeout records QMM_E_TIMEOUT, every warp still
 // reaches the end, and TMEM is freed.
 #include "qmm_device.cuh"
@@ -50,7 +54,6 @@ namespace kq {
 
 constexpr int BM = 128, BN = 128;
 constexpr int RAWX = 304;                 // a Q8_K super-block (292 B) as whole 16-byte chunks
-constexpr int NCX = RAWX / 16;            // 19
 constexpr int SC_SLOTS = 4;               // super-blocks of scales in flight
 constexpr int OP_BYTES = BM * 32 * 2;     // 8192: one 32-value block of one fp16 operand
 constexpr int MIN_BYTES = BM * 16 * 2;    // 4096: one 16-value min operand
@@ -82,8 +85,8 @@ struct Layout {
     static constexpr int OFF_SCC = OFF_SCD + SC_SLOTS * BM * 4;                // c_w per row
     static constexpr int OFF_SCX = OFF_SCC + SC_SLOTS * BM * 4;                // d_x per token
     static constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;
-    // op_full[S] mma_done[S] acc_full[2] acc_empty[2] sc_empty[SC_SLOTS]
-    static constexpr int NBARS = 2 * F::OP_SLOTS + 4 + SC_SLOTS;
+    // op_full[S] mma_done[S] acc_full[2] acc_empty[2] sc_empty[SC_SLOTS] raw_full[2 roles][2 stages]
+    static constexpr int NBARS = 2 * F::OP_SLOTS + 4 + SC_SLOTS + 4;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
 };
@@ -100,6 +103,8 @@ struct Bars {
     __device__ uint32_t acc_full(int i) const { return base + 8u * (2 * S + i); }
     __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * S + 2 + i); }
     __device__ uint32_t sc_empty(int i) const { return base + 8u * (2 * S + 4 + i); }
+    // the TMA box of role `role` (0 weights, 1 activation) landed in stage s
+    __device__ uint32_t raw_full(int role, int s) const { return base + 8u * (2 * S + 4 + SC_SLOTS + 2 * role + s); }
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -111,13 +116,18 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return false;
 }
 
-// 16-byte global -> shared copy (both addresses 16-byte aligned), completing per thread
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// A barrier among the NTHREADS threads (whole warps) that use barrier ID
+// (1..15; 0 is __syncthreads): true on every one of them if `cond` held on any.
+template <int ID, int NTHREADS>
+__device__ __forceinline__ bool named_bar_any(bool cond) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)cond), "n"(ID), "n"(NTHREADS)
+        : "memory");
+    return r != 0;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Byte offset of element k (0..15) of row r in a 16-value K-major operand:
 // core matrix (r/8, k/8) at ((r/8)*2 + k/8)*128.
@@ -133,12 +143,14 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// A thread's raw super-block in shared memory, chunk-major across the 128
-// threads of its role: chunk c at (c*128 + r)*16.  OFF is the (uniform) byte
-// offset of the super-block's first byte within chunk 0.
+// A thread's raw super-block in shared memory: its row of the role's TMA box,
+// the 16-byte chunks of the super-block's aligned superset in order.  OFF is
+// the (uniform) byte offset of the super-block's first byte within chunk 0.
+// The row pitches (Q4_K 144, Q5_K 176, Q8_K 304 bytes) put the 16-byte loads of
+// eight consecutive rows in distinct banks; Q2_K (96) and Q6_K (224) pair them.
 struct Raw {
     const uint8_t* p;  // this thread's chunk 0
-    __device__ __forceinline__ uint4 chunk(int c) const { return *reinterpret_cast<const uint4*>(p + c * 2048); }
+    __device__ __forceinline__ uint4 chunk(int c) const { return *reinterpret_cast<const uint4*>(p + c * 16); }
 };
 __device__ __forceinline__ uint32_t comp(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 
@@ -368,8 +380,8 @@ __device__ __forceinline__ void hdr_x(const Raw& raw, uint32_t* d_bits, uint32_t
 // ------------------------------------------------------------------ the kernel
 template <int WT>
 __global__ void __launch_bounds__(THREADS, 1)
-    matmul_kq_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq, float* __restrict__ Y, int M,
-                     int N, int K, int pdl) {
+    matmul_kq_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                     float* __restrict__ Y, int M, int N, int K, int pdl) {
     using F = Fmt<WT>;
     using L = Layout<WT>;
     constexpr int S = F::OP_SLOTS;
@@ -390,7 +402,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int o0 = blockIdx.x * BM, t0 = blockIdx.y * BN;
     const int nsb = K / 256;
-    const uint64_t rb = (uint64_t)nsb * F::BB, xrb = (uint64_t)nsb * 292;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; i++) {
@@ -402,6 +413,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
         }
         for (int i = 0; i < SC_SLOTS; i++) mbar_init(bars.sc_empty(i), NUM_EPI_WARPS);
+        for (int i = 0; i < 4; i++) mbar_init(bars.raw_full(i >> 1, i & 1), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -454,172 +466,179 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < EPI0) {
         // ------------------------------------------------------------ converters
         const bool is_w = warp < CONV0 + NUM_CONV_WARPS / 2;
+        const int role = is_w ? 0 : 1;
         const int r = (warp - (is_w ? CONV0 : CONV0 + NUM_CONV_WARPS / 2)) * 32 + lane;  // row or token
-        const uint8_t* src;
-        if (is_w) {
-            src = W + (uint64_t)min(o0 + r, N - 1) * rb;
-        } else {
-            if (pdl) pdl_wait();  // the activation comes from the previous kernel
-            src = xq + (uint64_t)min(t0 + r, M - 1) * xrb;
-        }
-        const int BBs = is_w ? F::BB : 292, NC = is_w ? L::NCW : NCX;
+        if (!is_w && pdl) pdl_wait();  // the activation comes from the previous kernel
+        const int BBs = is_w ? F::BB : 292;
+        const int pitch = is_w ? F::RAWW : RAWX;  // the box's row pitch in shared memory
         const uint32_t raw_role = is_w ? 0u : (uint32_t)(BM * F::RAWW);
-        auto prefetch = [&](int sb) {
-            if (sb < nsb) {
-                const uint64_t a = ((uint64_t)sb * BBs) & ~15ull;
-                const uint32_t dst = sbase + L::OFF_RAW + (uint32_t)((sb & 1) * L::RAW_STAGE) + raw_role + (uint32_t)r * 16u;
-                // the chunks stay inside the row (its bytes rounded up to 16: rows are 16-byte multiples)
-                if (QMM_IN_BOUNDS(g_matmul_kq_error, a + 16 * NC - 1, is_w ? (int64_t)rb : (int64_t)xrb))
-                    for (int c = 0; c < NC; c++) cp_async16(dst + (uint32_t)c * 2048u, src + a + 16 * c);
-            }
-            cp_async_commit();  // possibly empty: one group per super-block keeps the count uniform
+        // super-block sb of the role's 128 rows into stage sb & 1 (one thread of the role):
+        // the box starts at the 16-byte boundary at or below the super-block's first byte
+        auto load = [&](int sb) {
+            const uint32_t bar = bars.raw_full(role, sb & 1);
+            const uint32_t dst = sbase + L::OFF_RAW + (uint32_t)((sb & 1) * L::RAW_STAGE) + raw_role;
+            const int x = (int)((((uint64_t)sb * BBs) & ~15ull) / 8);  // in 8-byte elements: a 16-byte multiple
+            fence_proxy_async_smem();  // the stage's previous bytes were read through the generic proxy
+            mbar_arrive_expect_tx(bar, (uint32_t)(128 * pitch));
+            if (is_w) tma_load_2d(dst, &wmap, x, o0, bar);
+            else tma_load_2d(dst, &xmap, x, t0, bar);
         };
-        prefetch(0);
-        prefetch(1);
+        if (r == 0) {
+            load(0);
+            if (nsb > 1) load(1);
+        }
         for (int sb = 0; sb < nsb; sb++) {
-            cp_async_wait<1>();  // this super-block's group is complete (the next may still fly)
-            const Raw raw{smem + L::OFF_RAW + (sb & 1) * L::RAW_STAGE + raw_role + r * 16};
+            bool ok = wait_or_abort(bars.raw_full(role, sb & 1), (sb >> 1) & 1, abort_flag);
+            const Raw raw{smem + L::OFF_RAW + (sb & 1) * L::RAW_STAGE + raw_role + r * pitch};
             const int off = (int)(((uint64_t)sb * BBs) & 15u);
             const int ss = sb % SC_SLOTS, as = sb & 1;
-            if (sb >= SC_SLOTS && !wait_or_abort(bars.sc_empty(ss), ((sb / SC_SLOTS) - 1) & 1, abort_flag)) break;
-            Hdr h;
-            uint32_t xd = 0, bs[8];
-            if (is_w) {
-                if constexpr (WT == QMM_Q4_K || WT == QMM_Q5_K) {
-                    hdr_q4_K<0>(raw, h);
-                } else if constexpr (WT == QMM_Q2_K) {
-                    switch (off) {
-                    case 0: hdr_q2_K<0>(raw, h); break;
-                    case 4: hdr_q2_K<4>(raw, h); break;
-                    case 8: hdr_q2_K<8>(raw, h); break;
-                    default: hdr_q2_K<12>(raw, h); break;
+            if (ok && sb >= SC_SLOTS && !wait_or_abort(bars.sc_empty(ss), ((sb / SC_SLOTS) - 1) & 1, abort_flag))
+                ok = false;
+            if (ok) {
+                Hdr h;
+                uint32_t xd = 0, bs[8];
+                if (is_w) {
+                    if constexpr (WT == QMM_Q4_K || WT == QMM_Q5_K) {
+                        hdr_q4_K<0>(raw, h);
+                    } else if constexpr (WT == QMM_Q2_K) {
+                        switch (off) {
+                        case 0: hdr_q2_K<0>(raw, h); break;
+                        case 4: hdr_q2_K<4>(raw, h); break;
+                        case 8: hdr_q2_K<8>(raw, h); break;
+                        default: hdr_q2_K<12>(raw, h); break;
+                        }
+                    } else {
+                        switch (off) {
+                        case 0: hdr_q6_K<0>(raw, h); break;
+                        case 2: hdr_q6_K<2>(raw, h); break;
+                        case 4: hdr_q6_K<4>(raw, h); break;
+                        case 6: hdr_q6_K<6>(raw, h); break;
+                        case 8: hdr_q6_K<8>(raw, h); break;
+                        case 10: hdr_q6_K<10>(raw, h); break;
+                        case 12: hdr_q6_K<12>(raw, h); break;
+                        default: hdr_q6_K<14>(raw, h); break;
+                        }
                     }
+                    scd[ss * BM + r] = h2f(h.d_bits);
+                    scc[ss * BM + r] = h2f(h.c_bits);
                 } else {
                     switch (off) {
-                    case 0: hdr_q6_K<0>(raw, h); break;
-                    case 2: hdr_q6_K<2>(raw, h); break;
-                    case 4: hdr_q6_K<4>(raw, h); break;
-                    case 6: hdr_q6_K<6>(raw, h); break;
-                    case 8: hdr_q6_K<8>(raw, h); break;
-                    case 10: hdr_q6_K<10>(raw, h); break;
-                    case 12: hdr_q6_K<12>(raw, h); break;
-                    default: hdr_q6_K<14>(raw, h); break;
+                    case 0: hdr_x<0>(raw, &xd, bs); break;
+                    case 4: hdr_x<4>(raw, &xd, bs); break;
+                    case 8: hdr_x<8>(raw, &xd, bs); break;
+                    default: hdr_x<12>(raw, &xd, bs); break;
                     }
+                    scx[ss * BN + r] = __uint_as_float(xd);
                 }
-                scd[ss * BM + r] = h2f(h.d_bits);
-                scc[ss * BM + r] = h2f(h.c_bits);
-            } else {
-                switch (off) {
-                case 0: hdr_x<0>(raw, &xd, bs); break;
-                case 4: hdr_x<4>(raw, &xd, bs); break;
-                case 8: hdr_x<8>(raw, &xd, bs); break;
-                default: hdr_x<12>(raw, &xd, bs); break;
-                }
-                scx[ss * BN + r] = __uint_as_float(xd);
-            }
-            bool ok = true;
-            // blocks in groups of G: all of a group's loads are issued before its
-            // stores, so the group's decode chains overlap
-            constexpr int G = F::GROUP;
-            for (int jg = 0; jg < 8; jg += G) {
-                int osl[G];
+                // blocks in groups of G: all of a group's loads are issued before its
+                // stores, so the group's decode chains overlap
+                constexpr int G = F::GROUP;
+                for (int jg = 0; jg < 8; jg += G) {
+                    int osl[G];
 #pragma unroll
-                for (int u = 0; u < G; u++) {
-                    const int b = sb * 8 + jg + u;
-                    osl[u] = b % S;
-                    if (b >= S && !wait_or_abort(bars.op_empty(osl[u]), ((b / S) - 1) & 1, abort_flag)) ok = false;
-                }
-                if (!ok) break;
-                if (is_w) {
-                    if constexpr (WT == QMM_Q6_K) {
-                        uint32_t ql[G][8], qh[G][8];
+                    for (int u = 0; u < G; u++) {
+                        const int b = sb * 8 + jg + u;
+                        osl[u] = b % S;
+                        if (b >= S && !wait_or_abort(bars.op_empty(osl[u]), ((b / S) - 1) & 1, abort_flag)) ok = false;
+                    }
+                    if (!ok) break;
+                    if (is_w) {
+                        if constexpr (WT == QMM_Q6_K) {
+                            uint32_t ql[G][8], qh[G][8];
 #pragma unroll
-                        for (int u = 0; u < G; u++) {
-                            switch (off) {
-                            case 0: ld_q6_K<0>(raw, jg + u, ql[u], qh[u]); break;
-                            case 2: ld_q6_K<2>(raw, jg + u, ql[u], qh[u]); break;
-                            case 4: ld_q6_K<4>(raw, jg + u, ql[u], qh[u]); break;
-                            case 6: ld_q6_K<6>(raw, jg + u, ql[u], qh[u]); break;
-                            case 8: ld_q6_K<8>(raw, jg + u, ql[u], qh[u]); break;
-                            case 10: ld_q6_K<10>(raw, jg + u, ql[u], qh[u]); break;
-                            case 12: ld_q6_K<12>(raw, jg + u, ql[u], qh[u]); break;
-                            default: ld_q6_K<14>(raw, jg + u, ql[u], qh[u]); break;
+                            for (int u = 0; u < G; u++) {
+                                switch (off) {
+                                case 0: ld_q6_K<0>(raw, jg + u, ql[u], qh[u]); break;
+                                case 2: ld_q6_K<2>(raw, jg + u, ql[u], qh[u]); break;
+                                case 4: ld_q6_K<4>(raw, jg + u, ql[u], qh[u]); break;
+                                case 6: ld_q6_K<6>(raw, jg + u, ql[u], qh[u]); break;
+                                case 8: ld_q6_K<8>(raw, jg + u, ql[u], qh[u]); break;
+                                case 10: ld_q6_K<10>(raw, jg + u, ql[u], qh[u]); break;
+                                case 12: ld_q6_K<12>(raw, jg + u, ql[u], qh[u]); break;
+                                default: ld_q6_K<14>(raw, jg + u, ql[u], qh[u]); break;
+                                }
+                            }
+#pragma unroll
+                            for (int u = 0; u < G; u++)
+                                st_q6_K(h, jg + u, ql[u], qh[u], smem + L::OFF_OPA + osl[u] * OP_BYTES,
+                                        smem + L::OFF_OPH + osl[u] * OP_BYTES, r);
+                        } else if constexpr (WT == QMM_Q5_K) {
+                            uint32_t q[G][8], qh[8];
+                            words<0, 16, 8>(raw, qh);  // the fifth bits of every sub-block
+#pragma unroll
+                            for (int u = 0; u < G; u++) ld_q5_K<0>(raw, jg + u, q[u]);
+#pragma unroll
+                            for (int u = 0; u < G; u++)
+                                st_q5_K(h, jg + u, q[u], qh, smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
+                        } else {
+                            uint32_t q[G][8];
+#pragma unroll
+                            for (int u = 0; u < G; u++) {
+                                if constexpr (WT == QMM_Q4_K) {
+                                    ld_q4_K<0>(raw, jg + u, q[u]);
+                                } else {
+                                    switch (off) {
+                                    case 0: ld_q2_K<0>(raw, jg + u, q[u]); break;
+                                    case 4: ld_q2_K<4>(raw, jg + u, q[u]); break;
+                                    case 8: ld_q2_K<8>(raw, jg + u, q[u]); break;
+                                    default: ld_q2_K<12>(raw, jg + u, q[u]); break;
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int u = 0; u < G; u++) {
+                                if constexpr (WT == QMM_Q4_K)
+                                    st_q4_K(h, jg + u, q[u], smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
+                                else st_q2_K(h, jg + u, q[u], smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
                             }
                         }
-#pragma unroll
-                        for (int u = 0; u < G; u++)
-                            st_q6_K(h, jg + u, ql[u], qh[u], smem + L::OFF_OPA + osl[u] * OP_BYTES,
-                                    smem + L::OFF_OPH + osl[u] * OP_BYTES, r);
-                    } else if constexpr (WT == QMM_Q5_K) {
-                        uint32_t q[G][8], qh[8];
-                        words<0, 16, 8>(raw, qh);  // the fifth bits of every sub-block
-#pragma unroll
-                        for (int u = 0; u < G; u++) ld_q5_K<0>(raw, jg + u, q[u]);
-#pragma unroll
-                        for (int u = 0; u < G; u++) st_q5_K(h, jg + u, q[u], qh, smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
                     } else {
                         uint32_t q[G][8];
 #pragma unroll
                         for (int u = 0; u < G; u++) {
-                            if constexpr (WT == QMM_Q4_K) {
-                                ld_q4_K<0>(raw, jg + u, q[u]);
-                            } else {
-                                switch (off) {
-                                case 0: ld_q2_K<0>(raw, jg + u, q[u]); break;
-                                case 4: ld_q2_K<4>(raw, jg + u, q[u]); break;
-                                case 8: ld_q2_K<8>(raw, jg + u, q[u]); break;
-                                default: ld_q2_K<12>(raw, jg + u, q[u]); break;
-                                }
+                            switch (off) {
+                            case 0: ld_x<0>(raw, jg + u, q[u]); break;
+                            case 4: ld_x<4>(raw, jg + u, q[u]); break;
+                            case 8: ld_x<8>(raw, jg + u, q[u]); break;
+                            default: ld_x<12>(raw, jg + u, q[u]); break;
                             }
                         }
 #pragma unroll
-                        for (int u = 0; u < G; u++) {
-                            if constexpr (WT == QMM_Q4_K) st_q4_K(h, jg + u, q[u], smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
-                            else st_q2_K(h, jg + u, q[u], smem + L::OFF_OPA + osl[u] * OP_BYTES, r);
+                        for (int u = 0; u < G; u++) st_x(q[u], smem + L::OFF_OPB + osl[u] * OP_BYTES, r);
+                    }
+                    if (jg + G == 8) {
+                        // the min operands of this super-block; their slot was last read by
+                        // the min MMA of super-block sb - 2, complete once its acc_full fired
+                        if (sb >= 2 && !wait_or_abort(bars.acc_full(as), ((sb - 2) >> 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        uint32_t hv[8];
+                        if (is_w) {
+                            min_row<WT>(h, hv);
+                            put_min(smem + L::OFF_MINA + as * MIN_BYTES, r, hv);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; i++)
+                                hv[i] = h2_of((int)(int16_t)(bs[i] & 0xFFFFu), (int)(int16_t)(bs[i] >> 16));
+                            put_min(smem + L::OFF_MINB + as * MIN_BYTES, r, hv);
                         }
                     }
-                } else {
-                    uint32_t q[G][8];
+                    fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
+                    __syncwarp();
+                    if (lane == 0) {
 #pragma unroll
-                    for (int u = 0; u < G; u++) {
-                        switch (off) {
-                        case 0: ld_x<0>(raw, jg + u, q[u]); break;
-                        case 4: ld_x<4>(raw, jg + u, q[u]); break;
-                        case 8: ld_x<8>(raw, jg + u, q[u]); break;
-                        default: ld_x<12>(raw, jg + u, q[u]); break;
-                        }
+                        for (int u = 0; u < G; u++) mbar_arrive(bars.op_full(osl[u]));
                     }
-#pragma unroll
-                    for (int u = 0; u < G; u++) st_x(q[u], smem + L::OFF_OPB + osl[u] * OP_BYTES, r);
-                }
-                if (jg + G == 8) {
-                    // the min operands of this super-block; their slot was last read by
-                    // the min MMA of super-block sb - 2, complete once its acc_full fired
-                    if (sb >= 2 && !wait_or_abort(bars.acc_full(as), ((sb - 2) >> 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    uint32_t hv[8];
-                    if (is_w) {
-                        min_row<WT>(h, hv);
-                        put_min(smem + L::OFF_MINA + as * MIN_BYTES, r, hv);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; i++) hv[i] = h2_of((int)(int16_t)(bs[i] & 0xFFFFu), (int)(int16_t)(bs[i] >> 16));
-                        put_min(smem + L::OFF_MINB + as * MIN_BYTES, r, hv);
-                    }
-                }
-                fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
-                __syncwarp();
-                if (lane == 0) {
-#pragma unroll
-                    for (int u = 0; u < G; u++) mbar_arrive(bars.op_full(osl[u]));
                 }
             }
-            if (!ok) break;
-            prefetch(sb + 2);  // this stage's bytes are all read
+            // Every thread of the role has read this stage: one of them refills it.  The
+            // barrier also makes the decision to stop the same on all 128 threads, so none
+            // is left waiting at a later barrier.
+            const bool stop = !ok || *abort_flag;
+            if (is_w ? named_bar_any<1, 128>(stop) : named_bar_any<2, 128>(stop)) break;
+            if (r == 0 && sb + 2 < nsb) load(sb + 2);
         }
-        cp_async_wait<0>();
     } else {
         // ------------------------------------------------------------ epilogue
         const int e = warp - EPI0;
@@ -703,6 +722,14 @@ template <int WT>
 static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                             cudaStream_t stream, bool pdl) {
     using L = kq::Layout<WT>;
+    using F = kq::Fmt<WT>;
+    // the rows of W and of the activation as TMA maps of 8-byte elements; a box is
+    // one super-block's 16-byte aligned superset of 128 rows (tokens)
+    const uint64_t nsb = (uint64_t)(K / 256);
+    CUtensorMap wmap, xmap;
+    if (!make_row_map(&wmap, W, nsb * F::BB, (uint64_t)N, F::RAWW, 8) ||
+        !make_row_map(&xmap, xq, nsb * 292, (uint64_t)M, kq::RAWX, 8))
+        return QMM_E_CUDA;
     static PerDeviceOnce attr_once;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return QMM_E_CUDA;
@@ -723,8 +750,8 @@ static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kq::matmul_kq_kernel<WT>, (const uint8_t*)W, (const uint8_t*)xq, Y,
-                                             (int)M, (int)N, (int)K, pdl ? 1 : 0);
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, kq::matmul_kq_kernel<WT>, wmap, xmap, Y, (int)M, (int)N, (int)K, pdl ? 1 : 0);
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
 

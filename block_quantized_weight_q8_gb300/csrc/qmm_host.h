@@ -2,6 +2,7 @@
 // argument validation, device properties, and launch utilities.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -101,6 +102,13 @@ class PerDeviceOnce {
 // weight type.
 qmm_status linear_impl(int wt, const void* W, const float* x, void* scratch, size_t scratch_bytes, float* y,
                        int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+// A 2-D TMA map over `rows` rows of `row_bytes` bytes, viewed as elements of
+// `elem_bytes` (2 or 8) bytes, with boxes of `box_bytes` x 128 rows; reads past
+// the end of a row or below the last row return zeros.  False if the driver
+// rejects the map (or has no cuTensorMapEncodeTiled).
+bool make_row_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                  int elem_bytes);
 
 inline qmm_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_E_CUDA;
