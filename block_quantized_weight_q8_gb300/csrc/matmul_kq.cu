@@ -138,6 +138,7 @@ __device__ __forceinline__ uint32_t h2_of(int lo, int hi) {
     const __half2 h = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
     return *reinterpret_cast<const uint32_t*>(&h);
 }
+__device__ __forceinline__ uint32_t hpair(int v) { return h2_of(v, v); }
 __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
     const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
     return *reinterpret_cast<const uint32_t*>(&r);
@@ -194,12 +195,33 @@ __device__ __forceinline__ void put_block(uint8_t* op, int r, const uint32_t* q,
         *reinterpret_cast<uint4*>(op + op_off(r, kq)) = v;
     }
 }
+// The same for scales sc <= 63 (Q4_K, Q5_K, Q2_K): sc * q as one fma per pair,
+// (1024 + q) * sc - 1024 * sc, whose exact value q * sc < 2048 is an fp16
+// integer, so the fma's one rounding leaves it exact.  c_* = -1024 * s_*.
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                              *reinterpret_cast<const __half2*>(&c));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ void put_block_fma(uint8_t* op, int r, const uint32_t* q, int sc_lo, int sc_hi) {
+    const uint32_t slo = hpair(sc_lo), shi = hpair(sc_hi);
+    const uint32_t clo = hpair(-1024 * sc_lo), chi = hpair(-1024 * sc_hi);
+#pragma unroll
+    for (int kq = 0; kq < 4; kq++) {  // values 8kq..8kq+7: words 2kq, 2kq+1
+        const uint32_t s = kq < 2 ? slo : shi, c = kq < 2 ? clo : chi;
+        uint4 v;
+        v.x = h2_fma(bytes_to_h2(q[2 * kq], 0x5140), s, c);
+        v.y = h2_fma(bytes_to_h2(q[2 * kq], 0x7362), s, c);
+        v.z = h2_fma(bytes_to_h2(q[2 * kq + 1], 0x5140), s, c);
+        v.w = h2_fma(bytes_to_h2(q[2 * kq + 1], 0x7362), s, c);
+        *reinterpret_cast<uint4*>(op + op_off(r, kq)) = v;
+    }
+}
 // 16 fp16 values (as 8 pairs) into the min operand row r
 __device__ __forceinline__ void put_min(uint8_t* op, int r, const uint32_t* h) {
     *reinterpret_cast<uint4*>(op + min_off(r, 0)) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(op + min_off(r, 1)) = make_uint4(h[4], h[5], h[6], h[7]);
 }
-__device__ __forceinline__ uint32_t hpair(int v) { return h2_of(v, v); }
 
 // ------------------------------------------------------------------ weight decoders
 // Per super-block header, kept packed in registers (no arrays indexed at run
@@ -239,8 +261,7 @@ __device__ __forceinline__ void st_q4_K(const Hdr& h, int j, uint32_t* q, uint8_
     const int sh = (j & 1) * 4;
 #pragma unroll
     for (int i = 0; i < 8; i++) q[i] = (q[i] >> sh) & 0x0F0F0F0Fu;
-    const uint32_t s = hpair(sc_q4_K(h, j));
-    put_block(opA, r, q, s, s);
+    put_block_fma(opA, r, q, sc_q4_K(h, j), sc_q4_K(h, j));
 }
 
 // Q5_K: the Q4_K header (d, dmin, packed scales and mins) @0, qh[32]@16,
@@ -260,8 +281,7 @@ __device__ __forceinline__ void st_q5_K(const Hdr& h, int j, uint32_t* q, const 
     const int sh = (j & 1) * 4;
 #pragma unroll
     for (int i = 0; i < 8; i++) q[i] = ((q[i] >> sh) & 0x0F0F0F0Fu) | (((qh[i] >> j) & 0x01010101u) << 4);
-    const uint32_t s = hpair(sc_q4_K(h, j));
-    put_block(opA, r, q, s, s);
+    put_block_fma(opA, r, q, sc_q4_K(h, j), sc_q4_K(h, j));
 }
 
 // Q2_K: scales[16]@0 (sc low nibble, m high), qs[64]@16, d@80, dmin@82;
@@ -287,7 +307,7 @@ __device__ __forceinline__ void st_q2_K(const Hdr& h, int j, uint32_t* q, uint8_
     const int sh = 2 * (j & 3);
 #pragma unroll
     for (int i = 0; i < 8; i++) q[i] = (q[i] >> sh) & 0x03030303u;
-    put_block(opA, r, q, hpair(sc_q2_K(h, 2 * j)), hpair(sc_q2_K(h, 2 * j + 1)));
+    put_block_fma(opA, r, q, sc_q2_K(h, 2 * j), sc_q2_K(h, 2 * j + 1));
 }
 
 // Q6_K (GGUF layout, a reading): ql[128]@0, qh[64]@128, int8 scales[16]@192,
