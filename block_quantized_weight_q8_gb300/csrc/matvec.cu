@@ -163,8 +163,8 @@ __device__ __forceinline__ void issue_item(const uint8_t* W, uint64_t g0, uint64
 // (the weights, which nothing writes) before it waits for its predecessor's
 // grid; only then does it read the activation, issue the remaining copies and
 // write y.  Few copies are in flight while the activation is read, so its
-// loads are not queued behind the whole weight stream (a fused Q8_0 step with
-// several items per warp requests the rest once the row's loads are out).
+// loads are not queued behind the whole weight stream (Q8_0 weights with
+// several items per warp request the rest once the row's loads are out).
 //
 // A Q8_0 activation block (f16 scale bits, 8 code words) into the layout the
 // decoder of WT reads.
@@ -320,6 +320,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                 if (lpb == 4) fused_q8_0_lanes<WT, SU, FUSE, 4>(x, set.gamma, sn, xq_out, K, nsu, aq, ad, as, rest);
                 if (lpb == 2) fused_q8_0_lanes<WT, SU, FUSE, 2>(x, set.gamma, sn, xq_out, K, nsu, aq, ad, as, rest);
             }
+            // the same early request on a quantized Q8_0 row (unsplit rows only: the split
+            // 4096 x 12288 matrix measured 0.1 us slower; 12288 x 4096: 9.09 -> 8.92 us)
+            const bool early0 = !FUSE && !SPLIT && WT == QMM_Q8_0 && nitems >= 2 * nw;
+            bool done0 = false;
             for (int b = tid; lpb == 1 && b < nb; b += nthr) {
                 uint32_t w[8], dbits;
                 if constexpr (FUSE) {
@@ -339,8 +343,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) matvec_kernel(const __grid_
                     dbits = p[0];
 #pragma unroll
                     for (int i = 0; i < 8; i++) w[i] = (uint32_t)p[1 + 2 * i] | ((uint32_t)p[2 + 2 * i] << 16);
+                    if (early0 && !done0 && lane == 0) issue_rest();
+                    done0 = true;
                 }
                 put_act_block<WT, SU>(w, dbits, b, nb, nsu, aq, ad, as);
+            }
+            if (early0) {  // a warp with no block of the row still requests its ring
+                if (!done0 && lane == 0) issue_rest();
+                early = true;
             }
         } else {
             if constexpr (FUSE) {
