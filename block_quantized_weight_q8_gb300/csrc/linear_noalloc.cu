@@ -56,6 +56,7 @@ qmm_status qmm_linear_noalloc(int wtype, const void* W, const float* x, float* y
     void* scratch = nullptr;
     const qmm_status st = noalloc_scratch(&scratch);
     if (st != QMM_OK) return st;
+    const NoWorkspaceAllocScope no_alloc;  // the K-quant prefill keeps its in-kernel conversion
     return linear_impl(wtype, W, x, scratch, kNoAllocScratchBytes, y, M, N, K, (cudaStream_t)stream);
 }
 

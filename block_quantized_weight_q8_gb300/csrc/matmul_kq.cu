@@ -57,9 +57,23 @@ constexpr int RAWX = 304;                 // a Q8_K super-block (292 B) as whole
 constexpr int SC_SLOTS = 4;               // super-blocks of scales in flight
 constexpr int OP_BYTES = BM * 32 * 2;     // 8192: one 32-value block of one fp16 operand
 constexpr int MIN_BYTES = BM * 16 * 2;    // 4096: one 16-value min operand
-constexpr int NUM_CONV_WARPS = 8, NUM_EPI_WARPS = 16;
-constexpr int CONV0 = 1, EPI0 = CONV0 + NUM_CONV_WARPS;
-constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 800
+constexpr int NUM_W_WARPS = 4, NUM_EPI_WARPS = 16;
+constexpr int CONV0 = 1;  // first weight-converter warp
+// The activation side: four converter warps (XP false), or one warp that copies
+// the operands a pre-pass kernel prepared (XP true, see kq_xprep_kernel).
+template <bool XP>
+struct Roles {
+    static constexpr int X_WARPS = XP ? 1 : 4;
+    static constexpr int X0 = CONV0 + NUM_W_WARPS;        // first activation warp
+    static constexpr int EPI0 = X0 + X_WARPS;             // first epilogue warp
+    static constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 800, or 704 with the pre-pass
+    static constexpr int OP_FULL_WARPS = XP ? NUM_W_WARPS : NUM_W_WARPS + 4;  // arrivals per operand slot
+};
+// A super-block of prepared activation operands, as the pre-pass writes it and
+// one bulk copy brings it in: 8 blocks of fp16 codes (128 tokens x 32 values in
+// the UMMA K-major core-matrix layout), then the 16 group sums as fp16 in the
+// min operand's layout.
+constexpr int XP_BLOCK = BN * 32 * 2;                // 8192
 constexpr int TMEM_COLS = 512;            // 2 super-blocks x (value, min) x 128 columns
 
 template <int WT> struct Fmt;
@@ -70,29 +84,39 @@ template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, RAWW = 96, SPLI
 template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, RAWW = 224, SPLIT = 1, OP_SLOTS = 3, GROUP = 1; };
 template <> struct Fmt<QMM_Q5_K> { static constexpr int BB = 176, RAWW = 176, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
 
-template <int WT>
+constexpr int XP_BYTES = 8 * XP_BLOCK + MIN_BYTES;  // 69632
+
+template <int WT, bool XP = false>
 struct Layout {
     using F = Fmt<WT>;
     static constexpr int NCW = F::RAWW / 16;
-    static constexpr int RAW_STAGE = BM * F::RAWW + BN * RAWX;
+    static constexpr int RAW_STAGE = BM * F::RAWW + (XP ? 0 : BN * RAWX);
     static constexpr int OFF_RAW = 0;                                          // 2 stages
-    static constexpr int OFF_OPA = OFF_RAW + 2 * RAW_STAGE;                    // A (Q6_K: sc*(q&7))
+    static constexpr int OFF_XP = OFF_RAW + 2 * RAW_STAGE;                     // XP: 2 stages of XP_BYTES
+    static constexpr int OFF_OPA = OFF_XP + (XP ? 2 * XP_BYTES : 0);           // A (Q6_K: sc*(q&7))
     static constexpr int OFF_OPH = OFF_OPA + F::OP_SLOTS * OP_BYTES;           // Q6_K: 8*sc*(q>>3)
     static constexpr int OFF_OPB = OFF_OPH + F::SPLIT * F::OP_SLOTS * OP_BYTES;  // activation codes
-    static constexpr int OFF_MINA = OFF_OPB + F::OP_SLOTS * OP_BYTES;          // 2 slots of f_g
+    static constexpr int OFF_MINA = OFF_OPB + (XP ? 0 : F::OP_SLOTS * OP_BYTES);  // 2 slots of f_g
     static constexpr int OFF_MINB = OFF_MINA + 2 * MIN_BYTES;                  // 2 slots of bsum_g
-    static constexpr int OFF_SCD = OFF_MINB + 2 * MIN_BYTES;                   // d_w per row
+    static constexpr int OFF_SCD = OFF_MINB + (XP ? 0 : 2 * MIN_BYTES);        // d_w per row
     static constexpr int OFF_SCC = OFF_SCD + SC_SLOTS * BM * 4;                // c_w per row
     static constexpr int OFF_SCX = OFF_SCC + SC_SLOTS * BM * 4;                // d_x per token
-    static constexpr int OFF_BAR = OFF_SCX + SC_SLOTS * BN * 4;
+    static constexpr int OFF_BAR = OFF_SCX + (XP ? 0 : SC_SLOTS * BN * 4);
     // op_full[S] mma_done[S] acc_full[2] acc_empty[2] sc_empty[SC_SLOTS] raw_full[2 roles][2 stages]
-    static constexpr int NBARS = 2 * F::OP_SLOTS + 4 + SC_SLOTS + 4;
+    // x_empty[2] (XP: the MMAs of a prepared stage are done)
+    static constexpr int NBARS = 2 * F::OP_SLOTS + 4 + SC_SLOTS + 4 + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
 };
 static_assert(Layout<QMM_Q6_K>::SMEM <= 232448, "Q6_K layout exceeds shared memory");
 static_assert(Layout<QMM_Q4_K>::SMEM <= 232448, "Q4_K layout exceeds shared memory");
 static_assert(Layout<QMM_Q5_K>::SMEM <= 232448, "Q5_K layout exceeds shared memory");
+static_assert(Layout<QMM_Q4_K, true>::SMEM <= 232448 && Layout<QMM_Q2_K, true>::SMEM <= 232448 &&
+                  Layout<QMM_Q5_K, true>::SMEM <= 232448,
+              "pre-pass layout exceeds shared memory");
+static_assert(Layout<QMM_Q4_K, true>::OFF_OPA % 128 == 0 && Layout<QMM_Q2_K, true>::OFF_OPA % 128 == 0 &&
+                  Layout<QMM_Q5_K, true>::OFF_OPA % 128 == 0 && XP_BYTES % 128 == 0,
+              "operand tiles need 128-byte alignment");
 
 template <int WT>
 struct Bars {
@@ -103,8 +127,10 @@ struct Bars {
     __device__ uint32_t acc_full(int i) const { return base + 8u * (2 * S + i); }
     __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * S + 2 + i); }
     __device__ uint32_t sc_empty(int i) const { return base + 8u * (2 * S + 4 + i); }
-    // the TMA box of role `role` (0 weights, 1 activation) landed in stage s
+    // role `role`'s bytes (0 weights, 1 activation: a TMA box, or with the pre-pass
+    // its prepared operands) landed in stage s
     __device__ uint32_t raw_full(int role, int s) const { return base + 8u * (2 * S + 4 + SC_SLOTS + 2 * role + s); }
+    __device__ uint32_t x_empty(int s) const { return base + 8u * (2 * S + 4 + SC_SLOTS + 4 + s); }
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -397,13 +423,52 @@ __device__ __forceinline__ void hdr_x(const Raw& raw, uint32_t* d_bits, uint32_t
     words<OFF, 260, 8>(raw, bs);
 }
 
+// ------------------------------------------------------------------ the activation pre-pass
+// Every CTA of a token tile converts the same Q8_K rows, so with a workspace
+// they are converted once: CTA (sb, ty) writes super-block sb of token tile ty
+// as XP_BYTES of prepared operands -- for each of its 8 blocks the fp16 codes of
+// the tile's 128 tokens in the core-matrix layout the MMA reads, then the 16
+// group sums as fp16 -- and the tile's 128 scales d_x to dxg.  One thread per
+// token; tokens past M get zeros.  The same conversion as the in-kernel path
+// (st_x, the bsum pairs), so the operands are the same bits.
+__global__ void __launch_bounds__(BN) kq_xprep_kernel(const uint8_t* __restrict__ xq, uint8_t* __restrict__ xp,
+                                                      float* __restrict__ dxg, int M, int nsb, int pdl) {
+    if (pdl) pdl_launch_dependents();
+    if (pdl) pdl_wait();  // the rows come from the previous kernel
+    const int r = threadIdx.x, sb = blockIdx.x, ty = blockIdx.y;
+    const int t = ty * BN + r;
+    const size_t unit = (size_t)ty * nsb + sb;
+    uint8_t* out = xp + unit * XP_BYTES;
+    const bool real = t < M;
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(xq + ((size_t)(real ? t : 0) * nsb + sb) * 292);
+#pragma unroll 2
+    for (int j = 0; j < 8; j++) {  // block j: code words 1 + 8j .. 8 + 8j
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) q[i] = real ? row[1 + 8 * j + i] : 0x00000000u;
+        st_x(q, out + j * XP_BLOCK, r);
+    }
+    uint32_t hv[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const uint32_t bp = real ? row[65 + i] : 0u;  // the bsum pair of groups 2i, 2i + 1
+        hv[i] = h2_of((int)(int16_t)(bp & 0xFFFFu), (int)(int16_t)(bp >> 16));
+    }
+    put_min(out + 8 * XP_BLOCK, r, hv);
+    dxg[unit * BN + r] = real ? __uint_as_float(row[0]) : 0.0f;
+}
+
 // ------------------------------------------------------------------ the kernel
-template <int WT>
-__global__ void __launch_bounds__(THREADS, 1)
+// XP: the activation operands come prepared by kq_xprep_kernel (xp, and the
+// scales d_x in dxg); otherwise xmap's raw Q8_K rows are converted here.
+template <int WT, bool XP>
+__global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
     matmul_kq_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                     float* __restrict__ Y, int M, int N, int K, int pdl) {
+                     const uint8_t* __restrict__ xp, const float* __restrict__ dxg, float* __restrict__ Y, int M,
+                     int N, int K, int pdl) {
     using F = Fmt<WT>;
-    using L = Layout<WT>;
+    using L = Layout<WT, XP>;
+    using R = Roles<XP>;
     constexpr int S = F::OP_SLOTS;
     if (pdl) pdl_launch_dependents();
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -425,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; i++) {
-            mbar_init(bars.op_full(i), NUM_CONV_WARPS);
+            mbar_init(bars.op_full(i), R::OP_FULL_WARPS);
             mbar_init(bars.op_empty(i), 1);
         }
         for (int i = 0; i < 2; i++) {
@@ -434,6 +499,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int i = 0; i < SC_SLOTS; i++) mbar_init(bars.sc_empty(i), NUM_EPI_WARPS);
         for (int i = 0; i < 4; i++) mbar_init(bars.raw_full(i >> 1, i & 1), 1);
+        for (int i = 0; i < 2; i++) mbar_init(bars.x_empty(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -460,6 +526,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int sb = 0; sb < nsb; sb++) {
                 const int as = sb & 1;
                 if (sb >= 2 && !wait_or_abort(bars.acc_empty(as), ((sb >> 1) - 1) & 1, abort_flag)) break;
+                // the prepared activation operands of this super-block (XP)
+                if (XP && !wait_or_abort(bars.raw_full(1, sb & 1), (sb >> 1) & 1, abort_flag)) break;
+                const uint32_t xs = sbase + L::OFF_XP + (uint32_t)((sb & 1) * XP_BYTES);
                 const uint32_t dv = tmem + (uint32_t)(as * 128), dm = tmem + (uint32_t)(256 + as * 128);
                 bool ok = true;
                 for (int j = 0; j < 8; j++) {
@@ -467,27 +536,44 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (!wait_or_abort(bars.op_full(os), (b / S) & 1, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t so = (uint64_t)(os * (OP_BYTES >> 4));
-                    mma_f16(dv, a0 + so, b0 + so, idesc, j > 0 ? 1u : 0u);
-                    mma_f16(dv, a0 + so + (256 >> 4), b0 + so + (256 >> 4), idesc, 1u);
+                    const uint64_t bj = XP ? smem_desc(xs + (uint32_t)(j * XP_BLOCK), 128, 512) : b0 + so;
+                    mma_f16(dv, a0 + so, bj, idesc, j > 0 ? 1u : 0u);
+                    mma_f16(dv, a0 + so + (256 >> 4), bj + (256 >> 4), idesc, 1u);
                     if (F::SPLIT) {
                         mma_f16(dv, h0 + so, b0 + so, idesc, 1u);
                         mma_f16(dv, h0 + so + (256 >> 4), b0 + so + (256 >> 4), idesc, 1u);
                     }
                     if (j == 7) {
                         const uint64_t mo = (uint64_t)(as * (MIN_BYTES >> 4));
-                        mma_f16(dm, ma0 + mo, mb0 + mo, idesc, 0u);
+                        const uint64_t mb = XP ? smem_desc(xs + (uint32_t)(8 * XP_BLOCK), 128, 256) : mb0 + mo;
+                        mma_f16(dm, ma0 + mo, mb, idesc, 0u);
                     }
                     mma_commit(bars.op_empty(os));
                     if (j == 7) mma_commit(bars.acc_full(as));
+                    if (XP && j == 7) mma_commit(bars.x_empty(sb & 1));  // the stage may be refilled
                 }
                 if (!ok) break;
             }
         }
-    } else if (warp < EPI0) {
+    } else if (XP && warp == R::X0) {
+        // ------------------------------------------------------------ prepared activation operands
+        if (lane == 0) {
+            if (pdl) pdl_wait();  // the pre-pass kernel wrote them
+            const uint8_t* src = xp + (size_t)blockIdx.y * nsb * XP_BYTES;
+            for (int sb = 0; sb < nsb; sb++) {
+                const int s = sb & 1;
+                if (sb >= 2 && !wait_or_abort(bars.x_empty(s), ((sb >> 1) - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(bars.raw_full(1, s), (uint32_t)XP_BYTES);
+                // every CTA of this token tile reads the same bytes: no eviction hint
+                bulk_g2s_nohint(sbase + L::OFF_XP + (uint32_t)(s * XP_BYTES), src + (size_t)sb * XP_BYTES,
+                                (uint32_t)XP_BYTES, bars.raw_full(1, s));
+            }
+        }
+    } else if (warp < R::EPI0) {
         // ------------------------------------------------------------ converters
-        const bool is_w = warp < CONV0 + NUM_CONV_WARPS / 2;
+        const bool is_w = XP || warp < R::X0;
         const int role = is_w ? 0 : 1;
-        const int r = (warp - (is_w ? CONV0 : CONV0 + NUM_CONV_WARPS / 2)) * 32 + lane;  // row or token
+        const int r = (warp - (is_w ? CONV0 : R::X0)) * 32 + lane;  // row or token
         if (!is_w && pdl) pdl_wait();  // the activation comes from the previous kernel
         const int BBs = is_w ? F::BB : 292;
         const int pitch = is_w ? F::RAWW : RAWX;  // the box's row pitch in shared memory
@@ -661,7 +747,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int e = warp - EPI0;
+        const int e = warp - R::EPI0;
+        if (XP && pdl) pdl_wait();  // d_x comes from the pre-pass kernel
         const int quad = warp & 3, cg = e >> 2;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cg * 32);
@@ -675,7 +762,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float dw = scd[ss * BM + row], cw = scc[ss * BM + row];
             const uint64_t dw2 = f2_pack(__float_as_uint(dw), __float_as_uint(dw));
             const uint64_t cw2 = f2_pack(__float_as_uint(-cw), __float_as_uint(-cw));
-            const uint64_t* dxs = reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
+            const uint64_t* dxs =
+                XP ? reinterpret_cast<const uint64_t*>(dxg + ((size_t)blockIdx.y * nsb + sb) * BN + cg * 32)
+                   : reinterpret_cast<const uint64_t*>(scx + ss * BN + cg * 32);
 #pragma unroll
             for (int qq = 0; qq < 4; qq++) {  // 8 columns at a time
                 uint32_t v[8], m[8];
@@ -738,31 +827,36 @@ namespace qmm {
 // reasonably; other shapes run one matvec per token.
 static bool kq_tensor_core_shape(int64_t M, int64_t K) { return K % 2048 == 0 && M >= 8; }
 
-template <int WT>
-static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
-                            cudaStream_t stream, bool pdl) {
-    using L = kq::Layout<WT>;
+// One launch of the tensor-core kernel; XP: the activation operands were prepared
+// into xp / dxg by kq_xprep_kernel (xq is then not read).
+template <int WT, bool XP>
+static qmm_status launch_kq_kernel(const void* W, const void* xq, const uint8_t* xp, const float* dxg, float* Y,
+                                   int64_t M, int64_t N, int64_t K, cudaStream_t stream, bool pdl) {
+    using L = kq::Layout<WT, XP>;
     using F = kq::Fmt<WT>;
     // the rows of W and of the activation as TMA maps of 8-byte elements; a box is
     // one super-block's 16-byte aligned superset of 128 rows (tokens)
     const uint64_t nsb = (uint64_t)(K / 256);
     CUtensorMap wmap, xmap;
-    if (!make_row_map(&wmap, W, nsb * F::BB, (uint64_t)N, F::RAWW, 8) ||
-        !make_row_map(&xmap, xq, nsb * 292, (uint64_t)M, kq::RAWX, 8))
+    if (!make_row_map(&wmap, W, nsb * F::BB, (uint64_t)N, F::RAWW, 8)) return QMM_E_CUDA;
+    if (XP) {
+        xmap = CUtensorMap{};  // not read
+    } else if (!make_row_map(&xmap, xq, nsb * 292, (uint64_t)M, kq::RAWX, 8)) {
         return QMM_E_CUDA;
+    }
     static PerDeviceOnce attr_once;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return QMM_E_CUDA;
     const qmm_status ast = attr_once.run(dev, [] {
-        return cudaFuncSetAttribute(kq::matmul_kq_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) ==
-                       cudaSuccess
+        return cudaFuncSetAttribute(kq::matmul_kq_kernel<WT, XP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    L::SMEM) == cudaSuccess
                    ? QMM_OK
                    : QMM_E_CUDA;
     });
     if (ast != QMM_OK) return ast;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + kq::BM - 1) / kq::BM), (unsigned)((M + kq::BN - 1) / kq::BN));
-    cfg.blockDim = dim3(kq::THREADS);
+    cfg.blockDim = dim3(kq::Roles<XP>::THREADS);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -770,9 +864,53 @@ static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, kq::matmul_kq_kernel<WT>, wmap, xmap, Y, (int)M, (int)N, (int)K, pdl ? 1 : 0);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kq::matmul_kq_kernel<WT, XP>, wmap, xmap, xp, dxg, Y, (int)M, (int)N,
+                                             (int)K, pdl ? 1 : 0);
     return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
+
+// Set while qmm_linear_noalloc runs on this thread: its callers must not see an
+// allocation, so the prefill converts the activation in the kernel itself.
+thread_local bool tl_no_workspace_alloc = false;
+
+// Q4_K, Q2_K and Q5_K convert the activation once, in a pre-pass, into a
+// stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on the caller's
+// stream: ~4.4 MB for 512 tokens at K = 4096); without one (no pool memory, or
+// inside qmm_linear_noalloc) every CTA converts it (Q6_K always: its second
+// weight operand leaves no room for the prepared stages).
+template <int WT>
+static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
+                            cudaStream_t stream, bool pdl) {
+    if constexpr (WT != QMM_Q6_K) {
+        if (!tl_no_workspace_alloc) {
+            const int64_t ntt = (M + kq::BN - 1) / kq::BN, nsb = K / 256;
+            const size_t xp_bytes = (size_t)(ntt * nsb) * kq::XP_BYTES;
+            const size_t dx_bytes = (size_t)(ntt * nsb) * kq::BN * sizeof(float);
+            void* buf = nullptr;
+            if (ntt * nsb <= 0x7FFFFFFF && cudaMallocAsync(&buf, xp_bytes + dx_bytes, stream) == cudaSuccess) {
+                uint8_t* xp = static_cast<uint8_t*>(buf);
+                float* dxg = reinterpret_cast<float*>(xp + xp_bytes);
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3((unsigned)nsb, (unsigned)ntt);
+                cfg.blockDim = dim3(kq::BN);
+                cfg.stream = stream;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = pdl ? 1 : 0;
+                qmm_status st = cudaLaunchKernelEx(&cfg, kq::kq_xprep_kernel, (const uint8_t*)xq, xp, dxg, (int)M,
+                                                   (int)nsb, pdl ? 1 : 0) == cudaSuccess
+                                    ? QMM_OK
+                                    : QMM_E_CUDA;
+                if (st == QMM_OK) st = launch_kq_kernel<WT, true>(W, xq, xp, dxg, Y, M, N, K, stream, true);
+                if (cudaFreeAsync(buf, stream) != cudaSuccess && st == QMM_OK) st = QMM_E_CUDA;
+                return st;
+            }
+            (void)cudaGetLastError();  // no workspace: convert in the kernel
+        }
+    }
+    return launch_kq_kernel<WT, false>(W, xq, nullptr, nullptr, Y, M, N, K, stream, pdl);
 }
 
 bool kq_uses_tensor_cores(int wt, int64_t M, int64_t K);

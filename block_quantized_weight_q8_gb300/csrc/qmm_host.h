@@ -110,6 +110,16 @@ qmm_status linear_impl(int wt, const void* W, const float* x, void* scratch, siz
 bool make_row_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
                   int elem_bytes);
 
+// True while an entry point that promises no allocation runs on this thread:
+// the K-quant prefill then converts the activation in its kernel instead of in
+// a pre-pass with a stream-ordered workspace.
+extern thread_local bool tl_no_workspace_alloc;
+struct NoWorkspaceAllocScope {
+    bool prev;
+    NoWorkspaceAllocScope() : prev(tl_no_workspace_alloc) { tl_no_workspace_alloc = true; }
+    ~NoWorkspaceAllocScope() { tl_no_workspace_alloc = prev; }
+};
+
 inline qmm_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_E_CUDA;
 }
