@@ -79,8 +79,15 @@ constexpr int NUM_CONV_WARPS = NUM_W_WARPS + NUM_X_WARPS;
 // its 32 tokens); 16-19: weight converters (warp % 4 = the lane quadrant of the
 // 32 rows each writes into TMEM); 20-23: activation converters; 24: TMA producer
 // (and the TMEM allocation); 25: MMA issuer.
-constexpr int W0 = NUM_EPI_WARPS, X0 = W0 + NUM_W_WARPS, TMA_WARP = X0 + NUM_X_WARPS, MMA_WARP = TMA_WARP + 1;
-constexpr int THREADS = (MMA_WARP + 1) * 32;  // 832
+// With the activation pre-pass (XP) the activation converters are gone and the
+// producer also copies each chunk's prepared operands: 22 warps.
+constexpr int W0 = NUM_EPI_WARPS, X0 = W0 + NUM_W_WARPS;
+template <bool XP>
+struct Roles {
+    static constexpr int TMA_WARP = X0 + (XP ? 0 : NUM_X_WARPS), MMA_WARP = TMA_WARP + 1;
+    static constexpr int THREADS = (MMA_WARP + 1) * 32;  // 832, or 704 with the pre-pass
+    static constexpr int CONV_WARPS = NUM_W_WARPS + (XP ? 0 : NUM_X_WARPS);  // arrivals per slot / stage
+};
 
 // Weight block bytes of the 32-value formats (Q4_0 18, Q8_0 34, Q4_1 20, Q5_0 22, Q5_1 24).
 __host__ __device__ constexpr int block_bytes32(int wt) {
@@ -91,7 +98,7 @@ __host__ __device__ constexpr int block_bytes32(int wt) {
 // dynamic shared memory base): the raw stages, the activation operand slots and
 // the per-block scales.  Q4_1 and Q5_1 also carry each row's m_w and each
 // token's d_x * sum(a) per block, for the min term.
-template <int WT>
+template <int WT, bool XP = false>
 struct Lay {
     static constexpr int WB = block_bytes32(WT);
     static constexpr bool HAS_MIN = WT == QMM_Q4_1 || WT == QMM_Q5_1;
@@ -103,16 +110,22 @@ struct Lay {
     static constexpr int SC_SLOTS = 16;
     static_assert(SC_SLOTS >= OP_SLOTS + S_BUFS + 1, "scale slots must outlive the epilogue's reads");
     static constexpr int W_RAW = BM * KB * WB;
-    static constexpr int RAW_BYTES = W_RAW + X_RAW;
+    static constexpr int RAW_BYTES = W_RAW + (XP ? 0 : X_RAW);
+    // XP: a chunk of prepared activation operands, as the pre-pass writes it and
+    // one bulk copy brings it in: KB blocks of fp16 codes (the core-matrix layout
+    // the MMA reads), each block's d_x for the 128 tokens, and (min formats) each
+    // block's d_x * sum(a)
+    static constexpr int XPS = KB * OP_B + KB * BN * 4 + (HAS_MIN ? KB * BN * 4 : 0);
     static constexpr int OFF_RAW = 0;
-    static constexpr int OFF_OPB = OFF_RAW + RAW_STAGES * RAW_BYTES;
-    static constexpr int OFF_SCW = OFF_OPB + OP_SLOTS * OP_B;
+    static constexpr int OFF_XP = OFF_RAW + RAW_STAGES * RAW_BYTES;  // XP: RAW_STAGES chunks of XPS
+    static constexpr int OFF_OPB = OFF_XP + (XP ? RAW_STAGES * XPS : 0);
+    static constexpr int OFF_SCW = OFF_OPB + (XP ? 0 : OP_SLOTS * OP_B);
     static constexpr int OFF_SCX = OFF_SCW + SC_SLOTS * BM * 4;
     static constexpr int OFF_SCM = OFF_SCX + SC_SLOTS * BN * 4;            // m_w per row (min formats)
     static constexpr int OFF_SCS = OFF_SCM + (HAS_MIN ? SC_SLOTS * BM * 4 : 0);  // d_x * sum(a) per token
     static constexpr int OFF_BAR = OFF_SCS + (HAS_MIN ? SC_SLOTS * BN * 4 : 0);
-    // barriers: raw_full[2] raw_empty[2] op_full[4] mma_done[8] acc_empty[3]
-    static constexpr int NBARS = 2 * RAW_STAGES + OP_SLOTS + DONE_RING + S_BUFS;
+    // barriers: raw_full[2] raw_empty[2] op_full[4] mma_done[8] acc_empty[3] x_full[2] x_empty[2]
+    static constexpr int NBARS = 2 * RAW_STAGES + OP_SLOTS + DONE_RING + S_BUFS + 2 * RAW_STAGES;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM + 16;
 };
@@ -120,6 +133,15 @@ static_assert(Lay<QMM_Q4_0>::SMEM_BYTES <= 232448 && Lay<QMM_Q8_0>::SMEM_BYTES <
                   Lay<QMM_Q4_1>::SMEM_BYTES <= 232448 && Lay<QMM_Q5_0>::SMEM_BYTES <= 232448 &&
                   Lay<QMM_Q5_1>::SMEM_BYTES <= 232448,
               "prefill smem");
+static_assert(Lay<QMM_Q4_0, true>::SMEM_BYTES <= 232448 && Lay<QMM_Q8_0, true>::SMEM_BYTES <= 232448 &&
+                  Lay<QMM_Q4_1, true>::SMEM_BYTES <= 232448 && Lay<QMM_Q5_0, true>::SMEM_BYTES <= 232448 &&
+                  Lay<QMM_Q5_1, true>::SMEM_BYTES <= 232448,
+              "prefill smem (pre-pass)");
+static_assert(Lay<QMM_Q4_0, true>::OFF_XP % 128 == 0 && Lay<QMM_Q8_0, true>::OFF_XP % 128 == 0 &&
+                  Lay<QMM_Q4_1, true>::OFF_XP % 128 == 0 && Lay<QMM_Q5_0, true>::OFF_XP % 128 == 0 &&
+                  Lay<QMM_Q5_1, true>::OFF_XP % 128 == 0 && Lay<QMM_Q4_1, true>::XPS % 128 == 0 &&
+                  Lay<QMM_Q4_0, true>::XPS % 128 == 0,
+              "operand tiles need 128-byte alignment");
 
 struct Bars {
     uint32_t base;
@@ -131,6 +153,13 @@ struct Bars {
     __device__ uint32_t mma_done(int b) const { return base + 8u * (2 * RAW_STAGES + OP_SLOTS + (b & (DONE_RING - 1))); }
     // accumulator i read into registers by every epilogue warp
     __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * RAW_STAGES + OP_SLOTS + DONE_RING + i); }
+    // XP: the prepared chunk in stage i landed / was used by the MMAs and the epilogue
+    __device__ uint32_t x_full(int i) const {
+        return base + 8u * (2 * RAW_STAGES + OP_SLOTS + DONE_RING + S_BUFS + i);
+    }
+    __device__ uint32_t x_empty(int i) const {
+        return base + 8u * (3 * RAW_STAGES + OP_SLOTS + DONE_RING + S_BUFS + i);
+    }
 };
 
 // wait with a time limit; on failure set the error word and the CTA's abort flag.
@@ -167,10 +196,10 @@ __device__ __forceinline__ void put_operand(const uint32_t (&h)[16], uint32_t tm
 // token of the tile; per block it waits for the operand slot (freed by the MMAs
 // of block b - OP_SLOTS; that also frees the block's scale slot), converts, and
 // hands the block to the MMA issuer.
-template <int WT, bool IS_W>
+template <int WT, bool IS_W, bool XP>
 __device__ __forceinline__ void convert_loop(uint8_t* smem, uint32_t sbase, const Bars& bars, uint32_t tmem, int r,
                                              int nchunks, volatile int* abort_flag) {
-    using L = Lay<WT>;
+    using L = Lay<WT, XP>;
     constexpr int SC_SLOTS = L::SC_SLOTS, RAW_BYTES = L::RAW_BYTES, W_RAW = L::W_RAW;
     constexpr int RB = IS_W ? L::WB : 34;  // raw block bytes of this role
     static_assert(KB % OP_SLOTS == 0 && SC_SLOTS == 2 * KB && DONE_RING == KB,
@@ -182,10 +211,16 @@ __device__ __forceinline__ void convert_loop(uint8_t* smem, uint32_t sbase, cons
     float* const scale_row = reinterpret_cast<float*>(smem + (IS_W ? L::OFF_SCW : L::OFF_SCX)) + r;
     float* const mw_row = reinterpret_cast<float*>(smem + L::OFF_SCM) + r;
     float* const asum_row = reinterpret_cast<float*>(smem + L::OFF_SCS) + r;
+    // XP: the weight threads also move token r's prepared d_x (and d_x * sum(a)) of
+    // each block from the chunk's stage into the scale ring the epilogue reads
+    float* const xscale_row = reinterpret_cast<float*>(smem + L::OFF_SCX) + r;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; c++) {
         const int s = c % RAW_STAGES;
         if (!wait_or_abort(bars.raw_full(s), (c / RAW_STAGES) & 1, abort_flag)) break;
+        if (XP && IS_W && !__all_sync(0xffffffffu, wait_or_abort(bars.x_full(s), (c / RAW_STAGES) & 1, abort_flag)))
+            break;
+        const float* const xstage = reinterpret_cast<const float*>(smem + L::OFF_XP + s * L::XPS + KB * OP_B) + r;
         const uint8_t* row = smem + L::OFF_RAW + s * RAW_BYTES + (IS_W ? 0 : W_RAW) + r * (KB * RB);
         // the row's 8 blocks, read as two windows of 4 blocks from the 16-byte boundary at or
         // below each window's first byte (rows of 8 blocks are 16-byte multiples)
@@ -274,6 +309,10 @@ __device__ __forceinline__ void convert_loop(uint8_t* smem, uint32_t sbase, cons
                     scale_row[ssl * BN] = h2f(dbits);
                     if (!IS_W && L::HAS_MIN) asum_row[ssl * BN] = h2f(dbits) * (float)asum;
                 }
+                if (XP && IS_W) {  // token r's prepared scales of this block into the ring
+                    xscale_row[ssl * BN] = xstage[kb * BN];
+                    if (L::HAS_MIN) asum_row[ssl * BN] = xstage[(KB + kb) * BN];
+                }
                 put_operand<IS_W>(h, tmem_row + (uint32_t)(os * 16), opb_row + os * OP_B);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.op_full(os));
@@ -284,13 +323,58 @@ __device__ __forceinline__ void convert_loop(uint8_t* smem, uint32_t sbase, cons
         // to overwrite a window whose loads a converter had just issued.
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.raw_empty(s));
+        if (XP && IS_W && lane == 0) mbar_arrive(bars.x_empty(s));  // the chunk's scales are copied
     }
 }
 
-template <int WT>
-__global__ void __launch_bounds__(THREADS, 1)
+// ------------------------------------------------------------------ the activation pre-pass
+// Every CTA of a token tile converts the same Q8_0 rows, so with a workspace they
+// are converted once: token tile ty's chunk c (blocks 8c .. 8c + 7) becomes
+// Lay<WT, true>::XPS bytes -- per block the fp16 codes of the tile's 128 tokens in
+// the core-matrix layout the MMA reads, then per block the f32 d_x of the 128
+// tokens, then (MIN) per block d_x * sum(a).  CTA (b, ty) writes block b's parts,
+// one thread per token; tokens past M get zeros.  The conversions are the in-kernel converter's, so
+// the operands are the same bits.
+template <bool MIN>
+__global__ void __launch_bounds__(BN) q8_0_xprep_kernel(const uint8_t* __restrict__ xq, uint8_t* __restrict__ xp,
+                                                        int M, int nchunks, int chunk_bytes, int pdl) {
+    if (pdl) pdl_launch_dependents();
+    if (pdl) pdl_wait();  // the rows come from the previous kernel
+    const int r = threadIdx.x, b = blockIdx.x, ty = blockIdx.y;
+    const int c = b / KB, kb = b % KB;
+    const int t = ty * BN + r;
+    const bool real = t < M;
+    uint8_t* out = xp + ((size_t)ty * nchunks + c) * chunk_bytes;
+    const uint32_t m128 = 0x64806480u;  // (1152, 1152): 1024 + (a + 128) - 1152 = a
+    {
+        // 34-byte blocks are 2-byte aligned: 16-bit loads
+        const unsigned short* p =
+            reinterpret_cast<const unsigned short*>(xq + ((size_t)(real ? t : 0) * nchunks * KB + (size_t)b) * 34);
+        const uint32_t dbits = real ? p[0] : 0u;
+        int asum = 0;
+#pragma unroll
+        for (int kq = 0; kq < 4; kq++) {  // elements 8kq..8kq+7
+            const uint32_t c0 = real ? ((uint32_t)p[1 + 4 * kq] | ((uint32_t)p[2 + 4 * kq] << 16)) : 0u;
+            const uint32_t c1 = real ? ((uint32_t)p[3 + 4 * kq] | ((uint32_t)p[4 + 4 * kq] << 16)) : 0u;
+            if (MIN) asum = __dp4a((int)c1, 0x01010101, __dp4a((int)c0, 0x01010101, asum));
+            const uint32_t w0 = c0 ^ 0x80808080u, w1 = c1 ^ 0x80808080u;
+            const uint4 v = make_uint4(h2_sub(bytes_to_h2(w0, 0x5140), m128), h2_sub(bytes_to_h2(w0, 0x7362), m128),
+                                       h2_sub(bytes_to_h2(w1, 0x5140), m128), h2_sub(bytes_to_h2(w1, 0x7362), m128));
+            *reinterpret_cast<uint4*>(out + kb * OP_B + ((r >> 3) * 4 + kq) * 128 + (r & 7) * 16) = v;
+        }
+        float* sc = reinterpret_cast<float*>(out + KB * OP_B) + kb * BN + r;
+        sc[0] = h2f(dbits);
+        if (MIN) sc[KB * BN] = h2f(dbits) * (float)asum;
+    }
+}
+
+// XP: the activation operands come prepared by q8_0_xprep_kernel (xp, one chunk
+// of XPS bytes per token tile and 8 blocks); otherwise xmap's raw Q8_0 rows are
+// converted here.
+template <int WT, bool XP>
+__global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
     matmul_q_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                    float* __restrict__ Y, int M, int N, int K, int pdl) {
+                    const uint8_t* __restrict__ xp, float* __restrict__ Y, int M, int N, int K, int pdl) {
     if (pdl) pdl_launch_dependents();
     // used directly (not re-aligned by integer arithmetic) so that the compiler
     // keeps every access in the shared state space
@@ -300,7 +384,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (threadIdx.x == 0) atomicOr(&g_matmul_error, kErrTimeout);
         return;
     }
-    using L = Lay<WT>;
+    using L = Lay<WT, XP>;
+    using R = Roles<XP>;
+    constexpr int TMA_WARP = R::TMA_WARP, MMA_WARP = R::MMA_WARP;
     if (!QMM_IN_BOUNDS(g_matmul_error, L::SMEM_BYTES - 1, dynamic_smem_bytes())) return;  // the layout must fit
     constexpr int SC_SLOTS = L::SC_SLOTS, W_RAW = L::W_RAW, RAW_BYTES = L::RAW_BYTES, WB = L::WB;
     const Bars bars{sbase + L::OFF_BAR};
@@ -319,9 +405,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < RAW_STAGES; i++) {
             mbar_init(bars.raw_full(i), 1);
-            mbar_init(bars.raw_empty(i), NUM_CONV_WARPS);
+            mbar_init(bars.raw_empty(i), R::CONV_WARPS);
+            mbar_init(bars.x_full(i), 1);
+            mbar_init(bars.x_empty(i), 1 + NUM_W_WARPS);  // the chunk's last MMA commit, the scale copies
         }
-        for (int i = 0; i < OP_SLOTS; i++) mbar_init(bars.op_full(i), NUM_CONV_WARPS);
+        for (int i = 0; i < OP_SLOTS; i++) mbar_init(bars.op_full(i), R::CONV_WARPS);
         for (int i = 0; i < DONE_RING; i++) mbar_init(bars.mma_done(i), 1);
         for (int i = 0; i < S_BUFS; i++) mbar_init(bars.acc_empty(i), NUM_EPI_WARPS);
         *abort_flag = 0;
@@ -349,7 +437,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t dst = sbase + L::OFF_RAW + s * RAW_BYTES;
                 mbar_arrive_expect_tx(bars.raw_full(s), RAW_BYTES);
                 tma_load_2d(dst, &wmap, c * (KB * WB / 2), o0, bars.raw_full(s));
-                tma_load_2d(dst + W_RAW, &xmap, c * (KB * 34 / 2), t0, bars.raw_full(s));
+                if constexpr (XP) {
+                    if (c >= RAW_STAGES && !wait_or_abort(bars.x_empty(s), ((c / RAW_STAGES) - 1) & 1, abort_flag))
+                        break;
+                    // every CTA of this token tile reads the same chunk: no eviction hint
+                    mbar_arrive_expect_tx(bars.x_full(s), (uint32_t)L::XPS);
+                    bulk_g2s_nohint(sbase + L::OFF_XP + (uint32_t)(s * L::XPS),
+                                    xp + ((size_t)blockIdx.y * nchunks + c) * L::XPS, (uint32_t)L::XPS, bars.x_full(s));
+                } else {
+                    tma_load_2d(dst + W_RAW, &xmap, c * (KB * 34 / 2), t0, bars.raw_full(s));
+                }
             }
         }
     } else if (warp == MMA_WARP) {
@@ -362,15 +459,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             int sb = 0, s_phase = 0;
             for (int b = 0; b < nb; b++) {
                 const int os = b & (OP_SLOTS - 1);
+                const int xs = (b / KB) % RAW_STAGES, kb = b % KB;  // XP: the chunk's stage, the block in it
+                if (XP && kb == 0 && !wait_or_abort(bars.x_full(xs), (b / KB / RAW_STAGES) & 1, abort_flag)) break;
                 if (!wait_or_abort(bars.op_full(os), (b / OP_SLOTS) & 1, abort_flag)) break;
                 if (b >= S_BUFS && !wait_or_abort(bars.acc_empty(sb), s_phase ^ 1, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t a = tmem + (uint32_t)(A_COL0 + os * 16);
-                const uint64_t bd = b0 + (uint64_t)(os * (OP_B >> 4));
+                const uint64_t bd =
+                    XP ? smem_desc(sbase + L::OFF_XP + (uint32_t)(xs * L::XPS + kb * OP_B), 128, 512)
+                       : b0 + (uint64_t)(os * (OP_B >> 4));
                 const uint32_t d = tmem + (uint32_t)(sb * BN);
                 mma_f16_ts(d, a, bd, idesc, 0);                       // K 0..15: columns 0-7, core matrices 0, 1
                 mma_f16_ts(d, a + 8, bd + (256 >> 4), idesc, 1);      // K 16..31: columns 8-15, core matrices 2, 3
                 mma_commit(bars.mma_done(b));
+                if (XP && kb == KB - 1) mma_commit(bars.x_empty(xs));  // the chunk's operands are read
                 if (++sb == S_BUFS) {  // the next round of accumulators: wait for the previous round's release
                     sb = 0;
                     s_phase ^= 1;
@@ -379,10 +481,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp >= W0 && warp < X0) {
         // ------------------------------------------------------------ weight converters
-        convert_loop<WT, true>(smem, sbase, bars, tmem, (warp & 3) * 32 + lane, nchunks, abort_flag);
-    } else if (warp >= X0 && warp < TMA_WARP) {
+        convert_loop<WT, true, XP>(smem, sbase, bars, tmem, (warp & 3) * 32 + lane, nchunks, abort_flag);
+    } else if (!XP && warp >= X0 && warp < TMA_WARP) {
         // ------------------------------------------------------------ activation converters
-        convert_loop<WT, false>(smem, sbase, bars, tmem, (warp - X0) * 32 + lane, nchunks, abort_flag);
+        convert_loop<WT, false, XP>(smem, sbase, bars, tmem, (warp - X0) * 32 + lane, nchunks, abort_flag);
     } else {
         // ------------------------------------------------------------ epilogue (warps 0-15)
         const int quad = warp & 3;        // TMEM lane quadrant this warp may access
@@ -522,10 +624,53 @@ bool make_row_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64
 // enough tokens to fill a tile reasonably; other shapes run one matvec per token.
 static bool tensor_core_shape(int64_t M, int64_t K) { return K % 256 == 0 && M >= 8; }
 
+// One launch of the tensor-core kernel; XP: the activation operands were prepared
+// into xp by q8_0_xprep_kernel (xq is then not read).
+template <int WT, bool XP>
+static qmm_status matmul_q_kernel_launch(const void* W, const void* xq, const uint8_t* xp, float* Y, int64_t M,
+                                         int64_t N, int64_t K, cudaStream_t stream, bool pdl) {
+    using L = mm::Lay<WT, XP>;
+    CUtensorMap wmap, xmap;
+    if (!make_row_map(&wmap, W, row_bytes_of(WT, K), (uint64_t)N, mm::KB * L::WB, 2)) return QMM_E_CUDA;
+    if (XP) {
+        xmap = CUtensorMap{};  // not read
+    } else if (!make_row_map(&xmap, xq, row_bytes_of(QMM_Q8_0, K), (uint64_t)M, mm::KB * 34, 2)) {
+        return QMM_E_CUDA;
+    }
+    static PerDeviceOnce attr_once;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_E_CUDA;
+    const qmm_status ast = attr_once.run(dev, [] {
+        return cudaFuncSetAttribute(mm::matmul_q_kernel<WT, XP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    L::SMEM_BYTES) == cudaSuccess
+                   ? QMM_OK
+                   : QMM_E_CUDA;
+    });
+    if (ast != QMM_OK) return ast;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + mm::BN - 1) / mm::BN));
+    cfg.blockDim = dim3(mm::Roles<XP>::THREADS);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, mm::matmul_q_kernel<WT, XP>, wmap, xmap, xp, Y, (int)M, (int)N, (int)K, pdl ? 1 : 0);
+    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+}
+
+// Q4_1 and Q5_1 convert the activation once, in a pre-pass, into a stream-ordered
+// workspace (cudaMallocAsync / cudaFreeAsync on the caller's stream: ~4.5 MB for
+// 512 tokens at K = 4096): 10-11% faster at M = 128, 512 and 2048, their
+// in-kernel conversion also summing every block's codes for the min term.  For
+// Q4_0, Q8_0 and Q5_0 the pre-pass measured 4-7% slower, and without a workspace
+// (no pool memory, or inside qmm_linear_noalloc) every CTA converts it too.
 template <int WT>
 static qmm_status matmul_q_launch(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                                   cudaStream_t stream, bool pdl) {
-    using L = mm::Lay<WT>;
     if (!tensor_core_shape(M, K)) {
         const size_t xrb = row_bytes_of(QMM_Q8_0, K);
         for (int64_t t = 0; t < M; t++) {
@@ -535,33 +680,35 @@ static qmm_status matmul_q_launch(const void* W, const void* xq, float* Y, int64
         return QMM_OK;
     }
     if ((N + mm::BM - 1) / mm::BM > 0x7FFFFFFF || (M + mm::BN - 1) / mm::BN > 65535) return QMM_E_SHAPE;
-    CUtensorMap wmap, xmap;
-    if (!make_row_map(&wmap, W, row_bytes_of(WT, K), (uint64_t)N, mm::KB * L::WB, 2) ||
-        !make_row_map(&xmap, xq, row_bytes_of(QMM_Q8_0, K), (uint64_t)M, mm::KB * 34, 2))
-        return QMM_E_CUDA;
-    static PerDeviceOnce attr_once;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_E_CUDA;
-    const qmm_status ast = attr_once.run(dev, [] {
-        return cudaFuncSetAttribute(mm::matmul_q_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    L::SMEM_BYTES) == cudaSuccess
-                   ? QMM_OK
-                   : QMM_E_CUDA;
-    });
-    if (ast != QMM_OK) return ast;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + mm::BM - 1) / mm::BM), (unsigned)((M + mm::BN - 1) / mm::BN));
-    cfg.blockDim = dim3(mm::THREADS);
-    cfg.dynamicSmemBytes = L::SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, mm::matmul_q_kernel<WT>, wmap, xmap, Y, (int)M, (int)N, (int)K, pdl ? 1 : 0);
-    return e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+    if (mm::Lay<WT>::HAS_MIN && !tl_no_workspace_alloc) {
+        using LX = mm::Lay<WT, true>;
+        const int64_t ntt = (M + mm::BN - 1) / mm::BN, nchunks = K / 32 / mm::KB;
+        const size_t bytes = (size_t)(ntt * nchunks) * LX::XPS;
+        void* buf = nullptr;
+        if (cudaMallocAsync(&buf, bytes, stream) == cudaSuccess) {
+            uint8_t* xp = static_cast<uint8_t*>(buf);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(nchunks * mm::KB), (unsigned)ntt);
+            cfg.blockDim = dim3(mm::BN);
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = pdl ? 1 : 0;
+            const cudaError_t e =
+                LX::HAS_MIN ? cudaLaunchKernelEx(&cfg, mm::q8_0_xprep_kernel<true>, (const uint8_t*)xq, xp, (int)M,
+                                                 (int)nchunks, (int)LX::XPS, pdl ? 1 : 0)
+                            : cudaLaunchKernelEx(&cfg, mm::q8_0_xprep_kernel<false>, (const uint8_t*)xq, xp, (int)M,
+                                                 (int)nchunks, (int)LX::XPS, pdl ? 1 : 0);
+            qmm_status st = e == cudaSuccess ? QMM_OK : QMM_E_CUDA;
+            if (st == QMM_OK) st = matmul_q_kernel_launch<WT, true>(W, xq, xp, Y, M, N, K, stream, true);
+            if (cudaFreeAsync(buf, stream) != cudaSuccess && st == QMM_OK) st = QMM_E_CUDA;
+            return st;
+        }
+        (void)cudaGetLastError();  // no workspace: convert in the kernel
+    }
+    return matmul_q_kernel_launch<WT, false>(W, xq, nullptr, Y, M, N, K, stream, pdl);
 }
 
 // Whether an M-token multiply of this weight type takes a tensor-core prefill
