@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(BN) q8_0_xprep_kernel(const uint8_t* __restric
     const int r = threadIdx.x, b = blockIdx.x, ty = blockIdx.y;
     const int c = b / KB, kb = b % KB;
     const int t = ty * BN + r;
-    const bool real = t < M;
+    const bool real = t < M && QMM_IN_BOUNDS(g_matmul_error, t, M);
     uint8_t* out = xp + ((size_t)ty * nchunks + c) * chunk_bytes;
     const uint32_t m128 = 0x64806480u;  // (1152, 1152): 1024 + (a + 128) - 1152 = a
     {
@@ -439,6 +439,9 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                 tma_load_2d(dst, &wmap, c * (KB * WB / 2), o0, bars.raw_full(s));
                 if constexpr (XP) {
                     if (c >= RAW_STAGES && !wait_or_abort(bars.x_empty(s), ((c / RAW_STAGES) - 1) & 1, abort_flag))
+                        break;
+                    // the prepared chunks are gridDim.y token tiles x nchunks
+                    if (!QMM_IN_BOUNDS(g_matmul_error, (int64_t)blockIdx.y * nchunks + c, (int64_t)gridDim.y * nchunks))
                         break;
                     // every CTA of this token tile reads the same chunk: no eviction hint
                     mbar_arrive_expect_tx(bars.x_full(s), (uint32_t)L::XPS);

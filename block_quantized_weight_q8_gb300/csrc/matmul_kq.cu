@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(BN) kq_xprep_kernel(const uint8_t* __restrict_
     const int t = ty * BN + r;
     const size_t unit = (size_t)ty * nsb + sb;
     uint8_t* out = xp + unit * XP_BYTES;
-    const bool real = t < M;
+    const bool real = t < M && QMM_IN_BOUNDS(g_matmul_kq_error, t, M);
     const uint32_t* row = reinterpret_cast<const uint32_t*>(xq + ((size_t)(real ? t : 0) * nsb + sb) * 292);
 #pragma unroll 2
     for (int j = 0; j < 8; j++) {  // block j: code words 1 + 8j .. 8 + 8j
@@ -562,6 +562,8 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
             const uint8_t* src = xp + (size_t)blockIdx.y * nsb * XP_BYTES;
             for (int sb = 0; sb < nsb; sb++) {
                 const int s = sb & 1;
+                // the prepared units are gridDim.y token tiles x nsb super-blocks
+                if (!QMM_IN_BOUNDS(g_matmul_kq_error, (int64_t)blockIdx.y * nsb + sb, (int64_t)gridDim.y * nsb)) break;
                 if (sb >= 2 && !wait_or_abort(bars.x_empty(s), ((sb >> 1) - 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(bars.raw_full(1, s), (uint32_t)XP_BYTES);
                 // every CTA of this token tile reads the same bytes: no eviction hint
