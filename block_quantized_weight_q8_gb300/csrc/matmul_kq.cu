@@ -34,6 +34,11 @@
 //             the UMMA K-major core-matrix layout, plus the min operands and scales
 //   warps 9-24 epilogue: per super-block tcgen05.ld of both sums, the fp32 fold,
 //             and at the end the token-major store
+// With the activation pre-pass (Q4_K, Q2_K, Q5_K given a workspace; see
+// kq_xprep_kernel) the activation converters give way to one warp that
+// bulk-copies the prepared operands, and each weight row gets two threads:
+// warps 1-4 convert blocks 0-3 of every super-block, warps 5-8 blocks 4-7;
+// warp 9 copies; warps 10-25 are the epilogue.
 // Shapes: K a multiple of 2048 (so that every row of W and of the activation is
 // a whole number of 16-byte chunks, as a TMA row pitch must be) and M >= 8;
 // others run one matvec per token.
@@ -63,10 +68,13 @@ constexpr int CONV0 = 1;  // first weight-converter warp
 // the operands a pre-pass kernel prepared (XP true, see kq_xprep_kernel).
 template <bool XP>
 struct Roles {
+    // XP: two threads per weight row (8 warps), each half of them converting 4 of a
+    // super-block's 8 blocks
+    static constexpr int W_WARPS = XP ? 2 * NUM_W_WARPS : NUM_W_WARPS;
     static constexpr int X_WARPS = XP ? 1 : 4;
-    static constexpr int X0 = CONV0 + NUM_W_WARPS;        // first activation warp
+    static constexpr int X0 = CONV0 + W_WARPS;            // first activation warp
     static constexpr int EPI0 = X0 + X_WARPS;             // first epilogue warp
-    static constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 800, or 704 with the pre-pass
+    static constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 800, or 832 with the pre-pass
     static constexpr int OP_FULL_WARPS = XP ? NUM_W_WARPS : NUM_W_WARPS + 4;  // arrivals per operand slot
 };
 // A super-block of prepared activation operands, as the pre-pass writes it and
@@ -575,7 +583,9 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
         // ------------------------------------------------------------ converters
         const bool is_w = XP || warp < R::X0;
         const int role = is_w ? 0 : 1;
-        const int r = (warp - (is_w ? CONV0 : R::X0)) * 32 + lane;  // row or token
+        const int half = XP ? (warp - CONV0) / NUM_W_WARPS : 0;  // XP: blocks 4*half .. 4*half + 3
+        const int r = (is_w ? (warp - CONV0) % NUM_W_WARPS : warp - R::X0) * 32 + lane;  // row or token
+        const int j_begin = XP ? 4 * half : 0, j_end = XP ? j_begin + 4 : 8;
         if (!is_w && pdl) pdl_wait();  // the activation comes from the previous kernel
         const int BBs = is_w ? F::BB : 292;
         const int pitch = is_w ? F::RAWW : RAWX;  // the box's row pitch in shared memory
@@ -591,7 +601,7 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
             if (is_w) tma_load_2d(dst, &wmap, x, o0, bar);
             else tma_load_2d(dst, &xmap, x, t0, bar);
         };
-        if (r == 0) {
+        if (r == 0 && half == 0) {
             load(0);
             if (nsb > 1) load(1);
         }
@@ -600,7 +610,8 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
             const Raw raw{smem + L::OFF_RAW + (sb & 1) * L::RAW_STAGE + raw_role + r * pitch};
             const int off = (int)(((uint64_t)sb * BBs) & 15u);
             const int ss = sb % SC_SLOTS, as = sb & 1;
-            if (ok && sb >= SC_SLOTS && !wait_or_abort(bars.sc_empty(ss), ((sb / SC_SLOTS) - 1) & 1, abort_flag))
+            if (ok && half == 0 && sb >= SC_SLOTS &&
+                !wait_or_abort(bars.sc_empty(ss), ((sb / SC_SLOTS) - 1) & 1, abort_flag))
                 ok = false;
             if (ok) {
                 Hdr h;
@@ -627,8 +638,10 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                         default: hdr_q6_K<14>(raw, h); break;
                         }
                     }
-                    scd[ss * BM + r] = h2f(h.d_bits);
-                    scc[ss * BM + r] = h2f(h.c_bits);
+                    if (half == 0) {
+                        scd[ss * BM + r] = h2f(h.d_bits);
+                        scc[ss * BM + r] = h2f(h.c_bits);
+                    }
                 } else {
                     switch (off) {
                     case 0: hdr_x<0>(raw, &xd, bs); break;
@@ -641,7 +654,7 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                 // blocks in groups of G: all of a group's loads are issued before its
                 // stores, so the group's decode chains overlap
                 constexpr int G = F::GROUP;
-                for (int jg = 0; jg < 8; jg += G) {
+                for (int jg = j_begin; jg < j_end; jg += G) {
                     int osl[G];
 #pragma unroll
                     for (int u = 0; u < G; u++) {
@@ -741,11 +754,13 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                 }
             }
             // Every thread of the role has read this stage: one of them refills it.  The
-            // barrier also makes the decision to stop the same on all 128 threads, so none
-            // is left waiting at a later barrier.
+            // barrier also makes the decision to stop the same on all of the role's threads
+            // (128, or 256 weight threads with the pre-pass), so none is left waiting at a
+            // later barrier.
             const bool stop = !ok || *abort_flag;
-            if (is_w ? named_bar_any<1, 128>(stop) : named_bar_any<2, 128>(stop)) break;
-            if (r == 0 && sb + 2 < nsb) load(sb + 2);
+            if (is_w ? (XP ? named_bar_any<1, 256>(stop) : named_bar_any<1, 128>(stop)) : named_bar_any<2, 128>(stop))
+                break;
+            if (r == 0 && half == 0 && sb + 2 < nsb) load(sb + 2);
         }
     } else {
         // ------------------------------------------------------------ epilogue
