@@ -130,8 +130,10 @@ template <int WT>
 struct Bars {
     static constexpr int S = Fmt<WT>::OP_SLOTS;
     uint32_t base;
+    // Operand slots are handed over in groups of Fmt::GROUP blocks (the blocks a
+    // converter writes together): group g of the S / GROUP groups uses barrier g.
     __device__ uint32_t op_full(int i) const { return base + 8u * i; }
-    __device__ uint32_t op_empty(int i) const { return base + 8u * (S + i); }  // MMA of the slot's block done
+    __device__ uint32_t op_empty(int i) const { return base + 8u * (S + i); }  // MMAs of the group's blocks done
     __device__ uint32_t acc_full(int i) const { return base + 8u * (2 * S + i); }
     __device__ uint32_t acc_empty(int i) const { return base + 8u * (2 * S + 2 + i); }
     __device__ uint32_t sc_empty(int i) const { return base + 8u * (2 * S + 4 + i); }
@@ -539,9 +541,14 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                 const uint32_t xs = sbase + L::OFF_XP + (uint32_t)((sb & 1) * XP_BYTES);
                 const uint32_t dv = tmem + (uint32_t)(as * 128), dm = tmem + (uint32_t)(256 + as * 128);
                 bool ok = true;
+                constexpr int G = F::GROUP, NG = S / G;  // blocks handed over together, groups of slots
                 for (int j = 0; j < 8; j++) {
                     const int b = sb * 8 + j, os = b % S;
-                    if (!wait_or_abort(bars.op_full(os), (b / S) & 1, abort_flag)) { ok = false; break; }
+                    const int gi = b / G, gs = gi % NG;  // the block's group and its barrier
+                    if (b % G == 0 && !wait_or_abort(bars.op_full(gs), (gi / NG) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint64_t so = (uint64_t)(os * (OP_BYTES >> 4));
                     const uint64_t bj = XP ? smem_desc(xs + (uint32_t)(j * XP_BLOCK), 128, 512) : b0 + so;
@@ -556,7 +563,7 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                         const uint64_t mb = XP ? smem_desc(xs + (uint32_t)(8 * XP_BLOCK), 128, 256) : mb0 + mo;
                         mma_f16(dm, ma0 + mo, mb, idesc, 0u);
                     }
-                    mma_commit(bars.op_empty(os));
+                    if (b % G == G - 1) mma_commit(bars.op_empty(gs));  // the group's slots may be refilled
                     if (j == 7) mma_commit(bars.acc_full(as));
                     if (XP && j == 7) mma_commit(bars.x_empty(sb & 1));  // the stage may be refilled
                 }
@@ -657,11 +664,11 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                 for (int jg = j_begin; jg < j_end; jg += G) {
                     int osl[G];
 #pragma unroll
-                    for (int u = 0; u < G; u++) {
-                        const int b = sb * 8 + jg + u;
-                        osl[u] = b % S;
-                        if (b >= S && !wait_or_abort(bars.op_empty(osl[u]), ((b / S) - 1) & 1, abort_flag)) ok = false;
-                    }
+                    for (int u = 0; u < G; u++) osl[u] = (sb * 8 + jg + u) % S;
+                    // the group's slots, one barrier for all of them (last used NG groups ago)
+                    const int gi = (sb * 8 + jg) / G, gs = gi % (S / G);
+                    if (gi >= S / G && !wait_or_abort(bars.op_empty(gs), ((gi / (S / G)) - 1) & 1, abort_flag))
+                        ok = false;
                     if (!ok) break;
                     if (is_w) {
                         if constexpr (WT == QMM_Q6_K) {
@@ -747,10 +754,7 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                     }
                     fence_proxy_async_smem();  // the operands are read by the tensor core (async proxy)
                     __syncwarp();
-                    if (lane == 0) {
-#pragma unroll
-                        for (int u = 0; u < G; u++) mbar_arrive(bars.op_full(osl[u]));
-                    }
+                    if (lane == 0) mbar_arrive(bars.op_full(gi % (S / G)));
                 }
             }
             // Every thread of the role has read this stage: one of them refills it.  The
