@@ -68,8 +68,8 @@ constexpr int CONV0 = 1;  // first weight-converter warp
 // the operands a pre-pass kernel prepared (XP true, see kq_xprep_kernel).
 template <bool XP>
 struct Roles {
-    // XP: two threads per weight row (8 warps), each half of them converting 4 of a
-    // super-block's 8 blocks
+    // XP: two threads per weight row (8 warps); half h of them converts the groups of
+    // blocks of parity h (see the converters)
     static constexpr int W_WARPS = XP ? 2 * NUM_W_WARPS : NUM_W_WARPS;
     static constexpr int X_WARPS = XP ? 1 : 4;
     static constexpr int X0 = CONV0 + W_WARPS;            // first activation warp
@@ -590,9 +590,17 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
         // ------------------------------------------------------------ converters
         const bool is_w = XP || warp < R::X0;
         const int role = is_w ? 0 : 1;
-        const int half = XP ? (warp - CONV0) / NUM_W_WARPS : 0;  // XP: blocks 4*half .. 4*half + 3
+        // XP: half h converts every other group of blocks, those with gi % 2 == h.  Group
+        // gi fills slots and hands over on barrier gi % NG (NG = S / G, even), so each
+        // barrier is used by one half only and every one of its phases is waited on by
+        // that half, in order.  A parity wait is only right while the barrier is at most
+        // one phase away from it; a barrier shared by the halves, each waiting only on its
+        // own phases, could be two phases on and alias.
+        static_assert(!XP || ((S / F::GROUP) % 2 == 0 && 8 % (2 * F::GROUP) == 0),
+                      "with the pre-pass each operand barrier belongs to one converter half");
+        const int half = XP ? (warp - CONV0) / NUM_W_WARPS : 0;
         const int r = (is_w ? (warp - CONV0) % NUM_W_WARPS : warp - R::X0) * 32 + lane;  // row or token
-        const int j_begin = XP ? 4 * half : 0, j_end = XP ? j_begin + 4 : 8;
+        const int j_begin = XP ? F::GROUP * half : 0, j_step = XP ? 2 * F::GROUP : F::GROUP;
         if (!is_w && pdl) pdl_wait();  // the activation comes from the previous kernel
         const int BBs = is_w ? F::BB : 292;
         const int pitch = is_w ? F::RAWW : RAWX;  // the box's row pitch in shared memory
@@ -661,7 +669,7 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                 // blocks in groups of G: all of a group's loads are issued before its
                 // stores, so the group's decode chains overlap
                 constexpr int G = F::GROUP;
-                for (int jg = j_begin; jg < j_end; jg += G) {
+                for (int jg = j_begin; jg < 8; jg += j_step) {
                     int osl[G];
 #pragma unroll
                     for (int u = 0; u < G; u++) osl[u] = (sb * 8 + jg + u) % S;
