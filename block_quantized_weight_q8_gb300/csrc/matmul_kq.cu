@@ -34,11 +34,11 @@
 //             the UMMA K-major core-matrix layout, plus the min operands and scales
 //   warps 9-24 epilogue: per super-block tcgen05.ld of both sums, the fp32 fold,
 //             and at the end the token-major store
-// With the activation pre-pass (Q4_K, Q2_K, Q5_K given a workspace; see
+// With the activation pre-pass (every format, given a workspace; see
 // kq_xprep_kernel) the activation converters give way to one warp that
 // bulk-copies the prepared operands, and each weight row gets two threads:
-// warps 1-4 convert blocks 0-3 of every super-block, warps 5-8 blocks 4-7;
-// warp 9 copies; warps 10-25 are the epilogue.
+// warps 1-4 convert the even groups of blocks of every super-block, warps 5-8
+// the odd ones; warp 9 copies; warps 10-25 are the epilogue.
 // Shapes: K a multiple of 2048 (so that every row of W and of the activation is
 // a whole number of 16-byte chunks, as a TMA row pitch must be) and M >= 8;
 // others run one matvec per token.
@@ -93,6 +93,22 @@ template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, RAWW = 224, SP
 template <> struct Fmt<QMM_Q5_K> { static constexpr int BB = 176, RAWW = 176, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
 
 constexpr int XP_BYTES = 8 * XP_BLOCK + MIN_BYTES;  // 69632
+// The kernel takes a super-block's prepared operands in 8 / SPAN bulk copies of
+// SPAN blocks (the last one with the min operand) through a ring of two stages of
+// BYTES.  Q6_K, whose two weight operands need more slot space, takes half
+// super-blocks; the others whole ones, a full super-block ahead of the MMAs.
+template <int WT>
+struct XStage {
+    static constexpr int SPAN = WT == QMM_Q6_K ? 4 : 8;
+    static constexpr int COPIES = 8 / SPAN;  // per super-block
+    static constexpr int BYTES = SPAN * XP_BLOCK + MIN_BYTES;
+};
+// operand slots in flight: with the pre-pass Q6_K keeps 4 (an even number of
+// handover barriers: see the converters)
+template <int WT, bool XP>
+struct Slots {
+    static constexpr int S = (WT == QMM_Q6_K && XP) ? 4 : Fmt<WT>::OP_SLOTS;
+};
 
 template <int WT, bool XP = false>
 struct Layout {
@@ -100,11 +116,12 @@ struct Layout {
     static constexpr int NCW = F::RAWW / 16;
     static constexpr int RAW_STAGE = BM * F::RAWW + (XP ? 0 : BN * RAWX);
     static constexpr int OFF_RAW = 0;                                          // 2 stages
-    static constexpr int OFF_XP = OFF_RAW + 2 * RAW_STAGE;                     // XP: 2 stages of XP_BYTES
-    static constexpr int OFF_OPA = OFF_XP + (XP ? 2 * XP_BYTES : 0);           // A (Q6_K: sc*(q&7))
-    static constexpr int OFF_OPH = OFF_OPA + F::OP_SLOTS * OP_BYTES;           // Q6_K: 8*sc*(q>>3)
-    static constexpr int OFF_OPB = OFF_OPH + F::SPLIT * F::OP_SLOTS * OP_BYTES;  // activation codes
-    static constexpr int OFF_MINA = OFF_OPB + (XP ? 0 : F::OP_SLOTS * OP_BYTES);  // 2 slots of f_g
+    static constexpr int S = Slots<WT, XP>::S;
+    static constexpr int OFF_XP = OFF_RAW + 2 * RAW_STAGE;                     // XP: 2 stages of XStage::BYTES
+    static constexpr int OFF_OPA = OFF_XP + (XP ? 2 * XStage<WT>::BYTES : 0);  // A (Q6_K: sc*(q&7))
+    static constexpr int OFF_OPH = OFF_OPA + S * OP_BYTES;                     // Q6_K: 8*sc*(q>>3)
+    static constexpr int OFF_OPB = OFF_OPH + F::SPLIT * S * OP_BYTES;          // activation codes
+    static constexpr int OFF_MINA = OFF_OPB + (XP ? 0 : S * OP_BYTES);         // 2 slots of f_g
     static constexpr int OFF_MINB = OFF_MINA + 2 * MIN_BYTES;                  // 2 slots of bsum_g
     static constexpr int OFF_SCD = OFF_MINB + (XP ? 0 : 2 * MIN_BYTES);        // d_w per row
     static constexpr int OFF_SCC = OFF_SCD + SC_SLOTS * BM * 4;                // c_w per row
@@ -112,7 +129,7 @@ struct Layout {
     static constexpr int OFF_BAR = OFF_SCX + (XP ? 0 : SC_SLOTS * BN * 4);
     // op_full[S] mma_done[S] acc_full[2] acc_empty[2] sc_empty[SC_SLOTS] raw_full[2 roles][2 stages]
     // x_empty[2] (XP: the MMAs of a prepared stage are done)
-    static constexpr int NBARS = 2 * F::OP_SLOTS + 4 + SC_SLOTS + 4 + 2;
+    static constexpr int NBARS = 2 * S + 4 + SC_SLOTS + 4 + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
 };
@@ -120,15 +137,16 @@ static_assert(Layout<QMM_Q6_K>::SMEM <= 232448, "Q6_K layout exceeds shared memo
 static_assert(Layout<QMM_Q4_K>::SMEM <= 232448, "Q4_K layout exceeds shared memory");
 static_assert(Layout<QMM_Q5_K>::SMEM <= 232448, "Q5_K layout exceeds shared memory");
 static_assert(Layout<QMM_Q4_K, true>::SMEM <= 232448 && Layout<QMM_Q2_K, true>::SMEM <= 232448 &&
-                  Layout<QMM_Q5_K, true>::SMEM <= 232448,
+                  Layout<QMM_Q5_K, true>::SMEM <= 232448 && Layout<QMM_Q6_K, true>::SMEM <= 232448,
               "pre-pass layout exceeds shared memory");
 static_assert(Layout<QMM_Q4_K, true>::OFF_OPA % 128 == 0 && Layout<QMM_Q2_K, true>::OFF_OPA % 128 == 0 &&
-                  Layout<QMM_Q5_K, true>::OFF_OPA % 128 == 0 && XP_BYTES % 128 == 0,
+                  Layout<QMM_Q5_K, true>::OFF_OPA % 128 == 0 && Layout<QMM_Q6_K, true>::OFF_OPA % 128 == 0 &&
+                  XStage<QMM_Q6_K>::BYTES % 128 == 0 && XP_BYTES % 128 == 0,
               "operand tiles need 128-byte alignment");
 
-template <int WT>
+template <int WT, bool XP>
 struct Bars {
-    static constexpr int S = Fmt<WT>::OP_SLOTS;
+    static constexpr int S = Slots<WT, XP>::S;
     uint32_t base;
     // Operand slots are handed over in groups of Fmt::GROUP blocks (the blocks a
     // converter writes together): group g of the S / GROUP groups uses barrier g.
@@ -479,7 +497,7 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
     using F = Fmt<WT>;
     using L = Layout<WT, XP>;
     using R = Roles<XP>;
-    constexpr int S = F::OP_SLOTS;
+    constexpr int S = Slots<WT, XP>::S;
     if (pdl) pdl_launch_dependents();
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -487,7 +505,7 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
         if (threadIdx.x == 0) atomicOr(&g_matmul_kq_error, kErrTimeout);
         return;
     }
-    const Bars<WT> bars{sbase + L::OFF_BAR};
+    const Bars<WT, XP> bars{sbase + L::OFF_BAR};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_TMEM + 8);
     float* scd = reinterpret_cast<float*>(smem + L::OFF_SCD);
@@ -536,36 +554,44 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
             for (int sb = 0; sb < nsb; sb++) {
                 const int as = sb & 1;
                 if (sb >= 2 && !wait_or_abort(bars.acc_empty(as), ((sb >> 1) - 1) & 1, abort_flag)) break;
-                // the prepared activation operands of this super-block (XP)
-                if (XP && !wait_or_abort(bars.raw_full(1, sb & 1), (sb >> 1) & 1, abort_flag)) break;
-                const uint32_t xs = sbase + L::OFF_XP + (uint32_t)((sb & 1) * XP_BYTES);
                 const uint32_t dv = tmem + (uint32_t)(as * 128), dm = tmem + (uint32_t)(256 + as * 128);
                 bool ok = true;
                 constexpr int G = F::GROUP, NG = S / G;  // blocks handed over together, groups of slots
+                constexpr int SPAN = XStage<WT>::SPAN;   // XP: blocks per prepared copy
+                // unrolled: the issuing thread is on the critical path (a rolled loop made the
+                // Q4_K prefill 1.4x slower)
+#pragma unroll
                 for (int j = 0; j < 8; j++) {
                     const int b = sb * 8 + j, os = b % S;
                     const int gi = b / G, gs = gi % NG;  // the block's group and its barrier
+                    // XP: copy xc of the prepared activation operands holds block j, in stage xc & 1
+                    const int xc = sb * XStage<WT>::COPIES + j / SPAN;
+                    if (XP && j % SPAN == 0 && !wait_or_abort(bars.raw_full(1, xc & 1), (xc >> 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     if (b % G == 0 && !wait_or_abort(bars.op_full(gs), (gi / NG) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    const uint32_t xs = sbase + L::OFF_XP + (uint32_t)((xc & 1) * XStage<WT>::BYTES);
                     const uint64_t so = (uint64_t)(os * (OP_BYTES >> 4));
-                    const uint64_t bj = XP ? smem_desc(xs + (uint32_t)(j * XP_BLOCK), 128, 512) : b0 + so;
+                    const uint64_t bj = XP ? smem_desc(xs + (uint32_t)((j % SPAN) * XP_BLOCK), 128, 512) : b0 + so;
                     mma_f16(dv, a0 + so, bj, idesc, j > 0 ? 1u : 0u);
                     mma_f16(dv, a0 + so + (256 >> 4), bj + (256 >> 4), idesc, 1u);
                     if (F::SPLIT) {
-                        mma_f16(dv, h0 + so, b0 + so, idesc, 1u);
-                        mma_f16(dv, h0 + so + (256 >> 4), b0 + so + (256 >> 4), idesc, 1u);
+                        mma_f16(dv, h0 + so, bj, idesc, 1u);
+                        mma_f16(dv, h0 + so + (256 >> 4), bj + (256 >> 4), idesc, 1u);
                     }
                     if (j == 7) {
                         const uint64_t mo = (uint64_t)(as * (MIN_BYTES >> 4));
-                        const uint64_t mb = XP ? smem_desc(xs + (uint32_t)(8 * XP_BLOCK), 128, 256) : mb0 + mo;
+                        const uint64_t mb = XP ? smem_desc(xs + (uint32_t)(SPAN * XP_BLOCK), 128, 256) : mb0 + mo;
                         mma_f16(dm, ma0 + mo, mb, idesc, 0u);
                     }
                     if (b % G == G - 1) mma_commit(bars.op_empty(gs));  // the group's slots may be refilled
                     if (j == 7) mma_commit(bars.acc_full(as));
-                    if (XP && j == 7) mma_commit(bars.x_empty(sb & 1));  // the stage may be refilled
+                    if (XP && j % SPAN == SPAN - 1) mma_commit(bars.x_empty(xc & 1));  // the stage may be refilled
                 }
                 if (!ok) break;
             }
@@ -575,15 +601,19 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
         if (lane == 0) {
             if (pdl) pdl_wait();  // the pre-pass kernel wrote them
             const uint8_t* src = xp + (size_t)blockIdx.y * nsb * XP_BYTES;
-            for (int sb = 0; sb < nsb; sb++) {
-                const int s = sb & 1;
+            constexpr int SPAN = XStage<WT>::SPAN, COPIES = XStage<WT>::COPIES;
+            for (int xc = 0; xc < nsb * COPIES; xc++) {
+                // copy xc: part xc % COPIES of super-block xc / COPIES, into stage xc & 1
+                const int sb = xc / COPIES, part = xc % COPIES, s = xc & 1;
                 // the prepared units are gridDim.y token tiles x nsb super-blocks
                 if (!QMM_IN_BOUNDS(g_matmul_kq_error, (int64_t)blockIdx.y * nsb + sb, (int64_t)gridDim.y * nsb)) break;
-                if (sb >= 2 && !wait_or_abort(bars.x_empty(s), ((sb >> 1) - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(bars.raw_full(1, s), (uint32_t)XP_BYTES);
+                if (xc >= 2 && !wait_or_abort(bars.x_empty(s), ((xc >> 1) - 1) & 1, abort_flag)) break;
+                // SPAN blocks of codes, and after the last of them the min operand
+                const uint32_t bytes = (uint32_t)(SPAN * XP_BLOCK + (part == COPIES - 1 ? MIN_BYTES : 0));
+                mbar_arrive_expect_tx(bars.raw_full(1, s), bytes);
                 // every CTA of this token tile reads the same bytes: no eviction hint
-                bulk_g2s_nohint(sbase + L::OFF_XP + (uint32_t)(s * XP_BYTES), src + (size_t)sb * XP_BYTES,
-                                (uint32_t)XP_BYTES, bars.raw_full(1, s));
+                bulk_g2s_nohint(sbase + L::OFF_XP + (uint32_t)(s * XStage<WT>::BYTES),
+                                src + (size_t)sb * XP_BYTES + (size_t)part * SPAN * XP_BLOCK, bytes, bars.raw_full(1, s));
             }
         }
     } else if (warp < R::EPI0) {
@@ -902,42 +932,39 @@ static qmm_status launch_kq_kernel(const void* W, const void* xq, const uint8_t*
 // allocation, so the prefill converts the activation in the kernel itself.
 thread_local bool tl_no_workspace_alloc = false;
 
-// Q4_K, Q2_K and Q5_K convert the activation once, in a pre-pass, into a
-// stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on the caller's
-// stream: ~4.4 MB for 512 tokens at K = 4096); without one (no pool memory, or
-// inside qmm_linear_noalloc) every CTA converts it (Q6_K always: its second
-// weight operand leaves no room for the prepared stages).
+// The activation is converted once, in a pre-pass, into a stream-ordered
+// workspace (cudaMallocAsync / cudaFreeAsync on the caller's stream: ~4.4 MB for
+// 512 tokens at K = 4096); without one (no pool memory, or inside
+// qmm_linear_noalloc) every CTA converts it.
 template <int WT>
 static qmm_status launch_kq(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                             cudaStream_t stream, bool pdl) {
-    if constexpr (WT != QMM_Q6_K) {
-        if (!tl_no_workspace_alloc) {
-            const int64_t ntt = (M + kq::BN - 1) / kq::BN, nsb = K / 256;
-            const size_t xp_bytes = (size_t)(ntt * nsb) * kq::XP_BYTES;
-            const size_t dx_bytes = (size_t)(ntt * nsb) * kq::BN * sizeof(float);
-            void* buf = nullptr;
-            if (ntt * nsb <= 0x7FFFFFFF && cudaMallocAsync(&buf, xp_bytes + dx_bytes, stream) == cudaSuccess) {
-                uint8_t* xp = static_cast<uint8_t*>(buf);
-                float* dxg = reinterpret_cast<float*>(xp + xp_bytes);
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3((unsigned)nsb, (unsigned)ntt);
-                cfg.blockDim = dim3(kq::BN);
-                cfg.stream = stream;
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-                attr[0].val.programmaticStreamSerializationAllowed = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = pdl ? 1 : 0;
-                qmm_status st = cudaLaunchKernelEx(&cfg, kq::kq_xprep_kernel, (const uint8_t*)xq, xp, dxg, (int)M,
-                                                   (int)nsb, pdl ? 1 : 0) == cudaSuccess
-                                    ? QMM_OK
-                                    : QMM_E_CUDA;
-                if (st == QMM_OK) st = launch_kq_kernel<WT, true>(W, xq, xp, dxg, Y, M, N, K, stream, true);
-                if (cudaFreeAsync(buf, stream) != cudaSuccess && st == QMM_OK) st = QMM_E_CUDA;
-                return st;
-            }
-            (void)cudaGetLastError();  // no workspace: convert in the kernel
+    if (!tl_no_workspace_alloc) {
+        const int64_t ntt = (M + kq::BN - 1) / kq::BN, nsb = K / 256;
+        const size_t xp_bytes = (size_t)(ntt * nsb) * kq::XP_BYTES;
+        const size_t dx_bytes = (size_t)(ntt * nsb) * kq::BN * sizeof(float);
+        void* buf = nullptr;
+        if (ntt * nsb <= 0x7FFFFFFF && cudaMallocAsync(&buf, xp_bytes + dx_bytes, stream) == cudaSuccess) {
+            uint8_t* xp = static_cast<uint8_t*>(buf);
+            float* dxg = reinterpret_cast<float*>(xp + xp_bytes);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)nsb, (unsigned)ntt);
+            cfg.blockDim = dim3(kq::BN);
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = pdl ? 1 : 0;
+            qmm_status st = cudaLaunchKernelEx(&cfg, kq::kq_xprep_kernel, (const uint8_t*)xq, xp, dxg, (int)M,
+                                               (int)nsb, pdl ? 1 : 0) == cudaSuccess
+                                ? QMM_OK
+                                : QMM_E_CUDA;
+            if (st == QMM_OK) st = launch_kq_kernel<WT, true>(W, xq, xp, dxg, Y, M, N, K, stream, true);
+            if (cudaFreeAsync(buf, stream) != cudaSuccess && st == QMM_OK) st = QMM_E_CUDA;
+            return st;
         }
+        (void)cudaGetLastError();  // no workspace: convert in the kernel
     }
     return launch_kq_kernel<WT, false>(W, xq, nullptr, nullptr, Y, M, N, K, stream, pdl);
 }

@@ -47,9 +47,9 @@ def _close(y, ref):
                                          ("q2_K", 16, 130, 2048), ("q5_K", 8, 200, 4096), ("q4_1", 8, 300, 4096),
                                          ("q5_1", 130, 77, 2048)])
 def test_noalloc_matches_linear_twice(lib, wtype, M, N, K):
-    """qmm_linear_noalloc against qmm_linear_<w>, bit for bit.  At M >= 8 the Q4_K, Q2_K, Q5_K,
-    Q4_1 and Q5_1 prefills of qmm_linear_<w> take the activation pre-pass and those of
-    qmm_linear_noalloc convert the activation in the kernel: the two paths must agree exactly."""
+    """qmm_linear_noalloc against qmm_linear_<w>, bit for bit.  At M >= 8 the K-quant (Q4_K, Q2_K,
+    Q5_K, Q6_K), Q4_1 and Q5_1 prefills of qmm_linear_<w> take the activation pre-pass and those
+    of qmm_linear_noalloc convert the activation in the kernel: the two paths must agree exactly."""
     act = "q8_0" if wtype in ("q4_0", "q8_0", "q4_1", "q5_0", "q5_1") else "q8_K"
     Wq = oracle.quantize(wtype, workloads.weights_f32(N, K, seed=31, row_jitter=True))
     W = torch.from_numpy(Wq).cuda()
