@@ -91,6 +91,17 @@ template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, RAWW = 144, SP
 template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, RAWW = 96, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
 template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, RAWW = 224, SPLIT = 1, OP_SLOTS = 3, GROUP = 1; };
 template <> struct Fmt<QMM_Q5_K> { static constexpr int BB = 176, RAWW = 176, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
+// The weight box's row pitch in shared memory: an odd number of 16-byte chunks, so
+// that the 16-byte reads of eight consecutive rows fall in eight distinct bank
+// groups (Q2_K's 96 and Q6_K's 224 bytes are 6 and 14 chunks: rows r and r + 4
+// collided).  The box is that wide (the bytes past the super-block's superset are
+// the next one's, or the zero fill past the row).  Q6_K without the pre-pass keeps
+// 224: its shared memory is full.
+template <int WT, bool XP>
+struct WPitch {
+    static constexpr int P = WT == QMM_Q2_K ? 112 : (WT == QMM_Q6_K && XP) ? 240 : Fmt<WT>::RAWW;
+    static_assert(P >= Fmt<WT>::RAWW && P % 16 == 0, "the box covers the super-block's superset");
+};
 
 constexpr int XP_BYTES = 8 * XP_BLOCK + MIN_BYTES;  // 69632
 // The kernel takes a super-block's prepared operands in 8 / SPAN bulk copies of
@@ -113,8 +124,7 @@ struct Slots {
 template <int WT, bool XP = false>
 struct Layout {
     using F = Fmt<WT>;
-    static constexpr int NCW = F::RAWW / 16;
-    static constexpr int RAW_STAGE = BM * F::RAWW + (XP ? 0 : BN * RAWX);
+    static constexpr int RAW_STAGE = BM * WPitch<WT, XP>::P + (XP ? 0 : BN * RAWX);
     static constexpr int OFF_RAW = 0;                                          // 2 stages
     static constexpr int S = Slots<WT, XP>::S;
     static constexpr int OFF_XP = OFF_RAW + 2 * RAW_STAGE;                     // XP: 2 stages of XStage::BYTES
@@ -633,8 +643,8 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
         const int j_begin = XP ? F::GROUP * half : 0, j_step = XP ? 2 * F::GROUP : F::GROUP;
         if (!is_w && pdl) pdl_wait();  // the activation comes from the previous kernel
         const int BBs = is_w ? F::BB : 292;
-        const int pitch = is_w ? F::RAWW : RAWX;  // the box's row pitch in shared memory
-        const uint32_t raw_role = is_w ? 0u : (uint32_t)(BM * F::RAWW);
+        const int pitch = is_w ? WPitch<WT, XP>::P : RAWX;  // the box's row pitch in shared memory
+        const uint32_t raw_role = is_w ? 0u : (uint32_t)(BM * WPitch<WT, XP>::P);
         // super-block sb of the role's 128 rows into stage sb & 1 (one thread of the role):
         // the box starts at the 16-byte boundary at or below the super-block's first byte
         auto load = [&](int sb) {
@@ -897,7 +907,7 @@ static qmm_status launch_kq_kernel(const void* W, const void* xq, const uint8_t*
     // one super-block's 16-byte aligned superset of 128 rows (tokens)
     const uint64_t nsb = (uint64_t)(K / 256);
     CUtensorMap wmap, xmap;
-    if (!make_row_map(&wmap, W, nsb * F::BB, (uint64_t)N, F::RAWW, 8)) return QMM_E_CUDA;
+    if (!make_row_map(&wmap, W, nsb * F::BB, (uint64_t)N, kq::WPitch<WT, XP>::P, 8)) return QMM_E_CUDA;
     if (XP) {
         xmap = CUtensorMap{};  // not read
     } else if (!make_row_map(&xmap, xq, nsb * 292, (uint64_t)M, kq::RAWX, 8)) {
