@@ -104,21 +104,19 @@ struct WPitch {
 };
 
 constexpr int XP_BYTES = 8 * XP_BLOCK + MIN_BYTES;  // 69632
-// The kernel takes a super-block's prepared operands in 8 / SPAN bulk copies of
-// SPAN blocks (the last one with the min operand) through a ring of two stages of
-// BYTES.  Q6_K, whose two weight operands need more slot space, takes half
-// super-blocks; the others whole ones, a full super-block ahead of the MMAs.
-template <int WT>
-struct XStage {
-    static constexpr int SPAN = WT == QMM_Q6_K ? 4 : 8;
-    static constexpr int COPIES = 8 / SPAN;  // per super-block
-    static constexpr int BYTES = SPAN * XP_BLOCK + MIN_BYTES;
-};
-// operand slots in flight: with the pre-pass Q6_K keeps 4 (an even number of
-// handover barriers: see the converters)
+// The kernel takes a super-block's prepared operands in two bulk copies of half
+// a super-block, XSPAN blocks each (the second also carries the min operand),
+// through a ring of two stages of XSTAGE_BYTES.  Half stages leave the shared
+// memory for more weight-operand slots (Slots).
+constexpr int XSPAN = 4, XCOPIES = 8 / XSPAN;
+constexpr int XSTAGE_BYTES = XSPAN * XP_BLOCK + MIN_BYTES;  // 36864
+// Operand slots in flight.  With the pre-pass 8 (Q6_K, with two operands per
+// slot, 4), which lets the converters run further ahead of the MMA issuer than
+// the 4 that fit beside whole-super-block stages (Q4_K 110.6 -> 103.7 us at
+// M = 512); an even number of handover barriers either way (see the converters).
 template <int WT, bool XP>
 struct Slots {
-    static constexpr int S = (WT == QMM_Q6_K && XP) ? 4 : Fmt<WT>::OP_SLOTS;
+    static constexpr int S = XP ? (WT == QMM_Q6_K ? 4 : 8) : Fmt<WT>::OP_SLOTS;
 };
 
 template <int WT, bool XP = false>
@@ -127,8 +125,8 @@ struct Layout {
     static constexpr int RAW_STAGE = BM * WPitch<WT, XP>::P + (XP ? 0 : BN * RAWX);
     static constexpr int OFF_RAW = 0;                                          // 2 stages
     static constexpr int S = Slots<WT, XP>::S;
-    static constexpr int OFF_XP = OFF_RAW + 2 * RAW_STAGE;                     // XP: 2 stages of XStage::BYTES
-    static constexpr int OFF_OPA = OFF_XP + (XP ? 2 * XStage<WT>::BYTES : 0);  // A (Q6_K: sc*(q&7))
+    static constexpr int OFF_XP = OFF_RAW + 2 * RAW_STAGE;                     // XP: 2 stages of XSTAGE_BYTES
+    static constexpr int OFF_OPA = OFF_XP + (XP ? 2 * XSTAGE_BYTES : 0);       // A (Q6_K: sc*(q&7))
     static constexpr int OFF_OPH = OFF_OPA + S * OP_BYTES;                     // Q6_K: 8*sc*(q>>3)
     static constexpr int OFF_OPB = OFF_OPH + F::SPLIT * S * OP_BYTES;          // activation codes
     static constexpr int OFF_MINA = OFF_OPB + (XP ? 0 : S * OP_BYTES);         // 2 slots of f_g
@@ -151,7 +149,7 @@ static_assert(Layout<QMM_Q4_K, true>::SMEM <= 232448 && Layout<QMM_Q2_K, true>::
               "pre-pass layout exceeds shared memory");
 static_assert(Layout<QMM_Q4_K, true>::OFF_OPA % 128 == 0 && Layout<QMM_Q2_K, true>::OFF_OPA % 128 == 0 &&
                   Layout<QMM_Q5_K, true>::OFF_OPA % 128 == 0 && Layout<QMM_Q6_K, true>::OFF_OPA % 128 == 0 &&
-                  XStage<QMM_Q6_K>::BYTES % 128 == 0 && XP_BYTES % 128 == 0,
+                  XSTAGE_BYTES % 128 == 0 && XP_BYTES % 128 == 0,
               "operand tiles need 128-byte alignment");
 
 template <int WT, bool XP>
@@ -567,7 +565,6 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                 const uint32_t dv = tmem + (uint32_t)(as * 128), dm = tmem + (uint32_t)(256 + as * 128);
                 bool ok = true;
                 constexpr int G = F::GROUP, NG = S / G;  // blocks handed over together, groups of slots
-                constexpr int SPAN = XStage<WT>::SPAN;   // XP: blocks per prepared copy
                 // unrolled: the issuing thread is on the critical path (a rolled loop made the
                 // Q4_K prefill 1.4x slower)
 #pragma unroll
@@ -575,8 +572,8 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                     const int b = sb * 8 + j, os = b % S;
                     const int gi = b / G, gs = gi % NG;  // the block's group and its barrier
                     // XP: copy xc of the prepared activation operands holds block j, in stage xc & 1
-                    const int xc = sb * XStage<WT>::COPIES + j / SPAN;
-                    if (XP && j % SPAN == 0 && !wait_or_abort(bars.raw_full(1, xc & 1), (xc >> 1) & 1, abort_flag)) {
+                    const int xc = sb * XCOPIES + j / XSPAN;
+                    if (XP && j % XSPAN == 0 && !wait_or_abort(bars.raw_full(1, xc & 1), (xc >> 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -585,9 +582,9 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t xs = sbase + L::OFF_XP + (uint32_t)((xc & 1) * XStage<WT>::BYTES);
+                    const uint32_t xs = sbase + L::OFF_XP + (uint32_t)((xc & 1) * XSTAGE_BYTES);
                     const uint64_t so = (uint64_t)(os * (OP_BYTES >> 4));
-                    const uint64_t bj = XP ? smem_desc(xs + (uint32_t)((j % SPAN) * XP_BLOCK), 128, 512) : b0 + so;
+                    const uint64_t bj = XP ? smem_desc(xs + (uint32_t)((j % XSPAN) * XP_BLOCK), 128, 512) : b0 + so;
                     mma_f16(dv, a0 + so, bj, idesc, j > 0 ? 1u : 0u);
                     mma_f16(dv, a0 + so + (256 >> 4), bj + (256 >> 4), idesc, 1u);
                     if (F::SPLIT) {
@@ -596,12 +593,12 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
                     }
                     if (j == 7) {
                         const uint64_t mo = (uint64_t)(as * (MIN_BYTES >> 4));
-                        const uint64_t mb = XP ? smem_desc(xs + (uint32_t)(SPAN * XP_BLOCK), 128, 256) : mb0 + mo;
+                        const uint64_t mb = XP ? smem_desc(xs + (uint32_t)(XSPAN * XP_BLOCK), 128, 256) : mb0 + mo;
                         mma_f16(dm, ma0 + mo, mb, idesc, 0u);
                     }
                     if (b % G == G - 1) mma_commit(bars.op_empty(gs));  // the group's slots may be refilled
                     if (j == 7) mma_commit(bars.acc_full(as));
-                    if (XP && j % SPAN == SPAN - 1) mma_commit(bars.x_empty(xc & 1));  // the stage may be refilled
+                    if (XP && j % XSPAN == XSPAN - 1) mma_commit(bars.x_empty(xc & 1));  // the stage may be refilled
                 }
                 if (!ok) break;
             }
@@ -611,19 +608,18 @@ __global__ void __launch_bounds__(Roles<XP>::THREADS, 1)
         if (lane == 0) {
             if (pdl) pdl_wait();  // the pre-pass kernel wrote them
             const uint8_t* src = xp + (size_t)blockIdx.y * nsb * XP_BYTES;
-            constexpr int SPAN = XStage<WT>::SPAN, COPIES = XStage<WT>::COPIES;
-            for (int xc = 0; xc < nsb * COPIES; xc++) {
-                // copy xc: part xc % COPIES of super-block xc / COPIES, into stage xc & 1
-                const int sb = xc / COPIES, part = xc % COPIES, s = xc & 1;
+            for (int xc = 0; xc < nsb * XCOPIES; xc++) {
+                // copy xc: part xc % XCOPIES of super-block xc / XCOPIES, into stage xc & 1
+                const int sb = xc / XCOPIES, part = xc % XCOPIES, s = xc & 1;
                 // the prepared units are gridDim.y token tiles x nsb super-blocks
                 if (!QMM_IN_BOUNDS(g_matmul_kq_error, (int64_t)blockIdx.y * nsb + sb, (int64_t)gridDim.y * nsb)) break;
                 if (xc >= 2 && !wait_or_abort(bars.x_empty(s), ((xc >> 1) - 1) & 1, abort_flag)) break;
-                // SPAN blocks of codes, and after the last of them the min operand
-                const uint32_t bytes = (uint32_t)(SPAN * XP_BLOCK + (part == COPIES - 1 ? MIN_BYTES : 0));
+                // XSPAN blocks of codes, and after the last of them the min operand
+                const uint32_t bytes = (uint32_t)(XSPAN * XP_BLOCK + (part == XCOPIES - 1 ? MIN_BYTES : 0));
                 mbar_arrive_expect_tx(bars.raw_full(1, s), bytes);
                 // every CTA of this token tile reads the same bytes: no eviction hint
-                bulk_g2s_nohint(sbase + L::OFF_XP + (uint32_t)(s * XStage<WT>::BYTES),
-                                src + (size_t)sb * XP_BYTES + (size_t)part * SPAN * XP_BLOCK, bytes, bars.raw_full(1, s));
+                bulk_g2s_nohint(sbase + L::OFF_XP + (uint32_t)(s * XSTAGE_BYTES),
+                                src + (size_t)sb * XP_BYTES + (size_t)part * XSPAN * XP_BLOCK, bytes, bars.raw_full(1, s));
             }
         }
     } else if (warp < R::EPI0) {
