@@ -77,16 +77,17 @@ struct Roles {
     static constexpr int THREADS = (EPI0 + NUM_EPI_WARPS) * 32;  // 800, or 832 with the pre-pass
     static constexpr int OP_FULL_WARPS = XP ? NUM_W_WARPS : NUM_W_WARPS + 4;  // arrivals per operand slot
 };
-// A super-block of prepared activation operands, as the pre-pass writes it and
-// one bulk copy brings it in: 8 blocks of fp16 codes (128 tokens x 32 values in
-// the UMMA K-major core-matrix layout), then the 16 group sums as fp16 in the
-// min operand's layout.
+// A super-block of prepared activation operands, as the pre-pass writes it (the
+// kernel brings it in as two bulk copies of half of it, see XSPAN): 8 blocks of
+// fp16 codes (128 tokens x 32 values in the UMMA K-major core-matrix layout),
+// then the 16 group sums as fp16 in the min operand's layout.
 constexpr int XP_BLOCK = BN * 32 * 2;                // 8192
 constexpr int TMEM_COLS = 512;            // 2 super-blocks x (value, min) x 128 columns
 
 template <int WT> struct Fmt;
 // BB bytes per super-block, RAWW its 16-byte aligned superset, SPLIT: two
-// weight operands, OP_SLOTS blocks in flight, GROUP blocks converted together
+// weight operands, OP_SLOTS blocks in flight without the pre-pass (with it, see
+// Slots), GROUP blocks converted together
 template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, RAWW = 144, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
 template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, RAWW = 96, SPLIT = 0, OP_SLOTS = 4, GROUP = 2; };
 template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, RAWW = 224, SPLIT = 1, OP_SLOTS = 3, GROUP = 1; };
