@@ -33,7 +33,9 @@
  *             blocks are [M][K / block_values] blocks, and outputs are fp32
  *             [M][N], token-major ([minfer] s2.3 and s3.4: out is [nt][od]).
  *   Pointers. Device pointers, owned by the caller, valid for the whole
- *             asynchronous call.  Nothing is allocated on any call.
+ *             asynchronous call.  The library keeps no device memory between
+ *             calls; the one allocation is the prefill's stream-ordered
+ *             workspace (see "prefill matmul" below).
  *   Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *             default stream).  Calls are asynchronous on it; none synchronizes.
  *   Chaining. The matvec, linear and matmul kernels are launched as
@@ -336,7 +338,15 @@ QMM_API qmm_status qmm_linear_norm(int wtype, int G, const void* const* W, const
  * accumulator.  Q4_1 and Q5_1 add each block's min term after its value term:
  * y += (d_w*d_x) * isum; y += m_w * (d_x * sum(a)), with sum(a) the exact
  * integer sum of the token's block codes.  Results agree with the scalar order
- * within 1e-5 of the row's L2 norm. */
+ * within 1e-5 of the row's L2 norm.
+ * Workspace: on the tensor-core path, Q4_1 and Q5_1 here and every K-quant
+ * below convert the activation once, into a workspace taken with
+ * cudaMallocAsync and returned with cudaFreeAsync on `stream` (captured into a
+ * CUDA graph as memory nodes): ceil(M/128) * K/256 * 73,728 bytes for Q4_1 and
+ * Q5_1, * 70,144 for the K-quants (~4.7 / 4.5 MB at M = 512, K = 4096).  The
+ * qmm_linear_* calls that route M >= 8 here do the same.  If the allocation
+ * fails, every CTA converts the activation itself: the results are the same,
+ * bit for bit.  qmm_linear_noalloc never allocates. */
 QMM_API qmm_status qmm_matmul_q4_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
                            qmm_stream_t stream);
 QMM_API qmm_status qmm_matmul_q8_0(const void* W, const void* xq, float* Y, int64_t M, int64_t N, int64_t K,
