@@ -111,13 +111,14 @@ constexpr int XP_BYTES = 8 * XP_BLOCK + MIN_BYTES;  // 69632
 // memory for more weight-operand slots (Slots).
 constexpr int XSPAN = 4, XCOPIES = 8 / XSPAN;
 constexpr int XSTAGE_BYTES = XSPAN * XP_BLOCK + MIN_BYTES;  // 36864
-// Operand slots in flight.  With the pre-pass 8 (Q6_K, with two operands per
-// slot, 4), which lets the converters run further ahead of the MMA issuer than
-// the 4 that fit beside whole-super-block stages (Q4_K 110.6 -> 103.7 us at
-// M = 512); an even number of handover barriers either way (see the converters).
+// Operand slots in flight.  With the pre-pass 12 for Q4_K and Q5_K, 8 for Q2_K
+// (12 spilled more and ran slower) and 4 for Q6_K (two operands per slot): the
+// converters run further ahead of the MMA issuer than with the 4 that fit beside
+// whole-super-block stages (Q4_K at M = 512: 110.6 us with 4, 103.7 with 8, 102.5
+// with 12).  An even number of handover barriers in every case (see the converters).
 template <int WT, bool XP>
 struct Slots {
-    static constexpr int S = XP ? (WT == QMM_Q6_K ? 4 : 8) : Fmt<WT>::OP_SLOTS;
+    static constexpr int S = XP ? (WT == QMM_Q6_K ? 4 : WT == QMM_Q2_K ? 8 : 12) : Fmt<WT>::OP_SLOTS;
 };
 
 template <int WT, bool XP = false>
